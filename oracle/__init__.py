@@ -1,0 +1,229 @@
+"""CPU oracle (test infrastructure only).
+
+A plain, slow, obviously correct CPU implementation of the quantize and GEMM
+steps, in C++ (``oracle.cpp``), driven from numpy through ctypes.  Only the
+tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may
+import this package; the CUDA library never does, and the two share no code.
+
+Functions follow the pages on the subject (AstrAI ``ops/fp8.py``: the CPU
+kernels of ``custom::fp8_quantize`` and ``custom::fp8_gemm``; the POPCORNBENCH
+``Kimi-K2.6 l2_p13`` trace: INT8 absmax/127 quantization with round-half-even;
+the scmp_kernels README: per-row and per-head granularity).  Every function is
+pinned by ``tests/test_oracle_*.py`` against values that the pages print,
+closed forms, library routines and brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+E4M3, E5M2 = 0, 1
+NT, NN, TN = 0, 1, 2
+F32, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so next to its source: -O2, OpenMP, no FMA contraction."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-fopenmp",
+             "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+            L.or_fp8_decode.argtypes = [ctypes.c_uint8, i32]
+            L.or_fp8_decode.restype = ctypes.c_double
+            L.or_fp8_encode_array.argtypes = [vp, i64, i32, vp]
+            L.or_fp8_encode_array.restype = i32
+            L.or_fp8_code_is_nan.argtypes = [ctypes.c_uint8, i32]
+            L.or_fp8_code_is_nan.restype = i32
+            L.or_round_half_even.argtypes = [f32]
+            L.or_round_half_even.restype = ctypes.c_int32
+            L.or_bf16_round.argtypes = [f32]
+            L.or_bf16_round.restype = ctypes.c_uint16
+            L.or_quantize_rowwise_i8.argtypes = [vp, i32, i64, i64, i64, vp, vp]
+            L.or_quantize_rowwise_i8.restype = i32
+            L.or_quantize_fp8.argtypes = [vp, i64, f32, i32, vp, vp]
+            L.or_quantize_fp8.restype = i32
+            L.or_gemm_i8.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, vp, vp]
+            L.or_gemm_i8.restype = i32
+            L.or_gemm_fp8.argtypes = [vp, vp, i32, i32, i64, i64, i64, f32, f32, vp, i64, vp, vp]
+            L.or_gemm_fp8.restype = i32
+            L.or_num_threads.argtypes = []
+            L.or_num_threads.restype = i32
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {a.dtype}")
+    return a
+
+
+def num_threads() -> int:
+    return int(_load().or_num_threads())
+
+
+# ------------------------------------------------------------------ codec
+def fp8_decode(code: int, fmt: int) -> float:
+    return float(_load().or_fp8_decode(int(code) & 0xFF, int(fmt)))
+
+
+def fp8_decode_table(fmt: int) -> np.ndarray:
+    """The 256 decoded values (NaN for NaN codes) as float64."""
+    return np.array([fp8_decode(c, fmt) for c in range(256)], dtype=np.float64)
+
+
+def fp8_code_is_nan(code: int, fmt: int) -> bool:
+    return bool(_load().or_fp8_code_is_nan(int(code) & 0xFF, int(fmt)))
+
+
+def fp8_encode(t, fmt: int) -> np.ndarray:
+    """float32 -> FP8 codes (RNE, saturating to the largest finite value)."""
+    t = np.asarray(t, dtype=np.float32)
+    shape = t.shape
+    t = _c(t.reshape(-1), np.float32)
+    out = np.empty(t.shape, dtype=np.uint8)
+    if _load().or_fp8_encode_array(_ptr(t), t.size, int(fmt), _ptr(out)) != 0:
+        raise ValueError("bad fp8 format")
+    return out.reshape(shape)
+
+
+def round_half_even(t: float) -> int:
+    return int(_load().or_round_half_even(float(np.float32(t))))
+
+
+def bf16_round(f: float) -> int:
+    return int(_load().or_bf16_round(float(np.float32(f))))
+
+
+# ------------------------------------------------------------------ quantize
+def quantize_rowwise_i8(x: np.ndarray, dtype: int = F32):
+    """Per-row symmetric INT8 of a 2-D (or batched 3-D, per head) array.
+
+    x: float32 values (dtype=F32) or uint16 bf16 bits (dtype=BF16), last axis
+    is the row.  Returns (q int8 same shape, scales float32 of shape[:-1]).
+    """
+    x = np.ascontiguousarray(x)
+    if dtype == F32 and x.dtype != np.float32:
+        raise TypeError("F32 input must be float32")
+    if dtype == BF16 and x.dtype != np.uint16:
+        raise TypeError("BF16 input must be uint16 bit patterns")
+    cols = x.shape[-1]
+    rows = x.size // cols if cols else 0
+    q = np.empty(x.shape, dtype=np.int8)
+    s = np.empty(x.shape[:-1], dtype=np.float32)
+    if _load().or_quantize_rowwise_i8(_ptr(x), int(dtype), rows, cols, cols, _ptr(q), _ptr(s)) != 0:
+        raise ValueError("bad arguments")
+    return q, s
+
+
+def quantize_fp8(x_bf16: np.ndarray, scale: float, fmt: int):
+    """Per-tensor FP8 of bf16 bits with the scale divided out.  Returns (x8, amax)."""
+    x = _c(x_bf16, np.uint16)
+    x8 = np.empty(x.shape, dtype=np.uint8)
+    amax = np.zeros(1, dtype=np.float32)
+    if _load().or_quantize_fp8(_ptr(x), x.size, float(np.float32(scale)), int(fmt),
+                               _ptr(x8), _ptr(amax)) != 0:
+        raise ValueError("bad arguments")
+    return x8, np.float32(amax[0])
+
+
+# ------------------------------------------------------------------ GEMMs
+def gemm_i8(A, B, sa=None, sb=None, rows=None):
+    """C[b] = A[b] B[b]^T on int8 codes (2-D or batched 3-D).
+
+    Returns (acc int32, C float32 or None).  rows selects output rows of every
+    batch (None = all).  Raises OverflowError if an exact sum leaves int32.
+    """
+    A = _c(A, np.int8)
+    B = _c(B, np.int8)
+    batched = A.ndim == 3
+    if not batched:
+        A, B = A[None], B[None]
+        if sa is not None:
+            sa, sb = np.asarray(sa)[None], np.asarray(sb)[None]
+    nb, M, K = A.shape
+    _, N, K2 = B.shape
+    assert K == K2 and B.shape[0] == nb
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = M if r is None else r.size
+    acc = np.empty((nb, nr, N), dtype=np.int32)
+    C = None
+    if sa is not None:
+        sa = _c(np.asarray(sa, dtype=np.float32), np.float32)
+        sb = _c(np.asarray(sb, dtype=np.float32), np.float32)
+        C = np.empty((nb, nr, N), dtype=np.float32)
+    rc = _load().or_gemm_i8(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), nb, M, N, K, M * K, N * K,
+                            _ptr(r), nr, _ptr(acc), _ptr(C))
+    if rc < 0:
+        raise ValueError("bad arguments")
+    if rc == 1:
+        raise OverflowError("an exact INT8 accumulator does not fit int32")
+    if not batched:
+        acc = acc[0]
+        C = None if C is None else C[0]
+    return acc, C
+
+
+def gemm_fp8(A8, B8, fmt: int, layout: int, sa: float, sb: float, rows=None, want_bf16=True):
+    """FP8 GEMM reference.  Returns (ref float64 [rows, N], bf16 bits or None).
+
+    layout NT: A[M,K], B[N,K]; NN: A[M,K], B[K,N]; TN: A[K,M], B[K,N].
+    """
+    A8 = _c(A8, np.uint8)
+    B8 = _c(B8, np.uint8)
+    if layout == NT:
+        M, K = A8.shape
+        N = B8.shape[0]
+        assert B8.shape[1] == K
+    elif layout == NN:
+        M, K = A8.shape
+        N = B8.shape[1]
+        assert B8.shape[0] == K
+    elif layout == TN:
+        K, M = A8.shape
+        N = B8.shape[1]
+        assert B8.shape[0] == K
+    else:
+        raise ValueError("layout must be NT, NN or TN")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = M if r is None else r.size
+    ref = np.empty((nr, N), dtype=np.float64)
+    bf = np.empty((nr, N), dtype=np.uint16) if want_bf16 else None
+    rc = _load().or_gemm_fp8(_ptr(A8), _ptr(B8), int(fmt), int(layout), M, N, K,
+                             float(np.float32(sa)), float(np.float32(sb)), _ptr(r), nr,
+                             _ptr(ref), _ptr(bf))
+    if rc != 0:
+        raise ValueError("bad arguments")
+    return ref, bf
+
+
+def fp8_gemm_bound(ref: np.ndarray, K: int, sa: float, sb: float, maxa8: float, maxb8: float):
+    """Allowed |err| per element for a bf16 FP8-GEMM output against the fp64 reference:
+    1e-2*|ref| + 1e-3*sqrt(K)*sa*sb*max|a8|*max|b8|."""
+    return 1e-2 * np.abs(ref) + 1e-3 * np.sqrt(K) * float(sa) * float(sb) * maxa8 * maxb8
