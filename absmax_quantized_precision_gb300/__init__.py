@@ -1,0 +1,213 @@
+"""absmax-scaled quantization and scaled low-precision GEMM on GB300 (sm_103a).
+
+Thin binding over libsq.so, whose C ABI is declared in include/sq.h.  Every
+function here only marshals arguments (torch tensors -> device pointers, the
+current CUDA stream) and turns a non-OK status into an exception; all
+arithmetic runs in the library's CUDA kernels.  There is no CPU fallback: if
+libsq.so has not been built, importing the library raises.
+
+Entry points (names as in the C ABI):
+  sq_quantize_rowwise_i8  per-row symmetric INT8 (absmax/127, half-to-even)
+  sq_quantize_fp8         per-tensor FP8 E4M3/E5M2 with the amax fused in
+  sq_gemm_i8_rowscaled    exact INT8 GEMM, fp32 = acc * sA[i] * sB[j]
+  sq_gemm_fp8_scaled      FP8 GEMM, bf16 = acc * sa * sb, layouts NT/NN/TN
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsq.so")
+
+SQ_OK, SQ_ERR_INVALID_ARG, SQ_ERR_UNSUPPORTED, SQ_ERR_ALIGNMENT, SQ_ERR_CUDA, \
+    SQ_ERR_DEVICE_TIMEOUT = range(6)
+SQ_F32, SQ_BF16 = 0, 1
+SQ_FMT_E4M3, SQ_FMT_E5M2 = 0, 1
+SQ_NT, SQ_NN, SQ_TN = 0, 1, 2
+
+# every symbol include/sq.h declares
+EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "sq_quantize_fp8",
+           "sq_gemm_i8_workspace_bytes", "sq_gemm_i8_rowscaled", "sq_gemm_fp8_scaled",
+           "sq_get_last_device_error")
+
+_lib = None
+
+
+class SQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)}")
+        self.status = status
+
+
+def load_library():
+    """Load libsq.so (raises if it has not been built: no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libsq.so is not built ({LIB_PATH}); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.sq_status_string.argtypes = [i32]
+    L.sq_status_string.restype = ctypes.c_char_p
+    L.sq_workspace_bytes.argtypes = []
+    L.sq_workspace_bytes.restype = sz
+    L.sq_quantize_rowwise_i8.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp]
+    L.sq_quantize_rowwise_i8.restype = i32
+    L.sq_quantize_fp8.argtypes = [vp, i64, vp, i32, vp, vp, vp, vp]
+    L.sq_quantize_fp8.restype = i32
+    L.sq_gemm_i8_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    L.sq_gemm_i8_workspace_bytes.restype = sz
+    L.sq_gemm_i8_rowscaled.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, vp, vp,
+                                       vp, sz, vp]
+    L.sq_gemm_i8_rowscaled.restype = i32
+    L.sq_gemm_fp8_scaled.argtypes = [vp, vp, vp, vp, i32, i32, i64, i64, i64, vp, vp]
+    L.sq_gemm_fp8_scaled.restype = i32
+    L.sq_get_last_device_error.argtypes = [vp]
+    L.sq_get_last_device_error.restype = i32
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return load_library().sq_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != SQ_OK:
+        raise SQError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libsq works on CUDA tensors only")
+
+
+# ---------------------------------------------------------------- workspaces
+def workspace_bytes() -> int:
+    return int(load_library().sq_workspace_bytes())
+
+
+def new_workspace(device=None) -> torch.Tensor:
+    """A zeroed workspace for sq_quantize_fp8 (allocate once per stream)."""
+    return torch.zeros(workspace_bytes(), dtype=torch.uint8, device=device or "cuda")
+
+
+def gemm_i8_workspace_bytes(batch: int, M: int, N: int, K: int) -> int:
+    return int(load_library().sq_gemm_i8_workspace_bytes(batch, M, N, K))
+
+
+# ---------------------------------------------------------------- entry points
+def sq_quantize_rowwise_i8(x: torch.Tensor, q: torch.Tensor = None, scales: torch.Tensor = None,
+                           stream=None):
+    """Per-row INT8 of x (float32 or bfloat16, last dim = row, rows may be
+    strided).  Returns (q int8 packed, scales float32 of shape x.shape[:-1])."""
+    _need_cuda(x)
+    if x.dtype == torch.float32:
+        dt = SQ_F32
+    elif x.dtype == torch.bfloat16:
+        dt = SQ_BF16
+    else:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    cols = x.shape[-1]
+    x2 = x.reshape(-1, cols) if x.dim() != 2 else x
+    if x2.numel() and x2.stride(-1) != 1:
+        raise ValueError("rows of x must be contiguous")
+    rows = x2.shape[0]
+    ld = x2.stride(0) if rows > 1 else cols
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _check(load_library().sq_quantize_rowwise_i8(_ptr(x2), dt, rows, cols, ld, _ptr(q),
+                                                 _ptr(scales), _stream(stream)),
+           "sq_quantize_rowwise_i8")
+    return q, scales
+
+
+def sq_quantize_fp8(x: torch.Tensor, scale: torch.Tensor, fmt: int, workspace: torch.Tensor,
+                    x8: torch.Tensor = None, amax: torch.Tensor = None, stream=None):
+    """Per-tensor FP8 of bf16 x with the step `scale` (1-element float32 on the
+    device) divided out.  Returns (x8 uint8 codes, amax 1-element float32)."""
+    _need_cuda(x, scale, workspace)
+    if x.dtype != torch.bfloat16:
+        raise TypeError(f"x must be bfloat16, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if x8 is None:
+        x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(load_library().sq_quantize_fp8(_ptr(x), x.numel(), _ptr(scale), int(fmt), _ptr(x8),
+                                          _ptr(amax), _ptr(workspace), _stream(stream)),
+           "sq_quantize_fp8")
+    return x8, amax
+
+
+def sq_gemm_i8_rowscaled(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,
+                         workspace: torch.Tensor, C: torch.Tensor = None, acc_out=None,
+                         want_c: bool = True, stream=None):
+    """C[b] = A[b] B[b]^T on int8 codes with fp32 (acc * sA[i]) * sB[j].
+
+    A: [M,K] or [batch,M,K] int8, B: [N,K] or [batch,N,K].  Returns (C, acc_out);
+    pass acc_out=True to get the exact int32 accumulators too."""
+    _need_cuda(A, B, sA, sB, workspace)
+    batched = A.dim() == 3
+    A3 = A if batched else A.unsqueeze(0)
+    B3 = B if batched else B.unsqueeze(0)
+    nb, M, K = A3.shape
+    N = B3.shape[1]
+    if not (A3.is_contiguous() and B3.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    shape = (nb, M, N) if batched else (M, N)
+    if want_c and C is None:
+        C = torch.empty(shape, dtype=torch.float32, device=A.device)
+    if acc_out is True:
+        acc_out = torch.empty(shape, dtype=torch.int32, device=A.device)
+    elif acc_out is False:
+        acc_out = None
+    _check(load_library().sq_gemm_i8_rowscaled(
+        _ptr(A3), _ptr(sA), _ptr(B3), _ptr(sB), nb, M, N, K, M * K, N * K, M * N,
+        _ptr(C), _ptr(acc_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "sq_gemm_i8_rowscaled")
+    return C, acc_out
+
+
+def sq_gemm_fp8_scaled(A: torch.Tensor, B: torch.Tensor, sa: torch.Tensor, sb: torch.Tensor,
+                       fmt: int, layout: int, C: torch.Tensor = None, stream=None):
+    """bf16 C = (acc * sa) * sb for FP8 codes A, B (uint8) in layout NT/NN/TN."""
+    _need_cuda(A, B, sa, sb)
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    if layout == SQ_NT:
+        (M, K), N = A.shape, B.shape[0]
+    elif layout == SQ_NN:
+        (M, K), N = A.shape, B.shape[1]
+    elif layout == SQ_TN:
+        (K, M), N = A.shape, B.shape[1]
+    else:
+        raise ValueError("layout must be SQ_NT, SQ_NN or SQ_TN")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check(load_library().sq_gemm_fp8_scaled(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), int(fmt),
+                                             int(layout), M, N, K, _ptr(C), _stream(stream)),
+           "sq_gemm_fp8_scaled")
+    return C
+
+
+def sq_get_last_device_error(stream=None) -> int:
+    return int(load_library().sq_get_last_device_error(_stream(stream)))

@@ -1,0 +1,179 @@
+// C ABI of libsq (declared in include/sq.h): argument checks, per-device
+// state, and dispatch to the launchers.  No entry point allocates, frees or
+// synchronises on its hot path.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/sq.h"
+#include "sq_launch.h"
+
+// Device error word of this library, one per device.
+static __device__ unsigned g_sq_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::once_flag once;
+    int sms = 0;
+    unsigned* err_word = nullptr;
+    cudaError_t init_err = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+// SM count and the device address of the error word for the current device.
+DeviceState* device_state(cudaError_t* err) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    DeviceState& s = g_dev[dev];
+    std::call_once(s.once, [&] {
+        s.init_err = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (s.init_err == cudaSuccess)
+            s.init_err = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err_word), g_sq_device_error);
+    });
+    if (s.init_err != cudaSuccess) {
+        *err = s.init_err;
+        return nullptr;
+    }
+    return &s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SQ_OK : SQ_ERR_CUDA; }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+}  // namespace
+
+extern "C" {
+
+const char* sq_status_string(sq_status s) {
+    switch (s) {
+        case SQ_OK: return "SQ_OK";
+        case SQ_ERR_INVALID_ARG: return "SQ_ERR_INVALID_ARG: invalid size, pointer, dtype, fmt or layout";
+        case SQ_ERR_UNSUPPORTED: return "SQ_ERR_UNSUPPORTED: valid but outside this library's limits";
+        case SQ_ERR_ALIGNMENT: return "SQ_ERR_ALIGNMENT: a pointer or row length breaks the 16-byte rule";
+        case SQ_ERR_CUDA: return "SQ_ERR_CUDA: the CUDA runtime reported an error";
+        case SQ_ERR_DEVICE_TIMEOUT: return "SQ_ERR_DEVICE_TIMEOUT: a kernel gave up on a bounded wait";
+    }
+    return "SQ_ERR_UNKNOWN";
+}
+
+size_t sq_workspace_bytes(void) { return 256; }
+
+sq_status sq_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                                 int8_t* q, float* scales, sq_stream stream) {
+    if (dtype != SQ_F32 && dtype != SQ_BF16) return SQ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || ld < cols) return SQ_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return SQ_OK;
+    if (!x || !q || !scales) return SQ_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    const int64_t esz = dtype == SQ_F32 ? 4 : 2;
+    const bool vec_ok = aligned16(x) && aligned16(q) && ((ld * esz) % 16 == 0) && (cols % 16 == 0);
+    return from_cuda(sq::launch_quantize_rowwise_i8(x, dtype, rows, cols, ld, q, scales, vec_ok,
+                                                    reinterpret_cast<cudaStream_t>(stream), ds->sms));
+}
+
+sq_status sq_quantize_fp8(const uint16_t* x_bf16, int64_t numel, const float* scale, int fmt,
+                          uint8_t* x8, float* amax, void* workspace, sq_stream stream) {
+    if (fmt != SQ_FMT_E4M3 && fmt != SQ_FMT_E5M2) return SQ_ERR_INVALID_ARG;
+    if (numel < 0 || !scale || !amax || !workspace) return SQ_ERR_INVALID_ARG;
+    if (numel > 0 && (!x_bf16 || !x8)) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(x8) || !aligned16(workspace)) return SQ_ERR_ALIGNMENT;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    return from_cuda(sq::launch_quantize_fp8(x_bf16, numel, scale, fmt, x8, amax,
+                                             static_cast<unsigned*>(workspace),
+                                             reinterpret_cast<cudaStream_t>(stream), ds->sms));
+}
+
+size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K) {
+    if (batch <= 0 || M <= 0 || N <= 0 || K <= 0) return 0;
+    const size_t a = static_cast<size_t>(batch) * M * K * 2;
+    const size_t b = static_cast<size_t>(batch) * N * K * 2;
+    return ((a + 255) & ~static_cast<size_t>(255)) + ((b + 255) & ~static_cast<size_t>(255));
+}
+
+sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B, const float* sB,
+                               int64_t batch, int64_t M, int64_t N, int64_t K, int64_t strideA,
+                               int64_t strideB, int64_t strideC, float* C, int32_t* acc_out,
+                               void* workspace, size_t workspace_bytes, sq_stream stream) {
+    if (batch < 1 || M < 1 || N < 1 || K < 1) return SQ_ERR_INVALID_ARG;
+    if (!A || !B || !sA || !sB || !workspace || (!C && !acc_out)) return SQ_ERR_INVALID_ARG;
+    if (strideA < M * K || strideB < N * K || strideC < M * N) return SQ_ERR_INVALID_ARG;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (K > (int64_t(1) << 17)) return SQ_ERR_UNSUPPORTED;
+    if (batch > 65535 || M > kMaxDim || N > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    if (strideA % 16 != 0 || strideB % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(acc_out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SQ_ERR_ALIGNMENT;
+    if (workspace_bytes < sq_gemm_i8_workspace_bytes(batch, M, N, K)) return SQ_ERR_INVALID_ARG;
+    const int64_t mt = (M + 127) / 128, nt = (N + 127) / 128;
+    if (mt * nt * batch > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t* A16 = static_cast<uint16_t*>(workspace);
+    const size_t abytes = (static_cast<size_t>(batch) * M * K * 2 + 255) & ~static_cast<size_t>(255);
+    uint16_t* B16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + abytes);
+    e = sq::launch_i8_to_f16(A, batch, M, K, strideA, A16, st, ds->sms);
+    if (e != cudaSuccess) return SQ_ERR_CUDA;
+    e = sq::launch_i8_to_f16(B, batch, N, K, strideB, B16, st, ds->sms);
+    if (e != cudaSuccess) return SQ_ERR_CUDA;
+    return from_cuda(sq::launch_gemm_i8(A16, B16, sA, sB, static_cast<int>(batch),
+                                        static_cast<int>(M), static_cast<int>(N),
+                                        static_cast<int>(K), strideC, C, acc_out, ds->err_word, st,
+                                        ds->sms));
+}
+
+sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                             int fmt, int layout, int64_t M, int64_t N, int64_t K,
+                             uint16_t* C_bf16, sq_stream stream) {
+    if (fmt != SQ_FMT_E4M3 && fmt != SQ_FMT_E5M2) return SQ_ERR_INVALID_ARG;
+    if (layout != SQ_NT && layout != SQ_NN && layout != SQ_TN) return SQ_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1) return SQ_ERR_INVALID_ARG;
+    if (!A || !B || !sa || !sb || !C_bf16) return SQ_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C_bf16)) return SQ_ERR_ALIGNMENT;
+    // TMA row pitches must be multiples of 16 bytes
+    if (layout == SQ_NT && K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (layout == SQ_NN && (K % 16 != 0 || N % 16 != 0)) return SQ_ERR_ALIGNMENT;
+    if (layout == SQ_TN && (M % 16 != 0 || N % 16 != 0)) return SQ_ERR_ALIGNMENT;
+    if (((M + 127) / 128) * ((N + 127) / 128) > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    return from_cuda(sq::launch_gemm_fp8(A, B, sa, sb, fmt, layout, static_cast<int>(M),
+                                         static_cast<int>(N), static_cast<int>(K), C_bf16,
+                                         ds->err_word, reinterpret_cast<cudaStream_t>(stream),
+                                         ds->sms));
+}
+
+sq_status sq_get_last_device_error(sq_stream stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return SQ_ERR_CUDA;
+    unsigned word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_sq_device_error, sizeof(word));
+    if (e != cudaSuccess) return SQ_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_sq_device_error, &zero, sizeof(zero));
+        if (e != cudaSuccess) return SQ_ERR_CUDA;
+        return SQ_ERR_DEVICE_TIMEOUT;
+    }
+    return SQ_OK;
+}
+
+}  // extern "C"

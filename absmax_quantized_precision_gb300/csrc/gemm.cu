@@ -1,0 +1,576 @@
+// Tensor-core GEMMs on tcgen05 (sm_103a): the scaled FP8 GEMM and the exact
+// INT8 GEMM with its per-row x per-row dequantization epilogue.
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//   warp 0      TMA producer: streams 128x128-byte A tiles and BNx128-byte B
+//               tiles (128-byte swizzle) into a ring of shared-memory stages.
+//   warp 1      owns the TMEM allocation; one elected thread issues
+//               tcgen05.mma (M=128, N=BN, K=32 bytes per instruction) into one
+//               of two TMEM accumulators and releases each stage with
+//               tcgen05.commit.
+//   warps 2..   epilogue: tcgen05.ld of the accumulator, scaling, stores.  Two
+//               accumulators let the epilogue of one tile overlap the MMAs of
+//               the next.
+// Tiles are visited in groups of GROUP_M tile-rows so that consecutive CTAs
+// share B column blocks in L2 (grouped rasterisation, as the AstrAI commit
+// notes do for the NT forward).
+//
+// FP8 (AstrAI ops/fp8.py, custom::fp8_gemm): acc = sum_k a8*b8 in FP32 inside
+// the tensor core (kind::f8f6f4, E4M3 or E5M2), C = bf16(fl32(acc*sa)*sb).
+// NT, NN and TN are served by the same kernel: an operand stored with M (or
+// N) contiguous is loaded as [K rows x 128 bytes] boxes and described to the
+// MMA as MN-major, so no transposed copy is ever made.
+//
+// INT8 (scmp_kernels sc_matmul per_row / per_head, C = a @ b.T in float32):
+// sm_103a has no kind::i8, so the codes are staged as fp16 (exact for
+// |q| <= 127) and multiplied with kind::f16 into an FP32 accumulator.  Every
+// product is an integer of magnitude <= 127^2 and every partial sum of a
+// 1024-long K chunk is an integer below 127^2 * 1024 < 2^24, so the FP32
+// accumulation of a chunk is exact.  The epilogue converts each chunk to int32
+// and sums the chunks in registers, which keeps the whole K sum exact.
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "sq_device.cuh"
+#include "sq_launch.h"
+
+namespace sq {
+
+constexpr int kBM = 128;
+constexpr int kBKBytes = 128;   // bytes of K per stage row (one 128-B swizzle row)
+constexpr int kGroupM = 16;
+constexpr int kI8ChunkK = 1024; // K elements per exact FP32 chunk
+
+struct GemmParams {
+    int M, N, K;
+    int batch;
+    int mt, nt;            // tile counts along M and N
+    int nkb;               // k-blocks per tile
+    int kb_per_chunk;      // k-blocks per accumulator chunk
+    int nchunks;
+    const float* sa;       // FP8: scalar step of A; INT8: row scales [batch*M]
+    const float* sb;       // FP8: scalar step of B; INT8: row scales [batch*N]
+    void* C;               // FP8: bf16 [M,N]; INT8: f32, batch stride strideC
+    int32_t* acc_out;      // INT8 only (nullable)
+    int64_t strideC;
+    uint32_t idesc;
+    int vec_store;
+    unsigned* err_word;
+};
+
+template <int BN, bool I8, bool A_MN, bool B_MN>
+struct GemmCfg {
+    static constexpr int A_BYTES = kBM * kBKBytes;          // 16 KB
+    static constexpr int B_BYTES = BN * kBKBytes;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    // INT8 keeps its running int32 sums in registers: 8 epilogue warps, each
+    // owning 32 rows x EPI_COLS columns of the tile.
+    static constexpr int EPI_WARPS = I8 ? 8 : 4;
+    static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = STAGES * STAGE + BAR_BYTES + 1024;
+    // bytes the start address moves per MMA instruction along K
+    static constexpr int KSTEP_K = 32;                      // K-major: 32 B inside the row
+    static constexpr int KSTEP_MN = (I8 ? 16 : 32) * 128;   // MN-major: that many K rows
+    static constexpr int MN_LBO = kBKBytes * 128;           // 16 KB between 128-B column blocks
+    static_assert(2 * STAGES * 8 + 5 * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& b, int& mb, int& nb) {
+    const int per = p.mt * p.nt;
+    b = t / per;
+    const int r = t - b * per;
+    const int gsz = kGroupM * p.nt;
+    const int g = r / gsz;
+    const int first = g * kGroupM;
+    const int gm = min(p.mt - first, kGroupM);
+    const int rr = r - g * gsz;
+    mb = first + rr % gm;
+    nb = rr / gm;
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+template <int BN, bool I8, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE);
+    uint64_t* empty = full + Cfg::STAGES;
+    uint64_t* tfull = empty + Cfg::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], Cfg::EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total = p.mt * p.nt * p.batch;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[Cfg::STAGES];
+            for (int s = 0; s < Cfg::STAGES; ++s) issued_phase[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                int b, mb, nb;
+                tile_coords(t, p, b, mb, nb);
+                const int m0 = mb * kBM, n0 = nb * BN;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err_word)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sA = smem + stage * Cfg::STAGE;
+                    uint8_t* sB = sA + Cfg::A_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE);
+                    if (I8) {
+                        const int kx = kb * (kBKBytes / 2);
+                        tma_load_3d(sA, &tmA, &full[stage], kx, m0, b);
+                        tma_load_3d(sB, &tmB, &full[stage], kx, n0, b);
+                    } else {
+                        const int kx = kb * kBKBytes;
+                        if (A_MN) tma_load_2d(sA, &tmA, &full[stage], m0, kx);
+                        else tma_load_2d(sA, &tmA, &full[stage], kx, m0);
+                        if (B_MN) {
+#pragma unroll
+                            for (int j = 0; j < BN / 128; ++j)
+                                tma_load_2d(sB + j * Cfg::MN_LBO, &tmB, &full[stage], n0 + j * 128, kx);
+                        } else {
+                            tma_load_2d(sB, &tmB, &full[stage], kx, n0);
+                        }
+                    }
+                    issued_phase[stage] = static_cast<int>(phase);
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy this thread started land before the CTA exits
+                for (int s = 0; s < Cfg::STAGES; ++s)
+                    if (issued_phase[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(issued_phase[s]));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                for (int ch = 0; ch < p.nchunks && ok; ++ch) {
+                    const uint32_t ab = it & 1u;
+                    const uint32_t aph = (it >> 1) & 1u;
+                    if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, p.err_word)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + ab * BN;
+                    const int kb0 = ch * p.kb_per_chunk;
+                    const int kb1 = min(p.nkb, kb0 + p.kb_per_chunk);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag, p.err_word)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_addr(smem + stage * Cfg::STAGE);
+                        const uint32_t b_addr = a_addr + Cfg::A_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < kBKBytes / 32; ++kk) {
+                            const uint64_t ad =
+                                A_MN ? sdesc_sw128(a_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
+                                     : sdesc_sw128(a_addr + kk * Cfg::KSTEP_K, 16, 1024);
+                            const uint64_t bd =
+                                B_MN ? sdesc_sw128(b_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
+                                     : sdesc_sw128(b_addr + kk * Cfg::KSTEP_K, 16, 1024);
+                            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+                            if (I8) mma_f16(d_tmem, ad, bd, p.idesc, acc);
+                            else mma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
+                        }
+                        mma_commit(&empty[stage]);
+                        if (++stage == Cfg::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&tfull[ab]);
+                    ++it;
+                }
+            }
+            if (!ok) {
+                // make every MMA already issued finish before TMEM is released
+                mma_commit(drain);
+                mbar_wait_drain(drain, 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;
+        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+        const int colgrp = ew >> 2;            // INT8: which EPI_COLS-wide column group
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        float fsa = 0.0f, fsb = 0.0f;
+        if (!I8) {
+            fsa = *p.sa;
+            fsb = *p.sb;
+        }
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            int b, mb, nb;
+            tile_coords(t, p, b, mb, nb);
+            const int m0 = mb * kBM, n0 = nb * BN;
+            const int row = m0 + quarter * 32 + lane;
+            if (I8) {
+                constexpr int NC = Cfg::EPI_COLS / 32;
+                int32_t sums[NC][32];
+#pragma unroll
+                for (int c = 0; c < NC; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sums[c][i] = 0;
+                for (int ch = 0; ch < p.nchunks; ++ch) {
+                    const uint32_t ab = it & 1u;
+                    const uint32_t aph = (it >> 1) & 1u;
+                    if (!mbar_wait(&tfull[ab], aph, abort_flag, p.err_word)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tb = tmem_base + lane_off + ab * BN + colgrp * Cfg::EPI_COLS;
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tb + c * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sums[c][i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[ab]);
+                    ++it;
+                }
+                if (!ok) break;
+                if (row < p.M) {
+                    const float sArow = p.sa[static_cast<int64_t>(b) * p.M + row];
+                    const float* sBb = p.sb + static_cast<int64_t>(b) * p.N;
+                    const int64_t obase = static_cast<int64_t>(b) * p.strideC + static_cast<int64_t>(row) * p.N;
+                    float* Cf = static_cast<float*>(p.C);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const int col0 = n0 + colgrp * Cfg::EPI_COLS + c * 32;
+                        if (p.vec_store && col0 + 32 <= p.N) {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const float4 s4 = *reinterpret_cast<const float4*>(sBb + col0 + 4 * v);
+                                const int32_t a0 = sums[c][4 * v], a1 = sums[c][4 * v + 1];
+                                const int32_t a2 = sums[c][4 * v + 2], a3 = sums[c][4 * v + 3];
+                                if (p.acc_out)
+                                    st_v4(p.acc_out + obase + col0 + 4 * v,
+                                          make_uint4(a0, a1, a2, a3));
+                                if (Cf) {
+                                    float4 o;
+                                    o.x = __fmul_rn(__fmul_rn(__int2float_rn(a0), sArow), s4.x);
+                                    o.y = __fmul_rn(__fmul_rn(__int2float_rn(a1), sArow), s4.y);
+                                    o.z = __fmul_rn(__fmul_rn(__int2float_rn(a2), sArow), s4.z);
+                                    o.w = __fmul_rn(__fmul_rn(__int2float_rn(a3), sArow), s4.w);
+                                    st_v4(Cf + obase + col0 + 4 * v,
+                                          make_uint4(__float_as_uint(o.x), __float_as_uint(o.y),
+                                                     __float_as_uint(o.z), __float_as_uint(o.w)));
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int col = col0 + i;
+                                if (col < p.N) {
+                                    if (p.acc_out) p.acc_out[obase + col] = sums[c][i];
+                                    if (Cf)
+                                        Cf[obase + col] = __fmul_rn(
+                                            __fmul_rn(__int2float_rn(sums[c][i]), sArow), sBb[col]);
+                                }
+                            }
+                        }
+                    }
+                }
+            } else {
+                const uint32_t ab = it & 1u;
+                const uint32_t aph = (it >> 1) & 1u;
+                if (!mbar_wait(&tfull[ab], aph, abort_flag, p.err_word)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb = tmem_base + lane_off + ab * BN;
+                uint16_t* Cb = static_cast<uint16_t*>(p.C);
+                const int64_t obase = static_cast<int64_t>(row) * p.N;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + c * 32, r);
+                    tmem_ld_wait();
+                    const int col0 = n0 + c * 32;
+                    if (row < p.M) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float lo = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), fsa), fsb);
+                            const float hi = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), fsa), fsb);
+                            pk[i] = bf16_bits(lo) | (bf16_bits(hi) << 16);
+                        }
+                        if (p.vec_store && col0 + 32 <= p.N) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                st_v4(Cb + obase + col0 + 8 * v,
+                                      make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.N)
+                                    Cb[obase + col0 + i] =
+                                        static_cast<uint16_t>((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[ab]);
+                ++it;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// ====================================================================== host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major [outer, inner] (inner contiguous, row pitch `pitch` bytes), tiles
+// of box_inner x box_outer elements, 128-byte swizzle, zero fill outside.
+static bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                      uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                      uint64_t rows, uint64_t batch, uint64_t pitch, uint64_t bpitch,
+                      uint32_t box_inner, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {pitch, bpitch};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool I8, bool A_MN, bool B_MN>
+static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                            cudaStream_t st, int sms) {
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN>;
+    auto kern = gemm_tc_kernel<BN, I8, A_MN, B_MN>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int total = p.mt * p.nt * p.batch;
+    const int grid = total < sms ? total : sms;
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                            int fmt, int layout, int M, int N, int K, uint16_t* C,
+                            unsigned* err_word, cudaStream_t st, int sms) {
+    // 256-wide tiles when there are enough of them to fill the GPU
+    const int mt = (M + kBM - 1) / kBM;
+    const int BN = (static_cast<int64_t>(mt) * ((N + 255) / 256) >= sms) ? 256 : 128;
+    const bool a_mn = layout == 2;          // TN: A stored [K, M]
+    const bool b_mn = layout != 0;          // NN, TN: B stored [K, N]
+    CUtensorMap ta, tb;
+    bool ok;
+    if (a_mn) ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, M, 128, kBKBytes);
+    else ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, kBKBytes, kBM);
+    if (!ok) return cudaErrorInvalidValue;
+    if (b_mn) ok = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, N, K, N, 128, kBKBytes);
+    else ok = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, kBKBytes, BN);
+    if (!ok) return cudaErrorInvalidValue;
+
+    GemmParams p{};
+    p.M = M; p.N = N; p.K = K; p.batch = 1;
+    p.mt = mt; p.nt = (N + BN - 1) / BN;
+    p.nkb = (K + kBKBytes - 1) / kBKBytes;
+    p.kb_per_chunk = p.nkb;
+    p.nchunks = 1;
+    p.sa = sa; p.sb = sb; p.C = C; p.acc_out = nullptr; p.strideC = 0;
+    p.idesc = idesc_make(static_cast<uint32_t>(fmt), static_cast<uint32_t>(fmt), a_mn, b_mn, kBM, BN);
+    p.vec_store = (N % 8 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
+    p.err_word = err_word;
+    if (BN == 256) {
+        if (layout == 0) return run_gemm<256, false, false, false>(ta, tb, p, st, sms);
+        if (layout == 1) return run_gemm<256, false, false, true>(ta, tb, p, st, sms);
+        return run_gemm<256, false, true, true>(ta, tb, p, st, sms);
+    }
+    if (layout == 0) return run_gemm<128, false, false, false>(ta, tb, p, st, sms);
+    if (layout == 1) return run_gemm<128, false, false, true>(ta, tb, p, st, sms);
+    return run_gemm<128, false, true, true>(ta, tb, p, st, sms);
+}
+
+cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
+                           const float* sB, int batch, int M, int N, int K, int64_t strideC,
+                           float* C, int32_t* acc_out, unsigned* err_word, cudaStream_t st,
+                           int sms) {
+    constexpr int BN = 128;
+    const int bk = kBKBytes / 2;   // 64 fp16 per k-block
+    CUtensorMap ta, tb;
+    if (!encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A16, K, M, batch,
+                   static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(M) * K * 2, bk, kBM))
+        return cudaErrorInvalidValue;
+    if (!encode_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B16, K, N, batch,
+                   static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2, bk, BN))
+        return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.M = M; p.N = N; p.K = K; p.batch = batch;
+    p.mt = (M + kBM - 1) / kBM;
+    p.nt = (N + BN - 1) / BN;
+    p.nkb = (K + bk - 1) / bk;
+    p.kb_per_chunk = kI8ChunkK / bk;
+    p.nchunks = (p.nkb + p.kb_per_chunk - 1) / p.kb_per_chunk;
+    p.sa = sA; p.sb = sB; p.C = C; p.acc_out = acc_out; p.strideC = strideC;
+    p.idesc = idesc_make(0, 0, false, false, kBM, BN);   // F16 x F16 -> F32
+    p.vec_store = (N % 4 == 0) && (strideC % 4 == 0) &&
+                  (reinterpret_cast<uintptr_t>(C) % 16 == 0) &&
+                  (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0) &&
+                  (reinterpret_cast<uintptr_t>(sB) % 16 == 0);
+    p.err_word = err_word;
+    return run_gemm<BN, true, false, false>(ta, tb, p, st, sms);
+}
+
+// ---------------------------------------------------------------- staging
+__global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ src,
+                                                       int64_t batch, int64_t rows, int64_t K,
+                                                       int64_t stride, uint16_t* __restrict__ dst) {
+    // 16 codes per step: one 16-B load, two 16-B stores (K % 16 == 0)
+    const int64_t per_row = K / 16;
+    const int64_t per_batch = rows * per_row;
+    const int64_t total = batch * per_batch;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
+         v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t b = v / per_batch;
+        const int64_t r = v - b * per_batch;
+        const int8_t* s = src + b * stride + r * 16;
+        const uint4 raw = ld_stream_v4(s);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int8_t c0 = static_cast<int8_t>((w[i] >> (16 * h)) & 0xFF);
+                const int8_t c1 = static_cast<int8_t>((w[i] >> (16 * h + 8)) & 0xFF);
+                const uint32_t h0 = __half_as_ushort(__int2half_rn(c0));
+                const uint32_t h1 = __half_as_ushort(__int2half_rn(c1));
+                o[2 * i + h] = h0 | (h1 << 16);
+            }
+        }
+        uint16_t* d = dst + v * 16;
+        st_v4(d, make_uint4(o[0], o[1], o[2], o[3]));
+        st_v4(d + 8, make_uint4(o[4], o[5], o[6], o[7]));
+    }
+}
+
+cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
+                             int64_t stride, uint16_t* dst, cudaStream_t st, int sms) {
+    const int64_t total = batch * rows * (K / 16);
+    if (total == 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    i8_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, batch, rows, K, stride, dst);
+    return cudaGetLastError();
+}
+
+}  // namespace sq

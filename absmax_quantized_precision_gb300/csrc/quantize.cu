@@ -1,0 +1,304 @@
+// Quantize kernels (HBM-bound): per-row symmetric INT8 and per-tensor FP8
+// with the amax fused in.
+//
+// INT8 (POPCORNBENCH "Kimi-K2.6 l2_p13" trace, reference-model analysis and
+// rounding discussion; per-row / per-head granularity of the scmp_kernels
+// README): s = max(amax_row, 1e-8) / 127, q = clamp(rne(x / s), -127, 127),
+// one IEEE division per element (__fdiv_rn) and round-half-even
+// (__float2int_rn), never a reciprocal multiply or roundf.
+//
+// FP8 (AstrAI ops/fp8.py, custom::fp8_quantize and the commit notes): x8 =
+// fp8(x / scale) with round-to-nearest-even and saturation to the largest
+// finite value (cvt.rn.satfinite), amax = max|x| folded in by the last block
+// to finish (threadfence + ticket counter), so no second launch and no
+// per-call memset: the last block also resets the two workspace words.
+#include <cuda_bf16.h>
+
+#include "sq_device.cuh"
+#include "sq_launch.h"
+
+namespace sq {
+
+// ================================================================== INT8 rows
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+    static constexpr int kPerVec = 4;
+    __device__ static void unpack(const uint4& v, float (&f)[4]) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ static float load1(const float* p) { return *p; }
+};
+template <>
+struct Elem<uint16_t> {   // bf16 bit patterns; widening is exact
+    static constexpr int kPerVec = 8;
+    __device__ static void unpack(const uint4& v, float (&f)[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    __device__ static float load1(const uint16_t* p) {
+        return __uint_as_float(static_cast<uint32_t>(*p) << 16);
+    }
+};
+
+__device__ __forceinline__ int8_t encode_i8(float x, float s) {
+    int n = __float2int_rn(__fdiv_rn(x, s));
+    n = n > 127 ? 127 : (n < -127 ? -127 : n);
+    return static_cast<int8_t>(n);
+}
+
+__device__ __forceinline__ float row_scale(float amax) {
+    return __fdiv_rn(fmaxf(amax, 1e-8f), 127.0f);
+}
+
+// A group of TPR threads owns one row, held in registers (VPT 16-byte vectors
+// per thread).  Rows must start 16-byte aligned and cols be a multiple of 16.
+template <typename T, int TPR, int VPT>
+__global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x, int64_t rows,
+                                                        int64_t cols, int64_t ld,
+                                                        int8_t* __restrict__ q,
+                                                        float* __restrict__ scales) {
+    constexpr int EPV = Elem<T>::kPerVec;
+    constexpr int RPB = 256 / TPR;
+    __shared__ float red[8];
+    const int g = threadIdx.x / TPR;
+    const int lg = threadIdx.x % TPR;
+    const int64_t nvec = cols / EPV;
+    for (int64_t row0 = static_cast<int64_t>(blockIdx.x) * RPB; row0 < rows;
+         row0 += static_cast<int64_t>(gridDim.x) * RPB) {
+        const int64_t row = row0 + g;
+        const bool live = row < rows;
+        float v[VPT][EPV];
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
+            if (live && vi < nvec) {
+                uint4 raw = ld_stream_v4(x + row * ld + vi * EPV);
+                Elem<T>::unpack(raw, v[i]);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf(v[i][e]));
+            }
+        }
+        if (TPR <= 32) {
+#pragma unroll
+            for (int o = TPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        } else {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            __syncthreads();   // previous row's readers of red[] are done
+            if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+            __syncthreads();
+            m = red[0];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+        }
+        const float s = row_scale(m);
+        if (live) {
+            if (lg == 0) scales[row] = s;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
+                if (vi < nvec) {
+                    uint32_t packed[EPV / 4];
+#pragma unroll
+                    for (int w = 0; w < EPV / 4; ++w) {
+                        uint32_t b0 = static_cast<uint8_t>(encode_i8(v[i][4 * w + 0], s));
+                        uint32_t b1 = static_cast<uint8_t>(encode_i8(v[i][4 * w + 1], s));
+                        uint32_t b2 = static_cast<uint8_t>(encode_i8(v[i][4 * w + 2], s));
+                        uint32_t b3 = static_cast<uint8_t>(encode_i8(v[i][4 * w + 3], s));
+                        packed[w] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                    }
+                    int8_t* dst = q + row * cols + vi * EPV;
+                    if (EPV == 4) {
+                        *reinterpret_cast<uint32_t*>(dst) = packed[0];
+                    } else {
+                        *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[EPV / 4 - 1]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Any alignment, any row length: one CTA per row, two passes over the row
+// (the second pass is served from L2).
+template <typename T>
+__global__ void __launch_bounds__(256) quant_row_i8_scalar(const T* __restrict__ x, int64_t rows,
+                                                           int64_t cols, int64_t ld,
+                                                           int8_t* __restrict__ q,
+                                                           float* __restrict__ scales) {
+    __shared__ float red[8];
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const T* xr = x + row * ld;
+        float m = 0.0f;
+        for (int64_t k = threadIdx.x; k < cols; k += blockDim.x)
+            m = fmaxf(m, fabsf(Elem<T>::load1(xr + k)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        __syncthreads();
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        m = red[0];
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+        const float s = row_scale(m);
+        if (threadIdx.x == 0) scales[row] = s;
+        for (int64_t k = threadIdx.x; k < cols; k += blockDim.x)
+            q[row * cols + k] = encode_i8(Elem<T>::load1(xr + k), s);
+    }
+}
+
+template <typename T, int TPR, int VPT>
+static cudaError_t launch_row_vec(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
+                                  float* scales, cudaStream_t st, int sms) {
+    constexpr int RPB = 256 / TPR;
+    int64_t blocks = (rows + RPB - 1) / RPB;
+    const int64_t cap = static_cast<int64_t>(sms) * 64;
+    if (blocks > cap) blocks = cap;
+    quant_row_i8_vec<T, TPR, VPT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld,
+                                                                                q, scales);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
+                              float* scales, bool vec_ok, cudaStream_t st, int sms) {
+    constexpr int EPV = Elem<T>::kPerVec;
+    const int64_t nvec = cols / EPV;
+    if (vec_ok) {
+        if (nvec <= 16) return launch_row_vec<T, 16, 1>(x, rows, cols, ld, q, scales, st, sms);
+        if (nvec <= 32) return launch_row_vec<T, 32, 1>(x, rows, cols, ld, q, scales, st, sms);
+        if (nvec <= 64) return launch_row_vec<T, 32, 2>(x, rows, cols, ld, q, scales, st, sms);
+        if (nvec <= 128) return launch_row_vec<T, 32, 4>(x, rows, cols, ld, q, scales, st, sms);
+        if (nvec <= 256) return launch_row_vec<T, 32, 8>(x, rows, cols, ld, q, scales, st, sms);
+        if (nvec <= 512) return launch_row_vec<T, 256, 2>(x, rows, cols, ld, q, scales, st, sms);
+        if (nvec <= 1024) return launch_row_vec<T, 256, 4>(x, rows, cols, ld, q, scales, st, sms);
+        if (nvec <= 2048) return launch_row_vec<T, 256, 8>(x, rows, cols, ld, q, scales, st, sms);
+    }
+    int64_t blocks = rows;
+    const int64_t cap = static_cast<int64_t>(sms) * 64;
+    if (blocks > cap) blocks = cap;
+    quant_row_i8_scalar<T><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, q,
+                                                                          scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols,
+                                       int64_t ld, int8_t* q, float* scales, bool vec_ok,
+                                       cudaStream_t st, int sms) {
+    if (dtype == 0)
+        return launch_row<float>(static_cast<const float*>(x), rows, cols, ld, q, scales, vec_ok,
+                                 st, sms);
+    return launch_row<uint16_t>(static_cast<const uint16_t*>(x), rows, cols, ld, q, scales, vec_ok,
+                                st, sms);
+}
+
+// ================================================================== FP8 tensor
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
+    uint16_t r;
+    if (FMT == 0)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 16 bf16 (two 16-B words) -> 16 FP8 codes (one 16-B word); m = running max|x|.
+template <int FMT>
+__device__ __forceinline__ uint4 fp8_encode16(const uint4& a, const uint4& b, float s, float& m) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float f0 = __uint_as_float(w[2 * i] << 16);
+        float f1 = __uint_as_float(w[2 * i] & 0xFFFF0000u);
+        float f2 = __uint_as_float(w[2 * i + 1] << 16);
+        float f3 = __uint_as_float(w[2 * i + 1] & 0xFFFF0000u);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+        uint32_t lo = fp8x2<FMT>(__fdiv_rn(f0, s), __fdiv_rn(f1, s));
+        uint32_t hi = fp8x2<FMT>(__fdiv_rn(f2, s), __fdiv_rn(f3, s));
+        o[i] = lo | (hi << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Each thread converts 32 elements per step (four 16-B loads in flight).
+template <int FMT>
+__global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                        const float* __restrict__ scale,
+                                                        uint8_t* __restrict__ x8,
+                                                        float* __restrict__ amax_out,
+                                                        unsigned* __restrict__ ws) {
+    __shared__ float red[8];
+    __shared__ int is_last;
+    const float s = *scale;
+    float m = 0.0f;
+    const int64_t nchunk = n / 32;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t c = tid; c < nchunk; c += nthr) {
+        const uint16_t* src = x + c * 32;
+        uint4 a0 = ld_stream_v4(src);
+        uint4 a1 = ld_stream_v4(src + 8);
+        uint4 a2 = ld_stream_v4(src + 16);
+        uint4 a3 = ld_stream_v4(src + 24);
+        uint4 o0 = fp8_encode16<FMT>(a0, a1, s, m);
+        uint4 o1 = fp8_encode16<FMT>(a2, a3, s, m);
+        st_v4(x8 + c * 32, o0);
+        st_v4(x8 + c * 32 + 16, o1);
+    }
+    // ragged tail (< 32 elements)
+    const int64_t tail0 = nchunk * 32;
+    if (tid < n - tail0) {
+        const int64_t i = tail0 + tid;
+        float f = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
+        m = fmaxf(m, fabsf(f));
+        x8[i] = static_cast<uint8_t>(fp8x2<FMT>(__fdiv_rn(f, s), 0.0f) & 0xFFu);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float bm = red[0];
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) bm = fmaxf(bm, red[w]);
+        // max|x| >= 0, so the float order equals the unsigned order of the bits
+        atomicMax(&ws[0], __float_as_uint(bm));
+        __threadfence();
+        const unsigned ticket = atomicAdd(&ws[1], 1u);
+        is_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (is_last && threadIdx.x == 0) {
+        __threadfence();
+        const unsigned bits = atomicExch(&ws[0], 0u);
+        *amax_out = __uint_as_float(bits);
+        atomicExch(&ws[1], 0u);
+    }
+}
+
+cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
+                                uint8_t* x8, float* amax, unsigned* ws, cudaStream_t st,
+                                int sms) {
+    const int64_t nchunk = n / 32;
+    int64_t blocks = (nchunk + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (fmt == 0)
+        quant_fp8_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, n, scale, x8, amax, ws);
+    else
+        quant_fp8_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, n, scale, x8, amax, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace sq

@@ -1,0 +1,32 @@
+// Host-side launchers behind the C ABI (internal to libsq).  Arguments are
+// already validated by the entry points in api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sq {
+
+cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols,
+                                       int64_t ld, int8_t* q, float* scales, bool vec_ok,
+                                       cudaStream_t st, int sms);
+
+cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
+                                uint8_t* x8, float* amax, unsigned* ws, cudaStream_t st, int sms);
+
+// Staging of INT8 codes as exact fp16 values: dst[b][r][k] = src[b*stride + r*K + k].
+cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
+                             int64_t stride, uint16_t* dst, cudaStream_t st, int sms);
+
+// 0 on success, a cudaError_t otherwise; CUDA_ERROR_* from tensor-map encoding
+// is reported as cudaErrorInvalidValue.
+cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                            int fmt, int layout, int M, int N, int K, uint16_t* C,
+                            unsigned* err_word, cudaStream_t st, int sms);
+
+cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
+                           const float* sB, int batch, int M, int N, int K, int64_t strideC,
+                           float* C, int32_t* acc_out, unsigned* err_word, cudaStream_t st,
+                           int sms);
+
+}  // namespace sq

@@ -1,0 +1,175 @@
+/*
+ * sq.h -- absmax-scaled quantization and scaled low-precision GEMM on GB300
+ * (sm_103a).  C ABI of libsq.so.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor pointers are DEVICE pointers (cudaMalloc / torch memory on the
+ *    current device) unless a parameter says otherwise.  The caller owns every
+ *    buffer; the library never allocates or frees device memory, never reads a
+ *    device scalar on the host and never synchronises the stream on these
+ *    paths.  Work is enqueued on `stream` (NULL = the legacy default stream) and
+ *    runs on the device that is current when the call is made.
+ *  - Matrices are row-major and packed unless a leading dimension is given:
+ *    "A[M,K]" means element (i,k) sits at A[i*K + k].
+ *  - A call validates its arguments first and returns SQ_ERR_INVALID_ARG,
+ *    SQ_ERR_UNSUPPORTED or SQ_ERR_ALIGNMENT without enqueuing anything when a
+ *    check fails.  A launch failure returns SQ_ERR_CUDA.  Errors raised inside
+ *    a kernel (a bounded wait that ran out) are recorded on the device and read
+ *    back by sq_get_last_device_error().
+ *  - Inputs are finite.  Results for NaN or infinite inputs are unspecified.
+ *  - Calls that share a workspace must not overlap on the GPU (use one
+ *    workspace per stream).
+ *
+ * Sources (the three pages on the subject):
+ *  [P2] POPCORNBENCH "Kimi-K2.6 l2_p13" trace: the INT8 fake-quant formula
+ *       (amax = max|x| floored at 1e-8, scale = amax/127,
+ *       q = clamp(round(x/scale), -127, 127)) and its rounding discussion
+ *       (torch.round rounds halves to even, so roundf is wrong).
+ *  [P1] scmp_kernels README, SC quickstart and sc_matmul API: per-row and
+ *       per-head ("per_head requires 3D") granularity, C = a @ b.T with float32
+ *       in and out.
+ *  [P3] AstrAI astrai/extension/ops/fp8.py: module docstring (scales are
+ *       quantization steps divided out, x8 = x / scale; amax is returned),
+ *       custom::fp8_quantize (bf16 in, fused amax), custom::fp8_gemm
+ *       (a @ b * (sa * sb), FP32 accumulation, BF16 out), the fmt map
+ *       (0 = E4M3, 1 = E5M2) and the commit notes (last-block amax epilogue,
+ *       NT forward, crosswise dX/dW operands).
+ */
+#ifndef SQ_H_
+#define SQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* sq_stream;
+
+typedef enum {
+    SQ_OK = 0,
+    SQ_ERR_INVALID_ARG = 1,    /* a size, pointer, dtype, fmt or layout is invalid      */
+    SQ_ERR_UNSUPPORTED = 2,    /* valid but not implemented here (e.g. shape limits)     */
+    SQ_ERR_ALIGNMENT = 3,      /* a pointer or leading dimension breaks the 16-B rules  */
+    SQ_ERR_CUDA = 4,           /* the CUDA runtime reported an error                     */
+    SQ_ERR_DEVICE_TIMEOUT = 5  /* a kernel's bounded wait ran out (kernel returned early) */
+} sq_status;
+
+typedef enum { SQ_F32 = 0, SQ_BF16 = 1 } sq_dtype;
+
+/* Matches the fmt integers of [P3] (_FMT_TO_INT). */
+typedef enum { SQ_FMT_E4M3 = 0, SQ_FMT_E5M2 = 1 } sq_fp8_fmt;
+
+/* GEMM operand layouts (all row-major):
+ *   SQ_NT: A[M,K], B[N,K], C = A * B^T   (forward, X * W^T)
+ *   SQ_NN: A[M,K], B[K,N], C = A * B     (dX = G * W)
+ *   SQ_TN: A[K,M], B[K,N], C = A^T * B   (dW = G^T * X)                        */
+typedef enum { SQ_NT = 0, SQ_NN = 1, SQ_TN = 2 } sq_layout;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* sq_status_string(sq_status s);
+
+/* Bytes of workspace that sq_quantize_fp8 needs.  The caller allocates it once
+ * per stream, 16-byte aligned, and zeroes it once (cudaMemset to 0); every
+ * completed call leaves it zeroed again, so no per-call memset is needed. */
+size_t sq_workspace_bytes(void);
+
+/*
+ * Per-row symmetric INT8 quantization  [P2 formula; P1 per_row / per_head].
+ *
+ *   amax_r = max_k |x[r,k]|,  s_r = fl32(max(amax_r, 1e-8f) / 127),
+ *   q[r,k] = clamp(rne(fl32(x[r,k] / s_r)), -127, 127)
+ *
+ * with one IEEE float32 division per element and ties rounded to even.
+ * Per-head quantization of a (H, N, D) tensor is this call with rows = H*N,
+ * cols = D.
+ *
+ *   x       [rows, cols] with row stride `ld` elements (ld >= cols); float32
+ *           (dtype SQ_F32) or bf16 (SQ_BF16).
+ *   q       [rows, cols] int8, packed (row stride cols).
+ *   scales  [rows] float32.
+ * rows == 0 or cols == 0 is a no-op (returns SQ_OK; cols == 0 with rows > 0
+ * writes nothing).  Any alignment works; 16-byte aligned rows (x, q 16-B
+ * aligned, ld*elemsize and cols multiples of 16) take the vectorised path.
+ */
+sq_status sq_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols,
+                                 int64_t ld, int8_t* q, float* scales, sq_stream stream);
+
+/*
+ * Per-tensor FP8 quantization of bf16 with the amax fused in  [P3
+ * custom::fp8_quantize; commit notes: last-block epilogue, no extra launch].
+ *
+ *   x8[i] = enc_fmt(fl32(x[i] / *scale))   (RNE, saturating to +-448 / +-57344)
+ *   *amax = max_i |x[i]|                  (raw, no floor; 0 for numel == 0)
+ *
+ *   x_bf16     [numel] bf16, 16-byte aligned.
+ *   scale      device pointer to one float32, the quantization step (> 0).
+ *   fmt        SQ_FMT_E4M3 or SQ_FMT_E5M2.
+ *   x8         [numel] FP8 codes (uint8), 16-byte aligned.
+ *   amax       device pointer to one float32, written by the call.
+ *   workspace  sq_workspace_bytes() bytes, zeroed once by the caller.
+ */
+sq_status sq_quantize_fp8(const uint16_t* x_bf16, int64_t numel, const float* scale, int fmt,
+                          uint8_t* x8, float* amax, void* workspace, sq_stream stream);
+
+/*
+ * Bytes of workspace that sq_gemm_i8_rowscaled needs for these sizes (the
+ * INT8 codes are staged as exact 16-bit values for the tensor cores).
+ */
+size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K);
+
+/*
+ * INT8 GEMM with the per-row x per-row dequantization epilogue  [P1
+ * sc_matmul: C = a @ b.T, float32 out, per_row / per_head; P2 codes].
+ *
+ *   acc[b,i,j] = sum_k A[b,i,k] * B[b,j,k]             (exact, int32)
+ *   C[b,i,j]   = fl32(fl32(float(acc) * sA[b*M+i]) * sB[b*N+j])
+ *
+ *   A        int8 codes, batch b at A + b*strideA, [M,K] packed rows.
+ *   B        int8 codes, batch b at B + b*strideB, [N,K] packed rows.
+ *   sA, sB   float32 row scales, [batch*M] and [batch*N].
+ *   C        float32, batch b at C + b*strideC, [M,N] packed rows (nullable).
+ *   acc_out  int32, same layout as C (nullable).  At least one of C, acc_out.
+ *   workspace  sq_gemm_i8_workspace_bytes(batch, M, N, K) bytes, 256-B aligned,
+ *              contents need no initialisation.
+ * Limits: K a multiple of 16, 1 <= K <= 2^17 (so |acc| < 2^31 always), strides
+ * >= the packed batch sizes; all pointers 16-byte aligned.
+ */
+sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B,
+                               const float* sB, int64_t batch, int64_t M, int64_t N, int64_t K,
+                               int64_t strideA, int64_t strideB, int64_t strideC, float* C,
+                               int32_t* acc_out, void* workspace, size_t workspace_bytes,
+                               sq_stream stream);
+
+/*
+ * Scaled FP8 GEMM  [P3 custom::fp8_gemm: a @ b * (sa * sb), FP32 accumulate,
+ * BF16 out; layouts per the commit notes: NT forward, dX and dW].
+ *
+ *   C[i,j] = bf16_rne(fl32(fl32(acc[i,j] * *sa) * *sb)),  acc in float32
+ *
+ *   A, B     FP8 codes of the same fmt, laid out per `layout` (see sq_layout).
+ *   sa, sb   device pointers to one float32 each (quantization steps).
+ *   C_bf16   [M,N] bf16 output, packed rows.
+ * Limits: every operand's row length in bytes (K for NT; K and N for NN; M and
+ * N for TN) a multiple of 16; pointers 16-byte aligned; M, N, K >= 1.
+ */
+sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa,
+                             const float* sb, int fmt, int layout, int64_t M, int64_t N,
+                             int64_t K, uint16_t* C_bf16, sq_stream stream);
+
+/*
+ * Reads and clears the device-side error word of the current device after
+ * synchronising `stream`.  Returns SQ_ERR_DEVICE_TIMEOUT if a kernel gave up
+ * on a bounded wait since the last call, SQ_ERR_CUDA on a runtime error,
+ * else SQ_OK.
+ */
+sq_status sq_get_last_device_error(sq_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SQ_H_ */

@@ -1,0 +1,85 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every
+symbol include/sq.h declares, and rejects bad arguments before touching a
+device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import absmax_quantized_precision_gb300 as sq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return sq.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "sq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names, "no declarations found"
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(sq.EXPORTS)
+
+
+def test_exported_symbols_are_c_linkage():
+    out = os.popen(f"nm -D --defined-only {sq.LIB_PATH}").read()
+    for n in declared_functions():
+        assert re.search(rf"\sT\s{n}$", out, flags=re.M), n
+
+
+def test_status_strings_and_sizes(lib):
+    for s in range(6):
+        assert sq.status_string(s).startswith("SQ_")
+    assert sq.workspace_bytes() >= 8
+    assert sq.gemm_i8_workspace_bytes(1, 128, 512, 1024) == 128 * 1024 * 2 + 512 * 1024 * 2
+    assert sq.gemm_i8_workspace_bytes(0, 1, 1, 1) == 0
+
+
+def test_invalid_arguments_are_rejected_without_a_device(lib):
+    null = ctypes.c_void_p(0)
+    # bad dtype / negative sizes
+    assert lib.sq_quantize_rowwise_i8(null, 7, 1, 1, 1, null, null, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_rowwise_i8(null, 0, -1, 1, 1, null, null, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_rowwise_i8(null, 0, 2, 8, 4, null, null, null) == sq.SQ_ERR_INVALID_ARG
+    # empty input is a no-op
+    assert lib.sq_quantize_rowwise_i8(null, 0, 0, 8, 8, null, null, null) == sq.SQ_OK
+    # fp8: bad fmt, missing scale
+    assert lib.sq_quantize_fp8(null, 16, null, 5, null, null, null, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_fp8(null, 16, null, 0, null, null, null, null) == sq.SQ_ERR_INVALID_ARG
+    # misaligned FP8 operands
+    p1 = ctypes.c_void_p(0x1001)
+    p = ctypes.c_void_p(0x1000)
+    assert lib.sq_quantize_fp8(p1, 16, p, 0, p, p, p, null) == sq.SQ_ERR_ALIGNMENT
+    # gemm: bad layout, K not a multiple of 16, K too long
+    assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 9, 16, 16, 16, p, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 0, 16, 16, 24, p, null) == sq.SQ_ERR_ALIGNMENT
+    assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 1, 16, 24, 32, p, null) == sq.SQ_ERR_ALIGNMENT
+    assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 2, 24, 16, 32, p, null) == sq.SQ_ERR_ALIGNMENT
+    assert lib.sq_gemm_fp8_scaled(p1, p, p, p, 0, 0, 16, 16, 16, p, null) == sq.SQ_ERR_ALIGNMENT
+    assert lib.sq_gemm_i8_rowscaled(p, p, p, p, 1, 4, 4, 24, 96, 96, 16, p, null, p, 1 << 20,
+                                    null) == sq.SQ_ERR_ALIGNMENT
+    assert lib.sq_gemm_i8_rowscaled(p, p, p, p, 1, 4, 4, 1 << 18, 1 << 20, 1 << 20, 16, p, null,
+                                    p, 1 << 30, null) == sq.SQ_ERR_UNSUPPORTED
+    assert lib.sq_gemm_i8_rowscaled(p, p, p, p, 1, 4, 4, 16, 64, 64, 16, null, null, p, 1 << 20,
+                                    null) == sq.SQ_ERR_INVALID_ARG
+    # workspace too small
+    assert lib.sq_gemm_i8_rowscaled(p, p, p, p, 1, 4, 4, 16, 64, 64, 16, p, null, p, 8,
+                                    null) == sq.SQ_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        sq.sq_quantize_rowwise_i8(torch.zeros(4, 16))

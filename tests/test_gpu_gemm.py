@@ -1,0 +1,216 @@
+"""GPU parity of the tcgen05 GEMMs against the oracle.
+
+INT8: int32 accumulators and the fp32 dequantized output bit-exact.
+FP8:  bf16 output within 1e-2*|ref| + 1e-3*sqrt(K)*sa*sb*max|a8|*max|b8| of
+the fp64 reference, in the NT, NN and TN layouts, E4M3 and E5M2.
+Shapes cover several tiles, ragged M/N tails and the pages' workloads.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import absmax_quantized_precision_gb300 as sq
+import oracle
+import synth
+from gpu_util import DEV, bf16_to_f64, guard_intact, guarded, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    yield
+    assert sq.sq_get_last_device_error() == sq.SQ_OK
+
+
+def seed_of(name):
+    return zlib.crc32(name.encode()) % 10000
+
+
+# ------------------------------------------------------------------ INT8
+def run_i8(qa, sa, qb, sb):
+    batch = qa.shape[0] if qa.ndim == 3 else 1
+    M, K = qa.shape[-2:]
+    N = qb.shape[-2]
+    ws = torch.empty(sq.gemm_i8_workspace_bytes(batch, M, N, K), dtype=torch.uint8, device=DEV)
+    C, acc = sq.sq_gemm_i8_rowscaled(to_dev(qa), to_dev(sa), to_dev(qb), to_dev(sb), ws,
+                                     acc_out=True)
+    return C.cpu().numpy(), acc.cpu().numpy()
+
+
+I8_CASES = [
+    ("cfg1 128x512x1024 f32 N(0,1)", (128, 1024), (512, 1024)),
+    ("ragged 200x300x160", (200, 160), (300, 160)),
+    ("single tile 1x1x16", (1, 16), (1, 16)),
+    ("K 3072 (3 chunks) 256x384", (256, 3072), (384, 3072)),
+    ("K 1040 (chunk + tail) 130x129", (130, 1040), (129, 1040)),
+]
+
+
+@pytest.mark.parametrize("name,sa_shape,sb_shape", I8_CASES, ids=[c[0] for c in I8_CASES])
+def test_i8_gemm_parity(name, sa_shape, sb_shape):
+    s = seed_of(name)
+    a, b = synth.normal(s, sa_shape), synth.normal(s + 1, sb_shape)
+    qa, sa = oracle.quantize_rowwise_i8(a)
+    qb, sb = oracle.quantize_rowwise_i8(b)
+    oacc, oC = oracle.gemm_i8(qa, qb, sa, sb)
+    C, acc = run_i8(qa, sa, qb, sb)
+    assert np.array_equal(acc, oacc)
+    assert np.array_equal(C, oC)
+
+
+def test_i8_gemm_per_head_batched():
+    """16 heads of (196x64) . (196x64)^T, per-row scales within each head."""
+    q = synth.normal(41, (16, 196, 64))
+    k = synth.normal(42, (16, 196, 64))
+    qq, sq_ = oracle.quantize_rowwise_i8(q)
+    qk, sk = oracle.quantize_rowwise_i8(k)
+    oacc, oC = oracle.gemm_i8(qq, qk, sq_, sk)
+    C, acc = run_i8(qq, sq_, qk, sk)
+    assert acc.shape == (16, 196, 196)
+    assert np.array_equal(acc, oacc) and np.array_equal(C, oC)
+
+
+def test_i8_gemm_extreme_codes_stay_exact():
+    """All codes +-127 with K = 8192: every chunk sum sits at 127^2*1024 and
+    the total at 1.3e8 > 2^24, so any inexact accumulation shows."""
+    rng = np.random.default_rng(5)
+    M, N, K = 256, 256, 8192
+    qa = np.where(rng.random((M, K)) < 0.5, 127, -127).astype(np.int8)
+    qa[:8] = 127
+    qb = np.where(rng.random((N, K)) < 0.5, 127, -127).astype(np.int8)
+    qb[:8] = 127
+    qb[8:16] = -127
+    sa = np.abs(synth.normal(6, (M,))) + np.float32(1e-3)
+    sb = np.abs(synth.normal(7, (N,))) + np.float32(1e-3)
+    oacc, oC = oracle.gemm_i8(qa, qb, sa, sb)
+    C, acc = run_i8(qa, sa, qb, sb)
+    assert acc[0, 0] == 127 * 127 * K and acc[0, 8] == -127 * 127 * K
+    assert np.array_equal(acc, oacc) and np.array_equal(C, oC)
+
+
+def test_i8_gemm_random_codes_and_acc_only():
+    rng = np.random.default_rng(6)
+    qa = rng.integers(-127, 128, (300, 2048)).astype(np.int8)
+    qb = rng.integers(-127, 128, (260, 2048)).astype(np.int8)
+    oacc, _ = oracle.gemm_i8(qa, qb)
+    ws = torch.empty(sq.gemm_i8_workspace_bytes(1, 300, 260, 2048), dtype=torch.uint8, device=DEV)
+    ones_a = torch.ones(300, device=DEV)
+    ones_b = torch.ones(260, device=DEV)
+    acc, abuf, n = guarded((300, 260), torch.int32, -7)
+    C, acc = sq.sq_gemm_i8_rowscaled(to_dev(qa), ones_a, to_dev(qb), ones_b, ws, want_c=False,
+                                     acc_out=acc)
+    assert C is None
+    assert np.array_equal(acc.cpu().numpy(), oacc)
+    assert guard_intact(abuf, n, -7)
+
+
+# ------------------------------------------------------------------ FP8
+def fp8_inputs(name, M, N, K, fmt, std_a=1.0, std_b=0.02):
+    s = seed_of(name)
+    xa = synth.normal(s, (M, K), std=std_a, dtype=synth.BF16)
+    xb = synth.normal(s + 1, (N, K), std=std_b, dtype=synth.BF16)
+    fmax = 448.0 if fmt == 0 else 57344.0
+    pa = synth.bf16_bits_to_f32(synth.normal(s + 2, (M, K), std=std_a, dtype=synth.BF16))
+    pb = synth.bf16_bits_to_f32(synth.normal(s + 3, (N, K), std=std_b, dtype=synth.BF16))
+    sa = np.float32(np.abs(pa).max()) / np.float32(fmax)
+    sb = np.float32(np.abs(pb).max()) / np.float32(fmax)
+    a8, _ = oracle.quantize_fp8(xa, sa, fmt)
+    b8, _ = oracle.quantize_fp8(xb, sb, fmt)
+    return a8, b8, sa, sb
+
+
+def check_fp8(out, A8, B8, fmt, layout, K, sa, sb, rows=None):
+    ref, obf = oracle.gemm_fp8(A8, B8, fmt, layout, sa, sb, rows=rows)
+    tab = oracle.fp8_decode_table(fmt)
+    bound = oracle.fp8_gemm_bound(ref, K, sa, sb, np.abs(tab[A8]).max(), np.abs(tab[B8]).max())
+    got = bf16_to_f64(out)
+    if rows is not None:
+        got = got[rows]
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3g}"
+    # the bf16 codes agree with the oracle's rounding of the fp32 result almost everywhere
+    same = np.mean(out.view(torch.int16).cpu().numpy().astype(np.uint16)[
+        rows if rows is not None else slice(None)] == obf)
+    assert same > 0.9, same
+
+
+FP8_SHAPES = [
+    ("one tile 128x128x128", 128, 128, 128),
+    ("multi 256x384x512", 256, 384, 512),
+    ("ragged 200x176x320", 200, 176, 320),
+    ("wide 128x1024x256", 128, 1024, 256),
+    ("deep 130x144x2048", 130, 144, 2048),
+    ("short K 160x96x16", 160, 96, 16),
+]
+
+
+@pytest.mark.parametrize("layout", [sq.SQ_NT, sq.SQ_NN, sq.SQ_TN], ids=["NT", "NN", "TN"])
+@pytest.mark.parametrize("name,M,N,K", FP8_SHAPES, ids=[c[0] for c in FP8_SHAPES])
+def test_fp8_gemm_layouts(name, M, N, K, layout):
+    fmt = sq.SQ_FMT_E4M3
+    if layout == sq.SQ_TN and M % 16:
+        M += 16 - M % 16
+    a8, b8, sa, sb = fp8_inputs(name, M, N, K, fmt)
+    if layout == sq.SQ_NT:
+        A, B = a8, b8
+    elif layout == sq.SQ_NN:
+        A, B = a8, np.ascontiguousarray(b8.T)
+    else:
+        A, B = np.ascontiguousarray(a8.T), np.ascontiguousarray(b8.T)
+    C, cbuf, n = guarded((M, N), torch.bfloat16, 3.0)
+    sq.sq_gemm_fp8_scaled(to_dev(A), to_dev(B), torch.tensor([sa], device=DEV),
+                          torch.tensor([sb], device=DEV), fmt, layout, C=C)
+    check_fp8(C, A, B, fmt, layout, K, sa, sb)
+    assert guard_intact(cbuf, n, 3.0)
+
+
+@pytest.mark.parametrize("layout", [sq.SQ_NT, sq.SQ_NN, sq.SQ_TN], ids=["NT", "NN", "TN"])
+def test_fp8_gemm_e5m2(layout):
+    M, N, K = 256, 256, 1024
+    fmt = sq.SQ_FMT_E5M2
+    a8, b8, sa, sb = fp8_inputs("e5m2", M, N, K, fmt)
+    A = a8 if layout != sq.SQ_TN else np.ascontiguousarray(a8.T)
+    B = b8 if layout == sq.SQ_NT else np.ascontiguousarray(b8.T)
+    C = sq.sq_gemm_fp8_scaled(to_dev(A), to_dev(B), torch.tensor([sa], device=DEV),
+                              torch.tensor([sb], device=DEV), fmt, layout)
+    check_fp8(C, A, B, fmt, layout, K, sa, sb)
+
+
+def test_fp8_forward_nt_2048x1024x1024():
+    """X bf16 2048x1024 N(0,1), W bf16 1024x1024 N(0,0.02), delayed scales."""
+    M, N, K = 2048, 1024, 1024
+    a8, b8, sa, sb = fp8_inputs("fwd", M, N, K, 0)
+    C = sq.sq_gemm_fp8_scaled(to_dev(a8), to_dev(b8), torch.tensor([sa], device=DEV),
+                              torch.tensor([sb], device=DEV), 0, sq.SQ_NT)
+    rows = np.sort(np.random.default_rng(1).choice(M, 256, replace=False))
+    check_fp8(C, a8, b8, 0, sq.SQ_NT, K, sa, sb, rows=rows)
+
+
+def test_fp8_backward_dx_nn_and_dw_tn():
+    """MLP backward, dim 1024, hidden 4096, 2048 tokens, all E4M3:
+    dX = G W (NN) with G 2048x4096, W 4096x1024; dW = G^T X (TN)."""
+    T, H, D = 2048, 4096, 1024
+    fmt = 0
+    g = synth.normal(51, (T, H), std=1e-3, dtype=synth.BF16)
+    w = synth.normal(52, (H, D), std=0.02, dtype=synth.BF16)
+    x = synth.normal(53, (T, D), std=1.0, dtype=synth.BF16)
+
+    def scale_of(seed, shape, std):
+        p = synth.bf16_bits_to_f32(synth.normal(seed, shape, std=std, dtype=synth.BF16))
+        return np.float32(np.abs(p).max()) / np.float32(448.0)
+
+    sg, sw, sx = scale_of(61, (T, H), 1e-3), scale_of(62, (H, D), 0.02), scale_of(63, (T, D), 1.0)
+    g8, _ = oracle.quantize_fp8(g, sg, fmt)
+    w8, _ = oracle.quantize_fp8(w, sw, fmt)
+    x8, _ = oracle.quantize_fp8(x, sx, fmt)
+    tsg, tsw, tsx = (torch.tensor([v], device=DEV) for v in (sg, sw, sx))
+    dX = sq.sq_gemm_fp8_scaled(to_dev(g8), to_dev(w8), tsg, tsw, fmt, sq.SQ_NN)
+    rows = np.sort(np.random.default_rng(2).choice(T, 128, replace=False))
+    check_fp8(dX, g8, w8, fmt, sq.SQ_NN, H, sg, sw, rows=rows)
+    dW = sq.sq_gemm_fp8_scaled(to_dev(g8), to_dev(x8), tsg, tsx, fmt, sq.SQ_TN)
+    assert dW.shape == (H, D)
+    rows = np.sort(np.random.default_rng(3).choice(H, 128, replace=False))
+    check_fp8(dW, g8, x8, fmt, sq.SQ_TN, T, sg, sx, rows=rows)

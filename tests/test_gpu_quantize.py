@@ -1,0 +1,142 @@
+"""GPU parity of the quantize kernels against the oracle: bit-exact INT8 codes,
+row scales, FP8 codes and amax, on the pages' shapes plus ragged, strided,
+degenerate and long-row cases."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import absmax_quantized_precision_gb300 as sq
+import oracle
+import synth
+from gpu_util import DEV, guard_intact, guarded, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    yield
+    assert sq.sq_get_last_device_error() == sq.SQ_OK
+
+
+ROW_CASES = [
+    # (name, shape, dtype, draw)
+    ("int8 per-row A 128x1024 f32", (128, 1024), "f32", "normal"),
+    ("int8 per-row B 512x1024 f32", (512, 1024), "f32", "normal"),
+    ("int8 per-head Q 16x196x64 f32", (16, 196, 64), "f32", "normal"),
+    ("bf16 t3 300x8192 (CTA per row)", (300, 8192), "bf16", "t3"),
+    ("bf16 64x2048", (64, 2048), "bf16", "normal"),
+    ("f32 7x4096", (7, 4096), "f32", "t3"),
+    ("f32 ragged 37x17 (scalar path)", (37, 17), "f32", "normal"),
+    ("bf16 long rows 5x40000 (scalar path)", (5, 40000), "bf16", "t3"),
+    ("f32 tiny rows 1000x16", (1000, 16), "f32", "normal"),
+    ("bf16 1x8", (1, 8), "bf16", "normal"),
+]
+
+
+def draw(seed, shape, dt, kind):
+    d = synth.F32 if dt == "f32" else synth.BF16
+    if kind == "t3":
+        return synth.student_t(seed, shape, df=3, dtype=d)
+    return synth.normal(seed, shape, dtype=d)
+
+
+@pytest.mark.parametrize("name,shape,dt,kind", ROW_CASES, ids=[c[0] for c in ROW_CASES])
+def test_rowwise_i8_parity(name, shape, dt, kind):
+    x = draw(zlib.crc32(name.encode()) % 1000 + 10, shape, dt, kind)
+    oq, osc = oracle.quantize_rowwise_i8(x, oracle.F32 if dt == "f32" else oracle.BF16)
+    q, s = sq.sq_quantize_rowwise_i8(to_dev(x, bf16=(dt == "bf16")))
+    assert np.array_equal(s.cpu().numpy(), osc)
+    assert np.array_equal(q.cpu().numpy(), oq)
+
+
+def test_rowwise_i8_strided_rows_and_guard():
+    full = synth.normal(21, (96, 1040))
+    xd = to_dev(full)[:, :1024]          # row stride 1040 elements
+    oq, osc = oracle.quantize_rowwise_i8(np.ascontiguousarray(full[:, :1024]))
+    q, qbuf, n = guarded((96, 1024), torch.int8, 77)
+    s, sbuf, ns = guarded((96,), torch.float32, -5.0)
+    sq.sq_quantize_rowwise_i8(xd, q=q, scales=s)
+    assert np.array_equal(q.cpu().numpy(), oq) and np.array_equal(s.cpu().numpy(), osc)
+    assert guard_intact(qbuf, n, 77) and guard_intact(sbuf, ns, -5.0)
+
+
+def test_rowwise_i8_degenerate_rows_and_ties():
+    x = synth.normal(22, (6, 64))
+    x[0] = 0.0                              # all-zero row -> floor scale, zeros
+    x[1] = 1e-12                            # below the 1e-8 floor
+    x[2] = (np.arange(64) - 32) / 2.0       # many exact ties after scaling
+    x[2, 0] = 127.0
+    x[3] = -x[3]
+    x[4] = np.float32(3.0e38) * np.sign(x[4])   # huge but finite
+    x = x.astype(np.float32)
+    oq, osc = oracle.quantize_rowwise_i8(x)
+    q, s = sq.sq_quantize_rowwise_i8(to_dev(x))
+    assert np.array_equal(s.cpu().numpy(), osc) and np.array_equal(q.cpu().numpy(), oq)
+
+
+def test_rowwise_i8_empty():
+    q, s = sq.sq_quantize_rowwise_i8(torch.empty((0, 64), device=DEV))
+    assert q.shape == (0, 64) and s.shape == (0,)
+
+
+# ------------------------------------------------------------------ FP8
+def delayed_scale(seed, shape, std, fmt):
+    prev = synth.bf16_bits_to_f32(synth.normal(seed + 1, shape, std=std, dtype=synth.BF16))
+    fmax = 448.0 if fmt == sq.SQ_FMT_E4M3 else 57344.0
+    return np.float32(np.abs(prev).max()) / np.float32(fmax)
+
+
+FP8_CASES = [
+    ("X 2048x1024 N(0,1)", (2048, 1024), 1.0),
+    ("W 1024x1024 N(0,0.02)", (1024, 1024), 0.02),
+    ("G 2048x4096 N(0,1e-3)", (2048, 4096), 1e-3),
+    ("tail 1000003", (1000003,), 1.0),
+    ("tail 33", (33,), 1.0),
+    ("one", (1,), 1.0),
+]
+
+
+@pytest.mark.parametrize("fmt", [sq.SQ_FMT_E4M3, sq.SQ_FMT_E5M2], ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("name,shape,std", FP8_CASES, ids=[c[0] for c in FP8_CASES])
+def test_fp8_quantize_parity(name, shape, std, fmt):
+    seed = zlib.crc32(name.encode()) % 1000 + 100
+    x = synth.normal(seed, shape, std=std, dtype=synth.BF16)
+    scale = delayed_scale(seed, shape, std, fmt)
+    ox8, oamax = oracle.quantize_fp8(x, scale, fmt)
+    ws = sq.new_workspace(DEV)
+    x8, amax = sq.sq_quantize_fp8(to_dev(x, bf16=True),
+                                  torch.tensor([scale], dtype=torch.float32, device=DEV), fmt, ws)
+    assert np.array_equal(x8.cpu().numpy(), ox8)
+    assert amax.item() == float(oamax)
+    assert int(ws.sum().item()) == 0        # the last block reset the workspace
+
+
+def test_fp8_saturation_and_repeated_calls():
+    x = synth.student_t(31, (4096, 512), dtype=synth.BF16)
+    ws = sq.new_workspace(DEV)
+    xd = to_dev(x, bf16=True)
+    for fmt, scale in ((sq.SQ_FMT_E4M3, 1e-3), (sq.SQ_FMT_E5M2, 1e-6), (sq.SQ_FMT_E4M3, 0.5)):
+        ox8, oamax = oracle.quantize_fp8(x, scale, fmt)
+        x8, amax = sq.sq_quantize_fp8(xd, torch.tensor([scale], dtype=torch.float32, device=DEV),
+                                      fmt, ws)
+        assert np.array_equal(x8.cpu().numpy(), ox8)
+        assert amax.item() == float(oamax)
+    # a smaller tensor right after: amax must not leak from the previous call
+    y = synth.normal(32, (777,), std=1e-3, dtype=synth.BF16)
+    oy8, oyamax = oracle.quantize_fp8(y, 1e-5, 0)
+    y8, yamax = sq.sq_quantize_fp8(to_dev(y, bf16=True),
+                                   torch.tensor([1e-5], dtype=torch.float32, device=DEV), 0, ws)
+    assert np.array_equal(y8.cpu().numpy(), oy8) and yamax.item() == float(oyamax)
+
+
+def test_fp8_empty_and_zero():
+    ws = sq.new_workspace(DEV)
+    one = torch.ones(1, dtype=torch.float32, device=DEV)
+    _, amax = sq.sq_quantize_fp8(torch.empty(0, dtype=torch.bfloat16, device=DEV), one, 0, ws)
+    assert amax.item() == 0.0
+    z = torch.zeros(4096, dtype=torch.bfloat16, device=DEV)
+    z8, amax = sq.sq_quantize_fp8(z, one, 0, ws)
+    assert amax.item() == 0.0 and int(z8.sum().item()) == 0
