@@ -35,18 +35,25 @@ WORKLOAD = ("large: M=16384 N=8192 K=8192, A/B bf16 Student-t(3) seeded; FP8 E4M
             "delayed-scale quantize+NT GEMM (bf16 out) and INT8 per-row quantize+GEMM "
             "(exact int32 acc, fp32 out)")
 FLOPS_PER_STEP = 2 * (2.0 * M * N * K)
-CPU_SAMPLE_ROWS = 24
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="sq", choices=["sq", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--size", type=int, nargs=3, metavar=("M", "N", "K"),
+                    help="override the workload sizes (small cases for profiler captures)")
+    args = ap.parse_args()
+    if args.size:
+        global M, N, K, FLOPS_PER_STEP, WORKLOAD
+        M, N, K = args.size
+        FLOPS_PER_STEP = 2 * (2.0 * M * N * K)
+        WORKLOAD = WORKLOAD.replace("M=16384 N=8192 K=8192", f"M={M} N={N} K={K}")
+    return args
 
 
 def peaks():
@@ -60,41 +67,50 @@ def peaks():
 
 
 class Clocks:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with single-shot nvidia-smi queries
+    from a background thread while the timed region runs."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_s=0.1):
         self.index = index
-        self.proc = None
+        self.period = period_s
+        self.lines = []
+        self.errors = []
+
+    def _loop(self):
+        while not self._stop.is_set():
+            try:
+                r = subprocess.run(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                    "--format=csv,noheader,nounits"],
+                                   capture_output=True, text=True, timeout=10)
+                if r.returncode == 0:
+                    self.lines += [l for l in r.stdout.splitlines() if l.strip()]
+                elif len(self.errors) < 3:
+                    self.errors.append(r.stderr.strip()[:200])
+            except Exception as e:   # no nvidia-smi: no samples
+                if len(self.errors) < 3:
+                    self.errors.append(str(e)[:200])
+                return
+            self._stop.wait(self.period)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+        import threading
+        self._stop = threading.Event()
+        self._thr = threading.Thread(target=self._loop, daemon=True)
+        self._thr.start()
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except Exception:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        self._stop.set()
+        self._thr.join(timeout=15)
 
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        for l in self.lines:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -106,11 +122,13 @@ class Clocks:
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        loaded = [s for s in sm if mx is None or s > 0.5 * mx] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        if sm:
+            loaded = [x for x in sm if mx is None or x > 0.5 * mx] or sm
+            out["sm_mhz"] = statistics.median(loaded)
+        if self.errors:
+            out["errors"] = self.errors
+        return out
 
 
 def make_inputs():
@@ -129,24 +147,29 @@ def make_inputs():
 
 
 # ---------------------------------------------------------------- CPU oracle leg
-def cpu_oracle_sample(a, b, sa, sb, rows):
-    """The oracle on a bounded sample of the same step: quantize the sampled
-    rows of A and all of B (FP8 and INT8), then those rows of both GEMMs.
-    Returns (seconds, flops of the sampled GEMM rows, threads)."""
+def cpu_oracle_sample(a, b, sa, sb, rows_a, b0, b1):
+    """The oracle on a bounded sample of one step: FP8 and INT8 quantization of
+    the sampled rows of A and of rows b0..b1 of B, then the sampled block of
+    both GEMMs (full K).  Returns (seconds, GEMM flops of the block, threads)."""
     import numpy as np
 
     import oracle
-    r = np.asarray(rows)
+    r = np.asarray(rows_a)
     t0 = time.perf_counter()
     a_rows = np.ascontiguousarray(a[r])
+    b_rows = np.ascontiguousarray(b[b0:b1])
     a8, _ = oracle.quantize_fp8(a_rows, sa, oracle.E4M3)
-    b8, _ = oracle.quantize_fp8(b, sb, oracle.E4M3)
+    b8, _ = oracle.quantize_fp8(b_rows, sb, oracle.E4M3)
     oracle.gemm_fp8(a8, b8, oracle.E4M3, oracle.NT, sa, sb)
     qa, ssa = oracle.quantize_rowwise_i8(a_rows, oracle.BF16)
-    qb, ssb = oracle.quantize_rowwise_i8(b, oracle.BF16)
+    qb, ssb = oracle.quantize_rowwise_i8(b_rows, oracle.BF16)
     oracle.gemm_i8(qa, qb, ssa, ssb)
     dt = time.perf_counter() - t0
-    return dt, 2 * (2.0 * len(r) * N * K), oracle.num_threads()
+    return dt, 2 * (2.0 * len(r) * (b1 - b0) * K), oracle.num_threads()
+
+
+REF_ROWS_A, REF_ROWS_B = 2, 512          # per step of the reference arm
+CPU_ROWS_A = 4096                        # the one-off CPU baseline: 4096 rows x all of B
 
 
 def run_reference(args, rank, world):
@@ -160,13 +183,16 @@ def run_reference(args, rank, world):
     rng = np.random.default_rng(0)
     times, flops, thr = [], 0.0, 1
     for i in range(args.warmup + args.steps):
-        rows = np.sort(rng.choice(M, CPU_SAMPLE_ROWS // 3, replace=False))
-        dt, fl, thr = cpu_oracle_sample(a, b, sa, sb, rows)
+        rows = np.sort(rng.choice(M, REF_ROWS_A, replace=False))
+        b0 = int(rng.integers(0, N - REF_ROWS_B + 1))
+        dt, fl, thr = cpu_oracle_sample(a, b, sa, sb, rows, b0, b0 + REF_ROWS_B)
         if i >= args.warmup:
             times.append(dt)
-            flops = fl
+            flops += fl
     tot = sum(times)
-    value = flops * len(times) / tot / 1e12
+    value = flops / tot / 1e12
+    sample = (f"per step: {REF_ROWS_A} seeded rows of A x a {REF_ROWS_B}-row block of B, full K: "
+              "FP8 and INT8 quantize of those rows, then that block of both GEMMs")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
@@ -175,9 +201,7 @@ def run_reference(args, rank, world):
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
                    "l2": "inputs larger than L2 (no flush)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
-                         "sample": f"{CPU_SAMPLE_ROWS // 3} seeded rows of A per step: FP8 and INT8 "
-                                   "quantize of those rows and all of B, then those rows of both "
-                                   "GEMMs (full N, full K)"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -345,11 +369,11 @@ def run_sq(args, rank, world, local_rank):
     cpu = None
     if not args.no_cpu:
         import numpy as np
-        rows = np.sort(np.random.default_rng(0).choice(M, CPU_SAMPLE_ROWS, replace=False))
-        dt, fl, thr = cpu_oracle_sample(a_np, b_np, sa_np, sb_np, rows)
+        rows = np.sort(np.random.default_rng(0).choice(M, min(CPU_ROWS_A, M), replace=False))
+        dt, fl, thr = cpu_oracle_sample(a_np, b_np, sa_np, sb_np, rows, 0, N)
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": f"{CPU_SAMPLE_ROWS} seeded rows of A: FP8 and INT8 quantize of those "
-                         "rows and all of B, then those rows of both GEMMs (full N, full K)",
+               "sample": f"{len(rows)} seeded rows of A x all of B, full K: FP8 and INT8 quantize "
+                         "of those rows and of B, then those rows of both GEMMs",
                "seconds": dt}
 
     line = {
