@@ -34,7 +34,7 @@
  *       custom::fp8_quantize (bf16 in, fused amax), custom::fp8_gemm
  *       (a @ b * (sa * sb), FP32 accumulation, BF16 out), the fmt map
  *       (0 = E4M3, 1 = E5M2) and the commit notes (last-block amax epilogue,
- *       NT forward, crosswise dX/dW operands).
+ *       NT forward; dX and dW read transposed operands).
  */
 #ifndef SQ_H_
 #define SQ_H_
@@ -100,7 +100,8 @@ sq_status sq_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t
 
 /*
  * Per-tensor FP8 quantization of bf16 with the amax fused in  [P3
- * custom::fp8_quantize; commit notes: last-block epilogue, no extra launch].
+ * custom::fp8_quantize; commit notes: the last block to finish completes the
+ * amax in the same launch].
  *
  *   x8[i] = enc_fmt(fl32(x[i] / *scale))   (RNE, saturating to +-448 / +-57344)
  *   *amax = max_i |x[i]|                  (raw, no floor; 0 for numel == 0)
