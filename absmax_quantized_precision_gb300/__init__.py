@@ -31,7 +31,10 @@ SQ_NT, SQ_NN, SQ_TN = 0, 1, 2
 # every symbol include/sq.h declares
 EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "sq_quantize_fp8",
            "sq_gemm_i8_workspace_bytes", "sq_gemm_i8_rowscaled", "sq_gemm_fp8_scaled",
-           "sq_get_last_device_error")
+           "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc")
+
+# size of the fixed scratch array behind sq_gemm_i8_rowscaled_noalloc
+GEMM_I8_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 _lib = None
 
@@ -69,6 +72,9 @@ def load_library():
     L.sq_gemm_fp8_scaled.restype = i32
     L.sq_get_last_device_error.argtypes = [vp]
     L.sq_get_last_device_error.restype = i32
+    L.sq_gemm_i8_rowscaled_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
+                                               vp, vp, vp]
+    L.sq_gemm_i8_rowscaled_noalloc.restype = i32
     _lib = L
     return L
 
@@ -184,6 +190,40 @@ def sq_gemm_i8_rowscaled(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB:
         _ptr(A3), _ptr(sA), _ptr(B3), _ptr(sB), nb, M, N, K, M * K, N * K, M * N,
         _ptr(C), _ptr(acc_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)), "sq_gemm_i8_rowscaled")
+    return C, acc_out
+
+
+def sq_gemm_i8_rowscaled_noalloc(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor,
+                                 sB: torch.Tensor, C: torch.Tensor = None, acc_out=None,
+                                 want_c: bool = True, stream=None):
+    """sq_gemm_i8_rowscaled without a workspace argument: the library stages the
+    operands in its own fixed 16 MiB device array, so this call allocates
+    nothing (the output tensors are created here only when not passed in).
+    Problems whose staged operands exceed the array raise SQError
+    (SQ_ERR_UNSUPPORTED).  Calls that overlap on the GPU race on the array."""
+    _need_cuda(A, B, sA, sB)
+    batched = A.dim() == 3
+    A3 = A if batched else A.unsqueeze(0)
+    B3 = B if batched else B.unsqueeze(0)
+    nb, M, K = A3.shape
+    N = B3.shape[1]
+    if not (A3.is_contiguous() and B3.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    shape = (nb, M, N) if batched else (M, N)
+    if want_c and C is None:
+        C = torch.empty(shape, dtype=torch.float32, device=A.device)
+    if acc_out is True:
+        acc_out = torch.empty(shape, dtype=torch.int32, device=A.device)
+    elif acc_out is False:
+        acc_out = None
+    st = load_library().sq_gemm_i8_rowscaled_noalloc(
+        _ptr(A3), _ptr(sA), _ptr(B3), _ptr(sB), nb, M, N, K, M * K, N * K, M * N, _ptr(C),
+        _ptr(acc_out), _stream(stream))
+    if st == SQ_ERR_UNSUPPORTED:
+        raise SQError(st, "sq_gemm_i8_rowscaled_noalloc: staged operands "
+                          f"({gemm_i8_workspace_bytes(nb, M, N, K)} bytes) exceed the "
+                          f"{GEMM_I8_NOALLOC_SCRATCH_BYTES}-byte scratch array, or K > 2^17")
+    _check(st, "sq_gemm_i8_rowscaled_noalloc")
     return C, acc_out
 
 

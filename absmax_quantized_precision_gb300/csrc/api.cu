@@ -11,6 +11,12 @@
 // Device error word of this library, one per device.
 static __device__ unsigned g_sq_device_error = 0;
 
+// Staging scratch of sq_gemm_i8_rowscaled_noalloc.  Every device that loads
+// the library holds its own copy until the process exits.  Host code must not
+// hand this name to a kernel: on the host it only stands in for the symbol;
+// the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_sq_noalloc_scratch[SQ_GEMM_I8_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -159,6 +165,54 @@ sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa
                                          static_cast<int>(N), static_cast<int>(K), C_bf16,
                                          ds->err_word, reinterpret_cast<cudaStream_t>(stream),
                                          ds->sms));
+}
+
+namespace {
+
+// Device address of g_sq_noalloc_scratch for the current device, looked up
+// once per device (with that device current) on the first no-alloc call.
+struct NoAllocState {
+    std::once_flag once;
+    void* scratch = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+}  // namespace
+
+sq_status sq_gemm_i8_rowscaled_noalloc(const int8_t* A, const float* sA, const int8_t* B,
+                                       const float* sB, int64_t batch, int64_t M, int64_t N,
+                                       int64_t K, int64_t strideA, int64_t strideB,
+                                       int64_t strideC, float* C, int32_t* acc_out,
+                                       sq_stream stream) {
+    if (batch < 1 || M < 1 || N < 1 || K < 1) return SQ_ERR_INVALID_ARG;
+    if (!A || !B || !sA || !sB || (!C && !acc_out)) return SQ_ERR_INVALID_ARG;
+    if (strideA < M * K || strideB < N * K || strideC < M * N) return SQ_ERR_INVALID_ARG;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (K > (int64_t(1) << 17)) return SQ_ERR_UNSUPPORTED;
+    if (batch > 65535 || M > kMaxDim || N > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    // the staged copies must fit the fixed scratch array (checked before any
+    // product that could overflow: each factor is below 2^31 here)
+    if (static_cast<double>(batch) * (static_cast<double>(M) + static_cast<double>(N)) *
+            static_cast<double>(K) * 2.0 > static_cast<double>(SQ_GEMM_I8_NOALLOC_SCRATCH_BYTES))
+        return SQ_ERR_UNSUPPORTED;
+    const size_t need = sq_gemm_i8_workspace_bytes(batch, M, N, K);
+    if (need > SQ_GEMM_I8_NOALLOC_SCRATCH_BYTES) return SQ_ERR_UNSUPPORTED;
+    if (strideA % 16 != 0 || strideB % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(acc_out))
+        return SQ_ERR_ALIGNMENT;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return SQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SQ_ERR_UNSUPPORTED;
+    NoAllocState& na = g_noalloc[dev];
+    std::call_once(na.once, [&] {
+        na.err = cudaGetSymbolAddress(&na.scratch, g_sq_noalloc_scratch);
+    });
+    if (na.err != cudaSuccess || !na.scratch) return SQ_ERR_CUDA;
+    // the rest is the workspace entry point with the scratch array as workspace
+    return sq_gemm_i8_rowscaled(A, sA, B, sB, batch, M, N, K, strideA, strideB, strideC, C,
+                                acc_out, na.scratch, SQ_GEMM_I8_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 sq_status sq_get_last_device_error(sq_stream stream) {

@@ -169,6 +169,39 @@ sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa
  */
 sq_status sq_get_last_device_error(sq_stream stream);
 
+/*
+ * INT8 GEMM that allocates nothing: the same computation and results as
+ * sq_gemm_i8_rowscaled, but the 16-bit staging copy of A and B lives in a
+ * fixed device array inside libsq instead of a caller-provided workspace.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory on the path where they run this GEMM, for
+ * example code running inside a host framework or engine that owns the
+ * whole device memory pool and hands its plugins only the tensors they
+ * operate on, or callers that hold device pointers but no allocator.
+ *
+ *   Arguments are those of sq_gemm_i8_rowscaled without the workspace.
+ *   Limit: the staged operands, (batch*M*K + batch*N*K) * 2 bytes each padded
+ *   to 256 B (sq_gemm_i8_workspace_bytes), must fit in
+ *   SQ_GEMM_I8_NOALLOC_SCRATCH_BYTES (16 MiB); larger problems return
+ *   SQ_ERR_UNSUPPORTED and enqueue nothing.
+ *   Memory: every GPU that loads libsq holds the 16 MiB array until the
+ *   process exits.  No call makes cudaMalloc, cudaFree or any other
+ *   allocating call.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Sharing: all calls on a device share the one array and it keeps the last
+ *   call's contents (each call overwrites what it reads).  Calls that overlap
+ *   on the GPU (different streams, or different host threads) race on it and
+ *   give wrong results; serialise them on one stream.
+ */
+#define SQ_GEMM_I8_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+sq_status sq_gemm_i8_rowscaled_noalloc(const int8_t* A, const float* sA, const int8_t* B,
+                                       const float* sB, int64_t batch, int64_t M, int64_t N,
+                                       int64_t K, int64_t strideA, int64_t strideB,
+                                       int64_t strideC, float* C, int32_t* acc_out,
+                                       sq_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
