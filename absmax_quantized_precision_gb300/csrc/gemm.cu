@@ -286,11 +286,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
                     const uint32_t tb = tmem_base + lane_off + ab * BN + colgrp * Cfg::EPI_COLS;
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tb + c * 32, r);
-                        tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) sums[c][i] += __float2int_rn(__uint_as_float(r[i]));
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t r[16];
+                            tmem_ld16(tb + c * 32 + h * 16, r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                sums[c][h * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+                        }
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -503,7 +507,7 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
                            const float* sB, int batch, int M, int N, int K, int64_t strideC,
                            float* C, int32_t* acc_out, unsigned* err_word, cudaStream_t st,
                            int sms) {
-    constexpr int BN = 128;
+    constexpr int BN = 256;
     const int bk = kBKBytes / 2;   // 64 fp16 per k-block
     CUtensorMap ta, tb;
     if (!encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A16, K, M, batch,

@@ -4,11 +4,14 @@
 // INT8 (POPCORNBENCH "Kimi-K2.6 l2_p13" trace, reference-model analysis and
 // rounding discussion; per-row / per-head granularity of the scmp_kernels
 // README): s = max(amax_row, 1e-8) / 127, q = clamp(rne(x / s), -127, 127),
-// one IEEE division per element (__fdiv_rn) and round-half-even
-// (__float2int_rn), never a reciprocal multiply or roundf.
+// with the quotient rounded exactly as IEEE float32 division rounds it (via
+// __fdiv_rn, or the FMA-corrected reciprocal product below where that is
+// provably the same float) and round-half-even (__float2int_rn), never a
+// plain reciprocal multiply or roundf.
 //
 // FP8 (AstrAI ops/fp8.py, custom::fp8_quantize and the commit notes): x8 =
-// fp8(x / scale) with round-to-nearest-even and saturation to the largest
+// fp8(x / scale), the quotient rounded as IEEE division rounds it, then
+// round-to-nearest-even and saturation to the largest
 // finite value (cvt.rn.satfinite), amax = max|x| folded in by the last block
 // to finish (threadfence + ticket counter), so no second launch and no
 // per-call memset: the last block also resets the two workspace words.
@@ -49,10 +52,37 @@ struct Elem<uint16_t> {   // bf16 bit patterns; widening is exact
     }
 };
 
-__device__ __forceinline__ int8_t encode_i8(float x, float s) {
-    int n = __float2int_rn(__fdiv_rn(x, s));
+// Correctly rounded quotient x / s from y = RN(1/s), by the FMA correction
+// step of Markstein ("Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990; the division theorem
+// in Muller et al., Handbook of Floating-Point Arithmetic): q = RN(x*y) lies
+// within one ulp of x/s, so r = x - s*q is exact in one FMA, and RN(q + r*y)
+// is RN(x/s) -- provided no intermediate value underflows or overflows.
+// Callers use it only where that holds for every quotient whose value can
+// change the code they produce; elsewhere they divide with __fdiv_rn.
+__device__ __forceinline__ float div_rn_recip(float x, float s, float y) {
+    const float q = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q, s, x);
+    return __fmaf_rn(r, y, q);
+}
+
+// The INT8 quotient only matters where |x/s| >= 1/2; with s in [2^-34, 2^40]
+// (s >= 1e-8/127 > 2^-34 always) those quotients and their residuals stay in
+// the normal range, and |x/s| <= 128 rules out overflow.
+constexpr float kRecipLo = 0x1p-34f;
+constexpr float kRecipHi = 0x1p40f;
+
+__device__ __forceinline__ int8_t clamp_i8(int n) {
     n = n > 127 ? 127 : (n < -127 ? -127 : n);
     return static_cast<int8_t>(n);
+}
+
+__device__ __forceinline__ int8_t encode_i8(float x, float s) {
+    return clamp_i8(__float2int_rn(__fdiv_rn(x, s)));
+}
+
+__device__ __forceinline__ int8_t encode_i8_recip(float x, float s, float y) {
+    return clamp_i8(__float2int_rn(div_rn_recip(x, s, y)));
 }
 
 __device__ __forceinline__ float row_scale(float amax) {
@@ -102,6 +132,8 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
             for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
         }
         const float s = row_scale(m);
+        const bool fast = s <= kRecipHi;   // s >= kRecipLo always
+        const float y = __frcp_rn(s);
         if (live) {
             if (lg == 0) scales[row] = s;
 #pragma unroll
@@ -111,11 +143,12 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
                     uint32_t packed[EPV / 4];
 #pragma unroll
                     for (int w = 0; w < EPV / 4; ++w) {
-                        uint32_t b0 = static_cast<uint8_t>(encode_i8(v[i][4 * w + 0], s));
-                        uint32_t b1 = static_cast<uint8_t>(encode_i8(v[i][4 * w + 1], s));
-                        uint32_t b2 = static_cast<uint8_t>(encode_i8(v[i][4 * w + 2], s));
-                        uint32_t b3 = static_cast<uint8_t>(encode_i8(v[i][4 * w + 3], s));
-                        packed[w] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                        uint32_t b[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            b[e] = static_cast<uint8_t>(fast ? encode_i8_recip(v[i][4 * w + e], s, y)
+                                                             : encode_i8(v[i][4 * w + e], s));
+                        packed[w] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
                     }
                     int8_t* dst = q + row * cols + vi * EPV;
                     if (EPV == 4) {
@@ -213,19 +246,36 @@ __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
 }
 
 // 16 bf16 (two 16-B words) -> 16 FP8 codes (one 16-B word); m = running max|x|.
-template <int FMT>
-__device__ __forceinline__ uint4 fp8_encode16(const uint4& a, const uint4& b, float s, float& m) {
+// x / s for the FP8 path.  With s in [2^-40, 2^40] every quotient that can
+// change an FP8 code (|x/s| in [2^-18, 2^18]: below, the code is +-0; above,
+// it saturates) keeps its residual in the normal range, so div_rn_recip is
+// exact there.  Quotients that overflow keep q (they saturate either way) and
+// the sign is taken from x, as the sign of x/s is for s > 0 (this keeps -0).
+__device__ __forceinline__ float fp8_quotient(float x, float s, float y) {
+    const float q = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q, s, x);
+    float t = (fabsf(q) < 0x1p100f) ? __fmaf_rn(r, y, q) : q;
+    return __int_as_float((__float_as_int(t) & 0x7FFFFFFF) | (__float_as_int(x) & 0x80000000));
+}
+
+template <int FMT, bool FAST>
+__device__ __forceinline__ uint4 fp8_encode16(const uint4& a, const uint4& b, float s, float y,
+                                              float& m) {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        float f0 = __uint_as_float(w[2 * i] << 16);
-        float f1 = __uint_as_float(w[2 * i] & 0xFFFF0000u);
-        float f2 = __uint_as_float(w[2 * i + 1] << 16);
-        float f3 = __uint_as_float(w[2 * i + 1] & 0xFFFF0000u);
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
-        uint32_t lo = fp8x2<FMT>(__fdiv_rn(f0, s), __fdiv_rn(f1, s));
-        uint32_t hi = fp8x2<FMT>(__fdiv_rn(f2, s), __fdiv_rn(f3, s));
+        float f[4];
+        f[0] = __uint_as_float(w[2 * i] << 16);
+        f[1] = __uint_as_float(w[2 * i] & 0xFFFF0000u);
+        f[2] = __uint_as_float(w[2 * i + 1] << 16);
+        f[3] = __uint_as_float(w[2 * i + 1] & 0xFFFF0000u);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) t[e] = FAST ? fp8_quotient(f[e], s, y) : __fdiv_rn(f[e], s);
+        const uint32_t lo = fp8x2<FMT>(t[0], t[1]);
+        const uint32_t hi = fp8x2<FMT>(t[2], t[3]);
         o[i] = lo | (hi << 16);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
@@ -241,6 +291,8 @@ __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restri
     __shared__ float red[8];
     __shared__ int is_last;
     const float s = *scale;
+    const float y = __frcp_rn(s);
+    const bool fast = s >= 0x1p-40f && s <= 0x1p40f;
     float m = 0.0f;
     const int64_t nchunk = n / 32;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -251,8 +303,14 @@ __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restri
         uint4 a1 = ld_stream_v4(src + 8);
         uint4 a2 = ld_stream_v4(src + 16);
         uint4 a3 = ld_stream_v4(src + 24);
-        uint4 o0 = fp8_encode16<FMT>(a0, a1, s, m);
-        uint4 o1 = fp8_encode16<FMT>(a2, a3, s, m);
+        uint4 o0, o1;
+        if (fast) {
+            o0 = fp8_encode16<FMT, true>(a0, a1, s, y, m);
+            o1 = fp8_encode16<FMT, true>(a2, a3, s, y, m);
+        } else {
+            o0 = fp8_encode16<FMT, false>(a0, a1, s, y, m);
+            o1 = fp8_encode16<FMT, false>(a2, a3, s, y, m);
+        }
         st_v4(x8 + c * 32, o0);
         st_v4(x8 + c * 32 + 16, o1);
     }

@@ -140,3 +140,50 @@ def test_fp8_empty_and_zero():
     z = torch.zeros(4096, dtype=torch.bfloat16, device=DEV)
     z8, amax = sq.sq_quantize_fp8(z, one, 0, ws)
     assert amax.item() == 0.0 and int(z8.sum().item()) == 0
+
+
+# ------------------------------------------------------------------ division edge cases
+def test_rowwise_i8_near_ties_at_general_scales():
+    """Elements placed within a few ulps of (n + 1/2) * s for every n, at
+    scales that are not powers of two: the integer code depends on the last
+    bit of the float32 quotient, so the GPU's quotient must equal IEEE
+    division's exactly."""
+    rng = np.random.default_rng(17)
+    rows = []
+    for amax in rng.uniform(0.3, 50.0, size=24).astype(np.float32):
+        s = np.float32(amax) / np.float32(127.0)
+        mids = ((np.arange(-126, 126) + 0.5) * np.float64(s)).astype(np.float32)
+        cand = [mids]
+        up, dn = mids.copy(), mids.copy()
+        for _ in range(3):
+            up = np.nextafter(up, np.float32(np.inf))
+            dn = np.nextafter(dn, np.float32(-np.inf))
+            cand += [up, dn]
+        row = np.concatenate(cand)[:1759]
+        rows.append(np.concatenate([row, np.array([amax], dtype=np.float32)]))
+    x = np.stack(rows).astype(np.float32)
+    assert np.all(np.abs(x).max(axis=1) == np.abs(x[:, -1]))
+    oq, osc = oracle.quantize_rowwise_i8(x)
+    q, s = sq.sq_quantize_rowwise_i8(to_dev(x))
+    assert np.array_equal(s.cpu().numpy(), osc)
+    assert np.array_equal(q.cpu().numpy(), oq)
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -40, 2.0 ** 40, 2.0 ** -41, 2.0 ** 41, 3.3e-7, 7e11],
+                         ids=["lo_edge", "hi_edge", "below", "above", "small", "large"])
+def test_fp8_scales_across_the_division_paths(scale):
+    rng = np.random.default_rng(18)
+    # magnitudes spread so that x/scale sweeps the FP8 range for this scale
+    t = np.exp(rng.uniform(np.log(1e-6), np.log(1e6), 20000)) * rng.choice([-1, 1], 20000)
+    xf = (t * scale).astype(np.float32)
+    x = (xf.view(np.uint32) >> 16).astype(np.uint16)       # truncate to bf16 bits
+    x[:64] = 0x8000                                          # negative zeros
+    x[64:128] = 0x0000
+    ws = sq.new_workspace(DEV)
+    for fmt in (sq.SQ_FMT_E4M3, sq.SQ_FMT_E5M2):
+        ox8, oamax = oracle.quantize_fp8(x, scale, fmt)
+        x8, amax = sq.sq_quantize_fp8(to_dev(x, bf16=True),
+                                      torch.tensor([scale], dtype=torch.float32, device=DEV), fmt, ws)
+        assert np.array_equal(x8.cpu().numpy(), ox8)
+        assert amax.item() == float(oamax)
+        assert np.all(ox8[:64] == 0x80)
