@@ -59,12 +59,19 @@ struct GemmParams {
     unsigned* err_word;
 };
 
-template <int BN, bool I8, bool A_MN, bool B_MN>
+// PAIR = false: one CTA per SM computes 128 x BN tiles (cta_group::1).
+// PAIR = true:  a cluster of two CTAs on the two SMs of a TPC computes
+//               256 x BN tiles with cta_group::2 MMAs issued by the leader
+//               (rank 0): each CTA holds 128 rows of A and BN/2 rows of B, so
+//               each SM reads half of the B tile from its shared memory.
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
 struct GemmCfg {
-    static constexpr int A_BYTES = kBM * kBKBytes;          // 16 KB
-    static constexpr int B_BYTES = BN * kBKBytes;
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;           // B rows this CTA stages
+    static constexpr int A_BYTES = kBM * kBKBytes;              // 16 KB
+    static constexpr int B_BYTES = B_ROWS * kBKBytes;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int STAGES = (STAGE >= 48 * 1024) ? 4 : 6;
+    static constexpr int TILE_M = PAIR ? 2 * kBM : kBM;
     // INT8 keeps its running int32 sums in registers: 8 epilogue warps, each
     // owning 32 rows x EPI_COLS columns of the tile.
     static constexpr int EPI_WARPS = I8 ? 8 : 4;
@@ -79,6 +86,7 @@ struct GemmCfg {
     static constexpr int MN_LBO = kBKBytes * 128;           // 16 KB between 128-B column blocks
     static_assert(2 * STAGES * 8 + 5 * 8 + 8 <= BAR_BYTES, "barrier area");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(!B_MN || B_ROWS % 128 == 0, "MN-major B is staged in 128-column blocks");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& b, int& mb, int& nb) {
@@ -98,11 +106,11 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
 }
 
-template <int BN, bool I8, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+__global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
-    using Cfg = GemmCfg<BN, I8, A_MN, B_MN>;
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -116,6 +124,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;   // 0 = leader of the pair
+    const bool leader = rank == 0;
+    const int cta_unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int num_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -124,7 +136,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], Cfg::EPI_WARPS);
+            mbar_init(&tempty[a], (PAIR ? 2 : 1) * Cfg::EPI_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -135,11 +147,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) {
+        __syncwarp();
+        cluster_sync_all();   // the peer's barriers exist before anyone signals them
+    }
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -153,10 +174,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
             int issued_phase[Cfg::STAGES];
             for (int s = 0; s < Cfg::STAGES; ++s) issued_phase[s] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = cta_unit; t < total && ok; t += num_units) {
                 int b, mb, nb;
                 tile_coords(t, p, b, mb, nb);
-                const int m0 = mb * kBM, n0 = nb * BN;
+                const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
+                const int n0 = nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
                 for (int kb = 0; kb < p.nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err_word)) {
                         ok = false;
@@ -164,21 +186,43 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
                     }
                     uint8_t* sA = smem + stage * Cfg::STAGE;
                     uint8_t* sB = sA + Cfg::A_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE);
-                    if (I8) {
-                        const int kx = kb * (kBKBytes / 2);
-                        tma_load_3d(sA, &tmA, &full[stage], kx, m0, b);
-                        tma_load_3d(sB, &tmB, &full[stage], kx, n0, b);
-                    } else {
-                        const int kx = kb * kBKBytes;
-                        if (A_MN) tma_load_2d(sA, &tmA, &full[stage], m0, kx);
-                        else tma_load_2d(sA, &tmA, &full[stage], kx, m0);
-                        if (B_MN) {
-#pragma unroll
-                            for (int j = 0; j < BN / 128; ++j)
-                                tma_load_2d(sB + j * Cfg::MN_LBO, &tmB, &full[stage], n0 + j * 128, kx);
+                    if (PAIR) {
+                        // both CTAs' bytes complete on the leader's barrier
+                        const uint32_t fb = cluster_addr(&full[stage], 0);
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::STAGE);
+                        if (I8) {
+                            const int kx = kb * (kBKBytes / 2);
+                            tma_load_3d_pair(sA, &tmA, fb, kx, m0, b);
+                            tma_load_3d_pair(sB, &tmB, fb, kx, n0, b);
                         } else {
-                            tma_load_2d(sB, &tmB, &full[stage], kx, n0);
+                            const int kx = kb * kBKBytes;
+                            if (A_MN) tma_load_2d_pair(sA, &tmA, fb, m0, kx);
+                            else tma_load_2d_pair(sA, &tmA, fb, kx, m0);
+                            if (B_MN) {
+#pragma unroll
+                                for (int j = 0; j < Cfg::B_ROWS / 128; ++j)
+                                    tma_load_2d_pair(sB + j * Cfg::MN_LBO, &tmB, fb, n0 + j * 128, kx);
+                            } else {
+                                tma_load_2d_pair(sB, &tmB, fb, kx, n0);
+                            }
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], Cfg::STAGE);
+                        if (I8) {
+                            const int kx = kb * (kBKBytes / 2);
+                            tma_load_3d(sA, &tmA, &full[stage], kx, m0, b);
+                            tma_load_3d(sB, &tmB, &full[stage], kx, n0, b);
+                        } else {
+                            const int kx = kb * kBKBytes;
+                            if (A_MN) tma_load_2d(sA, &tmA, &full[stage], m0, kx);
+                            else tma_load_2d(sA, &tmA, &full[stage], kx, m0);
+                            if (B_MN) {
+#pragma unroll
+                                for (int j = 0; j < Cfg::B_ROWS / 128; ++j)
+                                    tma_load_2d(sB + j * Cfg::MN_LBO, &tmB, &full[stage], n0 + j * 128, kx);
+                            } else {
+                                tma_load_2d(sB, &tmB, &full[stage], kx, n0);
+                            }
                         }
                     }
                     issued_phase[stage] = static_cast<int>(phase);
@@ -188,20 +232,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
                     }
                 }
             }
-            if (!ok) {
-                // let every copy this thread started land before the CTA exits
+            if (!ok && leader) {
+                // let every copy signalled on this CTA's barriers land before it exits
                 for (int s = 0; s < Cfg::STAGES; ++s)
                     if (issued_phase[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(issued_phase[s]));
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (elect_one_sync()) {
+        // ------------------------------------------------------------ MMA issuer (leader)
+        if (leader && elect_one_sync()) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            bool issued = false;
+            for (int t = cta_unit; t < total && ok; t += num_units) {
                 for (int ch = 0; ch < p.nchunks && ok; ++ch) {
                     const uint32_t ab = it & 1u;
                     const uint32_t aph = (it >> 1) & 1u;
@@ -230,23 +275,32 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
                                 B_MN ? sdesc_sw128(b_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
                                      : sdesc_sw128(b_addr + kk * Cfg::KSTEP_K, 16, 1024);
                             const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-                            if (I8) mma_f16(d_tmem, ad, bd, p.idesc, acc);
-                            else mma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
+                            if (PAIR) {
+                                if (I8) mma_pair_f16(d_tmem, ad, bd, p.idesc, acc);
+                                else mma_pair_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
+                            } else {
+                                if (I8) mma_f16(d_tmem, ad, bd, p.idesc, acc);
+                                else mma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
+                            }
                         }
-                        mma_commit(&empty[stage]);
+                        issued = true;
+                        if (PAIR) mma_commit_pair(&empty[stage], 3);   // frees the stage in both CTAs
+                        else mma_commit(&empty[stage]);
                         if (++stage == Cfg::STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    mma_commit(&tfull[ab]);
+                    if (PAIR) mma_commit_pair(&tfull[ab], 3);          // both epilogues may read
+                    else mma_commit(&tfull[ab]);
                     ++it;
                 }
             }
-            if (!ok) {
+            if (!ok && issued) {
                 // make every MMA already issued finish before TMEM is released
-                mma_commit(drain);
+                if (PAIR) mma_commit_pair(drain, 1);
+                else mma_commit(drain);
                 mbar_wait_drain(drain, 0);
             }
         }
@@ -256,6 +310,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
         const int colgrp = ew >> 2;            // INT8: which EPI_COLS-wide column group
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        // where this warp reports that it has read an accumulator: the leader's barrier
+        const uint32_t tempty_leader[2] = {PAIR ? cluster_addr(&tempty[0], 0) : 0u,
+                                           PAIR ? cluster_addr(&tempty[1], 0) : 0u};
         float fsa = 0.0f, fsb = 0.0f;
         if (!I8) {
             fsa = *p.sa;
@@ -263,10 +320,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
         }
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        auto release = [&](uint32_t ab) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR && !leader) mbar_arrive_cluster(tempty_leader[ab]);
+                else mbar_arrive(&tempty[ab]);
+            }
+        };
+        for (int t = cta_unit; t < total && ok; t += num_units) {
             int b, mb, nb;
             tile_coords(t, p, b, mb, nb);
-            const int m0 = mb * kBM, n0 = nb * BN;
+            const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
+            const int n0 = nb * BN;
             const int row = m0 + quarter * 32 + lane;
             if (I8) {
                 constexpr int NC = Cfg::EPI_COLS / 32;
@@ -296,9 +362,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
                                 sums[c][h * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
                         }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[ab]);
+                    release(ab);
                     ++it;
                 }
                 if (!ok) break;
@@ -383,9 +447,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
                         }
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[ab]);
+                release(ab);
                 ++it;
             }
         }
@@ -393,10 +455,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN>::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR) {
+        __syncwarp();
+        cluster_sync_all();   // the leader's MMAs into the peer's TMEM are done
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if (PAIR) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
@@ -449,88 +516,153 @@ static bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool I8, bool A_MN, bool B_MN>
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
 static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                             cudaStream_t st, int sms) {
-    using Cfg = GemmCfg<BN, I8, A_MN, B_MN>;
-    auto kern = gemm_tc_kernel<BN, I8, A_MN, B_MN>;
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
+    auto kern = gemm_tc_kernel<BN, I8, A_MN, B_MN, PAIR>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
+    static int max_units = 0;   // CTAs (or CTA pairs) that fit the GPU at once
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        if (attr_err != cudaSuccess) return;
+        if (PAIR) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+            cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+            cfg.dynamicSmemBytes = Cfg::SMEM;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            attr_err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            max_units = n;
+        } else {
+            max_units = sms;
+        }
+        if (attr_err == cudaSuccess && max_units < 1) attr_err = cudaErrorInvalidConfiguration;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int total = p.mt * p.nt * p.batch;
-    const int grid = total < sms ? total : sms;
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(ta, tb, p);
-    return cudaGetLastError();
+    const int units = total < max_units ? total : max_units;
+    if (!PAIR) {
+        kern<<<units, Cfg::THREADS, Cfg::SMEM, st>>>(ta, tb, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * units, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+}
+
+// Tile shape: 256 x 256 on CTA pairs when there are enough such tiles to give
+// every pair of SMs work, else 128 x 256 or 128 x 128 on single CTAs.
+enum class Shape { Pair256, Single256, Single128 };
+
+static Shape pick_shape(int64_t M, int64_t N, int64_t batch, int sms) {
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256) * batch;
+    const int64_t wide_tiles = ((M + 127) / 128) * ((N + 255) / 256) * batch;
+    if (pair_tiles >= sms / 2) return Shape::Pair256;
+    if (wide_tiles >= sms) return Shape::Single256;
+    return Shape::Single128;
+}
+
+template <bool A_MN, bool B_MN, int BN, bool PAIR>
+static cudaError_t gemm_fp8_shape(const uint8_t* A, const uint8_t* B, int M, int N, int K,
+                                  GemmParams p, int fmt, cudaStream_t st, int sms) {
+    using Cfg = GemmCfg<BN, false, A_MN, B_MN, PAIR>;
+    CUtensorMap ta, tb;
+    bool ok;
+    if (A_MN) ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, M, 128, kBKBytes);
+    else ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, kBKBytes, kBM);
+    if (!ok) return cudaErrorInvalidValue;
+    if (B_MN) ok = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, N, K, N, 128, kBKBytes);
+    else ok = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, kBKBytes, Cfg::B_ROWS);
+    if (!ok) return cudaErrorInvalidValue;
+    p.mt = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
+    p.nt = (N + BN - 1) / BN;
+    p.idesc = idesc_make(static_cast<uint32_t>(fmt), static_cast<uint32_t>(fmt), A_MN, B_MN,
+                         Cfg::TILE_M, BN);
+    return run_gemm<BN, false, A_MN, B_MN, PAIR>(ta, tb, p, st, sms);
+}
+
+template <bool A_MN, bool B_MN>
+static cudaError_t gemm_fp8_layout(const uint8_t* A, const uint8_t* B, int M, int N, int K,
+                                   const GemmParams& p, int fmt, cudaStream_t st, int sms) {
+    switch (pick_shape(M, N, 1, sms)) {
+        case Shape::Pair256: return gemm_fp8_shape<A_MN, B_MN, 256, true>(A, B, M, N, K, p, fmt, st, sms);
+        case Shape::Single256: return gemm_fp8_shape<A_MN, B_MN, 256, false>(A, B, M, N, K, p, fmt, st, sms);
+        default: return gemm_fp8_shape<A_MN, B_MN, 128, false>(A, B, M, N, K, p, fmt, st, sms);
+    }
 }
 
 cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                             int fmt, int layout, int M, int N, int K, uint16_t* C,
                             unsigned* err_word, cudaStream_t st, int sms) {
-    // 256-wide tiles when there are enough of them to fill the GPU
-    const int mt = (M + kBM - 1) / kBM;
-    const int BN = (static_cast<int64_t>(mt) * ((N + 255) / 256) >= sms) ? 256 : 128;
-    const bool a_mn = layout == 2;          // TN: A stored [K, M]
-    const bool b_mn = layout != 0;          // NN, TN: B stored [K, N]
-    CUtensorMap ta, tb;
-    bool ok;
-    if (a_mn) ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, M, 128, kBKBytes);
-    else ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, kBKBytes, kBM);
-    if (!ok) return cudaErrorInvalidValue;
-    if (b_mn) ok = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, N, K, N, 128, kBKBytes);
-    else ok = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, kBKBytes, BN);
-    if (!ok) return cudaErrorInvalidValue;
-
     GemmParams p{};
     p.M = M; p.N = N; p.K = K; p.batch = 1;
-    p.mt = mt; p.nt = (N + BN - 1) / BN;
     p.nkb = (K + kBKBytes - 1) / kBKBytes;
     p.kb_per_chunk = p.nkb;
     p.nchunks = 1;
     p.sa = sa; p.sb = sb; p.C = C; p.acc_out = nullptr; p.strideC = 0;
-    p.idesc = idesc_make(static_cast<uint32_t>(fmt), static_cast<uint32_t>(fmt), a_mn, b_mn, kBM, BN);
     p.vec_store = (N % 8 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
     p.err_word = err_word;
-    if (BN == 256) {
-        if (layout == 0) return run_gemm<256, false, false, false>(ta, tb, p, st, sms);
-        if (layout == 1) return run_gemm<256, false, false, true>(ta, tb, p, st, sms);
-        return run_gemm<256, false, true, true>(ta, tb, p, st, sms);
-    }
-    if (layout == 0) return run_gemm<128, false, false, false>(ta, tb, p, st, sms);
-    if (layout == 1) return run_gemm<128, false, false, true>(ta, tb, p, st, sms);
-    return run_gemm<128, false, true, true>(ta, tb, p, st, sms);
+    if (layout == 0) return gemm_fp8_layout<false, false>(A, B, M, N, K, p, fmt, st, sms);
+    if (layout == 1) return gemm_fp8_layout<false, true>(A, B, M, N, K, p, fmt, st, sms);
+    return gemm_fp8_layout<true, true>(A, B, M, N, K, p, fmt, st, sms);
 }
 
-cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
-                           const float* sB, int batch, int M, int N, int K, int64_t strideC,
-                           float* C, int32_t* acc_out, unsigned* err_word, cudaStream_t st,
-                           int sms) {
-    constexpr int BN = 256;
+template <int BN, bool PAIR>
+static cudaError_t gemm_i8_shape(const uint16_t* A16, const uint16_t* B16, int batch, int M, int N,
+                                 int K, GemmParams p, cudaStream_t st, int sms) {
+    using Cfg = GemmCfg<BN, true, false, false, PAIR>;
     const int bk = kBKBytes / 2;   // 64 fp16 per k-block
     CUtensorMap ta, tb;
     if (!encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A16, K, M, batch,
                    static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(M) * K * 2, bk, kBM))
         return cudaErrorInvalidValue;
     if (!encode_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B16, K, N, batch,
-                   static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2, bk, BN))
+                   static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2, bk, Cfg::B_ROWS))
         return cudaErrorInvalidValue;
+    p.mt = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
+    p.nt = (N + BN - 1) / BN;
+    p.idesc = idesc_make(0, 0, false, false, Cfg::TILE_M, BN);   // F16 x F16 -> F32
+    return run_gemm<BN, true, false, false, PAIR>(ta, tb, p, st, sms);
+}
+
+cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
+                           const float* sB, int batch, int M, int N, int K, int64_t strideC,
+                           float* C, int32_t* acc_out, unsigned* err_word, cudaStream_t st,
+                           int sms) {
+    const int bk = kBKBytes / 2;
     GemmParams p{};
     p.M = M; p.N = N; p.K = K; p.batch = batch;
-    p.mt = (M + kBM - 1) / kBM;
-    p.nt = (N + BN - 1) / BN;
     p.nkb = (K + bk - 1) / bk;
     p.kb_per_chunk = kI8ChunkK / bk;
     p.nchunks = (p.nkb + p.kb_per_chunk - 1) / p.kb_per_chunk;
     p.sa = sA; p.sb = sB; p.C = C; p.acc_out = acc_out; p.strideC = strideC;
-    p.idesc = idesc_make(0, 0, false, false, kBM, BN);   // F16 x F16 -> F32
     p.vec_store = (N % 4 == 0) && (strideC % 4 == 0) &&
                   (reinterpret_cast<uintptr_t>(C) % 16 == 0) &&
                   (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0) &&
                   (reinterpret_cast<uintptr_t>(sB) % 16 == 0);
     p.err_word = err_word;
-    return run_gemm<BN, true, false, false>(ta, tb, p, st, sms);
+    if (pick_shape(M, N, batch, sms) == Shape::Pair256)
+        return gemm_i8_shape<256, true>(A16, B16, batch, M, N, K, p, st, sms);
+    return gemm_i8_shape<256, false>(A16, B16, batch, M, N, K, p, st, sms);
 }
 
 // ---------------------------------------------------------------- staging

@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--size", type=int, nargs=3, metavar=("M", "N", "K"),
                     help="override the workload sizes (small cases for profiler captures)")
+    ap.add_argument("--config", default="large",
+                    choices=["large", "int8_per_row", "int8_per_head", "fp8_fwd", "fp8_bwd", "all"],
+                    help="the pages' other workloads are measured with their own JSON line")
     args = ap.parse_args()
     if args.size:
         global M, N, K, FLOPS_PER_STEP, WORKLOAD
@@ -395,11 +398,182 @@ def run_sq(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- the other workloads
+SMALL_CONFIGS = ["int8_per_row", "int8_per_head", "fp8_fwd", "fp8_bwd"]
+
+
+def run_small_config(name, args):
+    """One JSON line for one of the pages' smaller workloads: L2 flushed
+    (256 MiB write) before every timed iteration, per-kernel CUDA events, and
+    the oracle run on the whole workload on the host for comparison."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import absmax_quantized_precision_gb300 as sq
+    import oracle
+    import synth
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def bf16_dev(u16):
+        return torch.from_numpy(u16.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def prev_scale(seed, shape, std, fmax=448.0):
+        p = synth.bf16_bits_to_f32(synth.normal(seed, shape, std=std, dtype=synth.BF16))
+        return np.float32(np.abs(p).max()) / np.float32(fmax)
+
+    ops = []          # (label, kind, bytes_or_flops, fn)
+    gemm_flops = 0.0
+    cpu = None
+    if name in ("int8_per_row", "int8_per_head"):
+        if name == "int8_per_row":
+            a = synth.normal(11, (128, 1024))
+            b = synth.normal(12, (512, 1024))
+            desc = "INT8 per-row: A f32 128x1024, B f32 512x1024 ~N(0,1); C = A B^T, fp32 out"
+        else:
+            a = synth.normal(21, (16, 196, 64))
+            b = synth.normal(22, (16, 196, 64))
+            desc = "INT8 per-head: Q, K f32 (16,196,64) ~N(0,1); C[h] = Q[h] K[h]^T, fp32 out"
+        A, B = torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)
+        qa = torch.empty(A.shape, dtype=torch.int8, device=dev)
+        qb = torch.empty(B.shape, dtype=torch.int8, device=dev)
+        sa = torch.empty(A.shape[:-1], device=dev)
+        sb = torch.empty(B.shape[:-1], device=dev)
+        nb = A.shape[0] if A.dim() == 3 else 1
+        Mi, Kk = A.shape[-2], A.shape[-1]
+        Ni = B.shape[-2]
+        ws = torch.empty(sq.gemm_i8_workspace_bytes(nb, Mi, Ni, Kk), dtype=torch.uint8, device=dev)
+        C = torch.empty((nb, Mi, Ni) if nb > 1 else (Mi, Ni), device=dev)
+        gemm_flops = 2.0 * nb * Mi * Ni * Kk
+        ops = [("quant_i8_A", "bytes", A.numel() * 5 + sa.numel() * 4,
+                lambda: sq.sq_quantize_rowwise_i8(A, q=qa, scales=sa)),
+               ("quant_i8_B", "bytes", B.numel() * 5 + sb.numel() * 4,
+                lambda: sq.sq_quantize_rowwise_i8(B, q=qb, scales=sb)),
+               ("gemm_i8", "flops", gemm_flops,
+                lambda: sq.sq_gemm_i8_rowscaled(qa, sa.reshape(-1), qb, sb.reshape(-1), ws, C=C))]
+        t0 = time.perf_counter()
+        oqa, osa = oracle.quantize_rowwise_i8(a)
+        oqb, osb = oracle.quantize_rowwise_i8(b)
+        oracle.gemm_i8(oqa, oqb, osa, osb)
+        cpu = time.perf_counter() - t0
+    else:
+        fmt = sq.SQ_FMT_E4M3
+        wsq = sq.new_workspace(dev)
+        if name == "fp8_fwd":
+            x = synth.normal(31, (2048, 1024), std=1.0, dtype=synth.BF16)
+            w = synth.normal(32, (1024, 1024), std=0.02, dtype=synth.BF16)
+            sx, sw = prev_scale(33, x.shape, 1.0), prev_scale(34, w.shape, 0.02)
+            X, W = bf16_dev(x), bf16_dev(w)
+            tsx, tsw = torch.tensor([sx], device=dev), torch.tensor([sw], device=dev)
+            x8 = torch.empty(X.shape, dtype=torch.uint8, device=dev)
+            w8 = torch.empty(W.shape, dtype=torch.uint8, device=dev)
+            ax, aw = torch.empty(1, device=dev), torch.empty(1, device=dev)
+            Y = torch.empty((2048, 1024), dtype=torch.bfloat16, device=dev)
+            gemm_flops = 2.0 * 2048 * 1024 * 1024
+            desc = ("FP8 E4M3 linear forward: X bf16 2048x1024 ~N(0,1), W bf16 1024x1024 "
+                    "~N(0,0.02), delayed scales; Y = X W^T (NT), bf16 out")
+            ops = [("quant_fp8_X", "bytes", X.numel() * 3,
+                    lambda: sq.sq_quantize_fp8(X, tsx, fmt, wsq, x8=x8, amax=ax)),
+                   ("quant_fp8_W", "bytes", W.numel() * 3,
+                    lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=aw)),
+                   ("gemm_fp8_nt", "flops", gemm_flops,
+                    lambda: sq.sq_gemm_fp8_scaled(x8, w8, tsx, tsw, fmt, sq.SQ_NT, C=Y))]
+            t0 = time.perf_counter()
+            ox8, _ = oracle.quantize_fp8(x, sx, 0)
+            ow8, _ = oracle.quantize_fp8(w, sw, 0)
+            oracle.gemm_fp8(ox8, ow8, 0, oracle.NT, sx, sw)
+            cpu = time.perf_counter() - t0
+        else:
+            T, H, D = 2048, 4096, 1024
+            g = synth.normal(41, (T, H), std=1e-3, dtype=synth.BF16)
+            w = synth.normal(42, (H, D), std=0.02, dtype=synth.BF16)
+            x = synth.normal(43, (T, D), std=1.0, dtype=synth.BF16)
+            sg, sw, sx = prev_scale(44, g.shape, 1e-3), prev_scale(45, w.shape, 0.02), \
+                prev_scale(46, x.shape, 1.0)
+            G, W, X = bf16_dev(g), bf16_dev(w), bf16_dev(x)
+            tsg, tsw, tsx = (torch.tensor([v], device=dev) for v in (sg, sw, sx))
+            g8 = torch.empty(G.shape, dtype=torch.uint8, device=dev)
+            w8 = torch.empty(W.shape, dtype=torch.uint8, device=dev)
+            x8 = torch.empty(X.shape, dtype=torch.uint8, device=dev)
+            am = [torch.empty(1, device=dev) for _ in range(3)]
+            dX = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+            dW = torch.empty((H, D), dtype=torch.bfloat16, device=dev)
+            gemm_flops = 2 * (2.0 * T * H * D)
+            desc = ("FP8 E4M3 MLP backward (dim 1024, hidden 4096, 2048 tokens): G bf16 2048x4096 "
+                    "~N(0,1e-3), W bf16 4096x1024 ~N(0,0.02), X bf16 2048x1024 ~N(0,1); "
+                    "dX = G W (NN), dW = G^T X (TN), bf16 out")
+            ops = [("quant_fp8_G", "bytes", G.numel() * 3,
+                    lambda: sq.sq_quantize_fp8(G, tsg, fmt, wsq, x8=g8, amax=am[0])),
+                   ("quant_fp8_W", "bytes", W.numel() * 3,
+                    lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=am[1])),
+                   ("quant_fp8_X", "bytes", X.numel() * 3,
+                    lambda: sq.sq_quantize_fp8(X, tsx, fmt, wsq, x8=x8, amax=am[2])),
+                   ("gemm_fp8_dX_nn", "flops", 2.0 * T * H * D,
+                    lambda: sq.sq_gemm_fp8_scaled(g8, w8, tsg, tsw, fmt, sq.SQ_NN, C=dX)),
+                   ("gemm_fp8_dW_tn", "flops", 2.0 * T * H * D,
+                    lambda: sq.sq_gemm_fp8_scaled(g8, x8, tsg, tsx, fmt, sq.SQ_TN, C=dW))]
+            t0 = time.perf_counter()
+            og8, _ = oracle.quantize_fp8(g, sg, 0)
+            ow8, _ = oracle.quantize_fp8(w, sw, 0)
+            ox8, _ = oracle.quantize_fp8(x, sx, 0)
+            oracle.gemm_fp8(og8, ow8, 0, oracle.NN, sg, sw, want_bf16=False)
+            oracle.gemm_fp8(og8, ox8, 0, oracle.TN, sg, sx, want_bf16=False)
+            cpu = time.perf_counter() - t0
+
+    iters = max(args.steps if args.steps != 300 else 50, 1)
+    for _ in range(max(args.warmup, 3)):
+        for _, _, _, fn in ops:
+            fn()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(iters)]
+    with Clocks(0) as clk:
+        for it in range(iters):
+            flush.fill_(it & 0xFF)           # evict the inputs from L2 before each pass
+            evs[it][0].record(stream)
+            for i, (_, _, _, fn) in enumerate(ops):
+                fn()
+                evs[it][i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    if sq.sq_get_last_device_error() != sq.SQ_OK:
+        raise RuntimeError("device error")
+    step_ms = statistics.median(evs[i][0].elapsed_time(evs[i][-1]) for i in range(iters))
+    pk = peaks()
+    kernels = {}
+    for j, (label, kind, amount, _) in enumerate(ops):
+        ms = statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(iters))
+        d = {"us": 1e3 * ms}
+        if kind == "bytes":
+            d["GB/s"] = amount / (ms * 1e-3) / 1e9
+            d["frac_hbm"] = d["GB/s"] / pk["hbm_gbs"]
+        else:
+            tf = amount / (ms * 1e-3) / 1e12
+            d["TFLOP/s"] = tf
+            d["frac_peak"] = tf / ((2.0 if "fp8" in label else 1.0) * pk["bf16_sustained"])
+        kernels[label] = d
+    line = {"metric": METRIC, "config": {"workload": name, "desc": desc,
+                                         "l2": "flushed before every pass"},
+            "value": gemm_flops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
+            "us_per_step": 1e3 * step_ms, "iters": iters, "kernels": kernels,
+            "clocks": clk.summary(),
+            "cpu_oracle": {"seconds": cpu, "cores": oracle.num_threads(),
+                           "sample": "the whole workload"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.config != "large" and args.impl == "sq":
+        for name in (SMALL_CONFIGS if args.config == "all" else [args.config]):
+            run_small_config(name, args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -214,3 +214,50 @@ def test_fp8_backward_dx_nn_and_dw_tn():
     assert dW.shape == (H, D)
     rows = np.sort(np.random.default_rng(3).choice(H, 128, replace=False))
     check_fp8(dW, g8, x8, fmt, sq.SQ_TN, T, sg, sx, rows=rows)
+
+
+# ------------------------------------------------------------------ CTA-pair shapes
+# Problems with at least one 256x256 tile per pair of SMs run on the 2-SM
+# (cta_group::2) kernel; these sizes select it and keep ragged tails in M and N.
+PAIR_FP8 = [
+    ("pair NT 2200x2208x320", 2200, 2208, 320, sq.SQ_NT),
+    ("pair NN 2200x2208x384", 2200, 2208, 384, sq.SQ_NN),
+    ("pair TN 2208x2208x256", 2208, 2208, 256, sq.SQ_TN),
+]
+
+
+@pytest.mark.parametrize("name,M,N,K,layout", PAIR_FP8, ids=[c[0] for c in PAIR_FP8])
+def test_fp8_gemm_cta_pair(name, M, N, K, layout):
+    a8, b8, sa, sb = fp8_inputs(name, M, N, K, sq.SQ_FMT_E4M3)
+    A = a8 if layout != sq.SQ_TN else np.ascontiguousarray(a8.T)
+    B = b8 if layout == sq.SQ_NT else np.ascontiguousarray(b8.T)
+    C, cbuf, n = guarded((M, N), torch.bfloat16, 5.0)
+    sq.sq_gemm_fp8_scaled(to_dev(A), to_dev(B), torch.tensor([sa], device=DEV),
+                          torch.tensor([sb], device=DEV), sq.SQ_FMT_E4M3, layout, C=C)
+    rows = np.sort(np.concatenate([np.arange(0, 8), np.arange(M - 8, M),
+                                   np.random.default_rng(4).choice(M, 240, replace=False)]))
+    rows = np.unique(rows)
+    check_fp8(C, A, B, sq.SQ_FMT_E4M3, layout, K, sa, sb, rows=rows)
+    assert guard_intact(cbuf, n, 5.0)
+
+
+def test_i8_gemm_cta_pair_ragged():
+    s = seed_of("pair i8")
+    a, b = synth.normal(s, (2200, 1040)), synth.normal(s + 1, (2300, 1040))
+    qa, sa = oracle.quantize_rowwise_i8(a)
+    qb, sb = oracle.quantize_rowwise_i8(b)
+    rows = np.unique(np.concatenate([np.arange(0, 4), np.arange(2196, 2200),
+                                     np.random.default_rng(5).choice(2200, 120, replace=False)]))
+    oacc, oC = oracle.gemm_i8(qa, qb, sa, sb, rows=rows)
+    C, acc = run_i8(qa, sa, qb, sb)
+    assert np.array_equal(acc[rows], oacc) and np.array_equal(C[rows], oC)
+
+
+def test_i8_gemm_cta_pair_batched_heads():
+    q = synth.normal(61, (24, 500, 64))
+    k = synth.normal(62, (24, 520, 64))
+    qq, sq_ = oracle.quantize_rowwise_i8(q)
+    qk, sk = oracle.quantize_rowwise_i8(k)
+    oacc, oC = oracle.gemm_i8(qq, qk, sq_, sk)
+    C, acc = run_i8(qq, sq_, qk, sk)
+    assert np.array_equal(acc, oacc) and np.array_equal(C, oC)
