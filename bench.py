@@ -59,6 +59,36 @@ def parse():
     return args
 
 
+# DRAM traffic per call (ncu dram__bytes_read.sum + dram__bytes_write.sum,
+# summed over the kernels of the call, full-size workload, 1-pass capture),
+# valid only for the kernel sources it was taken from: when the sha256 of
+# those sources no longer matches, the bench reports traffic as null.
+PROFILED_TRAFFIC = {
+    # profiles/traffic_large_step.md
+    "gemm_fp8_nt": {"bytes": 720160512, "sources_sha256": "1ad5ba9b2098993e888b520d3f6efbc864bea21a336be088f06bbcf0742b1dba"},
+    "gemm_i8": {"bytes": 3498969600, "sources_sha256": "1ad5ba9b2098993e888b520d3f6efbc864bea21a336be088f06bbcf0742b1dba"},
+}
+TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
+                   "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
+                   "absmax_quantized_precision_gb300/csrc/quantize.cu"]
+
+
+def sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel):
+    rec = PROFILED_TRAFFIC.get(kernel)
+    if not rec or rec.get("sources_sha256") != sources_sha256():
+        return None
+    return rec["bytes"]
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -363,11 +393,14 @@ def run_sq(args, rank, world, local_rank):
     dom_peak = fp8_peak if dom == "gemm_fp8_nt" else bf16_peak
     achieved = kernels[dom]["TFLOP/s"]
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": dom_peak,
-                "unit": "TFLOP/s", "frac": achieved / dom_peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / dom_peak,
+                "traffic": profiled_traffic(dom),
                 "peak_src": f"{pk['src']} bf16 sustained"
                             + (" x2 (nominal fp8:bf16)" if dom == "gemm_fp8_nt" else
                                " (INT8 runs on the f16 tensor path)"),
-                "algorithmic": "2*M*N*K flops per launch"}
+                "algorithmic": "2*M*N*K flops per call",
+                "timed": ("one sq_gemm_i8_rowscaled call: fp16 staging of A and B (2 launches) "
+                          "plus the GEMM" if dom == "gemm_i8" else "one sq_gemm_fp8_scaled launch")}
 
     cpu = None
     if not args.no_cpu:
@@ -542,6 +575,24 @@ def run_small_config(name, args):
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error")
     step_ms = statistics.median(evs[i][0].elapsed_time(evs[i][-1]) for i in range(iters))
+    # The same step captured once as a CUDA graph and replayed: launches go
+    # back to back, so this is device time without host submission gaps.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _, _, _, fn in ops:
+            fn()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
+    for it in range(iters):
+        flush.fill_(it & 0xFF)
+        gev[it][0].record(stream)
+        graph.replay()
+        gev[it][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if sq.sq_get_last_device_error() != sq.SQ_OK:
+        raise RuntimeError("device error in graph replay")
+    graph_ms = statistics.median(gev[i][0].elapsed_time(gev[i][1]) for i in range(iters))
     pk = peaks()
     kernels = {}
     for j, (label, kind, amount, _) in enumerate(ops):
@@ -557,8 +608,12 @@ def run_small_config(name, args):
         kernels[label] = d
     line = {"metric": METRIC, "config": {"workload": name, "desc": desc,
                                          "l2": "flushed before every pass"},
-            "value": gemm_flops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
-            "us_per_step": 1e3 * step_ms, "iters": iters, "kernels": kernels,
+            "value": gemm_flops / (graph_ms * 1e-3) / 1e12, "unit": UNIT,
+            "us_per_step_graph": 1e3 * graph_ms,
+            "us_per_step_eager": 1e3 * step_ms,
+            "value_eager": gemm_flops / (step_ms * 1e-3) / 1e12,
+            "launches_per_step": sum(3 if lbl == "gemm_i8" else 1 for lbl, _, _, _ in ops),
+            "iters": iters, "kernels_eager": kernels,
             "clocks": clk.summary(),
             "cpu_oracle": {"seconds": cpu, "cores": oracle.num_threads(),
                            "sample": "the whole workload"}}
