@@ -31,7 +31,9 @@ SQ_NT, SQ_NN, SQ_TN = 0, 1, 2
 # every symbol include/sq.h declares
 EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "sq_quantize_fp8",
            "sq_gemm_i8_workspace_bytes", "sq_gemm_i8_rowscaled", "sq_gemm_fp8_scaled",
-           "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc")
+           "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc", "sq_quantize_fp8_ring",
+           "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
+           "sq_quantize_grouped_i8", "sq_gemm_i8_grouped")
 
 # size of the fixed scratch array behind sq_gemm_i8_rowscaled_noalloc
 GEMM_I8_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -75,6 +77,17 @@ def load_library():
     L.sq_gemm_i8_rowscaled_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
                                                vp, vp, vp]
     L.sq_gemm_i8_rowscaled_noalloc.restype = i32
+    L.sq_quantize_fp8_ring.argtypes = [vp, i64, i32, vp, vp, vp, i64, i64, i32, vp, vp]
+    L.sq_quantize_fp8_ring.restype = i32
+    L.sq_gemm_fp8_scaled_e4m3.argtypes = [vp, vp, vp, vp, i32, i32, i64, i64, i64, vp, vp, vp]
+    L.sq_gemm_fp8_scaled_e4m3.restype = i32
+    L.sq_quantize_grouped_i8_workspace_bytes.argtypes = [i64, i64]
+    L.sq_quantize_grouped_i8_workspace_bytes.restype = sz
+    L.sq_quantize_grouped_i8.argtypes = [vp, i32, i64, i64, i64, i64, vp, vp, vp, sz, vp]
+    L.sq_quantize_grouped_i8.restype = i32
+    L.sq_gemm_i8_grouped.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
+                                     vp, vp, vp, sz, vp]
+    L.sq_gemm_i8_grouped.restype = i32
     _lib = L
     return L
 
@@ -164,6 +177,89 @@ def sq_quantize_fp8(x: torch.Tensor, scale: torch.Tensor, fmt: int, workspace: t
     return x8, amax
 
 
+def new_ring(hist_len: int, scale: float, device=None) -> torch.Tensor:
+    """A delayed-scaling ring float32[hist_len + 2] = [hist | scale | counter]
+    with an empty history, the given step, and a zero counter."""
+    r = torch.zeros(hist_len + 2, dtype=torch.float32, device=device or "cuda")
+    r[hist_len] = scale
+    return r
+
+
+def sq_quantize_fp8_ring(x: torch.Tensor, fmt: int, ring: torch.Tensor, idx: int, margin: int,
+                         workspace: torch.Tensor, x8: torch.Tensor = None,
+                         amax: torch.Tensor = None, stream=None):
+    """Per-tensor FP8 of bf16 x with the step ring[H]; records the amax in
+    ring[idx] and publishes the next step in ring[H] on the device."""
+    _need_cuda(x, ring, workspace)
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise TypeError("x must be a contiguous bfloat16 tensor")
+    if ring.dtype != torch.float32 or not ring.is_contiguous() or ring.numel() < 3:
+        raise TypeError("ring must be a contiguous float32 tensor of hist_len + 2 entries")
+    if x8 is None:
+        x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(load_library().sq_quantize_fp8_ring(_ptr(x), x.numel(), int(fmt), _ptr(x8), _ptr(amax),
+                                               _ptr(ring), ring.numel() - 2, int(idx), int(margin),
+                                               _ptr(workspace), _stream(stream)),
+           "sq_quantize_fp8_ring")
+    return x8, amax
+
+
+def sq_quantize_grouped_i8(x: torch.Tensor, group_rows: int, q: torch.Tensor = None,
+                           scales: torch.Tensor = None, workspace: torch.Tensor = None,
+                           stream=None):
+    """Row-group INT8 of a 2-D float32/bfloat16 x: groups of group_rows rows
+    share a scale (group_rows >= rows: per tensor).  Returns (q, scales)."""
+    _need_cuda(x)
+    dt = {torch.float32: SQ_F32, torch.bfloat16: SQ_BF16}.get(x.dtype)
+    if dt is None or x.dim() != 2 or (x.numel() and x.stride(1) != 1):
+        raise TypeError("x must be 2-D float32 or bfloat16 with contiguous rows")
+    rows, cols = x.shape
+    g = max(1, min(int(group_rows), rows)) if rows else 1
+    ng = (rows + g - 1) // g
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scales is None:
+        scales = torch.empty(ng, dtype=torch.float32, device=x.device)
+    if workspace is None and g > 1:
+        workspace = torch.empty(int(load_library().sq_quantize_grouped_i8_workspace_bytes(rows, g)),
+                                dtype=torch.uint8, device=x.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ld = x.stride(0) if rows > 1 else cols
+    _check(load_library().sq_quantize_grouped_i8(_ptr(x), dt, rows, cols, ld, g, _ptr(q),
+                                                 _ptr(scales), _ptr(workspace), nbytes,
+                                                 _stream(stream)),
+           "sq_quantize_grouped_i8")
+    return q, scales
+
+
+def sq_gemm_i8_grouped(A: torch.Tensor, sA: torch.Tensor, group_a: int, B: torch.Tensor,
+                       sB: torch.Tensor, group_b: int, workspace: torch.Tensor,
+                       C: torch.Tensor = None, acc_out=None, want_c: bool = True, stream=None):
+    """INT8 GEMM with row-group scales sA[b][i // group_a], sB[b][j // group_b]."""
+    _need_cuda(A, B, sA, sB, workspace)
+    batched = A.dim() == 3
+    A3 = A if batched else A.unsqueeze(0)
+    B3 = B if batched else B.unsqueeze(0)
+    nb, M, K = A3.shape
+    N = B3.shape[1]
+    if not (A3.is_contiguous() and B3.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    shape = (nb, M, N) if batched else (M, N)
+    if want_c and C is None:
+        C = torch.empty(shape, dtype=torch.float32, device=A.device)
+    if acc_out is True:
+        acc_out = torch.empty(shape, dtype=torch.int32, device=A.device)
+    elif acc_out is False:
+        acc_out = None
+    _check(load_library().sq_gemm_i8_grouped(
+        _ptr(A3), _ptr(sA), int(group_a), _ptr(B3), _ptr(sB), int(group_b), nb, M, N, K, M * K,
+        N * K, M * N, _ptr(C), _ptr(acc_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "sq_gemm_i8_grouped")
+    return C, acc_out
+
+
 def sq_gemm_i8_rowscaled(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,
                          workspace: torch.Tensor, C: torch.Tensor = None, acc_out=None,
                          want_c: bool = True, stream=None):
@@ -246,6 +342,30 @@ def sq_gemm_fp8_scaled(A: torch.Tensor, B: torch.Tensor, sa: torch.Tensor, sb: t
     _check(load_library().sq_gemm_fp8_scaled(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), int(fmt),
                                              int(layout), M, N, K, _ptr(C), _stream(stream)),
            "sq_gemm_fp8_scaled")
+    return C
+
+
+def sq_gemm_fp8_scaled_e4m3(A: torch.Tensor, B: torch.Tensor, sa: torch.Tensor, sb: torch.Tensor,
+                            fmt: int, layout: int, out_scale: torch.Tensor, C: torch.Tensor = None,
+                            stream=None):
+    """E4M3 codes C = e4m3((acc * sa) * sb / out_scale) for FP8 codes A, B."""
+    _need_cuda(A, B, sa, sb, out_scale)
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    if layout == SQ_NT:
+        (M, K), N = A.shape, B.shape[0]
+    elif layout == SQ_NN:
+        (M, K), N = A.shape, B.shape[1]
+    elif layout == SQ_TN:
+        (K, M), N = A.shape, B.shape[1]
+    else:
+        raise ValueError("layout must be SQ_NT, SQ_NN or SQ_TN")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.uint8, device=A.device)
+    _check(load_library().sq_gemm_fp8_scaled_e4m3(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), int(fmt),
+                                                  int(layout), M, N, K, _ptr(out_scale), _ptr(C),
+                                                  _stream(stream)),
+           "sq_gemm_fp8_scaled_e4m3")
     return C
 
 

@@ -99,8 +99,30 @@ sq_status sq_quantize_fp8(const uint16_t* x_bf16, int64_t numel, const float* sc
     DeviceState* ds = device_state(&e);
     if (!ds) return from_cuda(e);
     return from_cuda(sq::launch_quantize_fp8(x_bf16, numel, scale, fmt, x8, amax,
-                                             static_cast<unsigned*>(workspace),
+                                             static_cast<unsigned*>(workspace), nullptr, 0, 0, 0,
                                              reinterpret_cast<cudaStream_t>(stream), ds->sms));
+}
+
+sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, uint8_t* x8,
+                               float* amax, float* ring, int64_t hist_len, int64_t idx, int margin,
+                               void* workspace, sq_stream stream) {
+    if (fmt != SQ_FMT_E4M3 && fmt != SQ_FMT_E5M2) return SQ_ERR_INVALID_ARG;
+    if (numel < 0 || !amax || !ring || !workspace) return SQ_ERR_INVALID_ARG;
+    if (numel > 0 && (!x_bf16 || !x8)) return SQ_ERR_INVALID_ARG;
+    if (hist_len < 1 || hist_len > (int64_t(1) << 20) || idx < 0 || idx >= hist_len)
+        return SQ_ERR_INVALID_ARG;
+    if (margin < -64 || margin > 64) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(x8) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(ring) & 3u))
+        return SQ_ERR_ALIGNMENT;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    return from_cuda(sq::launch_quantize_fp8(x_bf16, numel, nullptr, fmt, x8, amax,
+                                             static_cast<unsigned*>(workspace), ring,
+                                             static_cast<int>(hist_len), static_cast<int>(idx),
+                                             margin, reinterpret_cast<cudaStream_t>(stream),
+                                             ds->sms));
 }
 
 size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K) {
@@ -110,11 +132,14 @@ size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K
     return ((a + 255) & ~static_cast<size_t>(255)) + ((b + 255) & ~static_cast<size_t>(255));
 }
 
-sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B, const float* sB,
-                               int64_t batch, int64_t M, int64_t N, int64_t K, int64_t strideA,
-                               int64_t strideB, int64_t strideC, float* C, int32_t* acc_out,
-                               void* workspace, size_t workspace_bytes, sq_stream stream) {
-    if (batch < 1 || M < 1 || N < 1 || K < 1) return SQ_ERR_INVALID_ARG;
+namespace {
+
+sq_status gemm_i8_common(const int8_t* A, const float* sA, int64_t ga, const int8_t* B,
+                         const float* sB, int64_t gb, int64_t batch, int64_t M, int64_t N,
+                         int64_t K, int64_t strideA, int64_t strideB, int64_t strideC, float* C,
+                         int32_t* acc_out, void* workspace, size_t workspace_bytes,
+                         sq_stream stream) {
+    if (batch < 1 || M < 1 || N < 1 || K < 1 || ga < 1 || gb < 1) return SQ_ERR_INVALID_ARG;
     if (!A || !B || !sA || !sB || !workspace || (!C && !acc_out)) return SQ_ERR_INVALID_ARG;
     if (strideA < M * K || strideB < N * K || strideC < M * N) return SQ_ERR_INVALID_ARG;
     if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
@@ -127,6 +152,8 @@ sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B
     if (workspace_bytes < sq_gemm_i8_workspace_bytes(batch, M, N, K)) return SQ_ERR_INVALID_ARG;
     const int64_t mt = (M + 127) / 128, nt = (N + 127) / 128;
     if (mt * nt * batch > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    if (ga > M) ga = M;
+    if (gb > N) gb = N;
     cudaError_t e = cudaSuccess;
     DeviceState* ds = device_state(&e);
     if (!ds) return from_cuda(e);
@@ -138,21 +165,72 @@ sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B
     if (e != cudaSuccess) return SQ_ERR_CUDA;
     e = sq::launch_i8_to_f16(B, batch, N, K, strideB, B16, st, ds->sms);
     if (e != cudaSuccess) return SQ_ERR_CUDA;
-    return from_cuda(sq::launch_gemm_i8(A16, B16, sA, sB, static_cast<int>(batch),
+    return from_cuda(sq::launch_gemm_i8(A16, B16, sA, sB, static_cast<int>(ga),
+                                        static_cast<int>(gb), static_cast<int>(batch),
                                         static_cast<int>(M), static_cast<int>(N),
                                         static_cast<int>(K), strideC, C, acc_out, ds->err_word, st,
                                         ds->sms));
 }
 
-sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
-                             int fmt, int layout, int64_t M, int64_t N, int64_t K,
-                             uint16_t* C_bf16, sq_stream stream) {
+}  // namespace
+
+sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B, const float* sB,
+                               int64_t batch, int64_t M, int64_t N, int64_t K, int64_t strideA,
+                               int64_t strideB, int64_t strideC, float* C, int32_t* acc_out,
+                               void* workspace, size_t workspace_bytes, sq_stream stream) {
+    return gemm_i8_common(A, sA, 1, B, sB, 1, batch, M, N, K, strideA, strideB, strideC, C,
+                          acc_out, workspace, workspace_bytes, stream);
+}
+
+sq_status sq_gemm_i8_grouped(const int8_t* A, const float* sA, int64_t group_a, const int8_t* B,
+                             const float* sB, int64_t group_b, int64_t batch, int64_t M, int64_t N,
+                             int64_t K, int64_t strideA, int64_t strideB, int64_t strideC,
+                             float* C, int32_t* acc_out, void* workspace, size_t workspace_bytes,
+                             sq_stream stream) {
+    return gemm_i8_common(A, sA, group_a, B, sB, group_b, batch, M, N, K, strideA, strideB,
+                          strideC, C, acc_out, workspace, workspace_bytes, stream);
+}
+
+size_t sq_quantize_grouped_i8_workspace_bytes(int64_t rows, int64_t group_rows) {
+    if (rows <= 0 || group_rows <= 0) return 0;
+    const size_t ng = static_cast<size_t>((rows + group_rows - 1) / group_rows);
+    return (ng * 4 + 255) & ~static_cast<size_t>(255);
+}
+
+sq_status sq_quantize_grouped_i8(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                                 int64_t group_rows, int8_t* q, float* scales, void* workspace,
+                                 size_t workspace_bytes, sq_stream stream) {
+    if (dtype != SQ_F32 && dtype != SQ_BF16) return SQ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || ld < cols || group_rows < 1) return SQ_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return SQ_OK;
+    if (!x || !q || !scales) return SQ_ERR_INVALID_ARG;
+    if (group_rows > rows) group_rows = rows;
+    if (group_rows > 1 && (!workspace ||
+                           workspace_bytes < sq_quantize_grouped_i8_workspace_bytes(rows, group_rows)))
+        return SQ_ERR_INVALID_ARG;
+    if (group_rows > 1 && (reinterpret_cast<uintptr_t>(workspace) & 3u)) return SQ_ERR_ALIGNMENT;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    const int64_t esz = dtype == SQ_F32 ? 4 : 2;
+    const bool vec_ok = aligned16(x) && aligned16(q) && ((ld * esz) % 16 == 0) && (cols % 16 == 0);
+    return from_cuda(sq::launch_quantize_grouped_i8(x, dtype, rows, cols, ld, group_rows, q, scales,
+                                                    static_cast<unsigned*>(workspace), vec_ok,
+                                                    reinterpret_cast<cudaStream_t>(stream),
+                                                    ds->sms));
+}
+
+namespace {
+
+sq_status gemm_fp8_common(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                          int fmt, int layout, int64_t M, int64_t N, int64_t K, void* C,
+                          const float* out_scale, sq_stream stream) {
     if (fmt != SQ_FMT_E4M3 && fmt != SQ_FMT_E5M2) return SQ_ERR_INVALID_ARG;
     if (layout != SQ_NT && layout != SQ_NN && layout != SQ_TN) return SQ_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1) return SQ_ERR_INVALID_ARG;
-    if (!A || !B || !sa || !sb || !C_bf16) return SQ_ERR_INVALID_ARG;
+    if (!A || !B || !sa || !sb || !C) return SQ_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return SQ_ERR_UNSUPPORTED;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C_bf16)) return SQ_ERR_ALIGNMENT;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return SQ_ERR_ALIGNMENT;
     // TMA row pitches must be multiples of 16 bytes
     if (layout == SQ_NT && K % 16 != 0) return SQ_ERR_ALIGNMENT;
     if (layout == SQ_NN && (K % 16 != 0 || N % 16 != 0)) return SQ_ERR_ALIGNMENT;
@@ -162,9 +240,25 @@ sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa
     DeviceState* ds = device_state(&e);
     if (!ds) return from_cuda(e);
     return from_cuda(sq::launch_gemm_fp8(A, B, sa, sb, fmt, layout, static_cast<int>(M),
-                                         static_cast<int>(N), static_cast<int>(K), C_bf16,
+                                         static_cast<int>(N), static_cast<int>(K), C, out_scale,
                                          ds->err_word, reinterpret_cast<cudaStream_t>(stream),
                                          ds->sms));
+}
+
+}  // namespace
+
+sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                             int fmt, int layout, int64_t M, int64_t N, int64_t K,
+                             uint16_t* C_bf16, sq_stream stream) {
+    return gemm_fp8_common(A, B, sa, sb, fmt, layout, M, N, K, C_bf16, nullptr, stream);
+}
+
+sq_status sq_gemm_fp8_scaled_e4m3(const uint8_t* A, const uint8_t* B, const float* sa,
+                                  const float* sb, int fmt, int layout, int64_t M, int64_t N,
+                                  int64_t K, const float* out_scale, uint8_t* C_e4m3,
+                                  sq_stream stream) {
+    if (!out_scale) return SQ_ERR_INVALID_ARG;
+    return gemm_fp8_common(A, B, sa, sb, fmt, layout, M, N, K, C_e4m3, out_scale, stream);
 }
 
 namespace {

@@ -57,6 +57,11 @@ struct GemmParams {
     uint32_t idesc;
     int vec_store;
     unsigned* err_word;
+    const float* out_scale; // FP8 with E4M3 output: the output step (divided out)
+    int out_e4m3;           // FP8: 1 = C is E4M3 codes [M,N], 0 = bf16
+    int ga, gb;             // INT8: rows per scale group of A and B (1 = per row)
+    int Mg, Ng;             // INT8: scale groups per batch, ceil(M/ga), ceil(N/gb)
+    int sb_vec;             // INT8: sB may be read 4 floats at a time
 };
 
 // PAIR = false: one CTA per SM computes 128 x BN tiles (cta_group::1).
@@ -313,10 +318,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
         // where this warp reports that it has read an accumulator: the leader's barrier
         const uint32_t tempty_leader[2] = {PAIR ? cluster_addr(&tempty[0], 0) : 0u,
                                            PAIR ? cluster_addr(&tempty[1], 0) : 0u};
-        float fsa = 0.0f, fsb = 0.0f;
+        float fsa = 0.0f, fsb = 0.0f, fos = 1.0f, foy = 1.0f;
+        bool ofast = true;
         if (!I8) {
             fsa = *p.sa;
             fsb = *p.sb;
+            if (p.out_e4m3) {
+                fos = *p.out_scale;
+                foy = __frcp_rn(fos);
+                ofast = fos >= 0x1p-40f && fos <= 0x1p40f;
+            }
         }
         uint32_t it = 0;
         bool ok = true;
@@ -367,8 +378,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                 }
                 if (!ok) break;
                 if (row < p.M) {
-                    const float sArow = p.sa[static_cast<int64_t>(b) * p.M + row];
-                    const float* sBb = p.sb + static_cast<int64_t>(b) * p.N;
+                    const float sArow = p.sa[static_cast<int64_t>(b) * p.Mg + row / p.ga];
+                    const float* sBb = p.sb + static_cast<int64_t>(b) * p.Ng;
                     const int64_t obase = static_cast<int64_t>(b) * p.strideC + static_cast<int64_t>(row) * p.N;
                     float* Cf = static_cast<float*>(p.C);
 #pragma unroll
@@ -377,7 +388,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                         if (p.vec_store && col0 + 32 <= p.N) {
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
-                                const float4 s4 = *reinterpret_cast<const float4*>(sBb + col0 + 4 * v);
+                                float4 s4;
+                                if (p.sb_vec) {
+                                    s4 = *reinterpret_cast<const float4*>(sBb + col0 + 4 * v);
+                                } else {
+                                    s4.x = sBb[(col0 + 4 * v) / p.gb];
+                                    s4.y = sBb[(col0 + 4 * v + 1) / p.gb];
+                                    s4.z = sBb[(col0 + 4 * v + 2) / p.gb];
+                                    s4.w = sBb[(col0 + 4 * v + 3) / p.gb];
+                                }
                                 const int32_t a0 = sums[c][4 * v], a1 = sums[c][4 * v + 1];
                                 const int32_t a2 = sums[c][4 * v + 2], a3 = sums[c][4 * v + 3];
                                 if (p.acc_out)
@@ -402,7 +421,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                                     if (p.acc_out) p.acc_out[obase + col] = sums[c][i];
                                     if (Cf)
                                         Cf[obase + col] = __fmul_rn(
-                                            __fmul_rn(__int2float_rn(sums[c][i]), sArow), sBb[col]);
+                                            __fmul_rn(__int2float_rn(sums[c][i]), sArow),
+                                            sBb[col / p.gb]);
                                 }
                             }
                         }
@@ -425,7 +445,30 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                     tmem_ld32(tb + c * 32, r);
                     tmem_ld_wait();
                     const int col0 = n0 + c * 32;
-                    if (row < p.M) {
+                    if (row < p.M && p.out_e4m3) {
+                        // E4M3 output: code = e4m3(fl32(fl32(acc*sa)*sb) / out_scale)
+                        uint8_t* C8 = static_cast<uint8_t*>(p.C);
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            float v[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float w = __fmul_rn(__fmul_rn(__uint_as_float(r[4 * i + e]), fsa), fsb);
+                                v[e] = ofast ? fp8_quotient(w, fos, foy) : __fdiv_rn(w, fos);
+                            }
+                            pk[i] = fp8x2<0>(v[0], v[1]) | (fp8x2<0>(v[2], v[3]) << 16);
+                        }
+                        if (p.vec_store && col0 + 32 <= p.N) {
+                            st_v4(C8 + obase + col0, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                            st_v4(C8 + obase + col0 + 16, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.N)
+                                    C8[obase + col0 + i] = static_cast<uint8_t>(pk[i >> 2] >> (8 * (i & 3)));
+                        }
+                    } else if (row < p.M) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -611,15 +654,20 @@ static cudaError_t gemm_fp8_layout(const uint8_t* A, const uint8_t* B, int M, in
 }
 
 cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
-                            int fmt, int layout, int M, int N, int K, uint16_t* C,
-                            unsigned* err_word, cudaStream_t st, int sms) {
+                            int fmt, int layout, int M, int N, int K, void* C,
+                            const float* out_scale, unsigned* err_word, cudaStream_t st, int sms) {
     GemmParams p{};
     p.M = M; p.N = N; p.K = K; p.batch = 1;
     p.nkb = (K + kBKBytes - 1) / kBKBytes;
     p.kb_per_chunk = p.nkb;
     p.nchunks = 1;
     p.sa = sa; p.sb = sb; p.C = C; p.acc_out = nullptr; p.strideC = 0;
-    p.vec_store = (N % 8 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
+    p.out_scale = out_scale;
+    p.out_e4m3 = out_scale != nullptr;
+    p.ga = p.gb = 1;
+    p.Mg = M; p.Ng = N;
+    // 16-byte stores: 8 bf16 or 16 E4M3 codes per row piece
+    p.vec_store = (N % (p.out_e4m3 ? 16 : 8) == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
     p.err_word = err_word;
     if (layout == 0) return gemm_fp8_layout<false, false>(A, B, M, N, K, p, fmt, st, sms);
     if (layout == 1) return gemm_fp8_layout<false, true>(A, B, M, N, K, p, fmt, st, sms);
@@ -645,9 +693,9 @@ static cudaError_t gemm_i8_shape(const uint16_t* A16, const uint16_t* B16, int b
 }
 
 cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
-                           const float* sB, int batch, int M, int N, int K, int64_t strideC,
-                           float* C, int32_t* acc_out, unsigned* err_word, cudaStream_t st,
-                           int sms) {
+                           const float* sB, int ga, int gb, int batch, int M, int N, int K,
+                           int64_t strideC, float* C, int32_t* acc_out, unsigned* err_word,
+                           cudaStream_t st, int sms) {
     const int bk = kBKBytes / 2;
     GemmParams p{};
     p.M = M; p.N = N; p.K = K; p.batch = batch;
@@ -655,10 +703,13 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
     p.kb_per_chunk = kI8ChunkK / bk;
     p.nchunks = (p.nkb + p.kb_per_chunk - 1) / p.kb_per_chunk;
     p.sa = sA; p.sb = sB; p.C = C; p.acc_out = acc_out; p.strideC = strideC;
+    p.ga = ga; p.gb = gb;
+    p.Mg = (M + ga - 1) / ga;
+    p.Ng = (N + gb - 1) / gb;
     p.vec_store = (N % 4 == 0) && (strideC % 4 == 0) &&
                   (reinterpret_cast<uintptr_t>(C) % 16 == 0) &&
-                  (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0) &&
-                  (reinterpret_cast<uintptr_t>(sB) % 16 == 0);
+                  (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0);
+    p.sb_vec = (gb == 1) && (N % 4 == 0) && (reinterpret_cast<uintptr_t>(sB) % 16 == 0);
     p.err_word = err_word;
     if (pick_shape(M, N, batch, sms) == Shape::Pair256)
         return gemm_i8_shape<256, true>(A16, B16, batch, M, N, K, p, st, sms);

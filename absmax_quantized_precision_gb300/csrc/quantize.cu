@@ -52,24 +52,9 @@ struct Elem<uint16_t> {   // bf16 bit patterns; widening is exact
     }
 };
 
-// Correctly rounded quotient x / s from y = RN(1/s), by the FMA correction
-// step of Markstein ("Computation of elementary functions on the IBM RISC
-// System/6000 processor", IBM J. Res. Dev. 34(1), 1990; the division theorem
-// in Muller et al., Handbook of Floating-Point Arithmetic): q = RN(x*y) lies
-// within one ulp of x/s, so r = x - s*q is exact in one FMA, and RN(q + r*y)
-// is RN(x/s) -- provided no intermediate value underflows or overflows.
-// Callers use it only where that holds for every quotient whose value can
-// change the code they produce; elsewhere they divide with __fdiv_rn.
-__device__ __forceinline__ float div_rn_recip(float x, float s, float y) {
-    const float q = __fmul_rn(x, y);
-    const float r = __fmaf_rn(-q, s, x);
-    return __fmaf_rn(r, y, q);
-}
-
 // The INT8 quotient only matters where |x/s| >= 1/2; with s in [2^-34, 2^40]
 // (s >= 1e-8/127 > 2^-34 always) those quotients and their residuals stay in
 // the normal range, and |x/s| <= 128 rules out overflow.
-constexpr float kRecipLo = 0x1p-34f;
 constexpr float kRecipHi = 0x1p40f;
 
 __device__ __forceinline__ int8_t clamp_i8(int n) {
@@ -234,30 +219,137 @@ cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, i
                                 st, sms);
 }
 
-// ================================================================== FP8 tensor
-template <int FMT>
-__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
-    uint16_t r;
-    if (FMT == 0)
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    else
-        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
+// ================================================================== INT8 row groups
+// Row-group quantization (scmp_kernels README group_a / group_b, per_tensor;
+// the POPCORNBENCH trace's per-tensor fake-quant): consecutive groups of
+// group_rows rows share s_g = max(amax_g, 1e-8) / 127.  Two passes, since a
+// group's scale depends on rows other CTAs read: (1) amax per group into a
+// zeroed workspace word (atomicMax on the bits; every warp owns a contiguous
+// run of rows and flushes once per group it touches), (2) encode.  Both
+// passes give each row to one warp; 16-byte vector access when rows allow it.
+template <typename T, bool VEC>
+__device__ __forceinline__ float row_absmax_warp(const T* xr, int64_t cols, int lane) {
+    constexpr int EPV = Elem<T>::kPerVec;
+    float m = 0.0f;
+    if (VEC) {
+        const int64_t nvec = cols / EPV;
+        for (int64_t vi = lane; vi < nvec; vi += 32) {
+            float v[EPV];
+            Elem<T>::unpack(ld_stream_v4(xr + vi * EPV), v);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf(v[e]));
+        }
+    } else {
+        for (int64_t k = lane; k < cols; k += 32) m = fmaxf(m, fabsf(Elem<T>::load1(xr + k)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    return m;
 }
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256) group_absmax_kernel(const T* __restrict__ x, int64_t rows,
+                                                           int64_t cols, int64_t ld,
+                                                           int64_t group_rows,
+                                                           unsigned* __restrict__ amax_bits) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t per = (rows + nwarps - 1) / nwarps;
+    const int64_t r0 = warp * per;
+    const int64_t r1 = r0 + per < rows ? r0 + per : rows;
+    int64_t gcur = -1;
+    float mcur = 0.0f;
+    for (int64_t r = r0; r < r1; ++r) {
+        const int64_t g = r / group_rows;
+        if (g != gcur) {
+            if (gcur >= 0 && lane == 0) atomicMax(&amax_bits[gcur], __float_as_uint(mcur));
+            gcur = g;
+            mcur = 0.0f;
+        }
+        mcur = fmaxf(mcur, row_absmax_warp<T, VEC>(x + r * ld, cols, lane));
+    }
+    if (gcur >= 0 && lane == 0) atomicMax(&amax_bits[gcur], __float_as_uint(mcur));
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256) group_encode_kernel(const T* __restrict__ x, int64_t rows,
+                                                           int64_t cols, int64_t ld,
+                                                           int64_t group_rows,
+                                                           const unsigned* __restrict__ amax_bits,
+                                                           int8_t* __restrict__ q,
+                                                           float* __restrict__ scales) {
+    constexpr int EPV = Elem<T>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t r = warp; r < rows; r += nwarps) {
+        const int64_t g = r / group_rows;
+        const float s = row_scale(__uint_as_float(amax_bits[g]));
+        const bool fast = s <= kRecipHi;
+        const float y = __frcp_rn(s);
+        if (lane == 0 && r == g * group_rows) scales[g] = s;
+        const T* xr = x + r * ld;
+        int8_t* qr = q + r * cols;
+        if (VEC) {
+            const int64_t nvec = cols / EPV;
+            for (int64_t vi = lane; vi < nvec; vi += 32) {
+                float v[EPV];
+                Elem<T>::unpack(ld_stream_v4(xr + vi * EPV), v);
+                uint32_t packed[EPV / 4];
+#pragma unroll
+                for (int w = 0; w < EPV / 4; ++w) {
+                    uint32_t b[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        b[e] = static_cast<uint8_t>(fast ? encode_i8_recip(v[4 * w + e], s, y)
+                                                         : encode_i8(v[4 * w + e], s));
+                    packed[w] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+                }
+                if (EPV == 4) *reinterpret_cast<uint32_t*>(qr + vi * EPV) = packed[0];
+                else *reinterpret_cast<uint2*>(qr + vi * EPV) = make_uint2(packed[0], packed[EPV / 4 - 1]);
+            }
+        } else {
+            for (int64_t k = lane; k < cols; k += 32) qr[k] = encode_i8(Elem<T>::load1(xr + k), s);
+        }
+    }
+}
+
+template <typename T>
+static cudaError_t launch_grouped(const T* x, int64_t rows, int64_t cols, int64_t ld,
+                                  int64_t group_rows, int8_t* q, float* scales, unsigned* ws,
+                                  bool vec_ok, cudaStream_t st, int sms) {
+    const int64_t ngroups = (rows + group_rows - 1) / group_rows;
+    cudaError_t e = cudaMemsetAsync(ws, 0, static_cast<size_t>(ngroups) * sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+    int64_t blocks = (rows + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (vec_ok) {
+        group_absmax_kernel<T, true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, group_rows, ws);
+        group_encode_kernel<T, true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, group_rows, ws, q, scales);
+    } else {
+        group_absmax_kernel<T, false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, group_rows, ws);
+        group_encode_kernel<T, false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, group_rows, ws, q, scales);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_grouped_i8(const void* x, int dtype, int64_t rows, int64_t cols,
+                                       int64_t ld, int64_t group_rows, int8_t* q, float* scales,
+                                       unsigned* ws, bool vec_ok, cudaStream_t st, int sms) {
+    if (group_rows == 1)
+        return launch_quantize_rowwise_i8(x, dtype, rows, cols, ld, q, scales, vec_ok, st, sms);
+    if (dtype == 0)
+        return launch_grouped<float>(static_cast<const float*>(x), rows, cols, ld, group_rows, q,
+                                     scales, ws, vec_ok, st, sms);
+    return launch_grouped<uint16_t>(static_cast<const uint16_t*>(x), rows, cols, ld, group_rows, q,
+                                    scales, ws, vec_ok, st, sms);
+}
+
+// ================================================================== FP8 tensor
 
 // 16 bf16 (two 16-B words) -> 16 FP8 codes (one 16-B word); m = running max|x|.
-// x / s for the FP8 path.  With s in [2^-40, 2^40] every quotient that can
-// change an FP8 code (|x/s| in [2^-18, 2^18]: below, the code is +-0; above,
-// it saturates) keeps its residual in the normal range, so div_rn_recip is
-// exact there.  Quotients that overflow keep q (they saturate either way) and
-// the sign is taken from x, as the sign of x/s is for s > 0 (this keeps -0).
-__device__ __forceinline__ float fp8_quotient(float x, float s, float y) {
-    const float q = __fmul_rn(x, y);
-    const float r = __fmaf_rn(-q, s, x);
-    float t = (fabsf(q) < 0x1p100f) ? __fmaf_rn(r, y, q) : q;
-    return __int_as_float((__float_as_int(t) & 0x7FFFFFFF) | (__float_as_int(x) & 0x80000000));
-}
-
 template <int FMT, bool FAST>
 __device__ __forceinline__ uint4 fp8_encode16(const uint4& a, const uint4& b, float s, float y,
                                               float& m) {
@@ -282,15 +374,27 @@ __device__ __forceinline__ uint4 fp8_encode16(const uint4& a, const uint4& b, fl
 }
 
 // Each thread converts 32 elements per step (four 16-B loads in flight).
+//
+// Plain mode (ring == nullptr): the step is *scale; ws = [amax bits | ticket].
+// Ring mode: delayed scaling with ring = [hist (hist_len) | scale | counter]
+// (the AstrAI commit notes' scale ring): the step is ring[hist_len], the
+// ticket counter is the ring's last word, and the last block records the amax
+// in hist[ring_idx], takes the max over the window and publishes the next
+// step fl32(fl32(max * 2^margin) / fmt_max) in ring[hist_len] (kept as it was
+// when the window max is 0) -- no extra launch.  ws[0] still accumulates the
+// amax bits.  Both modes leave their counter and ws[0] at zero.
 template <int FMT>
 __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restrict__ x, int64_t n,
                                                         const float* __restrict__ scale,
                                                         uint8_t* __restrict__ x8,
                                                         float* __restrict__ amax_out,
-                                                        unsigned* __restrict__ ws) {
+                                                        unsigned* __restrict__ ws, float* ring,
+                                                        int hist_len, int ring_idx, int margin) {
     __shared__ float red[8];
     __shared__ int is_last;
-    const float s = *scale;
+    __shared__ float s_amax;
+    const float s = ring ? ring[hist_len] : *scale;
+    unsigned* counter = ring ? reinterpret_cast<unsigned*>(ring + hist_len + 1) : ws + 1;
     const float y = __frcp_rn(s);
     const bool fast = s >= 0x1p-40f && s <= 0x1p40f;
     float m = 0.0f;
@@ -320,7 +424,8 @@ __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restri
         const int64_t i = tail0 + tid;
         float f = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
         m = fmaxf(m, fabsf(f));
-        x8[i] = static_cast<uint8_t>(fp8x2<FMT>(__fdiv_rn(f, s), 0.0f) & 0xFFu);
+        const float t = fast ? fp8_quotient(f, s, y) : __fdiv_rn(f, s);
+        x8[i] = static_cast<uint8_t>(fp8x2<FMT>(t, 0.0f) & 0xFFu);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -332,30 +437,53 @@ __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restri
         // max|x| >= 0, so the float order equals the unsigned order of the bits
         atomicMax(&ws[0], __float_as_uint(bm));
         __threadfence();
-        const unsigned ticket = atomicAdd(&ws[1], 1u);
+        const unsigned ticket = atomicAdd(counter, 1u);
         is_last = (ticket == gridDim.x - 1);
     }
     __syncthreads();
-    if (is_last && threadIdx.x == 0) {
-        __threadfence();
-        const unsigned bits = atomicExch(&ws[0], 0u);
-        *amax_out = __uint_as_float(bits);
-        atomicExch(&ws[1], 0u);
+    if (!is_last) return;          // uniform across the block
+    __threadfence();
+    if (threadIdx.x == 0) {
+        s_amax = __uint_as_float(atomicExch(&ws[0], 0u));
+        *amax_out = s_amax;
     }
+    if (ring) {
+        __syncthreads();
+        const float a = s_amax;
+        float wm = 0.0f;
+        for (int i = threadIdx.x; i < hist_len; i += blockDim.x)
+            wm = fmaxf(wm, i == ring_idx ? a : ring[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = wm;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < (int)(blockDim.x >> 5); ++w) wm = fmaxf(wm, red[w]);
+            wm = fmaxf(wm, red[0]);
+            ring[ring_idx] = a;
+            if (wm > 0.0f) {
+                const float fmax_v = FMT == 0 ? 448.0f : 57344.0f;
+                ring[hist_len] = __fdiv_rn(ldexpf(wm, margin), fmax_v);
+            }
+        }
+    }
+    if (threadIdx.x == 0) atomicExch(counter, 0u);
 }
 
 cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
-                                uint8_t* x8, float* amax, unsigned* ws, cudaStream_t st,
-                                int sms) {
+                                uint8_t* x8, float* amax, unsigned* ws, float* ring, int hist_len,
+                                int ring_idx, int margin, cudaStream_t st, int sms) {
     const int64_t nchunk = n / 32;
     int64_t blocks = (nchunk + 255) / 256;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (fmt == 0)
-        quant_fp8_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, n, scale, x8, amax, ws);
+        quant_fp8_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+            x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin);
     else
-        quant_fp8_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, n, scale, x8, amax, ws);
+        quant_fp8_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+            x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin);
     return cudaGetLastError();
 }
 

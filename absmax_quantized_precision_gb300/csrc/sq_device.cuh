@@ -337,6 +337,45 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
         : "memory");
 }
 
+// ------------------------------------------------------------------ division
+// Correctly rounded quotient x / s from y = RN(1/s), by the FMA correction
+// step of Markstein ("Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990; the division theorem
+// in Muller et al., Handbook of Floating-Point Arithmetic): q = RN(x*y) lies
+// within one ulp of x/s, so r = x - s*q is exact in one FMA, and RN(q + r*y)
+// is RN(x/s) -- provided no intermediate value underflows or overflows.
+// Callers use it only where that holds for every quotient whose value can
+// change the code they produce; elsewhere they divide with __fdiv_rn.
+__device__ __forceinline__ float div_rn_recip(float x, float s, float y) {
+    const float q = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q, s, x);
+    return __fmaf_rn(r, y, q);
+}
+
+// x / s for the FP8 path.  With s in [2^-40, 2^40] every quotient that can
+// change an FP8 code (|x/s| in [2^-18, 2^18]: below, the code is +-0; above,
+// it saturates) keeps its residual in the normal range, so div_rn_recip is
+// exact there.  Quotients that overflow keep q (they saturate either way) and
+// the sign is taken from x, as the sign of x/s is for s > 0 (this keeps -0).
+__device__ __forceinline__ float fp8_quotient(float x, float s, float y) {
+    const float q = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q, s, x);
+    float t = (fabsf(q) < 0x1p100f) ? __fmaf_rn(r, y, q) : q;
+    return __int_as_float((__float_as_int(t) & 0x7FFFFFFF) | (__float_as_int(x) & 0x80000000));
+}
+
+// Two floats to two FP8 codes (RNE, saturating to the largest finite value);
+// `lo` lands in the low byte.  FMT 0 = E4M3, 1 = E5M2.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
+    uint16_t r;
+    if (FMT == 0)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 v;

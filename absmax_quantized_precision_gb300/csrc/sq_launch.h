@@ -11,8 +11,17 @@ cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, i
                                        int64_t ld, int8_t* q, float* scales, bool vec_ok,
                                        cudaStream_t st, int sms);
 
+// Row groups of group_rows rows share one scale; ws holds ceil(rows/group_rows)
+// words (zeroed by the launcher with cudaMemsetAsync).
+cudaError_t launch_quantize_grouped_i8(const void* x, int dtype, int64_t rows, int64_t cols,
+                                       int64_t ld, int64_t group_rows, int8_t* q, float* scales,
+                                       unsigned* ws, bool vec_ok, cudaStream_t st, int sms);
+
+// ring == nullptr: plain per-tensor quantize with step *scale.  Otherwise
+// delayed scaling with ring = [hist (hist_len) | scale | counter].
 cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
-                                uint8_t* x8, float* amax, unsigned* ws, cudaStream_t st, int sms);
+                                uint8_t* x8, float* amax, unsigned* ws, float* ring, int hist_len,
+                                int ring_idx, int margin, cudaStream_t st, int sms);
 
 // Staging of INT8 codes as exact fp16 values: dst[b][r][k] = src[b*stride + r*K + k].
 cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
@@ -20,13 +29,16 @@ cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int
 
 // 0 on success, a cudaError_t otherwise; CUDA_ERROR_* from tensor-map encoding
 // is reported as cudaErrorInvalidValue.
+// C is bf16 [M,N] when out_scale == nullptr, else E4M3 codes [M,N] with the
+// output step *out_scale divided out.
 cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
-                            int fmt, int layout, int M, int N, int K, uint16_t* C,
-                            unsigned* err_word, cudaStream_t st, int sms);
+                            int fmt, int layout, int M, int N, int K, void* C,
+                            const float* out_scale, unsigned* err_word, cudaStream_t st, int sms);
 
+// Scales of row i of A in batch b: sA[b*ceil(M/ga) + i/ga] (ga = 1: per row).
 cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
-                           const float* sB, int batch, int M, int N, int K, int64_t strideC,
-                           float* C, int32_t* acc_out, unsigned* err_word, cudaStream_t st,
-                           int sms);
+                           const float* sB, int ga, int gb, int batch, int M, int N, int K,
+                           int64_t strideC, float* C, int32_t* acc_out, unsigned* err_word,
+                           cudaStream_t st, int sms);
 
 }  // namespace sq

@@ -117,6 +117,32 @@ sq_status sq_quantize_fp8(const uint16_t* x_bf16, int64_t numel, const float* sc
                           uint8_t* x8, float* amax, void* workspace, sq_stream stream);
 
 /*
+ * Per-tensor FP8 quantization with delayed scaling kept in a history ring
+ * [P3 linear_forward_fp8 / linear_backward_fp8 ring arguments; commit notes:
+ * the quantize kernel finishes the ring in its last block, so the next
+ * step's scale is published on the device with no extra launch].
+ *
+ *   ring     float32[hist_len + 2], device: [hist | scale | counter].  The
+ *            step used for this call is ring[hist_len].  The counter word
+ *            (uint32 bits) must be zero before the first call; every completed
+ *            call leaves it zero.
+ *   After the codes and the amax are written (as sq_quantize_fp8 does):
+ *            hist[idx] = amax;  m = max(hist[0..hist_len));
+ *            if m > 0: ring[hist_len] = fl32(fl32(m * 2^margin) / fmt_max)
+ *            (fmt_max 448 for E4M3, 57344 for E5M2); else the step is kept.
+ *            The pages state no formula; margin > 0 adds headroom and
+ *            margin 0 gives the previous-amax / fmt_max delayed recipe.
+ *   idx      0 <= idx < hist_len (the caller rolls it, e.g. step % hist_len).
+ *   margin   -64 .. 64.
+ *   workspace  sq_workspace_bytes() bytes, zeroed once (it holds the running
+ *            amax); x_bf16 and x8 16-byte aligned.
+ * Calls sharing a ring or a workspace must not overlap on the GPU.
+ */
+sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, uint8_t* x8,
+                               float* amax, float* ring, int64_t hist_len, int64_t idx, int margin,
+                               void* workspace, sq_stream stream);
+
+/*
  * Bytes of workspace that sq_gemm_i8_rowscaled needs for these sizes (the
  * INT8 codes are staged as exact 16-bit values for the tensor cores).
  */
@@ -146,6 +172,39 @@ sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B
                                sq_stream stream);
 
 /*
+ * Row-group symmetric INT8 quantization  [P1 sc_matmul group_a / group_b
+ * (row-group size) and per_tensor granularity; P2 formula, which is per
+ * tensor].  Consecutive groups of group_rows rows share one scale:
+ *
+ *   s_g = fl32(max(max|x| over the rows of group g, 1e-8) / 127),
+ *   q   = clamp(rne(fl32(x / s_g)), -127, 127)
+ *
+ * group_rows = 1 is sq_quantize_rowwise_i8; group_rows >= rows is per tensor.
+ *   scales    ceil(rows / group_rows) float32.
+ *   workspace sq_quantize_grouped_i8_workspace_bytes(rows, group_rows) bytes,
+ *             4-byte aligned, no initialisation needed (the call clears the
+ *             words it uses with cudaMemsetAsync); unused when group_rows = 1.
+ * Other arguments as sq_quantize_rowwise_i8.  Two passes over x (the scale of
+ * a group depends on rows that other blocks read).
+ */
+size_t sq_quantize_grouped_i8_workspace_bytes(int64_t rows, int64_t group_rows);
+sq_status sq_quantize_grouped_i8(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                                 int64_t group_rows, int8_t* q, float* scales, void* workspace,
+                                 size_t workspace_bytes, sq_stream stream);
+
+/*
+ * INT8 GEMM with row-group scales  [P1 sc_matmul group_a / group_b].  As
+ * sq_gemm_i8_rowscaled, but the dequantization reads
+ *   sA[b*ceil(M/group_a) + i/group_a]  and  sB[b*ceil(N/group_b) + j/group_b];
+ * group 1 is per row, group >= M (or N) is per tensor.
+ */
+sq_status sq_gemm_i8_grouped(const int8_t* A, const float* sA, int64_t group_a, const int8_t* B,
+                             const float* sB, int64_t group_b, int64_t batch, int64_t M, int64_t N,
+                             int64_t K, int64_t strideA, int64_t strideB, int64_t strideC,
+                             float* C, int32_t* acc_out, void* workspace, size_t workspace_bytes,
+                             sq_stream stream);
+
+/*
  * Scaled FP8 GEMM  [P3 custom::fp8_gemm: a @ b * (sa * sb), FP32 accumulate,
  * BF16 out; layouts per the commit notes: NT forward, dX and dW].
  *
@@ -160,6 +219,26 @@ sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B
 sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa,
                              const float* sb, int fmt, int layout, int64_t M, int64_t N,
                              int64_t K, uint16_t* C_bf16, sq_stream stream);
+
+/*
+ * Scaled FP8 GEMM with an FP8 E4M3 output  [P3 custom::fp8_gemm with
+ * out_dtype = 1 and mm_fp8(out_dtype="e4m3"): the output is quantized to E4M3
+ * with its own step out_scale, for layer-to-layer FP8 pipelines].
+ *
+ *   C[i,j] = e4m3(fl32(fl32(fl32(acc[i,j] * *sa) * *sb) / *out_scale))
+ *
+ * with the division rounded as IEEE float32 division and RNE, saturating
+ * encoding to +-448.  The pages disagree on whether out_scale multiplies or
+ * divides (the adapter's docstring calls it the output quantization step, its
+ * CPU path multiplies); this library divides, as for every other step.
+ *   out_scale  device pointer to one float32 (> 0).
+ *   C_e4m3     [M,N] E4M3 codes (uint8), packed rows, 16-byte aligned.
+ * Other arguments and limits as sq_gemm_fp8_scaled.
+ */
+sq_status sq_gemm_fp8_scaled_e4m3(const uint8_t* A, const uint8_t* B, const float* sa,
+                                  const float* sb, int fmt, int layout, int64_t M, int64_t N,
+                                  int64_t K, const float* out_scale, uint8_t* C_e4m3,
+                                  sq_stream stream);
 
 /*
  * Reads and clears the device-side error word of the current device after

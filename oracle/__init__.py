@@ -63,10 +63,20 @@ def _load():
             L.or_quantize_rowwise_i8.restype = i32
             L.or_quantize_fp8.argtypes = [vp, i64, f32, i32, vp, vp]
             L.or_quantize_fp8.restype = i32
+            L.or_quantize_fp8_ring.argtypes = [vp, i64, i32, vp, vp, vp, i64, i64, i32]
+            L.or_quantize_fp8_ring.restype = i32
             L.or_gemm_i8.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, vp, vp]
             L.or_gemm_i8.restype = i32
             L.or_gemm_fp8.argtypes = [vp, vp, i32, i32, i64, i64, i64, f32, f32, vp, i64, vp, vp]
             L.or_gemm_fp8.restype = i32
+            L.or_gemm_fp8_e4m3.argtypes = [vp, vp, i32, i32, i64, i64, i64, f32, f32, f32, vp, i64,
+                                           vp, vp]
+            L.or_gemm_fp8_e4m3.restype = i32
+            L.or_quantize_grouped_i8.argtypes = [vp, i32, i64, i64, i64, i64, vp, vp]
+            L.or_quantize_grouped_i8.restype = i32
+            L.or_gemm_i8_grouped.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64,
+                                             vp, vp]
+            L.or_gemm_i8_grouped.restype = i32
             L.or_num_threads.argtypes = []
             L.or_num_threads.restype = i32
             _lib = L
@@ -142,6 +152,46 @@ def quantize_rowwise_i8(x: np.ndarray, dtype: int = F32):
     return q, s
 
 
+def quantize_grouped_i8(x: np.ndarray, group_rows: int, dtype: int = F32):
+    """Row-group INT8 of a 2-D array (groups of group_rows consecutive rows;
+    group_rows >= rows is per tensor).  Returns (q, scales[ceil(rows/g)])."""
+    x = np.ascontiguousarray(x)
+    if (dtype == F32 and x.dtype != np.float32) or (dtype == BF16 and x.dtype != np.uint16):
+        raise TypeError("dtype mismatch")
+    rows, cols = x.shape
+    q = np.empty(x.shape, dtype=np.int8)
+    s = np.empty((rows + group_rows - 1) // group_rows, dtype=np.float32)
+    if _load().or_quantize_grouped_i8(_ptr(x), int(dtype), rows, cols, cols, int(group_rows),
+                                      _ptr(q), _ptr(s)) != 0:
+        raise ValueError("bad arguments")
+    return q, s
+
+
+def gemm_i8_grouped(A, B, sa, sb, ga: int, gb: int, rows=None):
+    """C[b] = A[b] B[b]^T with row-group scales sa[b][i // ga], sb[b][j // gb].
+    A, B 2-D or 3-D int8; sa, sb flat per batch.  Returns (acc, C)."""
+    A = _c(A, np.int8)
+    B = _c(B, np.int8)
+    batched = A.ndim == 3
+    if not batched:
+        A, B = A[None], B[None]
+    nb, M, K = A.shape
+    N = B.shape[1]
+    sa = _c(np.asarray(sa, dtype=np.float32).reshape(-1), np.float32)
+    sb = _c(np.asarray(sb, dtype=np.float32).reshape(-1), np.float32)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = M if r is None else r.size
+    acc = np.empty((nb, nr, N), dtype=np.int32)
+    C = np.empty((nb, nr, N), dtype=np.float32)
+    rc = _load().or_gemm_i8_grouped(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), int(ga), int(gb), nb,
+                                    M, N, K, _ptr(r), nr, _ptr(acc), _ptr(C))
+    if rc < 0:
+        raise ValueError("bad arguments")
+    if rc == 1:
+        raise OverflowError("an exact INT8 accumulator does not fit int32")
+    return (acc, C) if batched else (acc[0], C[0])
+
+
 def quantize_fp8(x_bf16: np.ndarray, scale: float, fmt: int):
     """Per-tensor FP8 of bf16 bits with the scale divided out.  Returns (x8, amax)."""
     x = _c(x_bf16, np.uint16)
@@ -149,6 +199,22 @@ def quantize_fp8(x_bf16: np.ndarray, scale: float, fmt: int):
     amax = np.zeros(1, dtype=np.float32)
     if _load().or_quantize_fp8(_ptr(x), x.size, float(np.float32(scale)), int(fmt),
                                _ptr(x8), _ptr(amax)) != 0:
+        raise ValueError("bad arguments")
+    return x8, np.float32(amax[0])
+
+
+def quantize_fp8_ring(x_bf16: np.ndarray, fmt: int, ring: np.ndarray, idx: int, margin: int = 0):
+    """Delayed-scaling quantize: uses ring[H] as the step, records the amax in
+    ring[idx] and publishes the next step in ring[H] (in place).
+    ring = float32[H + 2] laid out [hist | scale | counter].  Returns (x8, amax)."""
+    x = _c(x_bf16, np.uint16)
+    if ring.dtype != np.float32 or not ring.flags.c_contiguous or ring.size < 3:
+        raise TypeError("ring must be a contiguous float32 array of H + 2 entries")
+    H = ring.size - 2
+    x8 = np.empty(x.shape, dtype=np.uint8)
+    amax = np.zeros(1, dtype=np.float32)
+    if _load().or_quantize_fp8_ring(_ptr(x), x.size, int(fmt), _ptr(x8), _ptr(amax), _ptr(ring),
+                                    H, int(idx), int(margin)) != 0:
         raise ValueError("bad arguments")
     return x8, np.float32(amax[0])
 
@@ -221,6 +287,46 @@ def gemm_fp8(A8, B8, fmt: int, layout: int, sa: float, sb: float, rows=None, wan
     if rc != 0:
         raise ValueError("bad arguments")
     return ref, bf
+
+
+def gemm_fp8_e4m3(A8, B8, fmt: int, layout: int, sa: float, sb: float, out_scale: float,
+                  rows=None):
+    """FP8 GEMM with E4M3 output.  Returns (t_ref float64 = ref / out_scale,
+    codes uint8 from the oracle's own float32 scaling)."""
+    A8 = _c(A8, np.uint8)
+    B8 = _c(B8, np.uint8)
+    if layout == NT:
+        (M, K), N = A8.shape, B8.shape[0]
+    elif layout == NN:
+        (M, K), N = A8.shape, B8.shape[1]
+    elif layout == TN:
+        (K, M), N = A8.shape, B8.shape[1]
+    else:
+        raise ValueError("layout must be NT, NN or TN")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = M if r is None else r.size
+    t = np.empty((nr, N), dtype=np.float64)
+    codes = np.empty((nr, N), dtype=np.uint8)
+    rc = _load().or_gemm_fp8_e4m3(_ptr(A8), _ptr(B8), int(fmt), int(layout), M, N, K,
+                                  float(np.float32(sa)), float(np.float32(sb)),
+                                  float(np.float32(out_scale)), _ptr(r), nr, _ptr(t), _ptr(codes))
+    if rc != 0:
+        raise ValueError("bad arguments")
+    return t, codes
+
+
+def e4m3_acceptable(codes, t_ref, slack):
+    """True where the E4M3 code's value lies between the representable values
+    bracketing [t_ref - slack, t_ref + slack] (what RNE of any value in that
+    interval can give), saturating at +-448."""
+    tab = fp8_decode_table(E4M3)
+    vals = np.unique(tab[np.isfinite(tab)])
+    lo = np.clip(t_ref - slack, -448.0, 448.0)
+    hi = np.clip(t_ref + slack, -448.0, 448.0)
+    lo_rep = vals[np.clip(np.searchsorted(vals, lo, side="right") - 1, 0, vals.size - 1)]
+    hi_rep = vals[np.clip(np.searchsorted(vals, hi, side="left"), 0, vals.size - 1)]
+    got = tab[codes]
+    return (got >= lo_rep) & (got <= hi_rep)
 
 
 def fp8_gemm_bound(ref: np.ndarray, K: int, sa: float, sb: float, maxa8: float, maxb8: float):

@@ -210,6 +210,42 @@ int or_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols,
     return 0;
 }
 
+// Row-group symmetric INT8 (scmp_kernels README: group_a / group_b row-group
+// sizes; per_tensor granularity; the POPCORNBENCH trace's per-tensor formula):
+// rows are split into consecutive groups of group_rows rows (the last may be
+// shorter); each group g has s_g = fl32(max(max|x| over the group, 1e-8)/127)
+// and q = clamp(rne(fl32(x / s_g)), -127, 127).  group_rows = 1 is per row;
+// group_rows >= rows is per tensor.  scales: ceil(rows / group_rows) floats.
+int or_quantize_grouped_i8(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                           int64_t group_rows, int8_t* q, float* scales) {
+    if (rows < 0 || cols < 0 || ld < cols || group_rows < 1 || (dtype != 0 && dtype != 1))
+        return -1;
+    const int64_t ngroups = (rows + group_rows - 1) / group_rows;
+    const float floor_amax = 1e-8f;
+    for (int64_t g = 0; g < ngroups; ++g) {
+        const int64_t r0 = g * group_rows;
+        const int64_t r1 = r0 + group_rows < rows ? r0 + group_rows : rows;
+        float amax = 0.0f;
+        for (int64_t r = r0; r < r1; ++r)
+            for (int64_t k = 0; k < cols; ++k) {
+                float a = std::fabs(load_elem(x, dtype, r * ld + k));
+                if (a > amax) amax = a;
+            }
+        float a = amax < floor_amax ? floor_amax : amax;
+        float s = a / 127.0f;
+        scales[g] = s;
+        for (int64_t r = r0; r < r1; ++r)
+            for (int64_t k = 0; k < cols; ++k) {
+                float t = load_elem(x, dtype, r * ld + k) / s;
+                int32_t n = round_half_even(t);
+                if (n > 127) n = 127;
+                if (n < -127) n = -127;
+                q[r * cols + k] = (int8_t)n;
+            }
+    }
+    return 0;
+}
+
 // Per-tensor FP8 quantize of bf16 input with the scale divided out; returns
 // the raw amax = max|x| through *amax.
 int or_quantize_fp8(const uint16_t* x, int64_t n, float scale, int fmt, uint8_t* x8,
@@ -224,6 +260,33 @@ int or_quantize_fp8(const uint16_t* x, int64_t n, float scale, int fmt, uint8_t*
         x8[i] = encode(v / scale, *f);
     }
     *amax = m;
+    return 0;
+}
+
+// Delayed scaling with a history ring (AstrAI ops/fp8.py, linear_forward_fp8
+// docstring and commit notes: the measured amax lands in hist[idx] and the
+// next step's scale is published on the device).  ring = [hist (H) | scale |
+// counter]; the scale used for this quantization is ring[H].  After
+// quantizing: hist[idx] = amax; m = max(hist); if m > 0 the next step is
+// fl32(fl32(m * 2^margin) / fmt_max) (margin adds headroom; the pages give no
+// formula -- at margin 0 this is the previous-amax / fmt_max recipe), else
+// the scale is left as it was.  The counter slot is not touched.
+int or_quantize_fp8_ring(const uint16_t* x, int64_t n, int fmt, uint8_t* x8, float* amax,
+                         float* ring, int64_t H, int64_t idx, int margin) {
+    const Fp8* f = fmt_of(fmt);
+    if (!f || n < 0 || H < 1 || idx < 0 || idx >= H || margin < -64 || margin > 64) return -1;
+    const float scale = ring[H];
+    int rc = or_quantize_fp8(x, n, scale, fmt, x8, amax);
+    if (rc) return rc;
+    ring[idx] = *amax;
+    float m = 0.0f;
+    for (int64_t i = 0; i < H; ++i)
+        if (ring[i] > m) m = ring[i];
+    if (m > 0.0f) {
+        const float fmax_f = (float)decode(f->max_code, *f);
+        const float scaled = std::ldexp(m, margin);     // exact: a power-of-two scaling
+        ring[H] = scaled / fmax_f;
+    }
     return 0;
 }
 
@@ -265,6 +328,39 @@ int or_gemm_i8(const int8_t* A, const int8_t* B, const float* sa, const float* s
     return overflow;
 }
 
+// INT8 GEMM with row-group scales: like or_gemm_i8 but the dequantization
+// uses sa[b*ceil(M/ga) + i/ga] and sb[b*ceil(N/gb) + j/gb].
+int or_gemm_i8_grouped(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                       int64_t ga, int64_t gb, int64_t batch, int64_t M, int64_t N, int64_t K,
+                       const int64_t* rows, int64_t n_rows, int32_t* acc_out, float* c_out) {
+    if (batch < 0 || M < 0 || N < 0 || K < 0 || ga < 1 || gb < 1) return -1;
+    if (!rows) n_rows = M;
+    const int64_t Mg = (M + ga - 1) / ga, Ng = (N + gb - 1) / gb;
+    int overflow = 0;
+    for (int64_t b = 0; b < batch; ++b) {
+#pragma omp parallel for schedule(static) reduction(| : overflow)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            int64_t i = rows ? rows[r] : r;
+            const int8_t* a = A + (b * M + i) * K;
+            for (int64_t j = 0; j < N; ++j) {
+                const int8_t* bb = B + (b * N + j) * K;
+                int64_t acc = 0;
+                for (int64_t k = 0; k < K; ++k) acc += (int64_t)a[k] * (int64_t)bb[k];
+                if (acc > INT32_MAX || acc < INT32_MIN) overflow = 1;
+                int64_t o = (b * n_rows + r) * N + j;
+                if (acc_out) acc_out[o] = (int32_t)acc;
+                if (c_out) {
+                    float c = (float)(int32_t)acc;
+                    c = c * sa[b * Mg + i / ga];
+                    c = c * sb[b * Ng + j / gb];
+                    c_out[o] = c;
+                }
+            }
+        }
+    }
+    return overflow;
+}
+
 // FP8 GEMM reference.  layout 0 = NT: A[M,K], B[N,K], C = A B^T.
 // 1 = NN: A[M,K], B[K,N], C = A B.  2 = TN: A[K,M], B[K,N], C = A^T B.
 // All row-major and packed.  ref_out: [n_rows][N] fp64 sum of decoded
@@ -294,6 +390,41 @@ int or_gemm_fp8(const uint8_t* A, const uint8_t* B, int fmt, int layout,
                 c = c * sa;
                 c = c * sb;
                 bf16_out[r * N + j] = bf16_round(c);
+            }
+        }
+    }
+    return 0;
+}
+
+// FP8 GEMM with an E4M3 output (AstrAI ops/fp8.py, fp8_gemm with out_dtype 1:
+// the output quantized with its own step out_scale, divided out -- the
+// adapter's docstring reading; its CPU path multiplies, the pages disagree).
+// t_out: fp64 reference (sum * sa * sb) / out_scale; codes_out: E4M3 of
+// fl32(fl32(fl32(fl32(sum) * sa) * sb) / out_scale).  Both nullable.
+int or_gemm_fp8_e4m3(const uint8_t* A, const uint8_t* B, int fmt, int layout, int64_t M,
+                     int64_t N, int64_t K, float sa, float sb, float out_scale,
+                     const int64_t* rows, int64_t n_rows, double* t_out, uint8_t* codes_out) {
+    const Fp8* f = fmt_of(fmt);
+    if (!f || layout < 0 || layout > 2 || M < 0 || N < 0 || K < 0) return -1;
+    if (!rows) n_rows = M;
+    double table[256];
+    for (int c = 0; c < 256; ++c) table[c] = decode((uint8_t)c, *f);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        for (int64_t j = 0; j < N; ++j) {
+            double sum = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                uint8_t a = layout == 2 ? A[k * M + i] : A[i * K + k];
+                uint8_t b = layout == 0 ? B[j * K + k] : B[k * N + j];
+                sum += table[a] * table[b];
+            }
+            if (t_out) t_out[r * N + j] = sum * (double)sa * (double)sb / (double)out_scale;
+            if (codes_out) {
+                float c = (float)sum;
+                c = c * sa;
+                c = c * sb;
+                codes_out[r * N + j] = encode(c / out_scale, kE4M3);
             }
         }
     }

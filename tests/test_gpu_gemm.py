@@ -261,3 +261,84 @@ def test_i8_gemm_cta_pair_batched_heads():
     oacc, oC = oracle.gemm_i8(qq, qk, sq_, sk)
     C, acc = run_i8(qq, sq_, qk, sk)
     assert np.array_equal(acc, oacc) and np.array_equal(C, oC)
+
+
+# ------------------------------------------------------------------ E4M3 output
+E4M3_OUT = [
+    ("out8 NT 200x176x320", 200, 176, 320, sq.SQ_NT, sq.SQ_FMT_E4M3),
+    ("out8 NN 256x384x512", 256, 384, 512, sq.SQ_NN, sq.SQ_FMT_E4M3),
+    ("out8 TN 208x160x256", 208, 160, 256, sq.SQ_TN, sq.SQ_FMT_E5M2),
+    ("out8 pair NT 2200x2208x256", 2200, 2208, 256, sq.SQ_NT, sq.SQ_FMT_E4M3),
+]
+
+
+@pytest.mark.parametrize("name,M,N,K,layout,fmt", E4M3_OUT, ids=[c[0] for c in E4M3_OUT])
+def test_fp8_gemm_e4m3_output(name, M, N, K, layout, fmt):
+    """E4M3 codes of (acc*sa*sb)/out_scale: each code lies between the E4M3
+    values bracketing the fp64 reference widened by the GEMM bound, and the
+    output step is chosen so that some outputs saturate."""
+    a8, b8, sa, sb = fp8_inputs(name, M, N, K, fmt)
+    A = a8 if layout != sq.SQ_TN else np.ascontiguousarray(a8.T)
+    B = b8 if layout == sq.SQ_NT else np.ascontiguousarray(b8.T)
+    rows = None if M * N < 1_000_000 else np.unique(np.concatenate(
+        [np.arange(4), np.arange(M - 4, M), np.random.default_rng(9).choice(M, 120, replace=False)]))
+    ref, _ = oracle.gemm_fp8(A, B, fmt, layout, sa, sb, rows=rows, want_bf16=False)
+    out_scale = np.float32(np.abs(ref).max() / 448.0 * 0.8)   # ~2% of outputs saturate
+    t_ref, ocodes = oracle.gemm_fp8_e4m3(A, B, fmt, layout, sa, sb, out_scale, rows=rows)
+    C, cbuf, n = guarded((M, N), torch.uint8, 0xA5)
+    sq.sq_gemm_fp8_scaled_e4m3(to_dev(A), to_dev(B), torch.tensor([sa], device=DEV),
+                               torch.tensor([sb], device=DEV), fmt, layout,
+                               torch.tensor([out_scale], device=DEV), C=C)
+    got = C.cpu().numpy()
+    if rows is not None:
+        got = got[rows]
+    tab = oracle.fp8_decode_table(fmt)
+    bound = oracle.fp8_gemm_bound(ref, K, sa, sb, np.abs(tab[A]).max(), np.abs(tab[B]).max())
+    assert np.all(oracle.e4m3_acceptable(got, t_ref, bound / float(out_scale)))
+    assert np.mean(got == ocodes) > 0.95
+    assert np.any(np.abs(oracle.fp8_decode_table(0)[got]) == 448.0)
+    assert guard_intact(cbuf, n, 0xA5)
+
+
+# ------------------------------------------------------------------ row-group scales
+GROUPED_GEMM = [
+    ("per tensor both 128x512x1024", (128, 1024), (512, 1024), 128, 512),
+    ("groups 8 x 30 ragged 200x300x160", (200, 160), (300, 160), 8, 30),
+    ("pair per tensor A, per row B 2200x2300x256", (2200, 256), (2300, 256), 2200, 1),
+]
+
+
+@pytest.mark.parametrize("name,sa_shape,sb_shape,ga,gb", GROUPED_GEMM, ids=[c[0] for c in GROUPED_GEMM])
+def test_i8_gemm_grouped_scales(name, sa_shape, sb_shape, ga, gb):
+    s = seed_of(name)
+    a, b = synth.normal(s, sa_shape), synth.normal(s + 1, sb_shape)
+    qa, sa = oracle.quantize_grouped_i8(a, ga)
+    qb, sb = oracle.quantize_grouped_i8(b, gb)
+    M = sa_shape[0]
+    rows = None if M < 1000 else np.unique(np.concatenate(
+        [np.arange(4), np.arange(M - 4, M), np.random.default_rng(3).choice(M, 100, replace=False)]))
+    oacc, oC = oracle.gemm_i8_grouped(qa, qb, sa, sb, ga, gb, rows=rows)
+    ws = torch.empty(sq.gemm_i8_workspace_bytes(1, M, sb_shape[0], sa_shape[1]), dtype=torch.uint8,
+                     device=DEV)
+    C, acc = sq.sq_gemm_i8_grouped(to_dev(qa), to_dev(sa), ga, to_dev(qb), to_dev(sb), gb, ws,
+                                   acc_out=True)
+    C, acc = C.cpu().numpy(), acc.cpu().numpy()
+    if rows is not None:
+        C, acc = C[rows], acc[rows]
+    assert np.array_equal(acc, oacc) and np.array_equal(C, oC)
+
+
+def test_i8_gemm_grouped_batched_per_tensor_heads():
+    """Per-head batched product with one scale per head (per_tensor within each
+    head): group sizes equal to the head's row count."""
+    q = synth.normal(81, (16, 196, 64))
+    k = synth.normal(82, (16, 196, 64))
+    qq, sqs = zip(*[oracle.quantize_grouped_i8(np.ascontiguousarray(q[h]), 196) for h in range(16)])
+    qk, sks = zip(*[oracle.quantize_grouped_i8(np.ascontiguousarray(k[h]), 196) for h in range(16)])
+    qq, qk = np.stack(qq), np.stack(qk)
+    sqa, ska = np.concatenate(sqs), np.concatenate(sks)
+    oacc, oC = oracle.gemm_i8_grouped(qq, qk, sqa, ska, 196, 196)
+    ws = torch.empty(sq.gemm_i8_workspace_bytes(16, 196, 196, 64), dtype=torch.uint8, device=DEV)
+    C, acc = sq.sq_gemm_i8_grouped(to_dev(qq), to_dev(sqa), 196, to_dev(qk), to_dev(ska), 196, ws,
+                                   acc_out=True)
+    assert np.array_equal(acc.cpu().numpy(), oacc) and np.array_equal(C.cpu().numpy(), oC)

@@ -187,3 +187,59 @@ def test_fp8_scales_across_the_division_paths(scale):
         assert np.array_equal(x8.cpu().numpy(), ox8)
         assert amax.item() == float(oamax)
         assert np.all(ox8[:64] == 0x80)
+
+
+# ------------------------------------------------------------------ delayed-scaling ring
+@pytest.mark.parametrize("fmt", [sq.SQ_FMT_E4M3, sq.SQ_FMT_E5M2], ids=["e4m3", "e5m2"])
+def test_fp8_ring_sequence_matches_the_oracle(fmt):
+    """Twelve quantize steps through one ring (history 5, rolling index,
+    margins 0 and 1): codes, amax and the whole ring bit-exact every step."""
+    H = 5
+    ring_o = np.zeros(H + 2, dtype=np.float32)
+    ring_o[H] = 0.05
+    ring_d = sq.new_ring(H, 0.05, DEV)
+    ws = sq.new_workspace(DEV)
+    rng = np.random.default_rng(40 + fmt)
+    for step in range(12):
+        std = float(np.exp(rng.uniform(np.log(1e-3), np.log(10.0))))
+        n = int(rng.integers(1, 300_000))
+        x = synth.normal(900 + step, (n,), std=std, dtype=synth.BF16)
+        margin = step % 2
+        ox8, oamax = oracle.quantize_fp8_ring(x, fmt, ring_o, idx=step % H, margin=margin)
+        x8, amax = sq.sq_quantize_fp8_ring(to_dev(x, bf16=True), fmt, ring_d, step % H, margin, ws)
+        assert np.array_equal(x8.cpu().numpy(), ox8), step
+        assert amax.item() == float(oamax)
+        got = ring_d.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), ring_o.view(np.uint32)), (step, got, ring_o)
+    assert int(ws.sum().item()) == 0
+
+
+def test_fp8_ring_zero_history_keeps_the_step():
+    ring = sq.new_ring(4, 0.25, DEV)
+    ws = sq.new_workspace(DEV)
+    z = torch.zeros(10_000, dtype=torch.bfloat16, device=DEV)
+    x8, amax = sq.sq_quantize_fp8_ring(z, sq.SQ_FMT_E4M3, ring, 2, 0, ws)
+    r = ring.cpu().numpy()
+    assert amax.item() == 0.0 and r[4] == np.float32(0.25) and np.all(r[:4] == 0) and r[5] == 0
+
+
+# ------------------------------------------------------------------ row groups / per tensor
+GROUP_CASES = [
+    ("per tensor f32 128x1024", (128, 1024), "f32", 128),
+    ("per tensor bf16 t3 2048x2048", (2048, 2048), "bf16", 10**9),
+    ("groups of 8, ragged last, f32 100x256", (100, 256), "f32", 8),
+    ("groups of 3 bf16 64x4096", (64, 4096), "bf16", 3),
+    ("scalar path groups of 4 f32 37x17", (37, 17), "f32", 4),
+    ("per tensor, one row", (1, 512), "f32", 1),
+]
+
+
+@pytest.mark.parametrize("name,shape,dt,g", GROUP_CASES, ids=[c[0] for c in GROUP_CASES])
+def test_grouped_i8_parity(name, shape, dt, g):
+    seed = zlib.crc32(name.encode()) % 1000 + 300
+    x = draw(seed, shape, dt, "t3" if "t3" in name else "normal")
+    rows = shape[0]
+    oq, osc = oracle.quantize_grouped_i8(x, min(g, rows), oracle.F32 if dt == "f32" else oracle.BF16)
+    q, s = sq.sq_quantize_grouped_i8(to_dev(x, bf16=(dt == "bf16")), g)
+    assert np.array_equal(s.cpu().numpy(), osc)
+    assert np.array_equal(q.cpu().numpy(), oq)

@@ -189,3 +189,48 @@ def test_fp8_row_subset():
     rows = np.array([0, 7, 39])
     part, pb = oracle.gemm_fp8(A, B, 0, oracle.NT, 1.0, 1.0, rows=rows)
     assert np.array_equal(part, full[rows]) and np.array_equal(pb, fb[rows])
+
+
+# ------------------------------------------------------------------ E4M3 output
+def test_fp8_e4m3_output_identity_closed_form():
+    """A = identity (E4M3 1.0), sa = sb = 1: the output codes are B^T's codes
+    scaled by 1/out_scale -- identical for out_scale = 1, one binade down for
+    out_scale = 2 (so a multiply-instead-of-divide slip shows)."""
+    rng = np.random.default_rng(60)
+    K = 48
+    I = np.zeros((K, K), np.uint8)
+    np.fill_diagonal(I, 0x38)
+    tab = oracle.fp8_decode_table(0)
+    # B codes with magnitudes in [2^-5, 2^7] so halving stays exact in E4M3
+    ok = np.array([c for c in range(256) if np.isfinite(tab[c]) and 2 ** -5 <= abs(tab[c]) <= 2 ** 7],
+                  dtype=np.uint8)
+    B = rng.choice(ok, size=(20, K))
+    _, codes1 = oracle.gemm_fp8_e4m3(I, B, 0, oracle.NT, 1.0, 1.0, 1.0)
+    assert np.array_equal(codes1, B.T)
+    t2, codes2 = oracle.gemm_fp8_e4m3(I, B, 0, oracle.NT, 1.0, 1.0, 2.0)
+    assert np.array_equal(tab[codes2], tab[B.T] / 2) and np.array_equal(t2, tab[B.T] / 2)
+
+
+def test_fp8_e4m3_output_saturates_and_brackets():
+    rng = np.random.default_rng(61)
+    A, B = rand_codes(rng, (30, 64), 0), rand_codes(rng, (24, 64), 0)
+    t, codes = oracle.gemm_fp8_e4m3(A, B, 0, oracle.NT, 0.5, 0.25, 1e-3)
+    tab = oracle.fp8_decode_table(0)
+    assert np.all(np.abs(tab[codes][np.abs(t) > 500]) == 448.0)
+    assert np.all(oracle.e4m3_acceptable(codes, t, 1e-9 * np.abs(t) + 1e-30))
+
+
+def test_grouped_gemm_reduces_to_rowscaled_and_broadcasts_group_scales():
+    rng = np.random.default_rng(70)
+    A, B = rand_i8(rng, (2, 20, 64)), rand_i8(rng, (2, 30, 64))
+    sa = np.abs(synth.normal(71, (2, 20))) + np.float32(0.1)
+    sb = np.abs(synth.normal(72, (2, 30))) + np.float32(0.1)
+    acc1, C1 = oracle.gemm_i8(A, B, sa, sb)
+    acc2, C2 = oracle.gemm_i8_grouped(A, B, sa, sb, 1, 1)
+    assert np.array_equal(acc1, acc2) and np.array_equal(C1, C2)
+    # group sizes 8 (A) and 30 (B, per tensor): the same as expanding the scales
+    ga_s = np.abs(synth.normal(73, (2, 3))) + np.float32(0.1)
+    gb_s = np.abs(synth.normal(74, (2, 1))) + np.float32(0.1)
+    _, Cg = oracle.gemm_i8_grouped(A, B, ga_s, gb_s, 8, 30)
+    _, Ce = oracle.gemm_i8(A, B, np.repeat(ga_s, 8, axis=1)[:, :20], np.repeat(gb_s, 30, axis=1))
+    assert np.array_equal(Cg, Ce)

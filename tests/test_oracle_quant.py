@@ -158,3 +158,108 @@ def test_fp8_lossless_when_input_is_code_times_power_of_two(fmt):
         # +0 and -0 both decode to 0; the encoder keeps the sign of the input
         assert np.array_equal(x8, codes)
         assert amax == np.abs(vals).max()
+
+
+# ------------------------------------------------------------------ delayed-scaling ring
+def _ring(H, scale, hist=None):
+    r = np.zeros(H + 2, dtype=np.float32)
+    if hist is not None:
+        r[:H] = hist
+    r[H] = scale
+    return r
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_ring_quantizes_with_the_ring_scale_and_records_amax(fmt):
+    x = synth.normal(120, (300, 64), dtype=synth.BF16)
+    ring = _ring(8, 0.01, hist=[0.5, 0, 0, 0, 0, 0, 0, 0])
+    x8, amax = oracle.quantize_fp8_ring(x, fmt, ring, idx=3)
+    plain8, plain_amax = oracle.quantize_fp8(x, 0.01, fmt)
+    assert np.array_equal(x8, plain8) and amax == plain_amax
+    assert ring[3] == amax and ring[0] == np.float32(0.5)
+    assert np.all(ring[[1, 2, 4, 5, 6, 7]] == 0) and ring[9] == 0   # counter untouched
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_published_step_maps_the_window_max_to_the_largest_code(fmt):
+    """At margin 0 the next step sends the history's max to the largest finite
+    FP8 code, not past it (no saturation of the window max)."""
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        hist = rng.uniform(1e-3, 1e3, size=16).astype(np.float32)
+        ring = _ring(16, 1.0, hist)
+        x = (np.zeros(32, dtype=np.uint16))
+        oracle.quantize_fp8_ring(x, fmt, ring, idx=int(rng.integers(0, 16)), margin=0)
+        m = np.float32(ring[:16].max())
+        code = int(oracle.fp8_encode(np.float32(m) / ring[16], fmt))
+        assert code == (0x7E if fmt == oracle.E4M3 else 0x7B)
+
+
+def test_ring_margin_doubles_the_step_and_follows_the_delayed_recipe():
+    x = synth.normal(121, (512,), std=2.0, dtype=synth.BF16)
+    steps = []
+    for margin in (0, 1, 2, 5):
+        ring = _ring(4, 0.02)
+        oracle.quantize_fp8_ring(x, oracle.E4M3, ring, idx=0, margin=margin)
+        steps.append(ring[4])
+    assert steps[1] == 2 * steps[0] and steps[2] == 4 * steps[0] and steps[3] == 32 * steps[0]
+    # margin 0 with one entry: the previous-amax / 448 recipe of the delayed-scale workload
+    amax = np.abs(synth.bf16_bits_to_f32(x)).max()
+    assert steps[0] == np.float32(amax) / np.float32(448.0)
+
+
+def test_ring_keeps_the_scale_when_the_history_is_zero_and_rolls_the_window():
+    ring = _ring(3, 0.125)
+    oracle.quantize_fp8_ring(np.zeros(64, dtype=np.uint16), oracle.E4M3, ring, idx=1)
+    assert ring[3] == np.float32(0.125) and np.all(ring[:3] == 0)
+    # a large amax leaves the window after H further steps
+    big = synth.normal(122, (64,), std=100.0, dtype=synth.BF16)
+    small = synth.normal(123, (64,), std=0.01, dtype=synth.BF16)
+    oracle.quantize_fp8_ring(big, oracle.E4M3, ring, idx=0)
+    s_big = ring[3]
+    oracle.quantize_fp8_ring(small, oracle.E4M3, ring, idx=1)
+    oracle.quantize_fp8_ring(small, oracle.E4M3, ring, idx=2)
+    assert ring[3] == s_big                 # the big amax is still in the window
+    oracle.quantize_fp8_ring(small, oracle.E4M3, ring, idx=0)
+    assert ring[3] < s_big / 100            # now it has rolled out
+
+
+# ------------------------------------------------------------------ row groups / per tensor
+def test_grouped_with_one_row_per_group_is_per_row():
+    x = synth.normal(130, (37, 96))
+    qg, sg = oracle.quantize_grouped_i8(x, 1)
+    qr, sr = oracle.quantize_rowwise_i8(x)
+    assert np.array_equal(qg, qr) and np.array_equal(sg, sr)
+
+
+def test_per_tensor_follows_the_printed_fake_quant_formula():
+    """The POPCORNBENCH trace's reference model: amax = max|x| clamped at 1e-8,
+    scale = amax / 127, q = clamp(round_half_even(x / scale), -127, 127)."""
+    x = synth.student_t(131, (50, 70), df=3)
+    q, s = oracle.quantize_grouped_i8(x, 50)
+    assert s.shape == (1,)
+    amax = np.float32(max(np.abs(x).max(), np.float32(1e-8)))
+    assert s[0] == amax / np.float32(127.0)
+    t = x / s[0]
+    assert np.array_equal(q, brute_force_int8(t))
+    # only the tensor's absmax element reaches +-127
+    i = np.unravel_index(np.abs(x).argmax(), x.shape)
+    assert abs(int(q[i])) == 127
+
+
+def test_groups_are_independent_and_row_order_inside_a_group_does_not_matter():
+    x = synth.normal(132, (40, 64))
+    x[10:20] *= 50.0                          # group 1 (rows 8..15 with g=8) gets a big row
+    q, s = oracle.quantize_grouped_i8(x, 8)
+    assert s.shape == (5,)
+    for g in range(5):
+        qg, sg = oracle.quantize_grouped_i8(np.ascontiguousarray(x[8 * g:8 * g + 8]), 8)
+        assert sg[0] == s[g] and np.array_equal(qg, q[8 * g:8 * g + 8])
+    perm = np.concatenate([np.random.default_rng(1).permutation(8) + 8 * g for g in range(5)])
+    qp, sp = oracle.quantize_grouped_i8(np.ascontiguousarray(x[perm]), 8)
+    assert np.array_equal(sp, s) and np.array_equal(qp, q[perm])
+    # ragged last group
+    q7, s7 = oracle.quantize_grouped_i8(x, 7)
+    assert s7.shape == (6,)
+    qlast, slast = oracle.quantize_grouped_i8(np.ascontiguousarray(x[35:]), 5)
+    assert slast[0] == s7[5] and np.array_equal(qlast, q7[35:])
