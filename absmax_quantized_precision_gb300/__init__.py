@@ -27,13 +27,16 @@ SQ_OK, SQ_ERR_INVALID_ARG, SQ_ERR_UNSUPPORTED, SQ_ERR_ALIGNMENT, SQ_ERR_CUDA, \
 SQ_F32, SQ_BF16 = 0, 1
 SQ_FMT_E4M3, SQ_FMT_E5M2 = 0, 1
 SQ_NT, SQ_NN, SQ_TN = 0, 1, 2
+SQ_BIAS_NONE, SQ_BIAS_BF16, SQ_BIAS_FP8 = 0, 1, 2
+SQ_GRAD_INPUT, SQ_GRAD_WEIGHT, SQ_GRAD_BIAS = 1, 2, 4
 
 # every symbol include/sq.h declares
 EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "sq_quantize_fp8",
            "sq_gemm_i8_workspace_bytes", "sq_gemm_i8_rowscaled", "sq_gemm_fp8_scaled",
            "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc", "sq_quantize_fp8_ring",
            "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
-           "sq_quantize_grouped_i8", "sq_gemm_i8_grouped")
+           "sq_quantize_grouped_i8", "sq_gemm_i8_grouped", "sq_linear_workspace_bytes",
+           "sq_linear_forward_fp8", "sq_linear_backward_fp8")
 
 # size of the fixed scratch array behind sq_gemm_i8_rowscaled_noalloc
 GEMM_I8_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -88,6 +91,15 @@ def load_library():
     L.sq_gemm_i8_grouped.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
                                      vp, vp, vp, sz, vp]
     L.sq_gemm_i8_grouped.restype = i32
+    L.sq_linear_workspace_bytes.argtypes = [i64, i64, i64]
+    L.sq_linear_workspace_bytes.restype = sz
+    L.sq_linear_forward_fp8.argtypes = [vp, i64, i64, vp, i32, i64, vp, i32, vp, vp, vp, i32,
+                                        vp, i64, i64, i32, vp, i64, i64, i32,
+                                        vp, vp, vp, vp, vp, vp, sz, vp]
+    L.sq_linear_forward_fp8.restype = i32
+    L.sq_linear_backward_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp, vp, i32,
+                                         vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.sq_linear_backward_fp8.restype = i32
     _lib = L
     return L
 
@@ -367,6 +379,82 @@ def sq_gemm_fp8_scaled_e4m3(A: torch.Tensor, B: torch.Tensor, sa: torch.Tensor, 
                                                   _stream(stream)),
            "sq_gemm_fp8_scaled_e4m3")
     return C
+
+
+def linear_workspace(T: int, N: int, K: int, device=None) -> torch.Tensor:
+    """A zeroed workspace for the fused linear forward / backward."""
+    n = int(load_library().sq_linear_workspace_bytes(T, N, K))
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ring_args(ring, idx, margin):
+    if ring is None:
+        return None, 0, 0, 0
+    if ring.dtype != torch.float32 or not ring.is_contiguous() or ring.numel() < 3:
+        raise TypeError("a ring is a contiguous float32 tensor of hist_len + 2 entries")
+    return ring, ring.numel() - 2, int(idx), int(margin)
+
+
+def sq_linear_forward_fp8(x: torch.Tensor, w: torch.Tensor, bias, sx, sw, fmt: int,
+                          workspace: torch.Tensor, bias_scale=None, w_prequantized: bool = False,
+                          x_ring=None, x_ring_idx: int = 0, x_ring_margin: int = 0,
+                          w_ring=None, w_ring_idx: int = 0, w_ring_margin: int = 0, stream=None):
+    """Fused FP8 linear forward.  x bf16 [M, K]; w bf16 [N, K] (or FP8 codes
+    uint8 when w_prequantized); bias None, bf16 [N], or FP8 codes uint8 [N]
+    (with bias_scale).  Returns (out bf16 [M, N], x8, w8, amax_x, amax_w)."""
+    _need_cuda(x, w, workspace)
+    M, K = x.shape
+    N = w.shape[0]
+    if bias is None:
+        bkind = SQ_BIAS_NONE
+    elif bias.dtype == torch.bfloat16:
+        bkind = SQ_BIAS_BF16
+    elif bias.dtype == torch.uint8:
+        bkind = SQ_BIAS_FP8
+    else:
+        raise TypeError("bias must be bf16, FP8 codes (uint8) or None")
+    dev = x.device
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    x8 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    w8 = None if w_prequantized else torch.empty((N, K), dtype=torch.uint8, device=dev)
+    amax_x = torch.empty(1, dtype=torch.float32, device=dev)
+    amax_w = torch.empty(1, dtype=torch.float32, device=dev)
+    xr, xh, xi, xm = _ring_args(x_ring, x_ring_idx, x_ring_margin)
+    wr, wh, wi, wm = _ring_args(w_ring, w_ring_idx, w_ring_margin)
+    _check(load_library().sq_linear_forward_fp8(
+        _ptr(x), M, K, _ptr(w), int(bool(w_prequantized)), N, _ptr(bias), bkind, _ptr(bias_scale),
+        _ptr(sx), _ptr(sw), int(fmt), _ptr(xr), xh, xi, xm, _ptr(wr), wh, wi, wm, _ptr(out),
+        _ptr(x8), _ptr(w8), _ptr(amax_x), _ptr(amax_w), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "sq_linear_forward_fp8")
+    return out, x8, (w if w_prequantized else w8), amax_x, amax_w
+
+
+def sq_linear_backward_fp8(g: torch.Tensor, x: torch.Tensor, w: torch.Tensor, masks, sg, sw, sx,
+                           fmt: int, workspace: torch.Tensor, g_ring=None, g_ring_idx: int = 0,
+                           g_ring_margin: int = 0, stream=None):
+    """Fused FP8 linear backward for out = x w^T.  g bf16 [T, N], x bf16 [T, K],
+    w bf16 [N, K]; masks = (grad_input, grad_weight, grad_bias) booleans.
+    Returns (gx [T, K] or None, gw [N, K] or None, gb [N] or None, amax_g)."""
+    _need_cuda(g, x, w, workspace)
+    T, N = g.shape
+    K = x.shape[1]
+    m = (SQ_GRAD_INPUT if masks[0] else 0) | (SQ_GRAD_WEIGHT if masks[1] else 0) | \
+        (SQ_GRAD_BIAS if masks[2] else 0)
+    dev = g.device
+    gx = torch.empty((T, K), dtype=torch.bfloat16, device=dev) if masks[0] else None
+    gw = torch.empty((N, K), dtype=torch.bfloat16, device=dev) if masks[1] else None
+    gb = torch.empty(N, dtype=torch.bfloat16, device=dev) if masks[2] else None
+    amax_g = torch.empty(1, dtype=torch.float32, device=dev)
+    g8 = torch.empty((T, N), dtype=torch.uint8, device=dev)
+    w8 = torch.empty((N, K), dtype=torch.uint8, device=dev) if masks[0] else None
+    x8 = torch.empty((T, K), dtype=torch.uint8, device=dev) if masks[1] else None
+    gr, gh, gi, gm = _ring_args(g_ring, g_ring_idx, g_ring_margin)
+    _check(load_library().sq_linear_backward_fp8(
+        _ptr(g), _ptr(x), _ptr(w), T, N, K, m, _ptr(sg), _ptr(sw), _ptr(sx), int(fmt), _ptr(gr),
+        gh, gi, gm, _ptr(gx), _ptr(gw), _ptr(gb), _ptr(amax_g), _ptr(g8), _ptr(w8), _ptr(x8),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "sq_linear_backward_fp8")
+    return gx, gw, gb, amax_g
 
 
 def sq_get_last_device_error(stream=None) -> int:

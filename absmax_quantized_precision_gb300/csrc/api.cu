@@ -241,8 +241,8 @@ sq_status gemm_fp8_common(const uint8_t* A, const uint8_t* B, const float* sa, c
     if (!ds) return from_cuda(e);
     return from_cuda(sq::launch_gemm_fp8(A, B, sa, sb, fmt, layout, static_cast<int>(M),
                                          static_cast<int>(N), static_cast<int>(K), C, out_scale,
-                                         ds->err_word, reinterpret_cast<cudaStream_t>(stream),
-                                         ds->sms));
+                                         nullptr, ds->err_word,
+                                         reinterpret_cast<cudaStream_t>(stream), ds->sms));
 }
 
 }  // namespace
@@ -259,6 +259,171 @@ sq_status sq_gemm_fp8_scaled_e4m3(const uint8_t* A, const uint8_t* B, const floa
                                   sq_stream stream) {
     if (!out_scale) return SQ_ERR_INVALID_ARG;
     return gemm_fp8_common(A, B, sa, sb, fmt, layout, M, N, K, C_e4m3, out_scale, stream);
+}
+
+// ---------------------------------------------------------------- linear layer
+namespace {
+
+constexpr int kColsumSplits = 16;
+// workspace: [0, 256) quantize words (amax bits, ticket) and step slots;
+// then the float32 bias (N); then the column-sum slabs (16 x N floats).
+constexpr size_t kLinStepX = 64, kLinStepW = 68, kLinStepG = 72, kLinSinkW = 80, kLinSinkX = 84;
+
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// Quantize one operand: with a ring, the step used (sx, or the ring's slot)
+// is first copied to `used`, because the quantize publishes the next step
+// into the ring's slot when it finishes.  Returns the step pointer that the
+// GEMM must read.
+sq_status quantize_operand(const uint16_t* x, int64_t n, const float* step, int fmt, uint8_t* x8,
+                           float* amax, float* ring, int64_t hist, int64_t idx, int margin,
+                           unsigned* qws, float* used, const float** step_for_gemm,
+                           cudaStream_t st, int sms) {
+    if (!step && !ring) return SQ_ERR_INVALID_ARG;
+    if (ring && (hist < 1 || hist > (int64_t(1) << 20) || idx < 0 || idx >= hist || margin < -64 ||
+                 margin > 64 || (reinterpret_cast<uintptr_t>(ring) & 3u)))
+        return SQ_ERR_INVALID_ARG;
+    const float* s = step;
+    if (!s) {
+        if (cudaMemcpyAsync(used, ring + hist, sizeof(float), cudaMemcpyDeviceToDevice, st) !=
+            cudaSuccess)
+            return SQ_ERR_CUDA;
+        s = used;
+    }
+    *step_for_gemm = s;
+    return from_cuda(sq::launch_quantize_fp8(x, n, s, fmt, x8, amax, qws, ring,
+                                             static_cast<int>(hist), static_cast<int>(idx), margin,
+                                             st, sms));
+}
+
+}  // namespace
+
+size_t sq_linear_workspace_bytes(int64_t T, int64_t N, int64_t K) {
+    (void)T;
+    (void)K;
+    if (N <= 0) return 0;
+    return 256 + align256(static_cast<size_t>(N) * 4) +
+           align256(static_cast<size_t>(kColsumSplits) * N * 4);
+}
+
+sq_status sq_linear_forward_fp8(const uint16_t* x, int64_t M, int64_t K, const void* w,
+                                int w_prequantized, int64_t N, const void* bias, int bias_kind,
+                                const float* bias_scale, const float* sx, const float* sw, int fmt,
+                                float* x_ring, int64_t x_hist, int64_t x_idx, int x_margin,
+                                float* w_ring, int64_t w_hist, int64_t w_idx, int w_margin,
+                                uint16_t* out, uint8_t* x8, uint8_t* w8, float* amax_x,
+                                float* amax_w, void* workspace, size_t workspace_bytes,
+                                sq_stream stream) {
+    if (fmt != SQ_FMT_E4M3 && fmt != SQ_FMT_E5M2) return SQ_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1) return SQ_ERR_INVALID_ARG;
+    if (!x || !w || !out || !x8 || !amax_x || !amax_w || !workspace) return SQ_ERR_INVALID_ARG;
+    if (!w_prequantized && !w8) return SQ_ERR_INVALID_ARG;
+    if (bias_kind != SQ_BIAS_NONE && bias_kind != SQ_BIAS_BF16 && bias_kind != SQ_BIAS_FP8)
+        return SQ_ERR_INVALID_ARG;
+    if (bias_kind != SQ_BIAS_NONE && !bias) return SQ_ERR_INVALID_ARG;
+    if (bias_kind == SQ_BIAS_FP8 && !bias_scale) return SQ_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || !aligned16(x8) || !aligned16(w8) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SQ_ERR_ALIGNMENT;
+    if (workspace_bytes < sq_linear_workspace_bytes(M, N, K)) return SQ_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    unsigned* qws = reinterpret_cast<unsigned*>(wsb);
+    float* bias32 = reinterpret_cast<float*>(wsb + 256);
+    const float* sx_g = nullptr;
+    const float* sw_g = nullptr;
+    sq_status r = quantize_operand(x, M * K, sx, fmt, x8, amax_x, x_ring, x_hist, x_idx, x_margin, qws,
+                                   reinterpret_cast<float*>(wsb + kLinStepX), &sx_g, st, ds->sms);
+    if (r != SQ_OK) return r;
+    const uint8_t* wq = w8;
+    if (w_prequantized) {
+        wq = static_cast<const uint8_t*>(w);
+        if (!sw) return SQ_ERR_INVALID_ARG;
+        sw_g = sw;
+        if (cudaMemsetAsync(amax_w, 0, sizeof(float), st) != cudaSuccess) return SQ_ERR_CUDA;
+    } else {
+        r = quantize_operand(static_cast<const uint16_t*>(w), N * K, sw, fmt, w8, amax_w, w_ring,
+                             w_hist, w_idx, w_margin, qws,
+                             reinterpret_cast<float*>(wsb + kLinStepW), &sw_g, st, ds->sms);
+        if (r != SQ_OK) return r;
+    }
+    const float* bias_f = nullptr;
+    if (bias_kind != SQ_BIAS_NONE) {
+        e = sq::launch_bias_to_f32(bias, bias_kind, fmt, bias_scale, N, bias32, st);
+        if (e != cudaSuccess) return SQ_ERR_CUDA;
+        bias_f = bias32;
+    }
+    return from_cuda(sq::launch_gemm_fp8(x8, wq, sx_g, sw_g, fmt, SQ_NT, static_cast<int>(M),
+                                         static_cast<int>(N), static_cast<int>(K), out, nullptr,
+                                         bias_f, ds->err_word, st, ds->sms));
+}
+
+sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uint16_t* w,
+                                 int64_t T, int64_t N, int64_t K, int masks, const float* sg,
+                                 const float* sw, const float* sx, int fmt, float* g_ring,
+                                 int64_t g_hist, int64_t g_idx, int g_margin, uint16_t* gx,
+                                 uint16_t* gw, uint16_t* gb, float* amax_g, uint8_t* g8,
+                                 uint8_t* w8, uint8_t* x8, void* workspace, size_t workspace_bytes,
+                                 sq_stream stream) {
+    const bool want_gx = masks & SQ_GRAD_INPUT, want_gw = masks & SQ_GRAD_WEIGHT,
+               want_gb = masks & SQ_GRAD_BIAS;
+    if (fmt != SQ_FMT_E4M3 && fmt != SQ_FMT_E5M2) return SQ_ERR_INVALID_ARG;
+    if (T < 1 || N < 1 || K < 1 || (masks & ~7)) return SQ_ERR_INVALID_ARG;
+    if (!g || !amax_g || !g8 || !workspace) return SQ_ERR_INVALID_ARG;
+    if (want_gx && (!w || !sw || !w8 || !gx)) return SQ_ERR_INVALID_ARG;
+    if (want_gw && (!x || !sx || !x8 || !gw)) return SQ_ERR_INVALID_ARG;
+    if (want_gb && !gb) return SQ_ERR_INVALID_ARG;
+    if (T > kMaxDim || N > kMaxDim || K > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    if (N % 16 != 0 || K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (!aligned16(g) || !aligned16(x) || !aligned16(w) || !aligned16(gx) || !aligned16(gw) ||
+        !aligned16(g8) || !aligned16(w8) || !aligned16(x8) ||
+        (reinterpret_cast<uintptr_t>(gb) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SQ_ERR_ALIGNMENT;
+    if (workspace_bytes < sq_linear_workspace_bytes(T, N, K)) return SQ_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    unsigned* qws = reinterpret_cast<unsigned*>(wsb);
+    float* partial = reinterpret_cast<float*>(wsb + 256 + align256(static_cast<size_t>(N) * 4));
+    // one quantization of the gradient, shared by both products
+    const float* sg_g = nullptr;
+    sq_status r = quantize_operand(g, T * N, sg, fmt, g8, amax_g, g_ring, g_hist, g_idx, g_margin,
+                                   qws, reinterpret_cast<float*>(wsb + kLinStepG), &sg_g, st,
+                                   ds->sms);
+    if (r != SQ_OK) return r;
+    if (want_gx) {
+        e = sq::launch_quantize_fp8(w, N * K, sw, fmt, w8, reinterpret_cast<float*>(wsb + kLinSinkW),
+                                    qws, nullptr, 0, 0, 0, st, ds->sms);
+        if (e != cudaSuccess) return SQ_ERR_CUDA;
+        // dX[T,K] = G[T,N] W[N,K]  (NN)
+        e = sq::launch_gemm_fp8(g8, w8, sg_g, sw, fmt, SQ_NN, static_cast<int>(T),
+                                static_cast<int>(K), static_cast<int>(N), gx, nullptr, nullptr,
+                                ds->err_word, st, ds->sms);
+        if (e != cudaSuccess) return SQ_ERR_CUDA;
+    }
+    if (want_gw) {
+        e = sq::launch_quantize_fp8(x, T * K, sx, fmt, x8, reinterpret_cast<float*>(wsb + kLinSinkX),
+                                    qws, nullptr, 0, 0, 0, st, ds->sms);
+        if (e != cudaSuccess) return SQ_ERR_CUDA;
+        // dW[N,K] = G^T[N,T] X[T,K]  (TN, G stored [T,N])
+        e = sq::launch_gemm_fp8(g8, x8, sg_g, sx, fmt, SQ_TN, static_cast<int>(N),
+                                static_cast<int>(K), static_cast<int>(T), gw, nullptr, nullptr,
+                                ds->err_word, st, ds->sms);
+        if (e != cudaSuccess) return SQ_ERR_CUDA;
+    }
+    if (want_gb) {
+        const int splits = T < kColsumSplits ? static_cast<int>(T) : kColsumSplits;
+        e = sq::launch_colsum_bf16(g, T, N, splits, partial, gb, st);
+        if (e != cudaSuccess) return SQ_ERR_CUDA;
+    }
+    return SQ_OK;
 }
 
 namespace {

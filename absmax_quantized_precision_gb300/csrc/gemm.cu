@@ -62,6 +62,7 @@ struct GemmParams {
     int ga, gb;             // INT8: rows per scale group of A and B (1 = per row)
     int Mg, Ng;             // INT8: scale groups per batch, ceil(M/ga), ceil(N/gb)
     int sb_vec;             // INT8: sB may be read 4 floats at a time
+    const float* bias;      // FP8: float32 bias per output column, added after scaling (nullable)
 };
 
 // PAIR = false: one CTA per SM computes 128 x BN tiles (cta_group::1).
@@ -445,6 +446,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                     tmem_ld32(tb + c * 32, r);
                     tmem_ld_wait();
                     const int col0 = n0 + c * 32;
+                    if (p.bias && row < p.M) {
+                        // bias fused into the epilogue: fl32(fl32(acc*sa)*sb) + bias[col]
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int col = col0 + i;
+                            const float bj = col < p.N ? p.bias[col] : 0.0f;
+                            r[i] = __float_as_uint(__fadd_rn(
+                                __fmul_rn(__fmul_rn(__uint_as_float(r[i]), fsa), fsb), bj));
+                        }
+                    }
+                    const float esa = p.bias ? 1.0f : fsa;   // scaling already applied above
+                    const float esb = p.bias ? 1.0f : fsb;
                     if (row < p.M && p.out_e4m3) {
                         // E4M3 output: code = e4m3(fl32(fl32(acc*sa)*sb) / out_scale)
                         uint8_t* C8 = static_cast<uint8_t*>(p.C);
@@ -454,7 +467,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                             float v[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float w = __fmul_rn(__fmul_rn(__uint_as_float(r[4 * i + e]), fsa), fsb);
+                                const float w = __fmul_rn(__fmul_rn(__uint_as_float(r[4 * i + e]), esa), esb);
                                 v[e] = ofast ? fp8_quotient(w, fos, foy) : __fdiv_rn(w, fos);
                             }
                             pk[i] = fp8x2<0>(v[0], v[1]) | (fp8x2<0>(v[2], v[3]) << 16);
@@ -472,8 +485,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float lo = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), fsa), fsb);
-                            const float hi = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), fsa), fsb);
+                            const float lo = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), esa), esb);
+                            const float hi = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), esa), esb);
                             pk[i] = bf16_bits(lo) | (bf16_bits(hi) << 16);
                         }
                         if (p.vec_store && col0 + 32 <= p.N) {
@@ -655,8 +668,10 @@ static cudaError_t gemm_fp8_layout(const uint8_t* A, const uint8_t* B, int M, in
 
 cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                             int fmt, int layout, int M, int N, int K, void* C,
-                            const float* out_scale, unsigned* err_word, cudaStream_t st, int sms) {
+                            const float* out_scale, const float* bias, unsigned* err_word,
+                            cudaStream_t st, int sms) {
     GemmParams p{};
+    p.bias = bias;
     p.M = M; p.N = N; p.K = K; p.batch = 1;
     p.nkb = (K + kBKBytes - 1) / kBKBytes;
     p.kb_per_chunk = p.nkb;

@@ -377,7 +377,8 @@ __device__ __forceinline__ uint4 fp8_encode16(const uint4& a, const uint4& b, fl
 //
 // Plain mode (ring == nullptr): the step is *scale; ws = [amax bits | ticket].
 // Ring mode: delayed scaling with ring = [hist (hist_len) | scale | counter]
-// (the AstrAI commit notes' scale ring): the step is ring[hist_len], the
+// (the AstrAI commit notes' scale ring): the step is *scale if given, else
+// ring[hist_len], the
 // ticket counter is the ring's last word, and the last block records the amax
 // in hist[ring_idx], takes the max over the window and publishes the next
 // step fl32(fl32(max * 2^margin) / fmt_max) in ring[hist_len] (kept as it was
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restri
     __shared__ float red[8];
     __shared__ int is_last;
     __shared__ float s_amax;
-    const float s = ring ? ring[hist_len] : *scale;
+    const float s = scale ? *scale : ring[hist_len];
     unsigned* counter = ring ? reinterpret_cast<unsigned*>(ring + hist_len + 1) : ws + 1;
     const float y = __frcp_rn(s);
     const bool fast = s >= 0x1p-40f && s <= 0x1p40f;

@@ -33,7 +33,17 @@ cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int
 // output step *out_scale divided out.
 cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                             int fmt, int layout, int M, int N, int K, void* C,
-                            const float* out_scale, unsigned* err_word, cudaStream_t st, int sms);
+                            const float* out_scale, const float* bias, unsigned* err_word,
+                            cudaStream_t st, int sms);
+
+// Linear-layer helpers (linear.cu).
+// bias kind 1: bf16 [n] widened; kind 2: FP8 codes of fmt times *step.
+cudaError_t launch_bias_to_f32(const void* bias, int kind, int fmt, const float* step, int64_t n,
+                               float* out, cudaStream_t st);
+// gb[j] = bf16(sum_t g[t*N + j]): fp32 partial sums over `splits` row slabs in
+// `partial` (splits * N floats), then a fixed-order sum of the slabs.
+cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, int splits,
+                               float* partial, uint16_t* gb, cudaStream_t st);
 
 // Scales of row i of A in batch b: sA[b*ceil(M/ga) + i/ga] (ga = 1: per row).
 cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,

@@ -69,6 +69,12 @@ typedef enum { SQ_FMT_E4M3 = 0, SQ_FMT_E5M2 = 1 } sq_fp8_fmt;
  *   SQ_TN: A[K,M], B[K,N], C = A^T * B   (dW = G^T * X)                        */
 typedef enum { SQ_NT = 0, SQ_NN = 1, SQ_TN = 2 } sq_layout;
 
+/* Bias of the fused linear forward. */
+typedef enum { SQ_BIAS_NONE = 0, SQ_BIAS_BF16 = 1, SQ_BIAS_FP8 = 2 } sq_bias_kind;
+
+/* Gradients the fused linear backward computes (bit mask, [P3] masks). */
+typedef enum { SQ_GRAD_INPUT = 1, SQ_GRAD_WEIGHT = 2, SQ_GRAD_BIAS = 4 } sq_grad_mask;
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* sq_status_string(sq_status s);
 
@@ -239,6 +245,70 @@ sq_status sq_gemm_fp8_scaled_e4m3(const uint8_t* A, const uint8_t* B, const floa
                                   const float* sb, int fmt, int layout, int64_t M, int64_t N,
                                   int64_t K, const float* out_scale, uint8_t* C_e4m3,
                                   sq_stream stream);
+
+/*
+ * Workspace of the fused linear forward / backward: 256 bytes of quantize and
+ * step words, the float32 bias (N), and 16 x N floats of column-sum slabs.
+ * Zero it once (cudaMemset); the calls leave the words they rely on zeroed.
+ */
+size_t sq_linear_workspace_bytes(int64_t T, int64_t N, int64_t K);
+
+/*
+ * Fused FP8 linear forward  [P3 linear_forward_fp8: quantize x and w, FP8
+ * GEMM with the bias fused in the epilogue, return (out, x8, w8, amax_x,
+ * amax_w); optional rings finish the delayed scaling in the quantize kernels;
+ * static weights and bias may arrive pre-quantized].
+ *
+ *   x8  = enc(x / sx);  w8 = enc(w / sw)  (or w8 = w when w_prequantized)
+ *   out[i,j] = bf16(fl32(fl32(fl32(acc[i,j] * sx) * sw) + bias[j]))
+ *
+ *   x        bf16 [M, K];  w  bf16 [N, K], or FP8 codes [N, K] when
+ *            w_prequantized != 0 (then w8 is not written and *amax_w = 0).
+ *   bias     nullable per bias_kind: SQ_BIAS_BF16 = bf16 [N]; SQ_BIAS_FP8 =
+ *            FP8 codes [N] of fmt, value code * *bias_scale.
+ *   sx, sw   device steps; either may be NULL when its ring is given, and
+ *            the ring's step slot is then used.
+ *   x_ring, w_ring  nullable delayed-scaling rings as in sq_quantize_fp8_ring
+ *            (hist, idx, margin alike); the step the quantization used is the
+ *            one the GEMM uses, even though the ring publishes the next step.
+ *   out      bf16 [M, N];  x8 [M, K];  w8 [N, K];  amax_x, amax_w device floats.
+ *   workspace  sq_linear_workspace_bytes(M, N, K) bytes, 256-B aligned,
+ *            zeroed once.
+ * Limits: K a multiple of 16; pointers 16-byte aligned.
+ */
+sq_status sq_linear_forward_fp8(const uint16_t* x, int64_t M, int64_t K, const void* w,
+                                int w_prequantized, int64_t N, const void* bias, int bias_kind,
+                                const float* bias_scale, const float* sx, const float* sw, int fmt,
+                                float* x_ring, int64_t x_hist, int64_t x_idx, int x_margin,
+                                float* w_ring, int64_t w_hist, int64_t w_idx, int w_margin,
+                                uint16_t* out, uint8_t* x8, uint8_t* w8, float* amax_x,
+                                float* amax_w, void* workspace, size_t workspace_bytes,
+                                sq_stream stream);
+
+/*
+ * Fused FP8 linear backward  [P3 linear_backward_fp8: the gradient is
+ * quantized once (default E5M2 on the page) and feeds both FP8 products; w and
+ * x are quantized to the same fmt; returns (gx, gw, gb, amax_g); masks select
+ * the gradients].  For out = x w^T with x [T, K], w [N, K], g = dout [T, N]:
+ *
+ *   gx = g8 w8  (NN, [T, K]),  gw = g8^T x8  (TN, [N, K]),
+ *   gb[j] = bf16(sum_t g[t, j]) (float32 sums over 16 row slabs, added in a
+ *   fixed order),  each product scaled and rounded as sq_gemm_fp8_scaled.
+ *
+ *   masks    SQ_GRAD_INPUT | SQ_GRAD_WEIGHT | SQ_GRAD_BIAS.
+ *   sg, sw, sx  device steps (sg may be NULL when g_ring is given).
+ *   g8 [T,N], w8 [N,K], x8 [T,K]  caller buffers for the quantized operands
+ *            (w8 / x8 needed only for the gradients that use them).
+ *   amax_g   device float.  workspace as for the forward.
+ * Limits: N and K multiples of 16; pointers 16-byte aligned (gb 4-byte).
+ */
+sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uint16_t* w,
+                                 int64_t T, int64_t N, int64_t K, int masks, const float* sg,
+                                 const float* sw, const float* sx, int fmt, float* g_ring,
+                                 int64_t g_hist, int64_t g_idx, int g_margin, uint16_t* gx,
+                                 uint16_t* gw, uint16_t* gb, float* amax_g, uint8_t* g8,
+                                 uint8_t* w8, uint8_t* x8, void* workspace, size_t workspace_bytes,
+                                 sq_stream stream);
 
 /*
  * Reads and clears the device-side error word of the current device after

@@ -77,6 +77,13 @@ def _load():
             L.or_gemm_i8_grouped.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64,
                                              vp, vp]
             L.or_gemm_i8_grouped.restype = i32
+            L.or_gemm_fp8_bias.argtypes = [vp, vp, i32, i32, i64, i64, i64, f32, f32, vp, vp, i64,
+                                           vp, vp]
+            L.or_gemm_fp8_bias.restype = i32
+            L.or_fp8_bias_to_f32.argtypes = [vp, i64, i32, f32, vp]
+            L.or_fp8_bias_to_f32.restype = i32
+            L.or_colsum_bf16.argtypes = [vp, i64, i64, vp]
+            L.or_colsum_bf16.restype = i32
             L.or_num_threads.argtypes = []
             L.or_num_threads.restype = i32
             _lib = L
@@ -327,6 +334,48 @@ def e4m3_acceptable(codes, t_ref, slack):
     hi_rep = vals[np.clip(np.searchsorted(vals, hi, side="left"), 0, vals.size - 1)]
     got = tab[codes]
     return (got >= lo_rep) & (got <= hi_rep)
+
+
+def gemm_fp8_bias(A8, B8, fmt: int, layout: int, sa: float, sb: float, bias_f32=None, rows=None):
+    """FP8 GEMM plus a float32 bias per output column.  Returns (ref, bf16 bits)."""
+    A8 = _c(A8, np.uint8)
+    B8 = _c(B8, np.uint8)
+    if layout == NT:
+        (M, K), N = A8.shape, B8.shape[0]
+    elif layout == NN:
+        (M, K), N = A8.shape, B8.shape[1]
+    elif layout == TN:
+        (K, M), N = A8.shape, B8.shape[1]
+    else:
+        raise ValueError("layout must be NT, NN or TN")
+    bias = None if bias_f32 is None else _c(np.asarray(bias_f32, dtype=np.float32), np.float32)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = M if r is None else r.size
+    ref = np.empty((nr, N), dtype=np.float64)
+    bf = np.empty((nr, N), dtype=np.uint16)
+    if _load().or_gemm_fp8_bias(_ptr(A8), _ptr(B8), int(fmt), int(layout), M, N, K,
+                                float(np.float32(sa)), float(np.float32(sb)), _ptr(bias), _ptr(r),
+                                nr, _ptr(ref), _ptr(bf)) != 0:
+        raise ValueError("bad arguments")
+    return ref, bf
+
+
+def fp8_bias_to_f32(codes, fmt: int, step: float) -> np.ndarray:
+    codes = _c(np.asarray(codes, dtype=np.uint8), np.uint8)
+    out = np.empty(codes.shape, dtype=np.float32)
+    if _load().or_fp8_bias_to_f32(_ptr(codes), codes.size, int(fmt), float(np.float32(step)),
+                                  _ptr(out)) != 0:
+        raise ValueError("bad arguments")
+    return out
+
+
+def colsum_bf16(g_bf16: np.ndarray) -> np.ndarray:
+    g = _c(g_bf16, np.uint16)
+    T, N = g.shape
+    out = np.empty(N, dtype=np.float64)
+    if _load().or_colsum_bf16(_ptr(g), T, N, _ptr(out)) != 0:
+        raise ValueError("bad arguments")
+    return out
 
 
 def fp8_gemm_bound(ref: np.ndarray, K: int, sa: float, sb: float, maxa8: float, maxb8: float):

@@ -431,6 +431,62 @@ int or_gemm_fp8_e4m3(const uint8_t* A, const uint8_t* B, int fmt, int layout, in
     return 0;
 }
 
+// FP8 GEMM with the bias added in the epilogue (AstrAI ops/fp8.py,
+// linear_forward_fp8: the bias is fused into the GEMM epilogue).  bias_f32 is
+// the bias already in float32 (nullable): a bf16 bias widened exactly, or a
+// pre-quantized FP8 bias decoded and multiplied by its step (fl32).
+// ref_out: fp64 sum * sa * sb + bias; bf16_out: RNE(fl32(fl32(fl32(fl32(sum) *
+// sa) * sb) + bias)).
+int or_gemm_fp8_bias(const uint8_t* A, const uint8_t* B, int fmt, int layout, int64_t M,
+                     int64_t N, int64_t K, float sa, float sb, const float* bias_f32,
+                     const int64_t* rows, int64_t n_rows, double* ref_out, uint16_t* bf16_out) {
+    const Fp8* f = fmt_of(fmt);
+    if (!f || layout < 0 || layout > 2 || M < 0 || N < 0 || K < 0) return -1;
+    if (!rows) n_rows = M;
+    double table[256];
+    for (int c = 0; c < 256; ++c) table[c] = decode((uint8_t)c, *f);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        for (int64_t j = 0; j < N; ++j) {
+            double sum = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                uint8_t a = layout == 2 ? A[k * M + i] : A[i * K + k];
+                uint8_t b = layout == 0 ? B[j * K + k] : B[k * N + j];
+                sum += table[a] * table[b];
+            }
+            const float bj = bias_f32 ? bias_f32[j] : 0.0f;
+            if (ref_out) ref_out[r * N + j] = sum * (double)sa * (double)sb + (double)bj;
+            if (bf16_out) {
+                float c = (float)sum;
+                c = c * sa;
+                c = c * sb;
+                c = c + bj;
+                bf16_out[r * N + j] = bf16_round(c);
+            }
+        }
+    }
+    return 0;
+}
+
+// Decoded FP8 bias: out[j] = fl32(decode(code[j]) * step).
+int or_fp8_bias_to_f32(const uint8_t* codes, int64_t n, int fmt, float step, float* out) {
+    const Fp8* f = fmt_of(fmt);
+    if (!f || n < 0) return -1;
+    for (int64_t j = 0; j < n; ++j) out[j] = (float)decode(codes[j], *f) * step;
+    return 0;
+}
+
+// Column sums of a bf16 [T, N] matrix in fp64 (the gradient of a bias that
+// is broadcast over the T rows).
+int or_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, double* out) {
+    if (T < 0 || N < 0) return -1;
+    for (int64_t j = 0; j < N; ++j) out[j] = 0.0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t j = 0; j < N; ++j) out[j] += (double)bf16_widen(g[t * N + j]);
+    return 0;
+}
+
 int or_num_threads(void) {
     int n = 1;
 #pragma omp parallel

@@ -234,3 +234,29 @@ def test_grouped_gemm_reduces_to_rowscaled_and_broadcasts_group_scales():
     _, Cg = oracle.gemm_i8_grouped(A, B, ga_s, gb_s, 8, 30)
     _, Ce = oracle.gemm_i8(A, B, np.repeat(ga_s, 8, axis=1)[:, :20], np.repeat(gb_s, 30, axis=1))
     assert np.array_equal(Cg, Ce)
+
+
+# ------------------------------------------------------------------ linear layer pieces
+def test_gemm_bias_adds_the_bias_after_scaling():
+    rng = np.random.default_rng(80)
+    A, B = rand_codes(rng, (17, 64), 0), rand_codes(rng, (23, 64), 0)
+    bias = synth.normal(81, (23,), std=3.0)
+    ref0, bf0 = oracle.gemm_fp8(A, B, 0, oracle.NT, 0.3, 0.7)
+    ref1, bf1 = oracle.gemm_fp8_bias(A, B, 0, oracle.NT, 0.3, 0.7, bias)
+    assert np.allclose(ref1 - ref0, bias[None, :].astype(np.float64), rtol=0, atol=1e-12)
+    refn, bfn = oracle.gemm_fp8_bias(A, B, 0, oracle.NT, 0.3, 0.7, None)
+    assert np.array_equal(refn, ref0) and np.array_equal(bfn, bf0)
+
+
+def test_fp8_bias_decode_is_code_times_step():
+    tab = oracle.fp8_decode_table(1)
+    codes = np.array([0x00, 0x3C, 0xBC, 0x7B, 0x01], dtype=np.uint8)
+    out = oracle.fp8_bias_to_f32(codes, 1, 0.5)
+    assert list(out) == [0.0, 0.5, -0.5, 57344.0 * 0.5, 2.0 ** -16 * 0.5]
+    assert np.array_equal(out, (tab[codes] * 0.5).astype(np.float32))
+
+
+def test_colsum_matches_numpy():
+    g = synth.normal(82, (300, 40), dtype=synth.BF16)
+    want = synth.bf16_bits_to_f32(g).astype(np.float64).sum(axis=0)
+    assert np.allclose(oracle.colsum_bf16(g), want, rtol=1e-15, atol=1e-15)
