@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--size", type=int, nargs=3, metavar=("M", "N", "K"),
                     help="override the workload sizes (small cases for profiler captures)")
     ap.add_argument("--config", default="large",
-                    choices=["large", "int8_per_row", "int8_per_head", "fp8_fwd", "fp8_bwd", "all"],
+                    choices=["large", "int8_per_row", "int8_per_head", "fp8_fwd", "fp8_bwd", "all",
+                             "fp8_linear", "large_next", "cublaslt", "extra"],
                     help="the pages' other workloads are measured with their own JSON line")
     args = ap.parse_args()
     if args.size:
@@ -433,6 +434,7 @@ def run_sq(args, rank, world, local_rank):
 
 # ---------------------------------------------------------------- the other workloads
 SMALL_CONFIGS = ["int8_per_row", "int8_per_head", "fp8_fwd", "fp8_bwd"]
+EXTRA_CONFIGS = ["fp8_linear", "large_next", "cublaslt"]
 
 
 def run_small_config(name, args):
@@ -494,6 +496,8 @@ def run_small_config(name, args):
         oqb, osb = oracle.quantize_rowwise_i8(b)
         oracle.gemm_i8(oqa, oqb, osa, osb)
         cpu = time.perf_counter() - t0
+    elif name in EXTRA_CONFIGS:
+        desc, ops, gemm_flops, cpu = extra_config_ops(name, dev, bf16_dev, prev_scale)
     else:
         fmt = sq.SQ_FMT_E4M3
         wsq = sq.new_workspace(dev)
@@ -604,7 +608,8 @@ def run_small_config(name, args):
         else:
             tf = amount / (ms * 1e-3) / 1e12
             d["TFLOP/s"] = tf
-            d["frac_peak"] = tf / ((2.0 if "fp8" in label else 1.0) * pk["bf16_sustained"])
+            is_fp8 = "fp8" in label or label.startswith(("ours_", "cublaslt_", "linear_"))
+            d["frac_peak"] = tf / ((2.0 if is_fp8 else 1.0) * pk["bf16_sustained"])
         kernels[label] = d
     line = {"metric": METRIC, "config": {"workload": name, "desc": desc,
                                          "l2": "flushed before every pass"},
@@ -612,12 +617,136 @@ def run_small_config(name, args):
             "us_per_step_graph": 1e3 * graph_ms,
             "us_per_step_eager": 1e3 * step_ms,
             "value_eager": gemm_flops / (step_ms * 1e-3) / 1e12,
-            "launches_per_step": sum(3 if lbl == "gemm_i8" else 1 for lbl, _, _, _ in ops),
+            "calls_per_step": len(ops),
             "iters": iters, "kernels_eager": kernels,
             "clocks": clk.summary(),
-            "cpu_oracle": {"seconds": cpu, "cores": oracle.num_threads(),
-                           "sample": "the whole workload"}}
+            "cpu_oracle": None if cpu is None else {"seconds": cpu, "cores": oracle.num_threads(),
+                                                     "sample": "the whole workload"}}
     print(json.dumps(line), flush=True)
+
+
+def extra_config_ops(name, dev, bf16_dev, prev_scale):
+    """Workloads of the widened path: the fused FP8 linear layer, the large-size
+    ring / E4M3-output / per-tensor INT8 variants, and cuBLASLt's FP8 GEMM
+    (torch._scaled_mm, a library call) beside ours at the same shapes."""
+    import numpy as np
+    import torch
+
+    import absmax_quantized_precision_gb300 as sq
+    import oracle
+    import synth
+
+    if name == "fp8_linear":
+        M, K, N = 2048, 1024, 1024            # forward: X W^T + b
+        T, Hd, D = 2048, 4096, 1024           # backward of the MLP up-projection
+        x = bf16_dev(synth.normal(301, (M, K), dtype=synth.BF16))
+        w = bf16_dev(synth.normal(302, (N, K), std=0.02, dtype=synth.BF16))
+        b = bf16_dev(synth.normal(303, (N,), std=0.5, dtype=synth.BF16))
+        g = bf16_dev(synth.normal(304, (T, Hd), std=1e-3, dtype=synth.BF16))
+        wb = bf16_dev(synth.normal(305, (Hd, D), std=0.02, dtype=synth.BF16))
+        xb = bf16_dev(synth.normal(306, (T, D), dtype=synth.BF16))
+        xr = sq.new_ring(16, float(prev_scale(307, (M, K), 1.0)), dev)
+        wr = sq.new_ring(16, float(prev_scale(308, (N, K), 0.02)), dev)
+        gr = sq.new_ring(16, float(prev_scale(309, (T, Hd), 1e-3, 57344.0)), dev)
+        sw_b = torch.tensor([prev_scale(310, (Hd, D), 0.02, 57344.0)], device=dev)
+        sx_b = torch.tensor([prev_scale(311, (T, D), 1.0, 57344.0)], device=dev)
+        wsf = sq.linear_workspace(M, N, K, dev)
+        wsb = sq.linear_workspace(T, Hd, D, dev)
+        fwd_flops = 2.0 * M * N * K
+        bwd_flops = 2 * (2.0 * T * Hd * D)
+        ops = [("linear_forward_e4m3_rings_bias", "flops", fwd_flops,
+                lambda: sq.sq_linear_forward_fp8(x, w, b, None, None, sq.SQ_FMT_E4M3, wsf,
+                                                 x_ring=xr, w_ring=wr)),
+               ("linear_backward_e5m2_ring", "flops", bwd_flops,
+                lambda: sq.sq_linear_backward_fp8(g, xb, wb, (True, True, True), None, sw_b, sx_b,
+                                                  sq.SQ_FMT_E5M2, wsb, g_ring=gr))]
+        desc = ("fused FP8 linear: forward X bf16 2048x1024, W 1024x1024, bf16 bias, E4M3 with "
+                "delayed-scaling rings; backward of the 1024->4096 projection over 2048 tokens, "
+                "E5M2 gradient with a ring, dX + dW + bias gradient")
+        return desc, ops, fwd_flops + bwd_flops, None
+
+    if name == "large_next":
+        M, N, K = 16384, 8192, 8192
+        a = synth.student_t(SEED_A, (M, K), df=3, dtype=synth.BF16)
+        b = synth.student_t(SEED_B, (N, K), df=3, dtype=synth.BF16)
+        A, B = bf16_dev(a), bf16_dev(b)
+        sa_v = float(np.float32(np.abs(synth.bf16_bits_to_f32(a)).max()) / np.float32(448.0))
+        ring = sq.new_ring(16, sa_v, dev)
+        ws = sq.new_workspace(dev)
+        a8 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        b8 = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        amax = torch.empty(1, device=dev)
+        tsb = torch.tensor([sa_v], device=dev)
+        out_scale = torch.tensor([2.0], device=dev)
+        C8 = torch.empty((M, N), dtype=torch.uint8, device=dev)
+        qa = torch.empty((M, K), dtype=torch.int8, device=dev)
+        qb = torch.empty((N, K), dtype=torch.int8, device=dev)
+        sqa, sqb = torch.empty(1, device=dev), torch.empty(1, device=dev)
+        wga = torch.empty(sq.load_library().sq_quantize_grouped_i8_workspace_bytes(M, M),
+                          dtype=torch.uint8, device=dev)
+        wgb = torch.empty(sq.load_library().sq_quantize_grouped_i8_workspace_bytes(N, N),
+                          dtype=torch.uint8, device=dev)
+        wsi = torch.empty(sq.gemm_i8_workspace_bytes(1, M, N, K), dtype=torch.uint8, device=dev)
+        Ci = torch.empty((M, N), device=dev)
+        ops = [("quant_fp8_ring_A", "bytes", M * K * 3,
+                lambda: sq.sq_quantize_fp8_ring(A, sq.SQ_FMT_E4M3, ring, 0, 0, ws, x8=a8, amax=amax)),
+               ("quant_fp8_B", "bytes", N * K * 3,
+                lambda: sq.sq_quantize_fp8(B, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax)),
+               ("gemm_fp8_nt_e4m3_out", "flops", 2.0 * M * N * K,
+                lambda: sq.sq_gemm_fp8_scaled_e4m3(a8, b8, tsb, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT,
+                                                   out_scale, C=C8)),
+               ("quant_i8_per_tensor_A", "bytes", M * K * 3,
+                lambda: sq.sq_quantize_grouped_i8(A, M, q=qa, scales=sqa, workspace=wga)),
+               ("quant_i8_per_tensor_B", "bytes", N * K * 3,
+                lambda: sq.sq_quantize_grouped_i8(B, N, q=qb, scales=sqb, workspace=wgb)),
+               ("gemm_i8_per_tensor", "flops", 2.0 * M * N * K,
+                lambda: sq.sq_gemm_i8_grouped(qa, sqa, M, qb, sqb, N, wsi, C=Ci))]
+        desc = ("large M=16384 N=8192 K=8192 bf16 Student-t(3): FP8 quantize with a ring, FP8 GEMM "
+                "with E4M3 output; per-tensor INT8 quantize (two passes) and GEMM")
+        return desc, ops, 2 * (2.0 * M * N * K), None
+
+    # cuBLASLt FP8 GEMMs (torch._scaled_mm) beside ours on the same codes and steps
+    ops = []
+    total = 0.0
+    shapes = [("fwd_nt_2048x1024x1024", 2048, 1024, 1024, sq.SQ_NT),
+              ("dx_nn_2048x1024x4096", 2048, 1024, 4096, sq.SQ_NN),
+              ("dw_tn_4096x1024x2048", 4096, 1024, 2048, sq.SQ_TN),
+              ("large_nt_16384x8192x8192", 16384, 8192, 8192, sq.SQ_NT)]
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    for i, (lbl, M, N, K, layout) in enumerate(shapes):
+        rng = np.random.default_rng(400 + i)
+        ok = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+        if layout == sq.SQ_TN:
+            A = torch.from_numpy(rng.choice(ok, (K, M))).to(dev)        # stored [K, M]
+        else:
+            A = torch.from_numpy(rng.choice(ok, (M, K))).to(dev)
+        if layout == sq.SQ_NT:
+            B = torch.from_numpy(rng.choice(ok, (N, K))).to(dev)
+        else:
+            B = torch.from_numpy(rng.choice(ok, (K, N))).to(dev)        # stored [K, N]
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        sa = torch.tensor([0.01], device=dev)
+        fl = 2.0 * M * N * K
+        total += fl
+        ops.append((f"ours_{lbl}", "flops", fl,
+                    (lambda A=A, B=B, sa=sa, C=C, layout=layout:
+                     sq.sq_gemm_fp8_scaled(A, B, sa, sa, sq.SQ_FMT_E4M3, layout, C=C))))
+        # cuBLASLt wants mat1 row-major [M,K] and mat2 column-major [K,N]: the
+        # transposed copies it needs for NN / TN are made here, outside the timing
+        a_l = (A if layout != sq.SQ_TN else A.t().contiguous()).view(torch.float8_e4m3fn)
+        b_l = (B.view(torch.float8_e4m3fn).t() if layout == sq.SQ_NT
+               else B.t().contiguous().view(torch.float8_e4m3fn).t())
+        try:
+            torch._scaled_mm(a_l, b_l, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            ops.append((f"cublaslt_{lbl}", "flops", fl,
+                        (lambda a_l=a_l, b_l=b_l: torch._scaled_mm(
+                            a_l, b_l, scale_a=one, scale_b=one, out_dtype=torch.bfloat16))))
+        except Exception as e:   # comparator not available in this torch build
+            print(json.dumps({"cublaslt_unavailable": str(e)[:200]}), flush=True)
+    desc = ("FP8 E4M3 GEMMs, bf16 out, ours vs cuBLASLt torch._scaled_mm on the same codes "
+            "(its output comes from torch's caching allocator; the transposed operand copies "
+            "it needs for NN/TN are made before timing)")
+    return desc, ops, total, None
 
 
 def main():
@@ -626,7 +755,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.config != "large" and args.impl == "sq":
-        for name in (SMALL_CONFIGS if args.config == "all" else [args.config]):
+        names = {"all": SMALL_CONFIGS, "extra": EXTRA_CONFIGS}.get(args.config, [args.config])
+        for name in names:
             run_small_config(name, args)
         return
     if args.impl == "reference":
