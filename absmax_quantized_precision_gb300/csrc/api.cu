@@ -5,7 +5,7 @@
 
 #include <mutex>
 
-#include "../../include/sq.h"
+#include "sq.h"
 #include "sq_launch.h"
 
 // Device error word of this library, one per device.

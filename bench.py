@@ -49,7 +49,7 @@ def parse():
                     help="override the workload sizes (small cases for profiler captures)")
     ap.add_argument("--config", default="large",
                     choices=["large", "int8_per_row", "int8_per_head", "fp8_fwd", "fp8_bwd", "all",
-                             "fp8_linear", "large_next", "cublaslt", "extra"],
+                             "fp8_linear", "large_next", "cublaslt", "extra", "legacy_mma"],
                     help="the pages' other workloads are measured with their own JSON line")
     args = ap.parse_args()
     if args.size:
@@ -66,8 +66,8 @@ def parse():
 # those sources no longer matches, the bench reports traffic as null.
 PROFILED_TRAFFIC = {
     # profiles/traffic_large_step.md
-    "gemm_fp8_nt": {"bytes": 720160512, "sources_sha256": "1ad5ba9b2098993e888b520d3f6efbc864bea21a336be088f06bbcf0742b1dba"},
-    "gemm_i8": {"bytes": 3498969600, "sources_sha256": "1ad5ba9b2098993e888b520d3f6efbc864bea21a336be088f06bbcf0742b1dba"},
+    "gemm_fp8_nt": {"bytes": 771890176, "sources_sha256": "9f650c4356fa36957ad664350a19dcbabfe26d5547b01231086727396856b5db"},
+    "gemm_i8": {"bytes": 3516778752, "sources_sha256": "9f650c4356fa36957ad664350a19dcbabfe26d5547b01231086727396856b5db"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
@@ -749,11 +749,31 @@ def extra_config_ops(name, dev, bf16_dev, prev_scale):
     return desc, ops, total, None
 
 
+def run_legacy_mma_probe():
+    """Builds and runs probes/legacy_mma_rate.cu: the register-only rate of the
+    warp-level int8 and f16 mma.sync instructions on this GPU."""
+    import tempfile
+    src = os.path.join(ROOT, "absmax_quantized_precision_gb300", "probes", "legacy_mma_rate.cu")
+    exe = os.path.join(tempfile.mkdtemp(), "legacy_mma_rate")
+    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", src,
+                           "-o", exe])
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr)
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    line.update({"config": {"workload": "legacy_mma", "desc": "register-only mma.sync "
+                            "m16n8k32 s8 and m16n8k16 f16, 4 CTAs x 256 threads per SM"}})
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.config == "legacy_mma":
+        run_legacy_mma_probe()
+        return
     if args.config != "large" and args.impl == "sq":
         names = {"all": SMALL_CONFIGS, "extra": EXTRA_CONFIGS}.get(args.config, [args.config])
         for name in names:
