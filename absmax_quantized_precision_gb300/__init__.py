@@ -36,7 +36,7 @@ EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "
            "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc", "sq_quantize_fp8_ring",
            "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
            "sq_quantize_grouped_i8", "sq_gemm_i8_grouped", "sq_linear_workspace_bytes",
-           "sq_linear_forward_fp8", "sq_linear_backward_fp8")
+           "sq_linear_forward_fp8", "sq_linear_backward_fp8", "sq_selftest_bounded_wait")
 
 # size of the fixed scratch array behind sq_gemm_i8_rowscaled_noalloc
 GEMM_I8_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -100,6 +100,8 @@ def load_library():
     L.sq_linear_backward_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp, vp, i32,
                                          vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.sq_linear_backward_fp8.restype = i32
+    L.sq_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp]
+    L.sq_selftest_bounded_wait.restype = i32
     _lib = L
     return L
 
@@ -455,6 +457,12 @@ def sq_linear_backward_fp8(g: torch.Tensor, x: torch.Tensor, w: torch.Tensor, ma
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
         "sq_linear_backward_fp8")
     return gx, gw, gb, amax_g
+
+
+def sq_selftest_bounded_wait(limit_ns: int, stream=None):
+    """Launch the bounded-wait self-test kernel (see include/sq.h)."""
+    _check(load_library().sq_selftest_bounded_wait(int(limit_ns), _stream(stream)),
+           "sq_selftest_bounded_wait")
 
 
 def sq_get_last_device_error(stream=None) -> int:

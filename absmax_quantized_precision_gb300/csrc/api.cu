@@ -474,6 +474,15 @@ sq_status sq_gemm_i8_rowscaled_noalloc(const int8_t* A, const float* sA, const i
                                 acc_out, na.scratch, SQ_GEMM_I8_NOALLOC_SCRATCH_BYTES, stream);
 }
 
+sq_status sq_selftest_bounded_wait(uint64_t limit_ns, sq_stream stream) {
+    if (limit_ns == 0 || limit_ns > 2000000000ull) return SQ_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    return from_cuda(sq::launch_selftest_wait(ds->err_word, limit_ns,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 sq_status sq_get_last_device_error(sq_stream stream) {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return SQ_ERR_CUDA;

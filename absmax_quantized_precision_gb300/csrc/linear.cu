@@ -76,4 +76,24 @@ cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, int spli
     return cudaGetLastError();
 }
 
+// Self-test of the bounded waits: one CTA waits for a barrier phase that
+// nothing completes; the wait gives up after limit_ns, records the timeout in
+// the device error word and the kernel returns normally.
+__global__ void selftest_wait_kernel(unsigned* err_word, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_for(&bar, 0, &abort_flag, err_word, limit_ns);
+}
+
+cudaError_t launch_selftest_wait(unsigned* err_word, unsigned long long limit_ns, cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>(err_word, limit_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace sq

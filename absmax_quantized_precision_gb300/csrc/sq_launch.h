@@ -51,4 +51,7 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
                            int64_t strideC, float* C, int32_t* acc_out, unsigned* err_word,
                            cudaStream_t st, int sms);
 
+// One CTA waits on a barrier phase that never completes, for limit_ns.
+cudaError_t launch_selftest_wait(unsigned* err_word, unsigned long long limit_ns, cudaStream_t st);
+
 }  // namespace sq

@@ -311,6 +311,16 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
                                  sq_stream stream);
 
 /*
+ * Self-test of the failure path every kernel with waits takes: launches one
+ * CTA that waits on a barrier phase nothing completes; after limit_ns
+ * (1 .. 2e9) the wait gives up, the kernel records SQ_ERR_DEVICE_TIMEOUT in
+ * the device error word and returns normally (no trap, the context stays
+ * usable).  sq_get_last_device_error() then reports and clears it.  The
+ * GEMM kernels' waits behave the same way with a 2 s limit.
+ */
+sq_status sq_selftest_bounded_wait(uint64_t limit_ns, sq_stream stream);
+
+/*
  * Reads and clears the device-side error word of the current device after
  * synchronising `stream`.  Returns SQ_ERR_DEVICE_TIMEOUT if a kernel gave up
  * on a bounded wait since the last call, SQ_ERR_CUDA on a runtime error,
