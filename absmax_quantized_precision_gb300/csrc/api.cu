@@ -86,6 +86,7 @@ sq_status sq_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t
     const int64_t esz = dtype == SQ_F32 ? 4 : 2;
     const bool vec_ok = aligned16(x) && aligned16(q) && ((ld * esz) % 16 == 0) && (cols % 16 == 0);
     return from_cuda(sq::launch_quantize_rowwise_i8(x, dtype, rows, cols, ld, q, scales, vec_ok,
+                                                    ds->err_word,
                                                     reinterpret_cast<cudaStream_t>(stream), ds->sms));
 }
 
@@ -100,7 +101,8 @@ sq_status sq_quantize_fp8(const uint16_t* x_bf16, int64_t numel, const float* sc
     if (!ds) return from_cuda(e);
     return from_cuda(sq::launch_quantize_fp8(x_bf16, numel, scale, fmt, x8, amax,
                                              static_cast<unsigned*>(workspace), nullptr, 0, 0, 0,
-                                             reinterpret_cast<cudaStream_t>(stream), ds->sms));
+                                             ds->err_word, reinterpret_cast<cudaStream_t>(stream),
+                                             ds->sms));
 }
 
 sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, uint8_t* x8,
@@ -121,8 +123,8 @@ sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, u
     return from_cuda(sq::launch_quantize_fp8(x_bf16, numel, nullptr, fmt, x8, amax,
                                              static_cast<unsigned*>(workspace), ring,
                                              static_cast<int>(hist_len), static_cast<int>(idx),
-                                             margin, reinterpret_cast<cudaStream_t>(stream),
-                                             ds->sms));
+                                             margin, ds->err_word,
+                                             reinterpret_cast<cudaStream_t>(stream), ds->sms));
 }
 
 size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K) {
@@ -161,9 +163,9 @@ sq_status gemm_i8_common(const int8_t* A, const float* sA, int64_t ga, const int
     uint16_t* A16 = static_cast<uint16_t*>(workspace);
     const size_t abytes = (static_cast<size_t>(batch) * M * K * 2 + 255) & ~static_cast<size_t>(255);
     uint16_t* B16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + abytes);
-    e = sq::launch_i8_to_f16(A, batch, M, K, strideA, A16, st, ds->sms);
+    e = sq::launch_i8_to_f16(A, batch, M, K, strideA, A16, ds->err_word, st, ds->sms);
     if (e != cudaSuccess) return SQ_ERR_CUDA;
-    e = sq::launch_i8_to_f16(B, batch, N, K, strideB, B16, st, ds->sms);
+    e = sq::launch_i8_to_f16(B, batch, N, K, strideB, B16, ds->err_word, st, ds->sms);
     if (e != cudaSuccess) return SQ_ERR_CUDA;
     return from_cuda(sq::launch_gemm_i8(A16, B16, sA, sB, static_cast<int>(ga),
                                         static_cast<int>(gb), static_cast<int>(batch),
@@ -278,7 +280,7 @@ size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 sq_status quantize_operand(const uint16_t* x, int64_t n, const float* step, int fmt, uint8_t* x8,
                            float* amax, float* ring, int64_t hist, int64_t idx, int margin,
                            unsigned* qws, float* used, const float** step_for_gemm,
-                           cudaStream_t st, int sms) {
+                           unsigned* err_word, cudaStream_t st, int sms) {
     if (!step && !ring) return SQ_ERR_INVALID_ARG;
     if (ring && (hist < 1 || hist > (int64_t(1) << 20) || idx < 0 || idx >= hist || margin < -64 ||
                  margin > 64 || (reinterpret_cast<uintptr_t>(ring) & 3u)))
@@ -293,7 +295,7 @@ sq_status quantize_operand(const uint16_t* x, int64_t n, const float* step, int 
     *step_for_gemm = s;
     return from_cuda(sq::launch_quantize_fp8(x, n, s, fmt, x8, amax, qws, ring,
                                              static_cast<int>(hist), static_cast<int>(idx), margin,
-                                             st, sms));
+                                             err_word, st, sms));
 }
 
 }  // namespace
@@ -338,7 +340,7 @@ sq_status sq_linear_forward_fp8(const uint16_t* x, int64_t M, int64_t K, const v
     const float* sx_g = nullptr;
     const float* sw_g = nullptr;
     sq_status r = quantize_operand(x, M * K, sx, fmt, x8, amax_x, x_ring, x_hist, x_idx, x_margin, qws,
-                                   reinterpret_cast<float*>(wsb + kLinStepX), &sx_g, st, ds->sms);
+                                   reinterpret_cast<float*>(wsb + kLinStepX), &sx_g, ds->err_word, st, ds->sms);
     if (r != SQ_OK) return r;
     const uint8_t* wq = w8;
     if (w_prequantized) {
@@ -349,7 +351,8 @@ sq_status sq_linear_forward_fp8(const uint16_t* x, int64_t M, int64_t K, const v
     } else {
         r = quantize_operand(static_cast<const uint16_t*>(w), N * K, sw, fmt, w8, amax_w, w_ring,
                              w_hist, w_idx, w_margin, qws,
-                             reinterpret_cast<float*>(wsb + kLinStepW), &sw_g, st, ds->sms);
+                             reinterpret_cast<float*>(wsb + kLinStepW), &sw_g, ds->err_word, st,
+                             ds->sms);
         if (r != SQ_OK) return r;
     }
     const float* bias_f = nullptr;
@@ -395,12 +398,12 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
     // one quantization of the gradient, shared by both products
     const float* sg_g = nullptr;
     sq_status r = quantize_operand(g, T * N, sg, fmt, g8, amax_g, g_ring, g_hist, g_idx, g_margin,
-                                   qws, reinterpret_cast<float*>(wsb + kLinStepG), &sg_g, st,
-                                   ds->sms);
+                                   qws, reinterpret_cast<float*>(wsb + kLinStepG), &sg_g,
+                                   ds->err_word, st, ds->sms);
     if (r != SQ_OK) return r;
     if (want_gx) {
         e = sq::launch_quantize_fp8(w, N * K, sw, fmt, w8, reinterpret_cast<float*>(wsb + kLinSinkW),
-                                    qws, nullptr, 0, 0, 0, st, ds->sms);
+                                    qws, nullptr, 0, 0, 0, ds->err_word, st, ds->sms);
         if (e != cudaSuccess) return SQ_ERR_CUDA;
         // dX[T,K] = G[T,N] W[N,K]  (NN)
         e = sq::launch_gemm_fp8(g8, w8, sg_g, sw, fmt, SQ_NN, static_cast<int>(T),
@@ -410,7 +413,7 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
     }
     if (want_gw) {
         e = sq::launch_quantize_fp8(x, T * K, sx, fmt, x8, reinterpret_cast<float*>(wsb + kLinSinkX),
-                                    qws, nullptr, 0, 0, 0, st, ds->sms);
+                                    qws, nullptr, 0, 0, 0, ds->err_word, st, ds->sms);
         if (e != cudaSuccess) return SQ_ERR_CUDA;
         // dW[N,K] = G^T[N,T] X[T,K]  (TN, G stored [T,N])
         e = sq::launch_gemm_fp8(g8, x8, sg_g, sx, fmt, SQ_TN, static_cast<int>(N),

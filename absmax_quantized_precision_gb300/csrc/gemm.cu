@@ -764,10 +764,121 @@ __global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict
     }
 }
 
+// Contiguous source (batch stride == rows*K): a bulk-copy pipeline as in the
+// quantize kernels -- 8 KB int8 chunks in through a 4-stage ring, 16 KB fp16
+// chunks out through two buffers; each thread converts two 8-byte pieces
+// (conflict-free shared-memory access).  The ragged tail (a multiple of 16
+// codes, below one chunk) is done by block 0 with vector loads.
+constexpr int kStgChunk = 8192;       // codes per chunk
+constexpr int kStgStages = 4;
+constexpr int kStgThreads = 512;
+constexpr int kStgSmem = kStgStages * kStgChunk + 2 * kStgChunk * 2 + kStgStages * 8 + 128;
+
+__device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 w) {
+    const uint32_t in[2] = {w.x, w.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int8_t c0 = static_cast<int8_t>((in[i] >> (16 * h)) & 0xFF);
+            const int8_t c1 = static_cast<int8_t>((in[i] >> (16 * h + 8)) & 0xFF);
+            o[2 * i + h] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(c0))) |
+                           (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(c1))) << 16);
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(kStgThreads) i8_to_f16_bulk_kernel(const int8_t* __restrict__ src,
+                                                                    int64_t n,
+                                                                    uint16_t* __restrict__ dst,
+                                                                    unsigned* err_word) {
+    extern __shared__ uint8_t gsmem_raw[];
+    uint8_t* gsmem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(gsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    uint8_t* in_buf = gsmem;                                     // 4 x 8 KB
+    uint8_t* out_buf = in_buf + kStgStages * kStgChunk;          // 2 x 16 KB
+    uint64_t* full = reinterpret_cast<uint64_t*>(out_buf + 2 * kStgChunk * 2);
+    __shared__ int s_ok;
+    __shared__ int abort_flag;
+    const int64_t nfull = n / kStgChunk;
+    const int64_t G = gridDim.x;
+    const int64_t count = blockIdx.x < nfull ? (nfull - blockIdx.x + G - 1) / G : 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStgStages; ++i) mbar_init(&full[i], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        for (int64_t i = 0; i < count && i < kStgStages; ++i) {
+            mbar_arrive_expect_tx(&full[i], kStgChunk);
+            bulk_load(in_buf + i * kStgChunk, src + (blockIdx.x + i * G) * kStgChunk, kStgChunk, &full[i]);
+        }
+    }
+    __syncthreads();
+    int64_t i = 0;
+    for (; i < count; ++i) {
+        const int stage = static_cast<int>(i % kStgStages);
+        const int ob = static_cast<int>(i & 1);
+        if (threadIdx.x == 0) {
+            s_ok = mbar_wait(&full[stage], static_cast<uint32_t>((i / kStgStages) & 1), &abort_flag, err_word);
+            if (i >= 2) bulk_wait_read<1>();
+        }
+        __syncthreads();
+        if (!s_ok) break;
+        const uint8_t* in = in_buf + stage * kStgChunk;
+        uint8_t* out = out_buf + ob * kStgChunk * 2;
+        const int t = threadIdx.x;
+        const uint2 w0 = *reinterpret_cast<const uint2*>(in + t * 8);
+        const uint2 w1 = *reinterpret_cast<const uint2*>(in + kStgChunk / 2 + t * 8);
+        *reinterpret_cast<uint4*>(out + t * 16) = i8x8_to_f16x8(w0);
+        *reinterpret_cast<uint4*>(out + kStgChunk + t * 16) = i8x8_to_f16x8(w1);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int64_t c = blockIdx.x + i * G;
+            bulk_store(dst + c * kStgChunk, out, kStgChunk * 2);
+            bulk_commit();
+            if (i + kStgStages < count) {
+                mbar_arrive_expect_tx(&full[stage], kStgChunk);
+                bulk_load(in_buf + stage * kStgChunk, src + (c + kStgStages * G) * kStgChunk, kStgChunk,
+                          &full[stage]);
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (i < count) {
+            for (int64_t j = i; j < count && j < i + kStgStages; ++j)
+                mbar_wait_drain(&full[j % kStgStages], static_cast<uint32_t>((j / kStgStages) & 1));
+        }
+        bulk_wait_all();
+    }
+    if (blockIdx.x == 0) {
+        for (int64_t e = nfull * kStgChunk + threadIdx.x * 8; e < n; e += kStgThreads * 8) {
+            const uint2 w = *reinterpret_cast<const uint2*>(src + e);
+            *reinterpret_cast<uint4*>(dst + e) = i8x8_to_f16x8(w);
+        }
+    }
+}
+
 cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
-                             int64_t stride, uint16_t* dst, cudaStream_t st, int sms) {
+                             int64_t stride, uint16_t* dst, unsigned* err_word, cudaStream_t st,
+                             int sms) {
     const int64_t total = batch * rows * (K / 16);
     if (total == 0) return cudaSuccess;
+    const int64_t n = batch * rows * K;
+    if (err_word && (stride == rows * K || batch == 1) && n >= static_cast<int64_t>(kStgChunk) * sms) {
+        static cudaError_t attr = cudaFuncSetAttribute(i8_to_f16_bulk_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       kStgSmem);
+        if (attr != cudaSuccess) return attr;
+        int64_t blocks = n / kStgChunk;
+        const int64_t cap = static_cast<int64_t>(sms) * 2;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        i8_to_f16_bulk_kernel<<<static_cast<unsigned>(blocks), kStgThreads, kStgSmem, st>>>(src, n, dst,
+                                                                                         err_word);
+        return cudaGetLastError();
+    }
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;

@@ -22,6 +22,12 @@
 
 namespace sq {
 
+// Streaming kernels: persistent CTAs of kQThreads threads with a kQStages-deep
+// ring of shared-memory stages filled by bulk copies.
+constexpr int kQChunk = 8192;                       // FP8 path: bf16 per chunk, 16 KB in, 8 KB out
+constexpr int kQStages = 4;
+constexpr int kQThreads = 512;
+
 // ================================================================== INT8 rows
 template <typename T>
 struct Elem;
@@ -91,17 +97,19 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
          row0 += static_cast<int64_t>(gridDim.x) * RPB) {
         const int64_t row = row0 + g;
         const bool live = row < rows;
-        float v[VPT][EPV];
-        float m = 0.0f;
+        uint4 raw[VPT];                 // the row stays packed: 4 registers per 16 bytes
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
-            if (live && vi < nvec) {
-                uint4 raw = ld_stream_v4(x + row * ld + vi * EPV);
-                Elem<T>::unpack(raw, v[i]);
+            raw[i] = (live && vi < nvec) ? ld_stream_v4(x + row * ld + vi * EPV) : make_uint4(0, 0, 0, 0);
+        }
+        float m = 0.0f;
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf(v[i][e]));
-            }
+        for (int i = 0; i < VPT; ++i) {
+            float v[EPV];
+            Elem<T>::unpack(raw[i], v);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf(v[e]));
         }
         if (TPR <= 32) {
 #pragma unroll
@@ -125,14 +133,16 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
             for (int i = 0; i < VPT; ++i) {
                 const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
                 if (vi < nvec) {
+                    float v[EPV];
+                    Elem<T>::unpack(raw[i], v);
                     uint32_t packed[EPV / 4];
 #pragma unroll
                     for (int w = 0; w < EPV / 4; ++w) {
                         uint32_t b[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            b[e] = static_cast<uint8_t>(fast ? encode_i8_recip(v[i][4 * w + e], s, y)
-                                                             : encode_i8(v[i][4 * w + e], s));
+                            b[e] = static_cast<uint8_t>(fast ? encode_i8_recip(v[4 * w + e], s, y)
+                                                             : encode_i8(v[4 * w + e], s));
                         packed[w] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
                     }
                     int8_t* dst = q + row * cols + vi * EPV;
@@ -188,9 +198,11 @@ static cudaError_t launch_row_vec(const T* x, int64_t rows, int64_t cols, int64_
 
 template <typename T>
 static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
-                              float* scales, bool vec_ok, cudaStream_t st, int sms) {
+                              float* scales, bool vec_ok, unsigned* err_word, cudaStream_t st,
+                              int sms) {
     constexpr int EPV = Elem<T>::kPerVec;
     const int64_t nvec = cols / EPV;
+    (void)err_word;
     if (vec_ok) {
         if (nvec <= 16) return launch_row_vec<T, 16, 1>(x, rows, cols, ld, q, scales, st, sms);
         if (nvec <= 32) return launch_row_vec<T, 32, 1>(x, rows, cols, ld, q, scales, st, sms);
@@ -211,12 +223,12 @@ static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld
 
 cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols,
                                        int64_t ld, int8_t* q, float* scales, bool vec_ok,
-                                       cudaStream_t st, int sms) {
+                                       unsigned* err_word, cudaStream_t st, int sms) {
     if (dtype == 0)
         return launch_row<float>(static_cast<const float*>(x), rows, cols, ld, q, scales, vec_ok,
-                                 st, sms);
+                                 err_word, st, sms);
     return launch_row<uint16_t>(static_cast<const uint16_t*>(x), rows, cols, ld, q, scales, vec_ok,
-                                st, sms);
+                                err_word, st, sms);
 }
 
 // ================================================================== INT8 row groups
@@ -339,7 +351,8 @@ cudaError_t launch_quantize_grouped_i8(const void* x, int dtype, int64_t rows, i
                                        int64_t ld, int64_t group_rows, int8_t* q, float* scales,
                                        unsigned* ws, bool vec_ok, cudaStream_t st, int sms) {
     if (group_rows == 1)
-        return launch_quantize_rowwise_i8(x, dtype, rows, cols, ld, q, scales, vec_ok, st, sms);
+        return launch_quantize_rowwise_i8(x, dtype, rows, cols, ld, q, scales, vec_ok, nullptr, st,
+                                          sms);
     if (dtype == 0)
         return launch_grouped<float>(static_cast<const float*>(x), rows, cols, ld, group_rows, q,
                                      scales, ws, vec_ok, st, sms);
@@ -373,60 +386,139 @@ __device__ __forceinline__ uint4 fp8_encode16(const uint4& a, const uint4& b, fl
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Each thread converts 32 elements per step (four 16-B loads in flight).
+// 8 bf16 (one 16-B word) -> 8 FP8 codes (one 8-B word); m = running max|x|.
+template <int FMT, bool FAST>
+__device__ __forceinline__ uint2 fp8_encode8(const uint4& a, float s, float y, float& m) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t o[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float f[4];
+        f[0] = __uint_as_float(w[2 * i] << 16);
+        f[1] = __uint_as_float(w[2 * i] & 0xFFFF0000u);
+        f[2] = __uint_as_float(w[2 * i + 1] << 16);
+        f[3] = __uint_as_float(w[2 * i + 1] & 0xFFFF0000u);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) t[e] = FAST ? fp8_quotient(f[e], s, y) : __fdiv_rn(f[e], s);
+        o[i] = fp8x2<FMT>(t[0], t[1]) | (fp8x2<FMT>(t[2], t[3]) << 16);
+    }
+    return make_uint2(o[0], o[1]);
+}
+
+// Streaming pipeline: persistent CTAs of kQThreads threads; one thread moves
+// 16 KB input chunks into a ring of kQStages shared-memory stages with bulk
+// copies (cp.async.bulk) and writes each chunk's 8 KB of codes back with a
+// bulk store from one of two output buffers; every thread converts 16
+// elements per chunk from shared memory (two contiguous 16-B pieces, no bank
+// conflicts).  The ragged tail (< one chunk) is done by block 0 with plain
+// loads and stores.
 //
 // Plain mode (ring == nullptr): the step is *scale; ws = [amax bits | ticket].
 // Ring mode: delayed scaling with ring = [hist (hist_len) | scale | counter]
 // (the AstrAI commit notes' scale ring): the step is *scale if given, else
-// ring[hist_len], the
-// ticket counter is the ring's last word, and the last block records the amax
-// in hist[ring_idx], takes the max over the window and publishes the next
-// step fl32(fl32(max * 2^margin) / fmt_max) in ring[hist_len] (kept as it was
-// when the window max is 0) -- no extra launch.  ws[0] still accumulates the
-// amax bits.  Both modes leave their counter and ws[0] at zero.
+// ring[hist_len], the ticket counter is the ring's last word, and the last
+// block records the amax in hist[ring_idx], takes the max over the window and
+// publishes the next step fl32(fl32(max * 2^margin) / fmt_max) in
+// ring[hist_len] (kept as it was when the window max is 0) -- no extra
+// launch.  ws[0] still accumulates the amax bits.  Both modes leave their
+// counter and ws[0] at zero.
+constexpr int kQSmem = kQStages * kQChunk * 2 + 2 * kQChunk + kQStages * 8 + 128;
+
 template <int FMT>
-__global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restrict__ x, int64_t n,
-                                                        const float* __restrict__ scale,
-                                                        uint8_t* __restrict__ x8,
-                                                        float* __restrict__ amax_out,
-                                                        unsigned* __restrict__ ws, float* ring,
-                                                        int hist_len, int ring_idx, int margin) {
-    __shared__ float red[8];
+__global__ void __launch_bounds__(kQThreads) quant_fp8_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                              const float* __restrict__ scale,
+                                                              uint8_t* __restrict__ x8,
+                                                              float* __restrict__ amax_out,
+                                                              unsigned* __restrict__ ws, float* ring,
+                                                              int hist_len, int ring_idx, int margin,
+                                                              unsigned* err_word) {
+    extern __shared__ uint8_t qsmem_raw[];
+    uint8_t* qsmem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(qsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    uint8_t* in_buf = qsmem;                                   // kQStages x 16 KB
+    uint8_t* out_buf = in_buf + kQStages * kQChunk * 2;        // 2 x 8 KB
+    uint64_t* full = reinterpret_cast<uint64_t*>(out_buf + 2 * kQChunk);
+    __shared__ float red[kQThreads / 32];
     __shared__ int is_last;
     __shared__ float s_amax;
+    __shared__ int s_ok;
+    __shared__ int abort_flag;
+
     const float s = scale ? *scale : ring[hist_len];
     unsigned* counter = ring ? reinterpret_cast<unsigned*>(ring + hist_len + 1) : ws + 1;
     const float y = __frcp_rn(s);
     const bool fast = s >= 0x1p-40f && s <= 0x1p40f;
     float m = 0.0f;
-    const int64_t nchunk = n / 32;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t c = tid; c < nchunk; c += nthr) {
-        const uint16_t* src = x + c * 32;
-        uint4 a0 = ld_stream_v4(src);
-        uint4 a1 = ld_stream_v4(src + 8);
-        uint4 a2 = ld_stream_v4(src + 16);
-        uint4 a3 = ld_stream_v4(src + 24);
-        uint4 o0, o1;
-        if (fast) {
-            o0 = fp8_encode16<FMT, true>(a0, a1, s, y, m);
-            o1 = fp8_encode16<FMT, true>(a2, a3, s, y, m);
-        } else {
-            o0 = fp8_encode16<FMT, false>(a0, a1, s, y, m);
-            o1 = fp8_encode16<FMT, false>(a2, a3, s, y, m);
+
+    const int64_t nfull = n / kQChunk;
+    const int64_t G = gridDim.x;
+    const int64_t count = blockIdx.x < nfull ? (nfull - blockIdx.x + G - 1) / G : 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kQStages; ++i) mbar_init(&full[i], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        for (int64_t i = 0; i < count && i < kQStages; ++i) {
+            mbar_arrive_expect_tx(&full[i], kQChunk * 2);
+            bulk_load(in_buf + i * kQChunk * 2, x + (blockIdx.x + i * G) * kQChunk, kQChunk * 2, &full[i]);
         }
-        st_v4(x8 + c * 32, o0);
-        st_v4(x8 + c * 32 + 16, o1);
     }
-    // ragged tail (< 32 elements)
-    const int64_t tail0 = nchunk * 32;
-    if (tid < n - tail0) {
-        const int64_t i = tail0 + tid;
-        float f = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
-        m = fmaxf(m, fabsf(f));
-        const float t = fast ? fp8_quotient(f, s, y) : __fdiv_rn(f, s);
-        x8[i] = static_cast<uint8_t>(fp8x2<FMT>(t, 0.0f) & 0xFFu);
+    __syncthreads();
+    int64_t i = 0;
+    for (; i < count; ++i) {
+        const int stage = static_cast<int>(i % kQStages);
+        const int ob = static_cast<int>(i & 1);
+        if (threadIdx.x == 0) {
+            s_ok = mbar_wait(&full[stage], static_cast<uint32_t>((i / kQStages) & 1), &abort_flag, err_word);
+            if (i >= 2) bulk_wait_read<1>();   // the store from out_buf[ob] two chunks ago is read
+        }
+        __syncthreads();
+        if (!s_ok) break;
+        const uint8_t* in = in_buf + stage * kQChunk * 2;
+        uint8_t* out = out_buf + ob * kQChunk;
+        const int t = threadIdx.x;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(in + t * 16);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(in + kQChunk + t * 16);
+        uint2 o0, o1;
+        if (fast) {
+            o0 = fp8_encode8<FMT, true>(a0, s, y, m);
+            o1 = fp8_encode8<FMT, true>(a1, s, y, m);
+        } else {
+            o0 = fp8_encode8<FMT, false>(a0, s, y, m);
+            o1 = fp8_encode8<FMT, false>(a1, s, y, m);
+        }
+        *reinterpret_cast<uint2*>(out + t * 8) = o0;
+        *reinterpret_cast<uint2*>(out + kQChunk / 2 + t * 8) = o1;
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int64_t c = blockIdx.x + i * G;
+            bulk_store(x8 + c * kQChunk, out, kQChunk);
+            bulk_commit();
+            if (i + kQStages < count) {
+                mbar_arrive_expect_tx(&full[stage], kQChunk * 2);
+                bulk_load(in_buf + stage * kQChunk * 2, x + (c + kQStages * G) * kQChunk, kQChunk * 2,
+                          &full[stage]);
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (i < count) {
+            // gave up on a wait: let the loads already issued land before exiting
+            for (int64_t j = i; j < count && j < i + kQStages; ++j)
+                mbar_wait_drain(&full[j % kQStages], static_cast<uint32_t>((j / kQStages) & 1));
+        }
+        bulk_wait_all();
+    }
+    // ragged tail, fewer than kQChunk elements: block 0
+    if (blockIdx.x == 0) {
+        for (int64_t e = nfull * kQChunk + threadIdx.x; e < n; e += blockDim.x) {
+            const float f = __uint_as_float(static_cast<uint32_t>(x[e]) << 16);
+            m = fmaxf(m, fabsf(f));
+            const float t = fast ? fp8_quotient(f, s, y) : __fdiv_rn(f, s);
+            x8[e] = static_cast<uint8_t>(fp8x2<FMT>(t, 0.0f) & 0xFFu);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -434,7 +526,7 @@ __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restri
     __syncthreads();
     if (threadIdx.x == 0) {
         float bm = red[0];
-        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) bm = fmaxf(bm, red[w]);
+        for (int w = 1; w < kQThreads / 32; ++w) bm = fmaxf(bm, red[w]);
         // max|x| >= 0, so the float order equals the unsigned order of the bits
         atomicMax(&ws[0], __float_as_uint(bm));
         __threadfence();
@@ -452,15 +544,14 @@ __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restri
         __syncthreads();
         const float a = s_amax;
         float wm = 0.0f;
-        for (int i = threadIdx.x; i < hist_len; i += blockDim.x)
-            wm = fmaxf(wm, i == ring_idx ? a : ring[i]);
+        for (int j = threadIdx.x; j < hist_len; j += blockDim.x)
+            wm = fmaxf(wm, j == ring_idx ? a : ring[j]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
         if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = wm;
         __syncthreads();
         if (threadIdx.x == 0) {
-            for (int w = 1; w < (int)(blockDim.x >> 5); ++w) wm = fmaxf(wm, red[w]);
-            wm = fmaxf(wm, red[0]);
+            for (int w = 0; w < kQThreads / 32; ++w) wm = fmaxf(wm, red[w]);
             ring[ring_idx] = a;
             if (wm > 0.0f) {
                 const float fmax_v = FMT == 0 ? 448.0f : 57344.0f;
@@ -471,21 +562,32 @@ __global__ void __launch_bounds__(256) quant_fp8_kernel(const uint16_t* __restri
     if (threadIdx.x == 0) atomicExch(counter, 0u);
 }
 
+template <int FMT>
+static cudaError_t launch_fp8_fmt(const uint16_t* x, int64_t n, const float* scale, uint8_t* x8,
+                                  float* amax, unsigned* ws, float* ring, int hist_len,
+                                  int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
+                                  int sms) {
+    static cudaError_t attr = cudaFuncSetAttribute(quant_fp8_kernel<FMT>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+    if (attr != cudaSuccess) return attr;
+    const int64_t nfull = n / kQChunk;
+    int64_t blocks = nfull < 1 ? 1 : nfull;
+    const int64_t cap = static_cast<int64_t>(sms) * 2;
+    if (blocks > cap) blocks = cap;
+    quant_fp8_kernel<FMT><<<static_cast<unsigned>(blocks), kQThreads, kQSmem, st>>>(
+        x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin, err_word);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
                                 uint8_t* x8, float* amax, unsigned* ws, float* ring, int hist_len,
-                                int ring_idx, int margin, cudaStream_t st, int sms) {
-    const int64_t nchunk = n / 32;
-    int64_t blocks = (nchunk + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+                                int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
+                                int sms) {
     if (fmt == 0)
-        quant_fp8_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-            x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin);
-    else
-        quant_fp8_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-            x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin);
-    return cudaGetLastError();
+        return launch_fp8_fmt<0>(x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin,
+                                 err_word, st, sms);
+    return launch_fp8_fmt<1>(x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin, err_word,
+                             st, sms);
 }
 
 }  // namespace sq

@@ -7,9 +7,10 @@
 
 namespace sq {
 
+// err_word == nullptr keeps to the kernels without waits.
 cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols,
                                        int64_t ld, int8_t* q, float* scales, bool vec_ok,
-                                       cudaStream_t st, int sms);
+                                       unsigned* err_word, cudaStream_t st, int sms);
 
 // Row groups of group_rows rows share one scale; ws holds ceil(rows/group_rows)
 // words (zeroed by the launcher with cudaMemsetAsync).
@@ -21,11 +22,13 @@ cudaError_t launch_quantize_grouped_i8(const void* x, int dtype, int64_t rows, i
 // delayed scaling with ring = [hist (hist_len) | scale | counter].
 cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
                                 uint8_t* x8, float* amax, unsigned* ws, float* ring, int hist_len,
-                                int ring_idx, int margin, cudaStream_t st, int sms);
+                                int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
+                                int sms);
 
 // Staging of INT8 codes as exact fp16 values: dst[b][r][k] = src[b*stride + r*K + k].
 cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
-                             int64_t stride, uint16_t* dst, cudaStream_t st, int sms);
+                             int64_t stride, uint16_t* dst, unsigned* err_word, cudaStream_t st,
+                             int sms);
 
 // 0 on success, a cudaError_t otherwise; CUDA_ERROR_* from tensor-map encoding
 // is reported as cudaErrorInvalidValue.

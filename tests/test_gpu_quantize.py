@@ -33,6 +33,10 @@ ROW_CASES = [
     ("bf16 long rows 5x40000 (scalar path)", (5, 40000), "bf16", "t3"),
     ("f32 tiny rows 1000x16", (1000, 16), "f32", "normal"),
     ("bf16 1x8", (1, 8), "bf16", "normal"),
+    # enough rows of 4-16 KB to take the bulk-copy pipeline
+    ("bulk bf16 1000x2048", (1000, 2048), "bf16", "normal"),
+    ("bulk f32 700x4096", (700, 4096), "f32", "t3"),
+    ("bulk bf16 t3 900x6144", (900, 6144), "bf16", "t3"),
 ]
 
 
@@ -61,6 +65,17 @@ def test_rowwise_i8_strided_rows_and_guard():
     sq.sq_quantize_rowwise_i8(xd, q=q, scales=s)
     assert np.array_equal(q.cpu().numpy(), oq) and np.array_equal(s.cpu().numpy(), osc)
     assert guard_intact(qbuf, n, 77) and guard_intact(sbuf, ns, -5.0)
+
+
+def test_rowwise_i8_bulk_path_strided_rows_and_guard():
+    full = synth.normal(23, (800, 4096 + 64), dtype=synth.BF16)
+    xd = to_dev(full, bf16=True)[:, :4096]          # rows 8 KB, row stride 8320 B
+    oq, osc = oracle.quantize_rowwise_i8(np.ascontiguousarray(full[:, :4096]), oracle.BF16)
+    q, qbuf, n = guarded((800, 4096), torch.int8, 55)
+    s, sbuf, ns = guarded((800,), torch.float32, -3.0)
+    sq.sq_quantize_rowwise_i8(xd, q=q, scales=s)
+    assert np.array_equal(q.cpu().numpy(), oq) and np.array_equal(s.cpu().numpy(), osc)
+    assert guard_intact(qbuf, n, 55) and guard_intact(sbuf, ns, -3.0)
 
 
 def test_rowwise_i8_degenerate_rows_and_ties():
