@@ -34,25 +34,11 @@ struct Elem;
 template <>
 struct Elem<float> {
     static constexpr int kPerVec = 4;
-    __device__ static void unpack(const uint4& v, float (&f)[4]) {
-        f[0] = __uint_as_float(v.x);
-        f[1] = __uint_as_float(v.y);
-        f[2] = __uint_as_float(v.z);
-        f[3] = __uint_as_float(v.w);
-    }
     __device__ static float load1(const float* p) { return *p; }
 };
 template <>
 struct Elem<uint16_t> {   // bf16 bit patterns; widening is exact
     static constexpr int kPerVec = 8;
-    __device__ static void unpack(const uint4& v, float (&f)[8]) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-    }
     __device__ static float load1(const uint16_t* p) {
         return __uint_as_float(static_cast<uint32_t>(*p) << 16);
     }
@@ -72,13 +58,102 @@ __device__ __forceinline__ int8_t encode_i8(float x, float s) {
     return clamp_i8(__float2int_rn(__fdiv_rn(x, s)));
 }
 
-__device__ __forceinline__ int8_t encode_i8_recip(float x, float s, float y) {
-    return clamp_i8(__float2int_rn(div_rn_recip(x, s, y)));
-}
-
 __device__ __forceinline__ float row_scale(float amax) {
     return __fdiv_rn(fmaxf(amax, 1e-8f), 127.0f);
 }
+
+// ---- one 16-byte input vector at a time (8 bf16 or 4 f32 values)
+// |x| max folded into a running maximum.  bf16 values are compared as bf16
+// (sign bits cleared, then a packed max): comparisons are exact, so widening
+// the result afterwards gives the f32 maximum.  NaN lanes lose to numbers, as
+// with fmaxf.
+template <typename T>
+struct AbsMax;
+template <>
+struct AbsMax<float> {
+    float m = 0.0f;
+    __device__ __forceinline__ void add(const uint4& v) {
+        m = fmaxf(fmaxf(m, fabsf(__uint_as_float(v.x))), fabsf(__uint_as_float(v.y)));
+        m = fmaxf(fmaxf(m, fabsf(__uint_as_float(v.z))), fabsf(__uint_as_float(v.w)));
+    }
+    __device__ __forceinline__ float value() const { return m; }
+};
+template <>
+struct AbsMax<uint16_t> {
+    uint32_t m = 0u;   // two bf16 lanes
+    __device__ __forceinline__ static uint32_t max2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ __forceinline__ void add(const uint4& v) {
+        const uint32_t a = max2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+        const uint32_t b = max2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+        m = max2(m, max2(a, b));
+    }
+    __device__ __forceinline__ float value() const {
+        return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+    }
+};
+
+// Code of x for a scale in the reciprocal range, as the low byte of a word.
+// RNE(t) for |t| < 2^22 is what adding 1.5 * 2^23 leaves in the low bits (the
+// sum's ulp is 1 and RN breaks ties to even), and its low byte is the
+// two's-complement code.  No clamp is needed: s = RN(m/127) with every
+// |x| <= m bounds |x/s| by 127 / (1 - 2^-24) < 127.5, so RNE already lands in
+// [-127, 127].
+__device__ __forceinline__ uint32_t code_word(float x, float s, float y) {
+    return __float_as_uint(__fadd_rn(div_rn_recip(x, s, y), 12582912.0f));
+}
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// Codes of one vector stored at dst (4 or 8 bytes, aligned to that size);
+// FAST: s <= kRecipHi.
+template <typename T>
+struct Codes;
+template <>
+struct Codes<float> {
+    template <bool FAST>
+    __device__ __forceinline__ static void store(const uint4& v, float s, float y, int8_t* dst) {
+        const float f[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                            __uint_as_float(v.w)};
+        uint32_t w;
+        if (FAST) {
+            w = pack_low_bytes(code_word(f[0], s, y), code_word(f[1], s, y), code_word(f[2], s, y),
+                               code_word(f[3], s, y));
+        } else {
+            w = pack_low_bytes(static_cast<uint8_t>(encode_i8(f[0], s)),
+                               static_cast<uint8_t>(encode_i8(f[1], s)),
+                               static_cast<uint8_t>(encode_i8(f[2], s)),
+                               static_cast<uint8_t>(encode_i8(f[3], s)));
+        }
+        *reinterpret_cast<uint32_t*>(dst) = w;
+    }
+};
+template <>
+struct Codes<uint16_t> {
+    template <bool FAST>
+    __device__ __forceinline__ static void store(const uint4& v, float s, float y, int8_t* dst) {
+        const uint32_t src[4] = {v.x, v.y, v.z, v.w};
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = __uint_as_float(src[i] << 16);
+            const float hi = __uint_as_float(src[i] & 0xFFFF0000u);
+            if (FAST) {
+                c[2 * i] = code_word(lo, s, y);
+                c[2 * i + 1] = code_word(hi, s, y);
+            } else {
+                c[2 * i] = static_cast<uint8_t>(encode_i8(lo, s));
+                c[2 * i + 1] = static_cast<uint8_t>(encode_i8(hi, s));
+            }
+        }
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(pack_low_bytes(c[0], c[1], c[2], c[3]), pack_low_bytes(c[4], c[5], c[6], c[7]));
+    }
+};
 
 // A group of TPR threads owns one row, held in registers (VPT 16-byte vectors
 // per thread).  Rows must start 16-byte aligned and cols be a multiple of 16.
@@ -103,14 +178,10 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
             const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
             raw[i] = (live && vi < nvec) ? ld_stream_v4(x + row * ld + vi * EPV) : make_uint4(0, 0, 0, 0);
         }
-        float m = 0.0f;
+        AbsMax<T> am;
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            float v[EPV];
-            Elem<T>::unpack(raw[i], v);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf(v[e]));
-        }
+        for (int i = 0; i < VPT; ++i) am.add(raw[i]);
+        float m = am.value();
         if (TPR <= 32) {
 #pragma unroll
             for (int o = TPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -129,28 +200,17 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
         const float y = __frcp_rn(s);
         if (live) {
             if (lg == 0) scales[row] = s;
+            if (fast) {
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
-                if (vi < nvec) {
-                    float v[EPV];
-                    Elem<T>::unpack(raw[i], v);
-                    uint32_t packed[EPV / 4];
+                for (int i = 0; i < VPT; ++i) {
+                    const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
+                    if (vi < nvec) Codes<T>::template store<true>(raw[i], s, y, q + row * cols + vi * EPV);
+                }
+            } else {
 #pragma unroll
-                    for (int w = 0; w < EPV / 4; ++w) {
-                        uint32_t b[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            b[e] = static_cast<uint8_t>(fast ? encode_i8_recip(v[4 * w + e], s, y)
-                                                             : encode_i8(v[4 * w + e], s));
-                        packed[w] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-                    }
-                    int8_t* dst = q + row * cols + vi * EPV;
-                    if (EPV == 4) {
-                        *reinterpret_cast<uint32_t*>(dst) = packed[0];
-                    } else {
-                        *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[EPV / 4 - 1]);
-                    }
+                for (int i = 0; i < VPT; ++i) {
+                    const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
+                    if (vi < nvec) Codes<T>::template store<false>(raw[i], s, y, q + row * cols + vi * EPV);
                 }
             }
         }
@@ -184,6 +244,67 @@ __global__ void __launch_bounds__(256) quant_row_i8_scalar(const T* __restrict__
     }
 }
 
+// Rows of 2-16 KB with enough rows to fill the GPU: persistent CTAs of 256
+// threads walk rows blockIdx.x, +gridDim.x, ...; the next row is fetched into
+// the other half of a 2 x 16 KB shared-memory buffer with cp.async while the
+// current one is quantized, so every CTA always has a row in flight.  The
+// row is read from shared memory twice (absmax, then codes); codes go to
+// global memory directly.  Needs 16-byte aligned rows and cols % 16 == 0.
+constexpr int kPfRowBytes = 16384;
+
+template <typename T>
+__global__ void __launch_bounds__(256) quant_row_i8_pf(const T* __restrict__ x, int64_t rows,
+                                                       int64_t cols, int64_t ld,
+                                                       int8_t* __restrict__ q,
+                                                       float* __restrict__ scales) {
+    constexpr int EPV = Elem<T>::kPerVec;
+    __shared__ __align__(16) uint8_t buf[2][kPfRowBytes];
+    __shared__ float red[8];
+    const int nvec = static_cast<int>(cols / EPV);          // 16-byte vectors per row
+    const int64_t G = gridDim.x;
+    const int t = threadIdx.x;
+    auto fetch = [&](int64_t row, int b) {
+        const T* src = x + row * ld;
+        for (int vi = t; vi < nvec; vi += 256) cp_async16(&buf[b][vi * 16], src + vi * EPV);
+        cp_async_commit();
+    };
+    int64_t row = blockIdx.x;
+    if (row < rows) fetch(row, 0);
+    for (int i = 0; row < rows; ++i, row += G) {
+        const int b = i & 1;
+        if (row + G < rows) fetch(row + G, b ^ 1);
+        else cp_async_commit();                 // keep one group per iteration
+        cp_async_wait<1>();                     // this row's copies are done
+        __syncthreads();
+        AbsMax<T> am;
+        for (int vi = t; vi < nvec; vi += 256) am.add(*reinterpret_cast<const uint4*>(&buf[b][vi * 16]));
+        float m = am.value();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((t & 31) == 0) red[t >> 5] = m;
+        __syncthreads();
+        m = red[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+        const float s = row_scale(m);
+        const bool fast = s <= kRecipHi;
+        const float y = __frcp_rn(s);
+        if (t == 0) scales[row] = s;
+        int8_t* qr = q + row * cols;
+        if (fast) {
+            for (int vi = t; vi < nvec; vi += 256)
+                Codes<T>::template store<true>(*reinterpret_cast<const uint4*>(&buf[b][vi * 16]), s, y,
+                                  qr + vi * EPV);
+        } else {
+            for (int vi = t; vi < nvec; vi += 256)
+                Codes<T>::template store<false>(*reinterpret_cast<const uint4*>(&buf[b][vi * 16]), s, y,
+                                   qr + vi * EPV);
+        }
+        __syncthreads();                        // buffer b and red[] are free again
+    }
+    cp_async_wait<0>();
+}
+
 template <typename T, int TPR, int VPT>
 static cudaError_t launch_row_vec(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
                                   float* scales, cudaStream_t st, int sms) {
@@ -203,6 +324,14 @@ static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld
     constexpr int EPV = Elem<T>::kPerVec;
     const int64_t nvec = cols / EPV;
     (void)err_word;
+    const int64_t row_bytes = cols * static_cast<int64_t>(sizeof(T));
+    if (vec_ok && row_bytes >= 2048 && row_bytes <= kPfRowBytes && rows >= 2 * sms) {
+        int64_t blocks = rows;
+        const int64_t cap = static_cast<int64_t>(sms) * 6;
+        if (blocks > cap) blocks = cap;
+        quant_row_i8_pf<T><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, q, scales);
+        return cudaGetLastError();
+    }
     if (vec_ok) {
         if (nvec <= 16) return launch_row_vec<T, 16, 1>(x, rows, cols, ld, q, scales, st, sms);
         if (nvec <= 32) return launch_row_vec<T, 32, 1>(x, rows, cols, ld, q, scales, st, sms);
@@ -245,12 +374,9 @@ __device__ __forceinline__ float row_absmax_warp(const T* xr, int64_t cols, int 
     float m = 0.0f;
     if (VEC) {
         const int64_t nvec = cols / EPV;
-        for (int64_t vi = lane; vi < nvec; vi += 32) {
-            float v[EPV];
-            Elem<T>::unpack(ld_stream_v4(xr + vi * EPV), v);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf(v[e]));
-        }
+        AbsMax<T> am;
+        for (int64_t vi = lane; vi < nvec; vi += 32) am.add(ld_stream_v4(xr + vi * EPV));
+        m = am.value();
     } else {
         for (int64_t k = lane; k < cols; k += 32) m = fmaxf(m, fabsf(Elem<T>::load1(xr + k)));
     }
@@ -305,21 +431,12 @@ __global__ void __launch_bounds__(256) group_encode_kernel(const T* __restrict__
         int8_t* qr = q + r * cols;
         if (VEC) {
             const int64_t nvec = cols / EPV;
-            for (int64_t vi = lane; vi < nvec; vi += 32) {
-                float v[EPV];
-                Elem<T>::unpack(ld_stream_v4(xr + vi * EPV), v);
-                uint32_t packed[EPV / 4];
-#pragma unroll
-                for (int w = 0; w < EPV / 4; ++w) {
-                    uint32_t b[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        b[e] = static_cast<uint8_t>(fast ? encode_i8_recip(v[4 * w + e], s, y)
-                                                         : encode_i8(v[4 * w + e], s));
-                    packed[w] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-                }
-                if (EPV == 4) *reinterpret_cast<uint32_t*>(qr + vi * EPV) = packed[0];
-                else *reinterpret_cast<uint2*>(qr + vi * EPV) = make_uint2(packed[0], packed[EPV / 4 - 1]);
+            if (fast) {
+                for (int64_t vi = lane; vi < nvec; vi += 32)
+                    Codes<T>::template store<true>(ld_stream_v4(xr + vi * EPV), s, y, qr + vi * EPV);
+            } else {
+                for (int64_t vi = lane; vi < nvec; vi += 32)
+                    Codes<T>::template store<false>(ld_stream_v4(xr + vi * EPV), s, y, qr + vi * EPV);
             }
         } else {
             for (int64_t k = lane; k < cols; k += 32) qr[k] = encode_i8(Elem<T>::load1(xr + k), s);

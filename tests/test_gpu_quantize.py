@@ -92,6 +92,38 @@ def test_rowwise_i8_degenerate_rows_and_ties():
     assert np.array_equal(s.cpu().numpy(), osc) and np.array_equal(q.cpu().numpy(), oq)
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_rowwise_i8_degenerate_rows_in_streamed_rows(dt):
+    """The same special rows scattered through a tall matrix of 4-8 KB rows,
+    the shape rows are streamed through shared memory at."""
+    rows, cols = 2333, 1024 if dt == "f32" else 4096
+    x = synth.normal(24, (rows, cols), dtype=synth.BF16 if dt == "bf16" else synth.F32)
+    xf = synth.bf16_bits_to_f32(x) if dt == "bf16" else x
+    pick = np.random.default_rng(5).choice(rows, 60, replace=False)
+    for n, r in enumerate(pick):
+        kind = n % 5
+        if kind == 0:
+            xf[r] = 0.0
+        elif kind == 1:
+            xf[r] = 1e-12
+        elif kind == 2:
+            xf[r] = (np.arange(cols) % 64 - 32) / 2.0
+            xf[r, 0] = 127.0
+        elif kind == 3:
+            xf[r] *= np.float32(1e30)          # scales above 2^40
+        else:
+            xf[r] = np.float32(3.0e38) * np.sign(xf[r])
+    if dt == "bf16":
+        x = (xf.view(np.uint32) >> 16).astype(np.uint16)   # truncated to bf16; both sides see it
+        oq, osc = oracle.quantize_rowwise_i8(x, oracle.BF16)
+        q, s = sq.sq_quantize_rowwise_i8(to_dev(x, True))
+    else:
+        x = xf.astype(np.float32)
+        oq, osc = oracle.quantize_rowwise_i8(x)
+        q, s = sq.sq_quantize_rowwise_i8(to_dev(x))
+    assert np.array_equal(s.cpu().numpy(), osc) and np.array_equal(q.cpu().numpy(), oq)
+
+
 def test_rowwise_i8_empty():
     q, s = sq.sq_quantize_rowwise_i8(torch.empty((0, 64), device=DEV))
     assert q.shape == (0, 64) and s.shape == (0,)
