@@ -479,30 +479,6 @@ cudaError_t launch_quantize_grouped_i8(const void* x, int dtype, int64_t rows, i
 
 // ================================================================== FP8 tensor
 
-// 16 bf16 (two 16-B words) -> 16 FP8 codes (one 16-B word); m = running max|x|.
-template <int FMT, bool FAST>
-__device__ __forceinline__ uint4 fp8_encode16(const uint4& a, const uint4& b, float s, float y,
-                                              float& m) {
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float f[4];
-        f[0] = __uint_as_float(w[2 * i] << 16);
-        f[1] = __uint_as_float(w[2 * i] & 0xFFFF0000u);
-        f[2] = __uint_as_float(w[2 * i + 1] << 16);
-        f[3] = __uint_as_float(w[2 * i + 1] & 0xFFFF0000u);
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
-        float t[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) t[e] = FAST ? fp8_quotient(f[e], s, y) : __fdiv_rn(f[e], s);
-        const uint32_t lo = fp8x2<FMT>(t[0], t[1]);
-        const uint32_t hi = fp8x2<FMT>(t[2], t[3]);
-        o[i] = lo | (hi << 16);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // 8 bf16 (one 16-B word) -> 8 FP8 codes (one 8-B word); m = running max|x|.
 template <int FMT, bool FAST>
 __device__ __forceinline__ uint2 fp8_encode8(const uint4& a, float s, float y, float& m) {

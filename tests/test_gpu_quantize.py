@@ -236,6 +236,37 @@ def test_fp8_scales_across_the_division_paths(scale):
         assert np.all(ox8[:64] == 0x80)
 
 
+SPECIAL_BF16 = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x0080, 0x8080, 0x7F7F, 0xFF7F,
+                         0x7F80, 0xFF80, 0x7FC0, 0xFFC0, 0x3F80, 0xBF80], dtype=np.uint16)
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -40, 1e-12, 1.0, 2.0 ** 40, 1e13],
+                         ids=["2^-40", "1e-12", "1", "2^40", "1e13"])
+def test_fp8_special_values(scale):
+    """Zeros of both signs, bf16 subnormals, the largest bf16, infinities and
+    NaNs, in the streamed chunks and in the ragged tail, with step sizes at
+    and beyond both ends of the reciprocal range (products that overflow
+    float32 must still saturate).  A NaN input must give a NaN code; the sign
+    of that code is not fixed by the format, so only NaN-ness is compared
+    there, and every other code bit for bit."""
+    n = 3 * 8192 + 77
+    x = synth.normal(19, (n,), std=3.0, dtype=synth.BF16)
+    rng = np.random.default_rng(19)
+    for pos in np.concatenate([rng.choice(3 * 8192, 200, replace=False), np.arange(3 * 8192, n)]):
+        x[pos] = SPECIAL_BF16[pos % len(SPECIAL_BF16)]
+    ws = sq.new_workspace(DEV)
+    for fmt in (sq.SQ_FMT_E4M3, sq.SQ_FMT_E5M2):
+        ox8, oamax = oracle.quantize_fp8(x, np.float32(scale), fmt)
+        x8, amax = sq.sq_quantize_fp8(to_dev(x, bf16=True),
+                                      torch.tensor([scale], dtype=torch.float32, device=DEV), fmt, ws)
+        got = x8.cpu().numpy()
+        nan_in = (x & 0x7FFF) > 0x7F80
+        assert nan_in.sum() > 20
+        assert np.array_equal(got[~nan_in], ox8[~nan_in])
+        assert all(oracle.fp8_code_is_nan(int(c), fmt) for c in got[nan_in])
+        assert amax.item() == float(oamax) == np.inf
+
+
 # ------------------------------------------------------------------ delayed-scaling ring
 @pytest.mark.parametrize("fmt", [sq.SQ_FMT_E4M3, sq.SQ_FMT_E5M2], ids=["e4m3", "e5m2"])
 def test_fp8_ring_sequence_matches_the_oracle(fmt):
