@@ -22,12 +22,6 @@
 
 namespace sq {
 
-// Streaming kernels: persistent CTAs of kQThreads threads with a kQStages-deep
-// ring of shared-memory stages filled by bulk copies.
-constexpr int kQChunk = 8192;                       // FP8 path: bf16 per chunk, 16 KB in, 8 KB out
-constexpr int kQStages = 4;
-constexpr int kQThreads = 512;
-
 // ================================================================== INT8 rows
 template <typename T>
 struct Elem;
@@ -500,13 +494,16 @@ __device__ __forceinline__ uint2 fp8_encode8(const uint4& a, float s, float y, f
     return make_uint2(o[0], o[1]);
 }
 
-// Streaming pipeline: persistent CTAs of kQThreads threads; one thread moves
-// 16 KB input chunks into a ring of kQStages shared-memory stages with bulk
-// copies (cp.async.bulk) and writes each chunk's 8 KB of codes back with a
-// bulk store from one of two output buffers; every thread converts 16
-// elements per chunk from shared memory (two contiguous 16-B pieces, no bank
-// conflicts).  The ragged tail (< one chunk) is done by block 0 with plain
-// loads and stores.
+// Streaming pipeline, one per warp: persistent CTAs of kFWarps warps, and
+// every warp streams its own chunks of kFChunk bf16 (2 KB in, 1 KB of codes
+// out) with no CTA-wide barrier inside the loop.  Lane 0 keeps kFStages input
+// chunks in flight in the warp's shared-memory ring with bulk copies
+// (cp.async.bulk, completion on the warp's own mbarriers, bounded waits) and
+// writes each chunk's codes back with a bulk store from one of two output
+// buffers; every lane converts 32 elements per chunk (four 16-B pieces, lane-
+// contiguous, so no bank conflicts).  Chunks are dealt round-robin over all
+// warps of the grid.  The ragged tail (< one chunk) is done by block 0 with
+// plain loads and stores.
 //
 // Plain mode (ring == nullptr): the step is *scale; ws = [amax bits | ticket].
 // Ring mode: delayed scaling with ring = [hist (hist_len) | scale | counter]
@@ -517,26 +514,35 @@ __device__ __forceinline__ uint2 fp8_encode8(const uint4& a, float s, float y, f
 // ring[hist_len] (kept as it was when the window max is 0) -- no extra
 // launch.  ws[0] still accumulates the amax bits.  Both modes leave their
 // counter and ws[0] at zero.
-constexpr int kQSmem = kQStages * kQChunk * 2 + 2 * kQChunk + kQStages * 8 + 128;
+// One CTA of 24 warps per SM, two 2 KB stages per warp: 96 KB of loads in
+// flight per SM.  Measured on GB300 against 8-32 warps per SM, 0.5-4 KB
+// chunks and 2-6 stages, this was the fastest shape for both operands of
+// the large workload.
+constexpr int kFWarps = 24;
+constexpr int kFChunk = 1024;
+constexpr int kFStages = 2;
+constexpr int kFWarpBytes = kFStages * kFChunk * 2 + 2 * kFChunk;
+constexpr int kQSmem = kFWarps * kFWarpBytes + kFWarps * kFStages * 8 + 128;
 
 template <int FMT>
-__global__ void __launch_bounds__(kQThreads) quant_fp8_kernel(const uint16_t* __restrict__ x, int64_t n,
-                                                              const float* __restrict__ scale,
-                                                              uint8_t* __restrict__ x8,
-                                                              float* __restrict__ amax_out,
-                                                              unsigned* __restrict__ ws, float* ring,
-                                                              int hist_len, int ring_idx, int margin,
-                                                              unsigned* err_word) {
+__global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                                 const float* __restrict__ scale,
+                                                                 uint8_t* __restrict__ x8,
+                                                                 float* __restrict__ amax_out,
+                                                                 unsigned* __restrict__ ws, float* ring,
+                                                                 int hist_len, int ring_idx, int margin,
+                                                                 unsigned* err_word) {
     extern __shared__ uint8_t qsmem_raw[];
     uint8_t* qsmem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(qsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
-    uint8_t* in_buf = qsmem;                                   // kQStages x 16 KB
-    uint8_t* out_buf = in_buf + kQStages * kQChunk * 2;        // 2 x 8 KB
-    uint64_t* full = reinterpret_cast<uint64_t*>(out_buf + 2 * kQChunk);
-    __shared__ float red[kQThreads / 32];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* in_buf = qsmem + warp * kFWarpBytes;              // kFStages x 2 KB
+    uint8_t* out_buf = in_buf + kFStages * kFChunk * 2;        // 2 x 1 KB
+    uint64_t* full = reinterpret_cast<uint64_t*>(qsmem + kFWarps * kFWarpBytes) + warp * kFStages;
+    __shared__ float red[kFWarps];
     __shared__ int is_last;
     __shared__ float s_amax;
-    __shared__ int s_ok;
     __shared__ int abort_flag;
 
     const float s = scale ? *scale : ring[hist_len];
@@ -545,68 +551,72 @@ __global__ void __launch_bounds__(kQThreads) quant_fp8_kernel(const uint16_t* __
     const bool fast = s >= 0x1p-40f && s <= 0x1p40f;
     float m = 0.0f;
 
-    const int64_t nfull = n / kQChunk;
-    const int64_t G = gridDim.x;
-    const int64_t count = blockIdx.x < nfull ? (nfull - blockIdx.x + G - 1) / G : 0;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kQStages; ++i) mbar_init(&full[i], 1);
-        abort_flag = 0;
+    const int64_t nfull = n / kFChunk;
+    const int64_t GW = static_cast<int64_t>(gridDim.x) * kFWarps;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kFWarps + warp;
+    const int64_t count = gw < nfull ? (nfull - gw + GW - 1) / GW : 0;
+    if (threadIdx.x == 0) abort_flag = 0;
+    if (lane == 0) {
+        for (int k = 0; k < kFStages; ++k) mbar_init(&full[k], 1);
         fence_mbar_init();
-        for (int64_t i = 0; i < count && i < kQStages; ++i) {
-            mbar_arrive_expect_tx(&full[i], kQChunk * 2);
-            bulk_load(in_buf + i * kQChunk * 2, x + (blockIdx.x + i * G) * kQChunk, kQChunk * 2, &full[i]);
-        }
     }
     __syncthreads();
+    if (lane == 0) {
+        for (int64_t k = 0; k < count && k < kFStages; ++k) {
+            mbar_arrive_expect_tx(&full[k], kFChunk * 2);
+            bulk_load(in_buf + k * kFChunk * 2, x + (gw + k * GW) * kFChunk, kFChunk * 2, &full[k]);
+        }
+    }
     int64_t i = 0;
     for (; i < count; ++i) {
-        const int stage = static_cast<int>(i % kQStages);
+        const int stage = static_cast<int>(i % kFStages);
         const int ob = static_cast<int>(i & 1);
-        if (threadIdx.x == 0) {
-            s_ok = mbar_wait(&full[stage], static_cast<uint32_t>((i / kQStages) & 1), &abort_flag, err_word);
+        int ok = 1;
+        if (lane == 0) {
+            ok = mbar_wait(&full[stage], static_cast<uint32_t>((i / kFStages) & 1), &abort_flag, err_word);
             if (i >= 2) bulk_wait_read<1>();   // the store from out_buf[ob] two chunks ago is read
         }
-        __syncthreads();
-        if (!s_ok) break;
-        const uint8_t* in = in_buf + stage * kQChunk * 2;
-        uint8_t* out = out_buf + ob * kQChunk;
-        const int t = threadIdx.x;
-        const uint4 a0 = *reinterpret_cast<const uint4*>(in + t * 16);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(in + kQChunk + t * 16);
-        uint2 o0, o1;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();                          // orders lane 0's wait before the other lanes' reads
+        if (!ok) break;
+        const uint8_t* in = in_buf + stage * kFChunk * 2;
+        uint8_t* out = out_buf + ob * kFChunk;
+        uint4 a[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a[k] = *reinterpret_cast<const uint4*>(in + (k * 32 + lane) * 16);
         if (fast) {
-            o0 = fp8_encode8<FMT, true>(a0, s, y, m);
-            o1 = fp8_encode8<FMT, true>(a1, s, y, m);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint2*>(out + (k * 32 + lane) * 8) = fp8_encode8<FMT, true>(a[k], s, y, m);
         } else {
-            o0 = fp8_encode8<FMT, false>(a0, s, y, m);
-            o1 = fp8_encode8<FMT, false>(a1, s, y, m);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint2*>(out + (k * 32 + lane) * 8) = fp8_encode8<FMT, false>(a[k], s, y, m);
         }
-        *reinterpret_cast<uint2*>(out + t * 8) = o0;
-        *reinterpret_cast<uint2*>(out + kQChunk / 2 + t * 8) = o1;
         fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const int64_t c = blockIdx.x + i * G;
-            bulk_store(x8 + c * kQChunk, out, kQChunk);
+        __syncwarp();
+        if (lane == 0) {
+            const int64_t c = gw + i * GW;
+            bulk_store(x8 + c * kFChunk, out, kFChunk);
             bulk_commit();
-            if (i + kQStages < count) {
-                mbar_arrive_expect_tx(&full[stage], kQChunk * 2);
-                bulk_load(in_buf + stage * kQChunk * 2, x + (c + kQStages * G) * kQChunk, kQChunk * 2,
+            if (i + kFStages < count) {
+                mbar_arrive_expect_tx(&full[stage], kFChunk * 2);
+                bulk_load(in_buf + stage * kFChunk * 2, x + (c + kFStages * GW) * kFChunk, kFChunk * 2,
                           &full[stage]);
             }
         }
     }
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
         if (i < count) {
             // gave up on a wait: let the loads already issued land before exiting
-            for (int64_t j = i; j < count && j < i + kQStages; ++j)
-                mbar_wait_drain(&full[j % kQStages], static_cast<uint32_t>((j / kQStages) & 1));
+            for (int64_t j = i; j < count && j < i + kFStages; ++j)
+                mbar_wait_drain(&full[j % kFStages], static_cast<uint32_t>((j / kFStages) & 1));
         }
         bulk_wait_all();
     }
-    // ragged tail, fewer than kQChunk elements: block 0
+    // ragged tail, fewer than kFChunk elements: block 0
     if (blockIdx.x == 0) {
-        for (int64_t e = nfull * kQChunk + threadIdx.x; e < n; e += blockDim.x) {
+        for (int64_t e = nfull * kFChunk + threadIdx.x; e < n; e += blockDim.x) {
             const float f = __uint_as_float(static_cast<uint32_t>(x[e]) << 16);
             m = fmaxf(m, fabsf(f));
             const float t = fast ? fp8_quotient(f, s, y) : __fdiv_rn(f, s);
@@ -619,7 +629,7 @@ __global__ void __launch_bounds__(kQThreads) quant_fp8_kernel(const uint16_t* __
     __syncthreads();
     if (threadIdx.x == 0) {
         float bm = red[0];
-        for (int w = 1; w < kQThreads / 32; ++w) bm = fmaxf(bm, red[w]);
+        for (int w = 1; w < kFWarps; ++w) bm = fmaxf(bm, red[w]);
         // max|x| >= 0, so the float order equals the unsigned order of the bits
         atomicMax(&ws[0], __float_as_uint(bm));
         __threadfence();
@@ -644,7 +654,7 @@ __global__ void __launch_bounds__(kQThreads) quant_fp8_kernel(const uint16_t* __
         if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = wm;
         __syncthreads();
         if (threadIdx.x == 0) {
-            for (int w = 0; w < kQThreads / 32; ++w) wm = fmaxf(wm, red[w]);
+            for (int w = 0; w < kFWarps; ++w) wm = fmaxf(wm, red[w]);
             ring[ring_idx] = a;
             if (wm > 0.0f) {
                 const float fmax_v = FMT == 0 ? 448.0f : 57344.0f;
@@ -663,11 +673,12 @@ static cudaError_t launch_fp8_fmt(const uint16_t* x, int64_t n, const float* sca
     static cudaError_t attr = cudaFuncSetAttribute(quant_fp8_kernel<FMT>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
     if (attr != cudaSuccess) return attr;
-    const int64_t nfull = n / kQChunk;
-    int64_t blocks = nfull < 1 ? 1 : nfull;
-    const int64_t cap = static_cast<int64_t>(sms) * 2;
+    const int64_t nfull = n / kFChunk;
+    int64_t blocks = (nfull + kFWarps - 1) / kFWarps;
+    if (blocks < 1) blocks = 1;
+    const int64_t cap = static_cast<int64_t>(sms);
     if (blocks > cap) blocks = cap;
-    quant_fp8_kernel<FMT><<<static_cast<unsigned>(blocks), kQThreads, kQSmem, st>>>(
+    quant_fp8_kernel<FMT><<<static_cast<unsigned>(blocks), kFWarps * 32, kQSmem, st>>>(
         x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin, err_word);
     return cudaGetLastError();
 }
