@@ -732,6 +732,20 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
 }
 
 // ---------------------------------------------------------------- staging
+// Eight int8 codes -> eight exact fp16 values.  With u = c + 128 in [1, 255]
+// (the code's byte with its top bit flipped), the fp16 bit pattern 0x6400 | u
+// is the value 1024 + u exactly (the spacing of fp16 in [1024, 2048) is 1),
+// and subtracting 1152 leaves c exactly.
+__device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 w) {
+    const uint32_t a = w.x ^ 0x80808080u;
+    const uint32_t b = w.y ^ 0x80808080u;
+    uint32_t o[4] = {__byte_perm(a, 0x64646464u, 0x4140), __byte_perm(a, 0x64646464u, 0x4342),
+                     __byte_perm(b, 0x64646464u, 0x4140), __byte_perm(b, 0x64646464u, 0x4342)};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(o[k]) : "r"(0x64806480u));
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ src,
                                                        int64_t batch, int64_t rows, int64_t K,
                                                        int64_t stride, uint16_t* __restrict__ dst) {
@@ -745,117 +759,99 @@ __global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict
         const int64_t r = v - b * per_batch;
         const int8_t* s = src + b * stride + r * 16;
         const uint4 raw = ld_stream_v4(s);
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int8_t c0 = static_cast<int8_t>((w[i] >> (16 * h)) & 0xFF);
-                const int8_t c1 = static_cast<int8_t>((w[i] >> (16 * h + 8)) & 0xFF);
-                const uint32_t h0 = __half_as_ushort(__int2half_rn(c0));
-                const uint32_t h1 = __half_as_ushort(__int2half_rn(c1));
-                o[2 * i + h] = h0 | (h1 << 16);
-            }
-        }
         uint16_t* d = dst + v * 16;
-        st_v4(d, make_uint4(o[0], o[1], o[2], o[3]));
-        st_v4(d + 8, make_uint4(o[4], o[5], o[6], o[7]));
+        st_v4(d, i8x8_to_f16x8(make_uint2(raw.x, raw.y)));
+        st_v4(d + 8, i8x8_to_f16x8(make_uint2(raw.z, raw.w)));
     }
 }
 
-// Contiguous source (batch stride == rows*K): a bulk-copy pipeline as in the
-// quantize kernels -- 8 KB int8 chunks in through a 4-stage ring, 16 KB fp16
-// chunks out through two buffers; each thread converts two 8-byte pieces
-// (conflict-free shared-memory access).  The ragged tail (a multiple of 16
-// codes, below one chunk) is done by block 0 with vector loads.
-constexpr int kStgChunk = 8192;       // codes per chunk
-constexpr int kStgStages = 4;
-constexpr int kStgThreads = 512;
-constexpr int kStgSmem = kStgStages * kStgChunk + 2 * kStgChunk * 2 + kStgStages * 8 + 128;
+// Contiguous source (batch stride == rows*K): a bulk-copy pipeline per warp,
+// as in the FP8 quantize.  Every warp of a persistent CTA streams its own
+// chunks of kStgChunk codes (1 KB in, 2 KB of fp16 out) through a kStgStages-
+// deep ring with bulk copies and its own mbarriers; lane 0 waits and issues,
+// a warp barrier orders the other lanes, and no CTA-wide barrier is needed
+// inside the loop.  Each lane converts four 8-byte pieces (conflict-free
+// shared-memory access).  The ragged tail (a multiple of 16 codes, below one
+// chunk) is done by block 0 with vector loads.
+constexpr int kStgWarps = 24;
+constexpr int kStgChunk = 1024;       // codes per warp chunk
+constexpr int kStgStages = 2;
+constexpr int kStgWarpBytes = kStgStages * kStgChunk + 2 * kStgChunk * 2;
+constexpr int kStgSmem = kStgWarps * kStgWarpBytes + kStgWarps * kStgStages * 8 + 128;
 
-__device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 w) {
-    const uint32_t in[2] = {w.x, w.y};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int8_t c0 = static_cast<int8_t>((in[i] >> (16 * h)) & 0xFF);
-            const int8_t c1 = static_cast<int8_t>((in[i] >> (16 * h + 8)) & 0xFF);
-            o[2 * i + h] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(c0))) |
-                           (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(c1))) << 16);
-        }
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__global__ void __launch_bounds__(kStgThreads) i8_to_f16_bulk_kernel(const int8_t* __restrict__ src,
-                                                                    int64_t n,
-                                                                    uint16_t* __restrict__ dst,
-                                                                    unsigned* err_word) {
+__global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const int8_t* __restrict__ src,
+                                                                       int64_t n,
+                                                                       uint16_t* __restrict__ dst,
+                                                                       unsigned* err_word) {
     extern __shared__ uint8_t gsmem_raw[];
     uint8_t* gsmem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(gsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
-    uint8_t* in_buf = gsmem;                                     // 4 x 8 KB
-    uint8_t* out_buf = in_buf + kStgStages * kStgChunk;          // 2 x 16 KB
-    uint64_t* full = reinterpret_cast<uint64_t*>(out_buf + 2 * kStgChunk * 2);
-    __shared__ int s_ok;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* in_buf = gsmem + warp * kStgWarpBytes;              // kStgStages x 1 KB
+    uint8_t* out_buf = in_buf + kStgStages * kStgChunk;          // 2 x 2 KB
+    uint64_t* full = reinterpret_cast<uint64_t*>(gsmem + kStgWarps * kStgWarpBytes) + warp * kStgStages;
     __shared__ int abort_flag;
     const int64_t nfull = n / kStgChunk;
-    const int64_t G = gridDim.x;
-    const int64_t count = blockIdx.x < nfull ? (nfull - blockIdx.x + G - 1) / G : 0;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kStgStages; ++i) mbar_init(&full[i], 1);
-        abort_flag = 0;
+    const int64_t GW = static_cast<int64_t>(gridDim.x) * kStgWarps;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStgWarps + warp;
+    const int64_t count = gw < nfull ? (nfull - gw + GW - 1) / GW : 0;
+    if (threadIdx.x == 0) abort_flag = 0;
+    if (lane == 0) {
+        for (int k = 0; k < kStgStages; ++k) mbar_init(&full[k], 1);
         fence_mbar_init();
-        for (int64_t i = 0; i < count && i < kStgStages; ++i) {
-            mbar_arrive_expect_tx(&full[i], kStgChunk);
-            bulk_load(in_buf + i * kStgChunk, src + (blockIdx.x + i * G) * kStgChunk, kStgChunk, &full[i]);
-        }
     }
     __syncthreads();
+    if (lane == 0) {
+        for (int64_t k = 0; k < count && k < kStgStages; ++k) {
+            mbar_arrive_expect_tx(&full[k], kStgChunk);
+            bulk_load(in_buf + k * kStgChunk, src + (gw + k * GW) * kStgChunk, kStgChunk, &full[k]);
+        }
+    }
     int64_t i = 0;
     for (; i < count; ++i) {
         const int stage = static_cast<int>(i % kStgStages);
         const int ob = static_cast<int>(i & 1);
-        if (threadIdx.x == 0) {
-            s_ok = mbar_wait(&full[stage], static_cast<uint32_t>((i / kStgStages) & 1), &abort_flag, err_word);
-            if (i >= 2) bulk_wait_read<1>();
+        int ok = 1;
+        if (lane == 0) {
+            ok = mbar_wait(&full[stage], static_cast<uint32_t>((i / kStgStages) & 1), &abort_flag, err_word);
+            if (i >= 2) bulk_wait_read<1>();   // the store from out_buf[ob] two chunks ago is read
         }
-        __syncthreads();
-        if (!s_ok) break;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();                          // orders lane 0's wait before the other lanes' reads
+        if (!ok) break;
         const uint8_t* in = in_buf + stage * kStgChunk;
         uint8_t* out = out_buf + ob * kStgChunk * 2;
-        const int t = threadIdx.x;
-        const uint2 w0 = *reinterpret_cast<const uint2*>(in + t * 8);
-        const uint2 w1 = *reinterpret_cast<const uint2*>(in + kStgChunk / 2 + t * 8);
-        *reinterpret_cast<uint4*>(out + t * 16) = i8x8_to_f16x8(w0);
-        *reinterpret_cast<uint4*>(out + kStgChunk + t * 16) = i8x8_to_f16x8(w1);
+        uint2 w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[k] = *reinterpret_cast<const uint2*>(in + (k * 32 + lane) * 8);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(out + (k * 32 + lane) * 16) = i8x8_to_f16x8(w[k]);
         fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const int64_t c = blockIdx.x + i * G;
+        __syncwarp();
+        if (lane == 0) {
+            const int64_t c = gw + i * GW;
             bulk_store(dst + c * kStgChunk, out, kStgChunk * 2);
             bulk_commit();
             if (i + kStgStages < count) {
                 mbar_arrive_expect_tx(&full[stage], kStgChunk);
-                bulk_load(in_buf + stage * kStgChunk, src + (c + kStgStages * G) * kStgChunk, kStgChunk,
+                bulk_load(in_buf + stage * kStgChunk, src + (c + kStgStages * GW) * kStgChunk, kStgChunk,
                           &full[stage]);
             }
         }
     }
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
         if (i < count) {
+            // gave up on a wait: let the loads already issued land before exiting
             for (int64_t j = i; j < count && j < i + kStgStages; ++j)
                 mbar_wait_drain(&full[j % kStgStages], static_cast<uint32_t>((j / kStgStages) & 1));
         }
         bulk_wait_all();
     }
     if (blockIdx.x == 0) {
-        for (int64_t e = nfull * kStgChunk + threadIdx.x * 8; e < n; e += kStgThreads * 8) {
-            const uint2 w = *reinterpret_cast<const uint2*>(src + e);
-            *reinterpret_cast<uint4*>(dst + e) = i8x8_to_f16x8(w);
+        for (int64_t e = nfull * kStgChunk + threadIdx.x * 8; e < n; e += kStgWarps * 32 * 8) {
+            const uint2 v = *reinterpret_cast<const uint2*>(src + e);
+            *reinterpret_cast<uint4*>(dst + e) = i8x8_to_f16x8(v);
         }
     }
 }
@@ -871,12 +867,12 @@ cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        kStgSmem);
         if (attr != cudaSuccess) return attr;
-        int64_t blocks = n / kStgChunk;
-        const int64_t cap = static_cast<int64_t>(sms) * 2;
+        int64_t blocks = (n / kStgChunk + kStgWarps - 1) / kStgWarps;
+        const int64_t cap = static_cast<int64_t>(sms);
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        i8_to_f16_bulk_kernel<<<static_cast<unsigned>(blocks), kStgThreads, kStgSmem, st>>>(src, n, dst,
-                                                                                         err_word);
+        i8_to_f16_bulk_kernel<<<static_cast<unsigned>(blocks), kStgWarps * 32, kStgSmem, st>>>(src, n, dst,
+                                                                                             err_word);
         return cudaGetLastError();
     }
     int64_t blocks = (total + 255) / 256;

@@ -68,8 +68,8 @@ def parse():
 # those sources no longer matches, the bench reports traffic as null.
 PROFILED_TRAFFIC = {
     # profiles/traffic_large_step.md
-    "gemm_fp8_nt": {"bytes": 726742272, "sources_sha256": "c56ec4e9efd6277c7a3d9775807fd6a9c524f8a54435abc1a82788ab85d34edd"},
-    "gemm_i8": {"bytes": 3583950336, "sources_sha256": "c56ec4e9efd6277c7a3d9775807fd6a9c524f8a54435abc1a82788ab85d34edd"},
+    "gemm_fp8_nt": {"bytes": 740345600, "sources_sha256": "06de3db057ad92c91275d35e6c7ba13004559a2238cbafc1ece991545425618d"},
+    "gemm_i8": {"bytes": 3574921472, "sources_sha256": "06de3db057ad92c91275d35e6c7ba13004559a2238cbafc1ece991545425618d"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
