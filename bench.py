@@ -309,28 +309,30 @@ def run_sq(args, rank, world, local_rank):
     q_done = torch.cuda.Event()
     g_done = torch.cuda.Event()
 
-    def step(events=None):
+    def step(events=None, bufs=None):
+        xa, xb, c8, ci = bufs if bufs is not None else (A, B, C8, Ci)
+
         def mark(i, st):
             if events is not None:
                 events[i].record(st)
         mark(0, stream)
-        sq.sq_quantize_fp8(A, tsa, sq.SQ_FMT_E4M3, ws, x8=a8, amax=amax_a, stream=stream)
+        sq.sq_quantize_fp8(xa, tsa, sq.SQ_FMT_E4M3, ws, x8=a8, amax=amax_a, stream=stream)
         mark(1, stream)
-        sq.sq_quantize_fp8(B, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax_b, stream=stream)
+        sq.sq_quantize_fp8(xb, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax_b, stream=stream)
         mark(2, stream)
         q_done.record(stream)
-        sq.sq_gemm_fp8_scaled(a8, b8, tsa, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT, C=C8, stream=stream)
+        sq.sq_gemm_fp8_scaled(a8, b8, tsa, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT, C=c8, stream=stream)
         mark(3, stream)
         g_done.record(stream)
         s_i8.wait_event(q_done)
         mark(7, s_i8)
-        sq.sq_quantize_rowwise_i8(A, q=qa, scales=sA, stream=s_i8)
+        sq.sq_quantize_rowwise_i8(xa, q=qa, scales=sA, stream=s_i8)
         mark(4, s_i8)
-        sq.sq_quantize_rowwise_i8(B, q=qb, scales=sB, stream=s_i8)
+        sq.sq_quantize_rowwise_i8(xb, q=qb, scales=sB, stream=s_i8)
         mark(5, s_i8)
         s_i8.wait_event(g_done)
         mark(8, s_i8)
-        sq.sq_gemm_i8_rowscaled(qa, sA, qb, sB, wsi, C=Ci, stream=s_i8)
+        sq.sq_gemm_i8_rowscaled(qa, sA, qb, sB, wsi, C=ci, stream=s_i8)
         mark(6, s_i8)
         stream.wait_stream(s_i8)
 
@@ -365,35 +367,77 @@ def run_sq(args, rank, world, local_rank):
         raise RuntimeError("device error in the timed region")
 
     # ------------------------------------------------ e2e: host buffers, copies inside
+    # Every step copies its own inputs in from pinned host memory and its two
+    # results out to pinned host memory inside the timed region.  The copies
+    # are pipelined the way a serving loop runs them: step s+1's upload and
+    # step s-1's download run on their own streams (the copy engines) while
+    # step s computes, with double-buffered device inputs and outputs; events
+    # keep a buffer from being overwritten before its consumer is done.
     e2e = None
     if not args.no_e2e:
-        c8_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-        ci_host = torch.empty((M, N), dtype=torch.float32).pin_memory()
-        e_steps = max(2, min(args.steps, 5))
+        c8_host = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        ci_host = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _ in range(2)]
+        bufs = [(A, B, C8, Ci),
+                (torch.empty_like(A), torch.empty_like(B), torch.empty_like(C8), torch.empty_like(Ci))]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        in_free = [torch.cuda.Event() for _ in range(2)]
+        out_ready = [torch.cuda.Event() for _ in range(2)]
+        out_free = [torch.cuda.Event() for _ in range(2)]
+        e_steps = max(2, min(args.steps, 20))
 
-        def e2e_step():
-            A.copy_(a_host, non_blocking=True)
-            B.copy_(b_host, non_blocking=True)
-            step()
-            c8_host.copy_(C8, non_blocking=True)
-            ci_host.copy_(Ci, non_blocking=True)
+        def e2e_run(n):
+            s_in.wait_stream(stream)
+            s_out.wait_stream(stream)
+            for s in range(n):
+                k = s % 2
+                xa, xb, c8, ci = bufs[k]
+                if s >= 2:
+                    s_in.wait_event(in_free[k])      # step s-2 has finished reading xa, xb
+                with torch.cuda.stream(s_in):
+                    xa.copy_(a_host, non_blocking=True)
+                    xb.copy_(b_host, non_blocking=True)
+                in_ready[k].record(s_in)
+                stream.wait_event(in_ready[k])
+                if s >= 2:
+                    stream.wait_event(out_free[k])   # step s-2's results have been read out
+                step(bufs=bufs[k])
+                in_free[k].record(stream)
+                out_ready[k].record(stream)
+                s_out.wait_event(out_ready[k])
+                with torch.cuda.stream(s_out):
+                    c8_host[k].copy_(c8, non_blocking=True)
+                    ci_host[k].copy_(ci, non_blocking=True)
+                out_free[k].record(s_out)
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)
 
-        e2e_step()
+        e2e_run(2)
         torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         if dist:
             dist.barrier()
         e0.record(stream)
-        for _ in range(e_steps):
-            e2e_step()
+        e2e_run(e_steps)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = e0.elapsed_time(e1) / e_steps
         h2d = (a_host.numel() + b_host.numel()) * 2
         d2h = C8.numel() * 2 + Ci.numel() * 4
         e2e = {"ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "unit": UNIT, "value": FLOPS_PER_STEP / (e_ms * 1e-3) / 1e12}
+               "unit": UNIT, "value": FLOPS_PER_STEP / (e_ms * 1e-3) / 1e12, "steps": e_steps,
+               "schedule": "uploads of step s+1 and downloads of step s-1 overlap step s on two "
+                           "copy streams (double-buffered device tensors, pinned host buffers)"}
+        if sq.sq_get_last_device_error() != sq.SQ_OK:
+            raise RuntimeError("device error in the e2e region")
+        # every step has the same inputs: what reached the host must equal the
+        # device-resident results of the timed region (spot rows)
+        for k in range(2):
+            for rows in (slice(0, 64), slice(M - 64, M)):
+                if not (torch.equal(c8_host[k][rows], C8[rows].cpu()) and
+                        torch.equal(ci_host[k][rows], Ci[rows].cpu())):
+                    raise RuntimeError("e2e results differ from the device-resident ones")
 
     # ------------------------------------------------ max over ranks
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e["ms_per_step"] if e2e else 0.0], dist, dev)
