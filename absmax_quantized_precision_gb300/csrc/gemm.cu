@@ -30,6 +30,7 @@
 // and sums the chunks in registers, which keeps the whole K sum exact.
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "sq_device.cuh"
@@ -53,6 +54,7 @@ struct GemmParams {
     const float* sb;       // FP8: scalar step of B; INT8: row scales [batch*N]
     void* C;               // FP8: bf16 [M,N]; INT8: f32, batch stride strideC
     int32_t* acc_out;      // INT8 only (nullable)
+    int tma_store;         // FP8 bf16 output: stage 32x32 boxes in shared memory, store with TMA
     int64_t strideC;
     uint32_t idesc;
     int vec_store;
@@ -85,7 +87,9 @@ struct GemmCfg {
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = STAGES * STAGE + BAR_BYTES + 1024;
+    // FP8: two 32 x 32 bf16 output boxes (2 KB each) per epilogue warp
+    static constexpr int EPI_STAGE = I8 ? 0 : EPI_WARPS * 2 * 2048;
+    static constexpr int SMEM = STAGES * STAGE + EPI_STAGE + BAR_BYTES + 1024;
     // bytes the start address moves per MMA instruction along K
     static constexpr int KSTEP_K = 32;                      // K-major: 32 B inside the row
     static constexpr int KSTEP_MN = (I8 ? 16 : 32) * 128;   // MN-major: that many K rows
@@ -108,19 +112,23 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& b, 
     nb = rr / gm;
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+// Two floats to two bf16 (RN) in one word, lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE);
+    uint8_t* epi_stage = smem + Cfg::STAGES * Cfg::STAGE;     // 1024-aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_stage + Cfg::EPI_STAGE);
     uint64_t* empty = full + Cfg::STAGES;
     uint64_t* tfull = empty + Cfg::STAGES;
     uint64_t* tempty = tfull + 2;
@@ -151,6 +159,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (!I8 && p.tma_store) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -331,6 +340,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
             }
         }
         uint32_t it = 0;
+        uint32_t sc = 0;                       // output boxes this warp has stored
         bool ok = true;
         auto release = [&](uint32_t ab) {
             tc_fence_before();
@@ -481,13 +491,38 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                                 if (col0 + i < p.N)
                                     C8[obase + col0 + i] = static_cast<uint8_t>(pk[i >> 2] >> (8 * (i & 3)));
                         }
+                    } else if (!p.out_e4m3 && p.tma_store) {
+                        // The warp's 32 rows x 32 columns go out as one TMA box: each
+                        // lane writes its 64-byte row into a 64-byte-swizzled staging
+                        // buffer (16-byte piece j of row r sits at piece j ^ ((r >> 1) & 3),
+                        // which keeps the writes conflict-free); rows or columns past
+                        // the matrix are clipped by the store.
+                        uint8_t* buf = epi_stage + (ew * 2 + (sc & 1u)) * 2048;
+                        if (lane == 0 && sc >= 2) bulk_wait_read<1>();   // the box two back is read
+                        __syncwarp();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = bf16x2_bits(__fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), esa), esb),
+                                                __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), esa), esb));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, buf, col0, m0 + quarter * 32);
+                            bulk_commit();
+                        }
+                        ++sc;
                     } else if (row < p.M) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const float lo = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), esa), esb);
                             const float hi = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), esa), esb);
-                            pk[i] = bf16_bits(lo) | (bf16_bits(hi) << 16);
+                            pk[i] = bf16x2_bits(lo, hi);
                         }
                         if (p.vec_store && col0 + 32 <= p.N) {
 #pragma unroll
@@ -507,6 +542,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                 ++it;
             }
         }
+        // the staged output boxes must be written (and their buffers read) before exit
+        if (!I8 && lane == 0 && sc > 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -546,7 +583,8 @@ static EncodeTiledFn encode_fn() {
 // Row-major [outer, inner] (inner contiguous, row pitch `pitch` bytes), tiles
 // of box_inner x box_outer elements, 128-byte swizzle, zero fill outside.
 static bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                      uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+                      uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -554,7 +592,7 @@ static bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
     return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -573,8 +611,8 @@ static bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
 }
 
 template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
-static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                            cudaStream_t st, int sms) {
+static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                            const GemmParams& p, cudaStream_t st, int sms) {
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
     auto kern = gemm_tc_kernel<BN, I8, A_MN, B_MN, PAIR>;
     static std::once_flag once;
@@ -607,7 +645,7 @@ static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
     const int total = p.mt * p.nt * p.batch;
     const int units = total < max_units ? total : max_units;
     if (!PAIR) {
-        kern<<<units, Cfg::THREADS, Cfg::SMEM, st>>>(ta, tb, p);
+        kern<<<units, Cfg::THREADS, Cfg::SMEM, st>>>(ta, tb, tc, p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -622,7 +660,7 @@ static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
 }
 
 // Tile shape: 256 x 256 on CTA pairs when there are enough such tiles to give
@@ -653,7 +691,17 @@ static cudaError_t gemm_fp8_shape(const uint8_t* A, const uint8_t* B, int M, int
     p.nt = (N + BN - 1) / BN;
     p.idesc = idesc_make(static_cast<uint32_t>(fmt), static_cast<uint32_t>(fmt), A_MN, B_MN,
                          Cfg::TILE_M, BN);
-    return run_gemm<BN, false, A_MN, B_MN, PAIR>(ta, tb, p, st, sms);
+    // bf16 output leaves through 32 x 32 TMA boxes when its rows are 16-byte multiples
+    CUtensorMap tc;
+    memset(&tc, 0, sizeof(tc));
+    p.tma_store = 0;
+    if (!p.out_e4m3 && N % 8 == 0 && reinterpret_cast<uintptr_t>(p.C) % 16 == 0) {
+        if (!encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C, N, M, static_cast<uint64_t>(N) * 2,
+                       32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+        p.tma_store = 1;
+    }
+    return run_gemm<BN, false, A_MN, B_MN, PAIR>(ta, tb, tc, p, st, sms);
 }
 
 template <bool A_MN, bool B_MN>
@@ -704,7 +752,13 @@ static cudaError_t gemm_i8_shape(const uint16_t* A16, const uint16_t* B16, int b
     p.mt = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
     p.nt = (N + BN - 1) / BN;
     p.idesc = idesc_make(0, 0, false, false, Cfg::TILE_M, BN);   // F16 x F16 -> F32
-    return run_gemm<BN, true, false, false, PAIR>(ta, tb, p, st, sms);
+    // The INT8 epilogue stores from the threads: TMA stores of its fp32 boxes
+    // (twice the bytes of the FP8 output, from 8 warps) measured 17% slower on
+    // the large workload, competing with the operand loads for the TMA unit.
+    CUtensorMap tc;
+    memset(&tc, 0, sizeof(tc));
+    p.tma_store = 0;
+    return run_gemm<BN, true, false, false, PAIR>(ta, tb, tc, p, st, sms);
 }
 
 cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
