@@ -916,7 +916,9 @@ cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int
     const int64_t total = batch * rows * (K / 16);
     if (total == 0) return cudaSuccess;
     const int64_t n = batch * rows * K;
-    if (err_word && (stride == rows * K || batch == 1) && n >= static_cast<int64_t>(kStgChunk) * sms) {
+    // the per-warp pipeline pays off from about 8192 codes per SM; smaller
+    // tensors take the plain grid-stride kernel (no large shared-memory carveout)
+    if (err_word && (stride == rows * K || batch == 1) && n >= static_cast<int64_t>(8192) * sms) {
         static cudaError_t attr = cudaFuncSetAttribute(i8_to_f16_bulk_kernel,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        kStgSmem);

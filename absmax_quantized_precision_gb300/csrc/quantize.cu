@@ -539,7 +539,8 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
     const int lane = threadIdx.x & 31;
     uint8_t* in_buf = qsmem + warp * kFWarpBytes;              // kFStages x 2 KB
     uint8_t* out_buf = in_buf + kFStages * kFChunk * 2;        // 2 x 1 KB
-    uint64_t* full = reinterpret_cast<uint64_t*>(qsmem + kFWarps * kFWarpBytes) + warp * kFStages;
+    const int nwarps = static_cast<int>(blockDim.x >> 5);    // kFWarps, or fewer for small tensors
+    uint64_t* full = reinterpret_cast<uint64_t*>(qsmem + nwarps * kFWarpBytes) + warp * kFStages;
     __shared__ float red[kFWarps];
     __shared__ int is_last;
     __shared__ float s_amax;
@@ -552,8 +553,8 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
     float m = 0.0f;
 
     const int64_t nfull = n / kFChunk;
-    const int64_t GW = static_cast<int64_t>(gridDim.x) * kFWarps;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kFWarps + warp;
+    const int64_t GW = static_cast<int64_t>(gridDim.x) * nwarps;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t count = gw < nfull ? (nfull - gw + GW - 1) / GW : 0;
     if (threadIdx.x == 0) abort_flag = 0;
     if (lane == 0) {
@@ -629,7 +630,7 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
     __syncthreads();
     if (threadIdx.x == 0) {
         float bm = red[0];
-        for (int w = 1; w < kFWarps; ++w) bm = fmaxf(bm, red[w]);
+        for (int w = 1; w < nwarps; ++w) bm = fmaxf(bm, red[w]);
         // max|x| >= 0, so the float order equals the unsigned order of the bits
         atomicMax(&ws[0], __float_as_uint(bm));
         __threadfence();
@@ -654,7 +655,7 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
         if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = wm;
         __syncthreads();
         if (threadIdx.x == 0) {
-            for (int w = 0; w < kFWarps; ++w) wm = fmaxf(wm, red[w]);
+            for (int w = 0; w < nwarps; ++w) wm = fmaxf(wm, red[w]);
             ring[ring_idx] = a;
             if (wm > 0.0f) {
                 const float fmax_v = FMT == 0 ? 448.0f : 57344.0f;
@@ -674,11 +675,15 @@ static cudaError_t launch_fp8_fmt(const uint16_t* x, int64_t n, const float* sca
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
     if (attr != cudaSuccess) return attr;
     const int64_t nfull = n / kFChunk;
-    int64_t blocks = (nfull + kFWarps - 1) / kFWarps;
+    // Small tensors (under one chunk per warp of a full grid) run CTAs of 8
+    // warps, several per SM, which start faster than one 24-warp CTA per SM.
+    const int warps = nfull < static_cast<int64_t>(sms) * kFWarps ? 8 : kFWarps;
+    const int smem = warps * kFWarpBytes + warps * kFStages * 8 + 128;
+    int64_t blocks = (nfull + warps - 1) / warps;
     if (blocks < 1) blocks = 1;
-    const int64_t cap = static_cast<int64_t>(sms);
+    const int64_t cap = static_cast<int64_t>(sms) * (warps == kFWarps ? 1 : 3);
     if (blocks > cap) blocks = cap;
-    quant_fp8_kernel<FMT><<<static_cast<unsigned>(blocks), kFWarps * 32, kQSmem, st>>>(
+    quant_fp8_kernel<FMT><<<static_cast<unsigned>(blocks), warps * 32, smem, st>>>(
         x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin, err_word);
     return cudaGetLastError();
 }

@@ -167,6 +167,21 @@ def test_fp8_gemm_layouts(name, M, N, K, layout):
     assert guard_intact(cbuf, n, 3.0)
 
 
+@pytest.mark.parametrize("N", [100, 104, 2056], ids=["N100 thread stores", "N104 clipped box", "N2056 pair"])
+def test_fp8_gemm_nt_output_widths(N):
+    """Output rows that are not a multiple of 8 bf16 are stored by the threads;
+    multiples of 8 leave through 32x32 TMA boxes whose last column box is
+    clipped.  The guard band after C must stay untouched either way."""
+    M, K = 2304 if N > 1000 else 136, 256   # 2304 x 2056: 81 tile pairs, the CTA-pair kernel
+    fmt = sq.SQ_FMT_E4M3
+    a8, b8, sa, sb = fp8_inputs(f"width {N}", M, N, K, fmt)
+    C, cbuf, n = guarded((M, N), torch.bfloat16, -2.0)
+    sq.sq_gemm_fp8_scaled(to_dev(a8), to_dev(b8), torch.tensor([sa], device=DEV),
+                          torch.tensor([sb], device=DEV), fmt, sq.SQ_NT, C=C)
+    check_fp8(C, a8, b8, fmt, sq.SQ_NT, K, sa, sb)
+    assert guard_intact(cbuf, n, -2.0)
+
+
 @pytest.mark.parametrize("layout", [sq.SQ_NT, sq.SQ_NN, sq.SQ_TN], ids=["NT", "NN", "TN"])
 def test_fp8_gemm_e5m2(layout):
     M, N, K = 256, 256, 1024
