@@ -68,8 +68,8 @@ def parse():
 # those sources no longer matches, the bench reports traffic as null.
 PROFILED_TRAFFIC = {
     # profiles/traffic_large_step.md
-    "gemm_fp8_nt": {"bytes": 740345600, "sources_sha256": "06de3db057ad92c91275d35e6c7ba13004559a2238cbafc1ece991545425618d"},
-    "gemm_i8": {"bytes": 3574921472, "sources_sha256": "06de3db057ad92c91275d35e6c7ba13004559a2238cbafc1ece991545425618d"},
+    "gemm_fp8_nt": {"bytes": 756712960, "sources_sha256": "2962dee73e47a37a8e9ac508247cd83c91eecdc7bcbdd308fe55028bd2787cfd"},
+    "gemm_i8": {"bytes": 3662025216, "sources_sha256": "2962dee73e47a37a8e9ac508247cd83c91eecdc7bcbdd308fe55028bd2787cfd"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
@@ -681,10 +681,29 @@ def run_small_config(name, args):
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error in graph replay")
     graph_ms = statistics.median(gev[i][0].elapsed_time(gev[i][1]) for i in range(iters))
+    # Each call alone, captured as its own graph and replayed after an L2
+    # flush: its device time plus one launch, with no host submission gap
+    # (the eager per-call times above include the Python binding's).
+    op_graph_ms = []
+    for _, _, _, fn in ops:
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1):
+            fn()
+        g1.replay()
+        torch.cuda.synchronize(dev)
+        oev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
+        for it in range(iters):
+            flush.fill_(it & 0xFF)
+            oev[it][0].record(stream)
+            g1.replay()
+            oev[it][1].record(stream)
+        torch.cuda.synchronize(dev)
+        op_graph_ms.append(statistics.median(oev[i][0].elapsed_time(oev[i][1]) for i in range(iters)))
+    if sq.sq_get_last_device_error() != sq.SQ_OK:
+        raise RuntimeError("device error in per-call graph replay")
     pk = peaks()
-    kernels = {}
-    for j, (label, kind, amount, _) in enumerate(ops):
-        ms = statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(iters))
+
+    def rates(label, kind, amount, ms):
         d = {"us": 1e3 * ms}
         if kind == "bytes":
             d["GB/s"] = amount / (ms * 1e-3) / 1e9
@@ -694,7 +713,14 @@ def run_small_config(name, args):
             d["TFLOP/s"] = tf
             is_fp8 = "fp8" in label or label.startswith(("ours_", "cublaslt_", "linear_"))
             d["frac_peak"] = tf / ((2.0 if is_fp8 else 1.0) * pk["bf16_sustained"])
-        kernels[label] = d
+        return d
+
+    kernels = {}
+    kernels_graph = {}
+    for j, (label, kind, amount, _) in enumerate(ops):
+        ms = statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(iters))
+        kernels[label] = rates(label, kind, amount, ms)
+        kernels_graph[label] = rates(label, kind, amount, op_graph_ms[j])
     line = {"metric": METRIC, "config": {"workload": name, "desc": desc,
                                          "l2": "flushed before every pass"},
             "value": gemm_flops / (graph_ms * 1e-3) / 1e12, "unit": UNIT,
@@ -702,7 +728,7 @@ def run_small_config(name, args):
             "us_per_step_eager": 1e3 * step_ms,
             "value_eager": gemm_flops / (step_ms * 1e-3) / 1e12,
             "calls_per_step": len(ops),
-            "iters": iters, "kernels_eager": kernels,
+            "iters": iters, "kernels_eager": kernels, "kernels_graph": kernels_graph,
             "clocks": clk.summary(),
             "cpu_oracle": None if cpu is None else {"seconds": cpu, "cores": oracle.num_threads(),
                                                      "sample": "the whole workload"}}
