@@ -127,11 +127,15 @@ sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, u
                                              reinterpret_cast<cudaStream_t>(stream), ds->sms));
 }
 
+// fp16 copies of A and B, then 2 x 256 words of staging bounds
+constexpr size_t kI8BoundBytes = 2 * 256 * sizeof(unsigned);
+
 size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K) {
     if (batch <= 0 || M <= 0 || N <= 0 || K <= 0) return 0;
     const size_t a = static_cast<size_t>(batch) * M * K * 2;
     const size_t b = static_cast<size_t>(batch) * N * K * 2;
-    return ((a + 255) & ~static_cast<size_t>(255)) + ((b + 255) & ~static_cast<size_t>(255));
+    return ((a + 255) & ~static_cast<size_t>(255)) + ((b + 255) & ~static_cast<size_t>(255)) +
+           kI8BoundBytes;
 }
 
 namespace {
@@ -163,15 +167,21 @@ sq_status gemm_i8_common(const int8_t* A, const float* sA, int64_t ga, const int
     uint16_t* A16 = static_cast<uint16_t*>(workspace);
     const size_t abytes = (static_cast<size_t>(batch) * M * K * 2 + 255) & ~static_cast<size_t>(255);
     uint16_t* B16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + abytes);
-    e = sq::launch_i8_to_f16(A, batch, M, K, strideA, A16, ds->err_word, st, ds->sms);
+    const size_t bbytes = (static_cast<size_t>(batch) * N * K * 2 + 255) & ~static_cast<size_t>(255);
+    unsigned* bound_a = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + abytes + bbytes);
+    unsigned* bound_b = bound_a + 256;
+    int nparts_a = 0, nparts_b = 0;
+    e = sq::launch_i8_to_f16(A, batch, M, K, strideA, A16, bound_a, &nparts_a, ds->err_word, st,
+                             ds->sms);
     if (e != cudaSuccess) return SQ_ERR_CUDA;
-    e = sq::launch_i8_to_f16(B, batch, N, K, strideB, B16, ds->err_word, st, ds->sms);
+    e = sq::launch_i8_to_f16(B, batch, N, K, strideB, B16, bound_b, &nparts_b, ds->err_word, st,
+                             ds->sms);
     if (e != cudaSuccess) return SQ_ERR_CUDA;
     return from_cuda(sq::launch_gemm_i8(A16, B16, sA, sB, static_cast<int>(ga),
                                         static_cast<int>(gb), static_cast<int>(batch),
                                         static_cast<int>(M), static_cast<int>(N),
-                                        static_cast<int>(K), strideC, C, acc_out, ds->err_word, st,
-                                        ds->sms));
+                                        static_cast<int>(K), strideC, C, acc_out, bound_a,
+                                        nparts_a, bound_b, nparts_b, ds->err_word, st, ds->sms));
 }
 
 }  // namespace

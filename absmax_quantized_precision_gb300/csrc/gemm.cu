@@ -42,6 +42,8 @@ constexpr int kBM = 128;
 constexpr int kBKBytes = 128;   // bytes of K per stage row (one 128-B swizzle row)
 constexpr int kGroupM = 16;
 constexpr int kI8ChunkK = 1024; // K elements per exact FP32 chunk
+constexpr int kStgChunk = 1024; // codes per warp chunk of the INT8 staging pipeline
+constexpr int kStgMaxParts = 256; // per-CTA bound slots per operand (>= staging CTAs)
 
 struct GemmParams {
     int M, N, K;
@@ -55,6 +57,13 @@ struct GemmParams {
     void* C;               // FP8: bf16 [M,N]; INT8: f32, batch stride strideC
     int32_t* acc_out;      // INT8 only (nullable)
     int tma_store;         // FP8 bf16 output: stage 32x32 boxes in shared memory, store with TMA
+    // INT8: per-CTA maxima, written by the staging launches, of the sum of
+    // squared codes over any staged chunk of kStgChunk codes (nparts == 0:
+    // unknown), and how many such chunks one row can overlap
+    const unsigned* bound_a;
+    const unsigned* bound_b;
+    int nparts_a, nparts_b;
+    int row_chunks_a, row_chunks_b;
     int64_t strideC;
     uint32_t idesc;
     int vec_store;
@@ -94,7 +103,7 @@ struct GemmCfg {
     static constexpr int KSTEP_K = 32;                      // K-major: 32 B inside the row
     static constexpr int KSTEP_MN = (I8 ? 16 : 32) * 128;   // MN-major: that many K rows
     static constexpr int MN_LBO = kBKBytes * 128;           // 16 KB between 128-B column blocks
-    static_assert(2 * STAGES * 8 + 5 * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(2 * STAGES * 8 + 5 * 8 + 16 <= BAR_BYTES, "barrier area");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(!B_MN || B_ROWS % 128 == 0, "MN-major B is staged in 128-column blocks");
 };
@@ -135,6 +144,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    unsigned* bound_max = reinterpret_cast<unsigned*>(tmem_slot + 2);   // INT8: [A, B]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -161,6 +171,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
         tma_prefetch_desc(&tmB);
         if (!I8 && p.tma_store) tma_prefetch_desc(&tmC);
     }
+    if (I8 && (warp == 2 || warp == 3)) {
+        const unsigned* src = warp == 2 ? p.bound_a : p.bound_b;
+        const int np = warp == 2 ? p.nparts_a : p.nparts_b;
+        unsigned m = 0u;
+        for (int i = lane; i < np; i += 32) m = max(m, src[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) bound_max[warp - 2] = m;
+    }
     if (warp == 1) {
         if (PAIR) {
             tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
@@ -178,6 +197,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     }
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+
+    // INT8 exactness.  Every partial sum the tensor core forms for C[i,j] is an
+    // integer of magnitude at most sum_k |a_ik b_jk| <= |a_i|_2 |b_j|_2
+    // (Cauchy-Schwarz), and |a_i|_2^2 <= row_chunks_a * (largest sum of
+    // squares over a staged chunk).  When the product of the two bounds is
+    // below 2^48, every partial sum stays below 2^24 and is exact in fp32 in
+    // any order, so the whole K is accumulated in one chunk; otherwise the
+    // accumulator is drained into int32 every kI8ChunkK (127^2 * 1024 < 2^24).
+    int kbpc = p.kb_per_chunk, nch = p.nchunks;
+    if (I8 && p.nparts_a > 0 && p.nparts_b > 0) {
+        const unsigned long long a2 = static_cast<unsigned long long>(p.row_chunks_a) * bound_max[0];
+        const unsigned long long b2 = static_cast<unsigned long long>(p.row_chunks_b) * bound_max[1];
+        if (a2 * b2 < (1ull << 48)) {
+            kbpc = p.nkb;
+            nch = 1;
+        }
+    }
 
     const int total = p.mt * p.nt * p.batch;
 
@@ -262,7 +298,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
             bool ok = true;
             bool issued = false;
             for (int t = cta_unit; t < total && ok; t += num_units) {
-                for (int ch = 0; ch < p.nchunks && ok; ++ch) {
+                for (int ch = 0; ch < nch && ok; ++ch) {
                     const uint32_t ab = it & 1u;
                     const uint32_t aph = (it >> 1) & 1u;
                     if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, p.err_word)) {
@@ -271,8 +307,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + ab * BN;
-                    const int kb0 = ch * p.kb_per_chunk;
-                    const int kb1 = min(p.nkb, kb0 + p.kb_per_chunk);
+                    const int kb0 = ch * kbpc;
+                    const int kb1 = min(p.nkb, kb0 + kbpc);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&full[stage], phase, abort_flag, p.err_word)) {
                             ok = false;
@@ -363,7 +399,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                 for (int c = 0; c < NC; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) sums[c][i] = 0;
-                for (int ch = 0; ch < p.nchunks; ++ch) {
+                for (int ch = 0; ch < nch; ++ch) {
                     const uint32_t ab = it & 1u;
                     const uint32_t aph = (it >> 1) & 1u;
                     if (!mbar_wait(&tfull[ab], aph, abort_flag, p.err_word)) {
@@ -763,8 +799,9 @@ static cudaError_t gemm_i8_shape(const uint16_t* A16, const uint16_t* B16, int b
 
 cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
                            const float* sB, int ga, int gb, int batch, int M, int N, int K,
-                           int64_t strideC, float* C, int32_t* acc_out, unsigned* err_word,
-                           cudaStream_t st, int sms) {
+                           int64_t strideC, float* C, int32_t* acc_out, const unsigned* bound_a,
+                           int nparts_a, const unsigned* bound_b, int nparts_b,
+                           unsigned* err_word, cudaStream_t st, int sms) {
     const int bk = kBKBytes / 2;
     GemmParams p{};
     p.M = M; p.N = N; p.K = K; p.batch = batch;
@@ -780,6 +817,12 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
                   (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0);
     p.sb_vec = (gb == 1) && (N % 4 == 0) && (reinterpret_cast<uintptr_t>(sB) % 16 == 0);
     p.err_word = err_word;
+    p.bound_a = bound_a;
+    p.bound_b = bound_b;
+    p.nparts_a = bound_a ? nparts_a : 0;
+    p.nparts_b = bound_b ? nparts_b : 0;
+    // a row of K codes overlaps at most ceil(K / chunk) + 1 staged chunks
+    p.row_chunks_a = p.row_chunks_b = (K + kStgChunk - 1) / kStgChunk + 1;
     if (pick_shape(M, N, batch, sms) == Shape::Pair256)
         return gemm_i8_shape<256, true>(A16, B16, batch, M, N, K, p, st, sms);
     return gemm_i8_shape<256, false>(A16, B16, batch, M, N, K, p, st, sms);
@@ -828,7 +871,6 @@ __global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict
 // shared-memory access).  The ragged tail (a multiple of 16 codes, below one
 // chunk) is done by block 0 with vector loads.
 constexpr int kStgWarps = 24;
-constexpr int kStgChunk = 1024;       // codes per warp chunk
 constexpr int kStgStages = 2;
 constexpr int kStgWarpBytes = kStgStages * kStgChunk + 2 * kStgChunk * 2;
 constexpr int kStgSmem = kStgWarps * kStgWarpBytes + kStgWarps * kStgStages * 8 + 128;
@@ -836,6 +878,7 @@ constexpr int kStgSmem = kStgWarps * kStgWarpBytes + kStgWarps * kStgStages * 8 
 __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const int8_t* __restrict__ src,
                                                                        int64_t n,
                                                                        uint16_t* __restrict__ dst,
+                                                                       unsigned* __restrict__ parts,
                                                                        unsigned* err_word) {
     extern __shared__ uint8_t gsmem_raw[];
     uint8_t* gsmem = reinterpret_cast<uint8_t*>(
@@ -846,11 +889,17 @@ __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const in
     uint8_t* out_buf = in_buf + kStgStages * kStgChunk;          // 2 x 2 KB
     uint64_t* full = reinterpret_cast<uint64_t*>(gsmem + kStgWarps * kStgWarpBytes) + warp * kStgStages;
     __shared__ int abort_flag;
+    __shared__ unsigned warp_max[kStgWarps];
+    __shared__ unsigned tail_sq;
+    unsigned chunk_max = 0u;       // largest sum of squared codes over this warp's chunks
     const int64_t nfull = n / kStgChunk;
     const int64_t GW = static_cast<int64_t>(gridDim.x) * kStgWarps;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStgWarps + warp;
     const int64_t count = gw < nfull ? (nfull - gw + GW - 1) / GW : 0;
-    if (threadIdx.x == 0) abort_flag = 0;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        tail_sq = 0u;
+    }
     if (lane == 0) {
         for (int k = 0; k < kStgStages; ++k) mbar_init(&full[k], 1);
         fence_mbar_init();
@@ -881,6 +930,15 @@ __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const in
         for (int k = 0; k < 4; ++k) w[k] = *reinterpret_cast<const uint2*>(in + (k * 32 + lane) * 8);
 #pragma unroll
         for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(out + (k * 32 + lane) * 16) = i8x8_to_f16x8(w[k]);
+        int sq = 0;                // sum of squares of this lane's 32 codes (<= 32 * 127^2)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            sq = __dp4a(static_cast<int>(w[k].x), static_cast<int>(w[k].x), sq);
+            sq = __dp4a(static_cast<int>(w[k].y), static_cast<int>(w[k].y), sq);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        chunk_max = max(chunk_max, static_cast<unsigned>(sq));
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -902,17 +960,32 @@ __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const in
         }
         bulk_wait_all();
     }
+    if (lane == 0) warp_max[warp] = chunk_max;
     if (blockIdx.x == 0) {
+        // the ragged tail (< one chunk) counts as one more chunk
+        int tq = 0;
         for (int64_t e = nfull * kStgChunk + threadIdx.x * 8; e < n; e += kStgWarps * 32 * 8) {
             const uint2 v = *reinterpret_cast<const uint2*>(src + e);
             *reinterpret_cast<uint4*>(dst + e) = i8x8_to_f16x8(v);
+            tq = __dp4a(static_cast<int>(v.x), static_cast<int>(v.x), tq);
+            tq = __dp4a(static_cast<int>(v.y), static_cast<int>(v.y), tq);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tq += __shfl_xor_sync(0xffffffffu, tq, o);
+        if (lane == 0 && tq != 0) atomicAdd(&tail_sq, static_cast<unsigned>(tq));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && parts) {
+        unsigned m = tail_sq;
+        for (int w = 0; w < kStgWarps; ++w) m = max(m, warp_max[w]);
+        parts[blockIdx.x] = m;
     }
 }
 
 cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
-                             int64_t stride, uint16_t* dst, unsigned* err_word, cudaStream_t st,
-                             int sms) {
+                             int64_t stride, uint16_t* dst, unsigned* parts, int* nparts,
+                             unsigned* err_word, cudaStream_t st, int sms) {
+    if (nparts) *nparts = 0;
     const int64_t total = batch * rows * (K / 16);
     if (total == 0) return cudaSuccess;
     const int64_t n = batch * rows * K;
@@ -924,11 +997,13 @@ cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int
                                                        kStgSmem);
         if (attr != cudaSuccess) return attr;
         int64_t blocks = (n / kStgChunk + kStgWarps - 1) / kStgWarps;
-        const int64_t cap = static_cast<int64_t>(sms);
+        int64_t cap = static_cast<int64_t>(sms);
+        if (cap > kStgMaxParts) cap = kStgMaxParts;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        i8_to_f16_bulk_kernel<<<static_cast<unsigned>(blocks), kStgWarps * 32, kStgSmem, st>>>(src, n, dst,
-                                                                                             err_word);
+        i8_to_f16_bulk_kernel<<<static_cast<unsigned>(blocks), kStgWarps * 32, kStgSmem, st>>>(
+            src, n, dst, parts, err_word);
+        if (nparts) *nparts = static_cast<int>(blocks);
         return cudaGetLastError();
     }
     int64_t blocks = (total + 255) / 256;

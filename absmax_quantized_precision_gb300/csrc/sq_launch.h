@@ -26,9 +26,13 @@ cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale
                                 int sms);
 
 // Staging of INT8 codes as exact fp16 values: dst[b][r][k] = src[b*stride + r*K + k].
+// When the bulk pipeline runs (contiguous and large), each of its *nparts
+// CTAs writes to parts[cta] the largest sum of squared codes over any of its
+// 1024-code chunks (the ragged tail counts as one chunk); otherwise *nparts
+// is 0.  parts holds at least 256 words.
 cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
-                             int64_t stride, uint16_t* dst, unsigned* err_word, cudaStream_t st,
-                             int sms);
+                             int64_t stride, uint16_t* dst, unsigned* parts, int* nparts,
+                             unsigned* err_word, cudaStream_t st, int sms);
 
 // 0 on success, a cudaError_t otherwise; CUDA_ERROR_* from tensor-map encoding
 // is reported as cudaErrorInvalidValue.
@@ -49,10 +53,13 @@ cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, int spli
                                float* partial, uint16_t* gb, cudaStream_t st);
 
 // Scales of row i of A in batch b: sA[b*ceil(M/ga) + i/ga] (ga = 1: per row).
+// bound_a / bound_b: the staging launches' parts (nparts 0: not available);
+// when they prove every partial sum exact in fp32, K runs as one chunk.
 cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
                            const float* sB, int ga, int gb, int batch, int M, int N, int K,
-                           int64_t strideC, float* C, int32_t* acc_out, unsigned* err_word,
-                           cudaStream_t st, int sms);
+                           int64_t strideC, float* C, int32_t* acc_out, const unsigned* bound_a,
+                           int nparts_a, const unsigned* bound_b, int nparts_b,
+                           unsigned* err_word, cudaStream_t st, int sms);
 
 // One CTA waits on a barrier phase that never completes, for limit_ns.
 cudaError_t launch_selftest_wait(unsigned* err_word, unsigned long long limit_ns, cudaStream_t st);

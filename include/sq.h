@@ -149,8 +149,10 @@ sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, u
                                void* workspace, sq_stream stream);
 
 /*
- * Bytes of workspace that sq_gemm_i8_rowscaled needs for these sizes (the
- * INT8 codes are staged as exact 16-bit values for the tensor cores).
+ * Bytes of workspace that sq_gemm_i8_rowscaled needs for these sizes: the
+ * INT8 codes staged as exact 16-bit values for the tensor cores, plus 2 KB in
+ * which the staging records bounds on the codes' sums of squares (used to
+ * skip the exactness drains when they cannot be needed).
  */
 size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K);
 

@@ -43,7 +43,8 @@ def test_status_strings_and_sizes(lib):
     for s in range(6):
         assert sq.status_string(s).startswith("SQ_")
     assert sq.workspace_bytes() >= 8
-    assert sq.gemm_i8_workspace_bytes(1, 128, 512, 1024) == 128 * 1024 * 2 + 512 * 1024 * 2
+    # fp16 copies of A and B, then 2 x 256 words of staging bounds
+    assert sq.gemm_i8_workspace_bytes(1, 128, 512, 1024) == 128 * 1024 * 2 + 512 * 1024 * 2 + 2048
     assert sq.gemm_i8_workspace_bytes(0, 1, 1, 1) == 0
 
 

@@ -108,6 +108,25 @@ def test_i8_gemm_random_codes_and_acc_only():
 
 
 # ------------------------------------------------------------------ FP8
+@pytest.mark.parametrize("c", [42, 47], ids=["bound holds: one K chunk", "bound fails: drained"])
+def test_i8_exactness_with_and_without_drains(c):
+    """Constant codes c at K = 8192 (staged by the bulk pipeline).  With c = 42
+    the staging bound proves every partial sum below 2^24, so K runs as one
+    fp32 chunk; with c = 47 the sums reach 8192 * 47^2 > 2^24 with odd steps,
+    which only the per-1024-K drains keep exact.  Both must be bit-exact."""
+    M, N, K = 256, 320, 8192
+    qa = np.full((M, K), c, dtype=np.int8)
+    qb = np.full((N, K), c, dtype=np.int8)
+    qa[::3] = -c                                   # signs vary by row
+    sa = np.linspace(0.5, 2.0, M).astype(np.float32)
+    sb = np.linspace(0.25, 1.0, N).astype(np.float32)
+    oacc, oC = oracle.gemm_i8(qa, qb, sa, sb)
+    assert np.abs(oacc).max() == K * c * c
+    C, acc = run_i8(qa, sa, qb, sb)
+    assert np.array_equal(acc, oacc)
+    assert np.array_equal(C.view(np.uint32), oC.view(np.uint32))
+
+
 def fp8_inputs(name, M, N, K, fmt, std_a=1.0, std_b=0.02):
     s = seed_of(name)
     xa = synth.normal(s, (M, K), std=std_a, dtype=synth.BF16)
