@@ -40,7 +40,8 @@ namespace sq {
 
 constexpr int kBM = 128;
 constexpr int kBKBytes = 128;   // bytes of K per stage row (one 128-B swizzle row)
-constexpr int kGroupM = 16;
+constexpr int kGroupM = 16;      // FP8: tile rows per raster group
+constexpr int kGroupMI8 = 8;     // INT8: its 16-bit operand stripes are twice as large
 constexpr int kI8ChunkK = 1024; // K elements per exact FP32 chunk
 constexpr int kStgChunk = 1024; // codes per warp chunk of the INT8 staging pipeline
 constexpr int kStgMaxParts = 256; // per-CTA bound slots per operand (>= staging CTAs)
@@ -56,6 +57,7 @@ struct GemmParams {
     const float* sb;       // FP8: scalar step of B; INT8: row scales [batch*N]
     void* C;               // FP8: bf16 [M,N]; INT8: f32, batch stride strideC
     int32_t* acc_out;      // INT8 only (nullable)
+    int group_m;           // tile rows per raster group
     int tma_store;         // FP8 bf16 output: stage 32x32 boxes in shared memory, store with TMA
     // INT8: per-CTA maxima, written by the staging launches, of the sum of
     // squared codes over any staged chunk of kStgChunk codes (nparts == 0:
@@ -87,7 +89,8 @@ struct GemmCfg {
     static constexpr int A_BYTES = kBM * kBKBytes;              // 16 KB
     static constexpr int B_BYTES = B_ROWS * kBKBytes;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (STAGE >= 48 * 1024) ? 4 : 6;
+    // INT8 pair/128-wide tiles take a 7th stage (no output staging buffer there)
+    static constexpr int STAGES = (STAGE >= 48 * 1024) ? 4 : (I8 ? 7 : 6);
     static constexpr int TILE_M = PAIR ? 2 * kBM : kBM;
     // INT8 keeps its running int32 sums in registers: 8 epilogue warps, each
     // owning 32 rows x EPI_COLS columns of the tile.
@@ -112,10 +115,10 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& b, 
     const int per = p.mt * p.nt;
     b = t / per;
     const int r = t - b * per;
-    const int gsz = kGroupM * p.nt;
+    const int gsz = p.group_m * p.nt;
     const int g = r / gsz;
-    const int first = g * kGroupM;
-    const int gm = min(p.mt - first, kGroupM);
+    const int first = g * p.group_m;
+    const int gm = min(p.mt - first, p.group_m);
     const int rr = r - g * gsz;
     mb = first + rr % gm;
     nb = rr / gm;
@@ -763,6 +766,7 @@ cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa,
     p.sa = sa; p.sb = sb; p.C = C; p.acc_out = nullptr; p.strideC = 0;
     p.out_scale = out_scale;
     p.out_e4m3 = out_scale != nullptr;
+    p.group_m = kGroupM;
     p.ga = p.gb = 1;
     p.Mg = M; p.Ng = N;
     // 16-byte stores: 8 bf16 or 16 E4M3 codes per row piece
@@ -805,6 +809,7 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
     const int bk = kBKBytes / 2;
     GemmParams p{};
     p.M = M; p.N = N; p.K = K; p.batch = batch;
+    p.group_m = kGroupMI8;
     p.nkb = (K + bk - 1) / bk;
     p.kb_per_chunk = kI8ChunkK / bk;
     p.nchunks = (p.nkb + p.kb_per_chunk - 1) / p.kb_per_chunk;
