@@ -635,6 +635,8 @@ static bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Used for the INT8 path's fp16 operands; no L2 promotion measured ~1% faster
+// there than 256-byte promotion.
 static bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
                       uint64_t rows, uint64_t batch, uint64_t pitch, uint64_t bpitch,
                       uint32_t box_inner, uint32_t box_rows) {
@@ -646,7 +648,7 @@ static bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>

@@ -297,6 +297,19 @@ def test_i8_gemm_cta_pair_batched_heads():
     assert np.array_equal(acc, oacc) and np.array_equal(C, oC)
 
 
+def test_i8_gemm_batched_staged_in_bulk():
+    """Three heads of 600 x 2048 . (700 x 2048)^T: large enough that the codes
+    are staged by the bulk pipeline (which also bounds their sums), with
+    ragged 600- and 700-row heads; bit-exact against the oracle."""
+    q = synth.student_t(63, (3, 600, 2048))
+    k = synth.normal(64, (3, 700, 2048))
+    qq, sq_ = oracle.quantize_rowwise_i8(q)
+    qk, sk = oracle.quantize_rowwise_i8(k)
+    oacc, oC = oracle.gemm_i8(qq, qk, sq_, sk)
+    C, acc = run_i8(qq, sq_, qk, sk)
+    assert np.array_equal(acc, oacc) and np.array_equal(C, oC)
+
+
 # ------------------------------------------------------------------ E4M3 output
 E4M3_OUT = [
     ("out8 NT 200x176x320", 200, 176, 320, sq.SQ_NT, sq.SQ_FMT_E4M3),
