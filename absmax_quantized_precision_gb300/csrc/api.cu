@@ -171,11 +171,8 @@ sq_status gemm_i8_common(const int8_t* A, const float* sA, int64_t ga, const int
     unsigned* bound_a = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + abytes + bbytes);
     unsigned* bound_b = bound_a + 256;
     int nparts_a = 0, nparts_b = 0;
-    e = sq::launch_i8_to_f16(A, batch, M, K, strideA, A16, bound_a, &nparts_a, ds->err_word, st,
-                             ds->sms);
-    if (e != cudaSuccess) return SQ_ERR_CUDA;
-    e = sq::launch_i8_to_f16(B, batch, N, K, strideB, B16, bound_b, &nparts_b, ds->err_word, st,
-                             ds->sms);
+    e = sq::launch_i8_to_f16_pair(A, M, B, N, batch, K, strideA, strideB, A16, B16, bound_a,
+                                  &nparts_a, bound_b, &nparts_b, ds->err_word, st, ds->sms);
     if (e != cudaSuccess) return SQ_ERR_CUDA;
     return from_cuda(sq::launch_gemm_i8(A16, B16, sA, sB, static_cast<int>(ga),
                                         static_cast<int>(gb), static_cast<int>(batch),

@@ -25,14 +25,18 @@ cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale
                                 int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
                                 int sms);
 
-// Staging of INT8 codes as exact fp16 values: dst[b][r][k] = src[b*stride + r*K + k].
-// When the bulk pipeline runs (contiguous and large), each of its *nparts
-// CTAs writes to parts[cta] the largest sum of squared codes over any of its
-// 1024-code chunks (the ragged tail counts as one chunk); otherwise *nparts
-// is 0.  parts holds at least 256 words.
-cudaError_t launch_i8_to_f16(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
-                             int64_t stride, uint16_t* dst, unsigned* parts, int* nparts,
-                             unsigned* err_word, cudaStream_t st, int sms);
+// Staging of the INT8 codes of both GEMM operands as exact fp16 values:
+// a16[b][r][k] = a[b*stride_a + r*K + k] (M rows per batch), likewise b16.
+// An operand that is contiguous and large takes the bulk pipeline, whose
+// *nparts CTAs each write to parts[cta] the largest sum of squared codes over
+// any of their 1024-code chunks (the ragged tail counts as one chunk); the
+// other operands share one launch of a plain kernel and report *nparts = 0.
+// parts_a and parts_b hold at least 256 words each.
+cudaError_t launch_i8_to_f16_pair(const int8_t* a, int64_t M, const int8_t* b, int64_t N,
+                                  int64_t batch, int64_t K, int64_t stride_a, int64_t stride_b,
+                                  uint16_t* a16, uint16_t* b16, unsigned* parts_a, int* nparts_a,
+                                  unsigned* parts_b, int* nparts_b, unsigned* err_word,
+                                  cudaStream_t st, int sms);
 
 // 0 on success, a cudaError_t otherwise; CUDA_ERROR_* from tensor-map encoding
 // is reported as cudaErrorInvalidValue.
