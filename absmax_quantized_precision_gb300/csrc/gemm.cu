@@ -34,6 +34,7 @@
 #include <mutex>
 
 #include "sq_device.cuh"
+#include "sq_host.h"
 #include "sq_launch.h"
 
 namespace sq {
@@ -656,12 +657,12 @@ static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
                             const GemmParams& p, cudaStream_t st, int sms) {
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
     auto kern = gemm_tc_kernel<BN, I8, A_MN, B_MN, PAIR>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int max_units = 0;   // CTAs (or CTA pairs) that fit the GPU at once
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-        if (attr_err != cudaSuccess) return;
+    // CTAs (or CTA pairs) that fit this device at once
+    const std::pair<cudaError_t, int> fit = per_device_once(reinterpret_cast<const void*>(kern), [&] {
+        cudaError_t attr_err =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        int max_units = 0;
+        if (attr_err != cudaSuccess) return std::make_pair(attr_err, 0);
         if (PAIR) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
@@ -681,8 +682,10 @@ static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
             max_units = sms;
         }
         if (attr_err == cudaSuccess && max_units < 1) attr_err = cudaErrorInvalidConfiguration;
+        return std::make_pair(attr_err, max_units);
     });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (fit.first != cudaSuccess) return fit.first;
+    const int max_units = fit.second;
     const int total = p.mt * p.nt * p.batch;
     const int units = total < max_units ? total : max_units;
     if (!PAIR) {
@@ -1011,9 +1014,8 @@ static bool stage_bulk(const int8_t* src, int64_t batch, int64_t rows, int64_t K
     const int64_t n = batch * rows * K;
     if (!err_word || !(stride == rows * K || batch == 1) || n < static_cast<int64_t>(8192) * sms)
         return false;
-    static cudaError_t attr = cudaFuncSetAttribute(i8_to_f16_bulk_kernel,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   kStgSmem);
+    const cudaError_t attr =
+        set_max_dynamic_smem(reinterpret_cast<const void*>(i8_to_f16_bulk_kernel), kStgSmem);
     if (attr != cudaSuccess) {
         *err = attr;
         return true;

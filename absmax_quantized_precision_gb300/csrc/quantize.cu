@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 
 #include "sq_device.cuh"
+#include "sq_host.h"
 #include "sq_launch.h"
 
 namespace sq {
@@ -671,8 +672,8 @@ static cudaError_t launch_fp8_fmt(const uint16_t* x, int64_t n, const float* sca
                                   float* amax, unsigned* ws, float* ring, int hist_len,
                                   int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
                                   int sms) {
-    static cudaError_t attr = cudaFuncSetAttribute(quant_fp8_kernel<FMT>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+    const cudaError_t attr =
+        set_max_dynamic_smem(reinterpret_cast<const void*>(quant_fp8_kernel<FMT>), kQSmem);
     if (attr != cudaSuccess) return attr;
     const int64_t nfull = n / kFChunk;
     // Small tensors (under one chunk per warp of a full grid) run CTAs of 8

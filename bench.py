@@ -68,8 +68,8 @@ def parse():
 # those sources no longer matches, the bench reports traffic as null.
 PROFILED_TRAFFIC = {
     # profiles/traffic_large_step.md
-    "gemm_fp8_nt": {"bytes": 756712960, "sources_sha256": "2962dee73e47a37a8e9ac508247cd83c91eecdc7bcbdd308fe55028bd2787cfd"},
-    "gemm_i8": {"bytes": 3662025216, "sources_sha256": "2962dee73e47a37a8e9ac508247cd83c91eecdc7bcbdd308fe55028bd2787cfd"},
+    "gemm_fp8_nt": {"bytes": 759954432, "sources_sha256": "4bafa3ccc6fffa9d5311d19efc5e1390578fb0ba51a6493f42d4883fdea6110d"},
+    "gemm_i8": {"bytes": 3210467840, "sources_sha256": "4bafa3ccc6fffa9d5311d19efc5e1390578fb0ba51a6493f42d4883fdea6110d"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
