@@ -169,7 +169,10 @@ size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K
  *   C        float32, batch b at C + b*strideC, [M,N] packed rows (nullable).
  *   acc_out  int32, same layout as C (nullable).  At least one of C, acc_out.
  *   workspace  sq_gemm_i8_workspace_bytes(batch, M, N, K) bytes, 256-B aligned,
- *              contents need no initialisation.
+ *              contents need no initialisation.  The call writes the staged
+ *              operands and the bounds on their sums of squares there and
+ *              reads them back in its last launch, so calls that share a
+ *              workspace must not overlap on the GPU.
  * Limits: K a multiple of 16, 1 <= K <= 2^17 (so |acc| < 2^31 always), strides
  * >= the packed batch sizes; all pointers 16-byte aligned.
  */
