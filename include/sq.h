@@ -165,6 +165,8 @@ size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K
  *
  *   A        int8 codes, batch b at A + b*strideA, [M,K] packed rows.
  *   B        int8 codes, batch b at B + b*strideB, [N,K] packed rows.
+ *            Codes in [-127, 127], as the quantizers produce.  -128 is also
+ *            computed exactly, but then K * 128^2 must stay below 2^31.
  *   sA, sB   float32 row scales, [batch*M] and [batch*N].
  *   C        float32, batch b at C + b*strideC, [M,N] packed rows (nullable).
  *   acc_out  int32, same layout as C (nullable).  At least one of C, acc_out.
@@ -173,8 +175,9 @@ size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K
  *              operands and the bounds on their sums of squares there and
  *              reads them back in its last launch, so calls that share a
  *              workspace must not overlap on the GPU.
- * Limits: K a multiple of 16, 1 <= K <= 2^17 (so |acc| < 2^31 always), strides
- * >= the packed batch sizes; all pointers 16-byte aligned.
+ * Limits: K a multiple of 16, 1 <= K <= 2^17 (so |acc| < 2^31 for codes in
+ * [-127, 127]), strides >= the packed batch sizes; all pointers 16-byte
+ * aligned.
  */
 sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B,
                                const float* sB, int64_t batch, int64_t M, int64_t N, int64_t K,
