@@ -136,6 +136,7 @@ template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    pdl_begin();
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -688,23 +689,8 @@ static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
     const int max_units = fit.second;
     const int total = p.mt * p.nt * p.batch;
     const int units = total < max_units ? total : max_units;
-    if (!PAIR) {
-        kern<<<units, Cfg::THREADS, Cfg::SMEM, st>>>(ta, tb, tc, p);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * units, 1, 1);
-    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::SMEM;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+    if (!PAIR) return launch_pdl(kern, dim3(units), dim3(Cfg::THREADS), Cfg::SMEM, st, 1u, ta, tb, tc, p);
+    return launch_pdl(kern, dim3(2 * units), dim3(Cfg::THREADS), Cfg::SMEM, st, 2u, ta, tb, tc, p);
 }
 
 // Tile shape: 256 x 256 on CTA pairs when there are enough such tiles to give
@@ -868,6 +854,7 @@ struct StageJob {
 };
 
 __global__ void __launch_bounds__(256) i8_to_f16_kernel(const StageJob j0, const StageJob j1) {
+    pdl_begin();
     // 16 codes per step: one 16-B load, two 16-B stores (K % 16 == 0)
     const int64_t all = j0.total + j1.total;
     for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < all;
@@ -903,6 +890,7 @@ __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const in
                                                                        uint16_t* __restrict__ dst,
                                                                        unsigned* __restrict__ parts,
                                                                        unsigned* err_word) {
+    pdl_begin();
     extern __shared__ uint8_t gsmem_raw[];
     uint8_t* gsmem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(gsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -1025,10 +1013,9 @@ static bool stage_bulk(const int8_t* src, int64_t batch, int64_t rows, int64_t K
     if (cap > kStgMaxParts) cap = kStgMaxParts;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    i8_to_f16_bulk_kernel<<<static_cast<unsigned>(blocks), kStgWarps * 32, kStgSmem, st>>>(
-        src, n, dst, parts, err_word);
+    *err = launch_pdl(i8_to_f16_bulk_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kStgWarps * 32),
+                      kStgSmem, st, 1u, src, n, dst, parts, err_word);
     if (nparts) *nparts = static_cast<int>(blocks);
-    *err = cudaGetLastError();
     return true;
 }
 
@@ -1055,8 +1042,8 @@ cudaError_t launch_i8_to_f16_pair(const int8_t* a, int64_t M, const int8_t* b, i
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return cudaSuccess;
-    i8_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(small[0], small[1]);
-    return cudaGetLastError();
+    return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1u,
+                      small[0], small[1]);
 }
 
 }  // namespace sq

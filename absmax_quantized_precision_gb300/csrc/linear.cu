@@ -5,6 +5,7 @@
 #include <cuda_fp16.h>
 
 #include "sq_device.cuh"
+#include "sq_host.h"
 #include "sq_launch.h"
 
 namespace sq {
@@ -12,6 +13,7 @@ namespace sq {
 __global__ void __launch_bounds__(256) bias_to_f32_kernel(const void* __restrict__ bias, int kind,
                                                           int fmt, const float* __restrict__ step,
                                                           int64_t n, float* __restrict__ out) {
+    pdl_begin();
     const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (j >= n) return;
     if (kind == 1) {
@@ -30,9 +32,8 @@ __global__ void __launch_bounds__(256) bias_to_f32_kernel(const void* __restrict
 cudaError_t launch_bias_to_f32(const void* bias, int kind, int fmt, const float* step, int64_t n,
                                float* out, cudaStream_t st) {
     if (n <= 0) return cudaSuccess;
-    bias_to_f32_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(bias, kind, fmt, step,
-                                                                               n, out);
-    return cudaGetLastError();
+    return launch_pdl(bias_to_f32_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st,
+                      1u, bias, kind, fmt, step, n, out);
 }
 
 // Block (x, s): columns [512x, 512x + 512) (two per thread, one 4-byte load),
@@ -40,6 +41,7 @@ cudaError_t launch_bias_to_f32(const void* bias, int kind, int fmt, const float*
 __global__ void __launch_bounds__(256) colsum_partial_kernel(const uint16_t* __restrict__ g,
                                                              int64_t T, int64_t N, int splits,
                                                              float* __restrict__ partial) {
+    pdl_begin();
     const int64_t j = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 2;
     const int s = blockIdx.y;
     const int64_t rows_per = (T + splits - 1) / splits;
@@ -59,6 +61,7 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(const uint16_t* __r
 __global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restrict__ partial,
                                                            int splits, int64_t N,
                                                            uint16_t* __restrict__ gb) {
+    pdl_begin();
     const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (j >= N) return;
     float a = 0.0f;
@@ -70,16 +73,18 @@ cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, int spli
                                float* partial, uint16_t* gb, cudaStream_t st) {
     if (N <= 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>((N / 2 + 255) / 256), static_cast<unsigned>(splits));
-    colsum_partial_kernel<<<grid, 256, 0, st>>>(g, T, N, splits, partial);
-    colsum_final_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, st>>>(partial, splits, N,
-                                                                               gb);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(colsum_partial_kernel, grid, dim3(256), 0, st, 1u, g, T, N, splits, partial);
+    if (e != cudaSuccess) return e;
+    const float* cpartial = partial;
+    return launch_pdl(colsum_final_kernel, dim3(static_cast<unsigned>((N + 255) / 256)), dim3(256), 0, st,
+                      1u, cpartial, splits, N, gb);
 }
 
 // Self-test of the bounded waits: one CTA waits for a barrier phase that
 // nothing completes; the wait gives up after limit_ns, records the timeout in
 // the device error word and the kernel returns normally.
 __global__ void selftest_wait_kernel(unsigned* err_word, unsigned long long limit_ns) {
+    pdl_begin();
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x == 0) {
@@ -92,8 +97,7 @@ __global__ void selftest_wait_kernel(unsigned* err_word, unsigned long long limi
 }
 
 cudaError_t launch_selftest_wait(unsigned* err_word, unsigned long long limit_ns, cudaStream_t st) {
-    selftest_wait_kernel<<<1, 32, 0, st>>>(err_word, limit_ns);
-    return cudaGetLastError();
+    return launch_pdl(selftest_wait_kernel, dim3(1), dim3(32), 0, st, 1u, err_word, limit_ns);
 }
 
 }  // namespace sq

@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
                                                         int64_t cols, int64_t ld,
                                                         int8_t* __restrict__ q,
                                                         float* __restrict__ scales) {
+    pdl_begin();
     constexpr int EPV = Elem<T>::kPerVec;
     constexpr int RPB = 256 / TPR;
     __shared__ float red[8];
@@ -219,6 +220,7 @@ __global__ void __launch_bounds__(256) quant_row_i8_scalar(const T* __restrict__
                                                            int64_t cols, int64_t ld,
                                                            int8_t* __restrict__ q,
                                                            float* __restrict__ scales) {
+    pdl_begin();
     __shared__ float red[8];
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
         const T* xr = x + row * ld;
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(256) quant_row_i8_pf(const T* __restrict__ x, 
                                                        int64_t cols, int64_t ld,
                                                        int8_t* __restrict__ q,
                                                        float* __restrict__ scales) {
+    pdl_begin();
     constexpr int EPV = Elem<T>::kPerVec;
     __shared__ __align__(16) uint8_t buf[2][kPfRowBytes];
     __shared__ float red[8];
@@ -307,9 +310,8 @@ static cudaError_t launch_row_vec(const T* x, int64_t rows, int64_t cols, int64_
     int64_t blocks = (rows + RPB - 1) / RPB;
     const int64_t cap = static_cast<int64_t>(sms) * 64;
     if (blocks > cap) blocks = cap;
-    quant_row_i8_vec<T, TPR, VPT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld,
-                                                                                q, scales);
-    return cudaGetLastError();
+    return launch_pdl(quant_row_i8_vec<T, TPR, VPT>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                      1u, x, rows, cols, ld, q, scales);
 }
 
 template <typename T>
@@ -324,8 +326,8 @@ static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld
         int64_t blocks = rows;
         const int64_t cap = static_cast<int64_t>(sms) * 6;
         if (blocks > cap) blocks = cap;
-        quant_row_i8_pf<T><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, q, scales);
-        return cudaGetLastError();
+        return launch_pdl(quant_row_i8_pf<T>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1u, x,
+                          rows, cols, ld, q, scales);
     }
     if (vec_ok) {
         if (nvec <= 16) return launch_row_vec<T, 16, 1>(x, rows, cols, ld, q, scales, st, sms);
@@ -340,9 +342,8 @@ static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld
     int64_t blocks = rows;
     const int64_t cap = static_cast<int64_t>(sms) * 64;
     if (blocks > cap) blocks = cap;
-    quant_row_i8_scalar<T><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, q,
-                                                                          scales);
-    return cudaGetLastError();
+    return launch_pdl(quant_row_i8_scalar<T>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1u, x,
+                      rows, cols, ld, q, scales);
 }
 
 cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols,
@@ -385,6 +386,7 @@ __global__ void __launch_bounds__(256) group_absmax_kernel(const T* __restrict__
                                                            int64_t cols, int64_t ld,
                                                            int64_t group_rows,
                                                            unsigned* __restrict__ amax_bits) {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -412,6 +414,7 @@ __global__ void __launch_bounds__(256) group_encode_kernel(const T* __restrict__
                                                            const unsigned* __restrict__ amax_bits,
                                                            int8_t* __restrict__ q,
                                                            float* __restrict__ scales) {
+    pdl_begin();
     constexpr int EPV = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -449,14 +452,20 @@ static cudaError_t launch_grouped(const T* x, int64_t rows, int64_t cols, int64_
     int64_t blocks = (rows + 7) / 8;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    const unsigned* cws = ws;
     if (vec_ok) {
-        group_absmax_kernel<T, true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, group_rows, ws);
-        group_encode_kernel<T, true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, group_rows, ws, q, scales);
-    } else {
-        group_absmax_kernel<T, false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, group_rows, ws);
-        group_encode_kernel<T, false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, rows, cols, ld, group_rows, ws, q, scales);
+        e = launch_pdl(group_absmax_kernel<T, true>, grid, dim3(256), 0, st, 1u, x, rows, cols, ld,
+                       group_rows, ws);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(group_encode_kernel<T, true>, grid, dim3(256), 0, st, 1u, x, rows, cols, ld,
+                          group_rows, cws, q, scales);
     }
-    return cudaGetLastError();
+    e = launch_pdl(group_absmax_kernel<T, false>, grid, dim3(256), 0, st, 1u, x, rows, cols, ld,
+                   group_rows, ws);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(group_encode_kernel<T, false>, grid, dim3(256), 0, st, 1u, x, rows, cols, ld,
+                      group_rows, cws, q, scales);
 }
 
 cudaError_t launch_quantize_grouped_i8(const void* x, int dtype, int64_t rows, int64_t cols,
@@ -533,6 +542,7 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
                                                                  unsigned* __restrict__ ws, float* ring,
                                                                  int hist_len, int ring_idx, int margin,
                                                                  unsigned* err_word) {
+    pdl_begin();
     extern __shared__ uint8_t qsmem_raw[];
     uint8_t* qsmem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(qsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -684,9 +694,9 @@ static cudaError_t launch_fp8_fmt(const uint16_t* x, int64_t n, const float* sca
     if (blocks < 1) blocks = 1;
     const int64_t cap = static_cast<int64_t>(sms) * (warps == kFWarps ? 1 : 3);
     if (blocks > cap) blocks = cap;
-    quant_fp8_kernel<FMT><<<static_cast<unsigned>(blocks), warps * 32, smem, st>>>(
-        x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin, err_word);
-    return cudaGetLastError();
+    return launch_pdl(quant_fp8_kernel<FMT>, dim3(static_cast<unsigned>(blocks)), dim3(warps * 32),
+                      static_cast<size_t>(smem), st, 1u, x, n, scale, x8, amax, ws, ring, hist_len,
+                      ring_idx, margin, err_word);
 }
 
 cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
