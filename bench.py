@@ -586,13 +586,13 @@ def run_small_config(name, args):
                 lambda: sq.sq_quantize_rowwise_i8(B, q=qb, scales=sb)),
                ("gemm_i8", "flops", gemm_flops,
                 lambda: sq.sq_gemm_i8_rowscaled(qa, sa.reshape(-1), qb, sb.reshape(-1), ws, C=C))]
-        t0 = time.perf_counter()
-        oqa, osa = oracle.quantize_rowwise_i8(a)
-        oqb, osb = oracle.quantize_rowwise_i8(b)
-        oracle.gemm_i8(oqa, oqb, osa, osb)
-        cpu = time.perf_counter() - t0
+        def oracle_work():
+            oqa, osa = oracle.quantize_rowwise_i8(a)
+            oqb, osb = oracle.quantize_rowwise_i8(b)
+            oracle.gemm_i8(oqa, oqb, osa, osb)
     elif name in EXTRA_CONFIGS:
-        desc, ops, gemm_flops, cpu = extra_config_ops(name, dev, bf16_dev, prev_scale)
+        desc, ops, gemm_flops, _ = extra_config_ops(name, dev, bf16_dev, prev_scale)
+        oracle_work = None
     else:
         fmt = sq.SQ_FMT_E4M3
         wsq = sq.new_workspace(dev)
@@ -615,11 +615,10 @@ def run_small_config(name, args):
                     lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=aw)),
                    ("gemm_fp8_nt", "flops", gemm_flops,
                     lambda: sq.sq_gemm_fp8_scaled(x8, w8, tsx, tsw, fmt, sq.SQ_NT, C=Y))]
-            t0 = time.perf_counter()
-            ox8, _ = oracle.quantize_fp8(x, sx, 0)
-            ow8, _ = oracle.quantize_fp8(w, sw, 0)
-            oracle.gemm_fp8(ox8, ow8, 0, oracle.NT, sx, sw)
-            cpu = time.perf_counter() - t0
+            def oracle_work():
+                ox8, _ = oracle.quantize_fp8(x, sx, 0)
+                ow8, _ = oracle.quantize_fp8(w, sw, 0)
+                oracle.gemm_fp8(ox8, ow8, 0, oracle.NT, sx, sw)
         else:
             T, H, D = 2048, 4096, 1024
             g = synth.normal(41, (T, H), std=1e-3, dtype=synth.BF16)
@@ -649,13 +648,26 @@ def run_small_config(name, args):
                     lambda: sq.sq_gemm_fp8_scaled(g8, w8, tsg, tsw, fmt, sq.SQ_NN, C=dX)),
                    ("gemm_fp8_dW_tn", "flops", 2.0 * T * H * D,
                     lambda: sq.sq_gemm_fp8_scaled(g8, x8, tsg, tsx, fmt, sq.SQ_TN, C=dW))]
-            t0 = time.perf_counter()
-            og8, _ = oracle.quantize_fp8(g, sg, 0)
-            ow8, _ = oracle.quantize_fp8(w, sw, 0)
-            ox8, _ = oracle.quantize_fp8(x, sx, 0)
-            oracle.gemm_fp8(og8, ow8, 0, oracle.NN, sg, sw, want_bf16=False)
-            oracle.gemm_fp8(og8, ox8, 0, oracle.TN, sg, sx, want_bf16=False)
-            cpu = time.perf_counter() - t0
+            def oracle_work():
+                og8, _ = oracle.quantize_fp8(g, sg, 0)
+                ow8, _ = oracle.quantize_fp8(w, sw, 0)
+                ox8, _ = oracle.quantize_fp8(x, sx, 0)
+                oracle.gemm_fp8(og8, ow8, 0, oracle.NN, sg, sw, want_bf16=False)
+                oracle.gemm_fp8(og8, ox8, 0, oracle.TN, sg, sx, want_bf16=False)
+
+    # the oracle on the host: all cores, then one core
+    cpu = None
+    if oracle_work is not None:
+        cores = oracle.num_threads()
+        t0 = time.perf_counter()
+        oracle_work()
+        cpu = {"seconds": time.perf_counter() - t0, "cores": cores}
+        oracle.set_num_threads(1)
+        t0 = time.perf_counter()
+        oracle_work()
+        cpu["seconds_1core"] = time.perf_counter() - t0
+        oracle.set_num_threads(cores)
+        cpu["sample"] = "the whole workload"
 
     iters = max(args.steps if args.steps != 300 else 50, 1)
     for _ in range(max(args.warmup, 3)):
@@ -741,8 +753,7 @@ def run_small_config(name, args):
             "calls_per_step": len(ops),
             "iters": iters, "kernels_eager": kernels, "kernels_graph": kernels_graph,
             "clocks": clk.summary(),
-            "cpu_oracle": None if cpu is None else {"seconds": cpu, "cores": oracle.num_threads(),
-                                                     "sample": "the whole workload"}}
+            "cpu_oracle": cpu}
     print(json.dumps(line), flush=True)
 
 

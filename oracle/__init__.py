@@ -86,6 +86,8 @@ def _load():
             L.or_colsum_bf16.restype = i32
             L.or_num_threads.argtypes = []
             L.or_num_threads.restype = i32
+            L.or_set_num_threads.argtypes = [i32]
+            L.or_set_num_threads.restype = None
             _lib = L
     return _lib
 
@@ -103,6 +105,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(_load().or_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Thread count of the oracle's OpenMP loops (for timing it on one core)."""
+    _load().or_set_num_threads(int(n))
 
 
 # ------------------------------------------------------------------ codec

@@ -487,6 +487,11 @@ int or_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, double* out) {
     return 0;
 }
 
+// Timing support only: the OpenMP thread count of the loops below.
+void or_set_num_threads(int n) {
+    if (n > 0) omp_set_num_threads(n);
+}
+
 int or_num_threads(void) {
     int n = 1;
 #pragma omp parallel

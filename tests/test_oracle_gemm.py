@@ -260,3 +260,26 @@ def test_colsum_matches_numpy():
     g = synth.normal(82, (300, 40), dtype=synth.BF16)
     want = synth.bf16_bits_to_f32(g).astype(np.float64).sum(axis=0)
     assert np.allclose(oracle.colsum_bf16(g), want, rtol=1e-15, atol=1e-15)
+
+
+def test_oracle_results_do_not_depend_on_the_thread_count():
+    """The OpenMP loops split rows between threads; every output element is
+    still summed in one fixed order, so one thread and all threads agree bit
+    for bit (the one-core timing in bench.py relies on this too)."""
+    rng = np.random.default_rng(91)
+    qa = rng.integers(-127, 128, (37, 300)).astype(np.int8)
+    qb = rng.integers(-127, 128, (41, 300)).astype(np.int8)
+    sa = rng.uniform(0.1, 2.0, 37).astype(np.float32)
+    sb = rng.uniform(0.1, 2.0, 41).astype(np.float32)
+    a8 = rng.integers(0, 0x7F, (33, 256)).astype(np.uint8)
+    b8 = rng.integers(0, 0x7F, (29, 256)).astype(np.uint8)
+    n = oracle.num_threads()
+    try:
+        many = (oracle.gemm_i8(qa, qb, sa, sb), oracle.gemm_fp8(a8, b8, 0, oracle.NT, 0.01, 0.02))
+        oracle.set_num_threads(1)
+        assert oracle.num_threads() == 1
+        one = (oracle.gemm_i8(qa, qb, sa, sb), oracle.gemm_fp8(a8, b8, 0, oracle.NT, 0.01, 0.02))
+    finally:
+        oracle.set_num_threads(n)
+    for x, y in zip(many[0] + many[1], one[0] + one[1]):
+        assert np.array_equal(np.asarray(x), np.asarray(y))
