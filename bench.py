@@ -68,8 +68,8 @@ def parse():
 # those sources no longer matches, the bench reports traffic as null.
 PROFILED_TRAFFIC = {
     # profiles/traffic_large_step.md
-    "gemm_fp8_nt": {"bytes": 759954432, "sources_sha256": "4bafa3ccc6fffa9d5311d19efc5e1390578fb0ba51a6493f42d4883fdea6110d"},
-    "gemm_i8": {"bytes": 3210467840, "sources_sha256": "4bafa3ccc6fffa9d5311d19efc5e1390578fb0ba51a6493f42d4883fdea6110d"},
+    "gemm_fp8_nt": {"bytes": 845968384, "sources_sha256": "d52d307aa8cd82a1d280fc69e32ba94a3d857da39ac1ec301f6db0845da6def2"},
+    "gemm_i8": {"bytes": 3211070208, "sources_sha256": "d52d307aa8cd82a1d280fc69e32ba94a3d857da39ac1ec301f6db0845da6def2"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
