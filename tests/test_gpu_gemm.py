@@ -127,6 +127,26 @@ def test_i8_exactness_with_and_without_drains(c):
     assert np.array_equal(C.view(np.uint32), oC.view(np.uint32))
 
 
+@pytest.mark.parametrize("cmax", [127, 11], ids=["+-127: 128 drained chunks", "|q|<=11: one chunk"])
+def test_i8_gemm_at_the_maximum_k(cmax):
+    """K = 2^17, the largest the call accepts.  With codes up to 127 the
+    sums reach ~2^31 and every 1024-long chunk is drained; with |q| <= 11
+    the staging bound lets the whole K run as one fp32 chunk.  Bit-exact."""
+    M, N, K = 64, 96, 1 << 17
+    rng = np.random.default_rng(97 + cmax)
+    qa = rng.integers(-cmax, cmax + 1, (M, K)).astype(np.int8)
+    qb = rng.integers(-cmax, cmax + 1, (N, K)).astype(np.int8)
+    if cmax == 127:
+        qa[0] = 127
+        qb[0] = 127                               # one output at exactly 127^2 * 2^17
+    sa = rng.uniform(0.5, 1.5, M).astype(np.float32)
+    sb = rng.uniform(0.5, 1.5, N).astype(np.float32)
+    oacc, oC = oracle.gemm_i8(qa, qb, sa, sb)
+    C, acc = run_i8(qa, sa, qb, sb)
+    assert np.array_equal(acc, oacc)
+    assert np.array_equal(C.view(np.uint32), oC.view(np.uint32))
+
+
 def fp8_inputs(name, M, N, K, fmt, std_a=1.0, std_b=0.02):
     s = seed_of(name)
     xa = synth.normal(s, (M, K), std=std_a, dtype=synth.BF16)
@@ -184,6 +204,18 @@ def test_fp8_gemm_layouts(name, M, N, K, layout):
                           torch.tensor([sb], device=DEV), fmt, layout, C=C)
     check_fp8(C, A, B, fmt, layout, K, sa, sb)
     assert guard_intact(cbuf, n, 3.0)
+
+
+def test_fp8_gemm_long_k():
+    """K = 65536 in one fp32 accumulation, within the bound, which grows with
+    sqrt(K)."""
+    M, N, K = 128, 160, 1 << 16
+    fmt = sq.SQ_FMT_E4M3
+    a8, b8, sa, sb = fp8_inputs("long K", M, N, K, fmt)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    sq.sq_gemm_fp8_scaled(to_dev(a8), to_dev(b8), torch.tensor([sa], device=DEV),
+                          torch.tensor([sb], device=DEV), fmt, sq.SQ_NT, C=C)
+    check_fp8(C, a8, b8, fmt, sq.SQ_NT, K, sa, sb)
 
 
 @pytest.mark.parametrize("N", [100, 104, 2056], ids=["N100 thread stores", "N104 clipped box", "N2056 pair"])
