@@ -374,6 +374,36 @@ def run_sq(args, rank, world, local_rank):
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error in the timed region")
 
+    # Steady-state rate of each quantize call: 10 launches back to back (each
+    # overlapping the tail of the one before), events only around the batch.
+    # B's launches alternate between B and the first rows of A, so that no
+    # launch finds its input in L2 from the one before (A alone exceeds L2).
+    def steady(fn, reps=10, batches=3):
+        t = []
+        for _ in range(batches):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for r in range(reps):
+                fn(r)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            t.append(e0.elapsed_time(e1) / reps)
+        return statistics.median(t)
+
+    b_alt = A[:N] if M >= N else None
+    steady_ms = {
+        "quant_fp8_A": steady(lambda r: sq.sq_quantize_fp8(A, tsa, sq.SQ_FMT_E4M3, ws, x8=a8,
+                                                           amax=amax_a, stream=stream)),
+        "quant_fp8_B": steady(lambda r: sq.sq_quantize_fp8(B if (r % 2 == 0 or b_alt is None) else b_alt,
+                                                           tsb, sq.SQ_FMT_E4M3, ws, x8=b8,
+                                                           amax=amax_b, stream=stream)),
+        "quant_i8_A": steady(lambda r: sq.sq_quantize_rowwise_i8(A, q=qa, scales=sA, stream=stream)),
+        "quant_i8_B": steady(lambda r: sq.sq_quantize_rowwise_i8(
+            B if (r % 2 == 0 or b_alt is None) else b_alt, q=qb, scales=sB, stream=stream)),
+    }
+    if sq.sq_get_last_device_error() != sq.SQ_OK:
+        raise RuntimeError("device error in the steady-state pass")
+
     # ------------------------------------------------ e2e: host buffers, copies inside
     # Every step copies its own inputs in from pinned host memory and its two
     # results out to pinned host memory inside the timed region.  The copies
@@ -476,6 +506,11 @@ def run_sq(args, rank, world, local_rank):
             d["TFLOP/s"] = tf
             d["frac_peak"] = tf / (fp8_peak if n == "gemm_fp8_nt" else bf16_peak)
         kernels[n] = d
+    kernels_steady = {}
+    for n, ms in steady_ms.items():
+        by = quant_fp8_bytes.get(n) or quant_i8_bytes.get(n)
+        gbs = by / (ms * 1e-3) / 1e9
+        kernels_steady[n] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"]}
     dom = max(("gemm_fp8_nt", "gemm_i8"), key=lambda n: per_kernel[n])
     dom_peak = fp8_peak if dom == "gemm_fp8_nt" else bf16_peak
     achieved = kernels[dom]["TFLOP/s"]
@@ -513,6 +548,10 @@ def run_sq(args, rank, world, local_rank):
         "clocks": clk.summary(),
         "roofline": roofline,
         "kernels": kernels,
+        "kernels_steady": kernels_steady,
+        "kernels_steady_note": ("each quantize call launched 10 times back to back with events only "
+                                "around the batch; B alternates with a same-size block of A so "
+                                "no launch reads its input from L2"),
         "kernels_note": ("mean CUDA-event span of each call on the stream it ran on, from a second "
                          "pass of the same steps with events around every call (the step time comes "
                          "from a pass without them, where each kernel's launch overlaps the tail of "
