@@ -113,12 +113,12 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 
 // ------------------------------------------------------------------ launches
 // Every kernel of libsq is launched with programmatic stream serialization
-// (sq_host.h, launch_pdl) and starts with pdl_begin(): it first waits until
-// the kernel before it on the stream has completed and its memory is visible
-// (so nothing below this point can race with it), then allows the kernel
-// after it to be launched.  The next kernel's launch and set-up therefore
-// overlap this kernel's tail, and because each kernel waits before it does
-// anything, completion still implies the completion of every kernel before it.
+// (sq_host.h, launch_pdl) and calls pdl_begin() before its first global
+// memory access: it waits until the kernel before it on the stream has
+// completed and its memory is visible, then allows the next kernel to be
+// launched.  The next kernel's launch and set-up therefore overlap this
+// kernel's tail, and because each kernel waits before it touches memory,
+// completion still implies the completion of every kernel before it.
 __device__ __forceinline__ void pdl_begin() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

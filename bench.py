@@ -68,8 +68,8 @@ def parse():
 # those sources no longer matches, the bench reports traffic as null.
 PROFILED_TRAFFIC = {
     # profiles/traffic_large_step.md
-    "gemm_fp8_nt": {"bytes": 845968384, "sources_sha256": "d52d307aa8cd82a1d280fc69e32ba94a3d857da39ac1ec301f6db0845da6def2"},
-    "gemm_i8": {"bytes": 3211070208, "sources_sha256": "d52d307aa8cd82a1d280fc69e32ba94a3d857da39ac1ec301f6db0845da6def2"},
+    "gemm_fp8_nt": {"bytes": 796245760, "sources_sha256": "e411ed1e0a227cc74b70b823794219033ce8ba7482231e21f8dd0c0cae3c71c3"},
+    "gemm_i8": {"bytes": 3207587072, "sources_sha256": "e411ed1e0a227cc74b70b823794219033ce8ba7482231e21f8dd0c0cae3c71c3"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
