@@ -409,6 +409,38 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
             const int row = m0 + quarter * 32 + lane;
             if (I8) {
                 constexpr int NC = Cfg::EPI_COLS / 32;
+                // A CTA's last tile: every MMA has completed and no TMA load is
+                // pending once its last accumulator is read, so the operand
+                // stages are free.  Each warp stages its 32 rows there and then
+                // writes whole row runs (one 512-byte run, or two 256-byte ones,
+                // per instruction) instead of a 16-byte piece in each of 32
+                // rows.  On one-wave problems this store is the exposed tail of
+                // the kernel, so its scales are loaded before the accumulator
+                // is waited for.
+                constexpr int PITCH = Cfg::EPI_COLS + 4;   // int32 words per staged row
+                constexpr int F4_ROW = Cfg::EPI_COLS / 4;   // 16-byte pieces per row
+                constexpr int ROWS_STEP = 32 / F4_ROW;      // rows one warp-wide store covers
+                static_assert(Cfg::EPI_WARPS * 32 * PITCH * 4 <= Cfg::STAGES * Cfg::STAGE,
+                              "staged output fits in the operand stages");
+                const bool staged = p.vec_store && t + num_units >= total;
+                const int scol = n0 + colgrp * Cfg::EPI_COLS + 4 * (lane % F4_ROW);
+                const bool scol_ok = scol < p.N;   // N % 4 == 0: all four columns are in range
+                float st_sa = 0.0f;
+                float4 st_sb = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (staged) {
+                    if (row < p.M) st_sa = p.sa[static_cast<int64_t>(b) * p.Mg + row / p.ga];
+                    if (p.C && scol_ok) {
+                        const float* sBb = p.sb + static_cast<int64_t>(b) * p.Ng;
+                        if (p.sb_vec) {
+                            st_sb = *reinterpret_cast<const float4*>(sBb + scol);
+                        } else {
+                            st_sb.x = sBb[scol / p.gb];
+                            st_sb.y = sBb[(scol + 1) / p.gb];
+                            st_sb.z = sBb[(scol + 2) / p.gb];
+                            st_sb.w = sBb[(scol + 3) / p.gb];
+                        }
+                    }
+                }
                 int32_t sums[NC][32];
 #pragma unroll
                 for (int c = 0; c < NC; ++c)
@@ -439,18 +471,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                     ++it;
                 }
                 if (!ok) break;
-                // A CTA's last tile: every MMA has completed and no TMA load is
-                // pending, so the operand stages are free.  Each warp stages its
-                // 32 rows there and then writes whole row runs (one 512-byte run,
-                // or two 256-byte ones, per instruction) instead of a 16-byte
-                // piece in each of 32 rows.  On one-wave problems this store is
-                // the exposed tail of the kernel.
-                constexpr int PITCH = Cfg::EPI_COLS + 4;   // int32 words per staged row
-                constexpr int F4_ROW = Cfg::EPI_COLS / 4;   // 16-byte pieces per row
-                constexpr int ROWS_STEP = 32 / F4_ROW;      // rows one warp-wide store covers
-                static_assert(Cfg::EPI_WARPS * 32 * PITCH * 4 <= Cfg::STAGES * Cfg::STAGE,
-                              "staged output fits in the operand stages");
-                if (p.vec_store && t + num_units >= total) {
+                if (staged) {
                     int32_t* stg = reinterpret_cast<int32_t*>(smem) + ew * 32 * PITCH;
                     fence_proxy_async_smem();
 #pragma unroll
@@ -460,34 +481,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
                             *reinterpret_cast<int4*>(stg + lane * PITCH + c * 32 + 4 * v) =
                                 make_int4(sums[c][4 * v], sums[c][4 * v + 1], sums[c][4 * v + 2],
                                           sums[c][4 * v + 3]);
-                    const float sArow =
-                        row < p.M ? p.sa[static_cast<int64_t>(b) * p.Mg + row / p.ga] : 0.0f;
                     __syncwarp();
                     const int j = lane % F4_ROW;
-                    const int col = n0 + colgrp * Cfg::EPI_COLS + 4 * j;
-                    const bool col_ok = col < p.N;   // N % 4 == 0: all four columns are in range
                     float* Cf = static_cast<float*>(p.C);
-                    float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    if (Cf && col_ok) {
-                        const float* sBb = p.sb + static_cast<int64_t>(b) * p.Ng;
-                        if (p.sb_vec) {
-                            s4 = *reinterpret_cast<const float4*>(sBb + col);
-                        } else {
-                            s4.x = sBb[col / p.gb];
-                            s4.y = sBb[(col + 1) / p.gb];
-                            s4.z = sBb[(col + 2) / p.gb];
-                            s4.w = sBb[(col + 3) / p.gb];
-                        }
-                    }
+                    const float4 s4 = st_sb;
 #pragma unroll 4
                     for (int r0 = 0; r0 < 32; r0 += ROWS_STEP) {
                         const int r = r0 + lane / F4_ROW;
-                        const float sr = __shfl_sync(0xffffffffu, sArow, r);
+                        const float sr = __shfl_sync(0xffffffffu, st_sa, r);
                         const int grow = m0 + quarter * 32 + r;
-                        if (grow < p.M && col_ok) {
+                        if (grow < p.M && scol_ok) {
                             const int4 a = *reinterpret_cast<const int4*>(stg + r * PITCH + 4 * j);
                             const int64_t o = static_cast<int64_t>(b) * p.strideC +
-                                              static_cast<int64_t>(grow) * p.N + col;
+                                              static_cast<int64_t>(grow) * p.N + scol;
                             if (p.acc_out) st_v4(p.acc_out + o, make_uint4(a.x, a.y, a.z, a.w));
                             if (Cf)
                                 st_v4(Cf + o, make_uint4(
