@@ -68,8 +68,8 @@ def parse():
 # those sources no longer matches, the bench reports traffic as null.
 PROFILED_TRAFFIC = {
     # profiles/traffic_large_step.md
-    "gemm_fp8_nt": {"bytes": 796245760, "sources_sha256": "e411ed1e0a227cc74b70b823794219033ce8ba7482231e21f8dd0c0cae3c71c3"},
-    "gemm_i8": {"bytes": 3207587072, "sources_sha256": "e411ed1e0a227cc74b70b823794219033ce8ba7482231e21f8dd0c0cae3c71c3"},
+    "gemm_fp8_nt": {"bytes": 755166208, "sources_sha256": "af1fdb2bccc98fb3882b07c292766c3da12061a88e7d51c646f357ccf785ac44"},
+    "gemm_i8": {"bytes": 3206116352, "sources_sha256": "af1fdb2bccc98fb3882b07c292766c3da12061a88e7d51c646f357ccf785ac44"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
