@@ -138,6 +138,505 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     return d;
 }
 
+// Per-CTA state that the warp roles of gemm_tc_kernel share: pointers into
+// shared memory, the TMEM base, this CTA's identity and its tile range.
+struct GemmCta {
+    uint8_t* smem;              // operand stages (1024-aligned)
+    uint8_t* epi_stage;         // FP8: output staging boxes
+    uint64_t* full;             // [STAGES] stage landed
+    uint64_t* empty;            // [STAGES] stage consumed by the MMAs
+    uint64_t* tfull;            // [2] accumulator complete
+    uint64_t* tempty;           // [2] accumulator read by every epilogue warp
+    uint64_t* drain;            // MMAs issued before an abort have finished
+    volatile int* abort_flag;
+    uint32_t tmem_base;
+    uint32_t rank;              // 0 = leader of the pair
+    bool leader;
+    int cta_unit, num_units;    // this CTA's (or pair's) index and their count
+    int total;                  // tiles in the problem
+};
+
+// Warp 0: one elected thread streams the A and B boxes of every k-block of
+// this CTA's tiles into the ring of stages.
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+__device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                              const GemmParams& p, const GemmCta& c) {
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
+    uint8_t* smem = c.smem;
+    uint64_t* full = c.full;
+    uint64_t* empty = c.empty;
+    volatile int* abort_flag = c.abort_flag;
+    const uint32_t rank = c.rank;
+    const bool leader = c.leader;
+    const int cta_unit = c.cta_unit, num_units = c.num_units, total = c.total;
+    if (elect_one_sync()) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_phase[Cfg::STAGES];
+        for (int s = 0; s < Cfg::STAGES; ++s) issued_phase[s] = -1;
+        bool ok = true;
+        for (int t = cta_unit; t < total && ok; t += num_units) {
+            int b, mb, nb;
+            tile_coords(t, p, b, mb, nb);
+            const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
+            const int n0 = nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err_word)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sA = smem + stage * Cfg::STAGE;
+                uint8_t* sB = sA + Cfg::A_BYTES;
+                if (PAIR) {
+                    // both CTAs' bytes complete on the leader's barrier
+                    const uint32_t fb = cluster_addr(&full[stage], 0);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::STAGE);
+                    if (I8) {
+                        const int kx = kb * (kBKBytes / 2);
+                        tma_load_3d_pair(sA, &tmA, fb, kx, m0, b);
+                        tma_load_3d_pair(sB, &tmB, fb, kx, n0, b);
+                    } else {
+                        const int kx = kb * kBKBytes;
+                        if (A_MN) tma_load_2d_pair(sA, &tmA, fb, m0, kx);
+                        else tma_load_2d_pair(sA, &tmA, fb, kx, m0);
+                        if (B_MN) {
+#pragma unroll
+                            for (int j = 0; j < Cfg::B_ROWS / 128; ++j)
+                                tma_load_2d_pair(sB + j * Cfg::MN_LBO, &tmB, fb, n0 + j * 128, kx);
+                        } else {
+                            tma_load_2d_pair(sB, &tmB, fb, kx, n0);
+                        }
+                    }
+                } else {
+                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE);
+                    if (I8) {
+                        const int kx = kb * (kBKBytes / 2);
+                        tma_load_3d(sA, &tmA, &full[stage], kx, m0, b);
+                        tma_load_3d(sB, &tmB, &full[stage], kx, n0, b);
+                    } else {
+                        const int kx = kb * kBKBytes;
+                        if (A_MN) tma_load_2d(sA, &tmA, &full[stage], m0, kx);
+                        else tma_load_2d(sA, &tmA, &full[stage], kx, m0);
+                        if (B_MN) {
+#pragma unroll
+                            for (int j = 0; j < Cfg::B_ROWS / 128; ++j)
+                                tma_load_2d(sB + j * Cfg::MN_LBO, &tmB, &full[stage], n0 + j * 128, kx);
+                        } else {
+                            tma_load_2d(sB, &tmB, &full[stage], kx, n0);
+                        }
+                    }
+                }
+                issued_phase[stage] = static_cast<int>(phase);
+                if (++stage == Cfg::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && leader) {
+            // let every copy signalled on this CTA's barriers land before it exits
+            for (int s = 0; s < Cfg::STAGES; ++s)
+                if (issued_phase[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(issued_phase[s]));
+        }
+    }
+}
+
+// Warp 1: on the leader, one elected thread issues the MMAs of each k-block
+// into one of the two TMEM accumulators (kbpc k-blocks per accumulator
+// chunk, nch chunks per tile) and commits stages and accumulators.
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+__device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, int kbpc, int nch) {
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
+    uint8_t* smem = c.smem;
+    uint64_t* full = c.full;
+    uint64_t* empty = c.empty;
+    uint64_t* tfull = c.tfull;
+    uint64_t* tempty = c.tempty;
+    uint64_t* drain = c.drain;
+    volatile int* abort_flag = c.abort_flag;
+    const uint32_t tmem_base = c.tmem_base;
+    const bool leader = c.leader;
+    const int cta_unit = c.cta_unit, num_units = c.num_units, total = c.total;
+    if (leader && elect_one_sync()) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t it = 0;
+        bool ok = true;
+        bool issued = false;
+        for (int t = cta_unit; t < total && ok; t += num_units) {
+            for (int ch = 0; ch < nch && ok; ++ch) {
+                const uint32_t ab = it & 1u;
+                const uint32_t aph = (it >> 1) & 1u;
+                if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, p.err_word)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + ab * BN;
+                const int kb0 = ch * kbpc;
+                const int kb1 = min(p.nkb, kb0 + kbpc);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.err_word)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_addr(smem + stage * Cfg::STAGE);
+                    const uint32_t b_addr = a_addr + Cfg::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < kBKBytes / 32; ++kk) {
+                        const uint64_t ad =
+                            A_MN ? sdesc_sw128(a_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
+                                 : sdesc_sw128(a_addr + kk * Cfg::KSTEP_K, 16, 1024);
+                        const uint64_t bd =
+                            B_MN ? sdesc_sw128(b_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
+                                 : sdesc_sw128(b_addr + kk * Cfg::KSTEP_K, 16, 1024);
+                        const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+                        if (PAIR) {
+                            if (I8) mma_pair_f16(d_tmem, ad, bd, p.idesc, acc);
+                            else mma_pair_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
+                        } else {
+                            if (I8) mma_f16(d_tmem, ad, bd, p.idesc, acc);
+                            else mma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
+                        }
+                    }
+                    issued = true;
+                    if (PAIR) mma_commit_pair(&empty[stage], 3);   // frees the stage in both CTAs
+                    else mma_commit(&empty[stage]);
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (PAIR) mma_commit_pair(&tfull[ab], 3);          // both epilogues may read
+                else mma_commit(&tfull[ab]);
+                ++it;
+            }
+        }
+        if (!ok && issued) {
+            // make every MMA already issued finish before TMEM is released
+            if (PAIR) mma_commit_pair(drain, 1);
+            else mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    }
+}
+
+// Warps 2..: read each finished accumulator out of TMEM, scale it and store
+// the tile (INT8: int32 sums of nch chunks, fp32 dequantized output; FP8:
+// bf16 or E4M3 output).
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+__device__ __forceinline__ void gemm_epilogue(const CUtensorMap& tmC, const GemmParams& p,
+                                              const GemmCta& c, int nch) {
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* smem = c.smem;
+    uint8_t* epi_stage = c.epi_stage;
+    uint64_t* tfull = c.tfull;
+    uint64_t* tempty = c.tempty;
+    volatile int* abort_flag = c.abort_flag;
+    const uint32_t tmem_base = c.tmem_base;
+    const uint32_t rank = c.rank;
+    const bool leader = c.leader;
+    const int cta_unit = c.cta_unit, num_units = c.num_units, total = c.total;
+    const int ew = warp - 2;
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    const int colgrp = ew >> 2;            // which EPI_COLS-wide column group
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    // where this warp reports that it has read an accumulator: the leader's barrier
+    const uint32_t tempty_leader[2] = {PAIR ? cluster_addr(&tempty[0], 0) : 0u,
+                                       PAIR ? cluster_addr(&tempty[1], 0) : 0u};
+    float fsa = 0.0f, fsb = 0.0f, fos = 1.0f, foy = 1.0f;
+    bool ofast = true;
+    if (!I8) {
+        fsa = *p.sa;
+        fsb = *p.sb;
+        if (p.out_e4m3) {
+            fos = *p.out_scale;
+            foy = __frcp_rn(fos);
+            ofast = fos >= 0x1p-40f && fos <= 0x1p40f;
+        }
+    }
+    uint32_t it = 0;
+    uint32_t sc = 0;                       // output boxes this warp has stored
+    bool ok = true;
+    auto release = [&](uint32_t ab) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (PAIR && !leader) mbar_arrive_cluster(tempty_leader[ab]);
+            else mbar_arrive(&tempty[ab]);
+        }
+    };
+    for (int t = cta_unit; t < total && ok; t += num_units) {
+        int b, mb, nb;
+        tile_coords(t, p, b, mb, nb);
+        const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
+        const int n0 = nb * BN;
+        const int row = m0 + quarter * 32 + lane;
+        if (I8) {
+            constexpr int NC = Cfg::EPI_COLS / 32;
+            // A CTA's last tile: every MMA has completed and no TMA load is
+            // pending once its last accumulator is read, so the operand
+            // stages are free.  Each warp stages its 32 rows there and then
+            // writes whole row runs (one 512-byte run, or two 256-byte ones,
+            // per instruction) instead of a 16-byte piece in each of 32
+            // rows.  On one-wave problems this store is the exposed tail of
+            // the kernel, so its scales are loaded before the accumulator
+            // is waited for.
+            constexpr int PITCH = Cfg::EPI_COLS + 4;   // int32 words per staged row
+            constexpr int F4_ROW = Cfg::EPI_COLS / 4;   // 16-byte pieces per row
+            constexpr int ROWS_STEP = 32 / F4_ROW;      // rows one warp-wide store covers
+            static_assert(Cfg::EPI_WARPS * 32 * PITCH * 4 <= Cfg::STAGES * Cfg::STAGE,
+                          "staged output fits in the operand stages");
+            const bool staged = p.vec_store && t + num_units >= total;
+            const int scol = n0 + colgrp * Cfg::EPI_COLS + 4 * (lane % F4_ROW);
+            const bool scol_ok = scol < p.N;   // N % 4 == 0: all four columns are in range
+            float st_sa = 0.0f;
+            float4 st_sb = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (staged) {
+                if (row < p.M) st_sa = p.sa[static_cast<int64_t>(b) * p.Mg + row / p.ga];
+                if (p.C && scol_ok) {
+                    const float* sBb = p.sb + static_cast<int64_t>(b) * p.Ng;
+                    if (p.sb_vec) {
+                        st_sb = *reinterpret_cast<const float4*>(sBb + scol);
+                    } else {
+                        st_sb.x = sBb[scol / p.gb];
+                        st_sb.y = sBb[(scol + 1) / p.gb];
+                        st_sb.z = sBb[(scol + 2) / p.gb];
+                        st_sb.w = sBb[(scol + 3) / p.gb];
+                    }
+                }
+            }
+            int32_t sums[NC][32];
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sums[c][i] = 0;
+            for (int ch = 0; ch < nch; ++ch) {
+                const uint32_t ab = it & 1u;
+                const uint32_t aph = (it >> 1) & 1u;
+                if (!mbar_wait(&tfull[ab], aph, abort_flag, p.err_word)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb = tmem_base + lane_off + ab * BN + colgrp * Cfg::EPI_COLS;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t r[16];
+                        tmem_ld16(tb + c * 32 + h * 16, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            sums[c][h * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
+                }
+                release(ab);
+                ++it;
+            }
+            if (!ok) break;
+            if (staged) {
+                int32_t* stg = reinterpret_cast<int32_t*>(smem) + ew * 32 * PITCH;
+                fence_proxy_async_smem();
+#pragma unroll
+                for (int c = 0; c < NC; ++c)
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        *reinterpret_cast<int4*>(stg + lane * PITCH + c * 32 + 4 * v) =
+                            make_int4(sums[c][4 * v], sums[c][4 * v + 1], sums[c][4 * v + 2],
+                                      sums[c][4 * v + 3]);
+                __syncwarp();
+                const int j = lane % F4_ROW;
+                float* Cf = static_cast<float*>(p.C);
+                const float4 s4 = st_sb;
+#pragma unroll 4
+                for (int r0 = 0; r0 < 32; r0 += ROWS_STEP) {
+                    const int r = r0 + lane / F4_ROW;
+                    const float sr = __shfl_sync(0xffffffffu, st_sa, r);
+                    const int grow = m0 + quarter * 32 + r;
+                    if (grow < p.M && scol_ok) {
+                        const int4 a = *reinterpret_cast<const int4*>(stg + r * PITCH + 4 * j);
+                        const int64_t o = static_cast<int64_t>(b) * p.strideC +
+                                          static_cast<int64_t>(grow) * p.N + scol;
+                        if (p.acc_out) st_v4(p.acc_out + o, make_uint4(a.x, a.y, a.z, a.w));
+                        if (Cf)
+                            st_v4(Cf + o, make_uint4(
+                                __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.x), sr), s4.x)),
+                                __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.y), sr), s4.y)),
+                                __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.z), sr), s4.z)),
+                                __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.w), sr), s4.w))));
+                    }
+                }
+            } else if (row < p.M) {
+                const float sArow = p.sa[static_cast<int64_t>(b) * p.Mg + row / p.ga];
+                const float* sBb = p.sb + static_cast<int64_t>(b) * p.Ng;
+                const int64_t obase = static_cast<int64_t>(b) * p.strideC + static_cast<int64_t>(row) * p.N;
+                float* Cf = static_cast<float*>(p.C);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const int col0 = n0 + colgrp * Cfg::EPI_COLS + c * 32;
+                    if (p.vec_store && col0 + 32 <= p.N) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float4 s4;
+                            if (p.sb_vec) {
+                                s4 = *reinterpret_cast<const float4*>(sBb + col0 + 4 * v);
+                            } else {
+                                s4.x = sBb[(col0 + 4 * v) / p.gb];
+                                s4.y = sBb[(col0 + 4 * v + 1) / p.gb];
+                                s4.z = sBb[(col0 + 4 * v + 2) / p.gb];
+                                s4.w = sBb[(col0 + 4 * v + 3) / p.gb];
+                            }
+                            const int32_t a0 = sums[c][4 * v], a1 = sums[c][4 * v + 1];
+                            const int32_t a2 = sums[c][4 * v + 2], a3 = sums[c][4 * v + 3];
+                            if (p.acc_out)
+                                st_v4(p.acc_out + obase + col0 + 4 * v,
+                                      make_uint4(a0, a1, a2, a3));
+                            if (Cf) {
+                                float4 o;
+                                o.x = __fmul_rn(__fmul_rn(__int2float_rn(a0), sArow), s4.x);
+                                o.y = __fmul_rn(__fmul_rn(__int2float_rn(a1), sArow), s4.y);
+                                o.z = __fmul_rn(__fmul_rn(__int2float_rn(a2), sArow), s4.z);
+                                o.w = __fmul_rn(__fmul_rn(__int2float_rn(a3), sArow), s4.w);
+                                st_v4(Cf + obase + col0 + 4 * v,
+                                      make_uint4(__float_as_uint(o.x), __float_as_uint(o.y),
+                                                 __float_as_uint(o.z), __float_as_uint(o.w)));
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int col = col0 + i;
+                            if (col < p.N) {
+                                if (p.acc_out) p.acc_out[obase + col] = sums[c][i];
+                                if (Cf)
+                                    Cf[obase + col] = __fmul_rn(
+                                        __fmul_rn(__int2float_rn(sums[c][i]), sArow),
+                                        sBb[col / p.gb]);
+                            }
+                        }
+                    }
+                }
+            }
+        } else {
+            const uint32_t ab = it & 1u;
+            const uint32_t aph = (it >> 1) & 1u;
+            if (!mbar_wait(&tfull[ab], aph, abort_flag, p.err_word)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tb = tmem_base + lane_off + ab * BN + colgrp * Cfg::EPI_COLS;
+            uint16_t* Cb = static_cast<uint16_t*>(p.C);
+            const int64_t obase = static_cast<int64_t>(row) * p.N;
+            // one 32-column piece of this warp's 32 rows: scale, round, store
+            auto emit = [&](uint32_t (&r)[32], const int col0) {
+                if (p.bias && row < p.M) {
+                    // bias fused into the epilogue: fl32(fl32(acc*sa)*sb) + bias[col]
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = col0 + i;
+                        const float bj = col < p.N ? p.bias[col] : 0.0f;
+                        r[i] = __float_as_uint(__fadd_rn(
+                            __fmul_rn(__fmul_rn(__uint_as_float(r[i]), fsa), fsb), bj));
+                    }
+                }
+                const float esa = p.bias ? 1.0f : fsa;   // scaling already applied above
+                const float esb = p.bias ? 1.0f : fsb;
+                if (row < p.M && p.out_e4m3) {
+                    // E4M3 output: code = e4m3(fl32(fl32(acc*sa)*sb) / out_scale)
+                    uint8_t* C8 = static_cast<uint8_t*>(p.C);
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float w = __fmul_rn(__fmul_rn(__uint_as_float(r[4 * i + e]), esa), esb);
+                            v[e] = ofast ? fp8_quotient(w, fos, foy) : __fdiv_rn(w, fos);
+                        }
+                        pk[i] = fp8x2<0>(v[0], v[1]) | (fp8x2<0>(v[2], v[3]) << 16);
+                    }
+                    if (p.vec_store && col0 + 32 <= p.N) {
+                        st_v4(C8 + obase + col0, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                        st_v4(C8 + obase + col0 + 16, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < p.N)
+                                C8[obase + col0 + i] = static_cast<uint8_t>(pk[i >> 2] >> (8 * (i & 3)));
+                    }
+                } else if (!p.out_e4m3 && p.tma_store) {
+                    // The warp's 32 rows x 32 columns go out as one TMA box: each
+                    // lane writes its 64-byte row into a 64-byte-swizzled staging
+                    // buffer (16-byte piece j of row r sits at piece j ^ ((r >> 1) & 3),
+                    // which keeps the writes conflict-free); rows or columns past
+                    // the matrix are clipped by the store.
+                    uint8_t* buf = epi_stage + (ew * 2 + (sc & 1u)) * 2048;
+                    if (lane == 0 && sc >= 2) bulk_wait_read<1>();   // the box two back is read
+                    __syncwarp();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = bf16x2_bits(__fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), esa), esb),
+                                            __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), esa), esb));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, buf, col0, m0 + quarter * 32);
+                        bulk_commit();
+                    }
+                    ++sc;
+                } else if (row < p.M) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float lo = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), esa), esb);
+                        const float hi = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), esa), esb);
+                        pk[i] = bf16x2_bits(lo, hi);
+                    }
+                    if (p.vec_store && col0 + 32 <= p.N) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            st_v4(Cb + obase + col0 + 8 * v,
+                                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < p.N)
+                                Cb[obase + col0 + i] =
+                                    static_cast<uint16_t>((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
+                    }
+                }
+            };
+#pragma unroll 1
+            for (int c = 0; c < Cfg::EPI_COLS / 32; c += 2) {
+                // two TMEM loads in flight behind one wait
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tb + c * 32, r0);
+                tmem_ld32(tb + (c + 1) * 32, r1);
+                tmem_ld_wait();
+                const int col0 = n0 + colgrp * Cfg::EPI_COLS + c * 32;
+                emit(r0, col0);
+                emit(r1, col0 + 32);
+            }
+            release(ab);
+            ++it;
+        }
+    }
+    // the staged output boxes must be written (and their buffers read) before exit
+    if (!I8 && lane == 0 && sc > 0) bulk_wait_all();
+}
+
 template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -232,441 +731,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
 
     const int total = p.mt * p.nt * p.batch;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (elect_one_sync()) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int issued_phase[Cfg::STAGES];
-            for (int s = 0; s < Cfg::STAGES; ++s) issued_phase[s] = -1;
-            bool ok = true;
-            for (int t = cta_unit; t < total && ok; t += num_units) {
-                int b, mb, nb;
-                tile_coords(t, p, b, mb, nb);
-                const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
-                const int n0 = nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
-                for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err_word)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sA = smem + stage * Cfg::STAGE;
-                    uint8_t* sB = sA + Cfg::A_BYTES;
-                    if (PAIR) {
-                        // both CTAs' bytes complete on the leader's barrier
-                        const uint32_t fb = cluster_addr(&full[stage], 0);
-                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::STAGE);
-                        if (I8) {
-                            const int kx = kb * (kBKBytes / 2);
-                            tma_load_3d_pair(sA, &tmA, fb, kx, m0, b);
-                            tma_load_3d_pair(sB, &tmB, fb, kx, n0, b);
-                        } else {
-                            const int kx = kb * kBKBytes;
-                            if (A_MN) tma_load_2d_pair(sA, &tmA, fb, m0, kx);
-                            else tma_load_2d_pair(sA, &tmA, fb, kx, m0);
-                            if (B_MN) {
-#pragma unroll
-                                for (int j = 0; j < Cfg::B_ROWS / 128; ++j)
-                                    tma_load_2d_pair(sB + j * Cfg::MN_LBO, &tmB, fb, n0 + j * 128, kx);
-                            } else {
-                                tma_load_2d_pair(sB, &tmB, fb, kx, n0);
-                            }
-                        }
-                    } else {
-                        mbar_arrive_expect_tx(&full[stage], Cfg::STAGE);
-                        if (I8) {
-                            const int kx = kb * (kBKBytes / 2);
-                            tma_load_3d(sA, &tmA, &full[stage], kx, m0, b);
-                            tma_load_3d(sB, &tmB, &full[stage], kx, n0, b);
-                        } else {
-                            const int kx = kb * kBKBytes;
-                            if (A_MN) tma_load_2d(sA, &tmA, &full[stage], m0, kx);
-                            else tma_load_2d(sA, &tmA, &full[stage], kx, m0);
-                            if (B_MN) {
-#pragma unroll
-                                for (int j = 0; j < Cfg::B_ROWS / 128; ++j)
-                                    tma_load_2d(sB + j * Cfg::MN_LBO, &tmB, &full[stage], n0 + j * 128, kx);
-                            } else {
-                                tma_load_2d(sB, &tmB, &full[stage], kx, n0);
-                            }
-                        }
-                    }
-                    issued_phase[stage] = static_cast<int>(phase);
-                    if (++stage == Cfg::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok && leader) {
-                // let every copy signalled on this CTA's barriers land before it exits
-                for (int s = 0; s < Cfg::STAGES; ++s)
-                    if (issued_phase[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(issued_phase[s]));
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (leader)
-        if (leader && elect_one_sync()) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t it = 0;
-            bool ok = true;
-            bool issued = false;
-            for (int t = cta_unit; t < total && ok; t += num_units) {
-                for (int ch = 0; ch < nch && ok; ++ch) {
-                    const uint32_t ab = it & 1u;
-                    const uint32_t aph = (it >> 1) & 1u;
-                    if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, p.err_word)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + ab * BN;
-                    const int kb0 = ch * kbpc;
-                    const int kb1 = min(p.nkb, kb0 + kbpc);
-                    for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag, p.err_word)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a_addr = smem_addr(smem + stage * Cfg::STAGE);
-                        const uint32_t b_addr = a_addr + Cfg::A_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < kBKBytes / 32; ++kk) {
-                            const uint64_t ad =
-                                A_MN ? sdesc_sw128(a_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
-                                     : sdesc_sw128(a_addr + kk * Cfg::KSTEP_K, 16, 1024);
-                            const uint64_t bd =
-                                B_MN ? sdesc_sw128(b_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
-                                     : sdesc_sw128(b_addr + kk * Cfg::KSTEP_K, 16, 1024);
-                            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-                            if (PAIR) {
-                                if (I8) mma_pair_f16(d_tmem, ad, bd, p.idesc, acc);
-                                else mma_pair_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
-                            } else {
-                                if (I8) mma_f16(d_tmem, ad, bd, p.idesc, acc);
-                                else mma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
-                            }
-                        }
-                        issued = true;
-                        if (PAIR) mma_commit_pair(&empty[stage], 3);   // frees the stage in both CTAs
-                        else mma_commit(&empty[stage]);
-                        if (++stage == Cfg::STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                    if (PAIR) mma_commit_pair(&tfull[ab], 3);          // both epilogues may read
-                    else mma_commit(&tfull[ab]);
-                    ++it;
-                }
-            }
-            if (!ok && issued) {
-                // make every MMA already issued finish before TMEM is released
-                if (PAIR) mma_commit_pair(drain, 1);
-                else mma_commit(drain);
-                mbar_wait_drain(drain, 0);
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ epilogue
-        const int ew = warp - 2;
-        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
-        const int colgrp = ew >> 2;            // which EPI_COLS-wide column group
-        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        // where this warp reports that it has read an accumulator: the leader's barrier
-        const uint32_t tempty_leader[2] = {PAIR ? cluster_addr(&tempty[0], 0) : 0u,
-                                           PAIR ? cluster_addr(&tempty[1], 0) : 0u};
-        float fsa = 0.0f, fsb = 0.0f, fos = 1.0f, foy = 1.0f;
-        bool ofast = true;
-        if (!I8) {
-            fsa = *p.sa;
-            fsb = *p.sb;
-            if (p.out_e4m3) {
-                fos = *p.out_scale;
-                foy = __frcp_rn(fos);
-                ofast = fos >= 0x1p-40f && fos <= 0x1p40f;
-            }
-        }
-        uint32_t it = 0;
-        uint32_t sc = 0;                       // output boxes this warp has stored
-        bool ok = true;
-        auto release = [&](uint32_t ab) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (PAIR && !leader) mbar_arrive_cluster(tempty_leader[ab]);
-                else mbar_arrive(&tempty[ab]);
-            }
-        };
-        for (int t = cta_unit; t < total && ok; t += num_units) {
-            int b, mb, nb;
-            tile_coords(t, p, b, mb, nb);
-            const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
-            const int n0 = nb * BN;
-            const int row = m0 + quarter * 32 + lane;
-            if (I8) {
-                constexpr int NC = Cfg::EPI_COLS / 32;
-                // A CTA's last tile: every MMA has completed and no TMA load is
-                // pending once its last accumulator is read, so the operand
-                // stages are free.  Each warp stages its 32 rows there and then
-                // writes whole row runs (one 512-byte run, or two 256-byte ones,
-                // per instruction) instead of a 16-byte piece in each of 32
-                // rows.  On one-wave problems this store is the exposed tail of
-                // the kernel, so its scales are loaded before the accumulator
-                // is waited for.
-                constexpr int PITCH = Cfg::EPI_COLS + 4;   // int32 words per staged row
-                constexpr int F4_ROW = Cfg::EPI_COLS / 4;   // 16-byte pieces per row
-                constexpr int ROWS_STEP = 32 / F4_ROW;      // rows one warp-wide store covers
-                static_assert(Cfg::EPI_WARPS * 32 * PITCH * 4 <= Cfg::STAGES * Cfg::STAGE,
-                              "staged output fits in the operand stages");
-                const bool staged = p.vec_store && t + num_units >= total;
-                const int scol = n0 + colgrp * Cfg::EPI_COLS + 4 * (lane % F4_ROW);
-                const bool scol_ok = scol < p.N;   // N % 4 == 0: all four columns are in range
-                float st_sa = 0.0f;
-                float4 st_sb = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (staged) {
-                    if (row < p.M) st_sa = p.sa[static_cast<int64_t>(b) * p.Mg + row / p.ga];
-                    if (p.C && scol_ok) {
-                        const float* sBb = p.sb + static_cast<int64_t>(b) * p.Ng;
-                        if (p.sb_vec) {
-                            st_sb = *reinterpret_cast<const float4*>(sBb + scol);
-                        } else {
-                            st_sb.x = sBb[scol / p.gb];
-                            st_sb.y = sBb[(scol + 1) / p.gb];
-                            st_sb.z = sBb[(scol + 2) / p.gb];
-                            st_sb.w = sBb[(scol + 3) / p.gb];
-                        }
-                    }
-                }
-                int32_t sums[NC][32];
-#pragma unroll
-                for (int c = 0; c < NC; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) sums[c][i] = 0;
-                for (int ch = 0; ch < nch; ++ch) {
-                    const uint32_t ab = it & 1u;
-                    const uint32_t aph = (it >> 1) & 1u;
-                    if (!mbar_wait(&tfull[ab], aph, abort_flag, p.err_word)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t tb = tmem_base + lane_off + ab * BN + colgrp * Cfg::EPI_COLS;
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            uint32_t r[16];
-                            tmem_ld16(tb + c * 32 + h * 16, r);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                sums[c][h * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
-                        }
-                    }
-                    release(ab);
-                    ++it;
-                }
-                if (!ok) break;
-                if (staged) {
-                    int32_t* stg = reinterpret_cast<int32_t*>(smem) + ew * 32 * PITCH;
-                    fence_proxy_async_smem();
-#pragma unroll
-                    for (int c = 0; c < NC; ++c)
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            *reinterpret_cast<int4*>(stg + lane * PITCH + c * 32 + 4 * v) =
-                                make_int4(sums[c][4 * v], sums[c][4 * v + 1], sums[c][4 * v + 2],
-                                          sums[c][4 * v + 3]);
-                    __syncwarp();
-                    const int j = lane % F4_ROW;
-                    float* Cf = static_cast<float*>(p.C);
-                    const float4 s4 = st_sb;
-#pragma unroll 4
-                    for (int r0 = 0; r0 < 32; r0 += ROWS_STEP) {
-                        const int r = r0 + lane / F4_ROW;
-                        const float sr = __shfl_sync(0xffffffffu, st_sa, r);
-                        const int grow = m0 + quarter * 32 + r;
-                        if (grow < p.M && scol_ok) {
-                            const int4 a = *reinterpret_cast<const int4*>(stg + r * PITCH + 4 * j);
-                            const int64_t o = static_cast<int64_t>(b) * p.strideC +
-                                              static_cast<int64_t>(grow) * p.N + scol;
-                            if (p.acc_out) st_v4(p.acc_out + o, make_uint4(a.x, a.y, a.z, a.w));
-                            if (Cf)
-                                st_v4(Cf + o, make_uint4(
-                                    __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.x), sr), s4.x)),
-                                    __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.y), sr), s4.y)),
-                                    __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.z), sr), s4.z)),
-                                    __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.w), sr), s4.w))));
-                        }
-                    }
-                } else if (row < p.M) {
-                    const float sArow = p.sa[static_cast<int64_t>(b) * p.Mg + row / p.ga];
-                    const float* sBb = p.sb + static_cast<int64_t>(b) * p.Ng;
-                    const int64_t obase = static_cast<int64_t>(b) * p.strideC + static_cast<int64_t>(row) * p.N;
-                    float* Cf = static_cast<float*>(p.C);
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        const int col0 = n0 + colgrp * Cfg::EPI_COLS + c * 32;
-                        if (p.vec_store && col0 + 32 <= p.N) {
-#pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                float4 s4;
-                                if (p.sb_vec) {
-                                    s4 = *reinterpret_cast<const float4*>(sBb + col0 + 4 * v);
-                                } else {
-                                    s4.x = sBb[(col0 + 4 * v) / p.gb];
-                                    s4.y = sBb[(col0 + 4 * v + 1) / p.gb];
-                                    s4.z = sBb[(col0 + 4 * v + 2) / p.gb];
-                                    s4.w = sBb[(col0 + 4 * v + 3) / p.gb];
-                                }
-                                const int32_t a0 = sums[c][4 * v], a1 = sums[c][4 * v + 1];
-                                const int32_t a2 = sums[c][4 * v + 2], a3 = sums[c][4 * v + 3];
-                                if (p.acc_out)
-                                    st_v4(p.acc_out + obase + col0 + 4 * v,
-                                          make_uint4(a0, a1, a2, a3));
-                                if (Cf) {
-                                    float4 o;
-                                    o.x = __fmul_rn(__fmul_rn(__int2float_rn(a0), sArow), s4.x);
-                                    o.y = __fmul_rn(__fmul_rn(__int2float_rn(a1), sArow), s4.y);
-                                    o.z = __fmul_rn(__fmul_rn(__int2float_rn(a2), sArow), s4.z);
-                                    o.w = __fmul_rn(__fmul_rn(__int2float_rn(a3), sArow), s4.w);
-                                    st_v4(Cf + obase + col0 + 4 * v,
-                                          make_uint4(__float_as_uint(o.x), __float_as_uint(o.y),
-                                                     __float_as_uint(o.z), __float_as_uint(o.w)));
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int col = col0 + i;
-                                if (col < p.N) {
-                                    if (p.acc_out) p.acc_out[obase + col] = sums[c][i];
-                                    if (Cf)
-                                        Cf[obase + col] = __fmul_rn(
-                                            __fmul_rn(__int2float_rn(sums[c][i]), sArow),
-                                            sBb[col / p.gb]);
-                                }
-                            }
-                        }
-                    }
-                }
-            } else {
-                const uint32_t ab = it & 1u;
-                const uint32_t aph = (it >> 1) & 1u;
-                if (!mbar_wait(&tfull[ab], aph, abort_flag, p.err_word)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t tb = tmem_base + lane_off + ab * BN + colgrp * Cfg::EPI_COLS;
-                uint16_t* Cb = static_cast<uint16_t*>(p.C);
-                const int64_t obase = static_cast<int64_t>(row) * p.N;
-                // one 32-column piece of this warp's 32 rows: scale, round, store
-                auto emit = [&](uint32_t (&r)[32], const int col0) {
-                    if (p.bias && row < p.M) {
-                        // bias fused into the epilogue: fl32(fl32(acc*sa)*sb) + bias[col]
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int col = col0 + i;
-                            const float bj = col < p.N ? p.bias[col] : 0.0f;
-                            r[i] = __float_as_uint(__fadd_rn(
-                                __fmul_rn(__fmul_rn(__uint_as_float(r[i]), fsa), fsb), bj));
-                        }
-                    }
-                    const float esa = p.bias ? 1.0f : fsa;   // scaling already applied above
-                    const float esb = p.bias ? 1.0f : fsb;
-                    if (row < p.M && p.out_e4m3) {
-                        // E4M3 output: code = e4m3(fl32(fl32(acc*sa)*sb) / out_scale)
-                        uint8_t* C8 = static_cast<uint8_t*>(p.C);
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            float v[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float w = __fmul_rn(__fmul_rn(__uint_as_float(r[4 * i + e]), esa), esb);
-                                v[e] = ofast ? fp8_quotient(w, fos, foy) : __fdiv_rn(w, fos);
-                            }
-                            pk[i] = fp8x2<0>(v[0], v[1]) | (fp8x2<0>(v[2], v[3]) << 16);
-                        }
-                        if (p.vec_store && col0 + 32 <= p.N) {
-                            st_v4(C8 + obase + col0, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-                            st_v4(C8 + obase + col0 + 16, make_uint4(pk[4], pk[5], pk[6], pk[7]));
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (col0 + i < p.N)
-                                    C8[obase + col0 + i] = static_cast<uint8_t>(pk[i >> 2] >> (8 * (i & 3)));
-                        }
-                    } else if (!p.out_e4m3 && p.tma_store) {
-                        // The warp's 32 rows x 32 columns go out as one TMA box: each
-                        // lane writes its 64-byte row into a 64-byte-swizzled staging
-                        // buffer (16-byte piece j of row r sits at piece j ^ ((r >> 1) & 3),
-                        // which keeps the writes conflict-free); rows or columns past
-                        // the matrix are clipped by the store.
-                        uint8_t* buf = epi_stage + (ew * 2 + (sc & 1u)) * 2048;
-                        if (lane == 0 && sc >= 2) bulk_wait_read<1>();   // the box two back is read
-                        __syncwarp();
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = bf16x2_bits(__fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), esa), esb),
-                                                __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), esa), esb));
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmC, buf, col0, m0 + quarter * 32);
-                            bulk_commit();
-                        }
-                        ++sc;
-                    } else if (row < p.M) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float lo = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i]), esa), esb);
-                            const float hi = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * i + 1]), esa), esb);
-                            pk[i] = bf16x2_bits(lo, hi);
-                        }
-                        if (p.vec_store && col0 + 32 <= p.N) {
-#pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                st_v4(Cb + obase + col0 + 8 * v,
-                                      make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (col0 + i < p.N)
-                                    Cb[obase + col0 + i] =
-                                        static_cast<uint16_t>((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
-                        }
-                    }
-                };
-#pragma unroll 1
-                for (int c = 0; c < Cfg::EPI_COLS / 32; c += 2) {
-                    // two TMEM loads in flight behind one wait
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(tb + c * 32, r0);
-                    tmem_ld32(tb + (c + 1) * 32, r1);
-                    tmem_ld_wait();
-                    const int col0 = n0 + colgrp * Cfg::EPI_COLS + c * 32;
-                    emit(r0, col0);
-                    emit(r1, col0 + 32);
-                }
-                release(ab);
-                ++it;
-            }
-        }
-        // the staged output boxes must be written (and their buffers read) before exit
-        if (!I8 && lane == 0 && sc > 0) bulk_wait_all();
-    }
+    const GemmCta c{smem, epi_stage, full, empty, tfull, tempty, drain, abort_flag, tmem_base,
+                    rank, leader, cta_unit, num_units, total};
+    if (warp == 0) gemm_producer<BN, I8, A_MN, B_MN, PAIR>(tmA, tmB, p, c);
+    else if (warp == 1) gemm_mma<BN, I8, A_MN, B_MN, PAIR>(p, c, kbpc, nch);
+    else gemm_epilogue<BN, I8, A_MN, B_MN, PAIR>(tmC, p, c, nch);
 
     tc_fence_before();
     __syncthreads();

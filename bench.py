@@ -68,8 +68,8 @@ def parse():
 # those sources no longer matches, the bench reports traffic as null.
 PROFILED_TRAFFIC = {
     # profiles/traffic_large_step.md
-    "gemm_fp8_nt": {"bytes": 755166208, "sources_sha256": "af1fdb2bccc98fb3882b07c292766c3da12061a88e7d51c646f357ccf785ac44"},
-    "gemm_i8": {"bytes": 3206116352, "sources_sha256": "af1fdb2bccc98fb3882b07c292766c3da12061a88e7d51c646f357ccf785ac44"},
+    "gemm_fp8_nt": {"bytes": 775060736, "sources_sha256": "0c4c4962ef3b575962f3c4b354468457380cfe37f2bbaca93c64b58fb1ba69d5"},
+    "gemm_i8": {"bytes": 3189623296, "sources_sha256": "0c4c4962ef3b575962f3c4b354468457380cfe37f2bbaca93c64b58fb1ba69d5"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
