@@ -36,7 +36,8 @@ EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "
            "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc", "sq_quantize_fp8_ring",
            "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
            "sq_quantize_grouped_i8", "sq_gemm_i8_grouped", "sq_linear_workspace_bytes",
-           "sq_linear_forward_fp8", "sq_linear_backward_fp8", "sq_selftest_bounded_wait")
+           "sq_linear_forward_fp8", "sq_linear_backward_fp8", "sq_selftest_bounded_wait",
+           "sq_gemm_i8_stage", "sq_gemm_i8_rowscaled_staged")
 
 # size of the fixed scratch array behind sq_gemm_i8_rowscaled_noalloc
 GEMM_I8_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -100,6 +101,11 @@ def load_library():
     L.sq_linear_backward_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp, vp, i32,
                                          vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.sq_linear_backward_fp8.restype = i32
+    L.sq_gemm_i8_stage.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, vp, sz, vp]
+    L.sq_gemm_i8_stage.restype = i32
+    L.sq_gemm_i8_rowscaled_staged.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, i64, vp, vp,
+                                              vp, sz, vp]
+    L.sq_gemm_i8_rowscaled_staged.restype = i32
     L.sq_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp]
     L.sq_selftest_bounded_wait.restype = i32
     _lib = L
@@ -125,9 +131,92 @@ def _stream(stream=None):
 
 
 def _need_cuda(*ts):
+    """All given tensors on one CUDA device; returns that device.  The library
+    works on the current device, so every call runs under this device."""
+    dev = None
     for t in ts:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_cuda:
             raise ValueError("libsq works on CUDA tensors only")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"tensors on different devices: {dev} and {t.device}")
+    return dev
+
+
+def _need(t, dtype, numel=None, shape=None, what="tensor"):
+    """A caller-passed tensor of the given dtype, contiguous, and of the given
+    number of elements or shape: the library reads or writes exactly that many."""
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{what} must hold {numel} elements, got {t.numel()}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _i8_operands(A, B, sA, sB, group_a=1, group_b=1):
+    """Shapes of the INT8 GEMM operands, checked against each other and against
+    the scale vectors the epilogue reads (batch * ceil(M / group_a) and
+    batch * ceil(N / group_b) floats)."""
+    if A.dtype != torch.int8 or B.dtype != torch.int8:
+        raise TypeError("A and B must be int8 codes")
+    if A.dim() not in (2, 3) or B.dim() != A.dim():
+        raise ValueError("A and B must both be [rows, K] or both [batch, rows, K]")
+    batched = A.dim() == 3
+    A3 = A if batched else A.unsqueeze(0)
+    B3 = B if batched else B.unsqueeze(0)
+    nb, M, K = A3.shape
+    if B3.shape[0] != nb or B3.shape[2] != K:
+        raise ValueError(f"A {tuple(A.shape)} and B {tuple(B.shape)} do not share batch and K")
+    N = B3.shape[1]
+    if not (A3.is_contiguous() and B3.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    ga, gb = max(1, min(int(group_a), M)), max(1, min(int(group_b), N))
+    _need(sA, torch.float32, numel=nb * ((M + ga - 1) // ga), what="sA")
+    _need(sB, torch.float32, numel=nb * ((N + gb - 1) // gb), what="sB")
+    return A3, B3, nb, M, N, K, batched
+
+
+def _i8_outputs(C, acc_out, want_c, shape, dev):
+    if C is not None:
+        _need(C, torch.float32, shape=shape, what="C")
+    elif want_c:
+        C = torch.empty(shape, dtype=torch.float32, device=dev)
+    if acc_out is True:
+        acc_out = torch.empty(shape, dtype=torch.int32, device=dev)
+    elif acc_out is False:
+        acc_out = None
+    elif acc_out is not None:
+        _need(acc_out, torch.int32, shape=shape, what="acc_out")
+    if C is None and acc_out is None:
+        raise ValueError("ask for C, acc_out or both")
+    return C, acc_out
+
+
+def _fp8_shape(A, B, layout):
+    if A.dtype != torch.uint8 or B.dtype != torch.uint8:
+        raise TypeError("A and B must be FP8 codes (uint8)")
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    if layout == SQ_NT:
+        (M, K), (N, K2) = A.shape, B.shape
+    elif layout == SQ_NN:
+        (M, K), (K2, N) = A.shape, B.shape
+    elif layout == SQ_TN:
+        (K, M), (K2, N) = A.shape, B.shape
+    else:
+        raise ValueError("layout must be SQ_NT, SQ_NN or SQ_TN")
+    if K2 != K:
+        raise ValueError(f"A {tuple(A.shape)} and B {tuple(B.shape)} do not share K in this layout")
+    return M, N, K
 
 
 # ---------------------------------------------------------------- workspaces
@@ -149,7 +238,7 @@ def sq_quantize_rowwise_i8(x: torch.Tensor, q: torch.Tensor = None, scales: torc
                            stream=None):
     """Per-row INT8 of x (float32 or bfloat16, last dim = row, rows may be
     strided).  Returns (q int8 packed, scales float32 of shape x.shape[:-1])."""
-    _need_cuda(x)
+    dev = _need_cuda(x, q, scales)
     if x.dtype == torch.float32:
         dt = SQ_F32
     elif x.dtype == torch.bfloat16:
@@ -164,11 +253,14 @@ def sq_quantize_rowwise_i8(x: torch.Tensor, q: torch.Tensor = None, scales: torc
     ld = x2.stride(0) if rows > 1 else cols
     if q is None:
         q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    _need(q, torch.int8, numel=rows * cols, what="q")
     if scales is None:
         scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-    _check(load_library().sq_quantize_rowwise_i8(_ptr(x2), dt, rows, cols, ld, _ptr(q),
-                                                 _ptr(scales), _stream(stream)),
-           "sq_quantize_rowwise_i8")
+    _need(scales, torch.float32, numel=rows, what="scales")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_quantize_rowwise_i8(_ptr(x2), dt, rows, cols, ld, _ptr(q),
+                                                     _ptr(scales), _stream(stream)),
+               "sq_quantize_rowwise_i8")
     return q, scales
 
 
@@ -176,18 +268,21 @@ def sq_quantize_fp8(x: torch.Tensor, scale: torch.Tensor, fmt: int, workspace: t
                     x8: torch.Tensor = None, amax: torch.Tensor = None, stream=None):
     """Per-tensor FP8 of bf16 x with the step `scale` (1-element float32 on the
     device) divided out.  Returns (x8 uint8 codes, amax 1-element float32)."""
-    _need_cuda(x, scale, workspace)
-    if x.dtype != torch.bfloat16:
-        raise TypeError(f"x must be bfloat16, got {x.dtype}")
-    if not x.is_contiguous():
-        raise ValueError("x must be contiguous")
+    dev = _need_cuda(x, scale, workspace, x8, amax)
+    _need(x, torch.bfloat16, what="x")
+    _need(scale, torch.float32, numel=1, what="scale")
+    if workspace.numel() * workspace.element_size() < workspace_bytes():
+        raise ValueError("workspace is smaller than sq_workspace_bytes()")
     if x8 is None:
         x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _need(x8, torch.uint8, numel=x.numel(), what="x8")
     if amax is None:
         amax = torch.empty(1, dtype=torch.float32, device=x.device)
-    _check(load_library().sq_quantize_fp8(_ptr(x), x.numel(), _ptr(scale), int(fmt), _ptr(x8),
-                                          _ptr(amax), _ptr(workspace), _stream(stream)),
-           "sq_quantize_fp8")
+    _need(amax, torch.float32, numel=1, what="amax")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_quantize_fp8(_ptr(x), x.numel(), _ptr(scale), int(fmt), _ptr(x8),
+                                              _ptr(amax), _ptr(workspace), _stream(stream)),
+               "sq_quantize_fp8")
     return x8, amax
 
 
@@ -204,19 +299,24 @@ def sq_quantize_fp8_ring(x: torch.Tensor, fmt: int, ring: torch.Tensor, idx: int
                          amax: torch.Tensor = None, stream=None):
     """Per-tensor FP8 of bf16 x with the step ring[H]; records the amax in
     ring[idx] and publishes the next step in ring[H] on the device."""
-    _need_cuda(x, ring, workspace)
-    if x.dtype != torch.bfloat16 or not x.is_contiguous():
-        raise TypeError("x must be a contiguous bfloat16 tensor")
+    dev = _need_cuda(x, ring, workspace, x8, amax)
+    _need(x, torch.bfloat16, what="x")
     if ring.dtype != torch.float32 or not ring.is_contiguous() or ring.numel() < 3:
         raise TypeError("ring must be a contiguous float32 tensor of hist_len + 2 entries")
+    if workspace.numel() * workspace.element_size() < workspace_bytes():
+        raise ValueError("workspace is smaller than sq_workspace_bytes()")
     if x8 is None:
         x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _need(x8, torch.uint8, numel=x.numel(), what="x8")
     if amax is None:
         amax = torch.empty(1, dtype=torch.float32, device=x.device)
-    _check(load_library().sq_quantize_fp8_ring(_ptr(x), x.numel(), int(fmt), _ptr(x8), _ptr(amax),
-                                               _ptr(ring), ring.numel() - 2, int(idx), int(margin),
-                                               _ptr(workspace), _stream(stream)),
-           "sq_quantize_fp8_ring")
+    _need(amax, torch.float32, numel=1, what="amax")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_quantize_fp8_ring(_ptr(x), x.numel(), int(fmt), _ptr(x8),
+                                                   _ptr(amax), _ptr(ring), ring.numel() - 2,
+                                                   int(idx), int(margin), _ptr(workspace),
+                                                   _stream(stream)),
+               "sq_quantize_fp8_ring")
     return x8, amax
 
 
@@ -225,7 +325,7 @@ def sq_quantize_grouped_i8(x: torch.Tensor, group_rows: int, q: torch.Tensor = N
                            stream=None):
     """Row-group INT8 of a 2-D float32/bfloat16 x: groups of group_rows rows
     share a scale (group_rows >= rows: per tensor).  Returns (q, scales)."""
-    _need_cuda(x)
+    dev = _need_cuda(x, q, scales, workspace)
     dt = {torch.float32: SQ_F32, torch.bfloat16: SQ_BF16}.get(x.dtype)
     if dt is None or x.dim() != 2 or (x.numel() and x.stride(1) != 1):
         raise TypeError("x must be 2-D float32 or bfloat16 with contiguous rows")
@@ -234,43 +334,41 @@ def sq_quantize_grouped_i8(x: torch.Tensor, group_rows: int, q: torch.Tensor = N
     ng = (rows + g - 1) // g
     if q is None:
         q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    _need(q, torch.int8, numel=rows * cols, what="q")
     if scales is None:
         scales = torch.empty(ng, dtype=torch.float32, device=x.device)
+    _need(scales, torch.float32, numel=ng, what="scales")
     if workspace is None and g > 1:
         workspace = torch.empty(int(load_library().sq_quantize_grouped_i8_workspace_bytes(rows, g)),
                                 dtype=torch.uint8, device=x.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     ld = x.stride(0) if rows > 1 else cols
-    _check(load_library().sq_quantize_grouped_i8(_ptr(x), dt, rows, cols, ld, g, _ptr(q),
-                                                 _ptr(scales), _ptr(workspace), nbytes,
-                                                 _stream(stream)),
-           "sq_quantize_grouped_i8")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_quantize_grouped_i8(_ptr(x), dt, rows, cols, ld, g, _ptr(q),
+                                                     _ptr(scales), _ptr(workspace), nbytes,
+                                                     _stream(stream)),
+               "sq_quantize_grouped_i8")
     return q, scales
+
+
+def _ws_bytes(workspace):
+    return workspace.numel() * workspace.element_size()
 
 
 def sq_gemm_i8_grouped(A: torch.Tensor, sA: torch.Tensor, group_a: int, B: torch.Tensor,
                        sB: torch.Tensor, group_b: int, workspace: torch.Tensor,
                        C: torch.Tensor = None, acc_out=None, want_c: bool = True, stream=None):
     """INT8 GEMM with row-group scales sA[b][i // group_a], sB[b][j // group_b]."""
-    _need_cuda(A, B, sA, sB, workspace)
-    batched = A.dim() == 3
-    A3 = A if batched else A.unsqueeze(0)
-    B3 = B if batched else B.unsqueeze(0)
-    nb, M, K = A3.shape
-    N = B3.shape[1]
-    if not (A3.is_contiguous() and B3.is_contiguous()):
-        raise ValueError("A and B must be contiguous")
+    dev = _need_cuda(A, B, sA, sB, workspace, C,
+                     acc_out if isinstance(acc_out, torch.Tensor) else None)
+    A3, B3, nb, M, N, K, batched = _i8_operands(A, B, sA, sB, group_a, group_b)
     shape = (nb, M, N) if batched else (M, N)
-    if want_c and C is None:
-        C = torch.empty(shape, dtype=torch.float32, device=A.device)
-    if acc_out is True:
-        acc_out = torch.empty(shape, dtype=torch.int32, device=A.device)
-    elif acc_out is False:
-        acc_out = None
-    _check(load_library().sq_gemm_i8_grouped(
-        _ptr(A3), _ptr(sA), int(group_a), _ptr(B3), _ptr(sB), int(group_b), nb, M, N, K, M * K,
-        N * K, M * N, _ptr(C), _ptr(acc_out), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)), "sq_gemm_i8_grouped")
+    C, acc_out = _i8_outputs(C, acc_out, want_c, shape, A.device)
+    with torch.cuda.device(dev):
+        _check(load_library().sq_gemm_i8_grouped(
+            _ptr(A3), _ptr(sA), int(group_a), _ptr(B3), _ptr(sB), int(group_b), nb, M, N, K,
+            M * K, N * K, M * N, _ptr(C), _ptr(acc_out), _ptr(workspace), _ws_bytes(workspace),
+            _stream(stream)), "sq_gemm_i8_grouped")
     return C, acc_out
 
 
@@ -281,25 +379,57 @@ def sq_gemm_i8_rowscaled(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB:
 
     A: [M,K] or [batch,M,K] int8, B: [N,K] or [batch,N,K].  Returns (C, acc_out);
     pass acc_out=True to get the exact int32 accumulators too."""
-    _need_cuda(A, B, sA, sB, workspace)
-    batched = A.dim() == 3
-    A3 = A if batched else A.unsqueeze(0)
-    B3 = B if batched else B.unsqueeze(0)
-    nb, M, K = A3.shape
-    N = B3.shape[1]
-    if not (A3.is_contiguous() and B3.is_contiguous()):
-        raise ValueError("A and B must be contiguous")
+    dev = _need_cuda(A, B, sA, sB, workspace, C,
+                     acc_out if isinstance(acc_out, torch.Tensor) else None)
+    A3, B3, nb, M, N, K, batched = _i8_operands(A, B, sA, sB)
     shape = (nb, M, N) if batched else (M, N)
-    if want_c and C is None:
-        C = torch.empty(shape, dtype=torch.float32, device=A.device)
-    if acc_out is True:
-        acc_out = torch.empty(shape, dtype=torch.int32, device=A.device)
-    elif acc_out is False:
-        acc_out = None
-    _check(load_library().sq_gemm_i8_rowscaled(
-        _ptr(A3), _ptr(sA), _ptr(B3), _ptr(sB), nb, M, N, K, M * K, N * K, M * N,
-        _ptr(C), _ptr(acc_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)), "sq_gemm_i8_rowscaled")
+    C, acc_out = _i8_outputs(C, acc_out, want_c, shape, A.device)
+    with torch.cuda.device(dev):
+        _check(load_library().sq_gemm_i8_rowscaled(
+            _ptr(A3), _ptr(sA), _ptr(B3), _ptr(sB), nb, M, N, K, M * K, N * K, M * N,
+            _ptr(C), _ptr(acc_out), _ptr(workspace), _ws_bytes(workspace),
+            _stream(stream)), "sq_gemm_i8_rowscaled")
+    return C, acc_out
+
+
+def sq_gemm_i8_stage(A: torch.Tensor, B: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """First phase of sq_gemm_i8_rowscaled: stage the int8 codes of A and B
+    (shapes as there) in `workspace` for sq_gemm_i8_rowscaled_staged."""
+    dev = _need_cuda(A, B, workspace)
+    if A.dtype != torch.int8 or B.dtype != torch.int8:
+        raise TypeError("A and B must be int8 codes")
+    if A.dim() not in (2, 3) or B.dim() != A.dim():
+        raise ValueError("A and B must both be [rows, K] or both [batch, rows, K]")
+    A3 = A if A.dim() == 3 else A.unsqueeze(0)
+    B3 = B if B.dim() == 3 else B.unsqueeze(0)
+    nb, M, K = A3.shape
+    if B3.shape[0] != nb or B3.shape[2] != K or not (A3.is_contiguous() and B3.is_contiguous()):
+        raise ValueError("A and B must be contiguous and share batch and K")
+    N = B3.shape[1]
+    with torch.cuda.device(dev):
+        _check(load_library().sq_gemm_i8_stage(_ptr(A3), _ptr(B3), nb, M, N, K, M * K, N * K,
+                                               _ptr(workspace), _ws_bytes(workspace),
+                                               _stream(stream)), "sq_gemm_i8_stage")
+
+
+def sq_gemm_i8_rowscaled_staged(sA: torch.Tensor, sB: torch.Tensor, shape, workspace: torch.Tensor,
+                                C: torch.Tensor = None, acc_out=None, want_c: bool = True,
+                                stream=None):
+    """Second phase of sq_gemm_i8_rowscaled on a workspace staged by
+    sq_gemm_i8_stage for operands of shape = (batch, M, N, K) (batch 0: the
+    2-D form).  Returns (C, acc_out)."""
+    dev = _need_cuda(sA, sB, workspace, C, acc_out if isinstance(acc_out, torch.Tensor) else None)
+    nb, M, N, K = (int(v) for v in shape)
+    batched = nb > 0
+    nb = max(nb, 1)
+    _need(sA, torch.float32, numel=nb * M, what="sA")
+    _need(sB, torch.float32, numel=nb * N, what="sB")
+    oshape = (nb, M, N) if batched else (M, N)
+    C, acc_out = _i8_outputs(C, acc_out, want_c, oshape, sA.device)
+    with torch.cuda.device(dev):
+        _check(load_library().sq_gemm_i8_rowscaled_staged(
+            _ptr(sA), _ptr(sB), nb, M, N, K, M * K, N * K, M * N, _ptr(C), _ptr(acc_out),
+            _ptr(workspace), _ws_bytes(workspace), _stream(stream)), "sq_gemm_i8_rowscaled_staged")
     return C, acc_out
 
 
@@ -311,24 +441,14 @@ def sq_gemm_i8_rowscaled_noalloc(A: torch.Tensor, sA: torch.Tensor, B: torch.Ten
     nothing (the output tensors are created here only when not passed in).
     Problems whose staged operands exceed the array raise SQError
     (SQ_ERR_UNSUPPORTED).  Calls that overlap on the GPU race on the array."""
-    _need_cuda(A, B, sA, sB)
-    batched = A.dim() == 3
-    A3 = A if batched else A.unsqueeze(0)
-    B3 = B if batched else B.unsqueeze(0)
-    nb, M, K = A3.shape
-    N = B3.shape[1]
-    if not (A3.is_contiguous() and B3.is_contiguous()):
-        raise ValueError("A and B must be contiguous")
+    dev = _need_cuda(A, B, sA, sB, C, acc_out if isinstance(acc_out, torch.Tensor) else None)
+    A3, B3, nb, M, N, K, batched = _i8_operands(A, B, sA, sB)
     shape = (nb, M, N) if batched else (M, N)
-    if want_c and C is None:
-        C = torch.empty(shape, dtype=torch.float32, device=A.device)
-    if acc_out is True:
-        acc_out = torch.empty(shape, dtype=torch.int32, device=A.device)
-    elif acc_out is False:
-        acc_out = None
-    st = load_library().sq_gemm_i8_rowscaled_noalloc(
-        _ptr(A3), _ptr(sA), _ptr(B3), _ptr(sB), nb, M, N, K, M * K, N * K, M * N, _ptr(C),
-        _ptr(acc_out), _stream(stream))
+    C, acc_out = _i8_outputs(C, acc_out, want_c, shape, A.device)
+    with torch.cuda.device(dev):
+        st = load_library().sq_gemm_i8_rowscaled_noalloc(
+            _ptr(A3), _ptr(sA), _ptr(B3), _ptr(sB), nb, M, N, K, M * K, N * K, M * N, _ptr(C),
+            _ptr(acc_out), _stream(stream))
     if st == SQ_ERR_UNSUPPORTED:
         raise SQError(st, "sq_gemm_i8_rowscaled_noalloc: staged operands "
                           f"({gemm_i8_workspace_bytes(nb, M, N, K)} bytes) exceed the "
@@ -340,22 +460,17 @@ def sq_gemm_i8_rowscaled_noalloc(A: torch.Tensor, sA: torch.Tensor, B: torch.Ten
 def sq_gemm_fp8_scaled(A: torch.Tensor, B: torch.Tensor, sa: torch.Tensor, sb: torch.Tensor,
                        fmt: int, layout: int, C: torch.Tensor = None, stream=None):
     """bf16 C = (acc * sa) * sb for FP8 codes A, B (uint8) in layout NT/NN/TN."""
-    _need_cuda(A, B, sa, sb)
-    if not (A.is_contiguous() and B.is_contiguous()):
-        raise ValueError("A and B must be contiguous")
-    if layout == SQ_NT:
-        (M, K), N = A.shape, B.shape[0]
-    elif layout == SQ_NN:
-        (M, K), N = A.shape, B.shape[1]
-    elif layout == SQ_TN:
-        (K, M), N = A.shape, B.shape[1]
-    else:
-        raise ValueError("layout must be SQ_NT, SQ_NN or SQ_TN")
+    dev = _need_cuda(A, B, sa, sb, C)
+    M, N, K = _fp8_shape(A, B, layout)
+    _need(sa, torch.float32, numel=1, what="sa")
+    _need(sb, torch.float32, numel=1, what="sb")
     if C is None:
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    _check(load_library().sq_gemm_fp8_scaled(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), int(fmt),
-                                             int(layout), M, N, K, _ptr(C), _stream(stream)),
-           "sq_gemm_fp8_scaled")
+    _need(C, torch.bfloat16, shape=(M, N), what="C")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_gemm_fp8_scaled(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), int(fmt),
+                                                 int(layout), M, N, K, _ptr(C), _stream(stream)),
+               "sq_gemm_fp8_scaled")
     return C
 
 
@@ -363,23 +478,18 @@ def sq_gemm_fp8_scaled_e4m3(A: torch.Tensor, B: torch.Tensor, sa: torch.Tensor, 
                             fmt: int, layout: int, out_scale: torch.Tensor, C: torch.Tensor = None,
                             stream=None):
     """E4M3 codes C = e4m3((acc * sa) * sb / out_scale) for FP8 codes A, B."""
-    _need_cuda(A, B, sa, sb, out_scale)
-    if not (A.is_contiguous() and B.is_contiguous()):
-        raise ValueError("A and B must be contiguous")
-    if layout == SQ_NT:
-        (M, K), N = A.shape, B.shape[0]
-    elif layout == SQ_NN:
-        (M, K), N = A.shape, B.shape[1]
-    elif layout == SQ_TN:
-        (K, M), N = A.shape, B.shape[1]
-    else:
-        raise ValueError("layout must be SQ_NT, SQ_NN or SQ_TN")
+    dev = _need_cuda(A, B, sa, sb, out_scale, C)
+    M, N, K = _fp8_shape(A, B, layout)
+    for t, n in ((sa, "sa"), (sb, "sb"), (out_scale, "out_scale")):
+        _need(t, torch.float32, numel=1, what=n)
     if C is None:
         C = torch.empty((M, N), dtype=torch.uint8, device=A.device)
-    _check(load_library().sq_gemm_fp8_scaled_e4m3(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), int(fmt),
-                                                  int(layout), M, N, K, _ptr(out_scale), _ptr(C),
-                                                  _stream(stream)),
-           "sq_gemm_fp8_scaled_e4m3")
+    _need(C, torch.uint8, shape=(M, N), what="C")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_gemm_fp8_scaled_e4m3(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb),
+                                                      int(fmt), int(layout), M, N, K,
+                                                      _ptr(out_scale), _ptr(C), _stream(stream)),
+               "sq_gemm_fp8_scaled_e4m3")
     return C
 
 
@@ -404,9 +514,18 @@ def sq_linear_forward_fp8(x: torch.Tensor, w: torch.Tensor, bias, sx, sw, fmt: i
     """Fused FP8 linear forward.  x bf16 [M, K]; w bf16 [N, K] (or FP8 codes
     uint8 when w_prequantized); bias None, bf16 [N], or FP8 codes uint8 [N]
     (with bias_scale).  Returns (out bf16 [M, N], x8, w8, amax_x, amax_w)."""
-    _need_cuda(x, w, workspace)
+    dev = _need_cuda(x, w, workspace, bias, sx, sw, bias_scale, x_ring, w_ring)
+    _need(x, torch.bfloat16, what="x")
+    if x.dim() != 2 or w.dim() != 2:
+        raise ValueError("x and w must be 2-D")
     M, K = x.shape
     N = w.shape[0]
+    _need(w, torch.uint8 if w_prequantized else torch.bfloat16, shape=(N, K), what="w")
+    if bias is not None:
+        _need(bias, bias.dtype, numel=N, what="bias")
+    for t, n in ((sx, "sx"), (sw, "sw"), (bias_scale, "bias_scale")):
+        if t is not None:
+            _need(t, torch.float32, numel=1, what=n)
     if bias is None:
         bkind = SQ_BIAS_NONE
     elif bias.dtype == torch.bfloat16:
@@ -423,11 +542,12 @@ def sq_linear_forward_fp8(x: torch.Tensor, w: torch.Tensor, bias, sx, sw, fmt: i
     amax_w = torch.empty(1, dtype=torch.float32, device=dev)
     xr, xh, xi, xm = _ring_args(x_ring, x_ring_idx, x_ring_margin)
     wr, wh, wi, wm = _ring_args(w_ring, w_ring_idx, w_ring_margin)
-    _check(load_library().sq_linear_forward_fp8(
-        _ptr(x), M, K, _ptr(w), int(bool(w_prequantized)), N, _ptr(bias), bkind, _ptr(bias_scale),
-        _ptr(sx), _ptr(sw), int(fmt), _ptr(xr), xh, xi, xm, _ptr(wr), wh, wi, wm, _ptr(out),
-        _ptr(x8), _ptr(w8), _ptr(amax_x), _ptr(amax_w), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)), "sq_linear_forward_fp8")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_linear_forward_fp8(
+            _ptr(x), M, K, _ptr(w), int(bool(w_prequantized)), N, _ptr(bias), bkind,
+            _ptr(bias_scale), _ptr(sx), _ptr(sw), int(fmt), _ptr(xr), xh, xi, xm, _ptr(wr), wh, wi,
+            wm, _ptr(out), _ptr(x8), _ptr(w8), _ptr(amax_x), _ptr(amax_w), _ptr(workspace),
+            _ws_bytes(workspace), _stream(stream)), "sq_linear_forward_fp8")
     return out, x8, (w if w_prequantized else w8), amax_x, amax_w
 
 
@@ -437,9 +557,17 @@ def sq_linear_backward_fp8(g: torch.Tensor, x: torch.Tensor, w: torch.Tensor, ma
     """Fused FP8 linear backward for out = x w^T.  g bf16 [T, N], x bf16 [T, K],
     w bf16 [N, K]; masks = (grad_input, grad_weight, grad_bias) booleans.
     Returns (gx [T, K] or None, gw [N, K] or None, gb [N] or None, amax_g)."""
-    _need_cuda(g, x, w, workspace)
+    dev = _need_cuda(g, x, w, workspace, sg, sw, sx, g_ring)
+    if g.dim() != 2 or x.dim() != 2 or w.dim() != 2:
+        raise ValueError("g, x and w must be 2-D")
     T, N = g.shape
     K = x.shape[1]
+    _need(g, torch.bfloat16, what="g")
+    _need(x, torch.bfloat16, shape=(T, K), what="x")
+    _need(w, torch.bfloat16, shape=(N, K), what="w")
+    for t, n in ((sg, "sg"), (sw, "sw"), (sx, "sx")):
+        if t is not None:
+            _need(t, torch.float32, numel=1, what=n)
     m = (SQ_GRAD_INPUT if masks[0] else 0) | (SQ_GRAD_WEIGHT if masks[1] else 0) | \
         (SQ_GRAD_BIAS if masks[2] else 0)
     dev = g.device
@@ -451,11 +579,12 @@ def sq_linear_backward_fp8(g: torch.Tensor, x: torch.Tensor, w: torch.Tensor, ma
     w8 = torch.empty((N, K), dtype=torch.uint8, device=dev) if masks[0] else None
     x8 = torch.empty((T, K), dtype=torch.uint8, device=dev) if masks[1] else None
     gr, gh, gi, gm = _ring_args(g_ring, g_ring_idx, g_ring_margin)
-    _check(load_library().sq_linear_backward_fp8(
-        _ptr(g), _ptr(x), _ptr(w), T, N, K, m, _ptr(sg), _ptr(sw), _ptr(sx), int(fmt), _ptr(gr),
-        gh, gi, gm, _ptr(gx), _ptr(gw), _ptr(gb), _ptr(amax_g), _ptr(g8), _ptr(w8), _ptr(x8),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
-        "sq_linear_backward_fp8")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_linear_backward_fp8(
+            _ptr(g), _ptr(x), _ptr(w), T, N, K, m, _ptr(sg), _ptr(sw), _ptr(sx), int(fmt),
+            _ptr(gr), gh, gi, gm, _ptr(gx), _ptr(gw), _ptr(gb), _ptr(amax_g), _ptr(g8), _ptr(w8),
+            _ptr(x8), _ptr(workspace), _ws_bytes(workspace), _stream(stream)),
+            "sq_linear_backward_fp8")
     return gx, gw, gb, amax_g
 
 

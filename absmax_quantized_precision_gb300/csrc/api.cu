@@ -140,48 +140,132 @@ size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K
 
 namespace {
 
+// Where the staged operands and their bounds sit in an INT8 GEMM workspace.
+struct I8Workspace {
+    uint16_t* A16;
+    uint16_t* B16;
+    unsigned* bound_a;
+    unsigned* bound_b;
+};
+
+I8Workspace i8_workspace(void* workspace, int64_t batch, int64_t M, int64_t N, int64_t K) {
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    const size_t abytes = (static_cast<size_t>(batch) * M * K * 2 + 255) & ~static_cast<size_t>(255);
+    const size_t bbytes = (static_cast<size_t>(batch) * N * K * 2 + 255) & ~static_cast<size_t>(255);
+    unsigned* bound_a = reinterpret_cast<unsigned*>(w + abytes + bbytes);
+    return I8Workspace{reinterpret_cast<uint16_t*>(w), reinterpret_cast<uint16_t*>(w + abytes),
+                       bound_a, bound_a + 256};
+}
+
+// Checks shared by both phases of the INT8 GEMM: sizes, strides of the int8
+// operands and the workspace.
+sq_status i8_check_common(int64_t batch, int64_t M, int64_t N, int64_t K, int64_t strideA,
+                          int64_t strideB, const void* workspace, size_t workspace_bytes) {
+    if (batch < 1 || M < 1 || N < 1 || K < 1) return SQ_ERR_INVALID_ARG;
+    if (!workspace) return SQ_ERR_INVALID_ARG;
+    if (strideA < M * K || strideB < N * K) return SQ_ERR_INVALID_ARG;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (K > (int64_t(1) << 17)) return SQ_ERR_UNSUPPORTED;
+    if (batch > 65535 || M > kMaxDim || N > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    if (strideA % 16 != 0 || strideB % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SQ_ERR_ALIGNMENT;
+    if (workspace_bytes < sq_gemm_i8_workspace_bytes(batch, M, N, K)) return SQ_ERR_INVALID_ARG;
+    const int64_t mt = (M + 127) / 128, nt = (N + 127) / 128;
+    if (mt * nt * batch > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    return SQ_OK;
+}
+
+// Phase 1: the int8 codes of A and B staged as exact fp16 in the workspace,
+// with the per-CTA bounds on their sums of squares.
+sq_status i8_stage(const int8_t* A, const int8_t* B, int64_t batch, int64_t M, int64_t N,
+                   int64_t K, int64_t strideA, int64_t strideB, void* workspace,
+                   DeviceState* ds, cudaStream_t st) {
+    const I8Workspace w = i8_workspace(workspace, batch, M, N, K);
+    int nparts_a = 0, nparts_b = 0;
+    return from_cuda(sq::launch_i8_to_f16_pair(A, M, B, N, batch, K, strideA, strideB, w.A16, w.B16,
+                                               w.bound_a, &nparts_a, w.bound_b, &nparts_b,
+                                               ds->err_word, st, ds->sms));
+}
+
+// Phase 2: the GEMM on the staged operands with the dequantization epilogue.
+// The bound counts are those the staging of the same sizes reports.
+sq_status i8_gemm_staged(const float* sA, int64_t ga, const float* sB, int64_t gb, int64_t batch,
+                         int64_t M, int64_t N, int64_t K, int64_t strideA, int64_t strideB,
+                         int64_t strideC, float* C, int32_t* acc_out, const void* workspace,
+                         DeviceState* ds, cudaStream_t st) {
+    if (ga > M) ga = M;
+    if (gb > N) gb = N;
+    const I8Workspace w = i8_workspace(const_cast<void*>(workspace), batch, M, N, K);
+    const int nparts_a = sq::i8_staging_parts(batch, M, K, strideA, ds->sms);
+    const int nparts_b = sq::i8_staging_parts(batch, N, K, strideB, ds->sms);
+    return from_cuda(sq::launch_gemm_i8(w.A16, w.B16, sA, sB, static_cast<int>(ga),
+                                        static_cast<int>(gb), static_cast<int>(batch),
+                                        static_cast<int>(M), static_cast<int>(N),
+                                        static_cast<int>(K), strideC, C, acc_out, w.bound_a,
+                                        nparts_a, w.bound_b, nparts_b, ds->err_word, st, ds->sms));
+}
+
+sq_status i8_check_outputs(const float* sA, const float* sB, int64_t M, int64_t N,
+                           int64_t strideC, const float* C, const int32_t* acc_out, int64_t ga,
+                           int64_t gb) {
+    if (!sA || !sB || (!C && !acc_out) || ga < 1 || gb < 1) return SQ_ERR_INVALID_ARG;
+    if (strideC < M * N) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(C) || !aligned16(acc_out)) return SQ_ERR_ALIGNMENT;
+    return SQ_OK;
+}
+
 sq_status gemm_i8_common(const int8_t* A, const float* sA, int64_t ga, const int8_t* B,
                          const float* sB, int64_t gb, int64_t batch, int64_t M, int64_t N,
                          int64_t K, int64_t strideA, int64_t strideB, int64_t strideC, float* C,
                          int32_t* acc_out, void* workspace, size_t workspace_bytes,
                          sq_stream stream) {
-    if (batch < 1 || M < 1 || N < 1 || K < 1 || ga < 1 || gb < 1) return SQ_ERR_INVALID_ARG;
-    if (!A || !B || !sA || !sB || !workspace || (!C && !acc_out)) return SQ_ERR_INVALID_ARG;
-    if (strideA < M * K || strideB < N * K || strideC < M * N) return SQ_ERR_INVALID_ARG;
-    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
-    if (K > (int64_t(1) << 17)) return SQ_ERR_UNSUPPORTED;
-    if (batch > 65535 || M > kMaxDim || N > kMaxDim) return SQ_ERR_UNSUPPORTED;
-    if (strideA % 16 != 0 || strideB % 16 != 0) return SQ_ERR_ALIGNMENT;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(acc_out) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return SQ_ERR_ALIGNMENT;
-    if (workspace_bytes < sq_gemm_i8_workspace_bytes(batch, M, N, K)) return SQ_ERR_INVALID_ARG;
-    const int64_t mt = (M + 127) / 128, nt = (N + 127) / 128;
-    if (mt * nt * batch > kMaxDim) return SQ_ERR_UNSUPPORTED;
-    if (ga > M) ga = M;
-    if (gb > N) gb = N;
+    sq_status r = i8_check_common(batch, M, N, K, strideA, strideB, workspace, workspace_bytes);
+    if (r != SQ_OK) return r;
+    if (!A || !B) return SQ_ERR_INVALID_ARG;
+    r = i8_check_outputs(sA, sB, M, N, strideC, C, acc_out, ga, gb);
+    if (r != SQ_OK) return r;
+    if (!aligned16(A) || !aligned16(B)) return SQ_ERR_ALIGNMENT;
     cudaError_t e = cudaSuccess;
     DeviceState* ds = device_state(&e);
     if (!ds) return from_cuda(e);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    uint16_t* A16 = static_cast<uint16_t*>(workspace);
-    const size_t abytes = (static_cast<size_t>(batch) * M * K * 2 + 255) & ~static_cast<size_t>(255);
-    uint16_t* B16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + abytes);
-    const size_t bbytes = (static_cast<size_t>(batch) * N * K * 2 + 255) & ~static_cast<size_t>(255);
-    unsigned* bound_a = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + abytes + bbytes);
-    unsigned* bound_b = bound_a + 256;
-    int nparts_a = 0, nparts_b = 0;
-    e = sq::launch_i8_to_f16_pair(A, M, B, N, batch, K, strideA, strideB, A16, B16, bound_a,
-                                  &nparts_a, bound_b, &nparts_b, ds->err_word, st, ds->sms);
-    if (e != cudaSuccess) return SQ_ERR_CUDA;
-    return from_cuda(sq::launch_gemm_i8(A16, B16, sA, sB, static_cast<int>(ga),
-                                        static_cast<int>(gb), static_cast<int>(batch),
-                                        static_cast<int>(M), static_cast<int>(N),
-                                        static_cast<int>(K), strideC, C, acc_out, bound_a,
-                                        nparts_a, bound_b, nparts_b, ds->err_word, st, ds->sms));
+    r = i8_stage(A, B, batch, M, N, K, strideA, strideB, workspace, ds, st);
+    if (r != SQ_OK) return r;
+    return i8_gemm_staged(sA, ga, sB, gb, batch, M, N, K, strideA, strideB, strideC, C, acc_out,
+                          workspace, ds, st);
 }
 
 }  // namespace
+
+sq_status sq_gemm_i8_stage(const int8_t* A, const int8_t* B, int64_t batch, int64_t M, int64_t N,
+                           int64_t K, int64_t strideA, int64_t strideB, void* workspace,
+                           size_t workspace_bytes, sq_stream stream) {
+    sq_status r = i8_check_common(batch, M, N, K, strideA, strideB, workspace, workspace_bytes);
+    if (r != SQ_OK) return r;
+    if (!A || !B) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B)) return SQ_ERR_ALIGNMENT;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    return i8_stage(A, B, batch, M, N, K, strideA, strideB, workspace, ds,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+sq_status sq_gemm_i8_rowscaled_staged(const float* sA, const float* sB, int64_t batch, int64_t M,
+                                      int64_t N, int64_t K, int64_t strideA, int64_t strideB,
+                                      int64_t strideC, float* C, int32_t* acc_out,
+                                      const void* workspace, size_t workspace_bytes,
+                                      sq_stream stream) {
+    sq_status r = i8_check_common(batch, M, N, K, strideA, strideB, workspace, workspace_bytes);
+    if (r != SQ_OK) return r;
+    r = i8_check_outputs(sA, sB, M, N, strideC, C, acc_out, 1, 1);
+    if (r != SQ_OK) return r;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    return i8_gemm_staged(sA, 1, sB, 1, batch, M, N, K, strideA, strideB, strideC, C, acc_out,
+                          workspace, ds, reinterpret_cast<cudaStream_t>(stream));
+}
 
 sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B, const float* sB,
                                int64_t batch, int64_t M, int64_t N, int64_t K, int64_t strideA,

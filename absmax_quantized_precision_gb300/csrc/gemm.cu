@@ -1143,29 +1143,39 @@ __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const in
     }
 }
 
-// One operand through the bulk pipeline, when it qualifies: contiguous and
-// at least about 8192 codes per SM (smaller tensors take the plain kernel,
-// with no large shared-memory carveout).  Returns false if it does not.
+// How many bound slots the staging of one operand writes: the CTA count of
+// the bulk pipeline when the operand takes it (contiguous and at least about
+// 8192 codes per SM; smaller tensors take the plain kernel, with no large
+// shared-memory carveout), else 0.  The GEMM of a staged workspace recomputes
+// it from the same sizes.
+int i8_staging_parts(int64_t batch, int64_t rows, int64_t K, int64_t stride, int sms) {
+    const int64_t n = batch * rows * K;
+    if (!(stride == rows * K || batch == 1) || n < static_cast<int64_t>(8192) * sms) return 0;
+    int64_t blocks = (n / kStgChunk + kStgWarps - 1) / kStgWarps;
+    int64_t cap = static_cast<int64_t>(sms);
+    if (cap > kStgMaxParts) cap = kStgMaxParts;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+// One operand through the bulk pipeline, when it qualifies.  Returns false if
+// it does not.
 static bool stage_bulk(const int8_t* src, int64_t batch, int64_t rows, int64_t K, int64_t stride,
                        uint16_t* dst, unsigned* parts, int* nparts, unsigned* err_word,
                        cudaStream_t st, int sms, cudaError_t* err) {
+    const int blocks = i8_staging_parts(batch, rows, K, stride, sms);
+    if (!err_word || blocks == 0) return false;
     const int64_t n = batch * rows * K;
-    if (!err_word || !(stride == rows * K || batch == 1) || n < static_cast<int64_t>(8192) * sms)
-        return false;
     const cudaError_t attr =
         set_max_dynamic_smem(reinterpret_cast<const void*>(i8_to_f16_bulk_kernel), kStgSmem);
     if (attr != cudaSuccess) {
         *err = attr;
         return true;
     }
-    int64_t blocks = (n / kStgChunk + kStgWarps - 1) / kStgWarps;
-    int64_t cap = static_cast<int64_t>(sms);
-    if (cap > kStgMaxParts) cap = kStgMaxParts;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
     *err = launch_pdl(i8_to_f16_bulk_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kStgWarps * 32),
                       kStgSmem, st, 1u, src, n, dst, parts, err_word);
-    if (nparts) *nparts = static_cast<int>(blocks);
+    if (nparts) *nparts = blocks;
     return true;
 }
 

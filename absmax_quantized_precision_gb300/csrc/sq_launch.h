@@ -32,6 +32,11 @@ cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale
 // any of their 1024-code chunks (the ragged tail counts as one chunk); the
 // other operands share one launch of a plain kernel and report *nparts = 0.
 // parts_a and parts_b hold at least 256 words each.
+// The *nparts that launch_i8_to_f16_pair reports for one operand of these
+// sizes (0: it takes the plain kernel and records no bounds).  Every launch
+// that passes an error word takes the bulk pipeline when this is non-zero.
+int i8_staging_parts(int64_t batch, int64_t rows, int64_t K, int64_t stride, int sms);
+
 cudaError_t launch_i8_to_f16_pair(const int8_t* a, int64_t M, const int8_t* b, int64_t N,
                                   int64_t batch, int64_t K, int64_t stride_a, int64_t stride_b,
                                   uint16_t* a16, uint16_t* b16, unsigned* parts_a, int* nparts_a,

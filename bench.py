@@ -8,7 +8,14 @@ N=8192, K=8192, A and B bf16 Student-t(3), seeded):
         per-row fp32 dequant epilogue.
 Metric: quant+GEMM TFLOP/s = (2*M*N*K for each of the two GEMMs) / step time.
 
+The same JSON line also carries the pages' four smaller workloads under
+"configs" (INT8 per-row, INT8 per-head, the FP8 linear forward and the FP8
+MLP backward), each timed on the GPU after an L2 flush and run by the oracle
+on the host.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sq|reference]
+  python bench.py --config {int8_per_row,int8_per_head,fp8_fwd,fp8_bwd,all,
+                            fp8_linear,large_next,extra}   (one line each)
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 (the path shards into independent problems: no collective on the data path).
@@ -16,11 +23,13 @@ Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -36,6 +45,12 @@ WORKLOAD = ("large: M=16384 N=8192 K=8192, A/B bf16 Student-t(3) seeded; FP8 E4M
             "(exact int32 acc, fp32 out)")
 FLOPS_PER_STEP = 2 * (2.0 * M * N * K)
 
+# Nominal dense tensor rates of a GB300 (context beside the measured peaks).
+# INT8 codes run on the f16 tensor path here (sm_103a has no integer MMA
+# kind), so the INT8 GEMM is set against the f16 rate.
+NOMINAL_TFLOPS = {"fp8": 4500.0, "f16": 2250.0}
+NOMINAL_SM_MHZ = 2070.0
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -45,14 +60,16 @@ def parse():
     ap.add_argument("--impl", default="sq", choices=["sq", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave the four smaller workloads out of the default line")
     ap.add_argument("--overlap", action="store_true",
                     help="run the INT8 quantization on a second stream during the FP8 GEMM")
     ap.add_argument("--size", type=int, nargs=3, metavar=("M", "N", "K"),
                     help="override the workload sizes (small cases for profiler captures)")
     ap.add_argument("--config", default="large",
                     choices=["large", "int8_per_row", "int8_per_head", "fp8_fwd", "fp8_bwd", "all",
-                             "fp8_linear", "large_next", "cublaslt", "extra", "legacy_mma"],
-                    help="the pages' other workloads are measured with their own JSON line")
+                             "fp8_linear", "large_next", "extra"],
+                    help="the pages' other workloads, each with its own JSON line")
     args = ap.parse_args()
     if args.size:
         global M, N, K, FLOPS_PER_STEP, WORKLOAD
@@ -62,14 +79,21 @@ def parse():
     return args
 
 
-# DRAM traffic per call (ncu dram__bytes_read.sum + dram__bytes_write.sum,
-# summed over the kernels of the call, full-size workload, 1-pass capture),
-# valid only for the kernel sources it was taken from: when the sha256 of
-# those sources no longer matches, the bench reports traffic as null.
+def algo_bytes(kernel):
+    """Algorithmic bytes of one launch of the large workload's GEMMs (codes
+    read once, output written once): FP8 A8 + B8 + bf16 C; INT8 qa + qb +
+    fp32 C."""
+    return {"gemm_fp8_nt": M * K + N * K + 2 * M * N,
+            "gemm_i8_kernel": M * K + N * K + 4 * M * N}[kernel]
+
+
+# DRAM traffic per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum,
+# full-size workload, 1-pass capture), valid only for the kernel sources it
+# was taken from: when the sha256 of those sources no longer matches, the
+# bench reports traffic as null.
 PROFILED_TRAFFIC = {
-    # profiles/traffic_large_step.md
     "gemm_fp8_nt": {"bytes": 775060736, "sources_sha256": "0c4c4962ef3b575962f3c4b354468457380cfe37f2bbaca93c64b58fb1ba69d5"},
-    "gemm_i8": {"bytes": 3189623296, "sources_sha256": "0c4c4962ef3b575962f3c4b354468457380cfe37f2bbaca93c64b58fb1ba69d5"},
+    "gemm_i8_kernel": {"bytes": 2708078592, "sources_sha256": "0c4c4962ef3b575962f3c4b354468457380cfe37f2bbaca93c64b58fb1ba69d5"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
@@ -93,6 +117,9 @@ def profiled_traffic(kernel):
 
 
 def peaks():
+    """Roofline denominators.  Every kernel here is timed by CUDA events over a
+    short region, so the burst figures apply: HBM copy GB/s and the cuBLAS
+    bf16 burst rate; FP8 is twice the bf16 rate (nominal dense ratio)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
@@ -102,40 +129,124 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
 
 
+def tensor_peak(pk, fp8):
+    return (2.0 if fp8 else 1.0) * pk["bf16"]
+
+
+# ---------------------------------------------------------------- clocks
+class _Nvml:
+    """Read-only NVML queries through ctypes (no Python NVML package needed)."""
+    CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device):
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        bus = self._pci_bus_id(device)
+        if bus:
+            ok = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0
+        if not ok:
+            idx = device.index if device.index is not None else 0
+            if os.environ.get("CUDA_VISIBLE_DEVICES"):
+                raise RuntimeError("no PCI bus id to map the CUDA device to NVML")
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(self.h)) != 0:
+                raise RuntimeError("nvmlDeviceGetHandleByIndex failed")
+        self._reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    @staticmethod
+    def _pci_bus_id(device):
+        import torch
+        p = torch.cuda.get_device_properties(device)
+        try:
+            return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        except AttributeError:
+            return None
+
+    def sm_mhz(self):
+        v = ctypes.c_uint()
+        return v.value if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ctypes.byref(v)) == 0 else None
+
+    def sm_max_mhz(self):
+        v = ctypes.c_uint()
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(v)) == 0 else None
+
+    def reasons(self):
+        v = ctypes.c_ulonglong()
+        if self._reasons_fn(self.h, ctypes.byref(v)) != 0:
+            return None
+        return [n for bit, n in self.REASONS.items() if v.value & bit]
+
+    def power_w(self):
+        v = ctypes.c_uint()
+        return v.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(v)) == 0 else None
+
+
 class Clocks:
-    """Samples SM clocks and throttle reasons with single-shot nvidia-smi queries
-    from a background thread while the timed region runs."""
+    """Samples the SM clock, power and clock-event reasons while the timed
+    region runs: in process through NVML every `period_s` from a background
+    thread (read-only queries), else with nvidia-smi queries."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index, period_s=0.1):
-        self.index = index
+    def __init__(self, device, period_s=0.002):
+        self.device = device
         self.period = period_s
-        self.lines = []
+        self.samples = []        # (sm_mhz, reasons, power_w)
+        self.max_mhz = None
         self.errors = []
+        self.source = None
+        try:
+            self.nvml = _Nvml(device)
+            self.max_mhz = self.nvml.sm_max_mhz()
+            self.source = "nvml"
+        except Exception as e:
+            self.nvml = None
+            self.errors.append(f"nvml: {str(e)[:120]}")
+            self.source = "nvidia-smi"
 
-    def _loop(self):
+    def _loop_nvml(self):
+        while not self._stop.is_set():
+            self.samples.append((self.nvml.sm_mhz(), self.nvml.reasons(), self.nvml.power_w()))
+            time.sleep(self.period)
+
+    def _loop_smi(self):
+        idx = self.device.index if self.device.index is not None else 0
         while not self._stop.is_set():
             try:
-                r = subprocess.run(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                r = subprocess.run(["nvidia-smi", f"--id={idx}", f"--query-gpu={self.Q}",
                                     "--format=csv,noheader,nounits"],
                                    capture_output=True, text=True, timeout=10)
-                if r.returncode == 0:
-                    self.lines += [l for l in r.stdout.splitlines() if l.strip()]
-                elif len(self.errors) < 3:
-                    self.errors.append(r.stderr.strip()[:200])
-            except Exception as e:   # no nvidia-smi: no samples
-                if len(self.errors) < 3:
-                    self.errors.append(str(e)[:200])
+            except Exception as e:
+                self.errors.append(str(e)[:200])
                 return
-            self._stop.wait(self.period)
+            for line in r.stdout.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    mhz, self.max_mhz = float(f[1]), float(f[2])
+                except ValueError:
+                    continue
+                names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+                rs = [n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")]
+                try:
+                    pw = float(f[3])
+                except ValueError:
+                    pw = None
+                self.samples.append((mhz, rs, pw))
+            self._stop.wait(0.1)
 
     def __enter__(self):
-        import threading
         self._stop = threading.Event()
-        self._thr = threading.Thread(target=self._loop, daemon=True)
+        self._thr = threading.Thread(target=self._loop_nvml if self.nvml else self._loop_smi,
+                                     daemon=True)
         self._thr.start()
         return self
 
@@ -144,26 +255,21 @@ class Clocks:
         self._thr.join(timeout=15)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        out = {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [s[0] for s in self.samples if s[0] is not None]
+        reasons = sorted({r for s in self.samples if s[1] for r in s[1]})
+        out = {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(sm),
+               "source": self.source}
+        if self.nvml:
+            out["period_ms"] = 1e3 * self.period
         if sm:
-            loaded = [x for x in sm if mx is None or x > 0.5 * mx] or sm
+            loaded = [x for x in sm if self.max_mhz is None or x > 0.5 * self.max_mhz] or sm
             out["sm_mhz"] = statistics.median(loaded)
+            out["sm_mhz_min"] = min(loaded)
+        pw = [s[2] for s in self.samples if s[2] is not None]
+        if pw:
+            out["power_w_max"] = max(pw)
         if self.errors:
-            out["errors"] = self.errors
+            out["errors"] = self.errors[:3]
         return out
 
 
@@ -260,6 +366,13 @@ def whole_job_tflops(world, flops_per_step_per_rank, ms_per_step):
     return world * flops_per_step_per_rank / (ms_per_step * 1e-3) / 1e12
 
 
+def check_frac(name, frac):
+    """A kernel far above its measured peak is not doing the work it claims."""
+    if frac > 1.5:
+        raise RuntimeError(f"{name}: {frac:.2f} of its peak; the timed region does not hold the work")
+    return frac
+
+
 # ---------------------------------------------------------------- GPU leg
 def run_sq(args, rank, world, local_rank):
     import numpy as np
@@ -298,7 +411,6 @@ def run_sq(args, rank, world, local_rank):
     wsi = torch.empty(sq.gemm_i8_workspace_bytes(1, M, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    names = ["quant_fp8_A", "quant_fp8_B", "gemm_fp8_nt", "quant_i8_A", "quant_i8_B", "gemm_i8"]
     launches_per_step = 8   # the INT8 GEMM call stages A and B (2 launches) before its GEMM
 
     # One stream by default.  --overlap runs the INT8 quantization (memory-
@@ -309,30 +421,46 @@ def run_sq(args, rank, world, local_rank):
     q_done = torch.cuda.Event()
     g_done = torch.cuda.Event()
 
-    def step(events=None, bufs=None):
+    CALLS = ["quant_fp8_A", "quant_fp8_B", "gemm_fp8_nt", "quant_i8_A", "quant_i8_B", "gemm_i8"]
+
+    def step(events=None, bufs=None, skip=None):
+        """One step.  With `events`, the INT8 GEMM call runs as its two phases
+        (staging, then the GEMM kernel) with an event between them; `skip`
+        leaves one call out (for its marginal cost in the step)."""
         xa, xb, c8, ci = bufs if bufs is not None else (A, B, C8, Ci)
 
         def mark(i, st):
             if events is not None:
                 events[i].record(st)
         mark(0, stream)
-        sq.sq_quantize_fp8(xa, tsa, sq.SQ_FMT_E4M3, ws, x8=a8, amax=amax_a, stream=stream)
+        if skip != "quant_fp8_A":
+            sq.sq_quantize_fp8(xa, tsa, sq.SQ_FMT_E4M3, ws, x8=a8, amax=amax_a, stream=stream)
         mark(1, stream)
-        sq.sq_quantize_fp8(xb, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax_b, stream=stream)
+        if skip != "quant_fp8_B":
+            sq.sq_quantize_fp8(xb, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax_b, stream=stream)
         mark(2, stream)
         q_done.record(stream)
-        sq.sq_gemm_fp8_scaled(a8, b8, tsa, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT, C=c8, stream=stream)
+        if skip != "gemm_fp8_nt":
+            sq.sq_gemm_fp8_scaled(a8, b8, tsa, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT, C=c8, stream=stream)
         mark(3, stream)
         g_done.record(stream)
         s_i8.wait_event(q_done)
         mark(7, s_i8)
-        sq.sq_quantize_rowwise_i8(xa, q=qa, scales=sA, stream=s_i8)
+        if skip != "quant_i8_A":
+            sq.sq_quantize_rowwise_i8(xa, q=qa, scales=sA, stream=s_i8)
         mark(4, s_i8)
-        sq.sq_quantize_rowwise_i8(xb, q=qb, scales=sB, stream=s_i8)
+        if skip != "quant_i8_B":
+            sq.sq_quantize_rowwise_i8(xb, q=qb, scales=sB, stream=s_i8)
         mark(5, s_i8)
         s_i8.wait_event(g_done)
         mark(8, s_i8)
-        sq.sq_gemm_i8_rowscaled(qa, sA, qb, sB, wsi, C=ci, stream=s_i8)
+        if skip != "gemm_i8":
+            if events is None:
+                sq.sq_gemm_i8_rowscaled(qa, sA, qb, sB, wsi, C=ci, stream=s_i8)
+            else:
+                sq.sq_gemm_i8_stage(qa, qb, wsi, stream=s_i8)
+                mark(9, s_i8)
+                sq.sq_gemm_i8_rowscaled_staged(sA, sB, (0, M, N, K), wsi, C=ci, stream=s_i8)
         mark(6, s_i8)
         stream.wait_stream(s_i8)
 
@@ -343,16 +471,16 @@ def run_sq(args, rank, world, local_rank):
         raise RuntimeError("device error during warm-up")
 
     # ------------------------------------------------ timed region (device-resident)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    clk = Clocks(dev)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     # The step time: K steps back to back with nothing between the calls (an
     # event between two kernels would turn their programmatic launch overlap
     # back into plain stream order).
-    with Clocks(local_rank) as clk:
+    with clk:
         t_start.record(stream)
         for s in range(args.steps):
             step()
@@ -361,18 +489,34 @@ def run_sq(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
+    if sq.sq_get_last_device_error() != sq.SQ_OK:
+        raise RuntimeError("device error in the timed region")
+
     # The per-call breakdown: a second pass of the same steps with events
-    # around every call.
+    # around every call (and between the INT8 call's staging and its GEMM).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
     for s in range(args.steps):
         step(ev[s])
     torch.cuda.synchronize(dev)
-    # event pairs bracketing each call on the stream it ran on
     spans = {"quant_fp8_A": (0, 1), "quant_fp8_B": (1, 2), "gemm_fp8_nt": (2, 3),
-             "quant_i8_A": (7, 4), "quant_i8_B": (4, 5), "gemm_i8": (8, 6)}
+             "quant_i8_A": (7, 4), "quant_i8_B": (4, 5), "gemm_i8": (8, 6),
+             "stage_i8": (8, 9), "gemm_i8_kernel": (9, 6)}
     per_kernel = {n: statistics.mean(ev[s][a].elapsed_time(ev[s][b]) for s in range(args.steps))
                   for n, (a, b) in spans.items()}
     if sq.sq_get_last_device_error() != sq.SQ_OK:
-        raise RuntimeError("device error in the timed region")
+        raise RuntimeError("device error in the event pass")
+
+    # What each call costs inside the step: K steps without it, back to back,
+    # against the K full steps (programmatic launch overlap kept).
+    marginal_ms = {}
+    for name in CALLS:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(args.steps):
+            step(skip=name)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        marginal_ms[name] = (elapsed_ms - e0.elapsed_time(e1)) / args.steps
 
     # Steady-state rate of each quantize call: 10 launches back to back (each
     # overlapping the tail of the one before), events only around the batch.
@@ -476,6 +620,7 @@ def run_sq(args, rank, world, local_rank):
                 if not (torch.equal(c8_host[k][rows], C8[rows].cpu()) and
                         torch.equal(ci_host[k][rows], Ci[rows].cpu())):
                     raise RuntimeError("e2e results differ from the device-resident ones")
+        del c8_host, ci_host, bufs
 
     # ------------------------------------------------ max over ranks
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e["ms_per_step"] if e2e else 0.0], dist, dev)
@@ -490,49 +635,79 @@ def run_sq(args, rank, world, local_rank):
         return
 
     pk = peaks()
-    fp8_peak = 2.0 * pk["bf16_sustained"]          # nominal fp8:bf16 dense ratio 2
-    bf16_peak = pk["bf16_sustained"]
-    quant_fp8_bytes = {"quant_fp8_A": M * K * 3 + 4, "quant_fp8_B": N * K * 3 + 4}
-    quant_i8_bytes = {"quant_i8_A": M * K * 3 + M * 4, "quant_i8_B": N * K * 3 + N * 4}
-    kernels = {}
-    for n, ms in per_kernel.items():
+    clocks = clk.summary()
+    quant_bytes = {"quant_fp8_A": M * K * 3 + 4, "quant_fp8_B": N * K * 3 + 4,
+                   "quant_i8_A": M * K * 3 + M * 4, "quant_i8_B": N * K * 3 + N * 4,
+                   "stage_i8": (M + N) * K * 3}
+    gemm_flops = {"gemm_fp8_nt": 2.0 * M * N * K, "gemm_i8": 2.0 * M * N * K,
+                  "gemm_i8_kernel": 2.0 * M * N * K}
+
+    def rate(n, ms):
         d = {"ms": ms}
-        if n in quant_fp8_bytes or n in quant_i8_bytes:
-            by = quant_fp8_bytes.get(n) or quant_i8_bytes.get(n)
-            d["GB/s"] = by / (ms * 1e-3) / 1e9
+        if n in quant_bytes:
+            d["GB/s"] = quant_bytes[n] / (ms * 1e-3) / 1e9
             d["frac_hbm"] = d["GB/s"] / pk["hbm_gbs"]
-        else:
-            tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-            d["TFLOP/s"] = tf
-            d["frac_peak"] = tf / (fp8_peak if n == "gemm_fp8_nt" else bf16_peak)
-        kernels[n] = d
-    kernels_steady = {}
-    for n, ms in steady_ms.items():
-        by = quant_fp8_bytes.get(n) or quant_i8_bytes.get(n)
-        gbs = by / (ms * 1e-3) / 1e9
-        kernels_steady[n] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"]}
-    dom = max(("gemm_fp8_nt", "gemm_i8"), key=lambda n: per_kernel[n])
-    dom_peak = fp8_peak if dom == "gemm_fp8_nt" else bf16_peak
+        elif n in gemm_flops:
+            d["TFLOP/s"] = gemm_flops[n] / (ms * 1e-3) / 1e12
+            d["frac_peak"] = d["TFLOP/s"] / tensor_peak(pk, n == "gemm_fp8_nt")
+        return d
+
+    kernels = {n: rate(n, ms) for n, ms in per_kernel.items()}
+    kernels_marginal = {n: rate(n, ms) for n, ms in marginal_ms.items()}
+    kernels_steady = {n: rate(n, ms) for n, ms in steady_ms.items()}
+
+    # Roofline: the dominant kernel of the step (the longest single launch).
+    dom = max(("gemm_fp8_nt", "gemm_i8_kernel"), key=lambda n: per_kernel[n])
+    fp8 = dom == "gemm_fp8_nt"
+    dom_peak = tensor_peak(pk, fp8)
     achieved = kernels[dom]["TFLOP/s"]
-    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": dom_peak,
-                "unit": "TFLOP/s", "frac": achieved / dom_peak,
-                "traffic": profiled_traffic(dom),
-                "peak_src": f"{pk['src']} bf16 sustained"
-                            + (" x2 (nominal fp8:bf16)" if dom == "gemm_fp8_nt" else
-                               " (INT8 runs on the f16 tensor path)"),
-                "algorithmic": "2*M*N*K flops per call",
-                "timed": ("one sq_gemm_i8_rowscaled call: fp16 staging of A and B (2 launches) "
-                          "plus the GEMM" if dom == "gemm_i8" else "one sq_gemm_fp8_scaled launch")}
+    traffic = profiled_traffic(dom)
+    nominal = NOMINAL_TFLOPS["fp8" if fp8 else "f16"]
+    roofline = {
+        "kernel": dom, "bound": "tensor", "achieved": achieved, "peak": dom_peak,
+        "unit": "TFLOP/s", "frac": check_frac(dom, achieved / dom_peak), "traffic": traffic,
+        "peak_src": (f"{pk['src']} bf16 burst (cuBLAS bf16 GEMM, best of 10)"
+                     + (" x2, the nominal fp8:bf16 dense ratio" if fp8 else
+                        "; the INT8 codes run on the f16 tensor path (sm_103a has no integer "
+                        "MMA kind), whose dense rate equals bf16's")
+                     + "; the kernel is timed by CUDA events over a short region, so the burst "
+                       "figure applies"),
+        "algorithmic": "2*M*N*K flops per launch",
+        "algorithmic_bytes": algo_bytes(dom),
+        "traffic_vs_algorithmic": (traffic / algo_bytes(dom)) if traffic else None,
+        "timed": ("the INT8 GEMM kernel alone (sq_gemm_i8_rowscaled_staged; the call's fp16 "
+                  "staging of A and B is timed apart as stage_i8)" if not fp8 else
+                  "one sq_gemm_fp8_scaled launch"),
+        "vs_nominal": {"nominal_dense_tflops": nominal, "frac": achieved / nominal,
+                       "frac_at_sampled_clock": (achieved / (nominal * clocks["sm_mhz"] / NOMINAL_SM_MHZ)
+                                                 if clocks.get("sm_mhz") else None),
+                       "note": "nominal dense FP8 4.5 / f16 2.25 PFLOP/s at 2070 MHz"},
+    }
+    other = "gemm_i8_kernel" if fp8 else "gemm_fp8_nt"
+    other_rec = {"kernel": other, "achieved": kernels[other]["TFLOP/s"],
+                 "peak": tensor_peak(pk, other == "gemm_fp8_nt"),
+                 "frac": check_frac(other, kernels[other]["frac_peak"]),
+                 "traffic": profiled_traffic(other), "algorithmic_bytes": algo_bytes(other)}
+    if other_rec["traffic"]:
+        other_rec["traffic_vs_algorithmic"] = other_rec["traffic"] / algo_bytes(other)
+    roofline["other_gemm"] = other_rec
+    if clocks.get("sm_mhz"):
+        clocks["step_kcycles"] = ms_per_step * clocks["sm_mhz"]
 
     cpu = None
     if not args.no_cpu:
-        import numpy as np
         rows = np.sort(np.random.default_rng(0).choice(M, min(CPU_ROWS_A, M), replace=False))
         dt, fl, thr = cpu_oracle_sample(a_np, b_np, sa_np, sb_np, rows, 0, N)
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"{len(rows)} seeded rows of A x all of B, full K: FP8 and INT8 quantize "
                          "of those rows and of B, then those rows of both GEMMs",
                "seconds": dt}
+
+    configs = None
+    if not args.no_configs and not args.size and world == 1:
+        configs = {}
+        for name in SMALL_CONFIGS:
+            configs[name] = measure_config(name, args, with_cpu=not args.no_cpu, compact=True)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -545,19 +720,25 @@ def run_sq(args, rank, world, local_rank):
                                 "two streams: INT8 quantize of A and B during the FP8 GEMM; "
                                 "INT8 GEMM call after it")},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "roofline": roofline,
         "kernels": kernels,
+        "kernels_note": ("mean CUDA-event span of each call on the stream it ran on, from a second "
+                         "pass of the same steps with events around every call (each call then "
+                         "waits for the one before and pays its own launch); gemm_i8 is the whole "
+                         "INT8 call = stage_i8 + gemm_i8_kernel"
+                         + ("; with two streams the INT8 quantize spans overlap the FP8 GEMM and "
+                            "share the GPU with it" if args.overlap else "")),
+        "kernels_marginal": kernels_marginal,
+        "kernels_marginal_note": ("what each call adds to the step: K steps without it, back to "
+                                  "back, against the K full steps (launch overlap kept)"),
         "kernels_steady": kernels_steady,
         "kernels_steady_note": ("each quantize call launched 10 times back to back with events only "
                                 "around the batch; B alternates with a same-size block of A so "
                                 "no launch reads its input from L2"),
-        "kernels_note": ("mean CUDA-event span of each call on the stream it ran on, from a second "
-                         "pass of the same steps with events around every call (the step time comes "
-                         "from a pass without them, where each kernel's launch overlaps the tail of "
-                         "the one before)" + ("; with two streams the INT8 quantize spans overlap "
-                                              "the FP8 GEMM and share the GPU with it"
-                                              if args.overlap else "")),
+        "peaks": {"hbm_gbs": pk["hbm_gbs"], "bf16_burst_tflops": pk["bf16"],
+                  "fp8_tflops": 2.0 * pk["bf16"], "src": pk["src"]},
+        "configs": configs,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
@@ -568,13 +749,134 @@ def run_sq(args, rank, world, local_rank):
 
 # ---------------------------------------------------------------- the other workloads
 SMALL_CONFIGS = ["int8_per_row", "int8_per_head", "fp8_fwd", "fp8_bwd"]
-EXTRA_CONFIGS = ["fp8_linear", "large_next", "cublaslt"]
+EXTRA_CONFIGS = ["fp8_linear", "large_next"]
 
 
-def run_small_config(name, args):
-    """One JSON line for one of the pages' smaller workloads: L2 flushed
-    (256 MiB write) before every timed iteration, per-kernel CUDA events, and
-    the oracle run on the whole workload on the host for comparison."""
+def config_ops(name, dev, sq, synth, oracle, bf16_dev, prev_scale):
+    """(description, [(label, kind, amount, fn)], GEMM flops per step, the
+    oracle's work on the host or None) for one of the pages' workloads."""
+    import numpy as np
+    import torch
+
+    if name in ("int8_per_row", "int8_per_head"):
+        if name == "int8_per_row":
+            a = synth.normal(11, (128, 1024))
+            b = synth.normal(12, (512, 1024))
+            desc = "INT8 per-row: A f32 128x1024, B f32 512x1024 ~N(0,1); C = A B^T, fp32 out"
+        else:
+            a = synth.normal(21, (16, 196, 64))
+            b = synth.normal(22, (16, 196, 64))
+            desc = "INT8 per-head: Q, K f32 (16,196,64) ~N(0,1); C[h] = Q[h] K[h]^T, fp32 out"
+        A, B = torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)
+        qa = torch.empty(A.shape, dtype=torch.int8, device=dev)
+        qb = torch.empty(B.shape, dtype=torch.int8, device=dev)
+        sa = torch.empty(A.shape[:-1], device=dev)
+        sb = torch.empty(B.shape[:-1], device=dev)
+        nb = A.shape[0] if A.dim() == 3 else 1
+        Mi, Kk = A.shape[-2], A.shape[-1]
+        Ni = B.shape[-2]
+        ws = torch.empty(sq.gemm_i8_workspace_bytes(nb, Mi, Ni, Kk), dtype=torch.uint8, device=dev)
+        C = torch.empty((nb, Mi, Ni) if nb > 1 else (Mi, Ni), device=dev)
+        flops = 2.0 * nb * Mi * Ni * Kk
+        shape = (nb if A.dim() == 3 else 0, Mi, Ni, Kk)
+        ops = [("quant_i8_A", "bytes", A.numel() * 5 + sa.numel() * 4,
+                lambda: sq.sq_quantize_rowwise_i8(A, q=qa, scales=sa)),
+               ("quant_i8_B", "bytes", B.numel() * 5 + sb.numel() * 4,
+                lambda: sq.sq_quantize_rowwise_i8(B, q=qb, scales=sb)),
+               ("stage_i8", "bytes", (qa.numel() + qb.numel()) * 3,
+                lambda: sq.sq_gemm_i8_stage(qa, qb, ws)),
+               ("gemm_i8_kernel", "flops", flops,
+                lambda: sq.sq_gemm_i8_rowscaled_staged(sa.reshape(-1), sb.reshape(-1), shape, ws,
+                                                       C=C))]
+        call = ("gemm_i8", "flops", flops,
+                lambda: sq.sq_gemm_i8_rowscaled(qa, sa.reshape(-1), qb, sb.reshape(-1), ws, C=C))
+
+        def oracle_work():
+            oqa, osa = oracle.quantize_rowwise_i8(a)
+            oqb, osb = oracle.quantize_rowwise_i8(b)
+            oracle.gemm_i8(oqa, oqb, osa, osb)
+        return desc, ops, [call], flops, oracle_work
+
+    if name in EXTRA_CONFIGS:
+        desc, ops, flops = extra_config_ops(name, dev, bf16_dev, prev_scale)
+        return desc, ops, [], flops, None
+
+    fmt = sq.SQ_FMT_E4M3
+    wsq = sq.new_workspace(dev)
+    if name == "fp8_fwd":
+        x = synth.normal(31, (2048, 1024), std=1.0, dtype=synth.BF16)
+        w = synth.normal(32, (1024, 1024), std=0.02, dtype=synth.BF16)
+        sx, sw = prev_scale(33, x.shape, 1.0), prev_scale(34, w.shape, 0.02)
+        X, W = bf16_dev(x), bf16_dev(w)
+        tsx, tsw = torch.tensor([sx], device=dev), torch.tensor([sw], device=dev)
+        x8 = torch.empty(X.shape, dtype=torch.uint8, device=dev)
+        w8 = torch.empty(W.shape, dtype=torch.uint8, device=dev)
+        ax, aw = torch.empty(1, device=dev), torch.empty(1, device=dev)
+        Y = torch.empty((2048, 1024), dtype=torch.bfloat16, device=dev)
+        flops = 2.0 * 2048 * 1024 * 1024
+        desc = ("FP8 E4M3 linear forward: X bf16 2048x1024 ~N(0,1), W bf16 1024x1024 "
+                "~N(0,0.02), delayed scales; Y = X W^T (NT), bf16 out")
+        ops = [("quant_fp8_X", "bytes", X.numel() * 3,
+                lambda: sq.sq_quantize_fp8(X, tsx, fmt, wsq, x8=x8, amax=ax)),
+               ("quant_fp8_W", "bytes", W.numel() * 3,
+                lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=aw)),
+               ("gemm_fp8_nt", "flops", flops,
+                lambda: sq.sq_gemm_fp8_scaled(x8, w8, tsx, tsw, fmt, sq.SQ_NT, C=Y))]
+
+        def oracle_work():
+            ox8, _ = oracle.quantize_fp8(x, sx, 0)
+            ow8, _ = oracle.quantize_fp8(w, sw, 0)
+            oracle.gemm_fp8(ox8, ow8, 0, oracle.NT, sx, sw)
+        return desc, ops, [], flops, oracle_work
+
+    T, H, D = 2048, 4096, 1024
+    g = synth.normal(41, (T, H), std=1e-3, dtype=synth.BF16)
+    w = synth.normal(42, (H, D), std=0.02, dtype=synth.BF16)
+    x = synth.normal(43, (T, D), std=1.0, dtype=synth.BF16)
+    sg, sw, sx = prev_scale(44, g.shape, 1e-3), prev_scale(45, w.shape, 0.02), \
+        prev_scale(46, x.shape, 1.0)
+    G, W, X = bf16_dev(g), bf16_dev(w), bf16_dev(x)
+    tsg, tsw, tsx = (torch.tensor([v], device=dev) for v in (sg, sw, sx))
+    g8 = torch.empty(G.shape, dtype=torch.uint8, device=dev)
+    w8 = torch.empty(W.shape, dtype=torch.uint8, device=dev)
+    x8 = torch.empty(X.shape, dtype=torch.uint8, device=dev)
+    am = [torch.empty(1, device=dev) for _ in range(3)]
+    dX = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((H, D), dtype=torch.bfloat16, device=dev)
+    flops = 2 * (2.0 * T * H * D)
+    desc = ("FP8 E4M3 MLP backward (dim 1024, hidden 4096, 2048 tokens): G bf16 2048x4096 "
+            "~N(0,1e-3), W bf16 4096x1024 ~N(0,0.02), X bf16 2048x1024 ~N(0,1); "
+            "dX = G W (NN), dW = G^T X (TN), bf16 out")
+    ops = [("quant_fp8_G", "bytes", G.numel() * 3,
+            lambda: sq.sq_quantize_fp8(G, tsg, fmt, wsq, x8=g8, amax=am[0])),
+           ("quant_fp8_W", "bytes", W.numel() * 3,
+            lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=am[1])),
+           ("quant_fp8_X", "bytes", X.numel() * 3,
+            lambda: sq.sq_quantize_fp8(X, tsx, fmt, wsq, x8=x8, amax=am[2])),
+           ("gemm_fp8_dX_nn", "flops", 2.0 * T * H * D,
+            lambda: sq.sq_gemm_fp8_scaled(g8, w8, tsg, tsw, fmt, sq.SQ_NN, C=dX)),
+           ("gemm_fp8_dW_tn", "flops", 2.0 * T * H * D,
+            lambda: sq.sq_gemm_fp8_scaled(g8, x8, tsg, tsx, fmt, sq.SQ_TN, C=dW))]
+
+    def oracle_work():
+        og8, _ = oracle.quantize_fp8(g, sg, 0)
+        ow8, _ = oracle.quantize_fp8(w, sw, 0)
+        ox8, _ = oracle.quantize_fp8(x, sx, 0)
+        oracle.gemm_fp8(og8, ow8, 0, oracle.NN, sg, sw, want_bf16=False)
+        oracle.gemm_fp8(og8, ox8, 0, oracle.TN, sg, sx, want_bf16=False)
+    return desc, ops, [], flops, oracle_work
+
+
+def measure_config(name, args, with_cpu=True, compact=False):
+    """Times one of the pages' smaller workloads on cuda:0.  Every timed pass
+    runs after a 256 MiB write that evicts the inputs from L2:
+      step   the whole step (its calls in order) captured as one CUDA graph;
+      calls  each call alone, captured as its own graph (its device time plus
+             one launch);
+      in_step  what each call adds to the step graph (the step graph minus the
+             graph of the step without that call);
+    plus the oracle's time for the whole workload on the host (all cores and
+    one core).  Returns a dict; compact leaves out the eager timings."""
     import numpy as np
     import torch
 
@@ -596,107 +898,11 @@ def run_small_config(name, args):
         p = synth.bf16_bits_to_f32(synth.normal(seed, shape, std=std, dtype=synth.BF16))
         return np.float32(np.abs(p).max()) / np.float32(fmax)
 
-    ops = []          # (label, kind, bytes_or_flops, fn)
-    gemm_flops = 0.0
-    cpu = None
-    if name in ("int8_per_row", "int8_per_head"):
-        if name == "int8_per_row":
-            a = synth.normal(11, (128, 1024))
-            b = synth.normal(12, (512, 1024))
-            desc = "INT8 per-row: A f32 128x1024, B f32 512x1024 ~N(0,1); C = A B^T, fp32 out"
-        else:
-            a = synth.normal(21, (16, 196, 64))
-            b = synth.normal(22, (16, 196, 64))
-            desc = "INT8 per-head: Q, K f32 (16,196,64) ~N(0,1); C[h] = Q[h] K[h]^T, fp32 out"
-        A, B = torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)
-        qa = torch.empty(A.shape, dtype=torch.int8, device=dev)
-        qb = torch.empty(B.shape, dtype=torch.int8, device=dev)
-        sa = torch.empty(A.shape[:-1], device=dev)
-        sb = torch.empty(B.shape[:-1], device=dev)
-        nb = A.shape[0] if A.dim() == 3 else 1
-        Mi, Kk = A.shape[-2], A.shape[-1]
-        Ni = B.shape[-2]
-        ws = torch.empty(sq.gemm_i8_workspace_bytes(nb, Mi, Ni, Kk), dtype=torch.uint8, device=dev)
-        C = torch.empty((nb, Mi, Ni) if nb > 1 else (Mi, Ni), device=dev)
-        gemm_flops = 2.0 * nb * Mi * Ni * Kk
-        ops = [("quant_i8_A", "bytes", A.numel() * 5 + sa.numel() * 4,
-                lambda: sq.sq_quantize_rowwise_i8(A, q=qa, scales=sa)),
-               ("quant_i8_B", "bytes", B.numel() * 5 + sb.numel() * 4,
-                lambda: sq.sq_quantize_rowwise_i8(B, q=qb, scales=sb)),
-               ("gemm_i8", "flops", gemm_flops,
-                lambda: sq.sq_gemm_i8_rowscaled(qa, sa.reshape(-1), qb, sb.reshape(-1), ws, C=C))]
-        def oracle_work():
-            oqa, osa = oracle.quantize_rowwise_i8(a)
-            oqb, osb = oracle.quantize_rowwise_i8(b)
-            oracle.gemm_i8(oqa, oqb, osa, osb)
-    elif name in EXTRA_CONFIGS:
-        desc, ops, gemm_flops, _ = extra_config_ops(name, dev, bf16_dev, prev_scale)
-        oracle_work = None
-    else:
-        fmt = sq.SQ_FMT_E4M3
-        wsq = sq.new_workspace(dev)
-        if name == "fp8_fwd":
-            x = synth.normal(31, (2048, 1024), std=1.0, dtype=synth.BF16)
-            w = synth.normal(32, (1024, 1024), std=0.02, dtype=synth.BF16)
-            sx, sw = prev_scale(33, x.shape, 1.0), prev_scale(34, w.shape, 0.02)
-            X, W = bf16_dev(x), bf16_dev(w)
-            tsx, tsw = torch.tensor([sx], device=dev), torch.tensor([sw], device=dev)
-            x8 = torch.empty(X.shape, dtype=torch.uint8, device=dev)
-            w8 = torch.empty(W.shape, dtype=torch.uint8, device=dev)
-            ax, aw = torch.empty(1, device=dev), torch.empty(1, device=dev)
-            Y = torch.empty((2048, 1024), dtype=torch.bfloat16, device=dev)
-            gemm_flops = 2.0 * 2048 * 1024 * 1024
-            desc = ("FP8 E4M3 linear forward: X bf16 2048x1024 ~N(0,1), W bf16 1024x1024 "
-                    "~N(0,0.02), delayed scales; Y = X W^T (NT), bf16 out")
-            ops = [("quant_fp8_X", "bytes", X.numel() * 3,
-                    lambda: sq.sq_quantize_fp8(X, tsx, fmt, wsq, x8=x8, amax=ax)),
-                   ("quant_fp8_W", "bytes", W.numel() * 3,
-                    lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=aw)),
-                   ("gemm_fp8_nt", "flops", gemm_flops,
-                    lambda: sq.sq_gemm_fp8_scaled(x8, w8, tsx, tsw, fmt, sq.SQ_NT, C=Y))]
-            def oracle_work():
-                ox8, _ = oracle.quantize_fp8(x, sx, 0)
-                ow8, _ = oracle.quantize_fp8(w, sw, 0)
-                oracle.gemm_fp8(ox8, ow8, 0, oracle.NT, sx, sw)
-        else:
-            T, H, D = 2048, 4096, 1024
-            g = synth.normal(41, (T, H), std=1e-3, dtype=synth.BF16)
-            w = synth.normal(42, (H, D), std=0.02, dtype=synth.BF16)
-            x = synth.normal(43, (T, D), std=1.0, dtype=synth.BF16)
-            sg, sw, sx = prev_scale(44, g.shape, 1e-3), prev_scale(45, w.shape, 0.02), \
-                prev_scale(46, x.shape, 1.0)
-            G, W, X = bf16_dev(g), bf16_dev(w), bf16_dev(x)
-            tsg, tsw, tsx = (torch.tensor([v], device=dev) for v in (sg, sw, sx))
-            g8 = torch.empty(G.shape, dtype=torch.uint8, device=dev)
-            w8 = torch.empty(W.shape, dtype=torch.uint8, device=dev)
-            x8 = torch.empty(X.shape, dtype=torch.uint8, device=dev)
-            am = [torch.empty(1, device=dev) for _ in range(3)]
-            dX = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
-            dW = torch.empty((H, D), dtype=torch.bfloat16, device=dev)
-            gemm_flops = 2 * (2.0 * T * H * D)
-            desc = ("FP8 E4M3 MLP backward (dim 1024, hidden 4096, 2048 tokens): G bf16 2048x4096 "
-                    "~N(0,1e-3), W bf16 4096x1024 ~N(0,0.02), X bf16 2048x1024 ~N(0,1); "
-                    "dX = G W (NN), dW = G^T X (TN), bf16 out")
-            ops = [("quant_fp8_G", "bytes", G.numel() * 3,
-                    lambda: sq.sq_quantize_fp8(G, tsg, fmt, wsq, x8=g8, amax=am[0])),
-                   ("quant_fp8_W", "bytes", W.numel() * 3,
-                    lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=am[1])),
-                   ("quant_fp8_X", "bytes", X.numel() * 3,
-                    lambda: sq.sq_quantize_fp8(X, tsx, fmt, wsq, x8=x8, amax=am[2])),
-                   ("gemm_fp8_dX_nn", "flops", 2.0 * T * H * D,
-                    lambda: sq.sq_gemm_fp8_scaled(g8, w8, tsg, tsw, fmt, sq.SQ_NN, C=dX)),
-                   ("gemm_fp8_dW_tn", "flops", 2.0 * T * H * D,
-                    lambda: sq.sq_gemm_fp8_scaled(g8, x8, tsg, tsx, fmt, sq.SQ_TN, C=dW))]
-            def oracle_work():
-                og8, _ = oracle.quantize_fp8(g, sg, 0)
-                ow8, _ = oracle.quantize_fp8(w, sw, 0)
-                ox8, _ = oracle.quantize_fp8(x, sx, 0)
-                oracle.gemm_fp8(og8, ow8, 0, oracle.NN, sg, sw, want_bf16=False)
-                oracle.gemm_fp8(og8, ox8, 0, oracle.TN, sg, sx, want_bf16=False)
+    desc, ops, alt_calls, gemm_flops, oracle_work = config_ops(name, dev, sq, synth, oracle,
+                                                               bf16_dev, prev_scale)
 
-    # the oracle on the host: all cores, then one core
     cpu = None
-    if oracle_work is not None:
+    if with_cpu and oracle_work is not None:
         cores = oracle.num_threads()
         t0 = time.perf_counter()
         oracle_work()
@@ -708,61 +914,55 @@ def run_small_config(name, args):
         oracle.set_num_threads(cores)
         cpu["sample"] = "the whole workload"
 
-    iters = max(args.steps if args.steps != 300 else 50, 1)
+    iters = max(args.steps if args.steps != 300 else 50, 10)
     for _ in range(max(args.warmup, 3)):
-        for _, _, _, fn in ops:
+        for _, _, _, fn in ops + alt_calls:
             fn()
     torch.cuda.synchronize(dev)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(iters)]
-    with Clocks(0) as clk:
+
+    def capture(fns):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for fn in fns:
+                fn()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        return g
+
+    def time_graph(g):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
         for it in range(iters):
             flush.fill_(it & 0xFF)           # evict the inputs from L2 before each pass
+            ev[it][0].record(stream)
+            g.replay()
+            ev[it][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(ev[i][0].elapsed_time(ev[i][1]) for i in range(iters))
+
+    with Clocks(dev) as clk:
+        step_graph = capture([fn for _, _, _, fn in ops])
+        step_ms = time_graph(step_graph)
+        call_ms = [time_graph(capture([fn])) for _, _, _, fn in ops + alt_calls]
+        without_ms = [time_graph(capture([fn for i, (_, _, _, fn) in enumerate(ops) if i != j]))
+                      if len(ops) > 1 else 0.0 for j in range(len(ops))]
+    if sq.sq_get_last_device_error() != sq.SQ_OK:
+        raise RuntimeError("device error in the graph passes")
+
+    eager = None
+    if not compact:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)]
+               for _ in range(iters)]
+        for it in range(iters):
+            flush.fill_(it & 0xFF)
             evs[it][0].record(stream)
             for i, (_, _, _, fn) in enumerate(ops):
                 fn()
                 evs[it][i + 1].record(stream)
         torch.cuda.synchronize(dev)
-    if sq.sq_get_last_device_error() != sq.SQ_OK:
-        raise RuntimeError("device error")
-    step_ms = statistics.median(evs[i][0].elapsed_time(evs[i][-1]) for i in range(iters))
-    # The same step captured once as a CUDA graph and replayed: launches go
-    # back to back, so this is device time without host submission gaps.
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for _, _, _, fn in ops:
-            fn()
-    graph.replay()
-    torch.cuda.synchronize(dev)
-    gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
-    for it in range(iters):
-        flush.fill_(it & 0xFF)
-        gev[it][0].record(stream)
-        graph.replay()
-        gev[it][1].record(stream)
-    torch.cuda.synchronize(dev)
-    if sq.sq_get_last_device_error() != sq.SQ_OK:
-        raise RuntimeError("device error in graph replay")
-    graph_ms = statistics.median(gev[i][0].elapsed_time(gev[i][1]) for i in range(iters))
-    # Each call alone, captured as its own graph and replayed after an L2
-    # flush: its device time plus one launch, with no host submission gap
-    # (the eager per-call times above include the Python binding's).
-    op_graph_ms = []
-    for _, _, _, fn in ops:
-        g1 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g1):
-            fn()
-        g1.replay()
-        torch.cuda.synchronize(dev)
-        oev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
-        for it in range(iters):
-            flush.fill_(it & 0xFF)
-            oev[it][0].record(stream)
-            g1.replay()
-            oev[it][1].record(stream)
-        torch.cuda.synchronize(dev)
-        op_graph_ms.append(statistics.median(oev[i][0].elapsed_time(oev[i][1]) for i in range(iters)))
-    if sq.sq_get_last_device_error() != sq.SQ_OK:
-        raise RuntimeError("device error in per-call graph replay")
+        eager = statistics.median(evs[i][0].elapsed_time(evs[i][-1]) for i in range(iters))
+        if sq.sq_get_last_device_error() != sq.SQ_OK:
+            raise RuntimeError("device error in the eager pass")
+
     pk = peaks()
 
     def rates(label, kind, amount, ms):
@@ -773,38 +973,42 @@ def run_small_config(name, args):
         else:
             tf = amount / (ms * 1e-3) / 1e12
             d["TFLOP/s"] = tf
-            is_fp8 = "fp8" in label or label.startswith(("ours_", "cublaslt_", "linear_"))
-            d["frac_peak"] = tf / ((2.0 if is_fp8 else 1.0) * pk["bf16_sustained"])
+            is_fp8 = "fp8" in label or label.startswith("linear_")
+            d["frac_peak"] = tf / tensor_peak(pk, is_fp8)
         return d
 
-    kernels = {}
-    kernels_graph = {}
-    for j, (label, kind, amount, _) in enumerate(ops):
-        ms = statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(iters))
-        kernels[label] = rates(label, kind, amount, ms)
-        kernels_graph[label] = rates(label, kind, amount, op_graph_ms[j])
-    line = {"metric": METRIC, "config": {"workload": name, "desc": desc,
-                                         "l2": "flushed before every pass"},
-            "value": gemm_flops / (graph_ms * 1e-3) / 1e12, "unit": UNIT,
-            "us_per_step_graph": 1e3 * graph_ms,
-            "us_per_step_eager": 1e3 * step_ms,
-            "value_eager": gemm_flops / (step_ms * 1e-3) / 1e12,
-            "calls_per_step": len(ops),
-            "iters": iters, "kernels_eager": kernels, "kernels_graph": kernels_graph,
-            "clocks": clk.summary(),
-            "cpu_oracle": cpu}
+    calls = {}
+    for j, (label, kind, amount, _) in enumerate(ops + alt_calls):
+        calls[label] = rates(label, kind, amount, call_ms[j])
+    in_step = {}
+    if len(ops) > 1:
+        for j, (label, kind, amount, _) in enumerate(ops):
+            inc = step_ms - without_ms[j]
+            in_step[label] = ({"us": 1e3 * inc} if inc <= 0 else rates(label, kind, amount, inc))
+    out = {"desc": desc, "value": gemm_flops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
+           "us_per_step": 1e3 * step_ms, "calls": calls, "in_step": in_step,
+           "l2": "256 MiB write before every timed pass", "iters": iters,
+           "clocks": clk.summary(), "cpu_oracle": cpu}
+    if eager is not None:
+        out["us_per_step_eager"] = 1e3 * eager
+    return out
+
+
+def run_config(name, args):
+    rec = measure_config(name, args, with_cpu=not args.no_cpu)
+    line = {"metric": METRIC, "config": {"workload": name, "desc": rec.pop("desc"),
+                                         "l2": rec.pop("l2")}}
+    line.update(rec)
     print(json.dumps(line), flush=True)
 
 
 def extra_config_ops(name, dev, bf16_dev, prev_scale):
-    """Workloads of the widened path: the fused FP8 linear layer, the large-size
-    ring / E4M3-output / per-tensor INT8 variants, and cuBLASLt's FP8 GEMM
-    (torch._scaled_mm, a library call) beside ours at the same shapes."""
+    """Workloads of the widened path: the fused FP8 linear layer, and the
+    large-size ring / E4M3-output / per-tensor INT8 variants."""
     import numpy as np
     import torch
 
     import absmax_quantized_precision_gb300 as sq
-    import oracle
     import synth
 
     if name == "fp8_linear":
@@ -834,107 +1038,47 @@ def extra_config_ops(name, dev, bf16_dev, prev_scale):
         desc = ("fused FP8 linear: forward X bf16 2048x1024, W 1024x1024, bf16 bias, E4M3 with "
                 "delayed-scaling rings; backward of the 1024->4096 projection over 2048 tokens, "
                 "E5M2 gradient with a ring, dX + dW + bias gradient")
-        return desc, ops, fwd_flops + bwd_flops, None
+        return desc, ops, fwd_flops + bwd_flops
 
-    if name == "large_next":
-        M, N, K = 16384, 8192, 8192
-        a = synth.student_t(SEED_A, (M, K), df=3, dtype=synth.BF16)
-        b = synth.student_t(SEED_B, (N, K), df=3, dtype=synth.BF16)
-        A, B = bf16_dev(a), bf16_dev(b)
-        sa_v = float(np.float32(np.abs(synth.bf16_bits_to_f32(a)).max()) / np.float32(448.0))
-        ring = sq.new_ring(16, sa_v, dev)
-        ws = sq.new_workspace(dev)
-        a8 = torch.empty((M, K), dtype=torch.uint8, device=dev)
-        b8 = torch.empty((N, K), dtype=torch.uint8, device=dev)
-        amax = torch.empty(1, device=dev)
-        tsb = torch.tensor([sa_v], device=dev)
-        out_scale = torch.tensor([2.0], device=dev)
-        C8 = torch.empty((M, N), dtype=torch.uint8, device=dev)
-        qa = torch.empty((M, K), dtype=torch.int8, device=dev)
-        qb = torch.empty((N, K), dtype=torch.int8, device=dev)
-        sqa, sqb = torch.empty(1, device=dev), torch.empty(1, device=dev)
-        wga = torch.empty(sq.load_library().sq_quantize_grouped_i8_workspace_bytes(M, M),
-                          dtype=torch.uint8, device=dev)
-        wgb = torch.empty(sq.load_library().sq_quantize_grouped_i8_workspace_bytes(N, N),
-                          dtype=torch.uint8, device=dev)
-        wsi = torch.empty(sq.gemm_i8_workspace_bytes(1, M, N, K), dtype=torch.uint8, device=dev)
-        Ci = torch.empty((M, N), device=dev)
-        ops = [("quant_fp8_ring_A", "bytes", M * K * 3,
-                lambda: sq.sq_quantize_fp8_ring(A, sq.SQ_FMT_E4M3, ring, 0, 0, ws, x8=a8, amax=amax)),
-               ("quant_fp8_B", "bytes", N * K * 3,
-                lambda: sq.sq_quantize_fp8(B, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax)),
-               ("gemm_fp8_nt_e4m3_out", "flops", 2.0 * M * N * K,
-                lambda: sq.sq_gemm_fp8_scaled_e4m3(a8, b8, tsb, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT,
-                                                   out_scale, C=C8)),
-               ("quant_i8_per_tensor_A", "bytes", M * K * 3,
-                lambda: sq.sq_quantize_grouped_i8(A, M, q=qa, scales=sqa, workspace=wga)),
-               ("quant_i8_per_tensor_B", "bytes", N * K * 3,
-                lambda: sq.sq_quantize_grouped_i8(B, N, q=qb, scales=sqb, workspace=wgb)),
-               ("gemm_i8_per_tensor", "flops", 2.0 * M * N * K,
-                lambda: sq.sq_gemm_i8_grouped(qa, sqa, M, qb, sqb, N, wsi, C=Ci))]
-        desc = ("large M=16384 N=8192 K=8192 bf16 Student-t(3): FP8 quantize with a ring, FP8 GEMM "
-                "with E4M3 output; per-tensor INT8 quantize (two passes) and GEMM")
-        return desc, ops, 2 * (2.0 * M * N * K), None
-
-    # cuBLASLt FP8 GEMMs (torch._scaled_mm) beside ours on the same codes and steps
-    ops = []
-    total = 0.0
-    shapes = [("fwd_nt_2048x1024x1024", 2048, 1024, 1024, sq.SQ_NT),
-              ("dx_nn_2048x1024x4096", 2048, 1024, 4096, sq.SQ_NN),
-              ("dw_tn_4096x1024x2048", 4096, 1024, 2048, sq.SQ_TN),
-              ("large_nt_16384x8192x8192", 16384, 8192, 8192, sq.SQ_NT)]
-    one = torch.ones((), dtype=torch.float32, device=dev)
-    for i, (lbl, M, N, K, layout) in enumerate(shapes):
-        rng = np.random.default_rng(400 + i)
-        ok = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
-        if layout == sq.SQ_TN:
-            A = torch.from_numpy(rng.choice(ok, (K, M))).to(dev)        # stored [K, M]
-        else:
-            A = torch.from_numpy(rng.choice(ok, (M, K))).to(dev)
-        if layout == sq.SQ_NT:
-            B = torch.from_numpy(rng.choice(ok, (N, K))).to(dev)
-        else:
-            B = torch.from_numpy(rng.choice(ok, (K, N))).to(dev)        # stored [K, N]
-        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        sa = torch.tensor([0.01], device=dev)
-        fl = 2.0 * M * N * K
-        total += fl
-        ops.append((f"ours_{lbl}", "flops", fl,
-                    (lambda A=A, B=B, sa=sa, C=C, layout=layout:
-                     sq.sq_gemm_fp8_scaled(A, B, sa, sa, sq.SQ_FMT_E4M3, layout, C=C))))
-        # cuBLASLt wants mat1 row-major [M,K] and mat2 column-major [K,N]: the
-        # transposed copies it needs for NN / TN are made here, outside the timing
-        a_l = (A if layout != sq.SQ_TN else A.t().contiguous()).view(torch.float8_e4m3fn)
-        b_l = (B.view(torch.float8_e4m3fn).t() if layout == sq.SQ_NT
-               else B.t().contiguous().view(torch.float8_e4m3fn).t())
-        try:
-            torch._scaled_mm(a_l, b_l, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
-            ops.append((f"cublaslt_{lbl}", "flops", fl,
-                        (lambda a_l=a_l, b_l=b_l: torch._scaled_mm(
-                            a_l, b_l, scale_a=one, scale_b=one, out_dtype=torch.bfloat16))))
-        except Exception as e:   # comparator not available in this torch build
-            print(json.dumps({"cublaslt_unavailable": str(e)[:200]}), flush=True)
-    desc = ("FP8 E4M3 GEMMs, bf16 out, ours vs cuBLASLt torch._scaled_mm on the same codes "
-            "(its output comes from torch's caching allocator; the transposed operand copies "
-            "it needs for NN/TN are made before timing)")
-    return desc, ops, total, None
-
-
-def run_legacy_mma_probe():
-    """Builds and runs probes/legacy_mma_rate.cu: the register-only rate of the
-    warp-level int8 and f16 mma.sync instructions on this GPU."""
-    import tempfile
-    src = os.path.join(ROOT, "absmax_quantized_precision_gb300", "probes", "legacy_mma_rate.cu")
-    exe = os.path.join(tempfile.mkdtemp(), "legacy_mma_rate")
-    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", src,
-                           "-o", exe])
-    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
-    if out.returncode != 0:
-        raise RuntimeError(out.stderr)
-    line = json.loads(out.stdout.strip().splitlines()[-1])
-    line.update({"config": {"workload": "legacy_mma", "desc": "register-only mma.sync "
-                            "m16n8k32 s8 and m16n8k16 f16, 4 CTAs x 256 threads per SM"}})
-    print(json.dumps(line), flush=True)
+    # large_next
+    M, N, K = 16384, 8192, 8192
+    a = synth.student_t(SEED_A, (M, K), df=3, dtype=synth.BF16)
+    b = synth.student_t(SEED_B, (N, K), df=3, dtype=synth.BF16)
+    A, B = bf16_dev(a), bf16_dev(b)
+    sa_v = float(np.float32(np.abs(synth.bf16_bits_to_f32(a)).max()) / np.float32(448.0))
+    ring = sq.new_ring(16, sa_v, dev)
+    ws = sq.new_workspace(dev)
+    a8 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    b8 = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    amax = torch.empty(1, device=dev)
+    tsb = torch.tensor([sa_v], device=dev)
+    out_scale = torch.tensor([2.0], device=dev)
+    C8 = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    qa = torch.empty((M, K), dtype=torch.int8, device=dev)
+    qb = torch.empty((N, K), dtype=torch.int8, device=dev)
+    sqa, sqb = torch.empty(1, device=dev), torch.empty(1, device=dev)
+    wga = torch.empty(sq.load_library().sq_quantize_grouped_i8_workspace_bytes(M, M),
+                      dtype=torch.uint8, device=dev)
+    wgb = torch.empty(sq.load_library().sq_quantize_grouped_i8_workspace_bytes(N, N),
+                      dtype=torch.uint8, device=dev)
+    wsi = torch.empty(sq.gemm_i8_workspace_bytes(1, M, N, K), dtype=torch.uint8, device=dev)
+    Ci = torch.empty((M, N), device=dev)
+    ops = [("quant_fp8_ring_A", "bytes", M * K * 3,
+            lambda: sq.sq_quantize_fp8_ring(A, sq.SQ_FMT_E4M3, ring, 0, 0, ws, x8=a8, amax=amax)),
+           ("quant_fp8_B", "bytes", N * K * 3,
+            lambda: sq.sq_quantize_fp8(B, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax)),
+           ("gemm_fp8_nt_e4m3_out", "flops", 2.0 * M * N * K,
+            lambda: sq.sq_gemm_fp8_scaled_e4m3(a8, b8, tsb, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT,
+                                               out_scale, C=C8)),
+           ("quant_i8_per_tensor_A", "bytes", M * K * 3,
+            lambda: sq.sq_quantize_grouped_i8(A, M, q=qa, scales=sqa, workspace=wga)),
+           ("quant_i8_per_tensor_B", "bytes", N * K * 3,
+            lambda: sq.sq_quantize_grouped_i8(B, N, q=qb, scales=sqb, workspace=wgb)),
+           ("gemm_i8_per_tensor", "flops", 2.0 * M * N * K,
+            lambda: sq.sq_gemm_i8_grouped(qa, sqa, M, qb, sqb, N, wsi, C=Ci))]
+    desc = ("large M=16384 N=8192 K=8192 bf16 Student-t(3): FP8 quantize with a ring, FP8 GEMM "
+            "with E4M3 output; per-tensor INT8 quantize (two passes) and GEMM")
+    return desc, ops, 2 * (2.0 * M * N * K)
 
 
 def main():
@@ -942,13 +1086,10 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.config == "legacy_mma":
-        run_legacy_mma_probe()
-        return
     if args.config != "large" and args.impl == "sq":
         names = {"all": SMALL_CONFIGS, "extra": EXTRA_CONFIGS}.get(args.config, [args.config])
         for name in names:
-            run_small_config(name, args)
+            run_config(name, args)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -186,6 +186,32 @@ sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B
                                sq_stream stream);
 
 /*
+ * The INT8 GEMM call in two phases, for callers that time or schedule the
+ * staging apart from the GEMM.  sq_gemm_i8_rowscaled is exactly
+ * sq_gemm_i8_stage followed by sq_gemm_i8_rowscaled_staged on the same
+ * workspace and stream, and gives the same bits.
+ *
+ * sq_gemm_i8_stage writes the codes of A and B (arguments as in
+ * sq_gemm_i8_rowscaled) into `workspace` as exact 16-bit values, with the
+ * bounds on their sums of squares.
+ *
+ * sq_gemm_i8_rowscaled_staged runs the GEMM and the dequantization epilogue
+ * on a workspace that sq_gemm_i8_stage filled earlier in stream order with
+ * the same batch, M, N, K, strideA and strideB (the strides of the int8
+ * operands, which decide how the staging recorded its bounds).  The scales
+ * and outputs are as in sq_gemm_i8_rowscaled.  A workspace staged once may
+ * serve several GEMMs with different scales.  The workspace is only read.
+ */
+sq_status sq_gemm_i8_stage(const int8_t* A, const int8_t* B, int64_t batch, int64_t M, int64_t N,
+                           int64_t K, int64_t strideA, int64_t strideB, void* workspace,
+                           size_t workspace_bytes, sq_stream stream);
+sq_status sq_gemm_i8_rowscaled_staged(const float* sA, const float* sB, int64_t batch, int64_t M,
+                                      int64_t N, int64_t K, int64_t strideA, int64_t strideB,
+                                      int64_t strideC, float* C, int32_t* acc_out,
+                                      const void* workspace, size_t workspace_bytes,
+                                      sq_stream stream);
+
+/*
  * Row-group symmetric INT8 quantization  [P1 sc_matmul group_a / group_b
  * (row-group size) and per_tensor granularity; P2 formula, which is per
  * tensor].  Consecutive groups of group_rows rows share one scale:

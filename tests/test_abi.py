@@ -78,9 +78,57 @@ def test_invalid_arguments_are_rejected_without_a_device(lib):
     # workspace too small
     assert lib.sq_gemm_i8_rowscaled(p, p, p, p, 1, 4, 4, 16, 64, 64, 16, p, null, p, 8,
                                     null) == sq.SQ_ERR_INVALID_ARG
+    # the two phases check the same sizes, strides and workspace
+    assert lib.sq_gemm_i8_stage(p, p, 1, 4, 4, 24, 96, 96, p, 1 << 20, null) == sq.SQ_ERR_ALIGNMENT
+    assert lib.sq_gemm_i8_stage(null, p, 1, 4, 4, 16, 64, 64, p, 1 << 20,
+                                null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_gemm_i8_stage(p, p, 1, 4, 4, 16, 64, 64, p, 8, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 64, 64, 16, null, null, p, 1 << 20,
+                                           null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 32, 64, 16, p, null, p, 1 << 20,
+                                           null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 64, 64, 16, p1, null, p, 1 << 20,
+                                           null) == sq.SQ_ERR_ALIGNMENT
 
 
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     with pytest.raises(ValueError):
         sq.sq_quantize_rowwise_i8(torch.zeros(4, 16))
+
+
+def test_binding_checks_dtypes_and_sizes_before_calling(lib, monkeypatch):
+    """The wrappers reject wrong dtypes, scale lengths and output shapes before
+    anything reaches the library (the CUDA checks are bypassed: these tensors
+    are on the CPU and the library is never called)."""
+    import torch
+    monkeypatch.setattr(sq, "_need_cuda", lambda *ts: None)
+    a = torch.zeros(4, 16, dtype=torch.int8)
+    b = torch.zeros(6, 16, dtype=torch.int8)
+    with pytest.raises(TypeError):
+        sq._i8_operands(a.float(), b, torch.ones(4), torch.ones(6))
+    with pytest.raises(ValueError, match="sA"):
+        sq._i8_operands(a, b, torch.ones(3), torch.ones(6))
+    with pytest.raises(ValueError, match="sB"):
+        sq._i8_operands(a, b, torch.ones(4), torch.ones(4))
+    with pytest.raises(TypeError, match="sA"):
+        sq._i8_operands(a, b, torch.ones(4, dtype=torch.float64), torch.ones(6))
+    with pytest.raises(ValueError, match="share"):
+        sq._i8_operands(a, torch.zeros(6, 32, dtype=torch.int8), torch.ones(4), torch.ones(6))
+    # grouped scales: ceil(rows / group) per batch
+    sq._i8_operands(a, b, torch.ones(2), torch.ones(1), group_a=2, group_b=6)
+    with pytest.raises(ValueError, match="C"):
+        sq._i8_outputs(torch.zeros(4, 5), None, True, (4, 6), "cpu")
+    with pytest.raises(TypeError, match="acc_out"):
+        sq._i8_outputs(None, torch.zeros(4, 6, dtype=torch.int64), False, (4, 6), "cpu")
+    with pytest.raises(ValueError, match="acc_out"):
+        sq._i8_outputs(None, torch.zeros(4, 5, dtype=torch.int32), False, (4, 6), "cpu")
+    u = torch.zeros(8, 32, dtype=torch.uint8)
+    assert sq._fp8_shape(u, torch.zeros(16, 32, dtype=torch.uint8), sq.SQ_NT) == (8, 16, 32)
+    assert sq._fp8_shape(u, torch.zeros(32, 16, dtype=torch.uint8), sq.SQ_NN) == (8, 16, 32)
+    assert sq._fp8_shape(u.t().contiguous(), torch.zeros(32, 16, dtype=torch.uint8),
+                         sq.SQ_TN) == (8, 16, 32)
+    with pytest.raises(ValueError, match="share K"):
+        sq._fp8_shape(u, torch.zeros(16, 48, dtype=torch.uint8), sq.SQ_NT)
+    with pytest.raises(TypeError):
+        sq._fp8_shape(u.to(torch.int8), torch.zeros(16, 32, dtype=torch.uint8), sq.SQ_NT)

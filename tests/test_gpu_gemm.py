@@ -107,6 +107,46 @@ def test_i8_gemm_random_codes_and_acc_only():
     assert guard_intact(abuf, n, -7)
 
 
+# ------------------------------------------------------------------ INT8 in two phases
+TWO_PHASE = [
+    ("cfg1 128x512x1024 (plain staging)", 0, (128, 1024), (512, 1024)),
+    ("per head 16x196x196x64 (plain staging)", 16, (196, 64), (196, 64)),
+    ("2048x1024x1024 (bulk staging, bounds)", 0, (2048, 1024), (1024, 1024)),
+]
+
+
+@pytest.mark.parametrize("name,nb,sa_shape,sb_shape", TWO_PHASE, ids=[c[0] for c in TWO_PHASE])
+def test_i8_gemm_stage_then_staged_equals_one_call(name, nb, sa_shape, sb_shape):
+    """sq_gemm_i8_stage + sq_gemm_i8_rowscaled_staged give the bits of the
+    one-call form and of the oracle; a workspace staged once serves a second
+    GEMM with other scales."""
+    s = seed_of(name)
+    shape_a = (nb,) + sa_shape if nb else sa_shape
+    shape_b = (nb,) + sb_shape if nb else sb_shape
+    a, b = synth.normal(s, shape_a), synth.normal(s + 1, shape_b)
+    qa, sa = oracle.quantize_rowwise_i8(a)
+    qb, sb = oracle.quantize_rowwise_i8(b)
+    oacc, oC = oracle.gemm_i8(qa, qb, sa, sb)
+    M, K = sa_shape
+    N = sb_shape[0]
+    ws = torch.empty(sq.gemm_i8_workspace_bytes(max(nb, 1), M, N, K), dtype=torch.uint8,
+                     device=DEV)
+    tqa, tqb = to_dev(qa), to_dev(qb)
+    sq.sq_gemm_i8_stage(tqa, tqb, ws)
+    C, acc = sq.sq_gemm_i8_rowscaled_staged(to_dev(sa.reshape(-1)), to_dev(sb.reshape(-1)),
+                                            (nb, M, N, K), ws, acc_out=True)
+    assert np.array_equal(acc.cpu().numpy(), oacc)
+    assert np.array_equal(C.cpu().numpy(), oC)
+    # the same staged operands with doubled scales: exact powers of two, so
+    # every output doubles exactly
+    C2, _ = sq.sq_gemm_i8_rowscaled_staged(to_dev(2 * sa.reshape(-1)), to_dev(sb.reshape(-1)),
+                                           (nb, M, N, K), ws)
+    assert np.array_equal(C2.cpu().numpy(), 2 * oC)
+    C1, acc1 = sq.sq_gemm_i8_rowscaled(tqa, to_dev(sa.reshape(-1)), tqb, to_dev(sb.reshape(-1)),
+                                       ws, acc_out=True)
+    assert torch.equal(C1, C) and torch.equal(acc1, acc)
+
+
 # ------------------------------------------------------------------ FP8
 @pytest.mark.parametrize("c", [42, 47], ids=["bound holds: one K chunk", "bound fails: drained"])
 def test_i8_exactness_with_and_without_drains(c):
