@@ -326,8 +326,12 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, 
 // Warps 2..: read each finished accumulator out of TMEM, scale it and store
 // the tile (INT8: int32 sums of nch chunks, fp32 dequantized output; FP8:
 // bf16 or E4M3 output).
+// On CTA pairs the FP8 epilogue arrives on the cluster barrier (the one that
+// precedes the TMEM release) as soon as it has read its last accumulator, so
+// that the barrier completes while it converts and stores; it returns whether
+// it has arrived.
 template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
-__device__ __forceinline__ void gemm_epilogue(const CUtensorMap& tmC, const GemmParams& p,
+__device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const GemmParams& p,
                                               const GemmCta& c, int nch) {
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
     const int warp = threadIdx.x >> 5;
@@ -362,6 +366,7 @@ __device__ __forceinline__ void gemm_epilogue(const CUtensorMap& tmC, const Gemm
     uint32_t it = 0;
     uint32_t sc = 0;                       // output boxes this warp has stored
     bool ok = true;
+    bool arrived = false;
     auto release = [&](uint32_t ab) {
         tc_fence_before();
         __syncwarp();
@@ -534,6 +539,16 @@ __device__ __forceinline__ void gemm_epilogue(const CUtensorMap& tmC, const Gemm
             const uint32_t tb = tmem_base + lane_off + ab * BN + colgrp * Cfg::EPI_COLS;
             uint16_t* Cb = static_cast<uint16_t*>(p.C);
             const int64_t obase = static_cast<int64_t>(row) * p.N;
+            // A CTA's last tile: its MMAs have completed and no TMA load is
+            // pending, so the operand stages are free.  Each warp gives every
+            // one of its output boxes its own 2 KB there, and no box waits
+            // for an earlier box's store to be read (on one-wave problems this
+            // epilogue is the kernel's exposed tail).
+            const bool last_staged = p.tma_store && !p.out_e4m3 && t + num_units >= total;
+            static_assert(Cfg::EPI_WARPS * (Cfg::EPI_COLS / 32) * 2048 <= Cfg::STAGES * Cfg::STAGE,
+                          "a last tile's output boxes fit in the operand stages");
+            int box = 0;
+            if (last_staged) fence_proxy_async_smem();
             // one 32-column piece of this warp's 32 rows: scale, round, store
             auto emit = [&](uint32_t (&r)[32], const int col0) {
                 if (p.bias && row < p.M) {
@@ -577,9 +592,14 @@ __device__ __forceinline__ void gemm_epilogue(const CUtensorMap& tmC, const Gemm
                     // buffer (16-byte piece j of row r sits at piece j ^ ((r >> 1) & 3),
                     // which keeps the writes conflict-free); rows or columns past
                     // the matrix are clipped by the store.
-                    uint8_t* buf = epi_stage + (ew * 2 + (sc & 1u)) * 2048;
-                    if (lane == 0 && sc >= 2) bulk_wait_read<1>();   // the box two back is read
-                    __syncwarp();
+                    uint8_t* buf;
+                    if (last_staged) {
+                        buf = smem + (ew * (Cfg::EPI_COLS / 32) + box++) * 2048;
+                    } else {
+                        buf = epi_stage + (ew * 2 + (sc & 1u)) * 2048;
+                        if (lane == 0 && sc >= 2) bulk_wait_read<1>();   // the box two back is read
+                        __syncwarp();
+                    }
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -589,13 +609,16 @@ __device__ __forceinline__ void gemm_epilogue(const CUtensorMap& tmC, const Gemm
                     for (int j = 0; j < 4; ++j)
                         *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
                             make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    ++sc;
+                    // a last tile's boxes are stored together after the loop,
+                    // behind one proxy fence
+                    if (last_staged) return;
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         tma_store_2d(&tmC, buf, col0, m0 + quarter * 32);
                         bulk_commit();
                     }
-                    ++sc;
                 } else if (row < p.M) {
                     uint32_t pk[16];
 #pragma unroll
@@ -618,6 +641,7 @@ __device__ __forceinline__ void gemm_epilogue(const CUtensorMap& tmC, const Gemm
                     }
                 }
             };
+            const bool last = t + num_units >= total;
 #pragma unroll 1
             for (int c = 0; c < Cfg::EPI_COLS / 32; c += 2) {
                 // two TMEM loads in flight behind one wait
@@ -625,16 +649,38 @@ __device__ __forceinline__ void gemm_epilogue(const CUtensorMap& tmC, const Gemm
                 tmem_ld32(tb + c * 32, r0);
                 tmem_ld32(tb + (c + 1) * 32, r1);
                 tmem_ld_wait();
+                if (PAIR && last && c + 2 >= Cfg::EPI_COLS / 32) {
+                    // this warp's last read of TMEM, and no accumulator is
+                    // released after the last tile: nothing of this warp
+                    // touches the peer CTA or TMEM any more
+                    tc_fence_before();
+                    cluster_arrive();
+                    arrived = true;
+                }
                 const int col0 = n0 + colgrp * Cfg::EPI_COLS + c * 32;
                 emit(r0, col0);
                 emit(r1, col0 + 32);
             }
-            release(ab);
+            if (last_staged) {
+                // the shared-memory writes of every box, then their stores
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int b = 0; b < box; ++b)
+                        tma_store_2d(&tmC, smem + (ew * (Cfg::EPI_COLS / 32) + b) * 2048,
+                                     n0 + colgrp * Cfg::EPI_COLS + b * 32, m0 + quarter * 32);
+                    bulk_commit();
+                }
+            }
+            // the MMA warp waits for a released accumulator only before a
+            // next tile
+            if (!last) release(ab);
             ++it;
         }
     }
     // the staged output boxes must be written (and their buffers read) before exit
     if (!I8 && lane == 0 && sc > 0) bulk_wait_all();
+    return arrived;
 }
 
 template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
@@ -733,15 +779,25 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
 
     const GemmCta c{smem, epi_stage, full, empty, tfull, tempty, drain, abort_flag, tmem_base,
                     rank, leader, cta_unit, num_units, total};
+    bool arrived = false;
     if (warp == 0) gemm_producer<BN, I8, A_MN, B_MN, PAIR>(tmA, tmB, p, c);
     else if (warp == 1) gemm_mma<BN, I8, A_MN, B_MN, PAIR>(p, c, kbpc, nch);
-    else gemm_epilogue<BN, I8, A_MN, B_MN, PAIR>(tmC, p, c, nch);
+    else arrived = gemm_epilogue<BN, I8, A_MN, B_MN, PAIR>(tmC, p, c, nch);
 
     tc_fence_before();
+    if (PAIR && !arrived) {
+        // The producer and the MMA issuer arrive as soon as their roles end.
+        // The barrier completes once every epilogue warp of both CTAs has
+        // read its last accumulator, which it does only after the MMAs into
+        // its TMEM completed: then the leader's MMAs into the peer's TMEM are
+        // done and TMEM can be released.
+        __syncwarp();
+        cluster_arrive();
+    }
     __syncthreads();
     if (PAIR) {
         __syncwarp();
-        cluster_sync_all();   // the leader's MMAs into the peer's TMEM are done
+        cluster_wait();
     }
     if (warp == 1) {
         __syncwarp();
@@ -884,10 +940,41 @@ static cudaError_t gemm_fp8_shape(const uint8_t* A, const uint8_t* B, int M, int
     return run_gemm<BN, false, A_MN, B_MN, PAIR>(ta, tb, tc, p, st, sms);
 }
 
+// FP8 tile shape by estimated time: rounds of tiles over the SMs (or SM
+// pairs) times the k-blocks per tile times the time of one k-block on one SM,
+// in clocks.  A k-block is 128 bytes of K.  Measured on GB300 with every SM
+// loading: a single CTA's operand stages arrive at about 80 B/clk, so a
+// 128 x 128 tile (32 KB per k-block) waits on its loads (~410 clk) rather
+// than on its MMAs (256 clk); a 128 x 256 tile moves 48 KB (~614 clk); a CTA
+// of a pair holds 128 rows of A and half of B's 256 (32 KB) and is bound by
+// its MMAs (512 clk).  Ties go to the later entry of the list.  (A 256 x 128
+// pair tile, 24 KB per k-block per CTA, measured no faster than 128 x 128 on
+// the one-round shapes where it would be chosen: their short K loops wait on
+// the first loads, and a pair's set-up costs more.)
+static Shape pick_shape_fp8(int64_t M, int64_t N, int64_t K, int sms) {
+    struct Cand { Shape s; int64_t tm, tn, slots, clk; };
+    const Cand c[3] = {{Shape::Single256, 128, 256, sms, 614},
+                       {Shape::Single128, 128, 128, sms, 410},
+                       {Shape::Pair256, 256, 256, sms / 2, 512}};
+    const int64_t nkb = (K + kBKBytes - 1) / kBKBytes;
+    Shape best = Shape::Single128;
+    int64_t best_t = -1;
+    for (const Cand& x : c) {
+        const int64_t tiles = ((M + x.tm - 1) / x.tm) * ((N + x.tn - 1) / x.tn);
+        const int64_t rounds = (tiles + x.slots - 1) / x.slots;
+        const int64_t t = rounds * nkb * x.clk;
+        if (best_t < 0 || t <= best_t) {
+            best = x.s;
+            best_t = t;
+        }
+    }
+    return best;
+}
+
 template <bool A_MN, bool B_MN>
 static cudaError_t gemm_fp8_layout(const uint8_t* A, const uint8_t* B, int M, int N, int K,
                                    const GemmParams& p, int fmt, cudaStream_t st, int sms) {
-    switch (pick_shape(M, N, 1, sms)) {
+    switch (pick_shape_fp8(M, N, K, sms)) {
         case Shape::Pair256: return gemm_fp8_shape<A_MN, B_MN, 256, true>(A, B, M, N, K, p, fmt, st, sms);
         case Shape::Single256: return gemm_fp8_shape<A_MN, B_MN, 256, false>(A, B, M, N, K, p, fmt, st, sms);
         default: return gemm_fp8_shape<A_MN, B_MN, 128, false>(A, B, M, N, K, p, fmt, st, sms);

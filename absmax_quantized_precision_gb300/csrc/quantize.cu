@@ -557,10 +557,7 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
     __shared__ float s_amax;
     __shared__ int abort_flag;
 
-    const float s = scale ? *scale : ring[hist_len];
     unsigned* counter = ring ? reinterpret_cast<unsigned*>(ring + hist_len + 1) : ws + 1;
-    const float y = __frcp_rn(s);
-    const bool fast = s >= 0x1p-40f && s <= 0x1p40f;
     float m = 0.0f;
 
     const int64_t nfull = n / kFChunk;
@@ -579,6 +576,11 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
             bulk_load(in_buf + k * kFChunk * 2, x + (gw + k * GW) * kFChunk, kFChunk * 2, &full[k]);
         }
     }
+    // The step is read only now, so its memory latency overlaps that of the
+    // first chunks (bulk_load's memory clobber keeps the read below them).
+    const float s = scale ? *scale : ring[hist_len];
+    const float y = __frcp_rn(s);
+    const bool fast = s >= 0x1p-40f && s <= 0x1p40f;
     int64_t i = 0;
     for (; i < count; ++i) {
         const int stage = static_cast<int>(i % kFStages);
@@ -642,17 +644,23 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
     if (threadIdx.x == 0) {
         float bm = red[0];
         for (int w = 1; w < nwarps; ++w) bm = fmaxf(bm, red[w]);
-        // max|x| >= 0, so the float order equals the unsigned order of the bits
-        atomicMax(&ws[0], __float_as_uint(bm));
-        __threadfence();
-        const unsigned ticket = atomicAdd(counter, 1u);
+        // max|x| >= 0, so the float order equals the unsigned order of the
+        // bits.  The ticket is an acquire-release add: its release orders this
+        // block's maximum before the ticket, and the last block's acquire
+        // orders its read of the combined maximum after every other block's
+        // release (all tickets are one chain of read-modify-writes).
+        red_max_relaxed_gpu(&ws[0], __float_as_uint(bm));
+        const unsigned ticket = atom_add_acq_rel_gpu(counter, 1u);
         is_last = (ticket == gridDim.x - 1);
     }
     __syncthreads();
     if (!is_last) return;          // uniform across the block
-    __threadfence();
     if (threadIdx.x == 0) {
-        s_amax = __uint_as_float(atomicExch(&ws[0], 0u));
+        // every other block's maximum is visible (ordered by the ticket), and
+        // no block of this launch touches ws[0] any more: a read and a plain
+        // reset do what an exchange would, without waiting for it
+        s_amax = __uint_as_float(ld_relaxed_gpu(&ws[0]));
+        ws[0] = 0u;
         *amax_out = s_amax;
     }
     if (ring) {
@@ -674,7 +682,9 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
             }
         }
     }
-    if (threadIdx.x == 0) atomicExch(counter, 0u);
+    // every ticket of this launch is taken; the next launch on the stream
+    // starts after this one completes
+    if (threadIdx.x == 0) *counter = 0u;
 }
 
 template <int FMT>

@@ -111,6 +111,25 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
     return true;
 }
 
+// ------------------------------------------------------------------ global atomics
+// max into a global word, relaxed, GPU scope, no value returned.
+__device__ __forceinline__ void red_max_relaxed_gpu(unsigned* p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// add returning the old value, acquire-release, GPU scope.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------------ launches
 // Every kernel of libsq is launched with programmatic stream serialization
 // (sq_host.h, launch_pdl) and calls pdl_begin() before its first global
@@ -294,6 +313,16 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t ran
 
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of cluster_sync_all, for a thread that has finished its
+// part of the cluster's work well before it must wait for the others.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {

@@ -92,8 +92,8 @@ def algo_bytes(kernel):
 # was taken from: when the sha256 of those sources no longer matches, the
 # bench reports traffic as null.
 PROFILED_TRAFFIC = {
-    "gemm_fp8_nt": {"bytes": 775060736, "sources_sha256": "0c4c4962ef3b575962f3c4b354468457380cfe37f2bbaca93c64b58fb1ba69d5"},
-    "gemm_i8_kernel": {"bytes": 2708078592, "sources_sha256": "0c4c4962ef3b575962f3c4b354468457380cfe37f2bbaca93c64b58fb1ba69d5"},
+    "gemm_fp8_nt": {"bytes": 845101312, "sources_sha256": "4563eb120155e2e556fd197c8ef414dd2d00937fee2bbb048047666eadb9df2d"},
+    "gemm_i8_kernel": {"bytes": 2727098624, "sources_sha256": "4563eb120155e2e556fd197c8ef414dd2d00937fee2bbb048047666eadb9df2d"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
@@ -421,46 +421,37 @@ def run_sq(args, rank, world, local_rank):
     q_done = torch.cuda.Event()
     g_done = torch.cuda.Event()
 
-    CALLS = ["quant_fp8_A", "quant_fp8_B", "gemm_fp8_nt", "quant_i8_A", "quant_i8_B", "gemm_i8"]
-
-    def step(events=None, bufs=None, skip=None):
+    def step(events=None, bufs=None):
         """One step.  With `events`, the INT8 GEMM call runs as its two phases
-        (staging, then the GEMM kernel) with an event between them; `skip`
-        leaves one call out (for its marginal cost in the step)."""
+        (staging, then the GEMM kernel) with an event between them."""
         xa, xb, c8, ci = bufs if bufs is not None else (A, B, C8, Ci)
 
         def mark(i, st):
             if events is not None:
                 events[i].record(st)
         mark(0, stream)
-        if skip != "quant_fp8_A":
-            sq.sq_quantize_fp8(xa, tsa, sq.SQ_FMT_E4M3, ws, x8=a8, amax=amax_a, stream=stream)
+        sq.sq_quantize_fp8(xa, tsa, sq.SQ_FMT_E4M3, ws, x8=a8, amax=amax_a, stream=stream)
         mark(1, stream)
-        if skip != "quant_fp8_B":
-            sq.sq_quantize_fp8(xb, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax_b, stream=stream)
+        sq.sq_quantize_fp8(xb, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax_b, stream=stream)
         mark(2, stream)
         q_done.record(stream)
-        if skip != "gemm_fp8_nt":
-            sq.sq_gemm_fp8_scaled(a8, b8, tsa, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT, C=c8, stream=stream)
+        sq.sq_gemm_fp8_scaled(a8, b8, tsa, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT, C=c8, stream=stream)
         mark(3, stream)
         g_done.record(stream)
         s_i8.wait_event(q_done)
         mark(7, s_i8)
-        if skip != "quant_i8_A":
-            sq.sq_quantize_rowwise_i8(xa, q=qa, scales=sA, stream=s_i8)
+        sq.sq_quantize_rowwise_i8(xa, q=qa, scales=sA, stream=s_i8)
         mark(4, s_i8)
-        if skip != "quant_i8_B":
-            sq.sq_quantize_rowwise_i8(xb, q=qb, scales=sB, stream=s_i8)
+        sq.sq_quantize_rowwise_i8(xb, q=qb, scales=sB, stream=s_i8)
         mark(5, s_i8)
         s_i8.wait_event(g_done)
         mark(8, s_i8)
-        if skip != "gemm_i8":
-            if events is None:
-                sq.sq_gemm_i8_rowscaled(qa, sA, qb, sB, wsi, C=ci, stream=s_i8)
-            else:
-                sq.sq_gemm_i8_stage(qa, qb, wsi, stream=s_i8)
-                mark(9, s_i8)
-                sq.sq_gemm_i8_rowscaled_staged(sA, sB, (0, M, N, K), wsi, C=ci, stream=s_i8)
+        if events is None:
+            sq.sq_gemm_i8_rowscaled(qa, sA, qb, sB, wsi, C=ci, stream=s_i8)
+        else:
+            sq.sq_gemm_i8_stage(qa, qb, wsi, stream=s_i8)
+            mark(9, s_i8)
+            sq.sq_gemm_i8_rowscaled_staged(sA, sB, (0, M, N, K), wsi, C=ci, stream=s_i8)
         mark(6, s_i8)
         stream.wait_stream(s_i8)
 
@@ -506,17 +497,42 @@ def run_sq(args, rank, world, local_rank):
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error in the event pass")
 
-    # What each call costs inside the step: K steps without it, back to back,
-    # against the K full steps (programmatic launch overlap kept).
-    marginal_ms = {}
-    for name in CALLS:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+    # What each call costs inside the step (one stream): pass j runs the
+    # step's first j + 1 calls, with an event at the step's start and one after
+    # call j and nothing between, so the calls keep their launch overlap; call
+    # j's cost is the mean prefix time through j minus the one through j - 1.
+    # The INT8 call runs as its two phases, staging and the GEMM kernel.
+    seq = [("quant_fp8_A", lambda: sq.sq_quantize_fp8(A, tsa, sq.SQ_FMT_E4M3, ws, x8=a8,
+                                                        amax=amax_a, stream=stream)),
+           ("quant_fp8_B", lambda: sq.sq_quantize_fp8(B, tsb, sq.SQ_FMT_E4M3, ws, x8=b8,
+                                                        amax=amax_b, stream=stream)),
+           ("gemm_fp8_nt", lambda: sq.sq_gemm_fp8_scaled(a8, b8, tsa, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT,
+                                                         C=C8, stream=stream)),
+           ("quant_i8_A", lambda: sq.sq_quantize_rowwise_i8(A, q=qa, scales=sA, stream=stream)),
+           ("quant_i8_B", lambda: sq.sq_quantize_rowwise_i8(B, q=qb, scales=sB, stream=stream)),
+           ("stage_i8", lambda: sq.sq_gemm_i8_stage(qa, qb, wsi, stream=stream)),
+           ("gemm_i8_kernel", lambda: sq.sq_gemm_i8_rowscaled_staged(sA, sB, (0, M, N, K), wsi, C=Ci,
+                                                                     stream=stream))]
+    in_step_ms = {}
+    if not args.overlap:
+        # every round runs each prefix once, so that all prefixes see the same
+        # mix of clocks (the GPU may reach its power cap as the passes go on)
+        nseq = len(seq)
+        pe = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nseq)]
+              for _ in range(args.steps)]
         for s in range(args.steps):
-            step(skip=name)
-        e1.record(stream)
+            for j in range(nseq):
+                pe[s][j][0].record(stream)
+                for _, fn in seq[:j + 1]:
+                    fn()
+                pe[s][j][1].record(stream)
         torch.cuda.synchronize(dev)
-        marginal_ms[name] = (elapsed_ms - e0.elapsed_time(e1)) / args.steps
+        prefix = [statistics.mean(pe[s][j][0].elapsed_time(pe[s][j][1]) for s in range(args.steps))
+                  for j in range(nseq)]
+        for j, (name, _) in enumerate(seq):
+            in_step_ms[name] = prefix[j] - (prefix[j - 1] if j > 0 else 0.0)
+        if sq.sq_get_last_device_error() != sq.SQ_OK:
+            raise RuntimeError("device error in the prefix passes")
 
     # Steady-state rate of each quantize call: 10 launches back to back (each
     # overlapping the tail of the one before), events only around the batch.
@@ -653,7 +669,7 @@ def run_sq(args, rank, world, local_rank):
         return d
 
     kernels = {n: rate(n, ms) for n, ms in per_kernel.items()}
-    kernels_marginal = {n: rate(n, ms) for n, ms in marginal_ms.items()}
+    kernels_in_step = {n: rate(n, ms) for n, ms in in_step_ms.items()}
     kernels_steady = {n: rate(n, ms) for n, ms in steady_ms.items()}
 
     # Roofline: the dominant kernel of the step (the longest single launch).
@@ -729,9 +745,12 @@ def run_sq(args, rank, world, local_rank):
                          "INT8 call = stage_i8 + gemm_i8_kernel"
                          + ("; with two streams the INT8 quantize spans overlap the FP8 GEMM and "
                             "share the GPU with it" if args.overlap else "")),
-        "kernels_marginal": kernels_marginal,
-        "kernels_marginal_note": ("what each call adds to the step: K steps without it, back to "
-                                  "back, against the K full steps (launch overlap kept)"),
+        "kernels_in_step": kernels_in_step,
+        "kernels_in_step_note": ("what each call costs inside the step: the mean time of the "
+                                 "step's first j + 1 calls minus that of its first j calls, each "
+                                 "prefix timed over the K steps with events only at its two ends "
+                                 "(the calls keep their launch overlap); the first call's figure "
+                                 "includes its launch"),
         "kernels_steady": kernels_steady,
         "kernels_steady_note": ("each quantize call launched 10 times back to back with events only "
                                 "around the batch; B alternates with a same-size block of A so "
@@ -873,8 +892,9 @@ def measure_config(name, args, with_cpu=True, compact=False):
       step   the whole step (its calls in order) captured as one CUDA graph;
       calls  each call alone, captured as its own graph (its device time plus
              one launch);
-      in_step  what each call adds to the step graph (the step graph minus the
-             graph of the step without that call);
+      in_step  what each call adds to the step: the graph of the step's first
+             j + 1 calls minus the graph of its first j calls (the first
+             call's figure includes the replay's own start);
     plus the oracle's time for the whole workload on the host (all cores and
     one core).  Returns a dict; compact leaves out the eager timings."""
     import numpy as np
@@ -940,11 +960,11 @@ def measure_config(name, args, with_cpu=True, compact=False):
         return statistics.median(ev[i][0].elapsed_time(ev[i][1]) for i in range(iters))
 
     with Clocks(dev) as clk:
-        step_graph = capture([fn for _, _, _, fn in ops])
-        step_ms = time_graph(step_graph)
+        # prefix_ms[j]: the graph of the step's first j + 1 calls
+        prefix_ms = [time_graph(capture([fn for _, _, _, fn in ops[:j + 1]]))
+                     for j in range(len(ops))]
+        step_ms = prefix_ms[-1]
         call_ms = [time_graph(capture([fn])) for _, _, _, fn in ops + alt_calls]
-        without_ms = [time_graph(capture([fn for i, (_, _, _, fn) in enumerate(ops) if i != j]))
-                      if len(ops) > 1 else 0.0 for j in range(len(ops))]
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error in the graph passes")
 
@@ -981,10 +1001,9 @@ def measure_config(name, args, with_cpu=True, compact=False):
     for j, (label, kind, amount, _) in enumerate(ops + alt_calls):
         calls[label] = rates(label, kind, amount, call_ms[j])
     in_step = {}
-    if len(ops) > 1:
-        for j, (label, kind, amount, _) in enumerate(ops):
-            inc = step_ms - without_ms[j]
-            in_step[label] = ({"us": 1e3 * inc} if inc <= 0 else rates(label, kind, amount, inc))
+    for j, (label, kind, amount, _) in enumerate(ops):
+        inc = prefix_ms[j] - (prefix_ms[j - 1] if j > 0 else 0.0)
+        in_step[label] = ({"us": 1e3 * inc} if inc <= 0 else rates(label, kind, amount, inc))
     out = {"desc": desc, "value": gemm_flops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
            "us_per_step": 1e3 * step_ms, "calls": calls, "in_step": in_step,
            "l2": "256 MiB write before every timed pass", "iters": iters,

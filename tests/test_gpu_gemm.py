@@ -322,6 +322,37 @@ def test_fp8_backward_dx_nn_and_dw_tn():
     check_fp8(dW, g8, x8, fmt, sq.SQ_TN, T, sg, sx, rows=rows)
 
 
+# ------------------------------------------------------------------ the pages' one-wave shapes
+# The forward (NT 2048x1024x1024) and dX (NN) run on 128x128 tiles, dW (TN)
+# on 256x256 tiles of CTA pairs: one round of tiles each.  The ragged variants
+# clip M, N and K against those tiles.
+ONE_WAVE = [
+    ("fwd NT 2048x1024x1024 e5m2", 2048, 1024, 1024, sq.SQ_NT, sq.SQ_FMT_E5M2),
+    ("fwd NT ragged 2040x1000x1040", 2040, 1000, 1040, sq.SQ_NT, sq.SQ_FMT_E4M3),
+    ("fwd NT ragged 1800x936x1024", 1800, 936, 1024, sq.SQ_NT, sq.SQ_FMT_E4M3),
+    ("dX NN ragged 2040x1008x4096", 2040, 1008, 4096, sq.SQ_NN, sq.SQ_FMT_E4M3),
+    ("dW TN ragged 4080x1008x2048", 4080, 1008, 2048, sq.SQ_TN, sq.SQ_FMT_E4M3),
+    ("dW TN 4096x1024x2048 e5m2", 4096, 1024, 2048, sq.SQ_TN, sq.SQ_FMT_E5M2),
+]
+
+
+@pytest.mark.parametrize("name,M,N,K,layout,fmt", ONE_WAVE, ids=[c[0] for c in ONE_WAVE])
+def test_fp8_gemm_one_wave_shapes(name, M, N, K, layout, fmt):
+    a8, b8, sa, sb = fp8_inputs(name, M, N, K, fmt)
+    A = a8 if layout != sq.SQ_TN else np.ascontiguousarray(a8.T)
+    B = b8 if layout == sq.SQ_NT else np.ascontiguousarray(b8.T)
+    C, cbuf, n = guarded((M, N), torch.bfloat16, 3.0)
+    sq.sq_gemm_fp8_scaled(to_dev(A), to_dev(B), torch.tensor([sa], device=DEV),
+                          torch.tensor([sb], device=DEV), fmt, layout, C=C)
+    # every tile row band of both CTAs of a pair: the first and last rows of
+    # each 128-row block, plus seeded rows
+    edges = np.concatenate([np.arange(0, M, 128), np.minimum(np.arange(127, M + 127, 128), M - 1)])
+    rows = np.unique(np.concatenate([edges, np.random.default_rng(seed_of(name)).choice(M, 64,
+                                                                                        replace=False)]))
+    check_fp8(C, A, B, fmt, layout, K, sa, sb, rows=rows)
+    assert guard_intact(cbuf, n, 3.0)
+
+
 # ------------------------------------------------------------------ CTA-pair shapes
 # Problems with at least one 256x256 tile per pair of SMs run on the 2-SM
 # (cta_group::2) kernel; these sizes select it and keep ragged tails in M and N.
@@ -388,6 +419,7 @@ E4M3_OUT = [
     ("out8 NN 256x384x512", 256, 384, 512, sq.SQ_NN, sq.SQ_FMT_E4M3),
     ("out8 TN 208x160x256", 208, 160, 256, sq.SQ_TN, sq.SQ_FMT_E5M2),
     ("out8 pair NT 2200x2208x256", 2200, 2208, 256, sq.SQ_NT, sq.SQ_FMT_E4M3),
+    ("out8 one round NT 2040x1000x1024", 2040, 1000, 1024, sq.SQ_NT, sq.SQ_FMT_E4M3),
 ]
 
 
