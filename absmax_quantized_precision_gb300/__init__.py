@@ -37,7 +37,7 @@ EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "
            "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
            "sq_quantize_grouped_i8", "sq_gemm_i8_grouped", "sq_linear_workspace_bytes",
            "sq_linear_forward_fp8", "sq_linear_backward_fp8", "sq_selftest_bounded_wait",
-           "sq_gemm_i8_stage", "sq_gemm_i8_rowscaled_staged")
+           "sq_gemm_i8_stage", "sq_gemm_i8_rowscaled_staged", "sq_quantize_rowwise_i8_staged")
 
 # size of the fixed scratch array behind sq_gemm_i8_rowscaled_noalloc
 GEMM_I8_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -103,9 +103,11 @@ def load_library():
     L.sq_linear_backward_fp8.restype = i32
     L.sq_gemm_i8_stage.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, vp, sz, vp]
     L.sq_gemm_i8_stage.restype = i32
-    L.sq_gemm_i8_rowscaled_staged.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, i64, vp, vp,
-                                              vp, sz, vp]
+    L.sq_gemm_i8_rowscaled_staged.argtypes = [vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, sz, vp]
     L.sq_gemm_i8_rowscaled_staged.restype = i32
+    L.sq_quantize_rowwise_i8_staged.argtypes = [vp, i32, i64, i64, i64, vp, vp, i32, i64, i64, i64,
+                                                i64, vp, sz, vp]
+    L.sq_quantize_rowwise_i8_staged.restype = i32
     L.sq_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp]
     L.sq_selftest_bounded_wait.restype = i32
     _lib = L
@@ -428,9 +430,45 @@ def sq_gemm_i8_rowscaled_staged(sA: torch.Tensor, sB: torch.Tensor, shape, works
     C, acc_out = _i8_outputs(C, acc_out, want_c, oshape, sA.device)
     with torch.cuda.device(dev):
         _check(load_library().sq_gemm_i8_rowscaled_staged(
-            _ptr(sA), _ptr(sB), nb, M, N, K, M * K, N * K, M * N, _ptr(C), _ptr(acc_out),
+            _ptr(sA), _ptr(sB), nb, M, N, K, M * N, _ptr(C), _ptr(acc_out),
             _ptr(workspace), _ws_bytes(workspace), _stream(stream)), "sq_gemm_i8_rowscaled_staged")
     return C, acc_out
+
+
+def sq_quantize_rowwise_i8_staged(x: torch.Tensor, operand: int, shape, workspace: torch.Tensor,
+                                  q: torch.Tensor = None, scales: torch.Tensor = None,
+                                  stream=None):
+    """sq_quantize_rowwise_i8 of x that also stages its codes in an INT8 GEMM
+    workspace for operands of shape = (batch, M, N, K) (batch 0: the 2-D
+    form); operand 0 is A, 1 is B.  Returns (q, scales)."""
+    dev = _need_cuda(x, q, scales, workspace)
+    if x.dtype == torch.float32:
+        dt = SQ_F32
+    elif x.dtype == torch.bfloat16:
+        dt = SQ_BF16
+    else:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    nb, M, N, K = (int(v) for v in shape)
+    nb = max(nb, 1)
+    cols = x.shape[-1]
+    x2 = x.reshape(-1, cols) if x.dim() != 2 else x
+    if x2.numel() and x2.stride(-1) != 1:
+        raise ValueError("rows of x must be contiguous")
+    rows = x2.shape[0]
+    if rows != nb * (N if operand else M) or cols != K:
+        raise ValueError(f"x {tuple(x.shape)} is not operand {'B' if operand else 'A'} of {shape}")
+    ld = x2.stride(0) if rows > 1 else cols
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    _need(q, torch.int8, numel=rows * cols, what="q")
+    if scales is None:
+        scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _need(scales, torch.float32, numel=rows, what="scales")
+    with torch.cuda.device(dev):
+        _check(load_library().sq_quantize_rowwise_i8_staged(
+            _ptr(x2), dt, rows, cols, ld, _ptr(q), _ptr(scales), int(operand), nb, M, N, K,
+            _ptr(workspace), _ws_bytes(workspace), _stream(stream)), "sq_quantize_rowwise_i8_staged")
+    return q, scales
 
 
 def sq_gemm_i8_rowscaled_noalloc(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor,

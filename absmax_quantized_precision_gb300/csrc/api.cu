@@ -127,8 +127,8 @@ sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, u
                                              reinterpret_cast<cudaStream_t>(stream), ds->sms));
 }
 
-// fp16 copies of A and B, then 2 x 256 words of staging bounds
-constexpr size_t kI8BoundBytes = 2 * 256 * sizeof(unsigned);
+// fp16 copies of A and B, then the two operands' bound regions
+constexpr size_t kI8BoundBytes = 2 * sq::kBoundSlots * sizeof(unsigned);
 
 size_t sq_gemm_i8_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K) {
     if (batch <= 0 || M <= 0 || N <= 0 || K <= 0) return 0;
@@ -154,7 +154,7 @@ I8Workspace i8_workspace(void* workspace, int64_t batch, int64_t M, int64_t N, i
     const size_t bbytes = (static_cast<size_t>(batch) * N * K * 2 + 255) & ~static_cast<size_t>(255);
     unsigned* bound_a = reinterpret_cast<unsigned*>(w + abytes + bbytes);
     return I8Workspace{reinterpret_cast<uint16_t*>(w), reinterpret_cast<uint16_t*>(w + abytes),
-                       bound_a, bound_a + 256};
+                       bound_a, bound_a + sq::kBoundSlots};
 }
 
 // Checks shared by both phases of the INT8 GEMM: sizes, strides of the int8
@@ -181,28 +181,24 @@ sq_status i8_stage(const int8_t* A, const int8_t* B, int64_t batch, int64_t M, i
                    int64_t K, int64_t strideA, int64_t strideB, void* workspace,
                    DeviceState* ds, cudaStream_t st) {
     const I8Workspace w = i8_workspace(workspace, batch, M, N, K);
-    int nparts_a = 0, nparts_b = 0;
     return from_cuda(sq::launch_i8_to_f16_pair(A, M, B, N, batch, K, strideA, strideB, w.A16, w.B16,
-                                               w.bound_a, &nparts_a, w.bound_b, &nparts_b,
-                                               ds->err_word, st, ds->sms));
+                                               w.bound_a, w.bound_b, ds->err_word, st, ds->sms));
 }
 
 // Phase 2: the GEMM on the staged operands with the dequantization epilogue.
-// The bound counts are those the staging of the same sizes reports.
+// The staging recorded its bounds (or none) in the workspace.
 sq_status i8_gemm_staged(const float* sA, int64_t ga, const float* sB, int64_t gb, int64_t batch,
-                         int64_t M, int64_t N, int64_t K, int64_t strideA, int64_t strideB,
-                         int64_t strideC, float* C, int32_t* acc_out, const void* workspace,
-                         DeviceState* ds, cudaStream_t st) {
+                         int64_t M, int64_t N, int64_t K, int64_t strideC, float* C,
+                         int32_t* acc_out, const void* workspace, DeviceState* ds,
+                         cudaStream_t st) {
     if (ga > M) ga = M;
     if (gb > N) gb = N;
     const I8Workspace w = i8_workspace(const_cast<void*>(workspace), batch, M, N, K);
-    const int nparts_a = sq::i8_staging_parts(batch, M, K, strideA, ds->sms);
-    const int nparts_b = sq::i8_staging_parts(batch, N, K, strideB, ds->sms);
     return from_cuda(sq::launch_gemm_i8(w.A16, w.B16, sA, sB, static_cast<int>(ga),
                                         static_cast<int>(gb), static_cast<int>(batch),
                                         static_cast<int>(M), static_cast<int>(N),
                                         static_cast<int>(K), strideC, C, acc_out, w.bound_a,
-                                        nparts_a, w.bound_b, nparts_b, ds->err_word, st, ds->sms));
+                                        w.bound_b, ds->err_word, st, ds->sms));
 }
 
 sq_status i8_check_outputs(const float* sA, const float* sB, int64_t M, int64_t N,
@@ -231,8 +227,7 @@ sq_status gemm_i8_common(const int8_t* A, const float* sA, int64_t ga, const int
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     r = i8_stage(A, B, batch, M, N, K, strideA, strideB, workspace, ds, st);
     if (r != SQ_OK) return r;
-    return i8_gemm_staged(sA, ga, sB, gb, batch, M, N, K, strideA, strideB, strideC, C, acc_out,
-                          workspace, ds, st);
+    return i8_gemm_staged(sA, ga, sB, gb, batch, M, N, K, strideC, C, acc_out, workspace, ds, st);
 }
 
 }  // namespace
@@ -252,19 +247,41 @@ sq_status sq_gemm_i8_stage(const int8_t* A, const int8_t* B, int64_t batch, int6
 }
 
 sq_status sq_gemm_i8_rowscaled_staged(const float* sA, const float* sB, int64_t batch, int64_t M,
-                                      int64_t N, int64_t K, int64_t strideA, int64_t strideB,
-                                      int64_t strideC, float* C, int32_t* acc_out,
-                                      const void* workspace, size_t workspace_bytes,
-                                      sq_stream stream) {
-    sq_status r = i8_check_common(batch, M, N, K, strideA, strideB, workspace, workspace_bytes);
+                                      int64_t N, int64_t K, int64_t strideC, float* C,
+                                      int32_t* acc_out, const void* workspace,
+                                      size_t workspace_bytes, sq_stream stream) {
+    sq_status r = i8_check_common(batch, M, N, K, M * K, N * K, workspace, workspace_bytes);
     if (r != SQ_OK) return r;
     r = i8_check_outputs(sA, sB, M, N, strideC, C, acc_out, 1, 1);
     if (r != SQ_OK) return r;
     cudaError_t e = cudaSuccess;
     DeviceState* ds = device_state(&e);
     if (!ds) return from_cuda(e);
-    return i8_gemm_staged(sA, 1, sB, 1, batch, M, N, K, strideA, strideB, strideC, C, acc_out,
-                          workspace, ds, reinterpret_cast<cudaStream_t>(stream));
+    return i8_gemm_staged(sA, 1, sB, 1, batch, M, N, K, strideC, C, acc_out, workspace, ds,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+sq_status sq_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t rows, int64_t cols,
+                                        int64_t ld, int8_t* q, float* scales, int operand,
+                                        int64_t batch, int64_t M, int64_t N, int64_t K,
+                                        void* workspace, size_t workspace_bytes,
+                                        sq_stream stream) {
+    if (dtype != SQ_F32 && dtype != SQ_BF16) return SQ_ERR_INVALID_ARG;
+    if (operand != 0 && operand != 1) return SQ_ERR_INVALID_ARG;
+    sq_status r = i8_check_common(batch, M, N, K, M * K, N * K, workspace, workspace_bytes);
+    if (r != SQ_OK) return r;
+    if (rows != batch * (operand ? N : M) || cols != K || ld < cols) return SQ_ERR_INVALID_ARG;
+    if (!x || !q || !scales) return SQ_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    const int64_t esz = dtype == SQ_F32 ? 4 : 2;
+    const bool vec_ok = aligned16(x) && aligned16(q) && ((ld * esz) % 16 == 0) && (cols % 16 == 0);
+    const I8Workspace w = i8_workspace(workspace, batch, M, N, K);
+    return from_cuda(sq::launch_quantize_rowwise_i8_staged(
+        x, dtype, rows, cols, ld, q, scales, vec_ok, operand ? w.B16 : w.A16,
+        operand ? w.bound_b : w.bound_a, ds->err_word, reinterpret_cast<cudaStream_t>(stream),
+        ds->sms));
 }
 
 sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B, const float* sB,

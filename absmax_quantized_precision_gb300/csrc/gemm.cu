@@ -45,7 +45,7 @@ constexpr int kGroupM = 16;      // FP8: tile rows per raster group
 constexpr int kGroupMI8 = 8;     // INT8: its 16-bit operand stripes are twice as large
 constexpr int kI8ChunkK = 1024; // K elements per exact FP32 chunk
 constexpr int kStgChunk = 1024; // codes per warp chunk of the INT8 staging pipeline
-constexpr int kStgMaxParts = 256; // per-CTA bound slots per operand (>= staging CTAs)
+constexpr int kStgMaxParts = 256; // staging CTAs per operand (each writes one bound slot)
 
 struct GemmParams {
     int M, N, K;
@@ -60,12 +60,11 @@ struct GemmParams {
     int32_t* acc_out;      // INT8 only (nullable)
     int group_m;           // tile rows per raster group
     int tma_store;         // FP8 bf16 output: stage 32x32 boxes in shared memory, store with TMA
-    // INT8: per-CTA maxima, written by the staging launches, of the sum of
-    // squared codes over any staged chunk of kStgChunk codes (nparts == 0:
-    // unknown), and how many such chunks one row can overlap
+    // INT8: the bound regions that the staging wrote in the workspace
+    // (sq_bound.h layout: a header word, then one slot per staging CTA), and
+    // how many staged chunks of kStgChunk codes one row can overlap
     const unsigned* bound_a;
     const unsigned* bound_b;
-    int nparts_a, nparts_b;
     int row_chunks_a, row_chunks_b;
     int64_t strideC;
     uint32_t idesc;
@@ -84,7 +83,7 @@ struct GemmParams {
 //               256 x BN tiles with cta_group::2 MMAs issued by the leader
 //               (rank 0): each CTA holds 128 rows of A and BN/2 rows of B, so
 //               each SM reads half of the B tile from its shared memory.
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
 struct GemmCfg {
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;           // B rows this CTA stages
     static constexpr int A_BYTES = kBM * kBKBytes;              // 16 KB
@@ -96,9 +95,11 @@ struct GemmCfg {
     // Epilogue warps, each owning 32 rows x EPI_COLS columns of the tile.
     // INT8 keeps its running int32 sums in registers, so it takes 8.  FP8
     // takes 8 on 128-wide tiles, where one tile per CTA leaves the epilogue
-    // exposed (5-7% faster on one-wave shapes), and 4 on 256-wide tiles, whose
-    // epilogue overlaps the next tile's MMAs (8 measured about 1% slower).
-    static constexpr int EPI_WARPS = (I8 || BN == 128) ? 8 : 4;
+    // exposed (5-7% faster on one-wave shapes), and on 256-wide tiles of
+    // launches that run a single round of tiles (WIDE_EPI); 4 on 256-wide
+    // tiles of longer launches, whose epilogue overlaps the next tile's MMAs
+    // (8 measured about 1% slower there).
+    static constexpr int EPI_WARPS = (I8 || BN == 128 || WIDE_EPI) ? 8 : 4;
     static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int TMEM_COLS = 2 * BN;
@@ -110,7 +111,7 @@ struct GemmCfg {
     static constexpr int KSTEP_K = 32;                      // K-major: 32 B inside the row
     static constexpr int KSTEP_MN = (I8 ? 16 : 32) * 128;   // MN-major: that many K rows
     static constexpr int MN_LBO = kBKBytes * 128;           // 16 KB between 128-B column blocks
-    static_assert(2 * STAGES * 8 + 5 * 8 + 16 <= BAR_BYTES, "barrier area");
+    static_assert(2 * STAGES * 8 + 5 * 8 + 24 <= BAR_BYTES, "barrier area");
     static_assert(SMEM <= 232448, "shared memory budget");
     // the TMEM allocation is made before the grid-dependency wait, which
     // relies on no two GEMM CTAs (of any shape) sharing an SM
@@ -158,10 +159,10 @@ struct GemmCta {
 
 // Warp 0: one elected thread streams the A and B boxes of every k-block of
 // this CTA's tiles into the ring of stages.
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
 __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                               const GemmParams& p, const GemmCta& c) {
-    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
     uint8_t* smem = c.smem;
     uint64_t* full = c.full;
     uint64_t* empty = c.empty;
@@ -244,9 +245,9 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
 // Warp 1: on the leader, one elected thread issues the MMAs of each k-block
 // into one of the two TMEM accumulators (kbpc k-blocks per accumulator
 // chunk, nch chunks per tile) and commits stages and accumulators.
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
 __device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, int kbpc, int nch) {
-    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
     uint8_t* smem = c.smem;
     uint64_t* full = c.full;
     uint64_t* empty = c.empty;
@@ -330,10 +331,10 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, 
 // precedes the TMEM release) as soon as it has read its last accumulator, so
 // that the barrier completes while it converts and stores; it returns whether
 // it has arrived.
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
 __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const GemmParams& p,
                                               const GemmCta& c, int nch) {
-    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     uint8_t* smem = c.smem;
@@ -683,11 +684,11 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
     return arrived;
 }
 
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
-__global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
+__global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -699,7 +700,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    unsigned* bound_max = reinterpret_cast<unsigned*>(tmem_slot + 2);   // INT8: [A, B]
+    unsigned* bound_max = reinterpret_cast<unsigned*>(tmem_slot + 2);   // INT8: [A, B, mult A, mult B]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -740,15 +741,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     // tail.  (No two GEMM CTAs fit on one SM, so the allocation never waits
     // for an earlier GEMM's TMEM.)
     pdl_begin();
-    if (I8 && (warp == 2 || warp == 3)) {
-        const unsigned* src = warp == 2 ? p.bound_a : p.bound_b;
-        const int np = warp == 2 ? p.nparts_a : p.nparts_b;
-        unsigned m = 0u;
-        for (int i = lane; i < np; i += 32) m = max(m, src[i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) bound_max[warp - 2] = m;
-    }
     tc_fence_before();
     __syncthreads();
     if (PAIR) {
@@ -760,18 +752,43 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
 
     // INT8 exactness.  Every partial sum the tensor core forms for C[i,j] is an
     // integer of magnitude at most sum_k |a_ik b_jk| <= |a_i|_2 |b_j|_2
-    // (Cauchy-Schwarz), and |a_i|_2^2 <= row_chunks_a * (largest sum of
-    // squares over a staged chunk).  When the product of the two bounds is
-    // below 2^48, every partial sum stays below 2^24 and is exact in fp32 in
-    // any order, so the whole K is accumulated in one chunk; otherwise the
-    // accumulator is drained into int32 every kI8ChunkK (127^2 * 1024 < 2^24).
+    // (Cauchy-Schwarz).  The staging bounds |a_i|_2^2 either by the largest
+    // row norm itself or by row_chunks_a * (the largest sum of squares over a
+    // staged chunk).  When the product of the two bounds is below 2^48, every
+    // partial sum stays below 2^24 and is exact in fp32 in any order, so the
+    // whole K is accumulated in one chunk; otherwise the accumulator is
+    // drained into int32 every kI8ChunkK (127^2 * 1024 < 2^24).
+    //
+    // Only the MMA issuer and the epilogue need the decision: warps 2 and 3
+    // read the bounds while the producer already streams the first stages,
+    // and a named barrier among warps 1.. hands the result over.
     int kbpc = p.kb_per_chunk, nch = p.nchunks;
-    if (I8 && p.nparts_a > 0 && p.nparts_b > 0) {
-        const unsigned long long a2 = static_cast<unsigned long long>(p.row_chunks_a) * bound_max[0];
-        const unsigned long long b2 = static_cast<unsigned long long>(p.row_chunks_b) * bound_max[1];
-        if (a2 * b2 < (1ull << 48)) {
-            kbpc = p.nkb;
-            nch = 1;
+    if (I8 && warp >= 1 && p.bound_a && p.bound_b) {
+        if (warp == 2 || warp == 3) {
+            const unsigned* hdr = warp == 2 ? p.bound_a : p.bound_b;
+            const unsigned h = hdr[0];
+            const int np = min(static_cast<int>(h & kBoundCountMask), kBoundSlots - 1);
+            unsigned m = 0u;
+            for (int i = lane; i < np; i += 32) m = max(m, hdr[1 + i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) {
+                const unsigned mult = (h & kBoundRowNorms) ? 1u
+                                      : static_cast<unsigned>(warp == 2 ? p.row_chunks_a : p.row_chunks_b);
+                // 0: no bound recorded (the staging took the plain kernel)
+                bound_max[warp - 2] = np > 0 ? m : 0xFFFFFFFFu;
+                bound_max[warp] = mult;
+            }
+        }
+        named_barrier_sync(1, 32 * (1 + Cfg::EPI_WARPS));
+        if (bound_max[0] != 0xFFFFFFFFu && bound_max[1] != 0xFFFFFFFFu) {
+            const unsigned long long a2 = static_cast<unsigned long long>(bound_max[2]) * bound_max[0];
+            const unsigned long long b2 = static_cast<unsigned long long>(bound_max[3]) * bound_max[1];
+            // a2 * b2 < 2^48, without overflow (a2, b2 < 2^40)
+            if (a2 == 0 || b2 <= ((1ull << 48) - 1) / a2) {
+                kbpc = p.nkb;
+                nch = 1;
+            }
         }
     }
 
@@ -780,9 +797,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR>::THREADS, 1)
     const GemmCta c{smem, epi_stage, full, empty, tfull, tempty, drain, abort_flag, tmem_base,
                     rank, leader, cta_unit, num_units, total};
     bool arrived = false;
-    if (warp == 0) gemm_producer<BN, I8, A_MN, B_MN, PAIR>(tmA, tmB, p, c);
-    else if (warp == 1) gemm_mma<BN, I8, A_MN, B_MN, PAIR>(p, c, kbpc, nch);
-    else arrived = gemm_epilogue<BN, I8, A_MN, B_MN, PAIR>(tmC, p, c, nch);
+    if (warp == 0) gemm_producer<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>(tmA, tmB, p, c);
+    else if (warp == 1) gemm_mma<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>(p, c, kbpc, nch);
+    else arrived = gemm_epilogue<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>(tmC, p, c, nch);
 
     tc_fence_before();
     if (PAIR && !arrived) {
@@ -859,11 +876,11 @@ static bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
 static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                             const GemmParams& p, cudaStream_t st, int sms) {
-    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR>;
-    auto kern = gemm_tc_kernel<BN, I8, A_MN, B_MN, PAIR>;
+    using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
+    auto kern = gemm_tc_kernel<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
     // CTAs (or CTA pairs) that fit this device at once
     const std::pair<cudaError_t, int> fit = per_device_once(reinterpret_cast<const void*>(kern), [&] {
         cudaError_t attr_err =
@@ -914,7 +931,7 @@ static Shape pick_shape(int64_t M, int64_t N, int64_t batch, int sms) {
 template <bool A_MN, bool B_MN, int BN, bool PAIR>
 static cudaError_t gemm_fp8_shape(const uint8_t* A, const uint8_t* B, int M, int N, int K,
                                   GemmParams p, int fmt, cudaStream_t st, int sms) {
-    using Cfg = GemmCfg<BN, false, A_MN, B_MN, PAIR>;
+    using Cfg = GemmCfg<BN, false, A_MN, B_MN, PAIR, false>;   // tile geometry only
     CUtensorMap ta, tb;
     bool ok;
     if (A_MN) ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, M, 128, kBKBytes);
@@ -937,7 +954,10 @@ static cudaError_t gemm_fp8_shape(const uint8_t* A, const uint8_t* B, int M, int
             return cudaErrorInvalidValue;
         p.tma_store = 1;
     }
-    return run_gemm<BN, false, A_MN, B_MN, PAIR>(ta, tb, tc, p, st, sms);
+    // one round of 256-wide tiles leaves the epilogue exposed: give it 8 warps
+    if (BN == 256 && static_cast<int64_t>(p.mt) * p.nt <= (PAIR ? sms / 2 : sms))
+        return run_gemm<BN, false, A_MN, B_MN, PAIR, true>(ta, tb, tc, p, st, sms);
+    return run_gemm<BN, false, A_MN, B_MN, PAIR, false>(ta, tb, tc, p, st, sms);
 }
 
 // FP8 tile shape by estimated time: rounds of tiles over the SMs (or SM
@@ -1008,7 +1028,7 @@ cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa,
 template <int BN, bool PAIR>
 static cudaError_t gemm_i8_shape(const uint16_t* A16, const uint16_t* B16, int batch, int M, int N,
                                  int K, GemmParams p, cudaStream_t st, int sms) {
-    using Cfg = GemmCfg<BN, true, false, false, PAIR>;
+    using Cfg = GemmCfg<BN, true, false, false, PAIR, false>;
     const int bk = kBKBytes / 2;   // 64 fp16 per k-block
     CUtensorMap ta, tb;
     if (!encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A16, K, M, batch,
@@ -1026,14 +1046,13 @@ static cudaError_t gemm_i8_shape(const uint16_t* A16, const uint16_t* B16, int b
     CUtensorMap tc;
     memset(&tc, 0, sizeof(tc));
     p.tma_store = 0;
-    return run_gemm<BN, true, false, false, PAIR>(ta, tb, tc, p, st, sms);
+    return run_gemm<BN, true, false, false, PAIR, false>(ta, tb, tc, p, st, sms);
 }
 
 cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
                            const float* sB, int ga, int gb, int batch, int M, int N, int K,
                            int64_t strideC, float* C, int32_t* acc_out, const unsigned* bound_a,
-                           int nparts_a, const unsigned* bound_b, int nparts_b,
-                           unsigned* err_word, cudaStream_t st, int sms) {
+                           const unsigned* bound_b, unsigned* err_word, cudaStream_t st, int sms) {
     const int bk = kBKBytes / 2;
     GemmParams p{};
     p.M = M; p.N = N; p.K = K; p.batch = batch;
@@ -1052,8 +1071,6 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
     p.err_word = err_word;
     p.bound_a = bound_a;
     p.bound_b = bound_b;
-    p.nparts_a = bound_a ? nparts_a : 0;
-    p.nparts_b = bound_b ? nparts_b : 0;
     // a row of K codes overlaps at most ceil(K / chunk) + 1 staged chunks
     p.row_chunks_a = p.row_chunks_b = (K + kStgChunk - 1) / kStgChunk + 1;
     if (pick_shape(M, N, batch, sms) == Shape::Pair256)
@@ -1067,20 +1084,6 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
 }
 
 // ---------------------------------------------------------------- staging
-// Eight int8 codes -> eight exact fp16 values.  With u = c + 128 in [1, 255]
-// (the code's byte with its top bit flipped), the fp16 bit pattern 0x6400 | u
-// is the value 1024 + u exactly (the spacing of fp16 in [1024, 2048) is 1),
-// and subtracting 1152 leaves c exactly.
-__device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 w) {
-    const uint32_t a = w.x ^ 0x80808080u;
-    const uint32_t b = w.y ^ 0x80808080u;
-    uint32_t o[4] = {__byte_perm(a, 0x64646464u, 0x4140), __byte_perm(a, 0x64646464u, 0x4342),
-                     __byte_perm(b, 0x64646464u, 0x4140), __byte_perm(b, 0x64646464u, 0x4342)};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(o[k]) : "r"(0x64806480u));
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // Small or strided operands: a grid-stride kernel over up to two staging
 // jobs at once (A and B of one GEMM call share the launch).
 struct StageJob {
@@ -1088,10 +1091,15 @@ struct StageJob {
     int64_t rows, K, stride;    // rows per batch; batch b starts at src + b*stride
     int64_t total;              // 16-code pieces: batch * rows * K / 16
     uint16_t* dst;
+    unsigned* bound;            // the operand's bound header (nullable): set to "none"
 };
 
 __global__ void __launch_bounds__(256) i8_to_f16_kernel(const StageJob j0, const StageJob j1) {
     pdl_begin();
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (j0.bound) *j0.bound = 0u;   // this path records no bound
+        if (j1.bound) *j1.bound = 0u;
+    }
     // 16 codes per step: one 16-B load, two 16-B stores (K % 16 == 0)
     const int64_t all = j0.total + j1.total;
     for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < all;
@@ -1125,7 +1133,7 @@ constexpr int kStgSmem = kStgWarps * kStgWarpBytes + kStgWarps * kStgStages * 8 
 __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const int8_t* __restrict__ src,
                                                                        int64_t n,
                                                                        uint16_t* __restrict__ dst,
-                                                                       unsigned* __restrict__ parts,
+                                                                       unsigned* __restrict__ bound,
                                                                        unsigned* err_word) {
     pdl_begin();
     extern __shared__ uint8_t gsmem_raw[];
@@ -1223,19 +1231,19 @@ __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const in
         if (lane == 0 && tq != 0) atomicAdd(&tail_sq, static_cast<unsigned>(tq));
     }
     __syncthreads();
-    if (threadIdx.x == 0 && parts) {
+    if (threadIdx.x == 0 && bound) {
         unsigned m = tail_sq;
         for (int w = 0; w < kStgWarps; ++w) m = max(m, warp_max[w]);
-        parts[blockIdx.x] = m;
+        bound[1 + blockIdx.x] = m;
+        if (blockIdx.x == 0) bound[0] = gridDim.x;   // slot count; chunk sums
     }
 }
 
-// How many bound slots the staging of one operand writes: the CTA count of
-// the bulk pipeline when the operand takes it (contiguous and at least about
-// 8192 codes per SM; smaller tensors take the plain kernel, with no large
-// shared-memory carveout), else 0.  The GEMM of a staged workspace recomputes
-// it from the same sizes.
-int i8_staging_parts(int64_t batch, int64_t rows, int64_t K, int64_t stride, int sms) {
+// CTAs of the bulk pipeline for one operand (one bound slot each), or 0 when
+// the operand takes the plain kernel: contiguous operands of at least about
+// 8192 codes per SM take the pipeline; smaller ones the plain kernel, with no
+// large shared-memory carveout.
+static int i8_staging_blocks(int64_t batch, int64_t rows, int64_t K, int64_t stride, int sms) {
     const int64_t n = batch * rows * K;
     if (!(stride == rows * K || batch == 1) || n < static_cast<int64_t>(8192) * sms) return 0;
     int64_t blocks = (n / kStgChunk + kStgWarps - 1) / kStgWarps;
@@ -1249,9 +1257,9 @@ int i8_staging_parts(int64_t batch, int64_t rows, int64_t K, int64_t stride, int
 // One operand through the bulk pipeline, when it qualifies.  Returns false if
 // it does not.
 static bool stage_bulk(const int8_t* src, int64_t batch, int64_t rows, int64_t K, int64_t stride,
-                       uint16_t* dst, unsigned* parts, int* nparts, unsigned* err_word,
-                       cudaStream_t st, int sms, cudaError_t* err) {
-    const int blocks = i8_staging_parts(batch, rows, K, stride, sms);
+                       uint16_t* dst, unsigned* bound, unsigned* err_word, cudaStream_t st,
+                       int sms, cudaError_t* err) {
+    const int blocks = i8_staging_blocks(batch, rows, K, stride, sms);
     if (!err_word || blocks == 0) return false;
     const int64_t n = batch * rows * K;
     const cudaError_t attr =
@@ -1261,36 +1269,48 @@ static bool stage_bulk(const int8_t* src, int64_t batch, int64_t rows, int64_t K
         return true;
     }
     *err = launch_pdl(i8_to_f16_bulk_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kStgWarps * 32),
-                      kStgSmem, st, 1u, src, n, dst, parts, err_word);
-    if (nparts) *nparts = blocks;
+                      kStgSmem, st, 1u, src, n, dst, bound, err_word);
     return true;
+}
+
+static cudaError_t stage_plain(StageJob j0, StageJob j1, cudaStream_t st, int sms) {
+    const int64_t all = j0.total + j1.total;
+    int64_t blocks = (all + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1u,
+                      j0, j1);
 }
 
 cudaError_t launch_i8_to_f16_pair(const int8_t* a, int64_t M, const int8_t* b, int64_t N,
                                   int64_t batch, int64_t K, int64_t stride_a, int64_t stride_b,
-                                  uint16_t* a16, uint16_t* b16, unsigned* parts_a, int* nparts_a,
-                                  unsigned* parts_b, int* nparts_b, unsigned* err_word,
-                                  cudaStream_t st, int sms) {
-    *nparts_a = 0;
-    *nparts_b = 0;
+                                  uint16_t* a16, uint16_t* b16, unsigned* bound_a,
+                                  unsigned* bound_b, unsigned* err_word, cudaStream_t st,
+                                  int sms) {
     StageJob small[2];
     int nsmall = 0;
     cudaError_t e = cudaSuccess;
-    if (!stage_bulk(a, batch, M, K, stride_a, a16, parts_a, nparts_a, err_word, st, sms, &e))
-        small[nsmall++] = StageJob{a, M, K, stride_a, batch * M * (K / 16), a16};
+    // B first: in the usual order of calls (quantize A, quantize B, GEMM) its
+    // codes were written last and are the ones still in L2
+    if (!stage_bulk(b, batch, N, K, stride_b, b16, bound_b, err_word, st, sms, &e))
+        small[nsmall++] = StageJob{b, N, K, stride_b, batch * N * (K / 16), b16, bound_b};
     if (e != cudaSuccess) return e;
-    if (!stage_bulk(b, batch, N, K, stride_b, b16, parts_b, nparts_b, err_word, st, sms, &e))
-        small[nsmall++] = StageJob{b, N, K, stride_b, batch * N * (K / 16), b16};
+    if (!stage_bulk(a, batch, M, K, stride_a, a16, bound_a, err_word, st, sms, &e))
+        small[nsmall++] = StageJob{a, M, K, stride_a, batch * M * (K / 16), a16, bound_a};
     if (e != cudaSuccess) return e;
     if (nsmall == 0) return cudaSuccess;
-    if (nsmall == 1) small[1] = StageJob{nullptr, 1, 16, 0, 0, nullptr};
-    const int64_t all = small[0].total + small[1].total;
-    int64_t blocks = (all + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) return cudaSuccess;
-    return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1u,
-                      small[0], small[1]);
+    if (nsmall == 1) small[1] = StageJob{nullptr, 1, 16, 0, 0, nullptr, nullptr};
+    return stage_plain(small[0], small[1], st, sms);
+}
+
+cudaError_t launch_i8_to_f16_one(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
+                                 int64_t stride, uint16_t* dst, unsigned* bound,
+                                 unsigned* err_word, cudaStream_t st, int sms) {
+    cudaError_t e = cudaSuccess;
+    if (stage_bulk(src, batch, rows, K, stride, dst, bound, err_word, st, sms, &e)) return e;
+    return stage_plain(StageJob{src, rows, K, stride, batch * rows * (K / 16), dst, bound},
+                       StageJob{nullptr, 1, 16, 0, 0, nullptr, nullptr}, st, sms);
 }
 
 }  // namespace sq

@@ -104,33 +104,56 @@ __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint3
     return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
-// Codes of one vector stored at dst (4 or 8 bytes, aligned to that size);
-// FAST: s <= kRecipHi.
+// Codes of one 16-byte input vector: pack() returns them as packed bytes
+// (4 for float, 8 for bf16), store() writes them at dst (aligned to their
+// size), and stage() also writes them as exact fp16 values at dst16 and adds
+// their squares to sq.  FAST: s <= kRecipHi.
 template <typename T>
 struct Codes;
 template <>
 struct Codes<float> {
     template <bool FAST>
-    __device__ __forceinline__ static void store(const uint4& v, float s, float y, int8_t* dst) {
+    __device__ __forceinline__ static uint32_t pack(const uint4& v, float s, float y) {
         const float f[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
                             __uint_as_float(v.w)};
-        uint32_t w;
-        if (FAST) {
-            w = pack_low_bytes(code_word(f[0], s, y), code_word(f[1], s, y), code_word(f[2], s, y),
-                               code_word(f[3], s, y));
-        } else {
-            w = pack_low_bytes(static_cast<uint8_t>(encode_i8(f[0], s)),
-                               static_cast<uint8_t>(encode_i8(f[1], s)),
-                               static_cast<uint8_t>(encode_i8(f[2], s)),
-                               static_cast<uint8_t>(encode_i8(f[3], s)));
-        }
+        if (FAST)
+            return pack_low_bytes(code_word(f[0], s, y), code_word(f[1], s, y), code_word(f[2], s, y),
+                                  code_word(f[3], s, y));
+        return pack_low_bytes(static_cast<uint8_t>(encode_i8(f[0], s)),
+                              static_cast<uint8_t>(encode_i8(f[1], s)),
+                              static_cast<uint8_t>(encode_i8(f[2], s)),
+                              static_cast<uint8_t>(encode_i8(f[3], s)));
+    }
+    template <bool FAST>
+    __device__ __forceinline__ static void store(const uint4& v, float s, float y, int8_t* dst) {
+        *reinterpret_cast<uint32_t*>(dst) = pack<FAST>(v, s, y);
+    }
+    template <bool FAST>
+    __device__ __forceinline__ static void stage(const uint4& v, float s, float y, int8_t* dst,
+                                                 uint16_t* dst16, int& sq) {
+        const uint32_t w = pack<FAST>(v, s, y);
         *reinterpret_cast<uint32_t*>(dst) = w;
+        *reinterpret_cast<uint2*>(dst16) = i8x4_to_f16x4(w);
+        sq = __dp4a(static_cast<int>(w), static_cast<int>(w), sq);
     }
 };
 template <>
 struct Codes<uint16_t> {
     template <bool FAST>
     __device__ __forceinline__ static void store(const uint4& v, float s, float y, int8_t* dst) {
+        *reinterpret_cast<uint2*>(dst) = pack<FAST>(v, s, y);
+    }
+    template <bool FAST>
+    __device__ __forceinline__ static void stage(const uint4& v, float s, float y, int8_t* dst,
+                                                 uint16_t* dst16, int& sq) {
+        const uint2 w = pack<FAST>(v, s, y);
+        *reinterpret_cast<uint2*>(dst) = w;
+        *reinterpret_cast<uint4*>(dst16) = i8x8_to_f16x8(w);
+        sq = __dp4a(static_cast<int>(w.x), static_cast<int>(w.x), sq);
+        sq = __dp4a(static_cast<int>(w.y), static_cast<int>(w.y), sq);
+    }
+    template <bool FAST>
+    __device__ __forceinline__ static uint2 pack(const uint4& v, float s, float y) {
         const uint32_t src[4] = {v.x, v.y, v.z, v.w};
         uint32_t c[8];
 #pragma unroll
@@ -145,19 +168,24 @@ struct Codes<uint16_t> {
                 c[2 * i + 1] = static_cast<uint8_t>(encode_i8(hi, s));
             }
         }
-        *reinterpret_cast<uint2*>(dst) =
-            make_uint2(pack_low_bytes(c[0], c[1], c[2], c[3]), pack_low_bytes(c[4], c[5], c[6], c[7]));
+        return make_uint2(pack_low_bytes(c[0], c[1], c[2], c[3]), pack_low_bytes(c[4], c[5], c[6], c[7]));
     }
 };
 
 // A group of TPR threads owns one row, held in registers (VPT 16-byte vectors
 // per thread).  Rows must start 16-byte aligned and cols be a multiple of 16.
-template <typename T, int TPR, int VPT>
+// STAGE: the codes are also written as exact fp16 values at q16 (rows
+// packed) for the INT8 GEMM, and the operand's bound region is marked as
+// holding no bound.
+template <typename T, int TPR, int VPT, bool STAGE>
 __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x, int64_t rows,
                                                         int64_t cols, int64_t ld,
                                                         int8_t* __restrict__ q,
-                                                        float* __restrict__ scales) {
+                                                        float* __restrict__ scales,
+                                                        uint16_t* __restrict__ q16,
+                                                        unsigned* __restrict__ bound) {
     pdl_begin();
+    if (STAGE && blockIdx.x == 0 && threadIdx.x == 0) *bound = 0u;
     constexpr int EPV = Elem<T>::kPerVec;
     constexpr int RPB = 256 / TPR;
     __shared__ float red[8];
@@ -196,17 +224,18 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
         const float y = __frcp_rn(s);
         if (live) {
             if (lg == 0) scales[row] = s;
-            if (fast) {
+            int sq = 0;   // unused: this path records no bound
 #pragma unroll
-                for (int i = 0; i < VPT; ++i) {
-                    const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
-                    if (vi < nvec) Codes<T>::template store<true>(raw[i], s, y, q + row * cols + vi * EPV);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < VPT; ++i) {
-                    const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
-                    if (vi < nvec) Codes<T>::template store<false>(raw[i], s, y, q + row * cols + vi * EPV);
+            for (int i = 0; i < VPT; ++i) {
+                const int64_t vi = lg + static_cast<int64_t>(i) * TPR;
+                if (vi >= nvec) continue;
+                const int64_t o = row * cols + vi * EPV;
+                if (STAGE) {
+                    if (fast) Codes<T>::template stage<true>(raw[i], s, y, q + o, q16 + o, sq);
+                    else Codes<T>::template stage<false>(raw[i], s, y, q + o, q16 + o, sq);
+                } else {
+                    if (fast) Codes<T>::template store<true>(raw[i], s, y, q + o);
+                    else Codes<T>::template store<false>(raw[i], s, y, q + o);
                 }
             }
         }
@@ -303,23 +332,119 @@ __global__ void __launch_bounds__(256) quant_row_i8_pf(const T* __restrict__ x, 
     cp_async_wait<0>();
 }
 
-template <typename T, int TPR, int VPT>
+// quant_row_i8_pf that also stages the codes for the INT8 GEMM: every code
+// is written a second time as an exact fp16 value (q16, rows packed), and
+// each CTA records in the operand's bound region the largest row norm (sum
+// of squared codes) over its rows; block 0 writes the region's header.
+template <typename T>
+__global__ void __launch_bounds__(256) quant_row_i8_stage_pf(const T* __restrict__ x, int64_t rows,
+                                                             int64_t cols, int64_t ld,
+                                                             int8_t* __restrict__ q,
+                                                             float* __restrict__ scales,
+                                                             uint16_t* __restrict__ q16,
+                                                             unsigned* __restrict__ bound) {
+    pdl_begin();
+    constexpr int EPV = Elem<T>::kPerVec;
+    __shared__ __align__(16) uint8_t buf[2][kPfRowBytes];
+    __shared__ float red[8];
+    __shared__ int red_sq[8];
+    const int nvec = static_cast<int>(cols / EPV);          // 16-byte vectors per row
+    const int64_t G = gridDim.x;
+    const int t = threadIdx.x;
+    unsigned row_max = 0u;                                   // thread 0: largest row norm
+    auto fetch = [&](int64_t row, int b) {
+        const T* src = x + row * ld;
+        for (int vi = t; vi < nvec; vi += 256) cp_async16(&buf[b][vi * 16], src + vi * EPV);
+        cp_async_commit();
+    };
+    int64_t row = blockIdx.x;
+    if (row < rows) fetch(row, 0);
+    for (int i = 0; row < rows; ++i, row += G) {
+        const int b = i & 1;
+        if (row + G < rows) fetch(row + G, b ^ 1);
+        else cp_async_commit();                 // keep one group per iteration
+        cp_async_wait<1>();                     // this row's copies are done
+        __syncthreads();
+        AbsMax<T> am;
+        for (int vi = t; vi < nvec; vi += 256) am.add(*reinterpret_cast<const uint4*>(&buf[b][vi * 16]));
+        float m = am.value();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((t & 31) == 0) red[t >> 5] = m;
+        __syncthreads();
+        m = red[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+        const float s = row_scale(m);
+        const bool fast = s <= kRecipHi;
+        const float y = __frcp_rn(s);
+        if (t == 0) scales[row] = s;
+        int8_t* qr = q + row * cols;
+        uint16_t* q16r = q16 + row * cols;
+        int sq = 0;                             // <= 127^2 * cols < 2^31 (cols <= 8192)
+        if (fast) {
+            for (int vi = t; vi < nvec; vi += 256)
+                Codes<T>::template stage<true>(*reinterpret_cast<const uint4*>(&buf[b][vi * 16]), s, y,
+                                               qr + vi * EPV, q16r + vi * EPV, sq);
+        } else {
+            for (int vi = t; vi < nvec; vi += 256)
+                Codes<T>::template stage<false>(*reinterpret_cast<const uint4*>(&buf[b][vi * 16]), s, y,
+                                                qr + vi * EPV, q16r + vi * EPV, sq);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if ((t & 31) == 0) red_sq[t >> 5] = sq;
+        __syncthreads();                        // buffer b, red[] and red_sq[] are complete
+        if (t == 0) {
+            // red_sq is next written after two more barriers of the next row
+            int rs = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) rs += red_sq[w];
+            row_max = max(row_max, static_cast<unsigned>(rs));
+        }
+    }
+    cp_async_wait<0>();
+    if (t == 0) {
+        bound[1 + blockIdx.x] = row_max;
+        if (blockIdx.x == 0) bound[0] = static_cast<unsigned>(gridDim.x) | kBoundRowNorms;
+    }
+}
+
+template <typename T, int TPR, int VPT, bool STAGE>
 static cudaError_t launch_row_vec(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
-                                  float* scales, cudaStream_t st, int sms) {
+                                  float* scales, uint16_t* q16, unsigned* bound, cudaStream_t st,
+                                  int sms) {
     constexpr int RPB = 256 / TPR;
     int64_t blocks = (rows + RPB - 1) / RPB;
     const int64_t cap = static_cast<int64_t>(sms) * 64;
     if (blocks > cap) blocks = cap;
-    return launch_pdl(quant_row_i8_vec<T, TPR, VPT>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                      1u, x, rows, cols, ld, q, scales);
+    return launch_pdl(quant_row_i8_vec<T, TPR, VPT, STAGE>, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                      0, st, 1u, x, rows, cols, ld, q, scales, q16, bound);
+}
+
+// The register-resident shapes by row length (nvec 16-byte vectors per row);
+// false if the row is too long for them.
+template <typename T, bool STAGE>
+static bool launch_row_vec_any(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
+                               float* scales, uint16_t* q16, unsigned* bound, cudaStream_t st,
+                               int sms, cudaError_t* e) {
+    const int64_t nvec = cols / Elem<T>::kPerVec;
+    if (nvec <= 16) *e = launch_row_vec<T, 16, 1, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    else if (nvec <= 32) *e = launch_row_vec<T, 32, 1, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    else if (nvec <= 64) *e = launch_row_vec<T, 32, 2, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    else if (nvec <= 128) *e = launch_row_vec<T, 32, 4, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    else if (nvec <= 256) *e = launch_row_vec<T, 32, 8, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    else if (nvec <= 512) *e = launch_row_vec<T, 256, 2, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    else if (nvec <= 1024) *e = launch_row_vec<T, 256, 4, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    else if (nvec <= 2048) *e = launch_row_vec<T, 256, 8, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    else return false;
+    return true;
 }
 
 template <typename T>
 static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
                               float* scales, bool vec_ok, unsigned* err_word, cudaStream_t st,
                               int sms) {
-    constexpr int EPV = Elem<T>::kPerVec;
-    const int64_t nvec = cols / EPV;
     (void)err_word;
     const int64_t row_bytes = cols * static_cast<int64_t>(sizeof(T));
     if (vec_ok && row_bytes >= 2048 && row_bytes <= kPfRowBytes && rows >= 2 * sms) {
@@ -330,14 +455,9 @@ static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld
                           rows, cols, ld, q, scales);
     }
     if (vec_ok) {
-        if (nvec <= 16) return launch_row_vec<T, 16, 1>(x, rows, cols, ld, q, scales, st, sms);
-        if (nvec <= 32) return launch_row_vec<T, 32, 1>(x, rows, cols, ld, q, scales, st, sms);
-        if (nvec <= 64) return launch_row_vec<T, 32, 2>(x, rows, cols, ld, q, scales, st, sms);
-        if (nvec <= 128) return launch_row_vec<T, 32, 4>(x, rows, cols, ld, q, scales, st, sms);
-        if (nvec <= 256) return launch_row_vec<T, 32, 8>(x, rows, cols, ld, q, scales, st, sms);
-        if (nvec <= 512) return launch_row_vec<T, 256, 2>(x, rows, cols, ld, q, scales, st, sms);
-        if (nvec <= 1024) return launch_row_vec<T, 256, 4>(x, rows, cols, ld, q, scales, st, sms);
-        if (nvec <= 2048) return launch_row_vec<T, 256, 8>(x, rows, cols, ld, q, scales, st, sms);
+        cudaError_t e = cudaSuccess;
+        if (launch_row_vec_any<T, false>(x, rows, cols, ld, q, scales, nullptr, nullptr, st, sms, &e))
+            return e;
     }
     int64_t blocks = rows;
     const int64_t cap = static_cast<int64_t>(sms) * 64;
@@ -354,6 +474,41 @@ cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, i
                                  err_word, st, sms);
     return launch_row<uint16_t>(static_cast<const uint16_t*>(x), rows, cols, ld, q, scales, vec_ok,
                                 err_word, st, sms);
+}
+
+cudaError_t launch_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t rows,
+                                              int64_t cols, int64_t ld, int8_t* q,
+                                              float* scales, bool vec_ok, uint16_t* q16,
+                                              unsigned* bound, unsigned* err_word,
+                                              cudaStream_t st, int sms) {
+    const int64_t esz = dtype == 0 ? 4 : 2;
+    const int64_t row_bytes = cols * esz;
+    if (vec_ok && row_bytes >= 2048 && row_bytes <= kPfRowBytes && rows >= 2 * sms) {
+        int64_t blocks = rows;
+        int64_t cap = static_cast<int64_t>(sms) * 6;
+        if (cap > kBoundSlots - 1) cap = kBoundSlots - 1;
+        if (blocks > cap) blocks = cap;
+        if (dtype == 0)
+            return launch_pdl(quant_row_i8_stage_pf<float>, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                              0, st, 1u, static_cast<const float*>(x), rows, cols, ld, q, scales, q16,
+                              bound);
+        return launch_pdl(quant_row_i8_stage_pf<uint16_t>, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                          0, st, 1u, static_cast<const uint16_t*>(x), rows, cols, ld, q, scales, q16,
+                          bound);
+    }
+    cudaError_t e = cudaSuccess;
+    if (vec_ok) {
+        const bool done = dtype == 0
+            ? launch_row_vec_any<float, true>(static_cast<const float*>(x), rows, cols, ld, q, scales,
+                                              q16, bound, st, sms, &e)
+            : launch_row_vec_any<uint16_t, true>(static_cast<const uint16_t*>(x), rows, cols, ld, q,
+                                                 scales, q16, bound, st, sms, &e);
+        if (done) return e;
+    }
+    // other shapes: the plain quantize, then the staging of its codes
+    e = launch_quantize_rowwise_i8(x, dtype, rows, cols, ld, q, scales, vec_ok, err_word, st, sms);
+    if (e != cudaSuccess) return e;
+    return launch_i8_to_f16_one(q, 1, rows, cols, rows * cols, q16, bound, err_word, st, sms);
 }
 
 // ================================================================== INT8 row groups

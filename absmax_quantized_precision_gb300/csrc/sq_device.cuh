@@ -130,6 +130,11 @@ __device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
     return v;
 }
 
+// Named CTA barrier `id` (1..15) among `nthreads` threads (whole warps).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ------------------------------------------------------------------ launches
 // Every kernel of libsq is launched with programmatic stream serialization
 // (sq_host.h, launch_pdl) and calls pdl_begin() before its first global
@@ -480,6 +485,26 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------------------ int8 -> fp16
+// Four int8 codes -> four exact fp16 values.  With u = c + 128 in [1, 255]
+// (the code's byte with its top bit flipped), the fp16 bit pattern 0x6400 | u
+// is the value 1024 + u exactly (the spacing of fp16 in [1024, 2048) is 1),
+// and subtracting 1152 leaves c exactly.
+__device__ __forceinline__ uint2 i8x4_to_f16x4(uint32_t w) {
+    const uint32_t a = w ^ 0x80808080u;
+    uint32_t o[2] = {__byte_perm(a, 0x64646464u, 0x4140), __byte_perm(a, 0x64646464u, 0x4342)};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(o[k]) : "r"(0x64806480u));
+    return make_uint2(o[0], o[1]);
+}
+
+// Eight int8 codes -> eight exact fp16 values.
+__device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 w) {
+    const uint2 lo = i8x4_to_f16x4(w.x);
+    const uint2 hi = i8x4_to_f16x4(w.y);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // ------------------------------------------------------------------ misc

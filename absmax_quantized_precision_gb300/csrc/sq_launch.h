@@ -7,6 +7,17 @@
 
 namespace sq {
 
+// Bound region of an INT8 GEMM workspace, one per operand: a header word,
+// then one slot per CTA of the launch that staged the operand.  The header
+// holds the number of slots written (0: no bound recorded) and, in
+// kBoundRowNorms, whether each slot is a largest row norm (the sum of a
+// row's squared codes) or a largest sum of squared codes over a staged chunk
+// of 1024 codes.  Each staging launch writes its header and its slots, so the
+// region needs no initialisation.
+constexpr int kBoundSlots = 1024;                 // words per operand region
+constexpr unsigned kBoundCountMask = 0xFFFFu;
+constexpr unsigned kBoundRowNorms = 0x80000000u;
+
 // err_word == nullptr keeps to the kernels without waits.
 cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, int64_t cols,
                                        int64_t ld, int8_t* q, float* scales, bool vec_ok,
@@ -27,21 +38,33 @@ cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale
 
 // Staging of the INT8 codes of both GEMM operands as exact fp16 values:
 // a16[b][r][k] = a[b*stride_a + r*K + k] (M rows per batch), likewise b16.
-// An operand that is contiguous and large takes the bulk pipeline, whose
-// *nparts CTAs each write to parts[cta] the largest sum of squared codes over
-// any of their 1024-code chunks (the ragged tail counts as one chunk); the
-// other operands share one launch of a plain kernel and report *nparts = 0.
-// parts_a and parts_b hold at least 256 words each.
-// The *nparts that launch_i8_to_f16_pair reports for one operand of these
-// sizes (0: it takes the plain kernel and records no bounds).  Every launch
-// that passes an error word takes the bulk pipeline when this is non-zero.
-int i8_staging_parts(int64_t batch, int64_t rows, int64_t K, int64_t stride, int sms);
-
+// An operand that is contiguous and large takes the bulk pipeline, whose CTAs
+// record in its bound region (kBoundSlots words) the largest sum of squared
+// codes over any of their 1024-code chunks (the ragged tail counts as one
+// chunk); the other operands share one launch of a plain kernel, which marks
+// their regions as holding no bound.
 cudaError_t launch_i8_to_f16_pair(const int8_t* a, int64_t M, const int8_t* b, int64_t N,
                                   int64_t batch, int64_t K, int64_t stride_a, int64_t stride_b,
-                                  uint16_t* a16, uint16_t* b16, unsigned* parts_a, int* nparts_a,
-                                  unsigned* parts_b, int* nparts_b, unsigned* err_word,
-                                  cudaStream_t st, int sms);
+                                  uint16_t* a16, uint16_t* b16, unsigned* bound_a,
+                                  unsigned* bound_b, unsigned* err_word, cudaStream_t st,
+                                  int sms);
+
+// The same for one operand.
+cudaError_t launch_i8_to_f16_one(const int8_t* src, int64_t batch, int64_t rows, int64_t K,
+                                 int64_t stride, uint16_t* dst, unsigned* bound,
+                                 unsigned* err_word, cudaStream_t st, int sms);
+
+// Per-row INT8 quantization that also stages the codes for the GEMM: besides
+// q and scales, q16[r*cols + k] = the code as an exact fp16 value, and the
+// operand's bound region records the largest row norm (the sum of a row's
+// squared codes) per CTA.  Rows packed (ld == cols) in q16.  Shapes that the
+// fused kernel does not take go through the plain quantize and
+// launch_i8_to_f16_one.
+cudaError_t launch_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t rows,
+                                              int64_t cols, int64_t ld, int8_t* q,
+                                              float* scales, bool vec_ok, uint16_t* q16,
+                                              unsigned* bound, unsigned* err_word,
+                                              cudaStream_t st, int sms);
 
 // 0 on success, a cudaError_t otherwise; CUDA_ERROR_* from tensor-map encoding
 // is reported as cudaErrorInvalidValue.
@@ -62,13 +85,12 @@ cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, int spli
                                float* partial, uint16_t* gb, cudaStream_t st);
 
 // Scales of row i of A in batch b: sA[b*ceil(M/ga) + i/ga] (ga = 1: per row).
-// bound_a / bound_b: the staging launches' parts (nparts 0: not available);
-// when they prove every partial sum exact in fp32, K runs as one chunk.
+// bound_a / bound_b: the operands' bound regions (nullable: no bound); when
+// they prove every partial sum exact in fp32, K runs as one chunk.
 cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float* sA,
                            const float* sB, int ga, int gb, int batch, int M, int N, int K,
                            int64_t strideC, float* C, int32_t* acc_out, const unsigned* bound_a,
-                           int nparts_a, const unsigned* bound_b, int nparts_b,
-                           unsigned* err_word, cudaStream_t st, int sms);
+                           const unsigned* bound_b, unsigned* err_word, cudaStream_t st, int sms);
 
 // One CTA waits on a barrier phase that never completes, for limit_ns.
 cudaError_t launch_selftest_wait(unsigned* err_word, unsigned long long limit_ns, cudaStream_t st);

@@ -4,8 +4,9 @@ One step = the whole path over one batch of the large workload (M=16384,
 N=8192, K=8192, A and B bf16 Student-t(3), seeded):
   FP8:  quantize A and B to E4M3 with the amax fused in (delayed scales), then
         the scaled FP8 GEMM C = A B^T * sa * sb (bf16 out);
-  INT8: per-row quantize A and B, then the exact INT8 GEMM with the per-row x
-        per-row fp32 dequant epilogue.
+  INT8: per-row quantize A and B (each launch also stages its codes for the
+        GEMM), then the exact INT8 GEMM with the per-row x per-row fp32
+        dequant epilogue.
 Metric: quant+GEMM TFLOP/s = (2*M*N*K for each of the two GEMMs) / step time.
 
 The same JSON line also carries the pages' four smaller workloads under
@@ -411,7 +412,8 @@ def run_sq(args, rank, world, local_rank):
     wsi = torch.empty(sq.gemm_i8_workspace_bytes(1, M, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    launches_per_step = 8   # the INT8 GEMM call stages A and B (2 launches) before its GEMM
+    launches_per_step = 6
+    shape_i8 = (0, M, N, K)
 
     # One stream by default.  --overlap runs the INT8 quantization (memory-
     # bound) on a second stream during the FP8 GEMM (tensor-bound); the INT8
@@ -422,8 +424,7 @@ def run_sq(args, rank, world, local_rank):
     g_done = torch.cuda.Event()
 
     def step(events=None, bufs=None):
-        """One step.  With `events`, the INT8 GEMM call runs as its two phases
-        (staging, then the GEMM kernel) with an event between them."""
+        """One step of the path; with `events`, an event after every call."""
         xa, xb, c8, ci = bufs if bufs is not None else (A, B, C8, Ci)
 
         def mark(i, st):
@@ -440,18 +441,13 @@ def run_sq(args, rank, world, local_rank):
         g_done.record(stream)
         s_i8.wait_event(q_done)
         mark(7, s_i8)
-        sq.sq_quantize_rowwise_i8(xa, q=qa, scales=sA, stream=s_i8)
+        sq.sq_quantize_rowwise_i8_staged(xa, 0, shape_i8, wsi, q=qa, scales=sA, stream=s_i8)
         mark(4, s_i8)
-        sq.sq_quantize_rowwise_i8(xb, q=qb, scales=sB, stream=s_i8)
+        sq.sq_quantize_rowwise_i8_staged(xb, 1, shape_i8, wsi, q=qb, scales=sB, stream=s_i8)
         mark(5, s_i8)
         s_i8.wait_event(g_done)
         mark(8, s_i8)
-        if events is None:
-            sq.sq_gemm_i8_rowscaled(qa, sA, qb, sB, wsi, C=ci, stream=s_i8)
-        else:
-            sq.sq_gemm_i8_stage(qa, qb, wsi, stream=s_i8)
-            mark(9, s_i8)
-            sq.sq_gemm_i8_rowscaled_staged(sA, sB, (0, M, N, K), wsi, C=ci, stream=s_i8)
+        sq.sq_gemm_i8_rowscaled_staged(sA, sB, shape_i8, wsi, C=ci, stream=s_i8)
         mark(6, s_i8)
         stream.wait_stream(s_i8)
 
@@ -484,14 +480,13 @@ def run_sq(args, rank, world, local_rank):
         raise RuntimeError("device error in the timed region")
 
     # The per-call breakdown: a second pass of the same steps with events
-    # around every call (and between the INT8 call's staging and its GEMM).
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
+    # around every call.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
     for s in range(args.steps):
         step(ev[s])
     torch.cuda.synchronize(dev)
     spans = {"quant_fp8_A": (0, 1), "quant_fp8_B": (1, 2), "gemm_fp8_nt": (2, 3),
-             "quant_i8_A": (7, 4), "quant_i8_B": (4, 5), "gemm_i8": (8, 6),
-             "stage_i8": (8, 9), "gemm_i8_kernel": (9, 6)}
+             "quant_i8_A": (7, 4), "quant_i8_B": (4, 5), "gemm_i8_kernel": (8, 6)}
     per_kernel = {n: statistics.mean(ev[s][a].elapsed_time(ev[s][b]) for s in range(args.steps))
                   for n, (a, b) in spans.items()}
     if sq.sq_get_last_device_error() != sq.SQ_OK:
@@ -501,17 +496,17 @@ def run_sq(args, rank, world, local_rank):
     # step's first j + 1 calls, with an event at the step's start and one after
     # call j and nothing between, so the calls keep their launch overlap; call
     # j's cost is the mean prefix time through j minus the one through j - 1.
-    # The INT8 call runs as its two phases, staging and the GEMM kernel.
     seq = [("quant_fp8_A", lambda: sq.sq_quantize_fp8(A, tsa, sq.SQ_FMT_E4M3, ws, x8=a8,
                                                         amax=amax_a, stream=stream)),
            ("quant_fp8_B", lambda: sq.sq_quantize_fp8(B, tsb, sq.SQ_FMT_E4M3, ws, x8=b8,
                                                         amax=amax_b, stream=stream)),
            ("gemm_fp8_nt", lambda: sq.sq_gemm_fp8_scaled(a8, b8, tsa, tsb, sq.SQ_FMT_E4M3, sq.SQ_NT,
                                                          C=C8, stream=stream)),
-           ("quant_i8_A", lambda: sq.sq_quantize_rowwise_i8(A, q=qa, scales=sA, stream=stream)),
-           ("quant_i8_B", lambda: sq.sq_quantize_rowwise_i8(B, q=qb, scales=sB, stream=stream)),
-           ("stage_i8", lambda: sq.sq_gemm_i8_stage(qa, qb, wsi, stream=stream)),
-           ("gemm_i8_kernel", lambda: sq.sq_gemm_i8_rowscaled_staged(sA, sB, (0, M, N, K), wsi, C=Ci,
+           ("quant_i8_A", lambda: sq.sq_quantize_rowwise_i8_staged(A, 0, shape_i8, wsi, q=qa,
+                                                                    scales=sA, stream=stream)),
+           ("quant_i8_B", lambda: sq.sq_quantize_rowwise_i8_staged(B, 1, shape_i8, wsi, q=qb,
+                                                                    scales=sB, stream=stream)),
+           ("gemm_i8_kernel", lambda: sq.sq_gemm_i8_rowscaled_staged(sA, sB, shape_i8, wsi, C=Ci,
                                                                      stream=stream))]
     in_step_ms = {}
     if not args.overlap:
@@ -557,9 +552,11 @@ def run_sq(args, rank, world, local_rank):
         "quant_fp8_B": steady(lambda r: sq.sq_quantize_fp8(B if (r % 2 == 0 or b_alt is None) else b_alt,
                                                            tsb, sq.SQ_FMT_E4M3, ws, x8=b8,
                                                            amax=amax_b, stream=stream)),
-        "quant_i8_A": steady(lambda r: sq.sq_quantize_rowwise_i8(A, q=qa, scales=sA, stream=stream)),
-        "quant_i8_B": steady(lambda r: sq.sq_quantize_rowwise_i8(
-            B if (r % 2 == 0 or b_alt is None) else b_alt, q=qb, scales=sB, stream=stream)),
+        "quant_i8_A": steady(lambda r: sq.sq_quantize_rowwise_i8_staged(A, 0, shape_i8, wsi, q=qa,
+                                                                        scales=sA, stream=stream)),
+        "quant_i8_B": steady(lambda r: sq.sq_quantize_rowwise_i8_staged(
+            B if (r % 2 == 0 or b_alt is None) else b_alt, 1, shape_i8, wsi, q=qb, scales=sB,
+            stream=stream)),
     }
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error in the steady-state pass")
@@ -652,11 +649,10 @@ def run_sq(args, rank, world, local_rank):
 
     pk = peaks()
     clocks = clk.summary()
+    # INT8 quantize: bf16 in, int8 codes and their exact fp16 copy out, scales
     quant_bytes = {"quant_fp8_A": M * K * 3 + 4, "quant_fp8_B": N * K * 3 + 4,
-                   "quant_i8_A": M * K * 3 + M * 4, "quant_i8_B": N * K * 3 + N * 4,
-                   "stage_i8": (M + N) * K * 3}
-    gemm_flops = {"gemm_fp8_nt": 2.0 * M * N * K, "gemm_i8": 2.0 * M * N * K,
-                  "gemm_i8_kernel": 2.0 * M * N * K}
+                   "quant_i8_A": M * K * 5 + M * 4, "quant_i8_B": N * K * 5 + N * 4}
+    gemm_flops = {"gemm_fp8_nt": 2.0 * M * N * K, "gemm_i8_kernel": 2.0 * M * N * K}
 
     def rate(n, ms):
         d = {"ms": ms}
@@ -691,9 +687,8 @@ def run_sq(args, rank, world, local_rank):
         "algorithmic": "2*M*N*K flops per launch",
         "algorithmic_bytes": algo_bytes(dom),
         "traffic_vs_algorithmic": (traffic / algo_bytes(dom)) if traffic else None,
-        "timed": ("the INT8 GEMM kernel alone (sq_gemm_i8_rowscaled_staged; the call's fp16 "
-                  "staging of A and B is timed apart as stage_i8)" if not fp8 else
-                  "one sq_gemm_fp8_scaled launch"),
+        "timed": ("one sq_gemm_i8_rowscaled_staged launch (its operands were staged by the "
+                  "quantize launches)" if not fp8 else "one sq_gemm_fp8_scaled launch"),
         "vs_nominal": {"nominal_dense_tflops": nominal, "frac": achieved / nominal,
                        "frac_at_sampled_clock": (achieved / (nominal * clocks["sm_mhz"] / NOMINAL_SM_MHZ)
                                                  if clocks.get("sm_mhz") else None),
@@ -741,8 +736,9 @@ def run_sq(args, rank, world, local_rank):
         "kernels": kernels,
         "kernels_note": ("mean CUDA-event span of each call on the stream it ran on, from a second "
                          "pass of the same steps with events around every call (each call then "
-                         "waits for the one before and pays its own launch); gemm_i8 is the whole "
-                         "INT8 call = stage_i8 + gemm_i8_kernel"
+                         "waits for the one before and pays its own launch); the INT8 quantize "
+                         "calls (sq_quantize_rowwise_i8_staged) also stage their codes for "
+                         "sq_gemm_i8_rowscaled_staged"
                          + ("; with two streams the INT8 quantize spans overlap the FP8 GEMM and "
                             "share the GPU with it" if args.overlap else "")),
         "kernels_in_step": kernels_in_step,
@@ -798,15 +794,15 @@ def config_ops(name, dev, sq, synth, oracle, bf16_dev, prev_scale):
         C = torch.empty((nb, Mi, Ni) if nb > 1 else (Mi, Ni), device=dev)
         flops = 2.0 * nb * Mi * Ni * Kk
         shape = (nb if A.dim() == 3 else 0, Mi, Ni, Kk)
-        ops = [("quant_i8_A", "bytes", A.numel() * 5 + sa.numel() * 4,
-                lambda: sq.sq_quantize_rowwise_i8(A, q=qa, scales=sa)),
-               ("quant_i8_B", "bytes", B.numel() * 5 + sb.numel() * 4,
-                lambda: sq.sq_quantize_rowwise_i8(B, q=qb, scales=sb)),
-               ("stage_i8", "bytes", (qa.numel() + qb.numel()) * 3,
-                lambda: sq.sq_gemm_i8_stage(qa, qb, ws)),
+        # f32 in; int8 codes, their exact fp16 copy and the scales out
+        ops = [("quant_i8_A", "bytes", A.numel() * 7 + sa.numel() * 4,
+                lambda: sq.sq_quantize_rowwise_i8_staged(A, 0, shape, ws, q=qa, scales=sa)),
+               ("quant_i8_B", "bytes", B.numel() * 7 + sb.numel() * 4,
+                lambda: sq.sq_quantize_rowwise_i8_staged(B, 1, shape, ws, q=qb, scales=sb)),
                ("gemm_i8_kernel", "flops", flops,
                 lambda: sq.sq_gemm_i8_rowscaled_staged(sa.reshape(-1), sb.reshape(-1), shape, ws,
                                                        C=C))]
+        # the one-call form on the same codes (its own staging + the GEMM), for comparison
         call = ("gemm_i8", "flops", flops,
                 lambda: sq.sq_gemm_i8_rowscaled(qa, sa.reshape(-1), qb, sb.reshape(-1), ws, C=C))
 
@@ -934,7 +930,7 @@ def measure_config(name, args, with_cpu=True, compact=False):
         oracle.set_num_threads(cores)
         cpu["sample"] = "the whole workload"
 
-    iters = max(args.steps if args.steps != 300 else 50, 10)
+    iters = 100
     for _ in range(max(args.warmup, 3)):
         for _, _, _, fn in ops + alt_calls:
             fn()
@@ -949,22 +945,29 @@ def measure_config(name, args, with_cpu=True, compact=False):
         torch.cuda.synchronize(dev)
         return g
 
-    def time_graph(g):
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
+    def time_graphs(graphs):
+        """Median replay time of each graph; every round replays each graph
+        once, after an L2-evicting write, so that all see the same drift."""
+        ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in graphs]
+              for _ in range(iters)]
         for it in range(iters):
-            flush.fill_(it & 0xFF)           # evict the inputs from L2 before each pass
-            ev[it][0].record(stream)
-            g.replay()
-            ev[it][1].record(stream)
+            for j, g in enumerate(graphs):
+                flush.fill_((it + j) & 0xFF)   # evict the inputs from L2 before each pass
+                ev[it][j][0].record(stream)
+                g.replay()
+                ev[it][j][1].record(stream)
         torch.cuda.synchronize(dev)
-        return statistics.median(ev[i][0].elapsed_time(ev[i][1]) for i in range(iters))
+        return [statistics.median(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(iters))
+                for j in range(len(graphs))]
 
     with Clocks(dev) as clk:
-        # prefix_ms[j]: the graph of the step's first j + 1 calls
-        prefix_ms = [time_graph(capture([fn for _, _, _, fn in ops[:j + 1]]))
-                     for j in range(len(ops))]
+        # the graphs of the step's first j + 1 calls, then of each call alone
+        graphs = [capture([fn for _, _, _, fn in ops[:j + 1]]) for j in range(len(ops))]
+        graphs += [capture([fn]) for _, _, _, fn in ops + alt_calls]
+        times = time_graphs(graphs)
+        prefix_ms = times[:len(ops)]
         step_ms = prefix_ms[-1]
-        call_ms = [time_graph(capture([fn])) for _, _, _, fn in ops + alt_calls]
+        call_ms = times[len(ops):]
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error in the graph passes")
 

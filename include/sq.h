@@ -150,7 +150,7 @@ sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, u
 
 /*
  * Bytes of workspace that sq_gemm_i8_rowscaled needs for these sizes: the
- * INT8 codes staged as exact 16-bit values for the tensor cores, plus 2 KB in
+ * INT8 codes staged as exact 16-bit values for the tensor cores, plus 8 KB in
  * which the staging records bounds on the codes' sums of squares (used to
  * skip the exactness drains when they cannot be needed).
  */
@@ -196,20 +196,38 @@ sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B
  * bounds on their sums of squares.
  *
  * sq_gemm_i8_rowscaled_staged runs the GEMM and the dequantization epilogue
- * on a workspace that sq_gemm_i8_stage filled earlier in stream order with
- * the same batch, M, N, K, strideA and strideB (the strides of the int8
- * operands, which decide how the staging recorded its bounds).  The scales
- * and outputs are as in sq_gemm_i8_rowscaled.  A workspace staged once may
- * serve several GEMMs with different scales.  The workspace is only read.
+ * on a workspace staged earlier in stream order for the same batch, M, N and
+ * K, by sq_gemm_i8_stage or by sq_quantize_rowwise_i8_staged (both
+ * operands).  The scales and outputs are as in sq_gemm_i8_rowscaled.  A
+ * workspace staged once may serve several GEMMs with different scales; the
+ * call only reads it.
  */
 sq_status sq_gemm_i8_stage(const int8_t* A, const int8_t* B, int64_t batch, int64_t M, int64_t N,
                            int64_t K, int64_t strideA, int64_t strideB, void* workspace,
                            size_t workspace_bytes, sq_stream stream);
 sq_status sq_gemm_i8_rowscaled_staged(const float* sA, const float* sB, int64_t batch, int64_t M,
-                                      int64_t N, int64_t K, int64_t strideA, int64_t strideB,
-                                      int64_t strideC, float* C, int32_t* acc_out,
-                                      const void* workspace, size_t workspace_bytes,
-                                      sq_stream stream);
+                                      int64_t N, int64_t K, int64_t strideC, float* C,
+                                      int32_t* acc_out, const void* workspace,
+                                      size_t workspace_bytes, sq_stream stream);
+
+/*
+ * Per-row INT8 quantization that also stages the codes for the INT8 GEMM
+ * [P2 formula and rounding; P1 per_row / per_head]: the results q and scales
+ * of sq_quantize_rowwise_i8 (same arguments, same bits), and besides them
+ * the operand's share of an INT8 GEMM workspace, as sq_gemm_i8_stage would
+ * write it.  Quantizing A and B this way and then calling
+ * sq_gemm_i8_rowscaled_staged gives the bits of sq_gemm_i8_rowscaled on q,
+ * with one pass less over the codes.
+ *   operand    0: x is A, rows = batch*M; 1: x is B, rows = batch*N.
+ *   cols       must equal K.
+ *   batch, M, N, K, workspace, workspace_bytes  as in sq_gemm_i8_rowscaled.
+ * Calls that share a workspace must not overlap on the GPU.
+ */
+sq_status sq_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t rows, int64_t cols,
+                                        int64_t ld, int8_t* q, float* scales, int operand,
+                                        int64_t batch, int64_t M, int64_t N, int64_t K,
+                                        void* workspace, size_t workspace_bytes,
+                                        sq_stream stream);
 
 /*
  * Row-group symmetric INT8 quantization  [P1 sc_matmul group_a / group_b

@@ -43,8 +43,8 @@ def test_status_strings_and_sizes(lib):
     for s in range(6):
         assert sq.status_string(s).startswith("SQ_")
     assert sq.workspace_bytes() >= 8
-    # fp16 copies of A and B, then 2 x 256 words of staging bounds
-    assert sq.gemm_i8_workspace_bytes(1, 128, 512, 1024) == 128 * 1024 * 2 + 512 * 1024 * 2 + 2048
+    # fp16 copies of A and B, then two bound regions of 1024 words
+    assert sq.gemm_i8_workspace_bytes(1, 128, 512, 1024) == 128 * 1024 * 2 + 512 * 1024 * 2 + 8192
     assert sq.gemm_i8_workspace_bytes(0, 1, 1, 1) == 0
 
 
@@ -83,12 +83,21 @@ def test_invalid_arguments_are_rejected_without_a_device(lib):
     assert lib.sq_gemm_i8_stage(null, p, 1, 4, 4, 16, 64, 64, p, 1 << 20,
                                 null) == sq.SQ_ERR_INVALID_ARG
     assert lib.sq_gemm_i8_stage(p, p, 1, 4, 4, 16, 64, 64, p, 8, null) == sq.SQ_ERR_INVALID_ARG
-    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 64, 64, 16, null, null, p, 1 << 20,
+    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 16, null, null, p, 1 << 20,
                                            null) == sq.SQ_ERR_INVALID_ARG
-    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 32, 64, 16, p, null, p, 1 << 20,
+    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 8, p, null, p, 1 << 20,
                                            null) == sq.SQ_ERR_INVALID_ARG
-    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 64, 64, 16, p1, null, p, 1 << 20,
+    assert lib.sq_gemm_i8_rowscaled_staged(p, p, 1, 4, 4, 16, 16, p1, null, p, 1 << 20,
                                            null) == sq.SQ_ERR_ALIGNMENT
+    # the fused quantize-and-stage: operand, rows and cols must match the GEMM's shape
+    assert lib.sq_quantize_rowwise_i8_staged(p, 0, 4, 16, 16, p, p, 2, 1, 4, 4, 16, p, 1 << 20,
+                                             null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_rowwise_i8_staged(p, 0, 5, 16, 16, p, p, 0, 1, 4, 4, 16, p, 1 << 20,
+                                             null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_rowwise_i8_staged(p, 0, 4, 32, 32, p, p, 1, 1, 4, 4, 16, p, 1 << 20,
+                                             null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_rowwise_i8_staged(p, 0, 4, 16, 16, p, p, 1, 1, 4, 4, 16, p, 8,
+                                             null) == sq.SQ_ERR_INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -147,6 +147,66 @@ def test_i8_gemm_stage_then_staged_equals_one_call(name, nb, sa_shape, sb_shape)
     assert torch.equal(C1, C) and torch.equal(acc1, acc)
 
 
+# ------------------------------------------------------------------ INT8 quantized and staged in one pass
+def _bf16_signs(seed, shape):
+    """bf16 bits of +-1.0 with seeded signs: every code quantizes to +-127."""
+    sgn = np.random.default_rng(seed).integers(0, 2, shape)
+    return np.where(sgn == 1, 0xBF80, 0x3F80).astype(np.uint16)
+
+
+FUSED = [
+    # (name, batch, A shape, B shape, input kind)
+    ("cfg1 f32 128x512x1024 (rows in registers)", 0, (128, 1024), (512, 1024), "f32"),
+    ("per head 16x196x196x64 (rows in registers)", 16, (196, 64), (196, 64), "f32"),
+    ("bf16 512x384x2048 (row pipeline, row-norm bounds)", 0, (512, 2048), (384, 2048), "bf16"),
+    ("bf16 ragged 333x350x4096 (row pipeline)", 0, (333, 4096), (350, 4096), "bf16"),
+    ("f32 320x400x1024 (row pipeline)", 0, (320, 1024), (400, 1024), "f32"),
+    ("bf16 +-1 codes 320x336x2048 (bounds demand the drains)", 0, (320, 2048), (336, 2048), "signs"),
+    ("f32 long rows 40x48x20000 (quantize, then staging)", 0, (40, 20000), (48, 20000), "f32"),
+]
+
+
+@pytest.mark.parametrize("name,nb,sa_shape,sb_shape,kind", FUSED, ids=[c[0] for c in FUSED])
+def test_i8_quantize_staged_then_gemm(name, nb, sa_shape, sb_shape, kind):
+    """sq_quantize_rowwise_i8_staged on A and B, then the staged GEMM: codes,
+    scales, int32 accumulators and fp32 outputs equal the oracle's bit for
+    bit, whichever kernel the shape takes (rows in registers, the row
+    pipeline with row-norm bounds, or quantize then staging).  With every
+    code +-127 the row norms exceed the exactness bound, so the GEMM must
+    drain its fp32 sums every 1024 K; a wrong decision loses exactness."""
+    s = seed_of(name)
+    shape_a = (nb,) + sa_shape if nb else sa_shape
+    shape_b = (nb,) + sb_shape if nb else sb_shape
+    if kind == "f32":
+        a, b = synth.normal(s, shape_a), synth.normal(s + 1, shape_b)
+        dt, A, B = oracle.F32, to_dev(a), to_dev(b)
+    elif kind == "bf16":
+        a = synth.normal(s, shape_a, dtype=synth.BF16)
+        b = synth.normal(s + 1, shape_b, dtype=synth.BF16)
+        dt, A, B = oracle.BF16, to_dev(a, bf16=True), to_dev(b, bf16=True)
+    else:
+        a, b = _bf16_signs(s, shape_a), _bf16_signs(s + 1, shape_b)
+        dt, A, B = oracle.BF16, to_dev(a, bf16=True), to_dev(b, bf16=True)
+    oqa, osa = oracle.quantize_rowwise_i8(a, dt)
+    oqb, osb = oracle.quantize_rowwise_i8(b, dt)
+    if kind == "signs":
+        assert np.all(np.abs(oqa) == 127) and np.all(np.abs(oqb) == 127)
+    oacc, oC = oracle.gemm_i8(oqa, oqb, osa, osb)
+    M, K = sa_shape
+    N = sb_shape[0]
+    ws = torch.empty(sq.gemm_i8_workspace_bytes(max(nb, 1), M, N, K), dtype=torch.uint8,
+                     device=DEV)
+    shape = (nb, M, N, K)
+    qa, sa = sq.sq_quantize_rowwise_i8_staged(A, 0, shape, ws)
+    qb, sb = sq.sq_quantize_rowwise_i8_staged(B, 1, shape, ws)
+    assert np.array_equal(qa.cpu().numpy(), oqa) and np.array_equal(sa.cpu().numpy(), osa)
+    assert np.array_equal(qb.cpu().numpy(), oqb) and np.array_equal(sb.cpu().numpy(), osb)
+    C, acc = sq.sq_gemm_i8_rowscaled_staged(sa.reshape(-1), sb.reshape(-1), shape, ws,
+                                            acc_out=True)
+    assert np.array_equal(acc.cpu().numpy(), oacc)
+    assert np.array_equal(C.cpu().numpy(), oC)
+
+
 # ------------------------------------------------------------------ FP8
 @pytest.mark.parametrize("c", [42, 47], ids=["bound holds: one K chunk", "bound fails: drained"])
 def test_i8_exactness_with_and_without_drains(c):
@@ -420,6 +480,7 @@ E4M3_OUT = [
     ("out8 TN 208x160x256", 208, 160, 256, sq.SQ_TN, sq.SQ_FMT_E5M2),
     ("out8 pair NT 2200x2208x256", 2200, 2208, 256, sq.SQ_NT, sq.SQ_FMT_E4M3),
     ("out8 one round NT 2040x1000x1024", 2040, 1000, 1024, sq.SQ_NT, sq.SQ_FMT_E4M3),
+    ("out8 one round of pairs NT 2048x2048x512", 2048, 2048, 512, sq.SQ_NT, sq.SQ_FMT_E4M3),
 ]
 
 

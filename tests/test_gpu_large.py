@@ -71,3 +71,30 @@ def test_large_int8_per_row(inputs):
     ridx = torch.from_numpy(rows).to(DEV)
     assert np.array_equal(acc[ridx].cpu().numpy(), oacc)
     assert np.array_equal(C[ridx].cpu().numpy(), oC)
+
+
+def test_large_int8_per_row_quantized_and_staged(inputs):
+    """The benchmark's INT8 path: each operand quantized and staged in one
+    launch (sq_quantize_rowwise_i8_staged), then the staged GEMM; codes and
+    scales in full, GEMM outputs on sampled rows, and the same bits as the
+    one-call form on those rows."""
+    a, b = inputs
+    ws = torch.empty(sq.gemm_i8_workspace_bytes(1, M, N, K), dtype=torch.uint8, device=DEV)
+    shape = (0, M, N, K)
+    A, B = to_dev(a, bf16=True), to_dev(b, bf16=True)
+    qa, sa = sq.sq_quantize_rowwise_i8_staged(A, 0, shape, ws)
+    qb, sb = sq.sq_quantize_rowwise_i8_staged(B, 1, shape, ws)
+    C, acc = sq.sq_gemm_i8_rowscaled_staged(sa, sb, shape, ws, acc_out=True)
+    oqa, osa = oracle.quantize_rowwise_i8(a, oracle.BF16)
+    oqb, osb = oracle.quantize_rowwise_i8(b, oracle.BF16)
+    assert np.array_equal(sa.cpu().numpy(), osa) and np.array_equal(sb.cpu().numpy(), osb)
+    assert np.array_equal(qa.cpu().numpy(), oqa)
+    assert np.array_equal(qb.cpu().numpy(), oqb)
+    rows = np.sort(np.random.default_rng(9).choice(M, SAMPLE_ROWS, replace=False))
+    oacc, oC = oracle.gemm_i8(oqa, oqb, osa, osb, rows=rows)
+    ridx = torch.from_numpy(rows).to(DEV)
+    assert np.array_equal(acc[ridx].cpu().numpy(), oacc)
+    assert np.array_equal(C[ridx].cpu().numpy(), oC)
+    ws1 = torch.empty_like(ws)
+    C1, acc1 = sq.sq_gemm_i8_rowscaled(qa, sa, qb, sb, ws1, acc_out=True)
+    assert torch.equal(C1[ridx], C[ridx]) and torch.equal(acc1[ridx], acc[ridx])
