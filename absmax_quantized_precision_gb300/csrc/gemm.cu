@@ -962,27 +962,26 @@ static cudaError_t gemm_fp8_shape(const uint8_t* A, const uint8_t* B, int M, int
 
 // FP8 tile shape by estimated time: rounds of tiles over the SMs (or SM
 // pairs) times the k-blocks per tile times the time of one k-block on one SM,
-// in clocks.  A k-block is 128 bytes of K.  Measured on GB300 with every SM
-// loading: a single CTA's operand stages arrive at about 80 B/clk, so a
-// 128 x 128 tile (32 KB per k-block) waits on its loads (~410 clk) rather
-// than on its MMAs (256 clk); a 128 x 256 tile moves 48 KB (~614 clk); a CTA
-// of a pair holds 128 rows of A and half of B's 256 (32 KB) and is bound by
-// its MMAs (512 clk).  Ties go to the later entry of the list.  (A 256 x 128
-// pair tile, 24 KB per k-block per CTA, measured no faster than 128 x 128 on
-// the one-round shapes where it would be chosen: their short K loops wait on
-// the first loads, and a pair's set-up costs more.)
+// in clocks, plus a fixed cost for CTA pairs.  A k-block is 128 bytes of K.
+// The per-k-block times are those the large workload measured on GB300 with
+// every SM busy: 454 clk for a 128 x 128 tile, 784 for 128 x 256, 702 for
+// each CTA's 128 x 256 half of a 256 x 256 pair tile.  The pair's fixed cost
+// (~4000 clk) is its set-up (pair TMEM allocation, cluster barrier) and its
+// longer exposed epilogue, measured on one-round launches: there 256 x 256
+// pairs lost to single CTAs despite the shorter K loop.  Ties go to the later
+// entry of the list.
 static Shape pick_shape_fp8(int64_t M, int64_t N, int64_t K, int sms) {
-    struct Cand { Shape s; int64_t tm, tn, slots, clk; };
-    const Cand c[3] = {{Shape::Single256, 128, 256, sms, 614},
-                       {Shape::Single128, 128, 128, sms, 410},
-                       {Shape::Pair256, 256, 256, sms / 2, 512}};
+    struct Cand { Shape s; int64_t tm, tn, slots, clk, fixed; };
+    const Cand c[3] = {{Shape::Single256, 128, 256, sms, 784, 0},
+                       {Shape::Single128, 128, 128, sms, 454, 0},
+                       {Shape::Pair256, 256, 256, sms / 2, 702, 4000}};
     const int64_t nkb = (K + kBKBytes - 1) / kBKBytes;
     Shape best = Shape::Single128;
     int64_t best_t = -1;
     for (const Cand& x : c) {
         const int64_t tiles = ((M + x.tm - 1) / x.tm) * ((N + x.tn - 1) / x.tn);
         const int64_t rounds = (tiles + x.slots - 1) / x.slots;
-        const int64_t t = rounds * nkb * x.clk;
+        const int64_t t = rounds * nkb * x.clk + x.fixed;
         if (best_t < 0 || t <= best_t) {
             best = x.s;
             best_t = t;

@@ -522,10 +522,11 @@ def run_sq(args, rank, world, local_rank):
                     fn()
                 pe[s][j][1].record(stream)
         torch.cuda.synchronize(dev)
-        prefix = [statistics.mean(pe[s][j][0].elapsed_time(pe[s][j][1]) for s in range(args.steps))
-                  for j in range(nseq)]
+        pt = [[pe[s][j][0].elapsed_time(pe[s][j][1]) for j in range(nseq)] for s in range(args.steps)]
         for j, (name, _) in enumerate(seq):
-            in_step_ms[name] = prefix[j] - (prefix[j - 1] if j > 0 else 0.0)
+            # median over rounds of the paired difference of the two prefixes
+            in_step_ms[name] = statistics.median(pt[s][j] - (pt[s][j - 1] if j > 0 else 0.0)
+                                                 for s in range(args.steps))
         if sq.sq_get_last_device_error() != sq.SQ_OK:
             raise RuntimeError("device error in the prefix passes")
 
@@ -742,11 +743,11 @@ def run_sq(args, rank, world, local_rank):
                          + ("; with two streams the INT8 quantize spans overlap the FP8 GEMM and "
                             "share the GPU with it" if args.overlap else "")),
         "kernels_in_step": kernels_in_step,
-        "kernels_in_step_note": ("what each call costs inside the step: the mean time of the "
-                                 "step's first j + 1 calls minus that of its first j calls, each "
-                                 "prefix timed over the K steps with events only at its two ends "
-                                 "(the calls keep their launch overlap); the first call's figure "
-                                 "includes its launch"),
+        "kernels_in_step_note": ("what each call costs inside the step: the median over K "
+                                 "rounds of the time of the step's first j + 1 calls minus that of "
+                                 "its first j calls in the same round, each prefix timed with "
+                                 "events only at its two ends (the calls keep their launch "
+                                 "overlap); the first call's figure includes its launch"),
         "kernels_steady": kernels_steady,
         "kernels_steady_note": ("each quantize call launched 10 times back to back with events only "
                                 "around the batch; B alternates with a same-size block of A so "
@@ -888,9 +889,10 @@ def measure_config(name, args, with_cpu=True, compact=False):
       step   the whole step (its calls in order) captured as one CUDA graph;
       calls  each call alone, captured as its own graph (its device time plus
              one launch);
-      in_step  what each call adds to the step: the graph of the step's first
-             j + 1 calls minus the graph of its first j calls (the first
-             call's figure includes the replay's own start);
+      in_step  what each call adds to the step: the median over rounds of the
+             replay time of the step's first j + 1 calls minus that of its
+             first j calls in the same round (the first call's figure
+             includes the replay's own start);
     plus the oracle's time for the whole workload on the host (all cores and
     one core).  Returns a dict; compact leaves out the eager timings."""
     import numpy as np
@@ -930,7 +932,7 @@ def measure_config(name, args, with_cpu=True, compact=False):
         oracle.set_num_threads(cores)
         cpu["sample"] = "the whole workload"
 
-    iters = 100
+    iters = 200
     for _ in range(max(args.warmup, 3)):
         for _, _, _, fn in ops + alt_calls:
             fn()
@@ -946,8 +948,8 @@ def measure_config(name, args, with_cpu=True, compact=False):
         return g
 
     def time_graphs(graphs):
-        """Median replay time of each graph; every round replays each graph
-        once, after an L2-evicting write, so that all see the same drift."""
+        """Replay times [round][graph]: every round replays each graph once,
+        after an L2-evicting write, so that all see the same drift."""
         ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in graphs]
               for _ in range(iters)]
         for it in range(iters):
@@ -957,17 +959,21 @@ def measure_config(name, args, with_cpu=True, compact=False):
                 g.replay()
                 ev[it][j][1].record(stream)
         torch.cuda.synchronize(dev)
-        return [statistics.median(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(iters))
-                for j in range(len(graphs))]
+        return [[ev[i][j][0].elapsed_time(ev[i][j][1]) for j in range(len(graphs))]
+                for i in range(iters)]
 
     with Clocks(dev) as clk:
         # the graphs of the step's first j + 1 calls, then of each call alone
         graphs = [capture([fn for _, _, _, fn in ops[:j + 1]]) for j in range(len(ops))]
         graphs += [capture([fn]) for _, _, _, fn in ops + alt_calls]
-        times = time_graphs(graphs)
-        prefix_ms = times[:len(ops)]
-        step_ms = prefix_ms[-1]
-        call_ms = times[len(ops):]
+        t = time_graphs(graphs)
+        med = [statistics.median(t[i][j] for i in range(iters)) for j in range(len(graphs))]
+        step_ms = med[len(ops) - 1]
+        call_ms = med[len(ops):]
+        # a call's cost in the step: the median over rounds of the paired
+        # difference between the prefixes through it and through the call before
+        inc_ms = [statistics.median(t[i][j] - (t[i][j - 1] if j > 0 else 0.0) for i in range(iters))
+                  for j in range(len(ops))]
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error in the graph passes")
 
@@ -1005,7 +1011,7 @@ def measure_config(name, args, with_cpu=True, compact=False):
         calls[label] = rates(label, kind, amount, call_ms[j])
     in_step = {}
     for j, (label, kind, amount, _) in enumerate(ops):
-        inc = prefix_ms[j] - (prefix_ms[j - 1] if j > 0 else 0.0)
+        inc = inc_ms[j]
         in_step[label] = ({"us": 1e3 * inc} if inc <= 0 else rates(label, kind, amount, inc))
     out = {"desc": desc, "value": gemm_flops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
            "us_per_step": 1e3 * step_ms, "calls": calls, "in_step": in_step,

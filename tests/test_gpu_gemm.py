@@ -384,8 +384,8 @@ def test_fp8_backward_dx_nn_and_dw_tn():
 
 # ------------------------------------------------------------------ the pages' one-wave shapes
 # The forward (NT 2048x1024x1024) and dX (NN) run on 128x128 tiles, dW (TN)
-# on 256x256 tiles of CTA pairs: one round of tiles each.  The ragged variants
-# clip M, N and K against those tiles.
+# on 128x256 tiles: one round of tiles each.  The ragged variants clip M, N
+# and K against those tiles.
 ONE_WAVE = [
     ("fwd NT 2048x1024x1024 e5m2", 2048, 1024, 1024, sq.SQ_NT, sq.SQ_FMT_E5M2),
     ("fwd NT ragged 2040x1000x1040", 2040, 1000, 1040, sq.SQ_NT, sq.SQ_FMT_E4M3),
@@ -414,12 +414,13 @@ def test_fp8_gemm_one_wave_shapes(name, M, N, K, layout, fmt):
 
 
 # ------------------------------------------------------------------ CTA-pair shapes
-# Problems with at least one 256x256 tile per pair of SMs run on the 2-SM
-# (cta_group::2) kernel; these sizes select it and keep ragged tails in M and N.
+# Problems with several rounds of 256x256 tiles over the SM pairs and a long
+# enough K run on the 2-SM (cta_group::2) kernel; these sizes select it and
+# keep ragged tails in M and N (the last column of pair tiles is half empty).
 PAIR_FP8 = [
-    ("pair NT 2200x2208x320", 2200, 2208, 320, sq.SQ_NT),
-    ("pair NN 2200x2208x384", 2200, 2208, 384, sq.SQ_NN),
-    ("pair TN 2208x2208x256", 2208, 2208, 256, sq.SQ_TN),
+    ("pair NT 4000x3968x4096", 4000, 3968, 4096, sq.SQ_NT),
+    ("pair NN 4000x3968x4096", 4000, 3968, 4096, sq.SQ_NN),
+    ("pair TN 4000x3968x4096", 4000, 3968, 4096, sq.SQ_TN),
 ]
 
 
@@ -478,9 +479,9 @@ E4M3_OUT = [
     ("out8 NT 200x176x320", 200, 176, 320, sq.SQ_NT, sq.SQ_FMT_E4M3),
     ("out8 NN 256x384x512", 256, 384, 512, sq.SQ_NN, sq.SQ_FMT_E4M3),
     ("out8 TN 208x160x256", 208, 160, 256, sq.SQ_TN, sq.SQ_FMT_E5M2),
-    ("out8 pair NT 2200x2208x256", 2200, 2208, 256, sq.SQ_NT, sq.SQ_FMT_E4M3),
+    ("out8 pair NT 4000x3968x4096", 4000, 3968, 4096, sq.SQ_NT, sq.SQ_FMT_E4M3),
     ("out8 one round NT 2040x1000x1024", 2040, 1000, 1024, sq.SQ_NT, sq.SQ_FMT_E4M3),
-    ("out8 one round of pairs NT 2048x2048x512", 2048, 2048, 512, sq.SQ_NT, sq.SQ_FMT_E4M3),
+    ("out8 one round of 128x256 tiles NT 2048x2048x512", 2048, 2048, 512, sq.SQ_NT, sq.SQ_FMT_E4M3),
 ]
 
 
