@@ -93,8 +93,8 @@ def algo_bytes(kernel):
 # was taken from: when the sha256 of those sources no longer matches, the
 # bench reports traffic as null.
 PROFILED_TRAFFIC = {
-    "gemm_fp8_nt": {"bytes": 845101312, "sources_sha256": "4563eb120155e2e556fd197c8ef414dd2d00937fee2bbb048047666eadb9df2d"},
-    "gemm_i8_kernel": {"bytes": 2727098624, "sources_sha256": "4563eb120155e2e556fd197c8ef414dd2d00937fee2bbb048047666eadb9df2d"},
+    "gemm_fp8_nt": {"bytes": 788711680, "sources_sha256": "6d8b8bc3831d42b0adfdb562f85dad92f02a561257569dfbb142589843a8c7e6"},
+    "gemm_i8_kernel": {"bytes": 2727968512, "sources_sha256": "6d8b8bc3831d42b0adfdb562f85dad92f02a561257569dfbb142589843a8c7e6"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
