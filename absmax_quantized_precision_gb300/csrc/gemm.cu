@@ -1134,7 +1134,6 @@ __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const in
                                                                        uint16_t* __restrict__ dst,
                                                                        unsigned* __restrict__ bound,
                                                                        unsigned* err_word) {
-    pdl_begin();
     extern __shared__ uint8_t gsmem_raw[];
     uint8_t* gsmem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(gsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -1160,6 +1159,8 @@ __global__ void __launch_bounds__(kStgWarps * 32) i8_to_f16_bulk_kernel(const in
         fence_mbar_init();
     }
     __syncthreads();
+    // nothing above touches global memory (it overlaps the previous kernel)
+    pdl_begin();
     if (lane == 0) {
         for (int64_t k = 0; k < count && k < kStgStages; ++k) {
             mbar_arrive_expect_tx(&full[k], kStgChunk);

@@ -697,7 +697,6 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
                                                                  unsigned* __restrict__ ws, float* ring,
                                                                  int hist_len, int ring_idx, int margin,
                                                                  unsigned* err_word) {
-    pdl_begin();
     extern __shared__ uint8_t qsmem_raw[];
     uint8_t* qsmem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(qsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -725,6 +724,9 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
         fence_mbar_init();
     }
     __syncthreads();
+    // The barrier set-up above touches no global memory, so it overlaps the
+    // previous kernel's tail; global memory is accessed only from here on.
+    pdl_begin();
     if (lane == 0) {
         for (int64_t k = 0; k < count && k < kFStages; ++k) {
             mbar_arrive_expect_tx(&full[k], kFChunk * 2);
