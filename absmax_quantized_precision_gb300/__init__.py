@@ -37,7 +37,8 @@ EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "
            "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
            "sq_quantize_grouped_i8", "sq_gemm_i8_grouped", "sq_linear_workspace_bytes",
            "sq_linear_forward_fp8", "sq_linear_backward_fp8", "sq_selftest_bounded_wait",
-           "sq_gemm_i8_stage", "sq_gemm_i8_rowscaled_staged", "sq_quantize_rowwise_i8_staged")
+           "sq_gemm_i8_stage", "sq_gemm_i8_rowscaled_staged", "sq_quantize_rowwise_i8_staged",
+           "sq_set_clock_probe")
 
 # size of the fixed scratch array behind sq_gemm_i8_rowscaled_noalloc
 GEMM_I8_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -108,6 +109,8 @@ def load_library():
     L.sq_quantize_rowwise_i8_staged.argtypes = [vp, i32, i64, i64, i64, vp, vp, i32, i64, i64, i64,
                                                 i64, vp, sz, vp]
     L.sq_quantize_rowwise_i8_staged.restype = i32
+    L.sq_set_clock_probe.argtypes = [vp, vp, i32]
+    L.sq_set_clock_probe.restype = i32
     L.sq_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp]
     L.sq_selftest_bounded_wait.restype = i32
     _lib = L
@@ -624,6 +627,35 @@ def sq_linear_backward_fp8(g: torch.Tensor, x: torch.Tensor, w: torch.Tensor, ma
             _ptr(x8), _ptr(workspace), _ws_bytes(workspace), _stream(stream)),
             "sq_linear_backward_fp8")
     return gx, gw, gb, amax_g
+
+
+def sq_set_clock_probe(fp8_records: torch.Tensor = None, i8_records: torch.Tensor = None):
+    """Diagnostics: let the GEMM launches record their CTAs' SM cycles and
+    nanoseconds (int64 tensors of 4 * max_ctas words on the current device);
+    no arguments stop the records."""
+    dev = _need_cuda(fp8_records, i8_records)
+    caps = [t.numel() // 4 for t in (fp8_records, i8_records) if t is not None]
+    for t in (fp8_records, i8_records):
+        if t is not None:
+            _need(t, torch.int64, what="records")
+    with torch.cuda.device(dev or torch.cuda.current_device()):
+        _check(load_library().sq_set_clock_probe(_ptr(fp8_records), _ptr(i8_records),
+                                                 min(caps) if caps else 0), "sq_set_clock_probe")
+
+
+def clock_probe_mhz(records: torch.Tensor) -> dict:
+    """Median, minimum and maximum mean SM clock (MHz) over the CTAs that
+    wrote records (zero rows are unused slots), their median cycle count, and
+    the launch's span from the first CTA's start to the last one's end."""
+    r = records.view(-1, 4).cpu()
+    r = r[r[:, 3] > r[:, 2]]
+    if r.numel() == 0:
+        return {}
+    cyc = (r[:, 1] - r[:, 0]).double()
+    mhz = cyc / (r[:, 3] - r[:, 2]).double() * 1e3
+    return {"median": float(mhz.median()), "min": float(mhz.min()), "max": float(mhz.max()),
+            "ctas": int(r.shape[0]), "cycles_median": float(cyc.median()),
+            "span_ns": int(r[:, 3].max() - r[:, 2].min())}
 
 
 def sq_selftest_bounded_wait(limit_ns: int, stream=None):

@@ -585,6 +585,14 @@ sq_status sq_gemm_i8_rowscaled_noalloc(const int8_t* A, const float* sA, const i
                                 acc_out, na.scratch, SQ_GEMM_I8_NOALLOC_SCRATCH_BYTES, stream);
 }
 
+sq_status sq_set_clock_probe(unsigned long long* fp8_records, unsigned long long* i8_records,
+                             int max_ctas) {
+    if (max_ctas < 0 || ((fp8_records || i8_records) && max_ctas == 0)) return SQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(fp8_records) | reinterpret_cast<uintptr_t>(i8_records)) & 7u)
+        return SQ_ERR_ALIGNMENT;
+    return from_cuda(sq::set_gemm_clock_probe(fp8_records, i8_records, max_ctas));
+}
+
 sq_status sq_selftest_bounded_wait(uint64_t limit_ns, sq_stream stream) {
     if (limit_ns == 0 || limit_ns > 2000000000ull) return SQ_ERR_INVALID_ARG;
     cudaError_t e = cudaSuccess;

@@ -30,6 +30,7 @@
 // and sums the chunks in registers, which keeps the whole K sum exact.
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -76,6 +77,10 @@ struct GemmParams {
     int Mg, Ng;             // INT8: scale groups per batch, ceil(M/ga), ceil(N/gb)
     int sb_vec;             // INT8: sB may be read 4 floats at a time
     const float* bias;      // FP8: float32 bias per output column, added after scaling (nullable)
+    // Diagnostics (nullable): per CTA, SM cycles and %globaltimer at entry
+    // and at exit, [cycles0, cycles1, ns0, ns1], for CTAs below clk_cap
+    unsigned long long* clk;
+    int clk_cap;
 };
 
 // PAIR = false: one CTA per SM computes 128 x BN tiles (cta_group::1).
@@ -704,6 +709,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::T
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    unsigned long long clk0 = 0, ns0 = 0;
+    if (p.clk && threadIdx.x == 0) {
+        clk0 = clock64();
+        ns0 = global_ns_ordered();
+    }
     const uint32_t rank = PAIR ? cluster_rank() : 0u;   // 0 = leader of the pair
     const bool leader = rank == 0;
     const int cta_unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
@@ -822,9 +832,41 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::T
         if (PAIR) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
         else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
+    if (p.clk && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < p.clk_cap) {
+        const unsigned long long clk1 = clock64();
+        const unsigned long long ns1 = global_ns_ordered();
+        unsigned long long* r = p.clk + 4 * static_cast<int64_t>(blockIdx.x);
+        r[0] = clk0;
+        r[1] = clk1;
+        r[2] = ns0;
+        r[3] = ns1;
+    }
 }
 
 // ====================================================================== host
+// Per-device diagnostic buffers for the GEMM clock records (sq_set_clock_probe).
+struct ClockProbe {
+    std::atomic<unsigned long long*> fp8{nullptr};
+    std::atomic<unsigned long long*> i8{nullptr};
+    std::atomic<int> cap{0};
+};
+static ClockProbe g_clock_probe[64];
+
+static ClockProbe* current_probe() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    return &g_clock_probe[dev];
+}
+
+cudaError_t set_gemm_clock_probe(unsigned long long* fp8, unsigned long long* i8, int cap) {
+    ClockProbe* cp = current_probe();
+    if (!cp) return cudaErrorInvalidDevice;
+    cp->cap.store(cap);
+    cp->fp8.store(fp8);
+    cp->i8.store(i8);
+    return cudaSuccess;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1019,6 +1061,10 @@ cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa,
     // 16-byte stores: 8 bf16 or 16 E4M3 codes per row piece
     p.vec_store = (N % (p.out_e4m3 ? 16 : 8) == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
     p.err_word = err_word;
+    if (ClockProbe* cp = current_probe()) {
+        p.clk = cp->fp8.load();
+        p.clk_cap = p.clk ? cp->cap.load() : 0;
+    }
     if (layout == 0) return gemm_fp8_layout<false, false>(A, B, M, N, K, p, fmt, st, sms);
     if (layout == 1) return gemm_fp8_layout<false, true>(A, B, M, N, K, p, fmt, st, sms);
     return gemm_fp8_layout<true, true>(A, B, M, N, K, p, fmt, st, sms);
@@ -1068,6 +1114,10 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
                   (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0);
     p.sb_vec = (gb == 1) && (N % 4 == 0) && (reinterpret_cast<uintptr_t>(sB) % 16 == 0);
     p.err_word = err_word;
+    if (ClockProbe* cp = current_probe()) {
+        p.clk = cp->i8.load();
+        p.clk_cap = p.clk ? cp->cap.load() : 0;
+    }
     p.bound_a = bound_a;
     p.bound_b = bound_b;
     // a row of K codes overlaps at most ceil(K / chunk) + 1 staged chunks

@@ -31,6 +31,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// The same, kept in place with respect to the memory operations around it.
+__device__ __forceinline__ unsigned long long global_ns_ordered() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+    return t;
+}
+
 __device__ __forceinline__ bool elect_one_sync() {
     uint32_t pred = 0;
     asm volatile(

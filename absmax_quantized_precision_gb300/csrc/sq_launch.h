@@ -92,6 +92,10 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
                            int64_t strideC, float* C, int32_t* acc_out, const unsigned* bound_a,
                            const unsigned* bound_b, unsigned* err_word, cudaStream_t st, int sms);
 
+// Diagnostics: where the GEMM launches on the current device record their
+// CTAs' clocks (nullable; cap records of 4 words each).
+cudaError_t set_gemm_clock_probe(unsigned long long* fp8, unsigned long long* i8, int cap);
+
 // One CTA waits on a barrier phase that never completes, for limit_ns.
 cudaError_t launch_selftest_wait(unsigned* err_word, unsigned long long limit_ns, cudaStream_t st);
 

@@ -50,7 +50,6 @@ FLOPS_PER_STEP = 2 * (2.0 * M * N * K)
 # INT8 codes run on the f16 tensor path here (sm_103a has no integer MMA
 # kind), so the INT8 GEMM is set against the f16 rate.
 NOMINAL_TFLOPS = {"fp8": 4500.0, "f16": 2250.0}
-NOMINAL_SM_MHZ = 2070.0
 
 
 def parse():
@@ -492,6 +491,21 @@ def run_sq(args, rank, world, local_rank):
     if sq.sq_get_last_device_error() != sq.SQ_OK:
         raise RuntimeError("device error in the event pass")
 
+    # The SM clock the GEMMs actually ran at: one more pass of the K steps in
+    # which every GEMM launch records its CTAs' cycles and nanoseconds (the
+    # records left are those of the last step).
+    rec_fp8 = torch.zeros(4 * 1024, dtype=torch.int64, device=dev)
+    rec_i8 = torch.zeros(4 * 1024, dtype=torch.int64, device=dev)
+    sq.sq_set_clock_probe(rec_fp8, rec_i8)
+    try:
+        for s in range(args.steps):
+            step()
+        torch.cuda.synchronize(dev)
+    finally:
+        sq.sq_set_clock_probe()
+    kernel_mhz = {"gemm_fp8_nt": sq.clock_probe_mhz(rec_fp8),
+                  "gemm_i8_kernel": sq.clock_probe_mhz(rec_i8)}
+
     # What each call costs inside the step (one stream): pass j runs the
     # step's first j + 1 calls, with an event at the step's start and one after
     # call j and nothing between, so the calls keep their launch overlap; call
@@ -669,6 +683,23 @@ def run_sq(args, rank, world, local_rank):
     kernels_in_step = {n: rate(n, ms) for n, ms in in_step_ms.items()}
     kernels_steady = {n: rate(n, ms) for n, ms in steady_ms.items()}
 
+    # Fraction of the tensor pipe's peak at the clock the kernel ran at: dense
+    # MMA rates per SM per clock of 8192 FP8 and 4096 f16 multiply-adds.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def at_kernel_clock(name, tflops):
+        rec = kernel_mhz.get(name, {})
+        mhz = rec.get("median")
+        if not mhz:
+            return None
+        per_clk = 16384 if name == "gemm_fp8_nt" else 8192
+        return {"sm_mhz": mhz, "flops_per_sm_per_clk": per_clk, "sms": sms,
+                "peak_tflops": per_clk * sms * mhz * 1e6 / 1e12,
+                "frac": tflops / (per_clk * sms * mhz * 1e6 / 1e12),
+                # the same launches' own cycles: the flops over what the SMs could
+                # have done in the cycles the CTAs lived (independent of the clock)
+                "frac_of_cycles": (2.0 * M * N * K) / (per_clk * sms * rec["cycles_median"])}
+
     # Roofline: the dominant kernel of the step (the longest single launch).
     dom = max(("gemm_fp8_nt", "gemm_i8_kernel"), key=lambda n: per_kernel[n])
     fp8 = dom == "gemm_fp8_nt"
@@ -691,15 +722,15 @@ def run_sq(args, rank, world, local_rank):
         "timed": ("one sq_gemm_i8_rowscaled_staged launch (its operands were staged by the "
                   "quantize launches)" if not fp8 else "one sq_gemm_fp8_scaled launch"),
         "vs_nominal": {"nominal_dense_tflops": nominal, "frac": achieved / nominal,
-                       "frac_at_sampled_clock": (achieved / (nominal * clocks["sm_mhz"] / NOMINAL_SM_MHZ)
-                                                 if clocks.get("sm_mhz") else None),
-                       "note": "nominal dense FP8 4.5 / f16 2.25 PFLOP/s at 2070 MHz"},
+                       "note": "nominal dense FP8 4.5 / f16 2.25 PFLOP/s"},
+        "at_kernel_clock": at_kernel_clock(dom, achieved),
     }
     other = "gemm_i8_kernel" if fp8 else "gemm_fp8_nt"
     other_rec = {"kernel": other, "achieved": kernels[other]["TFLOP/s"],
                  "peak": tensor_peak(pk, other == "gemm_fp8_nt"),
                  "frac": check_frac(other, kernels[other]["frac_peak"]),
-                 "traffic": profiled_traffic(other), "algorithmic_bytes": algo_bytes(other)}
+                 "traffic": profiled_traffic(other), "algorithmic_bytes": algo_bytes(other),
+                 "at_kernel_clock": at_kernel_clock(other, kernels[other]["TFLOP/s"])}
     if other_rec["traffic"]:
         other_rec["traffic_vs_algorithmic"] = other_rec["traffic"] / algo_bytes(other)
     roofline["other_gemm"] = other_rec
@@ -733,6 +764,11 @@ def run_sq(args, rank, world, local_rank):
                                 "INT8 GEMM call after it")},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "kernel_clocks": kernel_mhz,
+        "kernel_clocks_note": ("mean SM clock of each GEMM launch's CTAs (their cycle counter over "
+                               "the global timer, recorded by the kernels), median over CTAs, last "
+                               "step of an extra pass; the NVML samples above miss the fast clock "
+                               "reductions under the tensor cores"),
         "roofline": roofline,
         "kernels": kernels,
         "kernels_note": ("mean CUDA-event span of each call on the stream it ran on, from a second "

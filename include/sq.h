@@ -363,6 +363,20 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
                                  sq_stream stream);
 
 /*
+ * Diagnostics (no counterpart on the pages): the SM clock that the GEMMs
+ * actually run at.  With a buffer set, every later GEMM launch of that kind
+ * (FP8 or INT8) on the current device writes, for each of its CTAs below
+ * max_ctas, four words at records[4*cta]: the SM cycle counter (clock64) and
+ * the global nanosecond timer at the CTA's start and at its end.  The
+ * cycles over the nanoseconds are the CTA's mean SM clock.  Each launch
+ * overwrites the records of the one before; NULL buffers stop the records.
+ * The buffers are device memory of 4 * max_ctas 64-bit words, 8-byte
+ * aligned, owned by the caller and read by it after synchronising.
+ */
+sq_status sq_set_clock_probe(unsigned long long* fp8_records, unsigned long long* i8_records,
+                             int max_ctas);
+
+/*
  * Self-test of the failure path every kernel with waits takes: launches one
  * CTA that waits on a barrier phase nothing completes; after limit_ns
  * (1 .. 2e9) the wait gives up, the kernel records SQ_ERR_DEVICE_TIMEOUT in

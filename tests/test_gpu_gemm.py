@@ -555,3 +555,39 @@ def test_i8_gemm_grouped_batched_per_tensor_heads():
     C, acc = sq.sq_gemm_i8_grouped(to_dev(qq), to_dev(sqa), 196, to_dev(qk), to_dev(ska), 196, ws,
                                    acc_out=True)
     assert np.array_equal(acc.cpu().numpy(), oacc) and np.array_equal(C.cpu().numpy(), oC)
+
+
+# ------------------------------------------------------------------ clock records
+def test_gemm_clock_probe_records_each_cta():
+    """With record buffers set, a GEMM launch writes per CTA its start and end
+    SM cycles and nanoseconds: the implied clocks are plausible, one record
+    per CTA, and clearing the buffers stops the records."""
+    rec8 = torch.zeros(256 * 4, dtype=torch.int64, device=DEV)
+    rec_i8 = torch.zeros(256 * 4, dtype=torch.int64, device=DEV)
+    sq.sq_set_clock_probe(rec8, rec_i8)
+    try:
+        a8, b8, sa, sb = fp8_inputs("clock probe", 1024, 1024, 2048, 0)
+        C = sq.sq_gemm_fp8_scaled(to_dev(a8), to_dev(b8), torch.tensor([sa], device=DEV),
+                                  torch.tensor([sb], device=DEV), 0, sq.SQ_NT)
+        qa = torch.randint(-127, 128, (512, 1024), dtype=torch.int8, device=DEV)
+        qb = torch.randint(-127, 128, (640, 1024), dtype=torch.int8, device=DEV)
+        ws = torch.empty(sq.gemm_i8_workspace_bytes(1, 512, 640, 1024), dtype=torch.uint8,
+                         device=DEV)
+        sq.sq_gemm_i8_rowscaled(qa, torch.ones(512, device=DEV), qb, torch.ones(640, device=DEV),
+                                ws)
+        torch.cuda.synchronize()
+    finally:
+        sq.sq_set_clock_probe()
+    for rec, ctas in ((rec8, 64), (rec_i8, 20)):   # 8x8 tiles of 128; 4x5 tiles of 128
+        r = rec.view(-1, 4)
+        used = r[r[:, 3] > 0]
+        assert used.shape[0] == ctas
+        assert bool(torch.all(used[:, 1] > used[:, 0])) and bool(torch.all(used[:, 3] > used[:, 2]))
+        mhz = sq.clock_probe_mhz(rec)
+        assert 300.0 < mhz["min"] <= mhz["max"] < 3000.0, mhz
+    check_fp8(C, a8, b8, 0, sq.SQ_NT, 2048, sa, sb)
+    rec8.zero_()
+    sq.sq_gemm_fp8_scaled(to_dev(a8), to_dev(b8), torch.tensor([sa], device=DEV),
+                          torch.tensor([sb], device=DEV), 0, sq.SQ_NT)
+    torch.cuda.synchronize()
+    assert int(rec8.count_nonzero().item()) == 0
