@@ -181,13 +181,15 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
         int issued_phase[Cfg::STAGES];
         for (int s = 0; s < Cfg::STAGES; ++s) issued_phase[s] = -1;
         bool ok = true;
+        bool first_round = true;   // the ring's stages are all free until it wraps
+        bool waited = false;
         for (int t = cta_unit; t < total && ok; t += num_units) {
             int b, mb, nb;
             tile_coords(t, p, b, mb, nb);
             const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
             const int n0 = nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
             for (int kb = 0; kb < p.nkb; ++kb) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err_word)) {
+                if (!first_round && !mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err_word)) {
                     ok = false;
                     break;
                 }
@@ -197,6 +199,10 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
                     // both CTAs' bytes complete on the leader's barrier
                     const uint32_t fb = cluster_addr(&full[stage], 0);
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::STAGE);
+                    if (!waited) {
+                        pdl_wait();   // the operands are the previous kernels' output
+                        waited = true;
+                    }
                     if (I8) {
                         const int kx = kb * (kBKBytes / 2);
                         tma_load_3d_pair(sA, &tmA, fb, kx, m0, b);
@@ -215,6 +221,10 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
                     }
                 } else {
                     mbar_arrive_expect_tx(&full[stage], Cfg::STAGE);
+                    if (!waited) {
+                        pdl_wait();   // the operands are the previous kernels' output
+                        waited = true;
+                    }
                     if (I8) {
                         const int kx = kb * (kBKBytes / 2);
                         tma_load_3d(sA, &tmA, &full[stage], kx, m0, b);
@@ -236,6 +246,7 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
                 if (++stage == Cfg::STAGES) {
                     stage = 0;
                     phase ^= 1u;
+                    first_round = false;
                 }
             }
         }
@@ -746,11 +757,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::T
             tmem_relinquish();
         }
     }
-    // Nothing above reads or writes global memory, so the barrier set-up, the
-    // descriptor fetches and the TMEM allocation overlap the previous kernel's
-    // tail.  (No two GEMM CTAs fit on one SM, so the allocation never waits
-    // for an earlier GEMM's TMEM.)
-    pdl_begin();
+    // Nothing above or in the shared set-up below reads or writes global
+    // memory, so it all overlaps the previous kernel's tail.  (No two GEMM
+    // CTAs fit on one SM, so the allocation never waits for an earlier GEMM's
+    // TMEM.)  Each role waits for the previous kernel right before its own
+    // first global access: the producer once its first stage is armed, the
+    // other warps below, thread 0 again before its clock record.
+    pdl_allow_next();
     tc_fence_before();
     __syncthreads();
     if (PAIR) {
@@ -772,6 +785,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::T
     // Only the MMA issuer and the epilogue need the decision: warps 2 and 3
     // read the bounds while the producer already streams the first stages,
     // and a named barrier among warps 1.. hands the result over.
+    if (warp != 0) pdl_wait();
     int kbpc = p.kb_per_chunk, nch = p.nchunks;
     if (I8 && warp >= 1 && p.bound_a && p.bound_b) {
         if (warp == 2 || warp == 3) {
@@ -833,6 +847,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::T
         else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
     if (p.clk && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < p.clk_cap) {
+        pdl_wait();
         const unsigned long long clk1 = clock64();
         const unsigned long long ns1 = global_ns_ordered();
         unsigned long long* r = p.clk + 4 * static_cast<int64_t>(blockIdx.x);

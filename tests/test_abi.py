@@ -141,3 +141,30 @@ def test_binding_checks_dtypes_and_sizes_before_calling(lib, monkeypatch):
         sq._fp8_shape(u, torch.zeros(16, 48, dtype=torch.uint8), sq.SQ_NT)
     with pytest.raises(TypeError):
         sq._fp8_shape(u.to(torch.int8), torch.zeros(16, 32, dtype=torch.uint8), sq.SQ_NT)
+
+
+def test_clock_record_summary_on_the_host():
+    """clock_probe_mhz: cycles over nanoseconds per CTA, unused (zero) rows
+    left out, and the launch's span from first start to last end."""
+    import torch
+    rec = torch.zeros(8 * 4, dtype=torch.int64)
+    # CTA 0: 2000 cycles in 1000 ns (2000 MHz); CTA 1: 1500 cycles in 1000 ns
+    rec[0:4] = torch.tensor([100, 2100, 5000, 6000])
+    rec[4:8] = torch.tensor([7, 1507, 5100, 6100])
+    s = sq.clock_probe_mhz(rec)
+    assert s["ctas"] == 2 and s["max"] == 2000.0 and s["min"] == 1500.0
+    assert s["span_ns"] == 1100 and s["cycles_median"] in (1500.0, 2000.0, 1750.0)
+    assert sq.clock_probe_mhz(torch.zeros(16, dtype=torch.int64)) == {}
+
+
+def test_quantize_and_stage_binding_checks_the_operand_shape(lib, monkeypatch):
+    import torch
+    monkeypatch.setattr(sq, "_need_cuda", lambda *ts: None)
+    x = torch.zeros(4, 16, dtype=torch.float32)
+    ws = torch.zeros(1, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="operand"):
+        sq.sq_quantize_rowwise_i8_staged(x, 0, (0, 5, 4, 16), ws)      # A must have M rows
+    with pytest.raises(ValueError, match="operand"):
+        sq.sq_quantize_rowwise_i8_staged(x, 1, (0, 4, 4, 32), ws)      # cols must equal K
+    with pytest.raises(TypeError):
+        sq.sq_quantize_rowwise_i8_staged(x.to(torch.float64), 0, (0, 4, 4, 16), ws)
