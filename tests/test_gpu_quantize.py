@@ -141,6 +141,9 @@ FP8_CASES = [
     ("W 1024x1024 N(0,0.02)", (1024, 1024), 0.02),
     ("G 2048x4096 N(0,1e-3)", (2048, 4096), 1e-3),
     ("tail 1000003", (1000003,), 1.0),
+    # 65537 chunks of 1024 (every warp of a full grid takes 17-18) and a
+    # 112-element tail
+    ("full grid and tail 67110000", (67110000,), 1.0),
     ("tail 33", (33,), 1.0),
     ("one", (1,), 1.0),
 ]
