@@ -432,6 +432,17 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
                     }
                 }
             }
+            // One chunk (the whole K summed exactly in fp32): the sums keep the
+            // accumulator's bits, each an exact integer, and become int32 only
+            // where acc_out asks for one; C takes the float itself (+0 for a
+            // zero sum, as float(0) is).  The float-to-int conversions, a slow
+            // pipe, then stay off a one-wave kernel's exposed tail.  Several
+            // chunks: each is converted and added in int32.
+            const bool raw = nch == 1;
+            auto as_f = [&](int32_t v) {
+                return raw ? __fadd_rn(__int_as_float(v), 0.0f) : __int2float_rn(v);
+            };
+            auto as_i = [&](int32_t v) { return raw ? __float2int_rn(__int_as_float(v)) : v; };
             int32_t sums[NC][32];
 #pragma unroll
             for (int c = 0; c < NC; ++c)
@@ -446,16 +457,24 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
                 }
                 tc_fence_after();
                 const uint32_t tb = tmem_base + lane_off + ab * BN + colgrp * Cfg::EPI_COLS;
+                if (raw) {
+                    // every column of this warp in flight behind one wait
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
+                    for (int c = 0; c < NC; ++c)
+                        tmem_ld32(tb + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sums[c][0]));
+                    tmem_ld_wait();
+                } else {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t r[16];
-                        tmem_ld16(tb + c * 32 + h * 16, r);
-                        tmem_ld_wait();
+                    for (int c = 0; c < NC; ++c) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            sums[c][h * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t r[16];
+                            tmem_ld16(tb + c * 32 + h * 16, r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                sums[c][h * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+                        }
                     }
                 }
                 release(ab);
@@ -485,13 +504,14 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
                         const int4 a = *reinterpret_cast<const int4*>(stg + r * PITCH + 4 * j);
                         const int64_t o = static_cast<int64_t>(b) * p.strideC +
                                           static_cast<int64_t>(grow) * p.N + scol;
-                        if (p.acc_out) st_v4(p.acc_out + o, make_uint4(a.x, a.y, a.z, a.w));
+                        if (p.acc_out)
+                            st_v4(p.acc_out + o, make_uint4(as_i(a.x), as_i(a.y), as_i(a.z), as_i(a.w)));
                         if (Cf)
                             st_v4(Cf + o, make_uint4(
-                                __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.x), sr), s4.x)),
-                                __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.y), sr), s4.y)),
-                                __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.z), sr), s4.z)),
-                                __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(a.w), sr), s4.w))));
+                                __float_as_uint(__fmul_rn(__fmul_rn(as_f(a.x), sr), s4.x)),
+                                __float_as_uint(__fmul_rn(__fmul_rn(as_f(a.y), sr), s4.y)),
+                                __float_as_uint(__fmul_rn(__fmul_rn(as_f(a.z), sr), s4.z)),
+                                __float_as_uint(__fmul_rn(__fmul_rn(as_f(a.w), sr), s4.w))));
                     }
                 }
             } else if (row < p.M) {
@@ -518,13 +538,13 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
                             const int32_t a2 = sums[c][4 * v + 2], a3 = sums[c][4 * v + 3];
                             if (p.acc_out)
                                 st_v4(p.acc_out + obase + col0 + 4 * v,
-                                      make_uint4(a0, a1, a2, a3));
+                                      make_uint4(as_i(a0), as_i(a1), as_i(a2), as_i(a3)));
                             if (Cf) {
                                 float4 o;
-                                o.x = __fmul_rn(__fmul_rn(__int2float_rn(a0), sArow), s4.x);
-                                o.y = __fmul_rn(__fmul_rn(__int2float_rn(a1), sArow), s4.y);
-                                o.z = __fmul_rn(__fmul_rn(__int2float_rn(a2), sArow), s4.z);
-                                o.w = __fmul_rn(__fmul_rn(__int2float_rn(a3), sArow), s4.w);
+                                o.x = __fmul_rn(__fmul_rn(as_f(a0), sArow), s4.x);
+                                o.y = __fmul_rn(__fmul_rn(as_f(a1), sArow), s4.y);
+                                o.z = __fmul_rn(__fmul_rn(as_f(a2), sArow), s4.z);
+                                o.w = __fmul_rn(__fmul_rn(as_f(a3), sArow), s4.w);
                                 st_v4(Cf + obase + col0 + 4 * v,
                                       make_uint4(__float_as_uint(o.x), __float_as_uint(o.y),
                                                  __float_as_uint(o.z), __float_as_uint(o.w)));
@@ -535,11 +555,10 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
                         for (int i = 0; i < 32; ++i) {
                             const int col = col0 + i;
                             if (col < p.N) {
-                                if (p.acc_out) p.acc_out[obase + col] = sums[c][i];
+                                if (p.acc_out) p.acc_out[obase + col] = as_i(sums[c][i]);
                                 if (Cf)
-                                    Cf[obase + col] = __fmul_rn(
-                                        __fmul_rn(__int2float_rn(sums[c][i]), sArow),
-                                        sBb[col / p.gb]);
+                                    Cf[obase + col] = __fmul_rn(__fmul_rn(as_f(sums[c][i]), sArow),
+                                                                sBb[col / p.gb]);
                             }
                         }
                     }

@@ -58,7 +58,7 @@ def test_i8_gemm_parity(name, sa_shape, sb_shape):
     oacc, oC = oracle.gemm_i8(qa, qb, sa, sb)
     C, acc = run_i8(qa, sa, qb, sb)
     assert np.array_equal(acc, oacc)
-    assert np.array_equal(C, oC)
+    assert np.array_equal(C.view(np.uint32), oC.view(np.uint32))
 
 
 def test_i8_gemm_per_head_batched():
@@ -205,6 +205,55 @@ def test_i8_quantize_staged_then_gemm(name, nb, sa_shape, sb_shape, kind):
                                             acc_out=True)
     assert np.array_equal(acc.cpu().numpy(), oacc)
     assert np.array_equal(C.cpu().numpy(), oC)
+    # C alone (the last tiles may leave through TMA boxes): the same bits
+    C_only, none = sq.sq_gemm_i8_rowscaled_staged(sa.reshape(-1), sb.reshape(-1), shape, ws)
+    assert none is None and torch.equal(C_only, C)
+
+
+C_ONLY = [
+    # (name, batch, M, N, K, scale groups of A and B or None for per row)
+    ("cfg1 128x512x1024", 0, 128, 512, 1024, None),
+    ("ragged 200x300x160", 0, 200, 300, 160, None),
+    ("per head 16x196x196x64", 16, 196, 196, 64, None),
+    ("ragged heads 3x130x132x256", 3, 130, 132, 256, None),
+    ("one round of 64 tiles 1024x1024x512", 0, 1024, 1024, 512, None),
+    ("groups 8 x 30 ragged 200x300x160", 0, 200, 300, 160, (8, 30)),
+]
+
+
+@pytest.mark.parametrize("name,nb,M,N,K,groups", C_ONLY, ids=[c[0] for c in C_ONLY])
+def test_i8_gemm_c_only_into_a_guarded_buffer(name, nb, M, N, K, groups):
+    """Only the fp32 C asked for, so no int32 accumulator is formed where one
+    K chunk holds the whole sum.  C matches the oracle bit for bit, including
+    the sign of zero where a row of zero codes meets a row of negative ones
+    (float(0) is +0), and nothing past it is written."""
+    s = seed_of(name)
+    shp_a, shp_b = ((nb, M, K), (nb, N, K)) if nb else ((M, K), (N, K))
+    a, b = synth.normal(s, shp_a), synth.student_t(s + 1, shp_b, df=3)
+    if groups:
+        qa, sa = oracle.quantize_grouped_i8(a, groups[0])
+        qb, sb = oracle.quantize_grouped_i8(b, groups[1])
+    else:
+        qa, sa = oracle.quantize_rowwise_i8(a)
+        qb, sb = oracle.quantize_rowwise_i8(b)
+    qa[..., :2, :] = 0
+    qb[..., :1, :] = -np.maximum(np.abs(qb[..., :1, :]), 1)
+    if groups:
+        _, oC = oracle.gemm_i8_grouped(qa, qb, sa, sb, groups[0], groups[1])
+    else:
+        _, oC = oracle.gemm_i8(qa, qb, sa, sb)
+    assert np.all(oC.view(np.uint32)[..., :2, :1] == 0)
+    ws = torch.empty(sq.gemm_i8_workspace_bytes(max(nb, 1), M, N, K), dtype=torch.uint8,
+                     device=DEV)
+    C, cbuf, n = guarded(oC.shape, torch.float32, -3.0)
+    if groups:
+        C2, acc = sq.sq_gemm_i8_grouped(to_dev(qa), to_dev(sa), groups[0], to_dev(qb), to_dev(sb),
+                                        groups[1], ws, C=C)
+    else:
+        C2, acc = sq.sq_gemm_i8_rowscaled(to_dev(qa), to_dev(sa), to_dev(qb), to_dev(sb), ws, C=C)
+    assert acc is None and C2.data_ptr() == C.data_ptr()
+    assert np.array_equal(C.cpu().numpy().view(np.uint32), oC.view(np.uint32))
+    assert guard_intact(cbuf, n, -3.0)
 
 
 # ------------------------------------------------------------------ FP8
