@@ -1162,7 +1162,15 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
     // spread over 128 x 128 tiles: measured 17-25% faster there, 6-10%
     // slower than 128 x 256 tiles once those fill a good part of the GPU.
     const int64_t wide_tiles = ((M + 127) / 128) * ((N + 255) / 256) * static_cast<int64_t>(batch);
-    if (wide_tiles < sms / 4) return gemm_i8_shape<128, false>(A16, B16, batch, M, N, K, p, st, sms);
+    if (wide_tiles < sms / 4) {
+        // When even 128 x 64 tiles make one round, take those: each CTA then
+        // streams half the B rows and stores half the outputs, which bound
+        // these few-CTA launches per SM, at the cost of reading A twice
+        // as often over twice the SMs.
+        const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128) * static_cast<int64_t>(batch);
+        if (2 * tiles <= sms) return gemm_i8_shape<64, false>(A16, B16, batch, M, N, K, p, st, sms);
+        return gemm_i8_shape<128, false>(A16, B16, batch, M, N, K, p, st, sms);
+    }
     return gemm_i8_shape<256, false>(A16, B16, batch, M, N, K, p, st, sms);
 }
 
