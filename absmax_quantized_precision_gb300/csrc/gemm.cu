@@ -103,8 +103,9 @@ struct GemmCfg {
     // exposed (5-7% faster on one-wave shapes), and on 256-wide tiles of
     // launches that run a single round of tiles (WIDE_EPI); 4 on 256-wide
     // tiles of longer launches, whose epilogue overlaps the next tile's MMAs
-    // (8 measured about 1% slower there).
-    static constexpr int EPI_WARPS = (I8 || BN == 128 || WIDE_EPI) ? 8 : 4;
+    // (8 measured about 1% slower there).  32-wide INT8 tiles take 4, one
+    // 32-column slice each.
+    static constexpr int EPI_WARPS = BN == 32 ? 4 : ((I8 || BN == 128 || WIDE_EPI) ? 8 : 4);
     static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int TMEM_COLS = 2 * BN;
@@ -1163,11 +1164,12 @@ cudaError_t launch_gemm_i8(const uint16_t* A16, const uint16_t* B16, const float
     // slower than 128 x 256 tiles once those fill a good part of the GPU.
     const int64_t wide_tiles = ((M + 127) / 128) * ((N + 255) / 256) * static_cast<int64_t>(batch);
     if (wide_tiles < sms / 4) {
-        // When even 128 x 64 tiles make one round, take those: each CTA then
-        // streams half the B rows and stores half the outputs, which bound
-        // these few-CTA launches per SM, at the cost of reading A twice
-        // as often over twice the SMs.
+        // When even 128 x 64 (or 128 x 32) tiles make one round, take those:
+        // each CTA then streams a half (a quarter) of the B rows and stores
+        // that share of the outputs, which bound these few-CTA launches per
+        // SM, at the cost of reading A more often over more SMs.
         const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128) * static_cast<int64_t>(batch);
+        if (4 * tiles <= sms) return gemm_i8_shape<32, false>(A16, B16, batch, M, N, K, p, st, sms);
         if (2 * tiles <= sms) return gemm_i8_shape<64, false>(A16, B16, batch, M, N, K, p, st, sms);
         return gemm_i8_shape<128, false>(A16, B16, batch, M, N, K, p, st, sms);
     }

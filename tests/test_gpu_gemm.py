@@ -627,8 +627,8 @@ def test_gemm_clock_probe_records_each_cta():
         torch.cuda.synchronize()
     finally:
         sq.sq_set_clock_probe()
-    # 8x8 tiles of 128 x 128; 4x10 tiles of 128 x 64
-    for rec, ctas in ((rec8, 64), (rec_i8, 40)):
+    # 8x8 tiles of 128 x 128; 4x20 tiles of 128 x 32
+    for rec, ctas in ((rec8, 64), (rec_i8, 80)):
         r = rec.view(-1, 4)
         used = r[r[:, 3] > 0]
         assert used.shape[0] == ctas
