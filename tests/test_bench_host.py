@@ -39,6 +39,6 @@ def test_fraction_far_above_peak_is_refused():
 
 
 def test_algorithmic_bytes_of_the_large_gemms():
-    # FP8: A8 + B8 + bf16 C; INT8: qa + qb + fp32 C (the survey's per-launch figures)
+    # FP8: A8 + B8 + bf16 C; INT8: qa + qb + fp32 C (codes read once, output written once)
     assert bench.algo_bytes("gemm_fp8_nt") == 469_762_048
     assert bench.algo_bytes("gemm_i8_kernel") == 738_197_504
