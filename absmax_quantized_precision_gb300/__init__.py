@@ -32,6 +32,7 @@ SQ_GRAD_INPUT, SQ_GRAD_WEIGHT, SQ_GRAD_BIAS = 1, 2, 4
 
 # every symbol include/sq.h declares
 EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "sq_quantize_fp8",
+           "sq_quantize_fp8_multi",
            "sq_gemm_i8_workspace_bytes", "sq_gemm_i8_rowscaled", "sq_gemm_fp8_scaled",
            "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc", "sq_quantize_fp8_ring",
            "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
@@ -70,6 +71,8 @@ def load_library():
     L.sq_quantize_rowwise_i8.restype = i32
     L.sq_quantize_fp8.argtypes = [vp, i64, vp, i32, vp, vp, vp, vp]
     L.sq_quantize_fp8.restype = i32
+    L.sq_quantize_fp8_multi.argtypes = [i32, vp, vp, vp, i32, vp, vp, vp, vp]
+    L.sq_quantize_fp8_multi.restype = i32
     L.sq_gemm_i8_workspace_bytes.argtypes = [i64, i64, i64, i64]
     L.sq_gemm_i8_workspace_bytes.restype = sz
     L.sq_gemm_i8_rowscaled.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, vp, vp,
@@ -289,6 +292,41 @@ def sq_quantize_fp8(x: torch.Tensor, scale: torch.Tensor, fmt: int, workspace: t
                                               _ptr(amax), _ptr(workspace), _stream(stream)),
                "sq_quantize_fp8")
     return x8, amax
+
+
+def sq_quantize_fp8_multi(xs, scales, fmt: int, workspace: torch.Tensor, x8s=None, amaxs=None,
+                          stream=None):
+    """sq_quantize_fp8 on 1-4 bf16 tensors in one launch, each with its own
+    step (1-element float32) and amax.  Returns (list of x8, list of amax)."""
+    xs, scales = list(xs), list(scales)
+    if not 1 <= len(xs) <= 4 or len(scales) != len(xs):
+        raise ValueError("1 to 4 tensors, one step each")
+    x8s = [None] * len(xs) if x8s is None else list(x8s)
+    amaxs = [None] * len(xs) if amaxs is None else list(amaxs)
+    if len(x8s) != len(xs) or len(amaxs) != len(xs):
+        raise ValueError("one output and one amax per tensor")
+    dev = _need_cuda(workspace, *xs, *scales, *[t for t in x8s + amaxs if t is not None])
+    if workspace.numel() * workspace.element_size() < workspace_bytes():
+        raise ValueError("workspace is smaller than sq_workspace_bytes()")
+    for t, (x, sc) in enumerate(zip(xs, scales)):
+        _need(x, torch.bfloat16, what=f"xs[{t}]")
+        _need(sc, torch.float32, numel=1, what=f"scales[{t}]")
+        if x8s[t] is None:
+            x8s[t] = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        _need(x8s[t], torch.uint8, numel=x.numel(), what=f"x8s[{t}]")
+        if amaxs[t] is None:
+            amaxs[t] = torch.empty(1, dtype=torch.float32, device=x.device)
+        _need(amaxs[t], torch.float32, numel=1, what=f"amaxs[{t}]")
+    n = len(xs)
+    P = ctypes.c_void_p * n
+    ptrs = lambda ts: P(*[_ptr(t) for t in ts])
+    numel = (ctypes.c_int64 * n)(*[x.numel() for x in xs])
+    with torch.cuda.device(dev):
+        _check(load_library().sq_quantize_fp8_multi(n, ptrs(xs), numel, ptrs(scales), int(fmt),
+                                                    ptrs(x8s), ptrs(amaxs), _ptr(workspace),
+                                                    _stream(stream)),
+               "sq_quantize_fp8_multi")
+    return x8s, amaxs
 
 
 def new_ring(hist_len: int, scale: float, device=None) -> torch.Tensor:

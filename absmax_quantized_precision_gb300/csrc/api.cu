@@ -105,6 +105,26 @@ sq_status sq_quantize_fp8(const uint16_t* x_bf16, int64_t numel, const float* sc
                                              ds->sms));
 }
 
+sq_status sq_quantize_fp8_multi(int count, const uint16_t* const* x_bf16, const int64_t* numel,
+                                const float* const* scale, int fmt, uint8_t* const* x8,
+                                float* const* amax, void* workspace, sq_stream stream) {
+    if (fmt != SQ_FMT_E4M3 && fmt != SQ_FMT_E5M2) return SQ_ERR_INVALID_ARG;
+    if (count < 1 || count > 4 || !x_bf16 || !numel || !scale || !x8 || !amax || !workspace)
+        return SQ_ERR_INVALID_ARG;
+    for (int t = 0; t < count; ++t) {
+        if (numel[t] < 0 || !scale[t] || !amax[t]) return SQ_ERR_INVALID_ARG;
+        if (numel[t] > 0 && (!x_bf16[t] || !x8[t])) return SQ_ERR_INVALID_ARG;
+        if (!aligned16(x_bf16[t]) || !aligned16(x8[t])) return SQ_ERR_ALIGNMENT;
+    }
+    if (!aligned16(workspace)) return SQ_ERR_ALIGNMENT;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    return from_cuda(sq::launch_quantize_fp8_multi(count, x_bf16, numel, scale, fmt, x8, amax,
+                                                   static_cast<unsigned*>(workspace), ds->err_word,
+                                                   reinterpret_cast<cudaStream_t>(stream), ds->sms));
+}
+
 sq_status sq_quantize_fp8_ring(const uint16_t* x_bf16, int64_t numel, int fmt, uint8_t* x8,
                                float* amax, float* ring, int64_t hist_len, int64_t idx, int margin,
                                void* workspace, sq_stream stream) {

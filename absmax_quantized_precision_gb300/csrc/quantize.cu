@@ -17,6 +17,9 @@
 // per-call memset: the last block also resets the two workspace words.
 #include <cuda_bf16.h>
 
+#include <cstdint>
+#include <cstring>
+
 #include "sq_device.cuh"
 #include "sq_host.h"
 #include "sq_launch.h"
@@ -687,13 +690,30 @@ constexpr int kFWarps = 24;
 constexpr int kFChunk = 1024;
 constexpr int kFStages = 2;
 constexpr int kFWarpBytes = kFStages * kFChunk * 2 + 2 * kFChunk;
+constexpr int kFMaxTensors = 4;   // tensors one launch quantizes
 constexpr int kQSmem = kFWarps * kFWarpBytes + kFWarps * kFStages * 8 + 128;
 
+// The tensors of one launch (1 to kFMaxTensors, each with its own step and
+// amax) and their chunks' place in the sequence the warps are dealt:
+// tensor t owns chunks [first[t], first[t + 1]); the unused entries of
+// `first` hold INT64_MAX, so that the owner of a chunk is a count of
+// comparisons.  Ring mode takes one tensor.
+struct Fp8Set {
+    const uint16_t* x[kFMaxTensors];
+    uint8_t* x8[kFMaxTensors];
+    const float* scale[kFMaxTensors];
+    float* amax[kFMaxTensors];
+    int64_t n[kFMaxTensors];
+    int64_t first[kFMaxTensors + 1];
+    int count;
+};
+
+// The workspace word that accumulates tensor t's amax bits (word 1 is the
+// ticket of plain mode).
+__device__ __forceinline__ int amax_word(int t) { return t == 0 ? 0 : t + 1; }
+
 template <int FMT>
-__global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t* __restrict__ x, int64_t n,
-                                                                 const float* __restrict__ scale,
-                                                                 uint8_t* __restrict__ x8,
-                                                                 float* __restrict__ amax_out,
+__global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_constant__ Fp8Set set,
                                                                  unsigned* __restrict__ ws, float* ring,
                                                                  int hist_len, int ring_idx, int margin,
                                                                  unsigned* err_word) {
@@ -706,18 +726,29 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
     uint8_t* out_buf = in_buf + kFStages * kFChunk * 2;        // 2 x 1 KB
     const int nwarps = static_cast<int>(blockDim.x >> 5);    // kFWarps, or fewer for small tensors
     uint64_t* full = reinterpret_cast<uint64_t*>(qsmem + nwarps * kFWarpBytes) + warp * kFStages;
-    __shared__ float red[kFWarps];
+    __shared__ float red[kFMaxTensors][kFWarps];
     __shared__ int is_last;
     __shared__ float s_amax;
     __shared__ int abort_flag;
 
     unsigned* counter = ring ? reinterpret_cast<unsigned*>(ring + hist_len + 1) : ws + 1;
-    float m = 0.0f;
+    // running max|x| per tensor
+    float m0 = 0.0f, m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
+    static_assert(kFMaxTensors == 4, "one running maximum per tensor below");
 
-    const int64_t nfull = n / kFChunk;
+    const int64_t nfull = set.first[set.count];
     const int64_t GW = static_cast<int64_t>(gridDim.x) * nwarps;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t count = gw < nfull ? (nfull - gw + GW - 1) / GW : 0;
+    // chunk c of the dealt sequence: its tensor, and its first element there
+    auto owner = [&](int64_t c) {
+        return static_cast<int>(c >= set.first[1]) + static_cast<int>(c >= set.first[2]) +
+               static_cast<int>(c >= set.first[3]);
+    };
+    auto src = [&](int64_t c) {
+        const int t = owner(c);
+        return set.x[t] + (c - set.first[t]) * kFChunk;
+    };
     if (threadIdx.x == 0) abort_flag = 0;
     if (lane == 0) {
         for (int k = 0; k < kFStages; ++k) mbar_init(&full[k], 1);
@@ -730,14 +761,19 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
     if (lane == 0) {
         for (int64_t k = 0; k < count && k < kFStages; ++k) {
             mbar_arrive_expect_tx(&full[k], kFChunk * 2);
-            bulk_load(in_buf + k * kFChunk * 2, x + (gw + k * GW) * kFChunk, kFChunk * 2, &full[k]);
+            bulk_load(in_buf + k * kFChunk * 2, src(gw + k * GW), kFChunk * 2, &full[k]);
         }
     }
-    // The step is read only now, so its memory latency overlaps that of the
-    // first chunks (bulk_load's memory clobber keeps the read below them).
-    const float s = scale ? *scale : ring[hist_len];
-    const float y = __frcp_rn(s);
-    const bool fast = s >= 0x1p-40f && s <= 0x1p40f;
+    // The steps are read only now, so their memory latency overlaps that of
+    // the first chunks (bulk_load's memory clobber keeps the reads below them).
+    float sv[kFMaxTensors], yv[kFMaxTensors];
+    bool fv[kFMaxTensors];
+#pragma unroll
+    for (int t = 0; t < kFMaxTensors; ++t) {
+        sv[t] = t < set.count ? (set.scale[t] ? *set.scale[t] : ring[hist_len]) : 1.0f;
+        yv[t] = __frcp_rn(sv[t]);
+        fv[t] = sv[t] >= 0x1p-40f && sv[t] <= 0x1p40f;
+    }
     int64_t i = 0;
     for (; i < count; ++i) {
         const int stage = static_cast<int>(i % kFStages);
@@ -750,30 +786,38 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();                          // orders lane 0's wait before the other lanes' reads
         if (!ok) break;
+        const int64_t c = gw + i * GW;
+        const int t = owner(c);
+        const float s = t == 0 ? sv[0] : t == 1 ? sv[1] : t == 2 ? sv[2] : sv[3];
+        const float y = t == 0 ? yv[0] : t == 1 ? yv[1] : t == 2 ? yv[2] : yv[3];
+        const bool fast = t == 0 ? fv[0] : t == 1 ? fv[1] : t == 2 ? fv[2] : fv[3];
         const uint8_t* in = in_buf + stage * kFChunk * 2;
         uint8_t* out = out_buf + ob * kFChunk;
         uint4 a[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) a[k] = *reinterpret_cast<const uint4*>(in + (k * 32 + lane) * 16);
+        float mc = 0.0f;
         if (fast) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint2*>(out + (k * 32 + lane) * 8) = fp8_encode8<FMT, true>(a[k], s, y, m);
+                *reinterpret_cast<uint2*>(out + (k * 32 + lane) * 8) = fp8_encode8<FMT, true>(a[k], s, y, mc);
         } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint2*>(out + (k * 32 + lane) * 8) = fp8_encode8<FMT, false>(a[k], s, y, m);
+                *reinterpret_cast<uint2*>(out + (k * 32 + lane) * 8) = fp8_encode8<FMT, false>(a[k], s, y, mc);
         }
+        m0 = t == 0 ? fmaxf(m0, mc) : m0;
+        m1 = t == 1 ? fmaxf(m1, mc) : m1;
+        m2 = t == 2 ? fmaxf(m2, mc) : m2;
+        m3 = t == 3 ? fmaxf(m3, mc) : m3;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            const int64_t c = gw + i * GW;
-            bulk_store(x8 + c * kFChunk, out, kFChunk);
+            bulk_store(set.x8[t] + (c - set.first[t]) * kFChunk, out, kFChunk);
             bulk_commit();
             if (i + kFStages < count) {
                 mbar_arrive_expect_tx(&full[stage], kFChunk * 2);
-                bulk_load(in_buf + stage * kFChunk * 2, x + (c + kFStages * GW) * kFChunk, kFChunk * 2,
-                          &full[stage]);
+                bulk_load(in_buf + stage * kFChunk * 2, src(c + kFStages * GW), kFChunk * 2, &full[stage]);
             }
         }
     }
@@ -785,40 +829,68 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
         }
         bulk_wait_all();
     }
-    // ragged tail, fewer than kFChunk elements: block 0
+    // ragged tails, fewer than kFChunk elements each: block 0
     if (blockIdx.x == 0) {
-        for (int64_t e = nfull * kFChunk + threadIdx.x; e < n; e += blockDim.x) {
-            const float f = __uint_as_float(static_cast<uint32_t>(x[e]) << 16);
-            m = fmaxf(m, fabsf(f));
-            const float t = fast ? fp8_quotient(f, s, y) : __fdiv_rn(f, s);
-            x8[e] = static_cast<uint8_t>(fp8x2<FMT>(t, 0.0f) & 0xFFu);
+#pragma unroll
+        for (int t = 0; t < kFMaxTensors; ++t) {
+            if (t >= set.count) break;
+            const uint16_t* x = set.x[t];
+            uint8_t* x8 = set.x8[t];
+            const float s = sv[t], y = yv[t];
+            const bool fast = fv[t];
+            float mt = 0.0f;
+            for (int64_t e = (set.n[t] / kFChunk) * kFChunk + threadIdx.x; e < set.n[t]; e += blockDim.x) {
+                const float f = __uint_as_float(static_cast<uint32_t>(x[e]) << 16);
+                mt = fmaxf(mt, fabsf(f));
+                const float q = fast ? fp8_quotient(f, s, y) : __fdiv_rn(f, s);
+                x8[e] = static_cast<uint8_t>(fp8x2<FMT>(q, 0.0f) & 0xFFu);
+            }
+            m0 = t == 0 ? fmaxf(m0, mt) : m0;
+            m1 = t == 1 ? fmaxf(m1, mt) : m1;
+            m2 = t == 2 ? fmaxf(m2, mt) : m2;
+            m3 = t == 3 ? fmaxf(m3, mt) : m3;
         }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    for (int o = 16; o > 0; o >>= 1) {
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+        m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+        m3 = fmaxf(m3, __shfl_xor_sync(0xffffffffu, m3, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red[0][threadIdx.x >> 5] = m0;
+        red[1][threadIdx.x >> 5] = m1;
+        red[2][threadIdx.x >> 5] = m2;
+        red[3][threadIdx.x >> 5] = m3;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        float bm = red[0];
-        for (int w = 1; w < nwarps; ++w) bm = fmaxf(bm, red[w]);
         // max|x| >= 0, so the float order equals the unsigned order of the
         // bits.  The ticket is an acquire-release add: its release orders this
-        // block's maximum before the ticket, and the last block's acquire
-        // orders its read of the combined maximum after every other block's
+        // block's maxima before the ticket, and the last block's acquire
+        // orders its read of the combined maxima after every other block's
         // release (all tickets are one chain of read-modify-writes).
-        red_max_relaxed_gpu(&ws[0], __float_as_uint(bm));
+        for (int t = 0; t < set.count; ++t) {
+            float bm = red[t][0];
+            for (int w = 1; w < nwarps; ++w) bm = fmaxf(bm, red[t][w]);
+            red_max_relaxed_gpu(&ws[amax_word(t)], __float_as_uint(bm));
+        }
         const unsigned ticket = atom_add_acq_rel_gpu(counter, 1u);
         is_last = (ticket == gridDim.x - 1);
     }
     __syncthreads();
     if (!is_last) return;          // uniform across the block
     if (threadIdx.x == 0) {
-        // every other block's maximum is visible (ordered by the ticket), and
-        // no block of this launch touches ws[0] any more: a read and a plain
-        // reset do what an exchange would, without waiting for it
-        s_amax = __uint_as_float(ld_relaxed_gpu(&ws[0]));
-        ws[0] = 0u;
-        *amax_out = s_amax;
+        // every other block's maxima are visible (ordered by the ticket), and
+        // no block of this launch touches the words any more: a read and a
+        // plain reset do what an exchange would, without waiting for it
+        for (int t = 0; t < set.count; ++t) {
+            const float a = __uint_as_float(ld_relaxed_gpu(&ws[amax_word(t)]));
+            ws[amax_word(t)] = 0u;
+            *set.amax[t] = a;
+            if (t == 0) s_amax = a;
+        }
     }
     if (ring) {
         __syncthreads();
@@ -828,10 +900,10 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
             wm = fmaxf(wm, j == ring_idx ? a : ring[j]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = wm;
+        if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = wm;
         __syncthreads();
         if (threadIdx.x == 0) {
-            for (int w = 0; w < nwarps; ++w) wm = fmaxf(wm, red[w]);
+            for (int w = 0; w < nwarps; ++w) wm = fmaxf(wm, red[0][w]);
             ring[ring_idx] = a;
             if (wm > 0.0f) {
                 const float fmax_v = FMT == 0 ? 448.0f : 57344.0f;
@@ -845,14 +917,13 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const uint16_t*
 }
 
 template <int FMT>
-static cudaError_t launch_fp8_fmt(const uint16_t* x, int64_t n, const float* scale, uint8_t* x8,
-                                  float* amax, unsigned* ws, float* ring, int hist_len,
+static cudaError_t launch_fp8_fmt(const Fp8Set& set, unsigned* ws, float* ring, int hist_len,
                                   int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
                                   int sms) {
     const cudaError_t attr =
         set_max_dynamic_smem(reinterpret_cast<const void*>(quant_fp8_kernel<FMT>), kQSmem);
     if (attr != cudaSuccess) return attr;
-    const int64_t nfull = n / kFChunk;
+    const int64_t nfull = set.first[set.count];
     // Small tensors (under one chunk per warp of a full grid) run CTAs of 8
     // warps, several per SM, which start faster than one 24-warp CTA per SM.
     const int warps = nfull < static_cast<int64_t>(sms) * kFWarps ? 8 : kFWarps;
@@ -862,19 +933,49 @@ static cudaError_t launch_fp8_fmt(const uint16_t* x, int64_t n, const float* sca
     const int64_t cap = static_cast<int64_t>(sms) * (warps == kFWarps ? 1 : 3);
     if (blocks > cap) blocks = cap;
     return launch_pdl(quant_fp8_kernel<FMT>, dim3(static_cast<unsigned>(blocks)), dim3(warps * 32),
-                      static_cast<size_t>(smem), st, 1u, x, n, scale, x8, amax, ws, ring, hist_len,
-                      ring_idx, margin, err_word);
+                      static_cast<size_t>(smem), st, 1u, set, ws, ring, hist_len, ring_idx, margin,
+                      err_word);
+}
+
+static Fp8Set make_set(int count, const uint16_t* const* x, const int64_t* n,
+                       const float* const* scale, uint8_t* const* x8, float* const* amax) {
+    Fp8Set set;
+    memset(&set, 0, sizeof(set));
+    set.count = count;
+    set.first[0] = 0;
+    for (int t = 0; t < kFMaxTensors; ++t) {
+        if (t < count) {
+            set.x[t] = x[t];
+            set.x8[t] = x8[t];
+            set.scale[t] = scale[t];
+            set.amax[t] = amax[t];
+            set.n[t] = n[t];
+            set.first[t + 1] = set.first[t] + n[t] / kFChunk;
+        } else {
+            set.first[t + 1] = INT64_MAX;
+        }
+    }
+    return set;
+}
+
+cudaError_t launch_quantize_fp8_multi(int count, const uint16_t* const* x, const int64_t* n,
+                                      const float* const* scale, int fmt, uint8_t* const* x8,
+                                      float* const* amax, unsigned* ws, unsigned* err_word,
+                                      cudaStream_t st, int sms) {
+    if (count < 1 || count > kFMaxTensors) return cudaErrorInvalidValue;
+    const Fp8Set set = make_set(count, x, n, scale, x8, amax);
+    if (fmt == 0) return launch_fp8_fmt<0>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
+    return launch_fp8_fmt<1>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
 }
 
 cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
                                 uint8_t* x8, float* amax, unsigned* ws, float* ring, int hist_len,
                                 int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
                                 int sms) {
+    const Fp8Set set = make_set(1, &x, &n, &scale, &x8, &amax);
     if (fmt == 0)
-        return launch_fp8_fmt<0>(x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin,
-                                 err_word, st, sms);
-    return launch_fp8_fmt<1>(x, n, scale, x8, amax, ws, ring, hist_len, ring_idx, margin, err_word,
-                             st, sms);
+        return launch_fp8_fmt<0>(set, ws, ring, hist_len, ring_idx, margin, err_word, st, sms);
+    return launch_fp8_fmt<1>(set, ws, ring, hist_len, ring_idx, margin, err_word, st, sms);
 }
 
 }  // namespace sq

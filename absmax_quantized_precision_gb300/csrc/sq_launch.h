@@ -36,6 +36,13 @@ cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale
                                 int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
                                 int sms);
 
+// Up to four tensors in one launch, each with its own step and amax; the
+// workspace words are shared (amax of tensor t in word 0 or t + 1).
+cudaError_t launch_quantize_fp8_multi(int count, const uint16_t* const* x, const int64_t* n,
+                                      const float* const* scale, int fmt, uint8_t* const* x8,
+                                      float* const* amax, unsigned* ws, unsigned* err_word,
+                                      cudaStream_t st, int sms);
+
 // Staging of the INT8 codes of both GEMM operands as exact fp16 values:
 // a16[b][r][k] = a[b*stride_a + r*K + k] (M rows per batch), likewise b16.
 // An operand that is contiguous and large takes the bulk pipeline, whose CTAs

@@ -430,6 +430,9 @@ def run_sq(args, rank, world, local_rank):
             if events is not None:
                 events[i].record(st)
         mark(0, stream)
+        # One launch per FP8 operand here: each saturates the GPU, and one
+        # launch of both (sq_quantize_fp8_multi, which the smaller workloads
+        # use) measured the same step time on this workload.
         sq.sq_quantize_fp8(xa, tsa, sq.SQ_FMT_E4M3, ws, x8=a8, amax=amax_a, stream=stream)
         mark(1, stream)
         sq.sq_quantize_fp8(xb, tsb, sq.SQ_FMT_E4M3, ws, x8=b8, amax=amax_b, stream=stream)
@@ -868,10 +871,10 @@ def config_ops(name, dev, sq, synth, oracle, bf16_dev, prev_scale):
         flops = 2.0 * 2048 * 1024 * 1024
         desc = ("FP8 E4M3 linear forward: X bf16 2048x1024 ~N(0,1), W bf16 1024x1024 "
                 "~N(0,0.02), delayed scales; Y = X W^T (NT), bf16 out")
-        ops = [("quant_fp8_X", "bytes", X.numel() * 3,
-                lambda: sq.sq_quantize_fp8(X, tsx, fmt, wsq, x8=x8, amax=ax)),
-               ("quant_fp8_W", "bytes", W.numel() * 3,
-                lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=aw)),
+        # X and W in one launch, each with its own step and amax
+        ops = [("quant_fp8_XW", "bytes", (X.numel() + W.numel()) * 3,
+                lambda: sq.sq_quantize_fp8_multi([X, W], [tsx, tsw], fmt, wsq, x8s=[x8, w8],
+                                                 amaxs=[ax, aw])),
                ("gemm_fp8_nt", "flops", flops,
                 lambda: sq.sq_gemm_fp8_scaled(x8, w8, tsx, tsw, fmt, sq.SQ_NT, C=Y))]
 
@@ -899,12 +902,10 @@ def config_ops(name, dev, sq, synth, oracle, bf16_dev, prev_scale):
     desc = ("FP8 E4M3 MLP backward (dim 1024, hidden 4096, 2048 tokens): G bf16 2048x4096 "
             "~N(0,1e-3), W bf16 4096x1024 ~N(0,0.02), X bf16 2048x1024 ~N(0,1); "
             "dX = G W (NN), dW = G^T X (TN), bf16 out")
-    ops = [("quant_fp8_G", "bytes", G.numel() * 3,
-            lambda: sq.sq_quantize_fp8(G, tsg, fmt, wsq, x8=g8, amax=am[0])),
-           ("quant_fp8_W", "bytes", W.numel() * 3,
-            lambda: sq.sq_quantize_fp8(W, tsw, fmt, wsq, x8=w8, amax=am[1])),
-           ("quant_fp8_X", "bytes", X.numel() * 3,
-            lambda: sq.sq_quantize_fp8(X, tsx, fmt, wsq, x8=x8, amax=am[2])),
+    # G, W and X in one launch, each with its own step and amax
+    ops = [("quant_fp8_GWX", "bytes", (G.numel() + W.numel() + X.numel()) * 3,
+            lambda: sq.sq_quantize_fp8_multi([G, W, X], [tsg, tsw, tsx], fmt, wsq,
+                                             x8s=[g8, w8, x8], amaxs=am)),
            ("gemm_fp8_dX_nn", "flops", 2.0 * T * H * D,
             lambda: sq.sq_gemm_fp8_scaled(g8, w8, tsg, tsw, fmt, sq.SQ_NN, C=dX)),
            ("gemm_fp8_dW_tn", "flops", 2.0 * T * H * D,

@@ -123,6 +123,28 @@ sq_status sq_quantize_fp8(const uint16_t* x_bf16, int64_t numel, const float* sc
                           uint8_t* x8, float* amax, void* workspace, sq_stream stream);
 
 /*
+ * sq_quantize_fp8 on several tensors in one launch  [P3 linear_forward_fp8 /
+ * linear_backward_fp8: each operand is quantized with its own step and its
+ * amax returned; one launch serves them all].
+ *
+ *   count        1 .. 4 tensors.
+ *   x_bf16[t], numel[t], scale[t], x8[t], amax[t]
+ *                tensor t's arguments as in sq_quantize_fp8: device pointers
+ *                (x and x8 16-byte aligned), passed in host arrays of count
+ *                entries that the call reads before it returns.
+ *   fmt          SQ_FMT_E4M3 or SQ_FMT_E5M2, for every tensor.
+ *   workspace    sq_workspace_bytes() bytes, zeroed once by the caller; every
+ *                completed call leaves it zero.
+ * Each tensor's codes and amax are those sq_quantize_fp8 gives it alone.
+ * Tensors must not overlap.  Errors: SQ_ERR_INVALID_ARG for a count outside
+ * 1 .. 4, a NULL array or entry, or a negative numel; SQ_ERR_ALIGNMENT as in
+ * sq_quantize_fp8.
+ */
+sq_status sq_quantize_fp8_multi(int count, const uint16_t* const* x_bf16, const int64_t* numel,
+                                const float* const* scale, int fmt, uint8_t* const* x8,
+                                float* const* amax, void* workspace, sq_stream stream);
+
+/*
  * Per-tensor FP8 quantization with delayed scaling kept in a history ring
  * [P3 linear_forward_fp8 / linear_backward_fp8 ring arguments; commit notes:
  * the quantize kernel finishes the ring in its last block, so the next

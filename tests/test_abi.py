@@ -63,6 +63,18 @@ def test_invalid_arguments_are_rejected_without_a_device(lib):
     p1 = ctypes.c_void_p(0x1001)
     p = ctypes.c_void_p(0x1000)
     assert lib.sq_quantize_fp8(p1, 16, p, 0, p, p, p, null) == sq.SQ_ERR_ALIGNMENT
+    # several tensors in one launch: count 1..4, entries as for one tensor
+    arr = (ctypes.c_void_p * 2)(p, p)
+    arr_mis = (ctypes.c_void_p * 2)(p, p1)
+    arr_null = (ctypes.c_void_p * 2)(p, null)
+    n2 = (ctypes.c_int64 * 2)(16, 16)
+    n_neg = (ctypes.c_int64 * 2)(16, -1)
+    assert lib.sq_quantize_fp8_multi(0, arr, n2, arr, 0, arr, arr, p, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_fp8_multi(5, arr, n2, arr, 0, arr, arr, p, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_fp8_multi(2, arr, n2, arr, 3, arr, arr, p, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_fp8_multi(2, arr, n_neg, arr, 0, arr, arr, p, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_fp8_multi(2, arr, n2, arr_null, 0, arr, arr, p, null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_fp8_multi(2, arr_mis, n2, arr, 0, arr, arr, p, null) == sq.SQ_ERR_ALIGNMENT
     # gemm: bad layout, K not a multiple of 16, K too long
     assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 9, 16, 16, 16, p, null) == sq.SQ_ERR_INVALID_ARG
     assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 0, 16, 16, 24, p, null) == sq.SQ_ERR_ALIGNMENT

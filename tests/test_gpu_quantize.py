@@ -164,6 +164,36 @@ def test_fp8_quantize_parity(name, shape, std, fmt):
     assert int(ws.sum().item()) == 0        # the last block reset the workspace
 
 
+MULTI = [
+    ("X 2048x1024 and W 1024x1024", [((2048, 1024), 1.0), ((1024, 1024), 0.02)]),
+    ("G, W, X of the MLP backward", [((2048, 4096), 1e-3), ((4096, 1024), 0.02), ((2048, 1024), 1.0)]),
+    ("four ragged, one empty", [((1000003,), 1.0), ((0,), 1.0), ((33,), 1.0), ((3, 5127), 2.0)]),
+    ("8192x8192 (full grid) and a 129-element tail", [((8192, 8192), 1.0), ((129,), 1.0)]),
+]
+
+
+@pytest.mark.parametrize("fmt", [sq.SQ_FMT_E4M3, sq.SQ_FMT_E5M2], ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("name,specs", MULTI, ids=[c[0] for c in MULTI])
+def test_fp8_multi_quantize_equals_one_call_per_tensor(name, specs, fmt):
+    """sq_quantize_fp8_multi: every tensor's codes and amax equal the
+    oracle's, whatever tensor its chunks follow in the launch, ragged tails
+    and empty tensors included, and the shared workspace ends zeroed."""
+    seed = zlib.crc32(name.encode()) % 1000 + 100
+    xs = [synth.normal(seed + 3 * i, shape, std=std, dtype=synth.BF16)
+          for i, (shape, std) in enumerate(specs)]
+    steps = [delayed_scale(seed + 3 * i, shape, std, fmt) if np.prod(shape) else np.float32(1.0)
+             for i, (shape, std) in enumerate(specs)]
+    ws = sq.new_workspace(DEV)
+    x8s, amaxs = sq.sq_quantize_fp8_multi(
+        [to_dev(x, bf16=True) for x in xs],
+        [torch.tensor([s], dtype=torch.float32, device=DEV) for s in steps], fmt, ws)
+    for x, s, x8, amax in zip(xs, steps, x8s, amaxs):
+        ox8, oamax = oracle.quantize_fp8(x, s, fmt)
+        assert np.array_equal(x8.cpu().numpy(), ox8)
+        assert amax.item() == float(oamax)
+    assert int(ws.sum().item()) == 0
+
+
 def test_fp8_saturation_and_repeated_calls():
     x = synth.student_t(31, (4096, 512), dtype=synth.BF16)
     ws = sq.new_workspace(DEV)
