@@ -32,7 +32,7 @@ SQ_GRAD_INPUT, SQ_GRAD_WEIGHT, SQ_GRAD_BIAS = 1, 2, 4
 
 # every symbol include/sq.h declares
 EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "sq_quantize_fp8",
-           "sq_quantize_fp8_multi",
+           "sq_quantize_fp8_multi", "sq_quantize_rowwise_i8_staged_pair",
            "sq_gemm_i8_workspace_bytes", "sq_gemm_i8_rowscaled", "sq_gemm_fp8_scaled",
            "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc", "sq_quantize_fp8_ring",
            "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
@@ -73,6 +73,9 @@ def load_library():
     L.sq_quantize_fp8.restype = i32
     L.sq_quantize_fp8_multi.argtypes = [i32, vp, vp, vp, i32, vp, vp, vp, vp]
     L.sq_quantize_fp8_multi.restype = i32
+    L.sq_quantize_rowwise_i8_staged_pair.argtypes = [vp, i64, vp, i64, i32, i64, i64, i64, i64, vp, vp,
+                                                     vp, vp, vp, sz, vp]
+    L.sq_quantize_rowwise_i8_staged_pair.restype = i32
     L.sq_gemm_i8_workspace_bytes.argtypes = [i64, i64, i64, i64]
     L.sq_gemm_i8_workspace_bytes.restype = sz
     L.sq_gemm_i8_rowscaled.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, vp, vp,
@@ -510,6 +513,53 @@ def sq_quantize_rowwise_i8_staged(x: torch.Tensor, operand: int, shape, workspac
             _ptr(x2), dt, rows, cols, ld, _ptr(q), _ptr(scales), int(operand), nb, M, N, K,
             _ptr(workspace), _ws_bytes(workspace), _stream(stream)), "sq_quantize_rowwise_i8_staged")
     return q, scales
+
+
+def sq_quantize_rowwise_i8_staged_pair(xa: torch.Tensor, xb: torch.Tensor, shape,
+                                       workspace: torch.Tensor, qa: torch.Tensor = None,
+                                       sa: torch.Tensor = None, qb: torch.Tensor = None,
+                                       sb: torch.Tensor = None, stream=None):
+    """sq_quantize_rowwise_i8_staged of A (xa) and B (xb) in one call (one
+    launch when both fit the register-resident kernel).  Returns
+    (qa, sa, qb, sb)."""
+    dev = _need_cuda(xa, xb, qa, sa, qb, sb, workspace)
+    if xa.dtype != xb.dtype:
+        raise TypeError("xa and xb must have the same dtype")
+    if xa.dtype == torch.float32:
+        dt = SQ_F32
+    elif xa.dtype == torch.bfloat16:
+        dt = SQ_BF16
+    else:
+        raise TypeError(f"x must be float32 or bfloat16, got {xa.dtype}")
+    nb, M, N, K = (int(v) for v in shape)
+    nb = max(nb, 1)
+    views = []
+    for x, rows, name in ((xa, nb * M, "A"), (xb, nb * N, "B")):
+        cols = x.shape[-1]
+        x2 = x.reshape(-1, cols) if x.dim() != 2 else x
+        if x2.numel() and x2.stride(-1) != 1:
+            raise ValueError("rows of x must be contiguous")
+        if x2.shape[0] != rows or cols != K:
+            raise ValueError(f"x {tuple(x.shape)} is not operand {name} of {shape}")
+        views.append((x2, x2.stride(0) if rows > 1 else cols))
+    if qa is None:
+        qa = torch.empty(xa.shape, dtype=torch.int8, device=xa.device)
+    if qb is None:
+        qb = torch.empty(xb.shape, dtype=torch.int8, device=xb.device)
+    if sa is None:
+        sa = torch.empty(xa.shape[:-1], dtype=torch.float32, device=xa.device)
+    if sb is None:
+        sb = torch.empty(xb.shape[:-1], dtype=torch.float32, device=xb.device)
+    _need(qa, torch.int8, numel=nb * M * K, what="qa")
+    _need(qb, torch.int8, numel=nb * N * K, what="qb")
+    _need(sa, torch.float32, numel=nb * M, what="sa")
+    _need(sb, torch.float32, numel=nb * N, what="sb")
+    (xa2, lda), (xb2, ldb) = views
+    with torch.cuda.device(dev):
+        _check(load_library().sq_quantize_rowwise_i8_staged_pair(
+            _ptr(xa2), lda, _ptr(xb2), ldb, dt, nb, M, N, K, _ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb),
+            _ptr(workspace), _ws_bytes(workspace), _stream(stream)), "sq_quantize_rowwise_i8_staged_pair")
+    return qa, sa, qb, sb
 
 
 def sq_gemm_i8_rowscaled_noalloc(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor,

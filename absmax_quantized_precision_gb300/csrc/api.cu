@@ -304,6 +304,28 @@ sq_status sq_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t rows, 
         ds->sms));
 }
 
+sq_status sq_quantize_rowwise_i8_staged_pair(const void* xa, int64_t lda, const void* xb, int64_t ldb,
+                                             int dtype, int64_t batch, int64_t M, int64_t N,
+                                             int64_t K, int8_t* qa, float* sa, int8_t* qb,
+                                             float* sb, void* workspace, size_t workspace_bytes,
+                                             sq_stream stream) {
+    if (dtype != SQ_F32 && dtype != SQ_BF16) return SQ_ERR_INVALID_ARG;
+    sq_status r = i8_check_common(batch, M, N, K, M * K, N * K, workspace, workspace_bytes);
+    if (r != SQ_OK) return r;
+    if (lda < K || ldb < K) return SQ_ERR_INVALID_ARG;
+    if (!xa || !qa || !sa || !xb || !qb || !sb) return SQ_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    const int64_t esz = dtype == SQ_F32 ? 4 : 2;
+    const bool vec_a = aligned16(xa) && aligned16(qa) && ((lda * esz) % 16 == 0) && (K % 16 == 0);
+    const bool vec_b = aligned16(xb) && aligned16(qb) && ((ldb * esz) % 16 == 0) && (K % 16 == 0);
+    const I8Workspace w = i8_workspace(workspace, batch, M, N, K);
+    return from_cuda(sq::launch_quantize_rowwise_i8_staged_pair(
+        xa, batch * M, lda, qa, sa, vec_a, w.A16, w.bound_a, xb, batch * N, ldb, qb, sb, vec_b,
+        w.B16, w.bound_b, dtype, K, ds->err_word, reinterpret_cast<cudaStream_t>(stream), ds->sms));
+}
+
 sq_status sq_gemm_i8_rowscaled(const int8_t* A, const float* sA, const int8_t* B, const float* sB,
                                int64_t batch, int64_t M, int64_t N, int64_t K, int64_t strideA,
                                int64_t strideB, int64_t strideC, float* C, int32_t* acc_out,

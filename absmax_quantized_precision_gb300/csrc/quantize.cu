@@ -180,15 +180,27 @@ struct Codes<uint16_t> {
 // STAGE: the codes are also written as exact fp16 values at q16 (rows
 // packed) for the INT8 GEMM, and the operand's bound region is marked as
 // holding no bound.
+// A second operand with the same row length may follow in the same launch
+// (rows2 > 0): its rows come after the first operand's in the deal.
+template <typename T>
+struct RowOperand {
+    const T* x;
+    int64_t rows, ld;
+    int8_t* q;
+    float* scales;
+    uint16_t* q16;
+    unsigned* bound;
+};
+
 template <typename T, int TPR, int VPT, bool STAGE>
-__global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x, int64_t rows,
-                                                        int64_t cols, int64_t ld,
-                                                        int8_t* __restrict__ q,
-                                                        float* __restrict__ scales,
-                                                        uint16_t* __restrict__ q16,
-                                                        unsigned* __restrict__ bound) {
+__global__ void __launch_bounds__(256) quant_row_i8_vec(const RowOperand<T> o1, const RowOperand<T> o2,
+                                                        int64_t cols) {
     pdl_begin();
-    if (STAGE && blockIdx.x == 0 && threadIdx.x == 0) *bound = 0u;
+    if (STAGE && blockIdx.x == 0 && threadIdx.x == 0) {
+        *o1.bound = 0u;
+        if (o2.rows > 0) *o2.bound = 0u;
+    }
+    const int64_t rows = o1.rows + o2.rows;
     constexpr int EPV = Elem<T>::kPerVec;
     constexpr int RPB = 256 / TPR;
     __shared__ float red[8];
@@ -197,8 +209,15 @@ __global__ void __launch_bounds__(256) quant_row_i8_vec(const T* __restrict__ x,
     const int64_t nvec = cols / EPV;
     for (int64_t row0 = static_cast<int64_t>(blockIdx.x) * RPB; row0 < rows;
          row0 += static_cast<int64_t>(gridDim.x) * RPB) {
-        const int64_t row = row0 + g;
-        const bool live = row < rows;
+        const int64_t rowd = row0 + g;   // in the deal: the first operand's rows, then the second's
+        const bool live = rowd < rows;
+        const bool second = rowd >= o1.rows;
+        const int64_t row = second ? rowd - o1.rows : rowd;
+        const T* x = second ? o2.x : o1.x;
+        const int64_t ld = second ? o2.ld : o1.ld;
+        int8_t* q = second ? o2.q : o1.q;
+        float* scales = second ? o2.scales : o1.scales;
+        uint16_t* q16 = second ? o2.q16 : o1.q16;
         uint4 raw[VPT];                 // the row stays packed: 4 registers per 16 bytes
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
@@ -414,34 +433,43 @@ __global__ void __launch_bounds__(256) quant_row_i8_stage_pf(const T* __restrict
 }
 
 template <typename T, int TPR, int VPT, bool STAGE>
-static cudaError_t launch_row_vec(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
-                                  float* scales, uint16_t* q16, unsigned* bound, cudaStream_t st,
-                                  int sms) {
+static cudaError_t launch_row_vec(const RowOperand<T>& o1, const RowOperand<T>& o2, int64_t cols,
+                                  cudaStream_t st, int sms) {
     constexpr int RPB = 256 / TPR;
-    int64_t blocks = (rows + RPB - 1) / RPB;
+    int64_t blocks = (o1.rows + o2.rows + RPB - 1) / RPB;
     const int64_t cap = static_cast<int64_t>(sms) * 64;
     if (blocks > cap) blocks = cap;
     return launch_pdl(quant_row_i8_vec<T, TPR, VPT, STAGE>, dim3(static_cast<unsigned>(blocks)), dim3(256),
-                      0, st, 1u, x, rows, cols, ld, q, scales, q16, bound);
+                      0, st, 1u, o1, o2, cols);
 }
 
-// The register-resident shapes by row length (nvec 16-byte vectors per row);
-// false if the row is too long for them.
+// The register-resident shapes by row length (nvec 16-byte vectors per row),
+// for one operand or two with the same row length (o2.rows > 0); false if
+// the row is too long for them.
 template <typename T, bool STAGE>
-static bool launch_row_vec_any(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
-                               float* scales, uint16_t* q16, unsigned* bound, cudaStream_t st,
-                               int sms, cudaError_t* e) {
+static bool launch_row_vec_any(const RowOperand<T>& o1, const RowOperand<T>& o2, int64_t cols,
+                               cudaStream_t st, int sms, cudaError_t* e) {
     const int64_t nvec = cols / Elem<T>::kPerVec;
-    if (nvec <= 16) *e = launch_row_vec<T, 16, 1, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
-    else if (nvec <= 32) *e = launch_row_vec<T, 32, 1, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
-    else if (nvec <= 64) *e = launch_row_vec<T, 32, 2, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
-    else if (nvec <= 128) *e = launch_row_vec<T, 32, 4, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
-    else if (nvec <= 256) *e = launch_row_vec<T, 32, 8, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
-    else if (nvec <= 512) *e = launch_row_vec<T, 256, 2, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
-    else if (nvec <= 1024) *e = launch_row_vec<T, 256, 4, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
-    else if (nvec <= 2048) *e = launch_row_vec<T, 256, 8, STAGE>(x, rows, cols, ld, q, scales, q16, bound, st, sms);
+    if (nvec <= 16) *e = launch_row_vec<T, 16, 1, STAGE>(o1, o2, cols, st, sms);
+    else if (nvec <= 32) *e = launch_row_vec<T, 32, 1, STAGE>(o1, o2, cols, st, sms);
+    else if (nvec <= 64) *e = launch_row_vec<T, 32, 2, STAGE>(o1, o2, cols, st, sms);
+    else if (nvec <= 128) *e = launch_row_vec<T, 32, 4, STAGE>(o1, o2, cols, st, sms);
+    else if (nvec <= 256) *e = launch_row_vec<T, 32, 8, STAGE>(o1, o2, cols, st, sms);
+    else if (nvec <= 512) *e = launch_row_vec<T, 256, 2, STAGE>(o1, o2, cols, st, sms);
+    else if (nvec <= 1024) *e = launch_row_vec<T, 256, 4, STAGE>(o1, o2, cols, st, sms);
+    else if (nvec <= 2048) *e = launch_row_vec<T, 256, 8, STAGE>(o1, o2, cols, st, sms);
     else return false;
     return true;
+}
+
+template <typename T>
+static bool launch_row_vec_one(const T* x, int64_t rows, int64_t cols, int64_t ld, int8_t* q,
+                               float* scales, uint16_t* q16, unsigned* bound, bool stage,
+                               cudaStream_t st, int sms, cudaError_t* e) {
+    const RowOperand<T> o1{x, rows, ld, q, scales, q16, bound};
+    const RowOperand<T> none{nullptr, 0, 0, nullptr, nullptr, nullptr, nullptr};
+    return stage ? launch_row_vec_any<T, true>(o1, none, cols, st, sms, e)
+                 : launch_row_vec_any<T, false>(o1, none, cols, st, sms, e);
 }
 
 template <typename T>
@@ -459,7 +487,7 @@ static cudaError_t launch_row(const T* x, int64_t rows, int64_t cols, int64_t ld
     }
     if (vec_ok) {
         cudaError_t e = cudaSuccess;
-        if (launch_row_vec_any<T, false>(x, rows, cols, ld, q, scales, nullptr, nullptr, st, sms, &e))
+        if (launch_row_vec_one<T>(x, rows, cols, ld, q, scales, nullptr, nullptr, false, st, sms, &e))
             return e;
     }
     int64_t blocks = rows;
@@ -479,14 +507,18 @@ cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, i
                                 err_word, st, sms);
 }
 
+// Whether the quantize-and-stage of `rows` rows takes the row pipeline.
+static bool stage_takes_pipeline(int dtype, int64_t rows, int64_t cols, bool vec_ok, int sms) {
+    const int64_t row_bytes = cols * (dtype == 0 ? 4 : 2);
+    return vec_ok && row_bytes >= 2048 && row_bytes <= kPfRowBytes && rows >= 2 * sms;
+}
+
 cudaError_t launch_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t rows,
                                               int64_t cols, int64_t ld, int8_t* q,
                                               float* scales, bool vec_ok, uint16_t* q16,
                                               unsigned* bound, unsigned* err_word,
                                               cudaStream_t st, int sms) {
-    const int64_t esz = dtype == 0 ? 4 : 2;
-    const int64_t row_bytes = cols * esz;
-    if (vec_ok && row_bytes >= 2048 && row_bytes <= kPfRowBytes && rows >= 2 * sms) {
+    if (stage_takes_pipeline(dtype, rows, cols, vec_ok, sms)) {
         int64_t blocks = rows;
         int64_t cap = static_cast<int64_t>(sms) * 6;
         if (cap > kBoundSlots - 1) cap = kBoundSlots - 1;
@@ -502,16 +534,47 @@ cudaError_t launch_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t 
     cudaError_t e = cudaSuccess;
     if (vec_ok) {
         const bool done = dtype == 0
-            ? launch_row_vec_any<float, true>(static_cast<const float*>(x), rows, cols, ld, q, scales,
-                                              q16, bound, st, sms, &e)
-            : launch_row_vec_any<uint16_t, true>(static_cast<const uint16_t*>(x), rows, cols, ld, q,
-                                                 scales, q16, bound, st, sms, &e);
+            ? launch_row_vec_one<float>(static_cast<const float*>(x), rows, cols, ld, q, scales, q16,
+                                        bound, true, st, sms, &e)
+            : launch_row_vec_one<uint16_t>(static_cast<const uint16_t*>(x), rows, cols, ld, q, scales,
+                                           q16, bound, true, st, sms, &e);
         if (done) return e;
     }
     // other shapes: the plain quantize, then the staging of its codes
     e = launch_quantize_rowwise_i8(x, dtype, rows, cols, ld, q, scales, vec_ok, err_word, st, sms);
     if (e != cudaSuccess) return e;
     return launch_i8_to_f16_one(q, 1, rows, cols, rows * cols, q16, bound, err_word, st, sms);
+}
+
+cudaError_t launch_quantize_rowwise_i8_staged_pair(const void* xa, int64_t rows_a, int64_t lda,
+                                                   int8_t* qa, float* sa, bool vec_ok_a,
+                                                   uint16_t* a16, unsigned* bound_a, const void* xb,
+                                                   int64_t rows_b, int64_t ldb, int8_t* qb, float* sb,
+                                                   bool vec_ok_b, uint16_t* b16, unsigned* bound_b,
+                                                   int dtype, int64_t cols, unsigned* err_word,
+                                                   cudaStream_t st, int sms) {
+    // both operands' rows in one launch of the register-resident kernel when
+    // each would take it alone; otherwise one launch (or two) per operand
+    if (vec_ok_a && vec_ok_b && !stage_takes_pipeline(dtype, rows_a, cols, true, sms) &&
+        !stage_takes_pipeline(dtype, rows_b, cols, true, sms)) {
+        cudaError_t e = cudaSuccess;
+        bool done;
+        if (dtype == 0) {
+            const RowOperand<float> oa{static_cast<const float*>(xa), rows_a, lda, qa, sa, a16, bound_a};
+            const RowOperand<float> ob{static_cast<const float*>(xb), rows_b, ldb, qb, sb, b16, bound_b};
+            done = launch_row_vec_any<float, true>(oa, ob, cols, st, sms, &e);
+        } else {
+            const RowOperand<uint16_t> oa{static_cast<const uint16_t*>(xa), rows_a, lda, qa, sa, a16, bound_a};
+            const RowOperand<uint16_t> ob{static_cast<const uint16_t*>(xb), rows_b, ldb, qb, sb, b16, bound_b};
+            done = launch_row_vec_any<uint16_t, true>(oa, ob, cols, st, sms, &e);
+        }
+        if (done) return e;
+    }
+    const cudaError_t e = launch_quantize_rowwise_i8_staged(xa, dtype, rows_a, cols, lda, qa, sa, vec_ok_a,
+                                                            a16, bound_a, err_word, st, sms);
+    if (e != cudaSuccess) return e;
+    return launch_quantize_rowwise_i8_staged(xb, dtype, rows_b, cols, ldb, qb, sb, vec_ok_b, b16,
+                                             bound_b, err_word, st, sms);
 }
 
 // ================================================================== INT8 row groups

@@ -73,6 +73,16 @@ cudaError_t launch_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t 
                                               unsigned* bound, unsigned* err_word,
                                               cudaStream_t st, int sms);
 
+// Both INT8 GEMM operands quantized and staged: one launch when both take the
+// register-resident kernel, else as two calls of the above.
+cudaError_t launch_quantize_rowwise_i8_staged_pair(const void* xa, int64_t rows_a, int64_t lda,
+                                                   int8_t* qa, float* sa, bool vec_ok_a,
+                                                   uint16_t* a16, unsigned* bound_a, const void* xb,
+                                                   int64_t rows_b, int64_t ldb, int8_t* qb, float* sb,
+                                                   bool vec_ok_b, uint16_t* b16, unsigned* bound_b,
+                                                   int dtype, int64_t cols, unsigned* err_word,
+                                                   cudaStream_t st, int sms);
+
 // 0 on success, a cudaError_t otherwise; CUDA_ERROR_* from tensor-map encoding
 // is reported as cudaErrorInvalidValue.
 // C is bf16 [M,N] when out_scale == nullptr, else E4M3 codes [M,N] with the

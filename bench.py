@@ -834,11 +834,11 @@ def config_ops(name, dev, sq, synth, oracle, bf16_dev, prev_scale):
         C = torch.empty((nb, Mi, Ni) if nb > 1 else (Mi, Ni), device=dev)
         flops = 2.0 * nb * Mi * Ni * Kk
         shape = (nb if A.dim() == 3 else 0, Mi, Ni, Kk)
-        # f32 in; int8 codes, their exact fp16 copy and the scales out
-        ops = [("quant_i8_A", "bytes", A.numel() * 7 + sa.numel() * 4,
-                lambda: sq.sq_quantize_rowwise_i8_staged(A, 0, shape, ws, q=qa, scales=sa)),
-               ("quant_i8_B", "bytes", B.numel() * 7 + sb.numel() * 4,
-                lambda: sq.sq_quantize_rowwise_i8_staged(B, 1, shape, ws, q=qb, scales=sb)),
+        # f32 in; int8 codes, their exact fp16 copy and the scales out; both
+        # operands in one call (one launch: their rows fit in registers)
+        ops = [("quant_i8_AB", "bytes", (A.numel() + B.numel()) * 7 + (sa.numel() + sb.numel()) * 4,
+                lambda: sq.sq_quantize_rowwise_i8_staged_pair(A, B, shape, ws, qa=qa, sa=sa, qb=qb,
+                                                              sb=sb)),
                ("gemm_i8_kernel", "flops", flops,
                 lambda: sq.sq_gemm_i8_rowscaled_staged(sa.reshape(-1), sb.reshape(-1), shape, ws,
                                                        C=C))]

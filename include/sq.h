@@ -252,6 +252,22 @@ sq_status sq_quantize_rowwise_i8_staged(const void* x, int dtype, int64_t rows, 
                                         sq_stream stream);
 
 /*
+ * sq_quantize_rowwise_i8_staged for both operands in one call: A (rows
+ * batch*M, row pitch lda elements) and B (rows batch*N, pitch ldb), both of
+ * dtype, rows of K elements.  The results are those of the two single calls
+ * (operand 0 then 1, same bits); when both operands' rows fit the
+ * register-resident kernel they are quantized by one launch.
+ *   qa, sa     [batch*M*K] codes and [batch*M] scales of A; qb, sb for B.
+ *   batch, M, N, K, workspace, workspace_bytes  as in sq_gemm_i8_rowscaled.
+ * Errors as in sq_quantize_rowwise_i8_staged.
+ */
+sq_status sq_quantize_rowwise_i8_staged_pair(const void* xa, int64_t lda, const void* xb, int64_t ldb,
+                                             int dtype, int64_t batch, int64_t M, int64_t N,
+                                             int64_t K, int8_t* qa, float* sa, int8_t* qb,
+                                             float* sb, void* workspace, size_t workspace_bytes,
+                                             sq_stream stream);
+
+/*
  * Row-group symmetric INT8 quantization  [P1 sc_matmul group_a / group_b
  * (row-group size) and per_tensor granularity; P2 formula, which is per
  * tensor].  Consecutive groups of group_rows rows share one scale:

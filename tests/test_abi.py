@@ -75,6 +75,13 @@ def test_invalid_arguments_are_rejected_without_a_device(lib):
     assert lib.sq_quantize_fp8_multi(2, arr, n_neg, arr, 0, arr, arr, p, null) == sq.SQ_ERR_INVALID_ARG
     assert lib.sq_quantize_fp8_multi(2, arr, n2, arr_null, 0, arr, arr, p, null) == sq.SQ_ERR_INVALID_ARG
     assert lib.sq_quantize_fp8_multi(2, arr_mis, n2, arr, 0, arr, arr, p, null) == sq.SQ_ERR_ALIGNMENT
+    # both INT8 operands quantized and staged: bad dtype, short pitch, missing output
+    assert lib.sq_quantize_rowwise_i8_staged_pair(p, 16, p, 16, 7, 1, 4, 4, 16, p, p, p, p, p, 1 << 20,
+                                                  null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_rowwise_i8_staged_pair(p, 8, p, 16, 0, 1, 4, 4, 16, p, p, p, p, p, 1 << 20,
+                                                  null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_quantize_rowwise_i8_staged_pair(p, 16, p, 16, 0, 1, 4, 4, 16, p, p, null, p, p,
+                                                  1 << 20, null) == sq.SQ_ERR_INVALID_ARG
     # gemm: bad layout, K not a multiple of 16, K too long
     assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 9, 16, 16, 16, p, null) == sq.SQ_ERR_INVALID_ARG
     assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 0, 16, 16, 24, p, null) == sq.SQ_ERR_ALIGNMENT

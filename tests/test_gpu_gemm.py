@@ -205,9 +205,18 @@ def test_i8_quantize_staged_then_gemm(name, nb, sa_shape, sb_shape, kind):
                                             acc_out=True)
     assert np.array_equal(acc.cpu().numpy(), oacc)
     assert np.array_equal(C.cpu().numpy(), oC)
-    # C alone (the last tiles may leave through TMA boxes): the same bits
+    # C alone: the same bits
     C_only, none = sq.sq_gemm_i8_rowscaled_staged(sa.reshape(-1), sb.reshape(-1), shape, ws)
     assert none is None and torch.equal(C_only, C)
+    # both operands in one call (one launch where both fit the register-
+    # resident kernel) into a fresh workspace: the same codes, scales and C
+    ws2 = torch.empty_like(ws)
+    qa2, sa2, qb2, sb2 = sq.sq_quantize_rowwise_i8_staged_pair(A, B, shape, ws2)
+    assert torch.equal(qa2, qa) and torch.equal(sa2, sa)
+    assert torch.equal(qb2, qb) and torch.equal(sb2, sb)
+    C2, acc2 = sq.sq_gemm_i8_rowscaled_staged(sa2.reshape(-1), sb2.reshape(-1), shape, ws2,
+                                              acc_out=True)
+    assert torch.equal(C2, C) and torch.equal(acc2, acc)
 
 
 C_ONLY = [
