@@ -775,7 +775,8 @@ struct Fp8Set {
 // ticket of plain mode).
 __device__ __forceinline__ int amax_word(int t) { return t == 0 ? 0 : t + 1; }
 
-template <int FMT>
+// MULTI = false: one tensor (set.count == 1), every chunk its own.
+template <int FMT, bool MULTI>
 __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_constant__ Fp8Set set,
                                                                  unsigned* __restrict__ ws, float* ring,
                                                                  int hist_len, int ring_idx, int margin,
@@ -805,6 +806,7 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
     const int64_t count = gw < nfull ? (nfull - gw + GW - 1) / GW : 0;
     // chunk c of the dealt sequence: its tensor, and its first element there
     auto owner = [&](int64_t c) {
+        if (!MULTI) return 0;
         return static_cast<int>(c >= set.first[1]) + static_cast<int>(c >= set.first[2]) +
                static_cast<int>(c >= set.first[3]);
     };
@@ -833,7 +835,8 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
     bool fv[kFMaxTensors];
 #pragma unroll
     for (int t = 0; t < kFMaxTensors; ++t) {
-        sv[t] = t < set.count ? (set.scale[t] ? *set.scale[t] : ring[hist_len]) : 1.0f;
+        sv[t] = (t == 0 || (MULTI && t < set.count)) ? (set.scale[t] ? *set.scale[t] : ring[hist_len])
+                                                     : 1.0f;
         yv[t] = __frcp_rn(sv[t]);
         fv[t] = sv[t] >= 0x1p-40f && sv[t] <= 0x1p40f;
     }
@@ -895,7 +898,7 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
     // ragged tails, fewer than kFChunk elements each: block 0
     if (blockIdx.x == 0) {
 #pragma unroll
-        for (int t = 0; t < kFMaxTensors; ++t) {
+        for (int t = 0; t < (MULTI ? kFMaxTensors : 1); ++t) {
             if (t >= set.count) break;
             const uint16_t* x = set.x[t];
             uint8_t* x8 = set.x8[t];
@@ -917,9 +920,11 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-        m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
-        m3 = fmaxf(m3, __shfl_xor_sync(0xffffffffu, m3, o));
+        if (MULTI) {
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+            m3 = fmaxf(m3, __shfl_xor_sync(0xffffffffu, m3, o));
+        }
     }
     if ((threadIdx.x & 31) == 0) {
         red[0][threadIdx.x >> 5] = m0;
@@ -979,12 +984,12 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
     if (threadIdx.x == 0) *counter = 0u;
 }
 
-template <int FMT>
+template <int FMT, bool MULTI>
 static cudaError_t launch_fp8_fmt(const Fp8Set& set, unsigned* ws, float* ring, int hist_len,
                                   int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
                                   int sms) {
     const cudaError_t attr =
-        set_max_dynamic_smem(reinterpret_cast<const void*>(quant_fp8_kernel<FMT>), kQSmem);
+        set_max_dynamic_smem(reinterpret_cast<const void*>(quant_fp8_kernel<FMT, MULTI>), kQSmem);
     if (attr != cudaSuccess) return attr;
     const int64_t nfull = set.first[set.count];
     // Small tensors (under one chunk per warp of a full grid) run CTAs of 8
@@ -995,7 +1000,7 @@ static cudaError_t launch_fp8_fmt(const Fp8Set& set, unsigned* ws, float* ring, 
     if (blocks < 1) blocks = 1;
     const int64_t cap = static_cast<int64_t>(sms) * (warps == kFWarps ? 1 : 3);
     if (blocks > cap) blocks = cap;
-    return launch_pdl(quant_fp8_kernel<FMT>, dim3(static_cast<unsigned>(blocks)), dim3(warps * 32),
+    return launch_pdl(quant_fp8_kernel<FMT, MULTI>, dim3(static_cast<unsigned>(blocks)), dim3(warps * 32),
                       static_cast<size_t>(smem), st, 1u, set, ws, ring, hist_len, ring_idx, margin,
                       err_word);
 }
@@ -1027,8 +1032,12 @@ cudaError_t launch_quantize_fp8_multi(int count, const uint16_t* const* x, const
                                       cudaStream_t st, int sms) {
     if (count < 1 || count > kFMaxTensors) return cudaErrorInvalidValue;
     const Fp8Set set = make_set(count, x, n, scale, x8, amax);
-    if (fmt == 0) return launch_fp8_fmt<0>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
-    return launch_fp8_fmt<1>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
+    if (count == 1) {
+        if (fmt == 0) return launch_fp8_fmt<0, false>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
+        return launch_fp8_fmt<1, false>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
+    }
+    if (fmt == 0) return launch_fp8_fmt<0, true>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
+    return launch_fp8_fmt<1, true>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
 }
 
 cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
@@ -1037,8 +1046,8 @@ cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale
                                 int sms) {
     const Fp8Set set = make_set(1, &x, &n, &scale, &x8, &amax);
     if (fmt == 0)
-        return launch_fp8_fmt<0>(set, ws, ring, hist_len, ring_idx, margin, err_word, st, sms);
-    return launch_fp8_fmt<1>(set, ws, ring, hist_len, ring_idx, margin, err_word, st, sms);
+        return launch_fp8_fmt<0, false>(set, ws, ring, hist_len, ring_idx, margin, err_word, st, sms);
+    return launch_fp8_fmt<1, false>(set, ws, ring, hist_len, ring_idx, margin, err_word, st, sms);
 }
 
 }  // namespace sq
