@@ -427,26 +427,52 @@ size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 // is first copied to `used`, because the quantize publishes the next step
 // into the ring's slot when it finishes.  Returns the step pointer that the
 // GEMM must read.
-sq_status quantize_operand(const uint16_t* x, int64_t n, const float* step, int fmt, uint8_t* x8,
-                           float* amax, float* ring, int64_t hist, int64_t idx, int margin,
-                           unsigned* qws, float* used, const float** step_for_gemm,
-                           unsigned* err_word, cudaStream_t st, int sms) {
+// An operand's step: given (step), or from its delayed-scaling ring.
+sq_status check_operand(const float* step, const float* ring, int64_t hist, int64_t idx, int margin) {
     if (!step && !ring) return SQ_ERR_INVALID_ARG;
     if (ring && (hist < 1 || hist > (int64_t(1) << 20) || idx < 0 || idx >= hist || margin < -64 ||
                  margin > 64 || (reinterpret_cast<uintptr_t>(ring) & 3u)))
         return SQ_ERR_INVALID_ARG;
-    const float* s = step;
-    if (!s) {
-        if (cudaMemcpyAsync(used, ring + hist, sizeof(float), cudaMemcpyDeviceToDevice, st) !=
-            cudaSuccess)
-            return SQ_ERR_CUDA;
-        s = used;
-    }
-    *step_for_gemm = s;
-    return from_cuda(sq::launch_quantize_fp8(x, n, s, fmt, x8, amax, qws, ring,
-                                             static_cast<int>(hist), static_cast<int>(idx), margin,
-                                             err_word, st, sms));
+    return SQ_OK;
 }
+
+// The operands of one linear call, quantized in one launch.  An operand
+// without a given step takes the one its ring holds; the kernel writes that
+// step into the operand's slot in the workspace, so the GEMM uses the step
+// the quantization used although the ring then publishes the next one.
+struct LinQuant {
+    int count = 0;
+    const uint16_t* x[4];
+    int64_t n[4];
+    const float* scale[4];
+    float* ring[4];
+    int hist[4], idx[4], margin[4];
+    float* used[4];
+    uint8_t* x8[4];
+    float* amax[4];
+
+    // the step the GEMM should use for the operand just added
+    const float* add(const uint16_t* xp, int64_t np, const float* step, float* rg, int64_t h,
+                     int64_t i, int mg, uint8_t* x8p, float* am, float* slot) {
+        const int t = count++;
+        x[t] = xp;
+        n[t] = np;
+        scale[t] = step;
+        ring[t] = rg;
+        hist[t] = static_cast<int>(h);
+        idx[t] = static_cast<int>(i);
+        margin[t] = mg;
+        used[t] = step ? nullptr : slot;
+        x8[t] = x8p;
+        amax[t] = am;
+        return step ? step : slot;
+    }
+
+    sq_status launch(int fmt, unsigned* qws, unsigned* err_word, cudaStream_t st, int sms) const {
+        return from_cuda(sq::launch_quantize_fp8_rings(count, x, n, scale, ring, hist, idx, margin,
+                                                       used, fmt, x8, amax, qws, err_word, st, sms));
+    }
+};
 
 }  // namespace
 
@@ -487,24 +513,29 @@ sq_status sq_linear_forward_fp8(const uint16_t* x, int64_t M, int64_t K, const v
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     unsigned* qws = reinterpret_cast<unsigned*>(wsb);
     float* bias32 = reinterpret_cast<float*>(wsb + 256);
-    const float* sx_g = nullptr;
-    const float* sw_g = nullptr;
-    sq_status r = quantize_operand(x, M * K, sx, fmt, x8, amax_x, x_ring, x_hist, x_idx, x_margin, qws,
-                                   reinterpret_cast<float*>(wsb + kLinStepX), &sx_g, ds->err_word, st, ds->sms);
+    sq_status r = check_operand(sx, x_ring, x_hist, x_idx, x_margin);
     if (r != SQ_OK) return r;
+    if (w_prequantized) {
+        if (!sw) return SQ_ERR_INVALID_ARG;
+    } else {
+        r = check_operand(sw, w_ring, w_hist, w_idx, w_margin);
+        if (r != SQ_OK) return r;
+    }
+    // x and (unless it comes quantized) w in one launch
+    LinQuant lq;
+    const float* sx_g = lq.add(x, M * K, sx, x_ring, x_hist, x_idx, x_margin, x8, amax_x,
+                               reinterpret_cast<float*>(wsb + kLinStepX));
+    const float* sw_g = sw;
     const uint8_t* wq = w8;
     if (w_prequantized) {
         wq = static_cast<const uint8_t*>(w);
-        if (!sw) return SQ_ERR_INVALID_ARG;
-        sw_g = sw;
         if (cudaMemsetAsync(amax_w, 0, sizeof(float), st) != cudaSuccess) return SQ_ERR_CUDA;
     } else {
-        r = quantize_operand(static_cast<const uint16_t*>(w), N * K, sw, fmt, w8, amax_w, w_ring,
-                             w_hist, w_idx, w_margin, qws,
-                             reinterpret_cast<float*>(wsb + kLinStepW), &sw_g, ds->err_word, st,
-                             ds->sms);
-        if (r != SQ_OK) return r;
+        sw_g = lq.add(static_cast<const uint16_t*>(w), N * K, sw, w_ring, w_hist, w_idx, w_margin,
+                      w8, amax_w, reinterpret_cast<float*>(wsb + kLinStepW));
     }
+    r = lq.launch(fmt, qws, ds->err_word, st, ds->sms);
+    if (r != SQ_OK) return r;
     const float* bias_f = nullptr;
     if (bias_kind != SQ_BIAS_NONE) {
         e = sq::launch_bias_to_f32(bias, bias_kind, fmt, bias_scale, N, bias32, st);
@@ -545,16 +576,20 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     unsigned* qws = reinterpret_cast<unsigned*>(wsb);
     float* partial = reinterpret_cast<float*>(wsb + 256 + align256(static_cast<size_t>(N) * 4));
-    // one quantization of the gradient, shared by both products
-    const float* sg_g = nullptr;
-    sq_status r = quantize_operand(g, T * N, sg, fmt, g8, amax_g, g_ring, g_hist, g_idx, g_margin,
-                                   qws, reinterpret_cast<float*>(wsb + kLinStepG), &sg_g,
-                                   ds->err_word, st, ds->sms);
+    sq_status r = check_operand(sg, g_ring, g_hist, g_idx, g_margin);
+    if (r != SQ_OK) return r;
+    // one quantization of the gradient, shared by both products, and the
+    // operands the asked-for products need, in one launch
+    LinQuant lq;
+    const float* sg_g = lq.add(g, T * N, sg, g_ring, g_hist, g_idx, g_margin, g8, amax_g,
+                               reinterpret_cast<float*>(wsb + kLinStepG));
+    if (want_gx)
+        lq.add(w, N * K, sw, nullptr, 0, 0, 0, w8, reinterpret_cast<float*>(wsb + kLinSinkW), nullptr);
+    if (want_gw)
+        lq.add(x, T * K, sx, nullptr, 0, 0, 0, x8, reinterpret_cast<float*>(wsb + kLinSinkX), nullptr);
+    r = lq.launch(fmt, qws, ds->err_word, st, ds->sms);
     if (r != SQ_OK) return r;
     if (want_gx) {
-        e = sq::launch_quantize_fp8(w, N * K, sw, fmt, w8, reinterpret_cast<float*>(wsb + kLinSinkW),
-                                    qws, nullptr, 0, 0, 0, ds->err_word, st, ds->sms);
-        if (e != cudaSuccess) return SQ_ERR_CUDA;
         // dX[T,K] = G[T,N] W[N,K]  (NN)
         e = sq::launch_gemm_fp8(g8, w8, sg_g, sw, fmt, SQ_NN, static_cast<int>(T),
                                 static_cast<int>(K), static_cast<int>(N), gx, nullptr, nullptr,
@@ -562,9 +597,6 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
         if (e != cudaSuccess) return SQ_ERR_CUDA;
     }
     if (want_gw) {
-        e = sq::launch_quantize_fp8(x, T * K, sx, fmt, x8, reinterpret_cast<float*>(wsb + kLinSinkX),
-                                    qws, nullptr, 0, 0, 0, ds->err_word, st, ds->sms);
-        if (e != cudaSuccess) return SQ_ERR_CUDA;
         // dW[N,K] = G^T[N,T] X[T,K]  (TN, G stored [T,N])
         e = sq::launch_gemm_fp8(g8, x8, sg_g, sx, fmt, SQ_TN, static_cast<int>(N),
                                 static_cast<int>(K), static_cast<int>(T), gw, nullptr, nullptr,

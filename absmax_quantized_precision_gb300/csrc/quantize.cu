@@ -736,15 +736,17 @@ __device__ __forceinline__ uint2 fp8_encode8(const uint4& a, float s, float y, f
 // warps of the grid.  The ragged tail (< one chunk) is done by block 0 with
 // plain loads and stores.
 //
-// Plain mode (ring == nullptr): the step is *scale; ws = [amax bits | ticket].
+// Plain mode (no ring): the step is *scale; ws = [amax bits of tensor 0 |
+// ticket | amax bits of tensors 1-3].
 // Ring mode: delayed scaling with ring = [hist (hist_len) | scale | counter]
 // (the AstrAI commit notes' scale ring): the step is *scale if given, else
-// ring[hist_len], the ticket counter is the ring's last word, and the last
-// block records the amax in hist[ring_idx], takes the max over the window and
-// publishes the next step fl32(fl32(max * 2^margin) / fmt_max) in
-// ring[hist_len] (kept as it was when the window max is 0) -- no extra
-// launch.  ws[0] still accumulates the amax bits.  Both modes leave their
-// counter and ws[0] at zero.
+// ring[hist_len], and the last block records the amax in hist[ring_idx],
+// takes the max over the window and publishes the next step
+// fl32(fl32(max * 2^margin) / fmt_max) in ring[hist_len] (kept as it was
+// when the window max is 0) -- no extra launch.  A launch of one tensor with
+// a ring takes the ring's counter word as its ticket; several tensors take
+// ws word 1, each with its own ring or none.  Every launch leaves its ticket
+// and the amax words at zero.
 // One CTA of 24 warps per SM, two 2 KB stages per warp: 96 KB of loads in
 // flight per SM.  Measured on GB300 against 8-32 warps per SM, 0.5-4 KB
 // chunks and 2-6 stages, this was the fastest shape for both operands of
@@ -760,7 +762,10 @@ constexpr int kQSmem = kFWarps * kFWarpBytes + kFWarps * kFStages * 8 + 128;
 // amax) and their chunks' place in the sequence the warps are dealt:
 // tensor t owns chunks [first[t], first[t + 1]); the unused entries of
 // `first` hold INT64_MAX, so that the owner of a chunk is a count of
-// comparisons.  Ring mode takes one tensor.
+// comparisons.  A tensor with a delayed-scaling ring (ring[t] non-null)
+// takes its step from the ring when scale[t] is null, and the last block
+// updates its ring; used[t] (nullable) receives the step the tensor used,
+// written by block 0.
 struct Fp8Set {
     const uint16_t* x[kFMaxTensors];
     uint8_t* x8[kFMaxTensors];
@@ -768,6 +773,9 @@ struct Fp8Set {
     float* amax[kFMaxTensors];
     int64_t n[kFMaxTensors];
     int64_t first[kFMaxTensors + 1];
+    float* ring[kFMaxTensors];
+    int hist[kFMaxTensors], ridx[kFMaxTensors], margin[kFMaxTensors];
+    float* used[kFMaxTensors];
     int count;
 };
 
@@ -778,9 +786,8 @@ __device__ __forceinline__ int amax_word(int t) { return t == 0 ? 0 : t + 1; }
 // MULTI = false: one tensor (set.count == 1), every chunk its own.
 template <int FMT, bool MULTI>
 __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_constant__ Fp8Set set,
-                                                                 unsigned* __restrict__ ws, float* ring,
-                                                                 int hist_len, int ring_idx, int margin,
-                                                                 unsigned* err_word) {
+                                                                 unsigned* __restrict__ ws,
+                                                                 unsigned* counter, unsigned* err_word) {
     extern __shared__ uint8_t qsmem_raw[];
     uint8_t* qsmem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(qsmem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -792,10 +799,8 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
     uint64_t* full = reinterpret_cast<uint64_t*>(qsmem + nwarps * kFWarpBytes) + warp * kFStages;
     __shared__ float red[kFMaxTensors][kFWarps];
     __shared__ int is_last;
-    __shared__ float s_amax;
+    __shared__ float s_amax[kFMaxTensors];
     __shared__ int abort_flag;
-
-    unsigned* counter = ring ? reinterpret_cast<unsigned*>(ring + hist_len + 1) : ws + 1;
     // running max|x| per tensor
     float m0 = 0.0f, m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
     static_assert(kFMaxTensors == 4, "one running maximum per tensor below");
@@ -835,10 +840,16 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
     bool fv[kFMaxTensors];
 #pragma unroll
     for (int t = 0; t < kFMaxTensors; ++t) {
-        sv[t] = (t == 0 || (MULTI && t < set.count)) ? (set.scale[t] ? *set.scale[t] : ring[hist_len])
-                                                     : 1.0f;
+        sv[t] = (t == 0 || (MULTI && t < set.count))
+                    ? (set.scale[t] ? *set.scale[t] : set.ring[t][set.hist[t]])
+                    : 1.0f;
         yv[t] = __frcp_rn(sv[t]);
         fv[t] = sv[t] >= 0x1p-40f && sv[t] <= 0x1p40f;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+#pragma unroll
+        for (int t = 0; t < kFMaxTensors; ++t)
+            if (t < set.count && set.used[t]) *set.used[t] = sv[t];
     }
     int64_t i = 0;
     for (; i < count; ++i) {
@@ -957,12 +968,18 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
             const float a = __uint_as_float(ld_relaxed_gpu(&ws[amax_word(t)]));
             ws[amax_word(t)] = 0u;
             *set.amax[t] = a;
-            if (t == 0) s_amax = a;
+            s_amax[t] = a;
         }
     }
-    if (ring) {
+    // delayed-scaling rings: hist[idx] = amax, the window's max, the next step
+#pragma unroll
+    for (int t = 0; t < (MULTI ? kFMaxTensors : 1); ++t) {
+        if (t >= set.count) break;
+        float* ring = set.ring[t];
+        if (!ring) continue;           // uniform across the block
+        const int hist_len = set.hist[t], ring_idx = set.ridx[t];
         __syncthreads();
-        const float a = s_amax;
+        const float a = s_amax[t];
         float wm = 0.0f;
         for (int j = threadIdx.x; j < hist_len; j += blockDim.x)
             wm = fmaxf(wm, j == ring_idx ? a : ring[j]);
@@ -975,7 +992,7 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
             ring[ring_idx] = a;
             if (wm > 0.0f) {
                 const float fmax_v = FMT == 0 ? 448.0f : 57344.0f;
-                ring[hist_len] = __fdiv_rn(ldexpf(wm, margin), fmax_v);
+                ring[hist_len] = __fdiv_rn(ldexpf(wm, set.margin[t]), fmax_v);
             }
         }
     }
@@ -985,9 +1002,8 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
 }
 
 template <int FMT, bool MULTI>
-static cudaError_t launch_fp8_fmt(const Fp8Set& set, unsigned* ws, float* ring, int hist_len,
-                                  int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
-                                  int sms) {
+static cudaError_t launch_fp8_fmt(const Fp8Set& set, unsigned* ws, unsigned* counter,
+                                  unsigned* err_word, cudaStream_t st, int sms) {
     const cudaError_t attr =
         set_max_dynamic_smem(reinterpret_cast<const void*>(quant_fp8_kernel<FMT, MULTI>), kQSmem);
     if (attr != cudaSuccess) return attr;
@@ -1001,8 +1017,7 @@ static cudaError_t launch_fp8_fmt(const Fp8Set& set, unsigned* ws, float* ring, 
     const int64_t cap = static_cast<int64_t>(sms) * (warps == kFWarps ? 1 : 3);
     if (blocks > cap) blocks = cap;
     return launch_pdl(quant_fp8_kernel<FMT, MULTI>, dim3(static_cast<unsigned>(blocks)), dim3(warps * 32),
-                      static_cast<size_t>(smem), st, 1u, set, ws, ring, hist_len, ring_idx, margin,
-                      err_word);
+                      static_cast<size_t>(smem), st, 1u, set, ws, counter, err_word);
 }
 
 static Fp8Set make_set(int count, const uint16_t* const* x, const int64_t* n,
@@ -1026,28 +1041,54 @@ static Fp8Set make_set(int count, const uint16_t* const* x, const int64_t* n,
     return set;
 }
 
+static cudaError_t launch_set(const Fp8Set& set, int fmt, unsigned* ws, unsigned* counter,
+                              unsigned* err_word, cudaStream_t st, int sms) {
+    if (set.count == 1) {
+        if (fmt == 0) return launch_fp8_fmt<0, false>(set, ws, counter, err_word, st, sms);
+        return launch_fp8_fmt<1, false>(set, ws, counter, err_word, st, sms);
+    }
+    if (fmt == 0) return launch_fp8_fmt<0, true>(set, ws, counter, err_word, st, sms);
+    return launch_fp8_fmt<1, true>(set, ws, counter, err_word, st, sms);
+}
+
 cudaError_t launch_quantize_fp8_multi(int count, const uint16_t* const* x, const int64_t* n,
                                       const float* const* scale, int fmt, uint8_t* const* x8,
                                       float* const* amax, unsigned* ws, unsigned* err_word,
                                       cudaStream_t st, int sms) {
+    return launch_quantize_fp8_rings(count, x, n, scale, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                     fmt, x8, amax, ws, err_word, st, sms);
+}
+
+cudaError_t launch_quantize_fp8_rings(int count, const uint16_t* const* x, const int64_t* n,
+                                      const float* const* scale, float* const* ring,
+                                      const int* hist, const int* idx, const int* margin,
+                                      float* const* used, int fmt, uint8_t* const* x8,
+                                      float* const* amax, unsigned* ws, unsigned* err_word,
+                                      cudaStream_t st, int sms) {
     if (count < 1 || count > kFMaxTensors) return cudaErrorInvalidValue;
-    const Fp8Set set = make_set(count, x, n, scale, x8, amax);
-    if (count == 1) {
-        if (fmt == 0) return launch_fp8_fmt<0, false>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
-        return launch_fp8_fmt<1, false>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
+    Fp8Set set = make_set(count, x, n, scale, x8, amax);
+    for (int t = 0; t < count; ++t) {
+        set.ring[t] = ring ? ring[t] : nullptr;
+        set.hist[t] = hist ? hist[t] : 0;
+        set.ridx[t] = idx ? idx[t] : 0;
+        set.margin[t] = margin ? margin[t] : 0;
+        set.used[t] = used ? used[t] : nullptr;
     }
-    if (fmt == 0) return launch_fp8_fmt<0, true>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
-    return launch_fp8_fmt<1, true>(set, ws, nullptr, 0, 0, 0, err_word, st, sms);
+    return launch_set(set, fmt, ws, ws + 1, err_word, st, sms);
 }
 
 cudaError_t launch_quantize_fp8(const uint16_t* x, int64_t n, const float* scale, int fmt,
                                 uint8_t* x8, float* amax, unsigned* ws, float* ring, int hist_len,
                                 int ring_idx, int margin, unsigned* err_word, cudaStream_t st,
                                 int sms) {
-    const Fp8Set set = make_set(1, &x, &n, &scale, &x8, &amax);
-    if (fmt == 0)
-        return launch_fp8_fmt<0, false>(set, ws, ring, hist_len, ring_idx, margin, err_word, st, sms);
-    return launch_fp8_fmt<1, false>(set, ws, ring, hist_len, ring_idx, margin, err_word, st, sms);
+    Fp8Set set = make_set(1, &x, &n, &scale, &x8, &amax);
+    set.ring[0] = ring;
+    set.hist[0] = hist_len;
+    set.ridx[0] = ring_idx;
+    set.margin[0] = margin;
+    // one tensor with a ring: the ticket is the ring's counter word
+    unsigned* counter = ring ? reinterpret_cast<unsigned*>(ring + hist_len + 1) : ws + 1;
+    return launch_set(set, fmt, ws, counter, err_word, st, sms);
 }
 
 }  // namespace sq

@@ -43,6 +43,16 @@ cudaError_t launch_quantize_fp8_multi(int count, const uint16_t* const* x, const
                                       float* const* amax, unsigned* ws, unsigned* err_word,
                                       cudaStream_t st, int sms);
 
+// The same with a delayed-scaling ring per tensor (ring[t] nullable; the step
+// comes from the ring when scale[t] is null) and, in used[t] (nullable), the
+// step each tensor used.  The ticket is workspace word 1.
+cudaError_t launch_quantize_fp8_rings(int count, const uint16_t* const* x, const int64_t* n,
+                                      const float* const* scale, float* const* ring,
+                                      const int* hist, const int* idx, const int* margin,
+                                      float* const* used, int fmt, uint8_t* const* x8,
+                                      float* const* amax, unsigned* ws, unsigned* err_word,
+                                      cudaStream_t st, int sms);
+
 // Staging of the INT8 codes of both GEMM operands as exact fp16 values:
 // a16[b][r][k] = a[b*stride_a + r*K + k] (M rows per batch), likewise b16.
 // An operand that is contiguous and large takes the bulk pipeline, whose CTAs
