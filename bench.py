@@ -92,8 +92,8 @@ def algo_bytes(kernel):
 # was taken from: when the sha256 of those sources no longer matches, the
 # bench reports traffic as null.
 PROFILED_TRAFFIC = {
-    "gemm_fp8_nt": {"bytes": 780238592, "sources_sha256": "fab267626690a6306e1f964617443c67b636c6f93b2e3de42eee9a27a88ea8a4"},
-    "gemm_i8_kernel": {"bytes": 2716727040, "sources_sha256": "fab267626690a6306e1f964617443c67b636c6f93b2e3de42eee9a27a88ea8a4"},
+    "gemm_fp8_nt": {"bytes": 788525824, "sources_sha256": "0eac820899b349a13395cc825034280120f43526bfa358f6bf2214574ddc6e57"},
+    "gemm_i8_kernel": {"bytes": 2731710720, "sources_sha256": "0eac820899b349a13395cc825034280120f43526bfa358f6bf2214574ddc6e57"},
 }
 TRAFFIC_SOURCES = ["absmax_quantized_precision_gb300/csrc/gemm.cu",
                    "absmax_quantized_precision_gb300/csrc/sq_device.cuh",
