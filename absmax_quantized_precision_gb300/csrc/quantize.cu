@@ -507,6 +507,9 @@ cudaError_t launch_quantize_rowwise_i8(const void* x, int dtype, int64_t rows, i
                                 err_word, st, sms);
 }
 
+// Inputs of both operands up to this size are quantized by one launch.
+constexpr int64_t kPairFusedMaxBytes = int64_t(16) << 20;
+
 // Whether the quantize-and-stage of `rows` rows takes the row pipeline.
 static bool stage_takes_pipeline(int dtype, int64_t rows, int64_t cols, bool vec_ok, int sms) {
     const int64_t row_bytes = cols * (dtype == 0 ? 4 : 2);
@@ -553,10 +556,15 @@ cudaError_t launch_quantize_rowwise_i8_staged_pair(const void* xa, int64_t rows_
                                                    bool vec_ok_b, uint16_t* b16, unsigned* bound_b,
                                                    int dtype, int64_t cols, unsigned* err_word,
                                                    cudaStream_t st, int sms) {
-    // both operands' rows in one launch of the register-resident kernel when
-    // each would take it alone; otherwise one launch (or two) per operand
-    if (vec_ok_a && vec_ok_b && !stage_takes_pipeline(dtype, rows_a, cols, true, sms) &&
-        !stage_takes_pipeline(dtype, rows_b, cols, true, sms)) {
+    // Both operands' rows in one launch of the register-resident kernel when
+    // each would take it alone, or when their inputs are small (the row
+    // pipeline pays off on large operands; on small ones a launch saved is
+    // worth more); otherwise one launch (or two) per operand.
+    const int64_t in_bytes = (rows_a + rows_b) * cols * (dtype == 0 ? 4 : 2);
+    if (vec_ok_a && vec_ok_b &&
+        ((!stage_takes_pipeline(dtype, rows_a, cols, true, sms) &&
+          !stage_takes_pipeline(dtype, rows_b, cols, true, sms)) ||
+         in_bytes <= kPairFusedMaxBytes)) {
         cudaError_t e = cudaSuccess;
         bool done;
         if (dtype == 0) {
