@@ -911,8 +911,13 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
             // gave up on a wait: let the loads already issued land before exiting
             for (int64_t j = i; j < count && j < i + kFStages; ++j)
                 mbar_wait_drain(&full[j % kFStages], static_cast<uint32_t>((j / kFStages) & 1));
+            bulk_wait_all();
+        } else {
+            // Only the stores' shared-memory reads are waited for: their
+            // global writes complete before the grid does, and nothing in
+            // this launch reads the codes.
+            bulk_wait_read<0>();
         }
-        bulk_wait_all();
     }
     // ragged tails, fewer than kFChunk elements each: block 0
     if (blockIdx.x == 0) {
@@ -971,36 +976,57 @@ __global__ void __launch_bounds__(kFWarps * 32) quant_fp8_kernel(const __grid_co
     if (threadIdx.x == 0) {
         // every other block's maxima are visible (ordered by the ticket), and
         // no block of this launch touches the words any more: a read and a
-        // plain reset do what an exchange would, without waiting for it
-        for (int t = 0; t < set.count; ++t) {
-            const float a = __uint_as_float(ld_relaxed_gpu(&ws[amax_word(t)]));
-            ws[amax_word(t)] = 0u;
-            *set.amax[t] = a;
-            s_amax[t] = a;
+        // plain reset do what an exchange would, without waiting for it.
+        // All words are read before any store, so the reads share one round
+        // trip.
+        constexpr int kT = MULTI ? kFMaxTensors : 1;
+        unsigned bits[kT];
+#pragma unroll
+        for (int t = 0; t < kT; ++t) bits[t] = t < set.count ? ld_relaxed_gpu(&ws[amax_word(t)]) : 0u;
+#pragma unroll
+        for (int t = 0; t < kT; ++t) {
+            if (t < set.count) {
+                const float a = __uint_as_float(bits[t]);
+                ws[amax_word(t)] = 0u;
+                *set.amax[t] = a;
+                s_amax[t] = a;
+            }
         }
     }
-    // delayed-scaling rings: hist[idx] = amax, the window's max, the next step
+    // delayed-scaling rings: hist[idx] = amax, the window's max, the next
+    // step; all rings at once, so that their reads share one round trip
+    constexpr int kR = MULTI ? kFMaxTensors : 1;
+    bool any_ring = false;
 #pragma unroll
-    for (int t = 0; t < (MULTI ? kFMaxTensors : 1); ++t) {
-        if (t >= set.count) break;
-        float* ring = set.ring[t];
-        if (!ring) continue;           // uniform across the block
-        const int hist_len = set.hist[t], ring_idx = set.ridx[t];
-        __syncthreads();
-        const float a = s_amax[t];
-        float wm = 0.0f;
-        for (int j = threadIdx.x; j < hist_len; j += blockDim.x)
-            wm = fmaxf(wm, j == ring_idx ? a : ring[j]);
+    for (int t = 0; t < kR; ++t) any_ring |= t < set.count && set.ring[t] != nullptr;
+    if (any_ring) {                    // uniform across the block
+        __syncthreads();               // s_amax
+        float wm[kR];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-        if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = wm;
+        for (int t = 0; t < kR; ++t) {
+            wm[t] = 0.0f;
+            if (t < set.count && set.ring[t]) {
+                const float a = s_amax[t];
+                for (int j = threadIdx.x; j < set.hist[t]; j += blockDim.x)
+                    wm[t] = fmaxf(wm[t], j == set.ridx[t] ? a : set.ring[t][j]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wm[t] = fmaxf(wm[t], __shfl_xor_sync(0xffffffffu, wm[t], o));
+            if ((threadIdx.x & 31) == 0) red[t][threadIdx.x >> 5] = wm[t];
+        }
         __syncthreads();
         if (threadIdx.x == 0) {
-            for (int w = 0; w < nwarps; ++w) wm = fmaxf(wm, red[0][w]);
-            ring[ring_idx] = a;
-            if (wm > 0.0f) {
-                const float fmax_v = FMT == 0 ? 448.0f : 57344.0f;
-                ring[hist_len] = __fdiv_rn(ldexpf(wm, set.margin[t]), fmax_v);
+#pragma unroll
+            for (int t = 0; t < kR; ++t) {
+                float* ring = set.ring[t];
+                if (t >= set.count || !ring) continue;
+                float m = red[t][0];
+                for (int w = 1; w < nwarps; ++w) m = fmaxf(m, red[t][w]);
+                ring[set.ridx[t]] = s_amax[t];
+                if (m > 0.0f) {
+                    const float fmax_v = FMT == 0 ? 448.0f : 57344.0f;
+                    ring[set.hist[t]] = __fdiv_rn(ldexpf(m, set.margin[t]), fmax_v);
+                }
             }
         }
     }
