@@ -11,6 +11,7 @@ Entry points (names as in the C ABI):
   sq_quantize_fp8         per-tensor FP8 E4M3/E5M2 with the amax fused in
   sq_gemm_i8_rowscaled    exact INT8 GEMM, fp32 = acc * sA[i] * sB[j]
   sq_gemm_fp8_scaled      FP8 GEMM, bf16 = acc * sa * sb, layouts NT/NN/TN
+  sq_gemm_fp8_scaled_pair two independent FP8 GEMMs in one call (e.g. dX and dW)
 """
 from __future__ import annotations
 
@@ -33,7 +34,7 @@ SQ_GRAD_INPUT, SQ_GRAD_WEIGHT, SQ_GRAD_BIAS = 1, 2, 4
 # every symbol include/sq.h declares
 EXPORTS = ("sq_status_string", "sq_workspace_bytes", "sq_quantize_rowwise_i8", "sq_quantize_fp8",
            "sq_quantize_fp8_multi", "sq_quantize_rowwise_i8_staged_pair",
-           "sq_gemm_i8_workspace_bytes", "sq_gemm_i8_rowscaled", "sq_gemm_fp8_scaled",
+           "sq_gemm_i8_workspace_bytes", "sq_gemm_i8_rowscaled", "sq_gemm_fp8_scaled", "sq_gemm_fp8_scaled_pair",
            "sq_get_last_device_error", "sq_gemm_i8_rowscaled_noalloc", "sq_quantize_fp8_ring",
            "sq_gemm_fp8_scaled_e4m3", "sq_quantize_grouped_i8_workspace_bytes",
            "sq_quantize_grouped_i8", "sq_gemm_i8_grouped", "sq_linear_workspace_bytes",
@@ -83,6 +84,9 @@ def load_library():
     L.sq_gemm_i8_rowscaled.restype = i32
     L.sq_gemm_fp8_scaled.argtypes = [vp, vp, vp, vp, i32, i32, i64, i64, i64, vp, vp]
     L.sq_gemm_fp8_scaled.restype = i32
+    # host arrays of two entries each
+    L.sq_gemm_fp8_scaled_pair.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
+    L.sq_gemm_fp8_scaled_pair.restype = i32
     L.sq_get_last_device_error.argtypes = [vp]
     L.sq_get_last_device_error.restype = i32
     L.sq_gemm_i8_rowscaled_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
@@ -601,6 +605,36 @@ def sq_gemm_fp8_scaled(A: torch.Tensor, B: torch.Tensor, sa: torch.Tensor, sb: t
                                                  int(layout), M, N, K, _ptr(C), _stream(stream)),
                "sq_gemm_fp8_scaled")
     return C
+
+
+def sq_gemm_fp8_scaled_pair(As, Bs, sas, sbs, fmt: int, layouts, Cs=None, stream=None):
+    """Two independent FP8 GEMMs in one call: problem i is
+    sq_gemm_fp8_scaled(As[i], Bs[i], sas[i], sbs[i], fmt, layouts[i], Cs[i])."""
+    if len(As) != 2 or len(Bs) != 2 or len(sas) != 2 or len(sbs) != 2 or len(layouts) != 2:
+        raise ValueError("two problems expected")
+    Cs = list(Cs) if Cs is not None else [None, None]
+    if len(Cs) != 2:
+        raise ValueError("two outputs expected")
+    dev = _need_cuda(*As, *Bs, *sas, *sbs, *[c for c in Cs if c is not None])
+    dims = []
+    for i in range(2):
+        M, N, K = _fp8_shape(As[i], Bs[i], layouts[i])
+        _need(sas[i], torch.float32, numel=1, what="sa")
+        _need(sbs[i], torch.float32, numel=1, what="sb")
+        if Cs[i] is None:
+            Cs[i] = torch.empty((M, N), dtype=torch.bfloat16, device=As[i].device)
+        _need(Cs[i], torch.bfloat16, shape=(M, N), what="C")
+        dims.append((M, N, K))
+    arr = ctypes.c_void_p * 2
+    i64x2 = ctypes.c_int64 * 2
+    with torch.cuda.device(dev):
+        _check(load_library().sq_gemm_fp8_scaled_pair(
+            arr(*[_ptr(t) for t in As]), arr(*[_ptr(t) for t in Bs]),
+            arr(*[_ptr(t) for t in sas]), arr(*[_ptr(t) for t in sbs]), int(fmt),
+            (ctypes.c_int * 2)(*[int(x) for x in layouts]), i64x2(*[d[0] for d in dims]),
+            i64x2(*[d[1] for d in dims]), i64x2(*[d[2] for d in dims]),
+            arr(*[_ptr(t) for t in Cs]), _stream(stream)), "sq_gemm_fp8_scaled_pair")
+    return Cs
 
 
 def sq_gemm_fp8_scaled_e4m3(A: torch.Tensor, B: torch.Tensor, sa: torch.Tensor, sb: torch.Tensor,

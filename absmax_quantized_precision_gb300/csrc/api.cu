@@ -374,9 +374,9 @@ sq_status sq_quantize_grouped_i8(const void* x, int dtype, int64_t rows, int64_t
 
 namespace {
 
-sq_status gemm_fp8_common(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
-                          int fmt, int layout, int64_t M, int64_t N, int64_t K, void* C,
-                          const float* out_scale, sq_stream stream) {
+// The argument checks of one scaled FP8 GEMM.
+sq_status check_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                         int fmt, int layout, int64_t M, int64_t N, int64_t K, const void* C) {
     if (fmt != SQ_FMT_E4M3 && fmt != SQ_FMT_E5M2) return SQ_ERR_INVALID_ARG;
     if (layout != SQ_NT && layout != SQ_NN && layout != SQ_TN) return SQ_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1) return SQ_ERR_INVALID_ARG;
@@ -388,6 +388,14 @@ sq_status gemm_fp8_common(const uint8_t* A, const uint8_t* B, const float* sa, c
     if (layout == SQ_NN && (K % 16 != 0 || N % 16 != 0)) return SQ_ERR_ALIGNMENT;
     if (layout == SQ_TN && (M % 16 != 0 || N % 16 != 0)) return SQ_ERR_ALIGNMENT;
     if (((M + 127) / 128) * ((N + 127) / 128) > kMaxDim) return SQ_ERR_UNSUPPORTED;
+    return SQ_OK;
+}
+
+sq_status gemm_fp8_common(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                          int fmt, int layout, int64_t M, int64_t N, int64_t K, void* C,
+                          const float* out_scale, sq_stream stream) {
+    const sq_status r = check_gemm_fp8(A, B, sa, sb, fmt, layout, M, N, K, C);
+    if (r != SQ_OK) return r;
     cudaError_t e = cudaSuccess;
     DeviceState* ds = device_state(&e);
     if (!ds) return from_cuda(e);
@@ -403,6 +411,43 @@ sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa
                              int fmt, int layout, int64_t M, int64_t N, int64_t K,
                              uint16_t* C_bf16, sq_stream stream) {
     return gemm_fp8_common(A, B, sa, sb, fmt, layout, M, N, K, C_bf16, nullptr, stream);
+}
+
+// Whether the byte ranges [p, p + a) and [q, q + b) meet.
+bool overlaps(const void* p, int64_t a, const void* q, int64_t b) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(p), y = reinterpret_cast<uintptr_t>(q);
+    return x < y + static_cast<uint64_t>(b) && y < x + static_cast<uint64_t>(a);
+}
+
+sq_status sq_gemm_fp8_scaled_pair(const uint8_t* const A[2], const uint8_t* const B[2],
+                                  const float* const sa[2], const float* const sb[2], int fmt,
+                                  const int layout[2], const int64_t M[2], const int64_t N[2],
+                                  const int64_t K[2], uint16_t* const C_bf16[2], sq_stream stream) {
+    if (!A || !B || !sa || !sb || !layout || !M || !N || !K || !C_bf16) return SQ_ERR_INVALID_ARG;
+    for (int i = 0; i < 2; ++i) {
+        const sq_status r = check_gemm_fp8(A[i], B[i], sa[i], sb[i], fmt, layout[i], M[i], N[i], K[i],
+                                           C_bf16[i]);
+        if (r != SQ_OK) return r;
+    }
+    // the problems run side by side: an output may meet no operand and not
+    // the other output
+    for (int i = 0; i < 2; ++i) {
+        const int j = 1 - i;
+        const int64_t c_bytes = M[i] * N[i] * 2;
+        if (overlaps(C_bf16[i], c_bytes, A[j], M[j] * K[j]) ||
+            overlaps(C_bf16[i], c_bytes, B[j], N[j] * K[j]) ||
+            overlaps(C_bf16[i], c_bytes, C_bf16[j], M[j] * N[j] * 2))
+            return SQ_ERR_INVALID_ARG;
+    }
+    cudaError_t e = cudaSuccess;
+    DeviceState* ds = device_state(&e);
+    if (!ds) return from_cuda(e);
+    sq::Fp8Problem q[2];
+    for (int i = 0; i < 2; ++i)
+        q[i] = sq::Fp8Problem{A[i], B[i], sa[i], sb[i], layout[i], static_cast<int>(M[i]),
+                              static_cast<int>(N[i]), static_cast<int>(K[i]), C_bf16[i]};
+    return from_cuda(sq::launch_gemm_fp8_pair(q, fmt, ds->err_word,
+                                              reinterpret_cast<cudaStream_t>(stream), ds->sms));
 }
 
 sq_status sq_gemm_fp8_scaled_e4m3(const uint8_t* A, const uint8_t* B, const float* sa,
@@ -589,14 +634,21 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
         lq.add(x, T * K, sx, nullptr, 0, 0, 0, x8, reinterpret_cast<float*>(wsb + kLinSinkX), nullptr);
     r = lq.launch(fmt, qws, ds->err_word, st, ds->sms);
     if (r != SQ_OK) return r;
-    if (want_gx) {
+    if (want_gx && want_gw) {
+        // dX[T,K] = G[T,N] W[N,K] (NN) and dW[N,K] = G^T[N,T] X[T,K] (TN, G
+        // stored [T,N]): independent products, dealt together
+        const sq::Fp8Problem q[2] = {
+            {g8, w8, sg_g, sw, SQ_NN, static_cast<int>(T), static_cast<int>(K), static_cast<int>(N), gx},
+            {g8, x8, sg_g, sx, SQ_TN, static_cast<int>(N), static_cast<int>(K), static_cast<int>(T), gw}};
+        e = sq::launch_gemm_fp8_pair(q, fmt, ds->err_word, st, ds->sms);
+        if (e != cudaSuccess) return SQ_ERR_CUDA;
+    } else if (want_gx) {
         // dX[T,K] = G[T,N] W[N,K]  (NN)
         e = sq::launch_gemm_fp8(g8, w8, sg_g, sw, fmt, SQ_NN, static_cast<int>(T),
                                 static_cast<int>(K), static_cast<int>(N), gx, nullptr, nullptr,
                                 ds->err_word, st, ds->sms);
         if (e != cudaSuccess) return SQ_ERR_CUDA;
-    }
-    if (want_gw) {
+    } else if (want_gw) {
         // dW[N,K] = G^T[N,T] X[T,K]  (TN, G stored [T,N])
         e = sq::launch_gemm_fp8(g8, x8, sg_g, sx, fmt, SQ_TN, static_cast<int>(N),
                                 static_cast<int>(K), static_cast<int>(T), gw, nullptr, nullptr,

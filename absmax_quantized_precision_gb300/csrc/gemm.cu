@@ -31,8 +31,10 @@
 #include <cuda_bf16.h>
 
 #include <atomic>
+#include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "sq_device.cuh"
 #include "sq_host.h"
@@ -81,6 +83,9 @@ struct GemmParams {
     // and at exit, [cycles0, cycles1, ns0, ns1], for CTAs below clk_cap
     unsigned long long* clk;
     int clk_cap;
+    // Grouped FP8 launches: this problem's operand layouts (1 = stored with M,
+    // or N, contiguous), which the other launches take from the template
+    int a_mn, b_mn;
 };
 
 // PAIR = false: one CTA per SM computes 128 x BN tiles (cta_group::1).
@@ -160,14 +165,29 @@ struct GemmCta {
     uint32_t rank;              // 0 = leader of the pair
     bool leader;
     int cta_unit, num_units;    // this CTA's (or pair's) index and their count
-    int total;                  // tiles in the problem
+    int total;                  // tiles in the launch
+    int total0;                 // grouped launches: tiles of the first problem (else total)
 };
+
+// The unit a CTA (or pair) takes in its r-th round of the tile loop.  Grouped
+// launches alternate the rounds' direction, so that the CTAs whose first unit
+// was a long tile of the first problem take the later rounds' units last.
+template <bool GRP>
+__device__ __forceinline__ int unit_of(int r, const GemmCta& c) {
+    return r * c.num_units + ((GRP && (r & 1)) ? c.num_units - 1 - c.cta_unit : c.cta_unit);
+}
+
+// The unit of round r, given t, the unit of round r - 1.
+template <bool GRP>
+__device__ __forceinline__ int next_unit(int t, int r, const GemmCta& c) {
+    return GRP ? unit_of<true>(r, c) : t + c.num_units;
+}
 
 // Warp 0: one elected thread streams the A and B boxes of every k-block of
 // this CTA's tiles into the ring of stages.
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
-__device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                              const GemmParams& p, const GemmCta& c) {
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI, bool GRP>
+__device__ __forceinline__ void gemm_producer(const CUtensorMap* tmAs, const CUtensorMap* tmBs,
+                                              const GemmParams* P, const GemmCta& c) {
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
     uint8_t* smem = c.smem;
     uint64_t* full = c.full;
@@ -175,7 +195,7 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
     volatile int* abort_flag = c.abort_flag;
     const uint32_t rank = c.rank;
     const bool leader = c.leader;
-    const int cta_unit = c.cta_unit, num_units = c.num_units, total = c.total;
+    const int total = c.total;
     if (elect_one_sync()) {
         int stage = 0;
         uint32_t phase = 0;
@@ -184,9 +204,15 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
         bool ok = true;
         bool first_round = true;   // the ring's stages are all free until it wraps
         bool waited = false;
-        for (int t = cta_unit; t < total && ok; t += num_units) {
+        for (int r = 0, t = c.cta_unit; t < total && ok; t = next_unit<GRP>(t, ++r, c)) {
+            const int pi = (GRP && t >= c.total0) ? 1 : 0;
+            const GemmParams& p = P[pi];
+            const CUtensorMap& tmA = tmAs[pi];
+            const CUtensorMap& tmB = tmBs[pi];
+            const bool a_mn = GRP ? p.a_mn != 0 : A_MN;
+            const bool b_mn = GRP ? p.b_mn != 0 : B_MN;
             int b, mb, nb;
-            tile_coords(t, p, b, mb, nb);
+            tile_coords(t - (pi ? c.total0 : 0), p, b, mb, nb);
             const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
             const int n0 = nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
             for (int kb = 0; kb < p.nkb; ++kb) {
@@ -210,9 +236,9 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
                         tma_load_3d_pair(sB, &tmB, fb, kx, n0, b);
                     } else {
                         const int kx = kb * kBKBytes;
-                        if (A_MN) tma_load_2d_pair(sA, &tmA, fb, m0, kx);
+                        if (a_mn) tma_load_2d_pair(sA, &tmA, fb, m0, kx);
                         else tma_load_2d_pair(sA, &tmA, fb, kx, m0);
-                        if (B_MN) {
+                        if (b_mn) {
 #pragma unroll
                             for (int j = 0; j < Cfg::B_ROWS / 128; ++j)
                                 tma_load_2d_pair(sB + j * Cfg::MN_LBO, &tmB, fb, n0 + j * 128, kx);
@@ -232,9 +258,9 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
                         tma_load_3d(sB, &tmB, &full[stage], kx, n0, b);
                     } else {
                         const int kx = kb * kBKBytes;
-                        if (A_MN) tma_load_2d(sA, &tmA, &full[stage], m0, kx);
+                        if (a_mn) tma_load_2d(sA, &tmA, &full[stage], m0, kx);
                         else tma_load_2d(sA, &tmA, &full[stage], kx, m0);
-                        if (B_MN) {
+                        if (b_mn) {
 #pragma unroll
                             for (int j = 0; j < Cfg::B_ROWS / 128; ++j)
                                 tma_load_2d(sB + j * Cfg::MN_LBO, &tmB, &full[stage], n0 + j * 128, kx);
@@ -262,8 +288,8 @@ __device__ __forceinline__ void gemm_producer(const CUtensorMap& tmA, const CUte
 // Warp 1: on the leader, one elected thread issues the MMAs of each k-block
 // into one of the two TMEM accumulators (kbpc k-blocks per accumulator
 // chunk, nch chunks per tile) and commits stages and accumulators.
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
-__device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, int kbpc, int nch) {
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI, bool GRP>
+__device__ __forceinline__ void gemm_mma(const GemmParams* P, const GemmCta& c, int kbpc, int nch) {
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
     uint8_t* smem = c.smem;
     uint64_t* full = c.full;
@@ -274,15 +300,21 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, 
     volatile int* abort_flag = c.abort_flag;
     const uint32_t tmem_base = c.tmem_base;
     const bool leader = c.leader;
-    const int cta_unit = c.cta_unit, num_units = c.num_units, total = c.total;
+    const int total = c.total;
     if (leader && elect_one_sync()) {
         int stage = 0;
         uint32_t phase = 0;
         uint32_t it = 0;
         bool ok = true;
         bool issued = false;
-        for (int t = cta_unit; t < total && ok; t += num_units) {
-            for (int ch = 0; ch < nch && ok; ++ch) {
+        for (int r = 0, t = c.cta_unit; t < total && ok; t = next_unit<GRP>(t, ++r, c)) {
+            const GemmParams& p = P[(GRP && t >= c.total0) ? 1 : 0];
+            const bool a_mn = GRP ? p.a_mn != 0 : A_MN;
+            const bool b_mn = GRP ? p.b_mn != 0 : B_MN;
+            // FP8 takes the whole K in one accumulator chunk
+            const int tkbpc = I8 ? kbpc : p.nkb;
+            const int tnch = I8 ? nch : 1;
+            for (int ch = 0; ch < tnch && ok; ++ch) {
                 const uint32_t ab = it & 1u;
                 const uint32_t aph = (it >> 1) & 1u;
                 if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, p.err_word)) {
@@ -291,8 +323,8 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, 
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * BN;
-                const int kb0 = ch * kbpc;
-                const int kb1 = min(p.nkb, kb0 + kbpc);
+                const int kb0 = ch * tkbpc;
+                const int kb1 = min(p.nkb, kb0 + tkbpc);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, p.err_word)) {
                         ok = false;
@@ -304,10 +336,10 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, 
 #pragma unroll
                     for (int kk = 0; kk < kBKBytes / 32; ++kk) {
                         const uint64_t ad =
-                            A_MN ? sdesc_sw128(a_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
+                            a_mn ? sdesc_sw128(a_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
                                  : sdesc_sw128(a_addr + kk * Cfg::KSTEP_K, 16, 1024);
                         const uint64_t bd =
-                            B_MN ? sdesc_sw128(b_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
+                            b_mn ? sdesc_sw128(b_addr + kk * Cfg::KSTEP_MN, Cfg::MN_LBO, 1024)
                                  : sdesc_sw128(b_addr + kk * Cfg::KSTEP_K, 16, 1024);
                         const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
                         if (PAIR) {
@@ -348,8 +380,8 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const GemmCta& c, 
 // precedes the TMEM release) as soon as it has read its last accumulator, so
 // that the barrier completes while it converts and stores; it returns whether
 // it has arrived.
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
-__device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const GemmParams& p,
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI, bool GRP>
+__device__ __forceinline__ bool gemm_epilogue(const CUtensorMap* tmCs, const GemmParams* P,
                                               const GemmCta& c, int nch) {
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
     const int warp = threadIdx.x >> 5;
@@ -362,7 +394,7 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
     const uint32_t tmem_base = c.tmem_base;
     const uint32_t rank = c.rank;
     const bool leader = c.leader;
-    const int cta_unit = c.cta_unit, num_units = c.num_units, total = c.total;
+    const int total = c.total;
     const int ew = warp - 2;
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int colgrp = ew >> 2;            // which EPI_COLS-wide column group
@@ -370,13 +402,18 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
     // where this warp reports that it has read an accumulator: the leader's barrier
     const uint32_t tempty_leader[2] = {PAIR ? cluster_addr(&tempty[0], 0) : 0u,
                                        PAIR ? cluster_addr(&tempty[1], 0) : 0u};
-    float fsa = 0.0f, fsb = 0.0f, fos = 1.0f, foy = 1.0f;
+    // FP8: each problem's two steps (grouped launches: bf16 outputs only)
+    float fsa2[2] = {0.0f, 0.0f}, fsb2[2] = {0.0f, 0.0f}, fos = 1.0f, foy = 1.0f;
     bool ofast = true;
     if (!I8) {
-        fsa = *p.sa;
-        fsb = *p.sb;
-        if (p.out_e4m3) {
-            fos = *p.out_scale;
+        fsa2[0] = *P[0].sa;
+        fsb2[0] = *P[0].sb;
+        if (GRP) {
+            fsa2[1] = *P[1].sa;
+            fsb2[1] = *P[1].sb;
+        }
+        if (P[0].out_e4m3) {
+            fos = *P[0].out_scale;
             foy = __frcp_rn(fos);
             ofast = fos >= 0x1p-40f && fos <= 0x1p40f;
         }
@@ -393,9 +430,14 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
             else mbar_arrive(&tempty[ab]);
         }
     };
-    for (int t = cta_unit; t < total && ok; t += num_units) {
+    for (int r = 0, t = c.cta_unit; t < total && ok; t = next_unit<GRP>(t, ++r, c)) {
+        const int pi = (GRP && t >= c.total0) ? 1 : 0;
+        const GemmParams& p = P[pi];
+        const CUtensorMap& tmC = tmCs[pi];
+        const float fsa = fsa2[pi], fsb = fsb2[pi];
+        const bool last = next_unit<GRP>(t, r + 1, c) >= total;   // this CTA's last tile
         int b, mb, nb;
-        tile_coords(t, p, b, mb, nb);
+        tile_coords(t - (pi ? c.total0 : 0), p, b, mb, nb);
         const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * kBM;
         const int n0 = nb * BN;
         const int row = m0 + quarter * 32 + lane;
@@ -414,7 +456,7 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
             constexpr int ROWS_STEP = 32 / F4_ROW;      // rows one warp-wide store covers
             static_assert(Cfg::EPI_WARPS * 32 * PITCH * 4 <= Cfg::STAGES * Cfg::STAGE,
                           "staged output fits in the operand stages");
-            const bool staged = p.vec_store && t + num_units >= total;
+            const bool staged = p.vec_store && last;
             const int scol = n0 + colgrp * Cfg::EPI_COLS + 4 * (lane % F4_ROW);
             const bool scol_ok = scol < p.N;   // N % 4 == 0: all four columns are in range
             float st_sa = 0.0f;
@@ -581,7 +623,7 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
             // one of its output boxes its own 2 KB there, and no box waits
             // for an earlier box's store to be read (on one-wave problems this
             // epilogue is the kernel's exposed tail).
-            const bool last_staged = p.tma_store && !p.out_e4m3 && t + num_units >= total;
+            const bool last_staged = p.tma_store && !p.out_e4m3 && last;
             static_assert(Cfg::EPI_WARPS * (Cfg::EPI_COLS / 32) * 2048 <= Cfg::STAGES * Cfg::STAGE,
                           "a last tile's output boxes fit in the operand stages");
             int box = 0;
@@ -678,7 +720,6 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
                     }
                 }
             };
-            const bool last = t + num_units >= total;
 #pragma unroll 1
             for (int c = 0; c < Cfg::EPI_COLS / 32; c += 2) {
                 // two TMEM loads in flight behind one wait
@@ -720,11 +761,15 @@ __device__ __forceinline__ bool gemm_epilogue(const CUtensorMap& tmC, const Gemm
     return arrived;
 }
 
-template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
-__global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+// The kernel body: P[0] (and on grouped launches P[1]) with their maps;
+// units [0, total0) are tiles of the first problem, [total0, total) of the
+// second.
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI, bool GRP>
+__device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                          const CUtensorMap* tmC, const GemmParams* P, int total0,
+                                          int total) {
     using Cfg = GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>;
+    const GemmParams& p = P[0];
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -764,9 +809,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::T
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-        if (!I8 && p.tma_store) tma_prefetch_desc(&tmC);
+#pragma unroll
+        for (int i = 0; i < (GRP ? 2 : 1); ++i) {
+            tma_prefetch_desc(&tmA[i]);
+            tma_prefetch_desc(&tmB[i]);
+            if (!I8 && P[i].tma_store) tma_prefetch_desc(&tmC[i]);
+        }
     }
     if (warp == 1) {
         if (PAIR) {
@@ -836,14 +884,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::T
         }
     }
 
-    const int total = p.mt * p.nt * p.batch;
-
     const GemmCta c{smem, epi_stage, full, empty, tfull, tempty, drain, abort_flag, tmem_base,
-                    rank, leader, cta_unit, num_units, total};
+                    rank, leader, cta_unit, num_units, total, total0};
     bool arrived = false;
-    if (warp == 0) gemm_producer<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>(tmA, tmB, p, c);
-    else if (warp == 1) gemm_mma<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>(p, c, kbpc, nch);
-    else arrived = gemm_epilogue<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>(tmC, p, c, nch);
+    if (warp == 0) gemm_producer<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI, GRP>(tmA, tmB, P, c);
+    else if (warp == 1) gemm_mma<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI, GRP>(P, c, kbpc, nch);
+    else arrived = gemm_epilogue<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI, GRP>(tmC, P, c, nch);
 
     tc_fence_before();
     if (PAIR && !arrived) {
@@ -876,6 +922,29 @@ __global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::T
         r[2] = ns0;
         r[3] = ns1;
     }
+}
+
+template <int BN, bool I8, bool A_MN, bool B_MN, bool PAIR, bool WIDE_EPI>
+__global__ void __launch_bounds__(GemmCfg<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI>::THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    const int total = p.mt * p.nt * p.batch;
+    gemm_body<BN, I8, A_MN, B_MN, PAIR, WIDE_EPI, false>(&tmA, &tmB, &tmC, &p, total, total);
+}
+
+// Two independent FP8 GEMMs (bf16 outputs) in one launch of single CTAs:
+// each problem keeps its own operand layouts, steps, output and raster.
+struct GemmGroup {
+    CUtensorMap tmA[2], tmB[2], tmC[2];
+    GemmParams p[2];
+    int total0, total;
+};
+
+template <int BN, bool WIDE_EPI>
+__global__ void __launch_bounds__(GemmCfg<BN, false, false, false, false, WIDE_EPI>::THREADS, 1)
+    gemm_tc_group_kernel(const __grid_constant__ GemmGroup g) {
+    gemm_body<BN, false, false, false, false, WIDE_EPI, true>(g.tmA, g.tmB, g.tmC, g.p, g.total0,
+                                                               g.total);
 }
 
 // ====================================================================== host
@@ -1005,32 +1074,43 @@ static Shape pick_shape(int64_t M, int64_t N, int64_t batch, int sms) {
     return Shape::Single128;
 }
 
+// One FP8 problem's operand maps (A in boxes of 128 rows; B in boxes of b_rows
+// rows, or of 128 columns when it is N-major) and, where its bf16 rows are
+// 16-byte multiples, the map of the 32 x 32 output boxes; sets p.mt, p.nt,
+// p.idesc and p.tma_store for tiles of tile_m x bn.
+static bool fp8_problem_maps(const uint8_t* A, const uint8_t* B, int M, int N, int K, bool a_mn,
+                             bool b_mn, int tile_m, int bn, int b_rows, int fmt, GemmParams& p,
+                             CUtensorMap* ta, CUtensorMap* tb, CUtensorMap* tc) {
+    bool ok;
+    if (a_mn) ok = encode_2d(ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, M, 128, kBKBytes);
+    else ok = encode_2d(ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, kBKBytes, kBM);
+    if (!ok) return false;
+    if (b_mn) ok = encode_2d(tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, N, K, N, 128, kBKBytes);
+    else ok = encode_2d(tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, kBKBytes, b_rows);
+    if (!ok) return false;
+    p.mt = (M + tile_m - 1) / tile_m;
+    p.nt = (N + bn - 1) / bn;
+    p.idesc = idesc_make(static_cast<uint32_t>(fmt), static_cast<uint32_t>(fmt), a_mn, b_mn,
+                         static_cast<uint32_t>(tile_m), static_cast<uint32_t>(bn));
+    memset(tc, 0, sizeof(*tc));
+    p.tma_store = 0;
+    if (!p.out_e4m3 && N % 8 == 0 && reinterpret_cast<uintptr_t>(p.C) % 16 == 0) {
+        if (!encode_2d(tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C, N, M, static_cast<uint64_t>(N) * 2,
+                       32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+            return false;
+        p.tma_store = 1;
+    }
+    return true;
+}
+
 template <bool A_MN, bool B_MN, int BN, bool PAIR>
 static cudaError_t gemm_fp8_shape(const uint8_t* A, const uint8_t* B, int M, int N, int K,
                                   GemmParams p, int fmt, cudaStream_t st, int sms) {
     using Cfg = GemmCfg<BN, false, A_MN, B_MN, PAIR, false>;   // tile geometry only
-    CUtensorMap ta, tb;
-    bool ok;
-    if (A_MN) ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, M, 128, kBKBytes);
-    else ok = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, kBKBytes, kBM);
-    if (!ok) return cudaErrorInvalidValue;
-    if (B_MN) ok = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, N, K, N, 128, kBKBytes);
-    else ok = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, kBKBytes, Cfg::B_ROWS);
-    if (!ok) return cudaErrorInvalidValue;
-    p.mt = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
-    p.nt = (N + BN - 1) / BN;
-    p.idesc = idesc_make(static_cast<uint32_t>(fmt), static_cast<uint32_t>(fmt), A_MN, B_MN,
-                         Cfg::TILE_M, BN);
-    // bf16 output leaves through 32 x 32 TMA boxes when its rows are 16-byte multiples
-    CUtensorMap tc;
-    memset(&tc, 0, sizeof(tc));
-    p.tma_store = 0;
-    if (!p.out_e4m3 && N % 8 == 0 && reinterpret_cast<uintptr_t>(p.C) % 16 == 0) {
-        if (!encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C, N, M, static_cast<uint64_t>(N) * 2,
-                       32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-            return cudaErrorInvalidValue;
-        p.tma_store = 1;
-    }
+    CUtensorMap ta, tb, tc;
+    if (!fp8_problem_maps(A, B, M, N, K, A_MN, B_MN, Cfg::TILE_M, BN, Cfg::B_ROWS, fmt, p, &ta, &tb,
+                          &tc))
+        return cudaErrorInvalidValue;
     // one round of 256-wide tiles leaves the epilogue exposed: give it 8 warps
     if (BN == 256 && static_cast<int64_t>(p.mt) * p.nt <= (PAIR ? sms / 2 : sms))
         return run_gemm<BN, false, A_MN, B_MN, PAIR, true>(ta, tb, tc, p, st, sms);
@@ -1047,7 +1127,7 @@ static cudaError_t gemm_fp8_shape(const uint8_t* A, const uint8_t* B, int M, int
 // longer exposed epilogue, measured on one-round launches: there 256 x 256
 // pairs lost to single CTAs despite the shorter K loop.  Ties go to the later
 // entry of the list.
-static Shape pick_shape_fp8(int64_t M, int64_t N, int64_t K, int sms) {
+static Shape pick_shape_fp8(int64_t M, int64_t N, int64_t K, int sms, int64_t* est = nullptr) {
     struct Cand { Shape s; int64_t tm, tn, slots, clk, fixed; };
     const Cand c[3] = {{Shape::Single256, 128, 256, sms, 784, 0},
                        {Shape::Single128, 128, 128, sms, 454, 0},
@@ -1064,6 +1144,7 @@ static Shape pick_shape_fp8(int64_t M, int64_t N, int64_t K, int sms) {
             best_t = t;
         }
     }
+    if (est) *est = best_t;
     return best;
 }
 
@@ -1103,6 +1184,102 @@ cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa,
     if (layout == 0) return gemm_fp8_layout<false, false>(A, B, M, N, K, p, fmt, st, sms);
     if (layout == 1) return gemm_fp8_layout<false, true>(A, B, M, N, K, p, fmt, st, sms);
     return gemm_fp8_layout<true, true>(A, B, M, N, K, p, fmt, st, sms);
+}
+
+// ------------------------------------------------------------- grouped FP8
+// Makespan, in clocks, of a grouped launch of tile_m x bn tiles: each tile of
+// problem i costs its k-blocks times clk_kb, and the units are dealt to
+// min(units, sms) CTAs in rounds of alternating direction, as unit_of deals
+// them.
+static int64_t group_makespan(const Fp8Problem* q, int bn, int64_t clk_kb, int sms) {
+    int64_t tiles[2], cost[2];
+    for (int i = 0; i < 2; ++i) {
+        tiles[i] = static_cast<int64_t>((q[i].M + kBM - 1) / kBM) * ((q[i].N + bn - 1) / bn);
+        cost[i] = static_cast<int64_t>((q[i].K + kBKBytes - 1) / kBKBytes) * clk_kb;
+    }
+    const int64_t total = tiles[0] + tiles[1];
+    const int64_t g = total < sms ? total : sms;
+    std::vector<int64_t> load(static_cast<size_t>(g), 0);
+    for (int64_t u = 0; u < total; ++u) {
+        const int64_t r = u / g, j = u % g;
+        load[static_cast<size_t>((r & 1) ? g - 1 - j : j)] += u < tiles[0] ? cost[0] : cost[1];
+    }
+    int64_t m = 0;
+    for (int64_t v : load) m = v > m ? v : m;
+    return m;
+}
+
+template <int BN, bool WIDE_EPI>
+static cudaError_t run_gemm_group(const Fp8Problem* q, int fmt, unsigned* err_word,
+                                  cudaStream_t st, int sms) {
+    using Cfg = GemmCfg<BN, false, false, false, false, WIDE_EPI>;
+    auto kern = gemm_tc_group_kernel<BN, WIDE_EPI>;
+    const cudaError_t attr = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), Cfg::SMEM);
+    if (attr != cudaSuccess) return attr;
+    GemmGroup g;
+    memset(&g, 0, sizeof(g));
+    ClockProbe* cp = current_probe();
+    for (int i = 0; i < 2; ++i) {
+        GemmParams& p = g.p[i];
+        p.M = q[i].M; p.N = q[i].N; p.K = q[i].K; p.batch = 1;
+        p.nkb = (q[i].K + kBKBytes - 1) / kBKBytes;
+        p.kb_per_chunk = p.nkb;
+        p.nchunks = 1;
+        p.sa = q[i].sa; p.sb = q[i].sb; p.C = q[i].C;
+        p.group_m = kGroupM;
+        p.ga = p.gb = 1;
+        p.Mg = q[i].M; p.Ng = q[i].N;
+        p.vec_store = (q[i].N % 8 == 0) && (reinterpret_cast<uintptr_t>(q[i].C) % 16 == 0);
+        p.err_word = err_word;
+        p.a_mn = q[i].layout == 2;
+        p.b_mn = q[i].layout != 0;
+        if (cp) {
+            p.clk = cp->fp8.load();
+            p.clk_cap = p.clk ? cp->cap.load() : 0;
+        }
+        if (!fp8_problem_maps(q[i].A, q[i].B, q[i].M, q[i].N, q[i].K, p.a_mn != 0, p.b_mn != 0, kBM,
+                              BN, BN, fmt, p, &g.tmA[i], &g.tmB[i], &g.tmC[i]))
+            return cudaErrorInvalidValue;
+    }
+    g.total0 = g.p[0].mt * g.p[0].nt;
+    g.total = g.total0 + g.p[1].mt * g.p[1].nt;
+    const int units = g.total < sms ? g.total : sms;
+    return launch_pdl(kern, dim3(units), dim3(Cfg::THREADS), Cfg::SMEM, st, 1u, g);
+}
+
+// Grouped when the estimate says one launch of both beats two launches: the
+// group's makespan (plus the last tile's exposed epilogue, ~0.9 us on 128-wide
+// tiles and ~1.7 us on 256-wide ones) against the two launches' estimates
+// plus the second launch's ramp (its CTAs start only as the first launch's
+// leave, then set up and wait for their first operands: ~2.5 us measured).
+// Only groups of at most four rounds of tiles are considered: larger
+// problems keep their own launches and CTA-pair tiles.
+cudaError_t launch_gemm_fp8_pair(const Fp8Problem* q, int fmt, unsigned* err_word, cudaStream_t st,
+                                 int sms) {
+    int64_t sep = 5000;
+    for (int i = 0; i < 2; ++i) {
+        int64_t e = 0;
+        pick_shape_fp8(q[i].M, q[i].N, q[i].K, sms, &e);
+        sep += e;
+    }
+    auto units = [&](int bn) {
+        int64_t u = 0;
+        for (int i = 0; i < 2; ++i)
+            u += static_cast<int64_t>((q[i].M + kBM - 1) / kBM) * ((q[i].N + bn - 1) / bn);
+        return u;
+    };
+    const int64_t cap = 4 * static_cast<int64_t>(sms);
+    const int64_t g128 = units(128) <= cap ? group_makespan(q, 128, 454, sms) + 1800 : INT64_MAX;
+    const int64_t g256 = units(256) <= cap ? group_makespan(q, 256, 784, sms) + 3400 : INT64_MAX;
+    if (g256 < sep && g256 <= g128) return run_gemm_group<256, true>(q, fmt, err_word, st, sms);
+    if (g128 < sep) return run_gemm_group<128, false>(q, fmt, err_word, st, sms);
+    for (int i = 0; i < 2; ++i) {
+        const cudaError_t e = launch_gemm_fp8(q[i].A, q[i].B, q[i].sa, q[i].sb, fmt, q[i].layout,
+                                              q[i].M, q[i].N, q[i].K, q[i].C, nullptr, nullptr,
+                                              err_word, st, sms);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int BN, bool PAIR>

@@ -102,6 +102,22 @@ cudaError_t launch_gemm_fp8(const uint8_t* A, const uint8_t* B, const float* sa,
                             const float* out_scale, const float* bias, unsigned* err_word,
                             cudaStream_t st, int sms);
 
+// One problem of a grouped FP8 launch (bf16 output, no bias).
+struct Fp8Problem {
+    const uint8_t* A;
+    const uint8_t* B;
+    const float* sa;
+    const float* sb;
+    int layout;           // 0 NT, 1 NN, 2 TN
+    int M, N, K;
+    void* C;
+};
+
+// Two independent FP8 GEMMs: one launch that deals both problems' tiles to
+// every SM when that is estimated faster, else two ordinary launches.
+cudaError_t launch_gemm_fp8_pair(const Fp8Problem* q, int fmt, unsigned* err_word, cudaStream_t st,
+                                 int sms);
+
 // Linear-layer helpers (linear.cu).
 // bias kind 1: bf16 [n] widened; kind 2: FP8 codes of fmt times *step.
 cudaError_t launch_bias_to_f32(const void* bias, int kind, int fmt, const float* step, int64_t n,

@@ -902,11 +902,16 @@ def config_ops(name, dev, sq, synth, oracle, bf16_dev, prev_scale):
     desc = ("FP8 E4M3 MLP backward (dim 1024, hidden 4096, 2048 tokens): G bf16 2048x4096 "
             "~N(0,1e-3), W bf16 4096x1024 ~N(0,0.02), X bf16 2048x1024 ~N(0,1); "
             "dX = G W (NN), dW = G^T X (TN), bf16 out")
-    # G, W and X in one launch, each with its own step and amax
+    # G, W and X in one launch, each with its own step and amax; then dX and
+    # dW in one call (one launch deals both products' tiles to every SM)
     ops = [("quant_fp8_GWX", "bytes", (G.numel() + W.numel() + X.numel()) * 3,
             lambda: sq.sq_quantize_fp8_multi([G, W, X], [tsg, tsw, tsx], fmt, wsq,
                                              x8s=[g8, w8, x8], amaxs=am)),
-           ("gemm_fp8_dX_nn", "flops", 2.0 * T * H * D,
+           ("gemm_fp8_dX_nn_dW_tn", "flops", 2 * (2.0 * T * H * D),
+            lambda: sq.sq_gemm_fp8_scaled_pair([g8, g8], [w8, x8], [tsg, tsg], [tsw, tsx], fmt,
+                                               [sq.SQ_NN, sq.SQ_TN], Cs=[dX, dW]))]
+    # each product as its own call, for comparison
+    alt = [("gemm_fp8_dX_nn", "flops", 2.0 * T * H * D,
             lambda: sq.sq_gemm_fp8_scaled(g8, w8, tsg, tsw, fmt, sq.SQ_NN, C=dX)),
            ("gemm_fp8_dW_tn", "flops", 2.0 * T * H * D,
             lambda: sq.sq_gemm_fp8_scaled(g8, x8, tsg, tsx, fmt, sq.SQ_TN, C=dW))]
@@ -917,7 +922,7 @@ def config_ops(name, dev, sq, synth, oracle, bf16_dev, prev_scale):
         ox8, _ = oracle.quantize_fp8(x, sx, 0)
         oracle.gemm_fp8(og8, ow8, 0, oracle.NN, sg, sw, want_bf16=False)
         oracle.gemm_fp8(og8, ox8, 0, oracle.TN, sg, sx, want_bf16=False)
-    return desc, ops, [], flops, oracle_work
+    return desc, ops, alt, flops, oracle_work
 
 
 def measure_config(name, args, with_cpu=True, compact=False):

@@ -317,6 +317,27 @@ sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa
                              int64_t K, uint16_t* C_bf16, sq_stream stream);
 
 /*
+ * Two independent scaled FP8 GEMMs in one call  [P3 custom::fp8_gemm; the
+ * commit notes' backward, where one quantized gradient G feeds dX = G W (NN)
+ * and dW = G^T X (TN)].  Problem i (i = 0, 1) computes exactly what
+ *   sq_gemm_fp8_scaled(A[i], B[i], sa[i], sb[i], fmt, layout[i], M[i], N[i],
+ *                      K[i], C_bf16[i], stream)
+ * computes, with the same arguments, limits and rounding; both share fmt.
+ *   A, B, sa, sb, layout, M, N, K, C_bf16   host arrays of two entries each
+ *                                            (the pointers in them are device
+ *                                            pointers).
+ * When the estimate says so, one launch deals the tiles of both problems to
+ * every SM (so that a small problem's SMs do not idle while the other runs);
+ * otherwise the two run as two launches on the stream.
+ * Errors: SQ_ERR_INVALID_ARG also when an output overlaps an operand or the
+ * output of the other problem (the problems may run side by side).
+ */
+sq_status sq_gemm_fp8_scaled_pair(const uint8_t* const A[2], const uint8_t* const B[2],
+                                  const float* const sa[2], const float* const sb[2], int fmt,
+                                  const int layout[2], const int64_t M[2], const int64_t N[2],
+                                  const int64_t K[2], uint16_t* const C_bf16[2], sq_stream stream);
+
+/*
  * Scaled FP8 GEMM with an FP8 E4M3 output  [P3 custom::fp8_gemm with
  * out_dtype = 1 and mm_fp8(out_dtype="e4m3"): the output is quantized to E4M3
  * with its own step out_scale, for layer-to-layer FP8 pipelines].

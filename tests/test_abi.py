@@ -82,6 +82,23 @@ def test_invalid_arguments_are_rejected_without_a_device(lib):
                                                   null) == sq.SQ_ERR_INVALID_ARG
     assert lib.sq_quantize_rowwise_i8_staged_pair(p, 16, p, 16, 0, 1, 4, 4, 16, p, p, null, p, p,
                                                   1 << 20, null) == sq.SQ_ERR_INVALID_ARG
+    # two GEMMs in one call: each problem checked as one GEMM, and an output
+    # may not meet the other problem's operands or output
+    def q(*vals, t=ctypes.c_void_p):
+        return (t * 2)(*vals)
+    PA, PB = q(0x10000, 0x20000), q(0x30000, 0x40000)
+    P16 = q(16, 16, t=ctypes.c_int64)
+    assert lib.sq_gemm_fp8_scaled_pair(PA, PB, PA, PB, 0, q(0, 9, t=ctypes.c_int), P16, P16, P16,
+                                       q(0x50000, 0x60000), null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_gemm_fp8_scaled_pair(PA, PB, PA, PB, 0, q(0, 0, t=ctypes.c_int), P16, P16,
+                                       q(16, 24, t=ctypes.c_int64), q(0x50000, 0x60000),
+                                       null) == sq.SQ_ERR_ALIGNMENT
+    assert lib.sq_gemm_fp8_scaled_pair(PA, PB, PA, PB, 0, q(0, 1, t=ctypes.c_int), P16, P16, P16,
+                                       q(0x50000, 0x10000), null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_gemm_fp8_scaled_pair(PA, PB, PA, PB, 0, q(0, 2, t=ctypes.c_int), P16, P16, P16,
+                                       q(0x50000, 0x50100), null) == sq.SQ_ERR_INVALID_ARG
+    assert lib.sq_gemm_fp8_scaled_pair(null, PB, PA, PB, 0, q(0, 0, t=ctypes.c_int), P16, P16, P16,
+                                       q(0x50000, 0x60000), null) == sq.SQ_ERR_INVALID_ARG
     # gemm: bad layout, K not a multiple of 16, K too long
     assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 9, 16, 16, 16, p, null) == sq.SQ_ERR_INVALID_ARG
     assert lib.sq_gemm_fp8_scaled(p, p, p, p, 0, 0, 16, 16, 24, p, null) == sq.SQ_ERR_ALIGNMENT

@@ -440,6 +440,107 @@ def test_fp8_backward_dx_nn_and_dw_tn():
     check_fp8(dW, g8, x8, fmt, sq.SQ_TN, T, sg, sx, rows=rows)
 
 
+# ------------------------------------------------------------------ two GEMMs in one call
+def fp8_operands(name, M, N, K, layout, fmt):
+    """FP8 codes of A (M x K) and B (N x K) stored as `layout` wants them."""
+    a8, b8, sa, sb = fp8_inputs(name, M, N, K, fmt)
+    A = a8 if layout != sq.SQ_TN else np.ascontiguousarray(a8.T)
+    B = b8 if layout == sq.SQ_NT else np.ascontiguousarray(b8.T)
+    return A, B, sa, sb
+
+
+def check_rows(C, A, B, fmt, layout, K, sa, sb, seed, n=64):
+    M = C.shape[0]
+    edges = np.concatenate([np.arange(0, M, 128), np.minimum(np.arange(127, M + 127, 128), M - 1)])
+    rows = np.unique(np.concatenate([edges, np.random.default_rng(seed).choice(M, min(n, M),
+                                                                               replace=False)]))
+    check_fp8(C, A, B, fmt, layout, K, sa, sb, rows=rows)
+
+
+# (problem 0, problem 1) as (M, N, K, layout); all small enough that one
+# launch takes both, on 128- or 256-wide tiles as the estimate picks
+FP8_PAIRS = [
+    ("ragged NT + TN", (200, 176, 320, sq.SQ_NT), (272, 96, 512, sq.SQ_TN)),
+    ("deep NN + short NT", (130, 144, 2048, sq.SQ_NN), (160, 96, 16, sq.SQ_NT)),
+    ("one tile + wide", (128, 128, 128, sq.SQ_TN), (128, 1024, 256, sq.SQ_NN)),
+    ("dX NN + dW TN ragged", (1016, 1008, 2048, sq.SQ_NN), (2032, 1008, 1024, sq.SQ_TN)),
+]
+
+
+@pytest.mark.parametrize("fmt", [sq.SQ_FMT_E4M3, sq.SQ_FMT_E5M2], ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("name,p0,p1", FP8_PAIRS, ids=[c[0] for c in FP8_PAIRS])
+def test_fp8_gemm_pair(name, p0, p1, fmt):
+    """Each problem of the pair matches the oracle as one GEMM does, and
+    neither output's guard band is touched."""
+    ops, outs = [], []
+    for i, (M, N, K, layout) in enumerate((p0, p1)):
+        A, B, sa, sb = fp8_operands(f"{name} {i}", M, N, K, layout, fmt)
+        C, cbuf, n = guarded((M, N), torch.bfloat16, 3.0 + i)
+        ops.append((A, B, sa, sb, layout, K))
+        outs.append((C, cbuf, n))
+    sq.sq_gemm_fp8_scaled_pair([to_dev(o[0]) for o in ops], [to_dev(o[1]) for o in ops],
+                               [torch.tensor([o[2]], device=DEV) for o in ops],
+                               [torch.tensor([o[3]], device=DEV) for o in ops], fmt,
+                               [o[4] for o in ops], Cs=[o[0] for o in outs])
+    assert sq.sq_get_last_device_error() == sq.SQ_OK
+    for i, ((A, B, sa, sb, layout, K), (C, cbuf, n)) in enumerate(zip(ops, outs)):
+        check_fp8(C, A, B, fmt, layout, K, sa, sb)
+        assert guard_intact(cbuf, n, 3.0 + i)
+
+
+def test_fp8_gemm_pair_backward_shapes_match_two_calls():
+    """dX = G W (NN) and dW = G^T X (TN) of the MLP backward (dim 1024,
+    hidden 4096, 2048 tokens) in one call: within the bound on sampled rows
+    (every 128-row band's edges), and equal to two separate calls wherever
+    both take the same tile width."""
+    T, H, D = 2048, 4096, 1024
+    fmt = sq.SQ_FMT_E4M3
+    g = synth.normal(71, (T, H), std=1e-3, dtype=synth.BF16)
+    w = synth.normal(72, (H, D), std=0.02, dtype=synth.BF16)
+    x = synth.normal(73, (T, D), std=1.0, dtype=synth.BF16)
+
+    def scale_of(seed, shape, std):
+        p = synth.bf16_bits_to_f32(synth.normal(seed, shape, std=std, dtype=synth.BF16))
+        return np.float32(np.abs(p).max()) / np.float32(448.0)
+
+    sg, sw, sx = scale_of(74, (T, H), 1e-3), scale_of(75, (H, D), 0.02), scale_of(76, (T, D), 1.0)
+    g8, _ = oracle.quantize_fp8(g, sg, fmt)
+    w8, _ = oracle.quantize_fp8(w, sw, fmt)
+    x8, _ = oracle.quantize_fp8(x, sx, fmt)
+    tsg, tsw, tsx = (torch.tensor([v], device=DEV) for v in (sg, sw, sx))
+    G8, W8, X8 = to_dev(g8), to_dev(w8), to_dev(x8)
+    dX, dW = sq.sq_gemm_fp8_scaled_pair([G8, G8], [W8, X8], [tsg, tsg], [tsw, tsx], fmt,
+                                        [sq.SQ_NN, sq.SQ_TN])
+    assert dX.shape == (T, D) and dW.shape == (H, D)
+    check_rows(dX, g8, w8, fmt, sq.SQ_NN, H, sg, sw, seed=77)
+    check_rows(dW, g8, x8, fmt, sq.SQ_TN, T, sg, sx, seed=78)
+    # the same products by the single-GEMM entry point: every element is one
+    # tile's fp32 sum over the same K order, so the codes agree except where a
+    # different tile width changes the tensor core's grouping of K
+    dX1 = sq.sq_gemm_fp8_scaled(G8, W8, tsg, tsw, fmt, sq.SQ_NN)
+    dW1 = sq.sq_gemm_fp8_scaled(G8, X8, tsg, tsx, fmt, sq.SQ_TN)
+    for a, b in ((dX, dX1), (dW, dW1)):
+        same = (a.view(torch.int16) == b.view(torch.int16)).float().mean().item()
+        assert same > 0.99, same
+
+
+def test_fp8_gemm_pair_of_large_problems_runs_as_two_launches():
+    """Problems with many rounds of tiles each are estimated faster as two
+    ordinary launches; the results are the same GEMMs."""
+    fmt = sq.SQ_FMT_E4M3
+    shapes = [(4096, 8192, 1024, sq.SQ_NT), (4096, 8192, 1024, sq.SQ_NN)]
+    ops = [fp8_operands(f"large pair {i}", *s[:3], s[3], fmt) for i, s in enumerate(shapes)]
+    Cs = sq.sq_gemm_fp8_scaled_pair([to_dev(o[0]) for o in ops], [to_dev(o[1]) for o in ops],
+                                    [torch.tensor([o[2]], device=DEV) for o in ops],
+                                    [torch.tensor([o[3]], device=DEV) for o in ops], fmt,
+                                    [s[3] for s in shapes])
+    for i, (C, (A, B, sa, sb), s) in enumerate(zip(Cs, ops, shapes)):
+        check_rows(C, A, B, fmt, s[3], s[2], sa, sb, seed=80 + i, n=32)
+        single = sq.sq_gemm_fp8_scaled(to_dev(A), to_dev(B), torch.tensor([sa], device=DEV),
+                                       torch.tensor([sb], device=DEV), fmt, s[3])
+        assert torch.equal(C.view(torch.int16), single.view(torch.int16))
+
+
 # ------------------------------------------------------------------ the pages' one-wave shapes
 # The forward (NT 2048x1024x1024) and dX (NN) run on 128x128 tiles, dW (TN)
 # on 128x256 tiles: one round of tiles each.  The ragged variants clip M, N
