@@ -464,6 +464,8 @@ FP8_PAIRS = [
     ("deep NN + short NT", (130, 144, 2048, sq.SQ_NN), (160, 96, 16, sq.SQ_NT)),
     ("one tile + wide", (128, 128, 128, sq.SQ_TN), (128, 1024, 256, sq.SQ_NN)),
     ("dX NN + dW TN ragged", (1016, 1008, 2048, sq.SQ_NN), (2032, 1008, 1024, sq.SQ_TN)),
+    # 320 tiles of 128x128 on the 152 SMs: three rounds, the second dealt backwards
+    ("three rounds NT + NN", (2048, 2048, 256, sq.SQ_NT), (1024, 1024, 128, sq.SQ_NN)),
 ]
 
 
