@@ -461,9 +461,8 @@ sq_status sq_gemm_fp8_scaled_e4m3(const uint8_t* A, const uint8_t* B, const floa
 // ---------------------------------------------------------------- linear layer
 namespace {
 
-constexpr int kColsumSplits = 16;
 // workspace: [0, 256) quantize words (amax bits, ticket) and step slots;
-// then the float32 bias (N); then the column-sum slabs (16 x N floats).
+// then the float32 bias (N).
 constexpr size_t kLinStepX = 64, kLinStepW = 68, kLinStepG = 72, kLinSinkW = 80, kLinSinkX = 84;
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
@@ -525,8 +524,7 @@ size_t sq_linear_workspace_bytes(int64_t T, int64_t N, int64_t K) {
     (void)T;
     (void)K;
     if (N <= 0) return 0;
-    return 256 + align256(static_cast<size_t>(N) * 4) +
-           align256(static_cast<size_t>(kColsumSplits) * N * 4);
+    return 256 + align256(static_cast<size_t>(N) * 4);
 }
 
 sq_status sq_linear_forward_fp8(const uint16_t* x, int64_t M, int64_t K, const void* w,
@@ -620,7 +618,6 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     unsigned* qws = reinterpret_cast<unsigned*>(wsb);
-    float* partial = reinterpret_cast<float*>(wsb + 256 + align256(static_cast<size_t>(N) * 4));
     sq_status r = check_operand(sg, g_ring, g_hist, g_idx, g_margin);
     if (r != SQ_OK) return r;
     // one quantization of the gradient, shared by both products, and the
@@ -656,8 +653,7 @@ sq_status sq_linear_backward_fp8(const uint16_t* g, const uint16_t* x, const uin
         if (e != cudaSuccess) return SQ_ERR_CUDA;
     }
     if (want_gb) {
-        const int splits = T < kColsumSplits ? static_cast<int>(T) : kColsumSplits;
-        e = sq::launch_colsum_bf16(g, T, N, splits, partial, gb, st);
+        e = sq::launch_colsum_bf16(g, T, N, gb, st);
         if (e != cudaSuccess) return SQ_ERR_CUDA;
     }
     return SQ_OK;

@@ -36,48 +36,95 @@ cudaError_t launch_bias_to_f32(const void* bias, int kind, int fmt, const float*
                       1u, bias, kind, fmt, step, n, out);
 }
 
-// Block (x, s): columns [512x, 512x + 512) (two per thread, one 4-byte load),
-// rows of slab s.  partial[s*N + j] = fp32 sum over the slab.
-__global__ void __launch_bounds__(256) colsum_partial_kernel(const uint16_t* __restrict__ g,
-                                                             int64_t T, int64_t N, int splits,
-                                                             float* __restrict__ partial) {
+// Bias gradient gb[j] = bf16(sum_t g[t*N + j]) in one launch.  Cluster x
+// (kColsumSlabs CTAs along y) owns the columns [128x, 128x + 128); CTA s of
+// it sums them over row slab s:
+// - each half-warp covers the 128 columns, lane l holding the 8 columns
+//   [128x + 8(l % 16), +8) (one 16-byte load per row);
+// - row stream q = 2w + l / 16 of warp w adds rows t0 + q, t0 + q + 32, ...
+//   in increasing order, eight rows' loads in flight at a time;
+// - the CTA adds its 32 row streams' sums in stream order into sums[128].
+// After a cluster barrier, CTA s adds, for its 16 columns [128x + 16s, +16),
+// the slabs' sums in slab order, read through distributed shared memory, and
+// writes the bf16 result.  A second barrier keeps every CTA's sums alive until
+// they are read.  The order of every addition is fixed, so the result is the
+// same on every call.  N % 8 == 0, g 16-byte aligned.
+constexpr int kColsumSlabs = 8;    // CTAs per cluster, one row slab each
+constexpr int kColsumWarps = 16;
+constexpr int kColsumStreams = 2 * kColsumWarps;   // row streams per CTA
+constexpr int kColsumCols = 128;   // columns per cluster
+constexpr int kColsumRows = 8;     // rows whose loads a thread keeps in flight
+__global__ void __cluster_dims__(1, kColsumSlabs, 1) __launch_bounds__(kColsumWarps * 32)
+    colsum_kernel(const uint16_t* __restrict__ g, int64_t T, int64_t N, uint16_t* __restrict__ gb) {
     pdl_begin();
-    const int64_t j = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 2;
+    __shared__ float red[kColsumStreams][kColsumCols];
+    __shared__ float sums[kColsumCols];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = 2 * warp + (lane >> 4);              // this thread's row stream
+    const int cl = 8 * (lane & 15);                    // its first column in the block
     const int s = blockIdx.y;
-    const int64_t rows_per = (T + splits - 1) / splits;
+    const int64_t rows_per = (T + kColsumSlabs - 1) / kColsumSlabs;
     const int64_t t0 = s * rows_per;
     const int64_t t1 = t0 + rows_per < T ? t0 + rows_per : T;
-    if (j >= N) return;
-    float a0 = 0.0f, a1 = 0.0f;
-    for (int64_t t = t0; t < t1; ++t) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(g + t * N + j);
-        a0 = __fadd_rn(a0, __uint_as_float(w << 16));
-        a1 = __fadd_rn(a1, __uint_as_float(w & 0xFFFF0000u));
+    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kColsumCols + cl;
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = 0.0f;
+    auto add = [&](const uint4& v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            a[2 * i] = __fadd_rn(a[2 * i], __uint_as_float(w[i] << 16));
+            a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __uint_as_float(w[i] & 0xFFFF0000u));
+        }
+    };
+    if (j0 < N) {
+        const uint16_t* col = g + j0;
+        int64_t t = t0 + q;
+        for (; t + (kColsumRows - 1) * kColsumStreams < t1; t += kColsumRows * kColsumStreams) {
+            uint4 v[kColsumRows];
+#pragma unroll
+            for (int r = 0; r < kColsumRows; ++r)
+                v[r] = *reinterpret_cast<const uint4*>(col + (t + r * kColsumStreams) * N);
+#pragma unroll
+            for (int r = 0; r < kColsumRows; ++r) add(v[r]);
+        }
+        for (; t < t1; t += kColsumStreams) add(*reinterpret_cast<const uint4*>(col + t * N));
     }
-    partial[s * N + j] = a0;
-    partial[s * N + j + 1] = a1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[q][cl + i] = a[i];
+    __syncthreads();
+    if (threadIdx.x < kColsumCols) {
+        float sum = red[0][threadIdx.x];
+#pragma unroll
+        for (int r = 1; r < kColsumStreams; ++r) sum = __fadd_rn(sum, red[r][threadIdx.x]);
+        sums[threadIdx.x] = sum;
+    }
+    cluster_sync_all();   // every slab's sums written and visible in the cluster
+    constexpr int kPer = kColsumCols / kColsumSlabs;   // columns each CTA finishes
+    if (threadIdx.x < kPer) {
+        const int c = kPer * s + static_cast<int>(threadIdx.x);
+        const int64_t j = static_cast<int64_t>(blockIdx.x) * kColsumCols + c;
+        float sum = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kColsumSlabs; ++r) {
+            float v;
+            asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                         : "=f"(v)
+                         : "r"(cluster_addr(&sums[c], static_cast<uint32_t>(r)))
+                         : "memory");
+            sum = r == 0 ? v : __fadd_rn(sum, v);
+        }
+        if (j < N) gb[j] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+    }
+    cluster_sync_all();   // no CTA leaves while another reads its sums
 }
 
-__global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restrict__ partial,
-                                                           int splits, int64_t N,
-                                                           uint16_t* __restrict__ gb) {
-    pdl_begin();
-    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (j >= N) return;
-    float a = 0.0f;
-    for (int s = 0; s < splits; ++s) a = __fadd_rn(a, partial[s * N + j]);
-    gb[j] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-}
-
-cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, int splits,
-                               float* partial, uint16_t* gb, cudaStream_t st) {
+cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, uint16_t* gb, cudaStream_t st) {
     if (N <= 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>((N / 2 + 255) / 256), static_cast<unsigned>(splits));
-    const cudaError_t e = launch_pdl(colsum_partial_kernel, grid, dim3(256), 0, st, 1u, g, T, N, splits, partial);
-    if (e != cudaSuccess) return e;
-    const float* cpartial = partial;
-    return launch_pdl(colsum_final_kernel, dim3(static_cast<unsigned>((N + 255) / 256)), dim3(256), 0, st,
-                      1u, cpartial, splits, N, gb);
+    const dim3 grid(static_cast<unsigned>((N + kColsumCols - 1) / kColsumCols),
+                    static_cast<unsigned>(kColsumSlabs));
+    return launch_pdl(colsum_kernel, grid, dim3(kColsumWarps * 32), 0, st, 1u, g, T, N, gb);
 }
 
 // Self-test of the bounded waits: one CTA waits for a barrier phase that

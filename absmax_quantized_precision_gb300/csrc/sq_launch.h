@@ -122,10 +122,9 @@ cudaError_t launch_gemm_fp8_pair(const Fp8Problem* q, int fmt, unsigned* err_wor
 // bias kind 1: bf16 [n] widened; kind 2: FP8 codes of fmt times *step.
 cudaError_t launch_bias_to_f32(const void* bias, int kind, int fmt, const float* step, int64_t n,
                                float* out, cudaStream_t st);
-// gb[j] = bf16(sum_t g[t*N + j]): fp32 partial sums over `splits` row slabs in
-// `partial` (splits * N floats), then a fixed-order sum of the slabs.
-cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, int splits,
-                               float* partial, uint16_t* gb, cudaStream_t st);
+// gb[j] = bf16(sum_t g[t*N + j]) (N % 8 == 0), in one launch: fp32 sums
+// over row slabs, then the slabs added in a fixed order.
+cudaError_t launch_colsum_bf16(const uint16_t* g, int64_t T, int64_t N, uint16_t* gb, cudaStream_t st);
 
 // Scales of row i of A in batch b: sA[b*ceil(M/ga) + i/ga] (ga = 1: per row).
 // bound_a / bound_b: the operands' bound regions (nullable: no bound); when

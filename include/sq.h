@@ -359,7 +359,7 @@ sq_status sq_gemm_fp8_scaled_e4m3(const uint8_t* A, const uint8_t* B, const floa
 
 /*
  * Workspace of the fused linear forward / backward: 256 bytes of quantize and
- * step words, the float32 bias (N), and 16 x N floats of column-sum slabs.
+ * step words and the float32 bias (N).
  * Zero it once (cudaMemset); the calls leave the words they rely on zeroed.
  */
 size_t sq_linear_workspace_bytes(int64_t T, int64_t N, int64_t K);
