@@ -183,3 +183,26 @@ def test_backward_masks_ragged_tokens_and_gradient_ring():
     ow8, _ = oracle.quantize_fp8(w, sw, fmt)
     ref, _ = oracle.gemm_fp8(og8b, ow8, fmt, oracle.NN, sg_used, sw, want_bf16=False)
     check_out(gx, ref, N, sg_used, sw, og8b, ow8, fmt)
+
+
+@pytest.mark.parametrize("T", [5, 1000], ids=["T5 empty slabs", "T1000"])
+def test_backward_bias_gradient_ragged_columns(T):
+    """The bias gradient alone, on 1008 columns (a partial 128-column block)
+    and on fewer tokens than row slabs; the same bits on a second call."""
+    N, K = 1008, 64
+    fmt = 0
+    g = synth.normal(261 + T, (T, N), std=1e-2, dtype=synth.BF16)
+    x = synth.normal(262, (T, K), dtype=synth.BF16)
+    w = synth.normal(263, (N, K), std=0.02, dtype=synth.BF16)
+    ws = sq.linear_workspace(T, N, K, DEV)
+    sg = torch.tensor([prev_step(264, (T, N), 1e-2, fmt)], device=DEV)
+    args = (to_dev(g, True), to_dev(x, True), to_dev(w, True), (False, False, True), sg, None, None,
+            fmt, ws)
+    gx, gw, gb, _ = sq.sq_linear_backward_fp8(*args)
+    assert gx is None and gw is None and gb.shape == (N,)
+    want = oracle.colsum_bf16(g)
+    gmax = np.abs(synth.bf16_bits_to_f32(g)).max()
+    tol = 2.0 ** -8 * np.abs(want) + T * gmax * 2.0 ** -22
+    assert np.all(np.abs(bf16_to_f64(gb) - want) <= tol)
+    _, _, gb2, _ = sq.sq_linear_backward_fp8(*args)
+    assert torch.equal(gb.view(torch.int16), gb2.view(torch.int16))
