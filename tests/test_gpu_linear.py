@@ -185,11 +185,12 @@ def test_backward_masks_ragged_tokens_and_gradient_ring():
     check_out(gx, ref, N, sg_used, sw, og8b, ow8, fmt)
 
 
-@pytest.mark.parametrize("T", [5, 1000], ids=["T5 empty slabs", "T1000"])
-def test_backward_bias_gradient_ragged_columns(T):
-    """The bias gradient alone, on 1008 columns (a partial 128-column block)
-    and on fewer tokens than row slabs; the same bits on a second call."""
-    N, K = 1008, 64
+@pytest.mark.parametrize("T,N", [(5, 1008), (1000, 1008), (64, 16)],
+                         ids=["T5 empty slabs", "T1000", "N16 one partial block"])
+def test_backward_bias_gradient_ragged_columns(T, N):
+    """The bias gradient alone, on a partial 128-column block and on fewer
+    tokens than row slabs; the same bits on a second call."""
+    K = 64
     fmt = 0
     g = synth.normal(261 + T, (T, N), std=1e-2, dtype=synth.BF16)
     x = synth.normal(262, (T, K), dtype=synth.BF16)
