@@ -329,8 +329,10 @@ sq_status sq_gemm_fp8_scaled(const uint8_t* A, const uint8_t* B, const float* sa
  * When the estimate says so, one launch deals the tiles of both problems to
  * every SM (so that a small problem's SMs do not idle while the other runs);
  * otherwise the two run as two launches on the stream.
- * Errors: SQ_ERR_INVALID_ARG also when an output overlaps an operand or the
- * output of the other problem (the problems may run side by side).
+ * Errors: as sq_gemm_fp8_scaled for each problem, and SQ_ERR_INVALID_ARG when
+ * either output overlaps the other problem's operands or output (the
+ * problems may run side by side).  Ownership: all buffers are the caller's;
+ * the call allocates nothing.
  */
 sq_status sq_gemm_fp8_scaled_pair(const uint8_t* const A[2], const uint8_t* const B[2],
                                   const float* const sa[2], const float* const sb[2], int fmt,
