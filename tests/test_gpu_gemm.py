@@ -526,6 +526,32 @@ def test_fp8_gemm_pair_backward_shapes_match_two_calls():
         assert same > 0.99, same
 
 
+def test_fp8_gemm_pair_in_a_cuda_graph():
+    """The paired call captured in a CUDA graph on a side stream: its replays
+    give the bits of the eager call."""
+    fmt = sq.SQ_FMT_E4M3
+    shapes = [(1016, 1008, 2048, sq.SQ_NN), (2032, 1008, 1024, sq.SQ_TN)]
+    ops = [fp8_operands(f"graph pair {i}", *s_[:3], s_[3], fmt) for i, s_ in enumerate(shapes)]
+    As, Bs = [to_dev(o[0]) for o in ops], [to_dev(o[1]) for o in ops]
+    sas = [torch.tensor([o[2]], device=DEV) for o in ops]
+    sbs = [torch.tensor([o[3]], device=DEV) for o in ops]
+    layouts = [s_[3] for s_ in shapes]
+    eager = sq.sq_gemm_fp8_scaled_pair(As, Bs, sas, sbs, fmt, layouts)
+    Cs = [torch.full_like(c, 7.0) for c in eager]
+    side = torch.cuda.Stream(DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        sq.sq_gemm_fp8_scaled_pair(As, Bs, sas, sbs, fmt, layouts, Cs=Cs)
+    for _ in range(2):
+        for c in Cs:
+            c.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(Cs, eager):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert sq.sq_get_last_device_error() == sq.SQ_OK
+
+
 def test_fp8_gemm_pair_of_large_problems_runs_as_two_launches():
     """Problems with many rounds of tiles each are estimated faster as two
     ordinary launches; the results are the same GEMMs."""
